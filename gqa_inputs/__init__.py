@@ -1,0 +1,95 @@
+"""Seeded synthetic inputs for chunked-prefill GQA attention.
+
+This module only draws random numbers and shapes them; it holds none of the
+attention arithmetic. Both the FP64 oracle (``oracle/``) and the CUDA path
+(``gqa_chunked_prefill_gb300``) are fed from here, so the two sides see the
+same bytes.
+
+Workloads follow the shapes of the dedicated BF16 prefill kernel described in
+"DCU使用技术报告（中篇）：gfx936 DCU上的Qwen3.5-27B Triton-ROCm Attention与GEMV深度优化实战",
+§1 (24 query heads, 4 KV heads, head_dim 256, GQA ratio 6, BF16) and the
+q_len x kv_len pairs measured in its §4 table (4096x8K, 4096x16K, 4096x32K,
+3072x16K, 512x32K), plus the short-KV cases its §8 coverage rule asks for.
+
+Recipe (one generator per shape, on the CPU so every machine gets the same
+bytes): ``torch.Generator('cpu').manual_seed(seed)``; draw Q, then K, then V
+as FP32 N(0, 1) and round each to BF16. The 512x4096 workload also draws, after
+V, one bias vector per KV head with standard deviation 0.5, adds it to every
+key of that head in FP32 and only then rounds K to BF16.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Dict, Optional
+
+import torch
+
+N_Q_HEADS = 24
+N_KV_HEADS = 4
+HEAD_DIM = 256
+DEFAULT_SCALE = 1.0 / 16.0  # 1/sqrt(head_dim)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    q_len: int
+    kv_len: int
+    seed: int
+    k_bias_std: Optional[float] = None  # per-KV-head key bias (N(0, std)), or None
+    scale: float = DEFAULT_SCALE
+    n_q_heads: int = N_Q_HEADS
+    n_kv_heads: int = N_KV_HEADS
+    head_dim: int = HEAD_DIM
+
+
+# The seven shapes of the five workload families. Seeds are 1000 + 10*family + variant.
+WORKLOADS: Dict[str, Workload] = {
+    w.name: w
+    for w in (
+        Workload("q128_kv256", 128, 256, 1000),
+        Workload("q512_kv4096_kbias", 512, 4096, 1010, k_bias_std=0.5),
+        Workload("q4096_kv8192", 4096, 8192, 1020),
+        Workload("q4096_kv16384", 4096, 16384, 1030),
+        Workload("q3072_kv16384", 3072, 16384, 1031),
+        Workload("q4096_kv32768", 4096, 32768, 1040),
+        Workload("q512_kv32768", 512, 32768, 1041),
+    )
+}
+
+
+def make_qkv(q_len: int, kv_len: int, seed: int, *, n_q_heads: int = N_Q_HEADS,
+             n_kv_heads: int = N_KV_HEADS, head_dim: int = HEAD_DIM,
+             k_bias_std: Optional[float] = None):
+    """Return CPU BF16 tensors q [q_len,Hq,d], k [kv_len,Hkv,d], v [kv_len,Hkv,d]."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = torch.randn((q_len, n_q_heads, head_dim), generator=g, dtype=torch.float32)
+    k = torch.randn((kv_len, n_kv_heads, head_dim), generator=g, dtype=torch.float32)
+    v = torch.randn((kv_len, n_kv_heads, head_dim), generator=g, dtype=torch.float32)
+    if k_bias_std is not None:
+        bias = torch.randn((n_kv_heads, head_dim), generator=g, dtype=torch.float32) * k_bias_std
+        k = k + bias.unsqueeze(0)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def make_workload(w: Workload):
+    return make_qkv(w.q_len, w.kv_len, w.seed, n_q_heads=w.n_q_heads,
+                    n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, k_bias_std=w.k_bias_std)
+
+
+def sample_rows(q_len: int, n_q_heads: int, n: int, seed: int) -> torch.Tensor:
+    """A fixed, stratified set of (token, head) row ids ``t*n_q_heads + h``.
+
+    Covers the first and last tokens, every head, and seeded random rows in
+    between, so that both the diagonal region and long-prefix rows are checked.
+    """
+    total = q_len * n_q_heads
+    if n >= total:
+        return torch.arange(total, dtype=torch.int64)
+    fixed = []
+    for t in (0, 1, q_len // 2, q_len - 2, q_len - 1):
+        if 0 <= t < q_len:
+            fixed.extend(t * n_q_heads + h for h in range(n_q_heads))
+    g = torch.Generator("cpu").manual_seed(seed)
+    extra = torch.randint(0, total, (max(n - len(fixed), 0),), generator=g)
+    return torch.unique(torch.cat([torch.tensor(fixed, dtype=torch.int64), extra]))

@@ -1,0 +1,104 @@
+"""FP64 CPU oracle for chunked-prefill causal GQA attention.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers. The product package never
+imports this module, and this module never imports the product package; the
+two share nothing but the seeded inputs of ``gqa_inputs``.
+
+``attention()`` runs the plain C++ definition in ``gqa_oracle.cpp`` (explicit
+full-row softmax in FP64, one std::thread per row at a time). ``restate_numpy``
+holds an independent numpy restatement used to cross-check it on tiny shapes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqa_oracle.cpp")
+_LIB = os.path.join(_HERE, "libgqa_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C++ compiler (plain -O2, no fast-math,
+    no FMA contraction, so x86 and Arm hosts give the same bits)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
+               "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", _LIB + ".tmp"]
+        subprocess.run(cmd, check=True)
+        os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        f = lib.gqa_oracle_attn
+        f.restype = ctypes.c_int
+        f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                      ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                      ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _f64(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().to("cpu", torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def attention(q, k, v, scale: float, rows=None, n_threads: Optional[int] = None,
+              with_prob_sum: bool = False):
+    """FP64 attention of a q_len chunk at the end of a kv_len prefix.
+
+    q: [q_len, Hq, d]; k, v: [kv_len, Hkv, d] (torch or numpy; BF16 is widened
+    exactly). ``rows`` optionally lists row ids t*Hq + h to compute.
+    Returns (out, lse[, prob_sum]) as numpy FP64: out [q_len, Hq, d] and
+    lse [q_len, Hq] when ``rows`` is None, else out [n_rows, d], lse [n_rows].
+    """
+    lib = _load()
+    q64, k64, v64 = _f64(q), _f64(k), _f64(v)
+    q_len, hq, d = q64.shape
+    kv_len, hkv, d2 = k64.shape
+    assert d2 == d and v64.shape == k64.shape
+    if rows is not None:
+        rows64 = np.ascontiguousarray(np.asarray(
+            rows.numpy() if isinstance(rows, torch.Tensor) else rows, dtype=np.int64))
+        n_rows = rows64.shape[0]
+        out = np.empty((n_rows, d), np.float64)
+        lse = np.empty((n_rows,), np.float64)
+        psum = np.empty((n_rows,), np.float64) if with_prob_sum else None
+        rows_ptr = rows64.ctypes.data
+    else:
+        n_rows = 0
+        out = np.empty((q_len, hq, d), np.float64)
+        lse = np.empty((q_len, hq), np.float64)
+        psum = np.empty((q_len, hq), np.float64) if with_prob_sum else None
+        rows_ptr = None
+    rc = lib.gqa_oracle_attn(q64.ctypes.data, k64.ctypes.data, v64.ctypes.data,
+                             q_len, kv_len, hq, hkv, d, float(scale), rows_ptr, n_rows,
+                             out.ctypes.data, lse.ctypes.data,
+                             psum.ctypes.data if psum is not None else None,
+                             int(n_threads or host_threads()))
+    if rc != 0:
+        raise ValueError(f"oracle rejected arguments (rc={rc})")
+    if with_prob_sum:
+        return out, lse, psum
+    return out, lse

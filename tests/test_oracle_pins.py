@@ -1,0 +1,200 @@
+"""Pins for the FP64 oracle: each test checks it against something other than
+itself — a closed form, a textbook library routine, an invariant the method
+must satisfy, or an independent numpy restatement — so that a dropped term, a
+wrong sign, a wrong index or a transposed operand in the oracle fails here.
+
+Definition pinned: QK^T, bottom-right causal mask, softmax and PV
+(DCU使用技术报告（中篇）, §2), query head h on KV head h/6
+(gfx936 DCU上实现INT8 QK MMAC, §5.2), LSE = natural log of the softmax
+normaliser of the scaled scores.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import restate_numpy as rn
+from gqa_inputs import make_qkv
+
+SCALE = 1.0 / 16.0
+
+
+def rand64(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+# --- closed forms ---------------------------------------------------------------
+
+def test_single_key_returns_v_and_dot_lse():
+    q, k, v = rand64((1, 24, 256), 1), rand64((1, 4, 256), 2), rand64((1, 4, 256), 3)
+    out, lse = oracle.attention(q, k, v, SCALE)
+    for h in range(24):
+        g = h // 6
+        assert np.array_equal(out[0, h], v[0, g])  # e = 1, Z = 1: exact
+        assert abs(lse[0, h] - SCALE * float(np.dot(q[0, h], k[0, g]))) < 1e-12
+
+
+def test_first_row_of_unprefixed_chunk_returns_v0():
+    q, k, v = rand64((7, 24, 256), 4), rand64((7, 4, 256), 5), rand64((7, 4, 256), 6)
+    out, _ = oracle.attention(q, k, v, SCALE)
+    for h in range(24):
+        assert np.array_equal(out[0, h], v[0, h // 6])
+
+
+@pytest.mark.parametrize("zero", ["q", "k"])
+def test_constant_scores_give_mean_of_visible_v(zero):
+    q_len, kv_len = 5, 11
+    q, k, v = rand64((q_len, 24, 64), 7), rand64((kv_len, 4, 64), 8), rand64((kv_len, 4, 64), 9)
+    if zero == "q":
+        q[:] = 0.0
+    else:
+        k[:] = 0.0
+    out, lse = oracle.attention(q, k, v, SCALE)
+    for t in range(q_len):
+        p = kv_len - q_len + t
+        for h in range(24):
+            np.testing.assert_allclose(out[t, h], v[: p + 1, h // 6].mean(axis=0), rtol=0, atol=1e-13)
+            assert abs(lse[t, h] - math.log(p + 1)) < 1e-13
+
+
+def test_linear_scores_geometric_series():
+    """q = a*e0, k_j = j*e0, v_j = j: scores c*j with c = scale*a; the output is the
+    mean key index under weights e^{c j}, j = 0..p, and lse = ln sum_j e^{c j}."""
+    q_len, kv_len, d, a = 6, 40, 32, 3.0
+    q = np.zeros((q_len, 24, d)); q[:, :, 0] = a
+    k = np.zeros((kv_len, 4, d)); k[:, :, 0] = np.arange(kv_len)[:, None]
+    v = np.zeros((kv_len, 4, d)); v[:, :, :] = np.arange(kv_len)[:, None, None]
+    scale = 0.05
+    c = scale * a
+    out, lse = oracle.attention(q, k, v, scale)
+    for t in range(q_len):
+        p = kv_len - q_len + t
+        r = math.exp(c)
+        z = (r ** (p + 1) - 1.0) / (r - 1.0)
+        # sum_j j r^j for j = 0..p
+        num = r * (1 - (p + 1) * r ** p + p * r ** (p + 1)) / (1 - r) ** 2
+        for h in range(24):
+            assert abs(lse[t, h] - math.log(z)) < 1e-11
+            np.testing.assert_allclose(out[t, h], num / z, rtol=1e-12, atol=0)
+
+
+def test_probabilities_sum_to_one():
+    q, k, v = make_qkv(9, 300, 11)
+    _, _, psum = oracle.attention(q, k, v, SCALE, with_prob_sum=True)
+    assert np.max(np.abs(psum - 1.0)) < 1e-12
+
+
+# --- invariants -----------------------------------------------------------------
+
+def test_future_keys_do_not_change_earlier_rows():
+    q_len, kv_len = 12, 40
+    q, k, v = rand64((q_len, 24, 32), 12), rand64((kv_len, 4, 32), 13), rand64((kv_len, 4, 32), 14)
+    out, lse = oracle.attention(q, k, v, SCALE)
+    t_star = 5
+    p_star = kv_len - q_len + t_star
+    k2, v2 = k.copy(), v.copy()
+    k2[p_star + 1:] += 10.0 * rand64(k2[p_star + 1:].shape, 15)
+    v2[p_star + 1:] -= 7.0
+    out2, lse2 = oracle.attention(q, k2, v2, SCALE)
+    assert np.array_equal(out[: t_star + 1], out2[: t_star + 1])
+    assert np.array_equal(lse[: t_star + 1], lse2[: t_star + 1])
+    assert not np.array_equal(out[t_star + 1:], out2[t_star + 1:])
+
+
+def test_per_head_key_shift_moves_lse_only():
+    q_len, kv_len = 6, 30
+    q, k, v = rand64((q_len, 24, 64), 16), rand64((kv_len, 4, 64), 17), rand64((kv_len, 4, 64), 18)
+    b = 0.5 * rand64((4, 64), 19)
+    out, lse = oracle.attention(q, k, v, SCALE)
+    out2, lse2 = oracle.attention(q, k + b[None], v, SCALE)
+    np.testing.assert_allclose(out2, out, rtol=0, atol=1e-12)
+    for h in range(24):
+        shift = SCALE * (q[:, h, :] @ b[h // 6])
+        np.testing.assert_allclose(lse2[:, h] - lse[:, h], shift, rtol=0, atol=1e-12)
+
+
+def test_thread_count_and_row_subset_are_bit_identical():
+    q, k, v = make_qkv(33, 200, 20)
+    out1, lse1 = oracle.attention(q, k, v, SCALE, n_threads=1)
+    out8, lse8 = oracle.attention(q, k, v, SCALE, n_threads=8)
+    assert np.array_equal(out1, out8) and np.array_equal(lse1, lse8)
+    rows = np.array([0, 5, 24 * 7 + 3, 24 * 33 - 1], dtype=np.int64)
+    o_r, l_r = oracle.attention(q, k, v, SCALE, rows=rows)
+    flat_o, flat_l = out1.reshape(-1, 256), lse1.reshape(-1)
+    assert np.array_equal(o_r, flat_o[rows]) and np.array_equal(l_r, flat_l[rows])
+
+
+# --- independent restatements ---------------------------------------------------
+
+@pytest.mark.parametrize("q_len,kv_len", [(1, 1), (1, 8), (3, 3), (3, 8), (8, 8), (5, 7)])
+@pytest.mark.parametrize("hq,hkv,d", [(24, 4, 256), (6, 1, 16), (8, 2, 8)])
+def test_brute_force_matches_numpy_replicated_heads(q_len, kv_len, hq, hkv, d):
+    seed = 100 * q_len + kv_len + hq
+    q, k, v = rand64((q_len, hq, d), seed), rand64((kv_len, hkv, d), seed + 1), rand64((kv_len, hkv, d), seed + 2)
+    out, lse = oracle.attention(q, k, v, 0.3)
+    out_r, lse_r = rn.gqa_by_replication(q, k, v, 0.3)
+    np.testing.assert_allclose(out, out_r, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_r, rtol=1e-12, atol=1e-12)
+
+
+def _sdpa(q, k, v, scale, mask=None, is_causal=False):
+    rep = q.shape[1] // k.shape[1]
+    qt = torch.from_numpy(q).permute(1, 0, 2)                       # [H, T, d]
+    kt = torch.from_numpy(k).repeat_interleave(rep, dim=1).permute(1, 0, 2)
+    vt = torch.from_numpy(v).repeat_interleave(rep, dim=1).permute(1, 0, 2)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt, vt, attn_mask=mask, is_causal=is_causal, scale=scale)
+    return o.permute(1, 0, 2).numpy()
+
+
+def test_square_chunk_is_textbook_causal_attention():
+    """q_len == kv_len: standard causal attention, where torch's top-left
+    is_causal alignment coincides with the chunk-at-the-end alignment."""
+    q, k, v = rand64((37, 24, 256), 30), rand64((37, 4, 256), 31), rand64((37, 4, 256), 32)
+    out, _ = oracle.attention(q, k, v, SCALE)
+    np.testing.assert_allclose(out, _sdpa(q, k, v, SCALE, is_causal=True), rtol=1e-10, atol=1e-12)
+
+
+def test_prefixed_chunk_matches_library_with_bottom_right_mask():
+    q_len, kv_len = 13, 50
+    q, k, v = rand64((q_len, 24, 64), 33), rand64((kv_len, 4, 64), 34), rand64((kv_len, 4, 64), 35)
+    mask = torch.ones(q_len, kv_len, dtype=torch.bool).tril(diagonal=kv_len - q_len)
+    out, lse = oracle.attention(q, k, v, SCALE)
+    np.testing.assert_allclose(out, _sdpa(q, k, v, SCALE, mask=mask), rtol=1e-10, atol=1e-12)
+    # LSE against torch.logsumexp of the masked scaled scores
+    qt = torch.from_numpy(q)
+    kt = torch.from_numpy(k).repeat_interleave(6, dim=1)
+    s = SCALE * torch.einsum("thd,jhd->htj", qt, kt)
+    s = s.masked_fill(~mask, float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).T.numpy(), rtol=0, atol=1e-12)
+
+
+def test_bf16_inputs_are_widened_exactly():
+    q, k, v = make_qkv(4, 9, 40)
+    out_a, lse_a = oracle.attention(q, k, v, SCALE)
+    out_b, lse_b = oracle.attention(q.double().numpy(), k.double().numpy(), v.double().numpy(), SCALE)
+    assert np.array_equal(out_a, out_b) and np.array_equal(lse_a, lse_b)
+
+
+def test_rejects_bad_arguments():
+    q, k, v = rand64((4, 24, 8), 1), rand64((3, 4, 8), 2), rand64((3, 4, 8), 3)
+    with pytest.raises(ValueError):
+        oracle.attention(q, k, v, SCALE)  # kv_len < q_len
+
+
+def test_stored_oracle_values_unchanged():
+    import os
+    from gqa_inputs import WORKLOADS, make_workload
+    path = os.path.join(os.path.dirname(__file__), "golden", "oracle_q128_kv256.txt")
+    lines = [l.split() for l in open(path) if not l.startswith("#")]
+    rows = [int(l[0]) for l in lines]
+    cols = [0, 1, 128, 255]
+    w = WORKLOADS["q128_kv256"]
+    q, k, v = make_workload(w)
+    out, lse = oracle.attention(q, k, v, w.scale, rows=rows)
+    for i, l in enumerate(lines):
+        assert abs(lse[i] - float(l[1])) < 1e-12
+        for j, c in enumerate(cols):
+            assert abs(out[i, c] - float(l[2 + j])) < 1e-12
