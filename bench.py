@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark: effective causal attention TFLOP/s of the GB300 chunked-prefill GQA
+attention (24 Q heads / 4 KV heads / head_dim 256, BF16, causal, scale 1/16).
+
+One step = one call of gqa_prefill_attn over the whole workload (default: the
+4096-token chunk at the end of a 32768-key prefix). Effective FLOPs count only
+visible (query, key) pairs: 4 * head_dim * n_q_heads * pairs (2*d for QK^T and
+2*d for PV per pair and head), masked and padded work excluded.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Timing: W untimed warm-up steps; then K steps, each timed with CUDA events on
+the launching stream; L2 is flushed (a 256 MB buffer write, outside the events)
+before every step; barrier + synchronize on both sides of the loop; the
+per-rank sum is reduced with MAX over ranks. For N > 1 (torchrun, one process
+per GPU) every rank runs an independent replica of the workload ("replicas
+only": the path needs no exchange), and value = all ranks' FLOPs / max time.
+
+--impl reference times the FP64 CPU oracle (the only other implementation)
+on the host cores, on a bounded sample of rows of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from gqa_inputs import WORKLOADS, make_workload, sample_rows  # noqa: E402
+
+METRIC = "effective causal attention TFLOPS and % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "q4096_kv32768"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel
+# launch from an ncu capture, keyed by workload, with the SHA-256 of the kernel
+# source it was measured on; reported as null once the source no longer matches.
+KNOWN_TRAFFIC: dict = {}
+
+
+def visible_pairs(q_len: int, kv_len: int) -> int:
+    p0 = kv_len - q_len
+    return q_len * p0 + q_len * (q_len + 1) // 2
+
+
+def effective_flops(w) -> int:
+    return 4 * w.head_dim * w.n_q_heads * visible_pairs(w.q_len, w.kv_len)
+
+
+def kernel_source_sha() -> str:
+    path = os.path.join(ROOT, "gqa_chunked_prefill_gb300", "csrc", "attn_fwd_sm103.cu")
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.t_start = self.t_stop = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            gpu = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            gpu = str(device_index)
+        self.cmd = ["nvidia-smi", "-i", gpu, f"--query-gpu={self.FIELDS}",
+                    "--format=csv,noheader,nounits", "-lms", "100"]
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, start: bool):
+        if start:
+            self.t_start = time.time()
+        else:
+            self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        window = [s for t, s in self.samples if self.t_start and self.t_start <= t <= (self.t_stop or t)]
+        note = None
+        if not window:  # timed region shorter than the sampling period: nearest samples
+            window = [s for _, s in self.samples[-3:]]
+            note = "timed region shorter than the 100 ms sampling period; nearest samples"
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in window:
+            parts = [x.strip() for x in s.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None,
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ----------------------------------------------------------------------------- oracle
+def oracle_sample(w, q, k, v, target_s: float, seed: int = 17):
+    """Time the FP64 oracle on a row sample sized for ~target_s seconds.
+    Returns (tflops, cores, description, rows, seconds)."""
+    import oracle
+    q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
+    cores = oracle.host_threads()
+    p0 = w.kv_len - w.q_len
+    calib = sample_rows(w.q_len, w.n_q_heads, 2 * cores, seed=seed + 1)
+    t0 = time.perf_counter()
+    oracle.attention(q64, k64, v64, w.scale, rows=calib, n_threads=cores)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(cores, min(w.q_len * w.n_q_heads, len(calib) * target_s / dt)))
+    rows = sample_rows(w.q_len, w.n_q_heads, n, seed=seed)
+    t0 = time.perf_counter()
+    oracle.attention(q64, k64, v64, w.scale, rows=rows, n_threads=cores)
+    secs = time.perf_counter() - t0
+    toks = rows.numpy() // w.n_q_heads
+    flops = float(np.sum(4.0 * w.head_dim * (p0 + toks + 1)))
+    desc = (f"{len(rows)} of {w.q_len * w.n_q_heads} (token, head) rows of {w.name} "
+            f"(stratified: first/middle/last tokens, all heads, seeded random rows), "
+            f"{flops / 1e9:.1f} GFLOP of effective work in {secs:.2f} s")
+    return flops / secs / 1e12, cores, desc, len(rows), secs
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.workload]
+    flops = effective_flops(w)
+
+    if args.impl == "reference":
+        return run_reference(args, w, flops, world, rank)
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    import gqa_chunked_prefill_gb300 as gqa
+
+    q_cpu, k_cpu, v_cpu = make_workload(w)
+    q, k, v = (t.to(dev) for t in (q_cpu, k_cpu, v_cpu))
+    out = torch.empty_like(q)
+    lse = torch.empty((w.q_len, w.n_q_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(events=None):
+        _, plan = gqa.gqa_prefill_attn_ex(q, k, v, out, lse, w.q_len, w.kv_len, w.n_q_heads,
+                                          w.n_kv_heads, w.head_dim, w.scale, stream=stream,
+                                          fwd_events=events)
+        return plan
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        plan = call()
+    torch.cuda.synchronize(dev)
+    if gqa.gqa_prefill_poll(stream) != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark(True)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        s0, s1, f0, f1 = ev[i]
+        s0.record(stream)
+        call((f0, f1))
+        s1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if sampler:
+        sampler.mark(False)
+    if pg:
+        pg.barrier()
+    step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
+    fwd_ms = [a.elapsed_time(b) for _, _, a, b in ev]
+    total_ms = sum(step_ms)
+    if pg:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if gqa.gqa_prefill_poll(stream) != 0:
+        raise RuntimeError("device-side wait timed out during the timed steps")
+    clocks = sampler.stop() if sampler else None
+
+    # ---- end to end through the public call with host buffers ----------------------
+    e2e_steps = min(args.steps, 10)
+    pin = lambda t: t.pin_memory()
+    hq, hk, hv = pin(q_cpu), pin(k_cpu), pin(v_cpu)
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
+    d2h = ho.numel() * 2 + hl.numel() * 4
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        gqa.gqa_prefill_attn(q, k, v, out, lse, w.q_len, w.kv_len, w.n_q_heads, w.n_kv_heads,
+                             w.head_dim, w.scale, stream)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(e2e_steps)]
+    for a, b in e_ev:
+        flush.zero_()
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e_ev) / e2e_steps
+    if pg:
+        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+
+    peaks, peak_kind = load_peaks()
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    fwd_avg_ms = sum(fwd_ms) / len(fwd_ms)
+    achieved = flops / (fwd_avg_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    known = KNOWN_TRAFFIC.get(w.name)
+    traffic = known["bytes"] if known and known["kernel_sha256"] == kernel_source_sha() else None
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded BF16 N(0,1) Q/K/V of the workload's shape)",
+        "config": {
+            "workload": w.name, "q_len": w.q_len, "kv_len": w.kv_len, "n_q_heads": w.n_q_heads,
+            "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "scale": w.scale, "causal": "bottom-right",
+            "effective_gflop_per_step": round(flops / 1e9, 2),
+            "l2": "flushed before every step (256 MB buffer write outside the step events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "plan": {k_: plan[k_] for k_ in ("splits", "n_units", "grid", "num_sms", "kernels_per_call")},
+        },
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "peak_source": f"{peak_kind} bf16_tflops (burst; kernel timed alone)",
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "kernel": "gqa_attn_fwd_sm103_kernel",
+            "kernel_ms": round(fwd_avg_ms, 4),
+        },
+        "e2e": {
+            "value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
+            "unit": UNIT,
+            "ms_per_step": round(e2e_ms, 4),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": args.steps * plan["kernels_per_call"],
+        "clocks": clocks,
+        "wall_s_timed_loop": round(wall, 4),
+    }
+    if not args.no_cpu_baseline:
+        tf, cores, desc, _, _ = oracle_sample(w, q_cpu, k_cpu, v_cpu, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(tf, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def run_reference(args, w, flops, world, rank):
+    """The FP64 oracle, as it stands, on the host cores (rank 0 only)."""
+    if world > 1 and rank != 0:
+        return 0
+    q, k, v = make_workload(w)
+    import oracle
+    q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
+    cores = oracle.host_threads()
+    p0 = w.kv_len - w.q_len
+    per_step_s = max(1.0, min(6.0, 150.0 / (args.steps + args.warmup)))
+    calib = sample_rows(w.q_len, w.n_q_heads, 2 * cores, seed=99)
+    t0 = time.perf_counter()
+    oracle.attention(q64, k64, v64, w.scale, rows=calib, n_threads=cores)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(cores, len(calib) * per_step_s / dt))
+    total_s, total_flops = 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        rows = sample_rows(w.q_len, w.n_q_heads, n, seed=1000 + i)
+        t0 = time.perf_counter()
+        oracle.attention(q64, k64, v64, w.scale, rows=rows, n_threads=cores)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            toks = rows.numpy() // w.n_q_heads
+            total_flops += float(np.sum(4.0 * w.head_dim * (p0 + toks + 1)))
+            total_s += dt
+    value = total_flops / total_s / 1e12
+    desc = (f"per step ~{n} of {w.q_len * w.n_q_heads} (token, head) rows of {w.name}, "
+            f"stratified sample re-drawn each step; value = sampled effective FLOPs / oracle time")
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * flops / (value * 1e12), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded BF16 N(0,1) Q/K/V of the workload's shape, widened to FP64)",
+        "config": {"workload": w.name, "q_len": w.q_len, "kv_len": w.kv_len, "n_q_heads": w.n_q_heads,
+                   "n_kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "scale": w.scale,
+                   "effective_gflop_per_step": round(flops / 1e9, 2),
+                   "note": "ms_per_step extrapolates the sampled rate to the whole workload"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

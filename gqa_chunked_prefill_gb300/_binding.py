@@ -1,0 +1,142 @@
+"""ctypes binding of libgqa_prefill.so (argument marshalling only).
+
+Every entry point keeps the name and argument order of include/gqa_prefill.h.
+Tensors may be passed as torch tensors (their data_ptr is used) or as raw
+integer addresses; streams as torch.cuda.Stream, raw handles, or None for the
+current torch stream. All computation happens in the CUDA library: if it is
+missing this module raises at import time instead of falling back to anything.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgqa_prefill.so")
+
+
+class GqaStatus(enum.IntEnum):
+    OK = 0
+    ERR_NULL = 1
+    ERR_SHAPE = 2
+    ERR_UNSUPPORTED = 3
+    ERR_ALIGN = 4
+    ERR_CUDA = 5
+    ERR_DEVICE_TIMEOUT = 6
+
+
+class GqaError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{GqaStatus(status).name}: {msg}")
+        self.status = GqaStatus(status)
+
+
+class PrefillOpts(ctypes.Structure):
+    _fields_ = [("force_splits", ctypes.c_int), ("wait_timeout_us", ctypes.c_uint32),
+                ("fwd_event_begin", ctypes.c_void_p), ("fwd_event_end", ctypes.c_void_p),
+                ("reserved", ctypes.c_int * 4)]
+
+
+class PrefillPlan(ctypes.Structure):
+    _fields_ = [("num_sms", ctypes.c_int), ("q_tiles", ctypes.c_int), ("n_items", ctypes.c_int),
+                ("splits", ctypes.c_int), ("n_units", ctypes.c_int), ("grid", ctypes.c_int),
+                ("kernels_per_call", ctypes.c_int), ("variant", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_int64), ("est_makespan_tiles", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is not built; run gqa_chunked_prefill_gb300.build.build() "
+                      "(there is no non-CUDA implementation to fall back to)")
+
+lib = ctypes.CDLL(_LIB_PATH)
+_vp, _i, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+_ATTN_ARGS = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
+lib.gqa_prefill_attn.argtypes = _ATTN_ARGS
+lib.gqa_prefill_attn.restype = _i
+lib.gqa_prefill_attn_ex.argtypes = _ATTN_ARGS + [ctypes.POINTER(PrefillOpts), ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_attn_ex.restype = _i
+lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_make_plan.restype = _i
+lib.gqa_prefill_poll.argtypes = [_vp, ctypes.POINTER(_i)]
+lib.gqa_prefill_poll.restype = _i
+lib.gqa_status_string.argtypes = [_i]
+lib.gqa_status_string.restype = ctypes.c_char_p
+lib.gqa_prefill_abi_version.argtypes = []
+lib.gqa_prefill_abi_version.restype = _i
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise GqaError(rc, lib.gqa_status_string(rc).decode())
+
+
+def gqa_status_string(status: int) -> str:
+    return lib.gqa_status_string(int(status)).decode()
+
+
+def gqa_prefill_abi_version() -> int:
+    return lib.gqa_prefill_abi_version()
+
+
+def gqa_prefill_attn(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
+                     stream=None, check=True) -> int:
+    rc = lib.gqa_prefill_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), q_len, kv_len,
+                              n_q_heads, n_kv_heads, head_dim, scale, _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_prefill_attn_ex(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
+                        stream=None, force_splits=0, wait_timeout_us=0, fwd_events=None,
+                        check=True):
+    """fwd_events: optional (begin, end) torch.cuda.Event pair recorded around the
+    attention kernel itself (not the split merge)."""
+    opts = PrefillOpts(force_splits=force_splits, wait_timeout_us=wait_timeout_us)
+    if fwd_events is not None:
+        opts.fwd_event_begin = fwd_events[0].cuda_event
+        opts.fwd_event_end = fwd_events[1].cuda_event
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_attn_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), q_len, kv_len,
+                                 n_q_heads, n_kv_heads, head_dim, scale, _stream(stream),
+                                 ctypes.byref(opts), ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def gqa_prefill_make_plan(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, num_sms, force_splits=0,
+                          check=True):
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_make_plan(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, num_sms,
+                                   force_splits, ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def gqa_prefill_poll(stream=None) -> int:
+    """Synchronise the stream; return (and clear) the device status word."""
+    value = ctypes.c_int(0)
+    _check(lib.gqa_prefill_poll(_stream(stream), ctypes.byref(value)))
+    return value.value

@@ -1,0 +1,523 @@
+// Chunked-prefill causal GQA attention forward for GB300 (sm_103a).
+//
+// Method (DCU使用技术报告（中篇）：gfx936 DCU上的Qwen3.5-27B Triton-ROCm Attention与
+// GEMV深度优化实战, §2): QK^T, causal mask, online softmax, PV, FP32 accumulation,
+// one sequence, 24 query heads / 4 KV heads / head_dim 256.
+//
+// GB300 design (what differs from the report's Triton kernels for gfx936):
+//  * GQA in the MMA M dimension. The report packs 5 tokens x 6 heads = 30 of 32
+//    rows (§2) and then enlarges the query block per K/V fetch (§4 "Q10", §5
+//    "Q20") so one K/V tile serves more queries. Here one 128-row tcgen05 MMA
+//    tile holds 21 tokens x 6 heads = 126 rows of one KV group, loaded by a
+//    single 3-D TMA box per 64-wide d chunk; rows 126/127 are idle (zeroed,
+//    never stored). Every K/V tile is fetched once per 126 query rows.
+//  * The report's two-stage KV software pipeline with a delayed V load (§3)
+//    becomes a 5-deep ring of 32 KB shared-memory stages fed by TMA and
+//    tracked by mbarriers; K of tile j+2 streams while V of tile j is used.
+//  * S = Q K^T and O += P V are tcgen05 MMAs (kind::f16, BF16 in, FP32 out).
+//    S is double-buffered in tensor memory (2 x 128 columns), O (128 x 256
+//    FP32) holds the other 256 columns; P is written back as BF16 over its own
+//    S buffer and fed to the PV MMA straight from tensor memory.
+//  * Warp specialisation: warp 4 issues TMA, warp 5 issues MMAs (one thread),
+//    warps 0-3 run the softmax with one thread per MMA row (tensor-memory lane),
+//    so row max and row sum need no cross-thread reduction.
+//  * Online softmax in base 2 with the scale folded into one FMA. O is only
+//    rescaled when a row's running max grows by more than 2^8; otherwise the
+//    stale max is kept, which is exact after the final division by the row sum.
+//  * Causal tiles entirely above the diagonal are never visited; only the (at
+//    most two) tiles that straddle it are masked element-wise.
+//  * Persistent grid (one CTA per SM); work units (query tile, KV group, KV
+//    split) are taken longest-first in a snake order across CTAs. When the
+//    planner splits the KV range, each unit writes a normalised FP32 partial
+//    and its base-2 LSE, and merge_splits_kernel combines them.
+//  * Every mbarrier wait is bounded: on time-out the kernel records
+//    GQA_ERR_DEVICE_TIMEOUT, waits for its own TMA copies in flight, frees its
+//    tensor memory and returns.
+
+#include "gqa_internal.h"
+#include "gqa_prefill.h"
+#include "sm100_ptx.cuh"
+
+namespace gqa {
+
+namespace {
+
+constexpr int kStages = 5;
+constexpr uint32_t kQChunkBytes = 128 * 128;   // 128 rows x 64 bf16 (one 128B-swizzle column)
+constexpr uint32_t kQBoxBytes = 126 * 128;     // the 21x6 rows one TMA box writes
+constexpr uint32_t kQBytes = 4 * kQChunkBytes;  // d = 256 -> 4 chunks
+constexpr uint32_t kStageBytes = 32768;
+constexpr uint32_t kKBoxBytes = 128 * 128;     // 128 keys x 64 d
+constexpr uint32_t kVBoxBytes = 64 * 128;      // 64 keys x 64 d
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 0;
+constexpr uint32_t kTmemS = 256;  // S buffer b at kTmemS + 128*b
+
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffStages = kOffQ + kQBytes;
+constexpr uint32_t kOffBars = kOffStages + kStages * kStageBytes;
+enum BarId : uint32_t {
+  kBarFull = 0,                 // [kStages] stage loaded (TMA tx)
+  kBarEmpty = kStages,          // [kStages] stage consumed (MMA commit)
+  kBarQFull = 2 * kStages,      // Q tile loaded
+  kBarQEmpty,                   // last QK^T of the unit done with Q
+  kBarSFull0,                   // [2] S buffer holds a finished QK^T
+  kBarSFull1,
+  kBarPFull0,                   // [2] P written, O corrected (128 softmax arrivals)
+  kBarPFull1,
+  kBarODone,                    // a PV MMA completed
+  kBarOFree,                    // epilogue finished reading O (128 arrivals)
+  kBarDrain,                    // MMA warp's final drain
+  kNumBars
+};
+constexpr uint32_t kOffTmemSlot = kOffBars + kNumBars * 8;
+constexpr uint32_t kSmemUsed = kOffTmemSlot + 16;
+constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base up to 1024
+
+constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
+constexpr float kLn2 = 0.693147180559945309f;
+
+__device__ int g_status_word = 0;
+
+struct Unit {
+  int g, qt, split, n0, n1;
+};
+
+// Units are numbered longest-first: q tiles from the last (most keys) down,
+// then KV group, then split.
+__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
+  const int per_qt = kKvHeads * p.splits;
+  Unit w;
+  w.qt = p.n_qtiles - 1 - u / per_qt;
+  const int rem = u % per_qt;
+  w.g = rem / p.splits;
+  w.split = rem % p.splits;
+  const int tok_end = min((w.qt + 1) * kTokPerTile, p.q_len);
+  const int nt = (p.p0 + tok_end + kBlockN - 1) / kBlockN;
+  w.n0 = static_cast<int>(static_cast<long long>(w.split) * nt / p.splits);
+  w.n1 = static_cast<int>(static_cast<long long>(w.split + 1) * nt / p.splits);
+  return w;
+}
+
+// Round r of CTA b in a snake order (alternate direction every round).
+__device__ __forceinline__ int unit_of(int b, int r, int G) {
+  return r * G + ((r & 1) ? (G - 1 - b) : b);
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const FwdParams& p) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((spin & 31u) == 0 && ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+      atomicExch(p.status, static_cast<int>(GQA_ERR_DEVICE_TIMEOUT));
+      return false;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw_base + 1023u) & ~1023u;
+  uint8_t* const smem = smem_raw + (base - raw_base);
+  const uint32_t q_smem = base + kOffQ;
+  const uint32_t stage_smem = base + kOffStages;
+  auto bar = [&](uint32_t id) { return base + kOffBars + 8u * id; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmemSlot);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- set-up: barriers, idle Q rows, tensor memory -------------------------
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(bar(kBarFull + s), 1);
+      ptx::mbar_init(bar(kBarEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(kBarQFull), 1);
+    ptx::mbar_init(bar(kBarQEmpty), 1);
+    ptx::mbar_init(bar(kBarSFull0), 1);
+    ptx::mbar_init(bar(kBarSFull1), 1);
+    ptx::mbar_init(bar(kBarPFull0), 4 * 32);
+    ptx::mbar_init(bar(kBarPFull1), 4 * 32);
+    ptx::mbar_init(bar(kBarODone), 1);
+    ptx::mbar_init(bar(kBarOFree), 4 * 32);
+    ptx::mbar_init(bar(kBarDrain), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp < 4) {
+    // Rows 126 and 127 of each Q chunk are never written by TMA: zero them once.
+    for (int i = threadIdx.x; i < 4 * 2 * 128 / 16; i += 128) {
+      const int chunk = i / 16, off = (i % 16) * 16;
+      *reinterpret_cast<uint4*>(smem + kOffQ + chunk * kQChunkBytes + kQBoxBytes + off) =
+          make_uint4(0, 0, 0, 0);
+    }
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int G = gridDim.x;
+
+  if (warp == kTmaWarp) {
+    // ======================= TMA producer ======================================
+    if (lane == 0) {
+      ptx::prefetch_tmap(&p.tmap_q);
+      ptx::prefetch_tmap(&p.tmap_k);
+      ptx::prefetch_tmap(&p.tmap_v);
+      const uint64_t pol_kv = ptx::policy_evict_last();
+      const uint64_t pol_q = ptx::policy_evict_first();
+      uint32_t st = 0, phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load issued / its phase
+      bool q_issued = false;
+      uint32_t q_parity = 0;
+      bool ok = true;
+      auto next_stage = [&](int n, bool is_k, int g) -> bool {
+        // Two 32 KB stages per K tile (d halves) and per V tile (key halves).
+        for (int half = 0; half < 2; ++half) {
+          if (!wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
+          const uint32_t fb = bar(kBarFull + st);
+          const uint32_t dst = stage_smem + st * kStageBytes;
+          ptx::mbar_arrive_expect_tx(fb, kStageBytes);
+          if (is_k) {
+            for (int c = 0; c < 2; ++c)
+              ptx::tma_load_3d(dst + c * kKBoxBytes, &p.tmap_k, fb, 128 * half + 64 * c, g,
+                               n * kBlockN, pol_kv);
+          } else {
+            for (int c = 0; c < 4; ++c)
+              ptx::tma_load_3d(dst + c * kVBoxBytes, &p.tmap_v, fb, 64 * c, g,
+                               n * kBlockN + 64 * half, pol_kv);
+          }
+          issued_mask |= 1u << st;
+          issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
+          if (++st == kStages) { st = 0; phase ^= 1u; }
+        }
+        return true;
+      };
+      int k = 0;
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of(blockIdx.x, r, G);
+        if (u >= p.n_units) break;
+        const Unit w = decode_unit(p, u);
+        if (k > 0 && !(ok = wait_bar(bar(kBarQEmpty), (k - 1) & 1, p))) break;
+        ptx::mbar_arrive_expect_tx(bar(kBarQFull), 4 * kQBoxBytes);
+        for (int c = 0; c < 4; ++c)
+          ptx::tma_load_3d(q_smem + c * kQChunkBytes, &p.tmap_q, bar(kBarQFull), 64 * c,
+                           kGroup * w.g, kTokPerTile * w.qt, pol_q);
+        q_issued = true;
+        q_parity = k & 1;
+        // Consumption order of the MMA warp: K0, K1, V0, K2, V1, ..., V(nt-1).
+        const int nt = w.n1 - w.n0;
+        for (int j = 0; j < nt && ok; ++j) {
+          ok = next_stage(w.n0 + j, true, w.g);
+          if (ok && j >= 1) ok = next_stage(w.n0 + j - 1, false, w.g);
+        }
+        if (ok) ok = next_stage(w.n1 - 1, false, w.g);
+        ++k;
+      }
+      if (!ok) {
+        // Give up: let every copy already issued land before the CTA exits.
+        for (int s = 0; s < kStages; ++s)
+          if (issued_mask & (1u << s)) wait_bar(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
+        if (q_issued) wait_bar(bar(kBarQFull), q_parity, p);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ======================= MMA issuer ========================================
+    if (lane == 0) {
+      uint32_t st = 0, phase = 0;
+      uint32_t tile = 0;  // tiles processed by this CTA so far (selects S buffer)
+      bool ok = true;
+      int k = 0;
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of(blockIdx.x, r, G);
+        if (u >= p.n_units) break;
+        const Unit w = decode_unit(p, u);
+        const int nt = w.n1 - w.n0;
+        if (!(ok = wait_bar(bar(kBarQFull), k & 1, p))) break;
+        ptx::tc_fence_after();
+        // S_b = Q K_j^T over d = 256: two stages (d halves) x 2 chunks x 4 k-steps of 16.
+        auto issue_qk = [&](int j) -> bool {
+          const uint32_t b = (tile + j) & 1u;
+          const uint32_t d_tmem = tmem + kTmemS + 128u * b;
+          for (int half = 0; half < 2; ++half) {
+            if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
+            ptx::tc_fence_after();
+            const uint32_t kst = stage_smem + st * kStageBytes;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t a = ptx::smem_desc(q_smem + (2 * half + c) * kQChunkBytes + 32 * kk,
+                                                  16, 1024, ptx::kSwizzle128B);
+                const uint64_t bd = ptx::smem_desc(kst + c * kKBoxBytes + 32 * kk, 16, 1024,
+                                                   ptx::kSwizzle128B);
+                ptx::mma_ss(d_tmem, a, bd, kIdescQK, (half | c | kk) != 0);
+              }
+            }
+            ptx::tc_commit(bar(kBarEmpty + st));
+            if (++st == kStages) { st = 0; phase ^= 1u; }
+          }
+          ptx::tc_commit(bar(b ? kBarSFull1 : kBarSFull0));
+          if (j == nt - 1) ptx::tc_commit(bar(kBarQEmpty));
+          return true;
+        };
+        ok = issue_qk(0);
+        if (ok && nt > 1) ok = issue_qk(1);
+        for (int j = 0; j < nt && ok; ++j) {
+          const uint32_t T = tile + j;
+          const uint32_t b = T & 1u;
+          if (!(ok = wait_bar(bar(b ? kBarPFull1 : kBarPFull0), (T >> 1) & 1u, p))) break;
+          if (j == 0 && k > 0 && !(ok = wait_bar(bar(kBarOFree), (k - 1) & 1, p))) break;
+          ptx::tc_fence_after();
+          // O += P_j V_j: two stages (key halves) x 4 k-steps of 16 keys, N = 256.
+          for (int half = 0; half < 2 && ok; ++half) {
+            if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
+            ptx::tc_fence_after();
+            const uint32_t vst = stage_smem + st * kStageBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              // V stage: 4 boxes (64-wide d chunks, 8 KB apart) of 64 keys x 128 B.
+              // MN-major B: LBO = next d chunk, SBO = next group of 8 keys.
+              const uint64_t bd = ptx::smem_desc(vst + 2048 * kk, kVBoxBytes, 1024,
+                                                 ptx::kSwizzle128B);
+              const uint32_t a_tmem = tmem + kTmemS + 128u * b + 32u * half + 8u * kk;
+              ptx::mma_ts(tmem + kTmemO, a_tmem, bd, kIdescPV, (j | half | kk) != 0);
+            }
+            ptx::tc_commit(bar(kBarEmpty + st));
+            if (++st == kStages) { st = 0; phase ^= 1u; }
+          }
+          if (!ok) break;
+          ptx::tc_commit(bar(kBarODone));
+          if (j + 2 < nt) ok = issue_qk(j + 2);
+        }
+        tile += nt;
+        ++k;
+      }
+      // Drain: every MMA issued above has completed once this barrier fires.
+      ptx::tc_commit(bar(kBarDrain));
+      wait_bar(bar(kBarDrain), 0, p);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax + correction + epilogue (warps 0-3) =======
+    const int row = threadIdx.x;  // MMA row == tensor-memory lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int tl = row / kGroup;
+    const int hj = row - tl * kGroup;
+    const float sl2 = p.scale_log2;
+    uint32_t tile = 0;
+    int k = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int u = unit_of(blockIdx.x, r, G);
+      if (u >= p.n_units) break;
+      const Unit w = decode_unit(p, u);
+      const int nt = w.n1 - w.n0;
+      const int tok = kTokPerTile * w.qt + tl;
+      const bool valid = row < kTokPerTile * kGroup && tok < p.q_len;
+      const int pos = p.p0 + tok;                          // last key this row may see
+      const int tile_min_pos = p.p0 + kTokPerTile * w.qt;  // smallest such key in the tile
+      float m_ref = kNegInf;  // max used in the exponent (base-2, scaled)
+      float l = 0.0f;         // running row sum of p
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t T = tile + j;
+        const uint32_t b = T & 1u;
+        ok = __all_sync(0xffffffffu, wait_bar(bar(b ? kBarSFull1 : kBarSFull0), (T >> 1) & 1u, p));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t sr[128];
+        ptx::tmem_ld_x128(lane_addr + kTmemS + 128u * b, sr);
+        float s[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        const int key0 = (w.n0 + j) * kBlockN;
+        if (key0 + kBlockN - 1 > tile_min_pos) {
+          // Diagonal tile: keys after this row's position are masked out.
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (key0 + c > pos) s[c] = kNegInf;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float m_new = fmaxf(m_ref, m_tile);
+        const bool need = m_new > m_ref + kRescaleThreshold;
+        if (j == 0) {
+          if (need) m_ref = m_new;  // O is overwritten by this unit's first PV
+        } else if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ptx::ex2_approx(m_ref - m_new) : 1.0f;
+          if (need) m_ref = m_new;
+          l *= alpha;
+          // O must hold PV_{j-1} before it is rescaled.
+          ok = __all_sync(0xffffffffu, wait_bar(bar(kBarODone), (T - 1) & 1u, p));
+          if (!ok) break;
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 256; c += 32) {
+            uint32_t o[32];
+            ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st_x32(lane_addr + kTmemO + c, o);
+          }
+          ptx::tmem_st_wait();
+        }
+        const float m_use = (m_ref == kNegInf) ? 0.0f : m_ref;
+        uint32_t pk[64];
+        float sum0 = 0.0f, sum1 = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float e0 = ptx::ex2_approx(fmaf(s[2 * c], sl2, -m_use));
+          const float e1 = ptx::ex2_approx(fmaf(s[2 * c + 1], sl2, -m_use));
+          sum0 += e0;
+          sum1 += e1;
+          pk[c] = ptx::pack_bf16x2(e0, e1);
+        }
+        l += sum0 + sum1;
+        ptx::tmem_st_x64(lane_addr + kTmemS + 128u * b, pk);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(b ? kBarPFull1 : kBarPFull0));
+      }
+      if (!ok) break;
+      // ---- epilogue: O / l -> out (or the split partial), LSE ----------------
+      ok = __all_sync(0xffffffffu, wait_bar(bar(kBarODone), (tile + nt - 1) & 1u, p));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+      const float lse2 = l > 0.0f ? m_ref + __log2f(l) : kNegInf;
+      const size_t qrow = static_cast<size_t>(tok) * kQHeads + kGroup * w.g + hj;
+      if (p.splits == 1) {
+        __nv_bfloat16* dst = p.out + qrow * kHeadDim;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
+          if (valid) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              pk[e] = ptx::pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
+                                       __uint_as_float(o[2 * e + 1]) * inv_l);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          }
+        }
+        if (valid && p.lse != nullptr) p.lse[qrow] = lse2 * kLn2;
+      } else {
+        const size_t prow = static_cast<size_t>(w.split) * p.q_len * kQHeads + qrow;
+        float* dst = p.part_o + prow * kHeadDim;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t o[32];
+          ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
+          if (valid) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              d4[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l,
+                                  __uint_as_float(o[4 * e + 1]) * inv_l,
+                                  __uint_as_float(o[4 * e + 2]) * inv_l,
+                                  __uint_as_float(o[4 * e + 3]) * inv_l);
+          }
+        }
+        if (valid) p.part_lse[prow] = lse2;
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(kBarOFree));
+      tile += nt;
+      ++k;
+    }
+  }
+
+  // ---- teardown ----------------------------------------------------------------
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Combine split-KV partials: lse = log2 sum_s 2^{lse_s}; out = sum_s 2^{lse_s - lse} O_s.
+// One warp per (token, head) row, 8 consecutive d per lane; fixed split order.
+__global__ void __launch_bounds__(256) merge_splits_kernel(const MergeParams p) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= p.rows) return;
+  float mx = kNegInf;
+  for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(s) * p.rows + row]);
+  const float m_use = (mx == kNegInf) ? 0.0f : mx;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float wsum = 0.0f;
+  for (int s = 0; s < p.splits; ++s) {
+    const size_t prow = static_cast<size_t>(s) * p.rows + row;
+    const float w = ptx::ex2_approx(p.part_lse[prow] - m_use);
+    wsum += w;
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * kHeadDim + 8 * lane);
+    const float4 a = src[0], b = src[1];
+    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+    acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+  }
+  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+  uint4 o;
+  o.x = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  o.y = ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  o.z = ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  o.w = ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(row) * kHeadDim + 8 * lane) = o;
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[row] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;
+}
+
+}  // namespace
+
+size_t fwd_smem_bytes() { return kSmemAlloc; }
+
+cudaError_t prepare_fwd_kernel() {
+  return cudaFuncSetAttribute(gqa_attn_fwd_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmemAlloc));
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
+  gqa_attn_fwd_sm103_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+  const int blocks = (p.rows + 7) / 8;
+  merge_splits_kernel<<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t status_word_address(int** ptr) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(ptr), g_status_word);
+}
+
+}  // namespace gqa

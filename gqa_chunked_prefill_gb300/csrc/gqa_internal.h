@@ -1,0 +1,58 @@
+// Internal interface between the host library (gqa_prefill_host.cu) and the
+// device kernels (attn_fwd_sm103.cu). Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace gqa {
+
+// Fixed problem geometry (the only shape the library accepts).
+constexpr int kHeadDim = 256;
+constexpr int kQHeads = 24;
+constexpr int kKvHeads = 4;
+constexpr int kGroup = kQHeads / kKvHeads;  // 6 query heads per KV head
+// One MMA M tile of 128 rows holds 21 tokens x 6 heads = 126 rows (+2 idle rows).
+constexpr int kTokPerTile = 21;
+constexpr int kRowsPerTile = 128;
+constexpr int kBlockN = 128;  // keys per KV tile
+
+constexpr int kThreads = 192;  // 4 softmax warps, 1 TMA warp, 1 MMA warp
+
+struct FwdParams {
+  CUtensorMap tmap_q;  // Q [q_len][24][256], box (64 d, 6 heads, 21 tokens), 128B swizzle
+  CUtensorMap tmap_k;  // K [kv_len][4][256], box (64 d, 1 head, 128 keys), 128B swizzle
+  CUtensorMap tmap_v;  // V [kv_len][4][256], box (64 d, 1 head, 64 keys), 128B swizzle
+  __nv_bfloat16* out;  // [q_len][24][256]                 (splits == 1)
+  float* lse;          // [q_len][24] natural log, or null  (splits == 1)
+  float* part_o;       // [splits][q_len][24][256] normalised partial O (splits > 1)
+  float* part_lse;     // [splits][q_len][24] base-2 partial LSE        (splits > 1)
+  int* status;         // per-device status word
+  int q_len;
+  int kv_len;
+  int p0;              // kv_len - q_len: position of the chunk's first token
+  int n_qtiles;        // ceil(q_len / 21)
+  int splits;
+  int n_units;         // n_qtiles * 4 * splits
+  float scale_log2;    // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+struct MergeParams {
+  const float* part_o;
+  const float* part_lse;
+  __nv_bfloat16* out;
+  float* lse;  // may be null
+  int rows;    // q_len * 24
+  int splits;
+};
+
+size_t fwd_smem_bytes();
+cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t prepare_fwd_kernel();                // per-device one-time attributes
+cudaError_t status_word_address(int** ptr);      // device address of the status word
+
+}  // namespace gqa

@@ -1,0 +1,132 @@
+/*
+ * gqa_prefill.h — C ABI of the GB300 (sm_103a) chunked-prefill causal GQA
+ * attention library (libgqa_prefill.so).
+ *
+ * The operation (DCU使用技术报告（中篇）：gfx936 DCU上的Qwen3.5-27B Triton-ROCm
+ * Attention与GEMV深度优化实战, §2 "专用 Prefill Attention"): one sequence, BF16,
+ * 24 query heads / 4 KV heads / head_dim 256 (GQA ratio 6, same report §1);
+ * QK^T, causal mask, online softmax and PV with FP32 accumulation. Query head h
+ * reads KV head h/6 (gfx936 DCU上实现INT8 QK MMAC：分页访存、Fragment映射与GQA适配,
+ * §5.2). The q_len new tokens of the chunk sit at the END of the kv_len-long
+ * K/V prefix (the prefix already holds the chunk's own keys), so query token t
+ * has absolute position kv_len - q_len + t and sees keys 0 .. kv_len - q_len + t
+ * (DCU report, §3: later chunks of a request see a longer kv_len).
+ *
+ * Shapes outside that contract are refused, never silently mapped (DCU report
+ * §2: unsupported shapes fall back; INT8 QK MMAC page §7: wrong layouts are
+ * rejected rather than run with a wrong mapping). This library has no fallback:
+ * a refused call returns an error code and launches nothing.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE memory on the current CUDA device, owned
+ *    by the caller; the library keeps no reference after the call returns.
+ *  - Tensors are dense, row-major, no padding:
+ *        q, out : [q_len,  n_q_heads,  head_dim]  BF16
+ *        k, v   : [kv_len, n_kv_heads, head_dim]  BF16
+ *        lse    : [q_len,  n_q_heads]             FP32, natural log
+ *    Every pointer must be 16-byte aligned (the kernels move tiles with TMA).
+ *  - `stream` is a cudaStream_t (CUstream) handle; NULL means the legacy
+ *    default stream. Calls are asynchronous on that stream: they return as
+ *    soon as the work is queued. Any temporary device memory is allocated and
+ *    freed in stream order on `stream`.
+ *  - Errors found on the host are returned before anything is launched. A
+ *    device-side wait that exceeds its time limit makes the kernel give up,
+ *    record GQA_ERR_DEVICE_TIMEOUT in a per-device status word and return;
+ *    read it with gqa_prefill_poll().
+ */
+#ifndef GQA_PREFILL_H_
+#define GQA_PREFILL_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GQA_PREFILL_ABI_VERSION 1
+
+typedef enum gqa_status {
+  GQA_OK = 0,
+  GQA_ERR_NULL = 1,           /* a required pointer is NULL                           */
+  GQA_ERR_SHAPE = 2,          /* q_len < 0, kv_len < q_len, kv_len == 0 with q_len > 0,
+                                 or scale not finite and > 0                            */
+  GQA_ERR_UNSUPPORTED = 3,    /* head counts / head_dim other than 24 / 4 / 256, or no
+                                 sm_103a-class device                                  */
+  GQA_ERR_ALIGN = 4,          /* a pointer is not 16-byte aligned                      */
+  GQA_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed                     */
+  GQA_ERR_DEVICE_TIMEOUT = 6  /* a device-side wait ran out of time (see _poll)        */
+} gqa_status;
+
+/*
+ * out[t, h, :] = softmax_j( scale * q[t,h,:] . k[j, h/6, :] ) v[j, h/6, :],
+ *                j = 0 .. kv_len - q_len + t
+ * lse[t, h]    = ln sum_j exp( scale * q[t,h,:] . k[j, h/6, :] )   (same j range)
+ *
+ * q_len == 0 returns GQA_OK without launching. `lse` may be NULL.
+ * `scale` is used as given (1/sqrt(head_dim) = 1/16 for this model); it must
+ * be finite and > 0.
+ */
+gqa_status gqa_prefill_attn(const void* q, const void* k, const void* v, void* out, float* lse,
+                            int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
+                            float scale, void* stream);
+
+/* Options for gqa_prefill_attn_ex (zero-initialise; zero fields mean "default"). */
+typedef struct gqa_prefill_opts {
+  int force_splits;           /* > 0: split every KV range into this many parts
+                                 (capped so no part is empty); 0: planner decides  */
+  uint32_t wait_timeout_us;   /* bound on any single device-side wait; 0 = 2 s      */
+  void* fwd_event_begin;      /* optional cudaEvent_t recorded on `stream` right
+                                 before the attention kernel launch                */
+  void* fwd_event_end;        /* optional cudaEvent_t recorded right after it (before
+                                 the split merge, if any): times the main kernel   */
+  int reserved[4];
+} gqa_prefill_opts;
+
+/* What the planner chose (the route check: which kernel ran and how). */
+typedef struct gqa_prefill_plan {
+  int num_sms;                /* SMs the grid was sized for                          */
+  int q_tiles;                /* ceil(q_len / 21): 21 tokens x 6 heads = 126 MMA rows */
+  int n_items;                /* q_tiles * n_kv_heads                                 */
+  int splits;                 /* KV splits per item (1 = no split, no merge kernel)   */
+  int n_units;                /* n_items * splits: work units of the persistent grid  */
+  int grid;                   /* CTAs launched for the attention kernel               */
+  int kernels_per_call;       /* launches per call: 1, or 2 with the split merge      */
+  int variant;                /* 1 = tcgen05 1-CTA M=128 kernel                       */
+  int64_t workspace_bytes;    /* temporary FP32 split partials (0 when splits == 1)   */
+  int64_t est_makespan_tiles; /* planner's cost of the busiest CTA, in KV tiles       */
+} gqa_prefill_plan;
+
+/* gqa_prefill_attn with options; `opts` and `plan_out` may each be NULL. */
+gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+                               int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
+                               float scale, void* stream, const gqa_prefill_opts* opts,
+                               gqa_prefill_plan* plan_out);
+
+/*
+ * Host-only planning (no CUDA call): fills *plan for a device with `num_sms`
+ * SMs exactly as gqa_prefill_attn_ex would. Validates shapes like the
+ * attention call (pointers are not involved).
+ */
+gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
+                                 int num_sms, int force_splits, gqa_prefill_plan* plan);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word (0 or GQA_ERR_DEVICE_TIMEOUT) into *device_status. Returns GQA_ERR_CUDA
+ * if the synchronisation itself fails. The status word is shared by all
+ * streams of the device: it reports any kernel of this library that gave up
+ * since the previous poll.
+ */
+gqa_status gqa_prefill_poll(void* stream, int* device_status);
+
+/* Static description of a status code (never NULL). */
+const char* gqa_status_string(gqa_status status);
+
+/* GQA_PREFILL_ABI_VERSION of the loaded library. */
+int gqa_prefill_abi_version(void);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* GQA_PREFILL_H_ */

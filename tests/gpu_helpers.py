@@ -1,0 +1,51 @@
+"""Shared helpers for the GPU tests: run the CUDA path through the C ABI and
+compare it with the FP64 oracle at the acceptance tolerance.
+
+Acceptance (elementwise on O, mean on O, absolute on LSE):
+    |out - ref| <= 1e-2 + 1e-2 * |ref|,  mean |out - ref| <= 2e-3,  |lse - ref| <= 1e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+ATOL, RTOL, MEAN_TOL, LSE_TOL = 1e-2, 1e-2, 2e-3, 1e-3
+
+
+def run_gpu(q, k, v, scale, force_splits=0, with_lse=True, stream=None):
+    """q, k, v: CPU or CUDA bf16. Returns (out bf16 CUDA, lse fp32 CUDA or None, plan)."""
+    import gqa_chunked_prefill_gb300 as gqa
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (t.to(dev).contiguous() for t in (q, k, v))
+    q_len, hq, d = qd.shape
+    kv_len, hkv, _ = kd.shape
+    out = torch.empty_like(qd)
+    lse = torch.empty((q_len, hq), dtype=torch.float32, device=dev) if with_lse else None
+    _, plan = gqa.gqa_prefill_attn_ex(qd, kd, vd, out, lse, q_len, kv_len, hq, hkv, d, scale,
+                                      stream=stream, force_splits=force_splits)
+    torch.cuda.synchronize()
+    assert gqa.gqa_prefill_poll() == 0, "device-side wait timed out"
+    return out, lse, plan
+
+
+def check_close(out_rows: np.ndarray, lse_rows, ref_out: np.ndarray, ref_lse, what: str = ""):
+    """out_rows/ref_out: [..., d] float64; lse: [...] or None."""
+    err = np.abs(out_rows - ref_out)
+    bound = ATOL + RTOL * np.abs(ref_out)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert np.all(err <= bound), (
+        f"{what}: elementwise tolerance exceeded at {worst}: got {out_rows[worst]}, "
+        f"ref {ref_out[worst]}, max err {err.max():.3e}")
+    assert err.mean() <= MEAN_TOL, f"{what}: mean |err| {err.mean():.3e} > {MEAN_TOL}"
+    if lse_rows is not None:
+        lerr = np.abs(lse_rows - ref_lse)
+        assert np.all(lerr <= LSE_TOL), f"{what}: LSE max err {lerr.max():.3e}"
+
+
+def gather_rows(out: torch.Tensor, lse, rows):
+    """Rows t*Hq + h of out [q_len,Hq,d] / lse [q_len,Hq] as float64 numpy."""
+    hq, d = out.shape[1], out.shape[2]
+    r = torch.as_tensor(rows, dtype=torch.int64, device=out.device)
+    o = out.reshape(-1, d).index_select(0, r).double().cpu().numpy()
+    l = lse.reshape(-1).index_select(0, r).double().cpu().numpy() if lse is not None else None
+    return o, l

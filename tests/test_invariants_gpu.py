@@ -1,0 +1,92 @@
+"""GPU invariants of the CUDA path: determinism, causality (bit-exact), split
+agreement, the ABI's refusals and empty chunks, and the route check (the plan
+the library reports for the call that ran)."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_inputs import WORKLOADS, make_qkv, make_workload
+from tests.gpu_helpers import check_close, run_gpu
+
+pytestmark = pytest.mark.gpu
+SCALE = 1.0 / 16.0
+
+
+@pytest.mark.parametrize("name", ["q512_kv4096_kbias", "q4096_kv8192", "q512_kv32768"])
+def test_run_twice_bit_identical(cuda_device, name):
+    q, k, v = make_workload(WORKLOADS[name])
+    o1, l1, _ = run_gpu(q, k, v, SCALE)
+    o2, l2, _ = run_gpu(q, k, v, SCALE)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("q_len,kv_len,t_star", [(100, 700, 40), (300, 300, 150), (512, 4096, 200)])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_future_keys_leave_earlier_rows_bit_identical(cuda_device, q_len, kv_len, t_star, splits):
+    q, k, v = make_qkv(q_len, kv_len, seed=q_len + kv_len)
+    o1, l1, _ = run_gpu(q, k, v, SCALE, force_splits=splits)
+    p_star = kv_len - q_len + t_star
+    k2, v2 = k.clone(), v.clone()
+    k2[p_star + 1:] = (k2[p_star + 1:].float() * 3.0 + 1.0).to(torch.bfloat16)
+    v2[p_star + 1:] = (-v2[p_star + 1:].float() + 2.0).to(torch.bfloat16)
+    o2, l2, _ = run_gpu(q, k2, v2, SCALE, force_splits=splits)
+    assert torch.equal(o1[: t_star + 1], o2[: t_star + 1])
+    assert torch.equal(l1[: t_star + 1], l2[: t_star + 1])
+    assert not torch.equal(o1[t_star + 1:], o2[t_star + 1:])
+
+
+def test_split_and_unsplit_agree(cuda_device):
+    w = WORKLOADS["q512_kv4096_kbias"]
+    q, k, v = make_workload(w)
+    o1, l1, p1 = run_gpu(q, k, v, SCALE, force_splits=1)
+    o4, l4, p4 = run_gpu(q, k, v, SCALE, force_splits=4)
+    assert p1["splits"] == 1 and p4["splits"] == 4 and p4["kernels_per_call"] == 2
+    check_close(o4.double().cpu().numpy(), l4.double().cpu().numpy(),
+                o1.double().cpu().numpy(), l1.double().cpu().numpy(), "split vs unsplit")
+
+
+def test_route_check_reports_planned_kernel(cuda_device):
+    import gqa_chunked_prefill_gb300 as gqa
+    q, k, v = make_qkv(4096, 8192, seed=1)
+    _, _, plan = run_gpu(q, k, v, SCALE)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    _, host_plan = gqa.gqa_prefill_make_plan(4096, 8192, 24, 4, 256, sms)
+    assert plan == host_plan
+    assert plan["variant"] == 1 and plan["num_sms"] == sms
+    assert plan["grid"] == min(plan["n_units"], sms)
+
+
+def test_empty_chunk_is_a_no_op(cuda_device):
+    import gqa_chunked_prefill_gb300 as gqa
+    k = torch.randn(10, 4, 256, device="cuda").to(torch.bfloat16)
+    rc = gqa.gqa_prefill_attn(None, k, k, None, None, 0, 10, 24, 4, 256, SCALE, check=False)
+    assert rc == 0
+
+
+def test_refusals_launch_nothing(cuda_device):
+    import gqa_chunked_prefill_gb300 as gqa
+    from gqa_chunked_prefill_gb300 import GqaStatus as S
+    q = torch.zeros(8, 24, 256, device="cuda", dtype=torch.bfloat16)
+    kv = torch.zeros(16, 4, 256, device="cuda", dtype=torch.bfloat16)
+    out = torch.full_like(q, 7.0)
+    f = lambda *a: gqa.gqa_prefill_attn(*a, check=False)
+    assert f(q, kv, kv, out, None, 8, 7, 24, 4, 256, SCALE) == S.ERR_SHAPE
+    assert f(q, kv, kv, out, None, 8, 16, 24, 4, 128, SCALE) == S.ERR_UNSUPPORTED
+    assert f(q, kv, kv, out, None, 8, 16, 24, 8, 256, SCALE) == S.ERR_UNSUPPORTED
+    assert f(q, kv, kv, out, None, 8, 16, 24, 4, 256, -1.0) == S.ERR_SHAPE
+    assert f(q, None, kv, out, None, 8, 16, 24, 4, 256, SCALE) == S.ERR_NULL
+    assert f(q.data_ptr() + 2, kv, kv, out, None, 8, 16, 24, 4, 256, SCALE) == S.ERR_ALIGN
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)  # nothing was launched
+
+
+def test_non_default_stream(cuda_device):
+    q, k, v = make_qkv(200, 900, seed=9)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o1, l1, _ = run_gpu(q, k, v, SCALE, stream=s)
+    o0, l0, _ = run_gpu(q, k, v, SCALE)
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
