@@ -177,6 +177,21 @@ def oracle_sample(w, q, k, v, target_s: float, seed: int = 17):
     return flops / secs / 1e12, cores, desc, len(rows), secs
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """MAX of a per-rank number over all ranks (identity when not distributed)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, flops_per_replica: int, max_ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every replica's work over the slowest rank's time."""
+    return world * flops_per_replica / (max_ms_per_step * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -232,6 +247,10 @@ def main():
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    for e in ev:  # torch creates the CUDA event on first record; the library records f0/f1 itself
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize(dev)
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -255,11 +274,7 @@ def main():
         pg.barrier()
     step_ms = [a.elapsed_time(b) for a, b, _, _ in ev]
     fwd_ms = [a.elapsed_time(b) for _, _, a, b in ev]
-    total_ms = sum(step_ms)
-    if pg:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), pg, dev)
     if gqa.gqa_prefill_poll(stream) != 0:
         raise RuntimeError("device-side wait timed out during the timed steps")
     clocks = sampler.stop() if sampler else None
@@ -292,11 +307,7 @@ def main():
         e2e_step()
         b.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e_ev) / e2e_steps
-    if pg:
-        t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_ev) / e2e_steps, pg, dev)
 
     if rank != 0:
         if pg:
@@ -305,7 +316,7 @@ def main():
 
     peaks, peak_kind = load_peaks()
     ms_per_step = total_ms / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(world, flops, ms_per_step)
     fwd_avg_ms = sum(fwd_ms) / len(fwd_ms)
     achieved = flops / (fwd_avg_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -346,7 +357,7 @@ def main():
             "kernel_ms": round(fwd_avg_ms, 4),
         },
         "e2e": {
-            "value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2),
+            "value": round(job_throughput(world, flops, e2e_ms), 2),
             "unit": UNIT,
             "ms_per_step": round(e2e_ms, 4),
             "h2d_bytes_per_step": h2d,

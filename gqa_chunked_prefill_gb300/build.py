@@ -7,6 +7,7 @@ machine without a GPU (it only needs the driver once a CUDA call is made).
 from __future__ import annotations
 
 import os
+import platform
 import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
@@ -16,7 +17,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgqa_prefill.so")
-BUILD_DIR = os.path.join(PKG, "_build")
+BUILD_DIR = os.path.join(PKG, "_build", platform.machine())
+STAMP = LIB + ".arch"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -39,8 +41,16 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _arch_matches() -> bool:
+    try:
+        return open(STAMP).read().strip() == platform.machine()
+    except OSError:
+        return False
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
+    force = force or not _arch_matches()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     objs, jobs = [], []
@@ -62,6 +72,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if force or jobs or _stale(LIB, objs):
         run([nvcc(), *ARCH, "-shared", "-o", LIB + ".tmp", *objs])
         os.replace(LIB + ".tmp", LIB)
+        with open(STAMP, "w") as f:
+            f.write(platform.machine())
     return LIB
 
 

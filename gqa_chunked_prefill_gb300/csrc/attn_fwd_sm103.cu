@@ -15,9 +15,14 @@
 //    becomes a 5-deep ring of 32 KB shared-memory stages fed by TMA and
 //    tracked by mbarriers; K of tile j+2 streams while V of tile j is used.
 //  * S = Q K^T and O += P V are tcgen05 MMAs (kind::f16, BF16 in, FP32 out).
-//    S is double-buffered in tensor memory (2 x 128 columns), O (128 x 256
-//    FP32) holds the other 256 columns; P is written back as BF16 over its own
-//    S buffer and fed to the PV MMA straight from tensor memory.
+//    Tensor memory (512 columns) holds O (128 x 256 FP32), one S tile
+//    (128 x 128 FP32) and two BF16 P tiles (64 columns each) that feed the PV
+//    MMA straight from tensor memory. No MMA ever writes columns that another
+//    in-flight MMA reads: the next QK^T may overwrite S as soon as the softmax
+//    has copied S into registers (s_free), and P[b] is rewritten only after
+//    the PV that read it has completed (pv_done[b]). tcgen05 only orders
+//    consecutive MMAs that share accumulator and shape, so these two barriers
+//    are what makes the S -> QK^T and P -> PV reuse safe.
 //  * Warp specialisation: warp 4 issues TMA, warp 5 issues MMAs (one thread),
 //    warps 0-3 run the softmax with one thread per MMA row (tensor-memory lane),
 //    so row max and row sum need no cross-thread reduction.
@@ -51,8 +56,9 @@ constexpr uint32_t kKBoxBytes = 128 * 128;     // 128 keys x 64 d
 constexpr uint32_t kVBoxBytes = 64 * 128;      // 64 keys x 64 d
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;
-constexpr uint32_t kTmemS = 256;  // S buffer b at kTmemS + 128*b
+constexpr uint32_t kTmemO = 0;    // O: 256 FP32 columns
+constexpr uint32_t kTmemS = 256;  // S: 128 FP32 columns
+constexpr uint32_t kTmemP = 384;  // P buffer b: 64 columns of packed BF16 pairs at kTmemP + 64*b
 
 constexpr int kTmaWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -66,11 +72,12 @@ enum BarId : uint32_t {
   kBarEmpty = kStages,          // [kStages] stage consumed (MMA commit)
   kBarQFull = 2 * kStages,      // Q tile loaded
   kBarQEmpty,                   // last QK^T of the unit done with Q
-  kBarSFull0,                   // [2] S buffer holds a finished QK^T
-  kBarSFull1,
-  kBarPFull0,                   // [2] P written, O corrected (128 softmax arrivals)
+  kBarSFull,                    // S holds a finished QK^T (MMA commit)
+  kBarSFree,                    // softmax copied S to registers (128 arrivals)
+  kBarPFull0,                   // [2] P[b] written, O corrected (128 arrivals)
   kBarPFull1,
-  kBarODone,                    // a PV MMA completed
+  kBarPvDone0,                  // [2] the PV that read P[b] completed (MMA commit)
+  kBarPvDone1,
   kBarOFree,                    // epilogue finished reading O (128 arrivals)
   kBarDrain,                    // MMA warp's final drain
   kNumBars
@@ -147,11 +154,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(bar(kBarQFull), 1);
     ptx::mbar_init(bar(kBarQEmpty), 1);
-    ptx::mbar_init(bar(kBarSFull0), 1);
-    ptx::mbar_init(bar(kBarSFull1), 1);
+    ptx::mbar_init(bar(kBarSFull), 1);
+    ptx::mbar_init(bar(kBarSFree), 4 * 32);
     ptx::mbar_init(bar(kBarPFull0), 4 * 32);
     ptx::mbar_init(bar(kBarPFull1), 4 * 32);
-    ptx::mbar_init(bar(kBarODone), 1);
+    ptx::mbar_init(bar(kBarPvDone0), 1);
+    ptx::mbar_init(bar(kBarPvDone1), 1);
     ptx::mbar_init(bar(kBarOFree), 4 * 32);
     ptx::mbar_init(bar(kBarDrain), 1);
     ptx::fence_mbar_init();
@@ -241,9 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ======================= MMA issuer ========================================
+    // Issue order per unit: QK_0, then for each tile j: QK_{j+1}, PV_j. QK_{j+1}
+    // runs on the tensor pipe while the softmax of tile j is in flight.
     if (lane == 0) {
       uint32_t st = 0, phase = 0;
-      uint32_t tile = 0;  // tiles processed by this CTA so far (selects S buffer)
+      uint32_t tile = 0;  // KV tiles this CTA has processed (global tile index T)
       bool ok = true;
       int k = 0;
       for (int r = 0; ok; ++r) {
@@ -253,10 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = w.n1 - w.n0;
         if (!(ok = wait_bar(bar(kBarQFull), k & 1, p))) break;
         ptx::tc_fence_after();
-        // S_b = Q K_j^T over d = 256: two stages (d halves) x 2 chunks x 4 k-steps of 16.
+        // S = Q K_j^T over d = 256: two stages (d halves) x 2 chunks x 4 k-steps of 16.
         auto issue_qk = [&](int j) -> bool {
-          const uint32_t b = (tile + j) & 1u;
-          const uint32_t d_tmem = tmem + kTmemS + 128u * b;
+          const uint32_t T = tile + j;
+          // S may be overwritten once the softmax holds tile T-1's scores in registers.
+          if (T > 0 && !wait_bar(bar(kBarSFree), (T - 1) & 1u, p)) return false;
+          ptx::tc_fence_after();
           for (int half = 0; half < 2; ++half) {
             if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
             ptx::tc_fence_after();
@@ -269,19 +281,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   16, 1024, ptx::kSwizzle128B);
                 const uint64_t bd = ptx::smem_desc(kst + c * kKBoxBytes + 32 * kk, 16, 1024,
                                                    ptx::kSwizzle128B);
-                ptx::mma_ss(d_tmem, a, bd, kIdescQK, (half | c | kk) != 0);
+                ptx::mma_ss(tmem + kTmemS, a, bd, kIdescQK, (half | c | kk) != 0);
               }
             }
             ptx::tc_commit(bar(kBarEmpty + st));
             if (++st == kStages) { st = 0; phase ^= 1u; }
           }
-          ptx::tc_commit(bar(b ? kBarSFull1 : kBarSFull0));
+          ptx::tc_commit(bar(kBarSFull));
           if (j == nt - 1) ptx::tc_commit(bar(kBarQEmpty));
           return true;
         };
         ok = issue_qk(0);
-        if (ok && nt > 1) ok = issue_qk(1);
         for (int j = 0; j < nt && ok; ++j) {
+          if (j + 1 < nt && !(ok = issue_qk(j + 1))) break;
           const uint32_t T = tile + j;
           const uint32_t b = T & 1u;
           if (!(ok = wait_bar(bar(b ? kBarPFull1 : kBarPFull0), (T >> 1) & 1u, p))) break;
@@ -298,15 +310,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               // MN-major B: LBO = next d chunk, SBO = next group of 8 keys.
               const uint64_t bd = ptx::smem_desc(vst + 2048 * kk, kVBoxBytes, 1024,
                                                  ptx::kSwizzle128B);
-              const uint32_t a_tmem = tmem + kTmemS + 128u * b + 32u * half + 8u * kk;
+              const uint32_t a_tmem = tmem + kTmemP + 64u * b + 32u * half + 8u * kk;
               ptx::mma_ts(tmem + kTmemO, a_tmem, bd, kIdescPV, (j | half | kk) != 0);
             }
             ptx::tc_commit(bar(kBarEmpty + st));
             if (++st == kStages) { st = 0; phase ^= 1u; }
           }
           if (!ok) break;
-          ptx::tc_commit(bar(kBarODone));
-          if (j + 2 < nt) ok = issue_qk(j + 2);
+          ptx::tc_commit(bar(b ? kBarPvDone1 : kBarPvDone0));
         }
         tile += nt;
         ++k;
@@ -340,11 +351,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nt; ++j) {
         const uint32_t T = tile + j;
         const uint32_t b = T & 1u;
-        ok = __all_sync(0xffffffffu, wait_bar(bar(b ? kBarSFull1 : kBarSFull0), (T >> 1) & 1u, p));
+        ok = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull), T & 1u, p));
         if (!ok) break;
         ptx::tc_fence_after();
         uint32_t sr[128];
-        ptx::tmem_ld_x128(lane_addr + kTmemS + 128u * b, sr);
+        ptx::tmem_ld_x128(lane_addr + kTmemS, sr);  // includes tcgen05.wait::ld
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(kBarSFree));  // the next QK^T may overwrite S now
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
@@ -372,8 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float alpha = need ? ptx::ex2_approx(m_ref - m_new) : 1.0f;
           if (need) m_ref = m_new;
           l *= alpha;
-          // O must hold PV_{j-1} before it is rescaled.
-          ok = __all_sync(0xffffffffu, wait_bar(bar(kBarODone), (T - 1) & 1u, p));
+          // O must hold PV_{j-1} (which read P[(T-1)&1], use (T-1)>>1) before it is rescaled.
+          ok = __all_sync(0xffffffffu, wait_bar(bar((T - 1) & 1u ? kBarPvDone1 : kBarPvDone0),
+                                                ((T - 1) >> 1) & 1u, p));
           if (!ok) break;
           ptx::tc_fence_after();
 #pragma unroll 1
@@ -398,14 +412,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[c] = ptx::pack_bf16x2(e0, e1);
         }
         l += sum0 + sum1;
-        ptx::tmem_st_x64(lane_addr + kTmemS + 128u * b, pk);
+        if (T >= 2) {
+          // P[b] was last read by PV_{T-2}: it must have completed before P[b] is rewritten.
+          ok = __all_sync(0xffffffffu, wait_bar(bar(b ? kBarPvDone1 : kBarPvDone0),
+                                                ((T - 2) >> 1) & 1u, p));
+          if (!ok) break;
+          ptx::tc_fence_after();
+        }
+        ptx::tmem_st_x64(lane_addr + kTmemP + 64u * b, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(b ? kBarPFull1 : kBarPFull0));
       }
       if (!ok) break;
       // ---- epilogue: O / l -> out (or the split partial), LSE ----------------
-      ok = __all_sync(0xffffffffu, wait_bar(bar(kBarODone), (tile + nt - 1) & 1u, p));
+      const uint32_t T_last = tile + nt - 1;
+      ok = __all_sync(0xffffffffu, wait_bar(bar(T_last & 1u ? kBarPvDone1 : kBarPvDone0),
+                                            (T_last >> 1) & 1u, p));
       if (!ok) break;
       ptx::tc_fence_after();
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;

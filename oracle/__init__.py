@@ -13,6 +13,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 from typing import Optional, Tuple
 
@@ -28,11 +29,19 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the oracle with the host C++ compiler (plain -O2, no fast-math,
     no FMA contraction, so x86 and Arm hosts give the same bits)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    stamp = _LIB + ".arch"
+    try:
+        same_arch = open(stamp).read().strip() == platform.machine()
+    except OSError:
+        same_arch = False
+    if (force or not same_arch or not os.path.exists(_LIB)
+            or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)):
         cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
                "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", _LIB + ".tmp"]
         subprocess.run(cmd, check=True)
         os.replace(_LIB + ".tmp", _LIB)
+        with open(stamp, "w") as f:
+            f.write(platform.machine())
     return _LIB
 
 

@@ -13,8 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def gqa():
-    from gqa_chunked_prefill_gb300.build import build
-    build()
+    import __graft_entry__
+    __graft_entry__.build()
     import gqa_chunked_prefill_gb300 as mod
     return mod
 
