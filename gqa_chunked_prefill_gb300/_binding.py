@@ -34,7 +34,7 @@ class GqaError(RuntimeError):
 class PrefillOpts(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int), ("wait_timeout_us", ctypes.c_uint32),
                 ("fwd_event_begin", ctypes.c_void_p), ("fwd_event_end", ctypes.c_void_p),
-                ("reserved", ctypes.c_int * 4)]
+                ("test_withhold_q", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
 
 
 class PrefillPlan(ctypes.Structure):
@@ -109,10 +109,11 @@ def gqa_prefill_attn(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, he
 
 def gqa_prefill_attn_ex(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
                         stream=None, force_splits=0, wait_timeout_us=0, fwd_events=None,
-                        check=True):
+                        test_withhold_q=False, check=True):
     """fwd_events: optional (begin, end) torch.cuda.Event pair recorded around the
     attention kernel itself (not the split merge)."""
-    opts = PrefillOpts(force_splits=force_splits, wait_timeout_us=wait_timeout_us)
+    opts = PrefillOpts(force_splits=force_splits, wait_timeout_us=wait_timeout_us,
+                       test_withhold_q=1 if test_withhold_q else 0)
     if fwd_events is not None:
         opts.fwd_event_begin = fwd_events[0].cuda_event
         opts.fwd_event_end = fwd_events[1].cuda_event

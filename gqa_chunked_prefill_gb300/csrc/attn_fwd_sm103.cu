@@ -224,12 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u >= p.n_units) break;
         const Unit w = decode_unit(p, u);
         if (k > 0 && !(ok = wait_bar(bar(kBarQEmpty), (k - 1) & 1, p))) break;
-        ptx::mbar_arrive_expect_tx(bar(kBarQFull), 4 * kQBoxBytes);
-        for (int c = 0; c < 4; ++c)
-          ptx::tma_load_3d(q_smem + c * kQChunkBytes, &p.tmap_q, bar(kBarQFull), 64 * c,
-                           kGroup * w.g, kTokPerTile * w.qt, pol_q);
-        q_issued = true;
-        q_parity = k & 1;
+        if (!(p.withhold_q && k == 0)) {
+          ptx::mbar_arrive_expect_tx(bar(kBarQFull), 4 * kQBoxBytes);
+          for (int c = 0; c < 4; ++c)
+            ptx::tma_load_3d(q_smem + c * kQChunkBytes, &p.tmap_q, bar(kBarQFull), 64 * c,
+                             kGroup * w.g, kTokPerTile * w.qt, pol_q);
+          q_issued = true;
+          q_parity = k & 1;
+        }
         // Consumption order of the MMA warp: K0, K1, V0, K2, V1, ..., V(nt-1).
         const int nt = w.n1 - w.n0;
         for (int j = 0; j < nt && ok; ++j) {
@@ -239,12 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = next_stage(w.n1 - 1, false, w.g);
         ++k;
       }
-      if (!ok) {
-        // Give up: let every copy already issued land before the CTA exits.
-        for (int s = 0; s < kStages; ++s)
-          if (issued_mask & (1u << s)) wait_bar(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
-        if (q_issued) wait_bar(bar(kBarQFull), q_parity, p);
-      }
+      // Every copy this warp issued must have landed before the CTA exits. On the
+      // normal path the consumers already waited for all of them (these return at
+      // once); after a time-out they may still be in flight.
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) wait_bar(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
+      if (q_issued) wait_bar(bar(kBarQFull), q_parity, p);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {

@@ -38,6 +38,7 @@ struct FwdParams {
   int n_units;         // n_qtiles * 4 * splits
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
+  int withhold_q;      // test only: the producer never loads the first Q tile
 };
 
 struct MergeParams {

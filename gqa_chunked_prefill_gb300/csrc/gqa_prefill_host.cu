@@ -254,6 +254,7 @@ gqa_status run(const void* q, const void* k, const void* v, void* out, float* ls
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = (opts && opts->wait_timeout_us) ? 1000ull * opts->wait_timeout_us
                                                  : kDefaultTimeoutNs;
+  p.withhold_q = (opts && opts->test_withhold_q) ? 1 : 0;
 
   void* ws = nullptr;
   if (plan.splits > 1) {

@@ -79,7 +79,13 @@ typedef struct gqa_prefill_opts {
                                  before the attention kernel launch                */
   void* fwd_event_end;        /* optional cudaEvent_t recorded right after it (before
                                  the split merge, if any): times the main kernel   */
-  int reserved[4];
+  int test_withhold_q;        /* TEST ONLY. 1: the TMA producer withholds each CTA's
+                                 first Q tile, so every consumer wait runs out after
+                                 wait_timeout_us; the kernel records
+                                 GQA_ERR_DEVICE_TIMEOUT, drains its copies, frees
+                                 tensor memory and returns (outputs undefined).
+                                 Exercises the time-out path without faulting.     */
+  int reserved[3];
 } gqa_prefill_opts;
 
 /* What the planner chose (the route check: which kernel ran and how). */
