@@ -23,6 +23,7 @@ class GqaStatus(enum.IntEnum):
     ERR_ALIGN = 4
     ERR_CUDA = 5
     ERR_DEVICE_TIMEOUT = 6
+    ERR_SCRATCH = 7
 
 
 class GqaError(RuntimeError):
@@ -58,6 +59,8 @@ lib.gqa_prefill_attn.argtypes = _ATTN_ARGS
 lib.gqa_prefill_attn.restype = _i
 lib.gqa_prefill_attn_ex.argtypes = _ATTN_ARGS + [ctypes.POINTER(PrefillOpts), ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_attn_ex.restype = _i
+lib.gqa_prefill_attn_noalloc.argtypes = _ATTN_ARGS
+lib.gqa_prefill_attn_noalloc.restype = _i
 lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan.restype = _i
 lib.gqa_prefill_poll.argtypes = [_vp, ctypes.POINTER(_i)]
@@ -102,6 +105,17 @@ def gqa_prefill_attn(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, he
                      stream=None, check=True) -> int:
     rc = lib.gqa_prefill_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), q_len, kv_len,
                               n_q_heads, n_kv_heads, head_dim, scale, _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_prefill_attn_noalloc(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim,
+                             scale, stream=None, check=True) -> int:
+    """The allocation-free entry point (split partials in the library's static scratch)."""
+    rc = lib.gqa_prefill_attn_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), q_len,
+                                      kv_len, n_q_heads, n_kv_heads, head_dim, scale,
+                                      _stream(stream))
     if check:
         _check(rc)
     return rc

@@ -277,10 +277,104 @@ gqa_status run(const void* q, const void* k, const void* v, void* out, float* ls
   return st;
 }
 
+// ---------------------------------------------------- allocation-free variant --
+// Split-KV partials of gqa_prefill_attn_noalloc live in this file-scope array
+// instead of the stream-ordered pool. In host code `g_noalloc_scratch` is only a
+// host-side stand-in for the symbol: its device address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+constexpr size_t kNoAllocScratchBytes = GQA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDeviceState {
+  std::once_flag once;
+  gqa_status status = GQA_OK;
+  int num_sms = 0;
+  int* status_word = nullptr;
+  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocDeviceState g_noalloc_dev[kMaxDevices];
+
+gqa_status noalloc_device_state(NoAllocDeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  NoAllocDeviceState& s = g_noalloc_dev[dev];
+  std::call_once(s.once, [&s, dev] {
+    cudaDeviceProp prop{};
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) { s.status = GQA_ERR_CUDA; return; }
+    if (!(prop.major == 10 && prop.minor == 3)) { s.status = GQA_ERR_UNSUPPORTED; return; }
+    s.num_sms = prop.multiProcessorCount;
+    if (prepare_fwd_kernel() != cudaSuccess || status_word_address(&s.status_word) != cudaSuccess ||
+        cudaGetSymbolAddress(&s.scratch, g_noalloc_scratch) != cudaSuccess || s.scratch == nullptr) {
+      s.status = GQA_ERR_CUDA;
+      return;
+    }
+  });
+  if (s.status != GQA_OK) return s.status;
+  *out = &s;
+  return GQA_OK;
+}
+
+gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
+                       int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
+                       float scale, void* stream_ptr) {
+  gqa_status st = validate_shape(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
+  if (st != GQA_OK) return st;
+  if (q_len == 0) return GQA_OK;
+  if (!q || !k || !v || !out) return GQA_ERR_NULL;
+  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(lse))
+    return GQA_ERR_ALIGN;
+  NoAllocDeviceState* dev = nullptr;
+  if ((st = noalloc_device_state(&dev)) != GQA_OK) return st;
+  gqa_prefill_plan plan{};
+  cached_plan(q_len, kv_len, dev->num_sms, 0, &plan);
+  if (plan.splits > 1 && static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes)
+    return GQA_ERR_SCRATCH;
+
+  auto stream = static_cast<cudaStream_t>(stream_ptr);
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if (!encode_3d(&p.tmap_q, q, kHeadDim, kQHeads, static_cast<uint64_t>(q_len), 64, kGroup,
+                 kTokPerTile) ||
+      !encode_3d(&p.tmap_k, k, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1, kBlockN) ||
+      !encode_3d(&p.tmap_v, v, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1, 64))
+    return GQA_ERR_CUDA;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.status = dev->status_word;
+  p.q_len = q_len;
+  p.kv_len = kv_len;
+  p.p0 = kv_len - q_len;
+  p.n_qtiles = plan.q_tiles;
+  p.splits = plan.splits;
+  p.n_units = plan.n_units;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.timeout_ns = kDefaultTimeoutNs;
+  if (plan.splits > 1) {
+    // Every partial row the merge reads is written by the attention kernel first,
+    // so the scratch needs no clearing between calls.
+    p.part_o = static_cast<float*>(dev->scratch);
+    p.part_lse = p.part_o + static_cast<size_t>(plan.splits) * q_len * kQHeads * kHeadDim;
+  }
+  if (launch_fwd(p, plan.grid, stream) != cudaSuccess) return GQA_ERR_CUDA;
+  if (plan.splits > 1) {
+    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len * kQHeads, plan.splits};
+    if (launch_merge(m, stream) != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
+}
+
 }  // namespace
 }  // namespace gqa
 
 extern "C" {
+
+gqa_status gqa_prefill_attn_noalloc(const void* q, const void* k, const void* v, void* out,
+                                    float* lse, int q_len, int kv_len, int n_q_heads,
+                                    int n_kv_heads, int head_dim, float scale, void* stream) {
+  return gqa::run_noalloc(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim,
+                          scale, stream);
+}
+
 
 gqa_status gqa_prefill_attn(const void* q, const void* k, const void* v, void* out, float* lse,
                             int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
@@ -338,6 +432,9 @@ const char* gqa_status_string(gqa_status status) {
     case GQA_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
     case GQA_ERR_CUDA: return "a CUDA call failed";
     case GQA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out; the kernel gave up";
+    case GQA_ERR_SCRATCH:
+      return "gqa_prefill_attn_noalloc: split partials exceed the 64 MiB static scratch "
+             "(use a shorter chunk or gqa_prefill_attn)";
   }
   return "unknown status";
 }

@@ -54,7 +54,9 @@ typedef enum gqa_status {
                                  sm_103a-class device                                  */
   GQA_ERR_ALIGN = 4,          /* a pointer is not 16-byte aligned                      */
   GQA_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed                     */
-  GQA_ERR_DEVICE_TIMEOUT = 6  /* a device-side wait ran out of time (see _poll)        */
+  GQA_ERR_DEVICE_TIMEOUT = 6, /* a device-side wait ran out of time (see _poll)        */
+  GQA_ERR_SCRATCH = 7         /* gqa_prefill_attn_noalloc: the call's split partials do
+                                 not fit the library's static scratch array            */
 } gqa_status;
 
 /*
@@ -124,6 +126,40 @@ gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_
  * since the previous poll.
  */
 gqa_status gqa_prefill_poll(void* stream, int* device_status);
+
+/*
+ * gqa_prefill_attn_noalloc — same operation, arguments and results as
+ * gqa_prefill_attn, but it allocates no device memory at all. (The subject
+ * pages have no counterpart to this entry point; it exists for callers of this
+ * library, not for the method.)
+ *
+ * Who needs it: callers that cannot allocate device memory in the middle of a
+ * call — serving engines that reserve the whole device-memory budget at
+ * start-up and forbid later allocations, code that must never risk the
+ * implicit device-wide synchronisation a cudaFree can cause, and hosts whose
+ * device allocator is owned by another framework. gqa_prefill_attn takes its
+ * split-KV partials from a stream-ordered pool; this variant takes them from a
+ * fixed scratch array compiled into the library instead.
+ *
+ * The scratch array is GQA_NOALLOC_SCRATCH_BYTES (64 MiB) of device memory,
+ * held on every GPU that loads the library until the process exits. The call
+ * plans exactly like gqa_prefill_attn; when that plan's partials
+ * (splits * q_len * n_q_heads * 257 * 4 bytes; 0 when the plan does not split)
+ * exceed the array, it returns GQA_ERR_SCRATCH and launches nothing.
+ *
+ * It calls no cudaMalloc, cudaFree or other allocating routine. Its first call
+ * on each device does a one-time set-up with that device current (device
+ * check, kernel attributes, and cudaGetSymbolAddress of the scratch array and
+ * the status word); make that first call before any stream capture. Every
+ * call shares the one array and it keeps the last call's contents (nothing in
+ * it needs to start at zero): calls whose work overlaps on the GPU — on
+ * different streams, or in different threads without ordering between them —
+ * race on it and give undefined results. Serialise such calls.
+ */
+#define GQA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+gqa_status gqa_prefill_attn_noalloc(const void* q, const void* k, const void* v, void* out,
+                                    float* lse, int q_len, int kv_len, int n_q_heads,
+                                    int n_kv_heads, int head_dim, float scale, void* stream);
 
 /* Static description of a status code (never NULL). */
 const char* gqa_status_string(gqa_status status);
