@@ -49,7 +49,11 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one attention-kernel
 # launch from an ncu capture, keyed by workload, with the SHA-256 of the kernel
 # source it was measured on; reported as null once the source no longer matches.
-KNOWN_TRAFFIC: dict = {}
+KNOWN_TRAFFIC: dict = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the full launch:
+    # 1.44 GB read + 199.37 MB written (split partials included).
+    "q4096_kv32768": {"bytes": 1_639_370_000, "kernel_sha256": "87cfe400611558bc9b7686a1261e15b6cfb4349ea3c46e79dfe28fe263c0d3af"},
+}
 
 
 def visible_pairs(q_len: int, kv_len: int) -> int:

@@ -254,6 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Issue order per unit: QK_0, then for each tile j: QK_{j+1}, PV_j. QK_{j+1}
     // runs on the tensor pipe while the softmax of tile j is in flight.
     if (lane == 0) {
+      const uint64_t q_desc0 = ptx::smem_desc(q_smem, 16, 1024, ptx::kSwizzle128B);
+      const uint64_t k_desc0 = ptx::smem_desc(stage_smem, 16, 1024, ptx::kSwizzle128B);
+      const uint64_t v_desc0 = ptx::smem_desc(stage_smem, kVBoxBytes, 1024, ptx::kSwizzle128B);
       uint32_t st = 0, phase = 0;
       uint32_t tile = 0;  // KV tiles this CTA has processed (global tile index T)
       bool ok = true;
@@ -266,23 +269,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_bar(bar(kBarQFull), k & 1, p))) break;
         ptx::tc_fence_after();
         // S = Q K_j^T over d = 256: two stages (d halves) x 2 chunks x 4 k-steps of 16.
+        // Descriptors are built once; an offset below 256 KB only touches the
+        // 14-bit start-address field, so stepping through a tile is one add.
         auto issue_qk = [&](int j) -> bool {
           const uint32_t T = tile + j;
           // S may be overwritten once the softmax holds tile T-1's scores in registers.
           if (T > 0 && !wait_bar(bar(kBarSFree), (T - 1) & 1u, p)) return false;
           ptx::tc_fence_after();
+#pragma unroll
           for (int half = 0; half < 2; ++half) {
             if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
             ptx::tc_fence_after();
-            const uint32_t kst = stage_smem + st * kStageBytes;
+            const uint64_t kd = k_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = ptx::smem_desc(q_smem + (2 * half + c) * kQChunkBytes + 32 * kk,
-                                                  16, 1024, ptx::kSwizzle128B);
-                const uint64_t bd = ptx::smem_desc(kst + c * kKBoxBytes + 32 * kk, 16, 1024,
-                                                   ptx::kSwizzle128B);
+                const uint64_t a = q_desc0 + (((2 * half + c) * kQChunkBytes + 32 * kk) >> 4);
+                const uint64_t bd = kd + ((c * kKBoxBytes + 32 * kk) >> 4);
                 ptx::mma_ss(tmem + kTmemS, a, bd, kIdescQK, (half | c | kk) != 0);
               }
             }
@@ -305,13 +309,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int half = 0; half < 2 && ok; ++half) {
             if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
             ptx::tc_fence_after();
-            const uint32_t vst = stage_smem + st * kStageBytes;
+            const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
               // V stage: 4 boxes (64-wide d chunks, 8 KB apart) of 64 keys x 128 B.
               // MN-major B: LBO = next d chunk, SBO = next group of 8 keys.
-              const uint64_t bd = ptx::smem_desc(vst + 2048 * kk, kVBoxBytes, 1024,
-                                                 ptx::kSwizzle128B);
+              const uint64_t bd = vd + ((2048 * kk) >> 4);
               const uint32_t a_tmem = tmem + kTmemP + 64u * b + 32u * half + 8u * kk;
               ptx::mma_ts(tmem + kTmemO, a_tmem, bd, kIdescPV, (j | half | kk) != 0);
             }
@@ -372,11 +375,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 4; c < 128; c += 8) {
+          mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+          mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
         }
         const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
         const float m_new = fmaxf(m_ref, m_tile);
@@ -404,15 +407,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float m_use = (m_ref == kNegInf) ? 0.0f : m_ref;
         uint32_t pk[64];
-        float sum0 = 0.0f, sum1 = 0.0f;
+        // p = 2^(s*scale*log2e - m): one packed FMA per pair, two ex2, one packed add.
+        const uint64_t scale2 = ptx::f32x2(sl2, sl2);
+        const uint64_t neg_m2 = ptx::f32x2(-m_use, -m_use);
+        uint64_t sum2 = ptx::f32x2(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float e0 = ptx::ex2_approx(fmaf(s[2 * c], sl2, -m_use));
-          const float e1 = ptx::ex2_approx(fmaf(s[2 * c + 1], sl2, -m_use));
-          sum0 += e0;
-          sum1 += e1;
+          float x0, x1;
+          ptx::f32x2_split(ptx::fma_f32x2(ptx::f32x2(s[2 * c], s[2 * c + 1]), scale2, neg_m2), x0, x1);
+          const float e0 = ptx::ex2_approx(x0);
+          const float e1 = ptx::ex2_approx(x1);
+          sum2 = ptx::add_f32x2(sum2, ptx::f32x2(e0, e1));
           pk[c] = ptx::pack_bf16x2(e0, e1);
         }
+        float sum0, sum1;
+        ptx::f32x2_split(sum2, sum0, sum1);
         l += sum0 + sum1;
         if (T >= 2) {
           // P[b] was last read by PV_{T-2}: it must have completed before P[b] is rewritten.
