@@ -31,16 +31,19 @@
 //    stale max is kept, which is exact after the final division by the row sum.
 //  * Causal tiles entirely above the diagonal are never visited; only the (at
 //    most two) tiles that straddle it are masked element-wise.
-//  * Persistent grid (one CTA per SM); work units (query tile, KV group, KV
-//    split) are taken longest-first in a snake order across CTAs. When the
-//    planner splits the KV range, each unit writes a normalised FP32 partial
-//    and its base-2 LSE, and merge_splits_kernel combines them.
+//  * Persistent grid (one CTA per SM). Work items (query tile, KV group) are
+//    ordered longest first and either dealt out whole in a snake order, or
+//    laid end to end as one sequence of KV tiles cut into equal contiguous
+//    ranges, one per CTA (gqa_schedule.h). Items cut by a range boundary are
+//    computed in pieces that write normalised FP32 partials plus their base-2
+//    LSE; merge_ranges_kernel combines them.
 //  * Every mbarrier wait is bounded: on time-out the kernel records
 //    GQA_ERR_DEVICE_TIMEOUT, waits for its own TMA copies in flight, frees its
 //    tensor memory and returns.
 
 #include "gqa_internal.h"
 #include "gqa_prefill.h"
+#include "gqa_schedule.h"
 #include "sm100_ptx.cuh"
 
 namespace gqa {
@@ -94,31 +97,6 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between resca
 constexpr float kLn2 = 0.693147180559945309f;
 
 __device__ int g_status_word = 0;
-
-struct Unit {
-  int g, qt, split, n0, n1;
-};
-
-// Units are numbered longest-first: q tiles from the last (most keys) down,
-// then KV group, then split.
-__device__ __forceinline__ Unit decode_unit(const FwdParams& p, int u) {
-  const int per_qt = kKvHeads * p.splits;
-  Unit w;
-  w.qt = p.n_qtiles - 1 - u / per_qt;
-  const int rem = u % per_qt;
-  w.g = rem / p.splits;
-  w.split = rem % p.splits;
-  const int tok_end = min((w.qt + 1) * kTokPerTile, p.q_len);
-  const int nt = (p.p0 + tok_end + kBlockN - 1) / kBlockN;
-  w.n0 = static_cast<int>(static_cast<long long>(w.split) * nt / p.splits);
-  w.n1 = static_cast<int>(static_cast<long long>(w.split + 1) * nt / p.splits);
-  return w;
-}
-
-// Round r of CTA b in a snake order (alternate direction every round).
-__device__ __forceinline__ int unit_of(int b, int r, int G) {
-  return r * G + ((r & 1) ? (G - 1 - b) : b);
-}
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const FwdParams& p) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -181,7 +159,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int G = gridDim.x;
+  const Geometry geo{p.q_len, p.p0, p.n_qtiles};
+  PieceIter pieces;  // this CTA's work, in order; each role walks its own copy
+  pieces.init(geo, p.schedule, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x),
+              p.total_tiles);
 
   if (warp == kTmaWarp) {
     // ======================= TMA producer ======================================
@@ -219,10 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       int k = 0;
-      for (int r = 0; ok; ++r) {
-        const int u = unit_of(blockIdx.x, r, G);
-        if (u >= p.n_units) break;
-        const Unit w = decode_unit(p, u);
+      Piece w;
+      while (ok && pieces.next(w)) {
         if (k > 0 && !(ok = wait_bar(bar(kBarQEmpty), (k - 1) & 1, p))) break;
         if (!(p.withhold_q && k == 0)) {
           ptx::mbar_arrive_expect_tx(bar(kBarQFull), 4 * kQBoxBytes);
@@ -261,10 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tile = 0;  // KV tiles this CTA has processed (global tile index T)
       bool ok = true;
       int k = 0;
-      for (int r = 0; ok; ++r) {
-        const int u = unit_of(blockIdx.x, r, G);
-        if (u >= p.n_units) break;
-        const Unit w = decode_unit(p, u);
+      Piece w;
+      while (ok && pieces.next(w)) {
         const int nt = w.n1 - w.n0;
         if (!(ok = wait_bar(bar(kBarQFull), k & 1, p))) break;
         ptx::tc_fence_after();
@@ -342,10 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tile = 0;
     int k = 0;
     bool ok = true;
-    for (int r = 0; ok; ++r) {
-      const int u = unit_of(blockIdx.x, r, G);
-      if (u >= p.n_units) break;
-      const Unit w = decode_unit(p, u);
+    Piece w;
+    while (ok && pieces.next(w)) {
       const int nt = w.n1 - w.n0;
       const int tok = kTokPerTile * w.qt + tl;
       const bool valid = row < kTokPerTile * kGroup && tok < p.q_len;
@@ -445,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
       const float lse2 = l > 0.0f ? m_ref + __log2f(l) : kNegInf;
       const size_t qrow = static_cast<size_t>(tok) * kQHeads + kGroup * w.g + hj;
-      if (p.splits == 1) {
+      if (w.slot < 0) {
         __nv_bfloat16* dst = p.out + qrow * kHeadDim;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
@@ -465,7 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (valid && p.lse != nullptr) p.lse[qrow] = lse2 * kLn2;
       } else {
-        const size_t prow = static_cast<size_t>(w.split) * p.q_len * kQHeads + qrow;
+        // A piece of a cut item: normalised partial rows go to this CTA's slot.
+        const size_t prow = static_cast<size_t>(w.slot) * kRowsPerTile + row;
         float* dst = p.part_o + prow * kHeadDim;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
@@ -499,35 +475,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Combine split-KV partials: lse = log2 sum_s 2^{lse_s}; out = sum_s 2^{lse_s - lse} O_s.
-// One warp per (token, head) row, 8 consecutive d per lane; fixed split order.
-__global__ void __launch_bounds__(256) merge_splits_kernel(const MergeParams p) {
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+// Combine the pieces of every item cut by a range boundary (kScheduleRanges).
+// Block m looks at boundary m (first tile of CTA m's range); it merges the item
+// the boundary cuts unless an earlier boundary already cut the same item. The
+// pieces come from CTAs m-1 .. owner(last tile), CTA m-1's piece in slot
+// 2(m-1)+1 and every later one in slot 2b; they are combined in CTA order:
+// lse = log2 sum_b 2^{lse_b}, out = sum_b 2^{lse_b - lse} O_b. One warp per row.
+__global__ void __launch_bounds__(256) merge_ranges_kernel(const MergeParams p) {
+  const Geometry geo{p.q_len, p.p0, p.n_qtiles};
+  const int m = blockIdx.x + 1;
+  const long long W = p.total_tiles;
+  const long long t = range_lo(W, p.grid, m);
+  const ItemPos it = locate(geo, t);
+  if (t == it.start || range_lo(W, p.grid, m - 1) > it.start) return;
+  const int b_lo = m - 1;
+  const int b_hi = range_owner(W, p.grid, it.start + it.nt - 1);
+  const int qt = geo.n_qtiles - 1 - it.r;
   const int lane = threadIdx.x & 31;
-  if (row >= p.rows) return;
-  float mx = kNegInf;
-  for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, p.part_lse[static_cast<size_t>(s) * p.rows + row]);
-  const float m_use = (mx == kNegInf) ? 0.0f : mx;
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  float wsum = 0.0f;
-  for (int s = 0; s < p.splits; ++s) {
-    const size_t prow = static_cast<size_t>(s) * p.rows + row;
-    const float w = ptx::ex2_approx(p.part_lse[prow] - m_use);
-    wsum += w;
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * kHeadDim + 8 * lane);
-    const float4 a = src[0], b = src[1];
-    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-    acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
+  for (int row = threadIdx.x >> 5; row < kTokPerTile * kGroup; row += 8) {
+    const int tok = kTokPerTile * qt + row / kGroup;
+    if (tok >= p.q_len) break;
+    float mx = kNegInf;
+    for (int b = b_lo; b <= b_hi; ++b) {
+      const int slot = b == b_lo ? 2 * b + 1 : 2 * b;
+      mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slot) * kRowsPerTile + row]);
+    }
+    const float m_use = (mx == kNegInf) ? 0.0f : mx;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    float wsum = 0.0f;
+    for (int b = b_lo; b <= b_hi; ++b) {
+      const size_t prow = static_cast<size_t>(b == b_lo ? 2 * b + 1 : 2 * b) * kRowsPerTile + row;
+      const float w = ptx::ex2_approx(p.part_lse[prow] - m_use);
+      wsum += w;
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * kHeadDim + 8 * lane);
+      const float4 a = src[0], c = src[1];
+      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+      acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+    }
+    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+    uint4 o;
+    o.x = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    o.y = ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    o.z = ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    o.w = ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    const size_t orow = static_cast<size_t>(tok) * kQHeads + kGroup * it.g + row % kGroup;
+    *reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 8 * lane) = o;
+    if (lane == 0 && p.lse != nullptr)
+      p.lse[orow] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;
   }
-  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-  uint4 o;
-  o.x = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  o.y = ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv);
-  o.z = ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv);
-  o.w = ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv);
-  *reinterpret_cast<uint4*>(p.out + static_cast<size_t>(row) * kHeadDim + 8 * lane) = o;
-  if (lane == 0 && p.lse != nullptr)
-    p.lse[row] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;
 }
 
 }  // namespace
@@ -545,8 +540,8 @@ cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
-  const int blocks = (p.rows + 7) / 8;
-  merge_splits_kernel<<<blocks, 256, 0, stream>>>(p);
+  if (p.grid < 2) return cudaSuccess;
+  merge_ranges_kernel<<<p.grid - 1, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

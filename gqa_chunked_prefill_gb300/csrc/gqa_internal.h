@@ -25,29 +25,32 @@ struct FwdParams {
   CUtensorMap tmap_q;  // Q [q_len][24][256], box (64 d, 6 heads, 21 tokens), 128B swizzle
   CUtensorMap tmap_k;  // K [kv_len][4][256], box (64 d, 1 head, 128 keys), 128B swizzle
   CUtensorMap tmap_v;  // V [kv_len][4][256], box (64 d, 1 head, 64 keys), 128B swizzle
-  __nv_bfloat16* out;  // [q_len][24][256]                 (splits == 1)
-  float* lse;          // [q_len][24] natural log, or null  (splits == 1)
-  float* part_o;       // [splits][q_len][24][256] normalised partial O (splits > 1)
-  float* part_lse;     // [splits][q_len][24] base-2 partial LSE        (splits > 1)
+  __nv_bfloat16* out;  // [q_len][24][256]
+  float* lse;          // [q_len][24] natural log, or null
+  float* part_o;       // [2*grid][128 rows][256] normalised partial O of cut items
+  float* part_lse;     // [2*grid][128 rows] base-2 partial LSE of cut items
   int* status;         // per-device status word
   int q_len;
   int kv_len;
   int p0;              // kv_len - q_len: position of the chunk's first token
   int n_qtiles;        // ceil(q_len / 21)
-  int splits;
-  int n_units;         // n_qtiles * 4 * splits
+  int schedule;        // kScheduleItems or kScheduleRanges (gqa_schedule.h)
+  long long total_tiles;  // KV tiles over all items
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
   int withhold_q;      // test only: the producer never loads the first Q tile
 };
 
 struct MergeParams {
-  const float* part_o;
-  const float* part_lse;
+  const float* part_o;    // as FwdParams::part_o
+  const float* part_lse;  // as FwdParams::part_lse
   __nv_bfloat16* out;
-  float* lse;  // may be null
-  int rows;    // q_len * 24
-  int splits;
+  float* lse;             // may be null
+  int q_len;
+  int p0;
+  int n_qtiles;
+  int grid;               // CTAs of the attention launch
+  long long total_tiles;
 };
 
 size_t fwd_smem_bytes();

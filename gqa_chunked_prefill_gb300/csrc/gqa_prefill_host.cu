@@ -21,6 +21,7 @@
 
 #include "gqa_internal.h"
 #include "gqa_prefill.h"
+#include "gqa_schedule.h"
 
 namespace gqa {
 namespace {
@@ -29,100 +30,93 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per device-side wait
 
 // ------------------------------------------------------------------ planner --
-// Cost model in units of one 128-key KV tile of one work unit (QK^T + PV of a
-// 128 x 128 x 256 block, ~1.3 us of tensor-core time on one SM at peak).
-constexpr int64_t kUnitOverheadTiles = 2;  // Q load, pipeline fill, epilogue
-constexpr double kTileUs = 1.9;            // planning estimate at ~70% of peak
-constexpr double kMergeBytesPerUs = 6.0e6;  // HBM bandwidth for the merge pass
+// Cost model in units of one 128-key KV tile of one item (QK^T + PV of a
+// 128 x 128 x 256 block: ~1.3 us of tensor-core time on one SM at peak).
+constexpr int64_t kPieceOverheadTiles = 2;   // Q load, pipeline fill, epilogue
+constexpr double kTileUs = 1.5;              // planning estimate per tile
+constexpr double kMergeBytesPerUs = 6.0e6;   // HBM bandwidth for the merge pass
 constexpr double kMergeLaunchUs = 4.0;
+constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
 
-int ceil_div(int a, int b) { return (a + b - 1) / b; }
-
-int item_tiles(int qt, int q_len, int p0) {
-  const int tok_end = std::min((qt + 1) * kTokPerTile, q_len);
-  return ceil_div(p0 + tok_end, kBlockN);
+Geometry geometry(int q_len, int kv_len) {
+  return Geometry{q_len, kv_len - q_len, (q_len + kTokPerTile - 1) / kTokPerTile};
 }
 
-// Busiest CTA's cost, in KV tiles, for the device-side snake schedule.
-int64_t simulate_makespan(int q_len, int p0, int n_qtiles, int splits, int grid) {
-  std::vector<int64_t> load(static_cast<size_t>(grid), 0);
-  const int per_qt = kKvHeads * splits;
-  const int n_units = n_qtiles * per_qt;
-  for (int u = 0; u < n_units; ++u) {
-    const int r = u / grid, pos = u % grid;
-    const int b = (r & 1) ? (grid - 1 - pos) : pos;
-    const int qt = n_qtiles - 1 - u / per_qt;
-    const int split = (u % per_qt) % splits;
-    const int nt = item_tiles(qt, q_len, p0);
-    const int64_t n0 = static_cast<int64_t>(split) * nt / splits;
-    const int64_t n1 = static_cast<int64_t>(split + 1) * nt / splits;
-    load[static_cast<size_t>(b)] += (n1 - n0) + kUnitOverheadTiles;
+// Fills *plan for one schedule on `grid_cap` CTAs at most; returns the estimated time in us.
+double plan_schedule(int q_len, int kv_len, int num_sms, int grid_cap, int schedule,
+                     gqa_prefill_plan* plan) {
+  const Geometry geo = geometry(q_len, kv_len);
+  const int n_items = geo.n_qtiles * kKvHeads;
+  const int64_t W = total_tiles(geo);
+  int grid = schedule == kScheduleItems ? std::min(n_items, grid_cap)
+                                        : static_cast<int>(std::min<int64_t>(W, grid_cap));
+  grid = std::max(grid, 1);
+  // Busiest CTA and number of cut items, by walking every CTA's pieces.
+  int64_t makespan = 0;
+  int cut = 0;
+  for (int b = 0; b < grid; ++b) {
+    PieceIter it;
+    it.init(geo, schedule, grid, b, W);
+    Piece w;
+    int64_t load = 0;
+    while (it.next(w)) {
+      load += (w.n1 - w.n0) + kPieceOverheadTiles;
+      if (w.slot >= 0 && w.n0 == 0) ++cut;  // each cut item once, at its first piece
+    }
+    makespan = std::max(makespan, load);
   }
-  return *std::max_element(load.begin(), load.end());
-}
-
-void fill_plan(int q_len, int kv_len, int num_sms, int splits, gqa_prefill_plan* plan) {
-  const int p0 = kv_len - q_len;
-  const int n_qtiles = ceil_div(q_len, kTokPerTile);
-  const int n_units = n_qtiles * kKvHeads * splits;
-  const int grid = std::min(n_units, num_sms);
+  std::memset(plan, 0, sizeof(*plan));
   plan->num_sms = num_sms;
-  plan->q_tiles = n_qtiles;
-  plan->n_items = n_qtiles * kKvHeads;
-  plan->splits = splits;
-  plan->n_units = n_units;
+  plan->q_tiles = geo.n_qtiles;
+  plan->n_items = n_items;
+  plan->schedule = schedule;
   plan->grid = grid;
-  plan->kernels_per_call = splits > 1 ? 2 : 1;
+  plan->split_items = cut;
+  plan->kernels_per_call = cut > 0 ? 2 : 1;
   plan->variant = 1;
-  plan->workspace_bytes =
-      splits > 1 ? static_cast<int64_t>(splits) * q_len * kQHeads * (kHeadDim + 1) * 4 : 0;
-  plan->est_makespan_tiles = simulate_makespan(q_len, p0, n_qtiles, splits, grid);
+  plan->total_tiles = W;
+  plan->workspace_bytes = cut > 0 ? int64_t{2} * grid * kRowsPerTile * kPartialRowBytes : 0;
+  plan->est_makespan_tiles = makespan;
+  double us = static_cast<double>(makespan) * kTileUs;
+  if (cut > 0) {
+    // Each cut item is read back in ~2-3 pieces and written once.
+    const double bytes = cut * static_cast<double>(kRowsPerTile) * (3.0 * kPartialRowBytes + 520.0);
+    us += bytes / kMergeBytesPerUs + kMergeLaunchUs;
+  }
+  return us;
 }
 
-// Pure function of (q_len, kv_len, num_sms, force_splits).
-void compute_plan(int q_len, int kv_len, int num_sms, int force_splits, gqa_prefill_plan* plan) {
-  const int p0 = kv_len - q_len;
-  const int n_qtiles = ceil_div(q_len, kTokPerTile);
-  // No split may be empty: cap at the KV tile count of the shortest item.
-  const int min_tiles = item_tiles(0, q_len, p0);
-  const int max_splits = std::max(1, std::min(min_tiles, 32));
-  if (force_splits > 0) {
-    fill_plan(q_len, kv_len, num_sms, std::min(force_splits, max_splits), plan);
+// Pure function of its arguments.
+void compute_plan(int q_len, int kv_len, int num_sms, int force_schedule, int force_grid,
+                  gqa_prefill_plan* plan) {
+  const int cap = force_grid > 0 ? std::min(force_grid, num_sms) : num_sms;
+  if (force_schedule == 1) {
+    plan_schedule(q_len, kv_len, num_sms, cap, kScheduleItems, plan);
     return;
   }
-  static const int kCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 20, 24, 32};
-  double best_us = 0.0;
-  bool have = false;
-  gqa_prefill_plan cand{};
-  for (int s : kCandidates) {
-    if (s > max_splits) break;
-    fill_plan(q_len, kv_len, num_sms, s, &cand);
-    double us = static_cast<double>(cand.est_makespan_tiles) * kTileUs;
-    if (s > 1) {
-      const double rows = static_cast<double>(q_len) * kQHeads;
-      const double bytes = rows * (s * (kHeadDim + 1) * 4.0 + kHeadDim * 2.0 + 4.0);
-      us += bytes / kMergeBytesPerUs + kMergeLaunchUs;
-    }
-    (void)n_qtiles;
-    if (!have || us < best_us * 0.98) {  // a split must win clearly to be chosen
-      best_us = us;
-      *plan = cand;
-      have = true;
-    }
+  if (force_schedule == 2) {
+    plan_schedule(q_len, kv_len, num_sms, cap, kScheduleRanges, plan);
+    return;
   }
+  gqa_prefill_plan whole{}, ranges{};
+  const double t_whole = plan_schedule(q_len, kv_len, num_sms, cap, kScheduleItems, &whole);
+  const double t_ranges = plan_schedule(q_len, kv_len, num_sms, cap, kScheduleRanges, &ranges);
+  *plan = t_ranges < 0.98 * t_whole ? ranges : whole;  // cutting items must win clearly
 }
 
 struct PlanKey {
-  int q_len, kv_len, num_sms, force;
+  int q_len, kv_len, num_sms, force_schedule, force_grid;
   bool operator<(const PlanKey& o) const {
-    return std::tie(q_len, kv_len, num_sms, force) < std::tie(o.q_len, o.kv_len, o.num_sms, o.force);
+    return std::tie(q_len, kv_len, num_sms, force_schedule, force_grid) <
+           std::tie(o.q_len, o.kv_len, o.num_sms, o.force_schedule, o.force_grid);
   }
 };
 
-void cached_plan(int q_len, int kv_len, int num_sms, int force_splits, gqa_prefill_plan* plan) {
+void cached_plan(int q_len, int kv_len, int num_sms, int force_schedule, int force_grid,
+                 gqa_prefill_plan* plan) {
   static std::mutex mu;
   static std::map<PlanKey, gqa_prefill_plan> cache;
-  const PlanKey key{q_len, kv_len, num_sms, force_splits};
+  const PlanKey key{q_len, kv_len, num_sms, force_schedule, force_grid};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -131,7 +125,7 @@ void cached_plan(int q_len, int kv_len, int num_sms, int force_splits, gqa_prefi
       return;
     }
   }
-  compute_plan(q_len, kv_len, num_sms, force_splits, plan);
+  compute_plan(q_len, kv_len, num_sms, force_schedule, force_grid, plan);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache.emplace(key, *plan);
@@ -229,9 +223,9 @@ gqa_status run(const void* q, const void* k, const void* v, void* out, float* ls
   DeviceState* dev = nullptr;
   if ((st = device_state(&dev)) != GQA_OK) return st;
 
-  const int force = opts ? opts->force_splits : 0;
   gqa_prefill_plan plan{};
-  cached_plan(q_len, kv_len, dev->num_sms, force, &plan);
+  cached_plan(q_len, kv_len, dev->num_sms, opts ? opts->force_schedule : 0,
+              opts ? opts->force_grid : 0, &plan);
   if (plan_out) *plan_out = plan;
 
   auto stream = static_cast<cudaStream_t>(stream_ptr);
@@ -249,28 +243,29 @@ gqa_status run(const void* q, const void* k, const void* v, void* out, float* ls
   p.kv_len = kv_len;
   p.p0 = kv_len - q_len;
   p.n_qtiles = plan.q_tiles;
-  p.splits = plan.splits;
-  p.n_units = plan.n_units;
+  p.schedule = plan.schedule;
+  p.total_tiles = plan.total_tiles;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = (opts && opts->wait_timeout_us) ? 1000ull * opts->wait_timeout_us
                                                  : kDefaultTimeoutNs;
   p.withhold_q = (opts && opts->test_withhold_q) ? 1 : 0;
 
   void* ws = nullptr;
-  if (plan.splits > 1) {
+  if (plan.split_items > 0) {
     if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(plan.workspace_bytes), dev->pool, stream) !=
         cudaSuccess)
       return GQA_ERR_CUDA;
     p.part_o = static_cast<float*>(ws);
-    p.part_lse = p.part_o + static_cast<size_t>(plan.splits) * q_len * kQHeads * kHeadDim;
+    p.part_lse = p.part_o + static_cast<size_t>(2) * plan.grid * kRowsPerTile * kHeadDim;
   }
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   if (st == GQA_OK && launch_fwd(p, plan.grid, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   if (st == GQA_OK && ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) st = GQA_ERR_CUDA;
-  if (st == GQA_OK && plan.splits > 1) {
-    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len * kQHeads, plan.splits};
+  if (st == GQA_OK && plan.split_items > 0) {
+    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.p0, p.n_qtiles, plan.grid,
+                  plan.total_tiles};
     if (launch_merge(m, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   }
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) st = GQA_ERR_CUDA;
@@ -326,9 +321,8 @@ gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, f
   NoAllocDeviceState* dev = nullptr;
   if ((st = noalloc_device_state(&dev)) != GQA_OK) return st;
   gqa_prefill_plan plan{};
-  cached_plan(q_len, kv_len, dev->num_sms, 0, &plan);
-  if (plan.splits > 1 && static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes)
-    return GQA_ERR_SCRATCH;
+  cached_plan(q_len, kv_len, dev->num_sms, 0, 0, &plan);
+  if (static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes) return GQA_ERR_SCRATCH;
 
   auto stream = static_cast<cudaStream_t>(stream_ptr);
   FwdParams p;
@@ -345,19 +339,20 @@ gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, f
   p.kv_len = kv_len;
   p.p0 = kv_len - q_len;
   p.n_qtiles = plan.q_tiles;
-  p.splits = plan.splits;
-  p.n_units = plan.n_units;
+  p.schedule = plan.schedule;
+  p.total_tiles = plan.total_tiles;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = kDefaultTimeoutNs;
-  if (plan.splits > 1) {
+  if (plan.split_items > 0) {
     // Every partial row the merge reads is written by the attention kernel first,
     // so the scratch needs no clearing between calls.
     p.part_o = static_cast<float*>(dev->scratch);
-    p.part_lse = p.part_o + static_cast<size_t>(plan.splits) * q_len * kQHeads * kHeadDim;
+    p.part_lse = p.part_o + static_cast<size_t>(2) * plan.grid * kRowsPerTile * kHeadDim;
   }
   if (launch_fwd(p, plan.grid, stream) != cudaSuccess) return GQA_ERR_CUDA;
-  if (plan.splits > 1) {
-    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len * kQHeads, plan.splits};
+  if (plan.split_items > 0) {
+    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.p0, p.n_qtiles, plan.grid,
+                  plan.total_tiles};
     if (launch_merge(m, stream) != cudaSuccess) return GQA_ERR_CUDA;
   }
   return GQA_OK;
@@ -392,7 +387,8 @@ gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void
 }
 
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int num_sms, int force_splits, gqa_prefill_plan* plan) {
+                                 int num_sms, int force_schedule, int force_grid,
+                                 gqa_prefill_plan* plan) {
   if (!plan) return GQA_ERR_NULL;
   const gqa_status st =
       gqa::validate_shape(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, 1.0f / 16.0f);
@@ -400,7 +396,7 @@ gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_
   if (num_sms <= 0) return GQA_ERR_SHAPE;
   std::memset(plan, 0, sizeof(*plan));
   if (q_len == 0) return GQA_OK;
-  gqa::cached_plan(q_len, kv_len, num_sms, force_splits, plan);
+  gqa::cached_plan(q_len, kv_len, num_sms, force_schedule, force_grid, plan);
   return GQA_OK;
 }
 

@@ -1,6 +1,6 @@
 """CPU-only checks of the C ABI: the library loads without a GPU, exports every
 function include/*.h declares, refuses bad calls before touching CUDA, and its
-host planner behaves (no empty splits, deterministic, grid within SM count)."""
+host planner behaves (deterministic, grid within SM count, balanced ranges)."""
 import ctypes
 import glob
 import os
@@ -62,36 +62,47 @@ SHAPES = [(1, 1), (21, 21), (22, 5000), (128, 256), (512, 4096), (4096, 8192), (
           (3072, 16384), (4096, 32768), (512, 32768)]
 
 
+def _total_tiles(q_len, kv_len):
+    p0, nq = kv_len - q_len, -(-q_len // 21)
+    return sum(4 * (-(-(p0 + min(21 * (qt + 1), q_len)) // 128)) for qt in range(nq))
+
+
 @pytest.mark.parametrize("q_len,kv_len", SHAPES)
 @pytest.mark.parametrize("sms", [148, 152])
-def test_planner_invariants(gqa, q_len, kv_len, sms):
-    _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms)
+@pytest.mark.parametrize("force", [0, 1, 2])
+def test_planner_invariants(gqa, q_len, kv_len, sms, force):
+    _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_schedule=force)
     q_tiles = -(-q_len // 21)
-    assert p["q_tiles"] == q_tiles and p["n_items"] == 4 * q_tiles
-    assert p["n_units"] == p["n_items"] * p["splits"]
-    assert 1 <= p["grid"] <= sms and p["grid"] == min(p["n_units"], sms)
-    # no split may be empty: splits <= KV tiles of the shortest item
-    p0 = kv_len - q_len
-    shortest = -(-(p0 + min(21, q_len)) // 128)
-    assert 1 <= p["splits"] <= shortest
-    assert p["kernels_per_call"] == (2 if p["splits"] > 1 else 1)
-    expect_ws = p["splits"] * q_len * 24 * 257 * 4 if p["splits"] > 1 else 0
-    assert p["workspace_bytes"] == expect_ws
-    # the busiest CTA carries at least the average load
-    total = 0
-    for qt in range(q_tiles):
-        nt = -(-(p0 + min(21 * (qt + 1), q_len)) // 128)
-        total += 4 * nt
-    assert p["est_makespan_tiles"] * p["grid"] >= total
-    _, again = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms)
+    W = _total_tiles(q_len, kv_len)
+    assert p["q_tiles"] == q_tiles and p["n_items"] == 4 * q_tiles and p["total_tiles"] == W
+    assert p["schedule"] in (0, 1) and (force == 0 or p["schedule"] == force - 1)
+    assert 1 <= p["grid"] <= sms
+    if p["schedule"] == 0:
+        assert p["grid"] == min(4 * q_tiles, sms) and p["split_items"] == 0
+    else:
+        assert p["grid"] == min(W, sms) and p["split_items"] <= p["grid"] - 1
+    assert p["kernels_per_call"] == (2 if p["split_items"] else 1)
+    assert p["workspace_bytes"] == (2 * p["grid"] * 128 * 257 * 4 if p["split_items"] else 0)
+    assert p["est_makespan_tiles"] * p["grid"] >= W  # the busiest CTA carries at least the mean
+    _, again = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_schedule=force)
     assert again == p
 
 
-def test_forced_splits_are_capped(gqa):
-    _, p = gqa.gqa_prefill_make_plan(128, 256, 24, 4, 256, 148, force_splits=64)
-    assert p["splits"] == 2  # shortest item covers keys 0..148 -> 2 KV tiles
-    _, p = gqa.gqa_prefill_make_plan(512, 32768, 24, 4, 256, 148, force_splits=5)
-    assert p["splits"] == 5 and p["kernels_per_call"] == 2
+def test_ranges_balance_long_chunks(gqa):
+    """On the long workloads the balanced ranges beat whole items by the tail they remove."""
+    for q_len, kv_len in ((4096, 16384), (4096, 32768)):
+        _, whole = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, force_schedule=1)
+        _, ranges = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, force_schedule=2)
+        assert ranges["est_makespan_tiles"] < 0.95 * whole["est_makespan_tiles"]
+        mean = -(-ranges["total_tiles"] // 152)
+        assert ranges["est_makespan_tiles"] <= mean + 2 * 12  # within a few piece overheads
+
+
+def test_force_grid_caps_the_grid(gqa):
+    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_schedule=2, force_grid=3)
+    assert p["grid"] == 3 and p["split_items"] >= 1
+    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_schedule=1, force_grid=5)
+    assert p["grid"] == 5 and p["split_items"] == 0
 
 
 def test_make_plan_validates(gqa):

@@ -1,5 +1,5 @@
-"""GPU invariants of the CUDA path: determinism, causality (bit-exact), split
-agreement, the ABI's refusals and empty chunks, and the route check (the plan
+"""GPU invariants of the CUDA path: determinism, causality (bit-exact), agreement
+of whole and cut work items, the ABI's refusals and empty chunks, and the route check (the plan
 the library reports for the call that ran)."""
 import ctypes
 
@@ -24,28 +24,31 @@ def test_run_twice_bit_identical(cuda_device, name):
 
 
 @pytest.mark.parametrize("q_len,kv_len,t_star", [(100, 700, 40), (300, 300, 150), (512, 4096, 200)])
-@pytest.mark.parametrize("splits", [0, 3])
-def test_future_keys_leave_earlier_rows_bit_identical(cuda_device, q_len, kv_len, t_star, splits):
+@pytest.mark.parametrize("schedule,grid", [(0, 0), (2, 9)])
+def test_future_keys_leave_earlier_rows_bit_identical(cuda_device, q_len, kv_len, t_star, schedule,
+                                                      grid):
     q, k, v = make_qkv(q_len, kv_len, seed=q_len + kv_len)
-    o1, l1, _ = run_gpu(q, k, v, SCALE, force_splits=splits)
+    o1, l1, _ = run_gpu(q, k, v, SCALE, force_schedule=schedule, force_grid=grid)
     p_star = kv_len - q_len + t_star
     k2, v2 = k.clone(), v.clone()
     k2[p_star + 1:] = (k2[p_star + 1:].float() * 3.0 + 1.0).to(torch.bfloat16)
     v2[p_star + 1:] = (-v2[p_star + 1:].float() + 2.0).to(torch.bfloat16)
-    o2, l2, _ = run_gpu(q, k2, v2, SCALE, force_splits=splits)
+    o2, l2, _ = run_gpu(q, k2, v2, SCALE, force_schedule=schedule, force_grid=grid)
     assert torch.equal(o1[: t_star + 1], o2[: t_star + 1])
     assert torch.equal(l1[: t_star + 1], l2[: t_star + 1])
     assert not torch.equal(o1[t_star + 1:], o2[t_star + 1:])
 
 
-def test_split_and_unsplit_agree(cuda_device):
-    w = WORKLOADS["q512_kv4096_kbias"]
+@pytest.mark.parametrize("name", ["q512_kv4096_kbias", "q4096_kv8192"])
+def test_whole_and_cut_items_agree(cuda_device, name):
+    w = WORKLOADS[name]
     q, k, v = make_workload(w)
-    o1, l1, p1 = run_gpu(q, k, v, SCALE, force_splits=1)
-    o4, l4, p4 = run_gpu(q, k, v, SCALE, force_splits=4)
-    assert p1["splits"] == 1 and p4["splits"] == 4 and p4["kernels_per_call"] == 2
-    check_close(o4.double().cpu().numpy(), l4.double().cpu().numpy(),
-                o1.double().cpu().numpy(), l1.double().cpu().numpy(), "split vs unsplit")
+    o1, l1, p1 = run_gpu(q, k, v, SCALE, force_schedule=1)
+    o2, l2, p2 = run_gpu(q, k, v, SCALE, force_schedule=2)
+    assert p1["schedule"] == 0 and p1["split_items"] == 0
+    assert p2["schedule"] == 1 and p2["split_items"] > 0 and p2["kernels_per_call"] == 2
+    check_close(o2.double().cpu().numpy(), l2.double().cpu().numpy(),
+                o1.double().cpu().numpy(), l1.double().cpu().numpy(), "cut vs whole items")
 
 
 def test_route_check_reports_planned_kernel(cuda_device):
@@ -55,8 +58,7 @@ def test_route_check_reports_planned_kernel(cuda_device):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     _, host_plan = gqa.gqa_prefill_make_plan(4096, 8192, 24, 4, 256, sms)
     assert plan == host_plan
-    assert plan["variant"] == 1 and plan["num_sms"] == sms
-    assert plan["grid"] == min(plan["n_units"], sms)
+    assert plan["variant"] == 1 and plan["num_sms"] == sms and plan["grid"] <= sms
 
 
 def test_empty_chunk_is_a_no_op(cuda_device):

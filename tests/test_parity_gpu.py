@@ -44,15 +44,29 @@ def test_small_shapes_every_element(cuda_device, q_len, kv_len):
                 f"{q_len}x{kv_len}")
 
 
-@pytest.mark.parametrize("q_len,kv_len", [(22, 1000), (129, 1000), (43, 257), (7, 700)])
-@pytest.mark.parametrize("splits", [2, 3, 7])
-def test_forced_splits_every_element(cuda_device, q_len, kv_len, splits):
+@pytest.mark.parametrize("q_len,kv_len", [(22, 1000), (129, 1000), (43, 257), (7, 700), (300, 300)])
+@pytest.mark.parametrize("grid", [1, 3, 7, 40])
+def test_balanced_ranges_every_element(cuda_device, q_len, kv_len, grid):
+    """Schedule 1 on few CTAs: items are cut into many pieces and merged."""
     q, k, v = make_qkv(q_len, kv_len, seed=11 * q_len + kv_len)
-    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits)
-    assert plan["splits"] >= 1 and plan["kernels_per_call"] == (2 if plan["splits"] > 1 else 1)
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_schedule=2, force_grid=grid)
+    assert plan["schedule"] == 1 and plan["grid"] <= grid
+    assert plan["kernels_per_call"] == (2 if plan["split_items"] > 0 else 1)
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
-                f"{q_len}x{kv_len} splits={splits}")
+                f"{q_len}x{kv_len} ranges on {grid} CTAs")
+
+
+@pytest.mark.parametrize("q_len,kv_len", [(129, 1000), (300, 300)])
+@pytest.mark.parametrize("grid", [1, 5])
+def test_whole_items_on_few_ctas(cuda_device, q_len, kv_len, grid):
+    """Schedule 0 with more items than CTAs: each CTA walks many items in turn."""
+    q, k, v = make_qkv(q_len, kv_len, seed=13 * q_len + kv_len)
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_schedule=1, force_grid=grid)
+    assert plan["schedule"] == 0 and plan["split_items"] == 0 and plan["kernels_per_call"] == 1
+    ref_o, ref_l = oracle.attention(q, k, v, SCALE)
+    check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
+                f"{q_len}x{kv_len} whole items on {grid} CTAs")
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
