@@ -346,7 +346,7 @@ def main():
             "effective_gflop_per_step": round(flops / 1e9, 2),
             "l2": "flushed before every step (256 MB buffer write outside the step events)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "plan": {k_: plan[k_] for k_ in ("schedule", "grid", "split_items", "total_tiles",
+            "plan": {k_: plan[k_] for k_ in ("head_rounds", "tail_items", "tail_splits", "grid",
                                              "num_sms", "kernels_per_call")},
         },
         "pct_of_peak": round(100.0 * value / world / peak, 2),

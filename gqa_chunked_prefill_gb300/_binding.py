@@ -33,7 +33,7 @@ class GqaError(RuntimeError):
 
 
 class PrefillOpts(ctypes.Structure):
-    _fields_ = [("force_schedule", ctypes.c_int), ("force_grid", ctypes.c_int),
+    _fields_ = [("force_splits", ctypes.c_int), ("force_grid", ctypes.c_int),
                 ("wait_timeout_us", ctypes.c_uint32),
                 ("fwd_event_begin", ctypes.c_void_p), ("fwd_event_end", ctypes.c_void_p),
                 ("test_withhold_q", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
@@ -41,7 +41,8 @@ class PrefillOpts(ctypes.Structure):
 
 class PrefillPlan(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int), ("q_tiles", ctypes.c_int), ("n_items", ctypes.c_int),
-                ("schedule", ctypes.c_int), ("grid", ctypes.c_int), ("split_items", ctypes.c_int),
+                ("head_rounds", ctypes.c_int), ("tail_items", ctypes.c_int),
+                ("tail_splits", ctypes.c_int), ("n_units", ctypes.c_int), ("grid", ctypes.c_int),
                 ("kernels_per_call", ctypes.c_int), ("variant", ctypes.c_int),
                 ("total_tiles", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("est_makespan_tiles", ctypes.c_int64)]
@@ -124,11 +125,11 @@ def gqa_prefill_attn_noalloc(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_h
 
 
 def gqa_prefill_attn_ex(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
-                        stream=None, force_schedule=0, force_grid=0, wait_timeout_us=0,
+                        stream=None, force_splits=0, force_grid=0, wait_timeout_us=0,
                         fwd_events=None, test_withhold_q=False, check=True):
     """fwd_events: optional (begin, end) torch.cuda.Event pair recorded around the
     attention kernel itself (not the split merge)."""
-    opts = PrefillOpts(force_schedule=force_schedule, force_grid=force_grid,
+    opts = PrefillOpts(force_splits=force_splits, force_grid=force_grid,
                        wait_timeout_us=wait_timeout_us, test_withhold_q=1 if test_withhold_q else 0)
     if fwd_events is not None:
         opts.fwd_event_begin = fwd_events[0].cuda_event
@@ -143,10 +144,10 @@ def gqa_prefill_attn_ex(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
 
 
 def gqa_prefill_make_plan(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, num_sms,
-                          force_schedule=0, force_grid=0, check=True):
+                          force_splits=0, force_grid=0, check=True):
     plan = PrefillPlan()
     rc = lib.gqa_prefill_make_plan(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, num_sms,
-                                   force_schedule, force_grid, ctypes.byref(plan))
+                                   force_splits, force_grid, ctypes.byref(plan))
     if check:
         _check(rc)
     return rc, plan.as_dict()

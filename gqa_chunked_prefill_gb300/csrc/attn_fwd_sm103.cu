@@ -32,11 +32,11 @@
 //  * Causal tiles entirely above the diagonal are never visited; only the (at
 //    most two) tiles that straddle it are masked element-wise.
 //  * Persistent grid (one CTA per SM). Work items (query tile, KV group) are
-//    ordered longest first and either dealt out whole in a snake order, or
-//    laid end to end as one sequence of KV tiles cut into equal contiguous
-//    ranges, one per CTA (gqa_schedule.h). Items cut by a range boundary are
-//    computed in pieces that write normalised FP32 partials plus their base-2
-//    LSE; merge_ranges_kernel combines them.
+//    ordered longest first and dealt out in a snake, whole items in full
+//    rounds; the items of the last, partial round are split along KV into
+//    equal pieces so that they spread over all CTAs (gqa_schedule.h). Each
+//    piece writes a normalised FP32 partial plus its base-2 LSE, and
+//    merge_tail_kernel combines them.
 //  * Every mbarrier wait is bounded: on time-out the kernel records
 //    GQA_ERR_DEVICE_TIMEOUT, waits for its own TMA copies in flight, frees its
 //    tensor memory and returns.
@@ -161,8 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Geometry geo{p.q_len, p.p0, p.n_qtiles};
   PieceIter pieces;  // this CTA's work, in order; each role walks its own copy
-  pieces.init(geo, p.schedule, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x),
-              p.total_tiles);
+  pieces.init(geo, Schedule{p.head_items, p.tail_splits, p.n_units}, static_cast<int>(gridDim.x),
+              static_cast<int>(blockIdx.x));
 
   if (warp == kTmaWarp) {
     // ======================= TMA producer ======================================
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (valid && p.lse != nullptr) p.lse[qrow] = lse2 * kLn2;
       } else {
-        // A piece of a cut item: normalised partial rows go to this CTA's slot.
+        // A piece of a split item: normalised partial rows go to the piece's slot.
         const size_t prow = static_cast<size_t>(w.slot) * kRowsPerTile + row;
         float* dst = p.part_o + prow * kHeadDim;
 #pragma unroll 1
@@ -475,36 +475,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Combine the pieces of every item cut by a range boundary (kScheduleRanges).
-// Block m looks at boundary m (first tile of CTA m's range); it merges the item
-// the boundary cuts unless an earlier boundary already cut the same item. The
-// pieces come from CTAs m-1 .. owner(last tile), CTA m-1's piece in slot
-// 2(m-1)+1 and every later one in slot 2b; they are combined in CTA order:
-// lse = log2 sum_b 2^{lse_b}, out = sum_b 2^{lse_b - lse} O_b. One warp per row.
-__global__ void __launch_bounds__(256) merge_ranges_kernel(const MergeParams p) {
-  const Geometry geo{p.q_len, p.p0, p.n_qtiles};
-  const int m = blockIdx.x + 1;
-  const long long W = p.total_tiles;
-  const long long t = range_lo(W, p.grid, m);
-  const ItemPos it = locate(geo, t);
-  if (t == it.start || range_lo(W, p.grid, m - 1) > it.start) return;
-  const int b_lo = m - 1;
-  const int b_hi = range_owner(W, p.grid, it.start + it.nt - 1);
-  const int qt = geo.n_qtiles - 1 - it.r;
+// Combine the S pieces of every split (tail) item: block j merges item
+// head_items + j from slots j*S .. j*S + S-1, in that fixed order:
+// lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s. One warp per row.
+__global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
+  const int j = blockIdx.x;
+  const int item = p.head_items + j;
+  const int qt = p.n_qtiles - 1 - item / 4;
+  const int g = item % 4;
+  const int S = p.tail_splits;
   const int lane = threadIdx.x & 31;
   for (int row = threadIdx.x >> 5; row < kTokPerTile * kGroup; row += 8) {
     const int tok = kTokPerTile * qt + row / kGroup;
     if (tok >= p.q_len) break;
     float mx = kNegInf;
-    for (int b = b_lo; b <= b_hi; ++b) {
-      const int slot = b == b_lo ? 2 * b + 1 : 2 * b;
-      mx = fmaxf(mx, p.part_lse[static_cast<size_t>(slot) * kRowsPerTile + row]);
-    }
+    for (int s = 0; s < S; ++s)
+      mx = fmaxf(mx, p.part_lse[static_cast<size_t>(j * S + s) * kRowsPerTile + row]);
     const float m_use = (mx == kNegInf) ? 0.0f : mx;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float wsum = 0.0f;
-    for (int b = b_lo; b <= b_hi; ++b) {
-      const size_t prow = static_cast<size_t>(b == b_lo ? 2 * b + 1 : 2 * b) * kRowsPerTile + row;
+    for (int s = 0; s < S; ++s) {
+      const size_t prow = static_cast<size_t>(j * S + s) * kRowsPerTile + row;
       const float w = ptx::ex2_approx(p.part_lse[prow] - m_use);
       wsum += w;
       const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * kHeadDim + 8 * lane);
@@ -518,7 +509,7 @@ __global__ void __launch_bounds__(256) merge_ranges_kernel(const MergeParams p) 
     o.y = ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv);
     o.z = ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv);
     o.w = ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    const size_t orow = static_cast<size_t>(tok) * kQHeads + kGroup * it.g + row % kGroup;
+    const size_t orow = static_cast<size_t>(tok) * kQHeads + kGroup * g + row % kGroup;
     *reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 8 * lane) = o;
     if (lane == 0 && p.lse != nullptr)
       p.lse[orow] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;
@@ -540,8 +531,8 @@ cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
-  if (p.grid < 2) return cudaSuccess;
-  merge_ranges_kernel<<<p.grid - 1, 256, 0, stream>>>(p);
+  if (p.tail_items < 1 || p.tail_splits < 2) return cudaSuccess;
+  merge_tail_kernel<<<p.tail_items, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -27,15 +27,16 @@ struct FwdParams {
   CUtensorMap tmap_v;  // V [kv_len][4][256], box (64 d, 1 head, 64 keys), 128B swizzle
   __nv_bfloat16* out;  // [q_len][24][256]
   float* lse;          // [q_len][24] natural log, or null
-  float* part_o;       // [2*grid][128 rows][256] normalised partial O of cut items
-  float* part_lse;     // [2*grid][128 rows] base-2 partial LSE of cut items
+  float* part_o;       // [tail pieces][128 rows][256] normalised partial O (tail_splits > 1)
+  float* part_lse;     // [tail pieces][128 rows] base-2 partial LSE        (tail_splits > 1)
   int* status;         // per-device status word
   int q_len;
   int kv_len;
   int p0;              // kv_len - q_len: position of the chunk's first token
   int n_qtiles;        // ceil(q_len / 21)
-  int schedule;        // kScheduleItems or kScheduleRanges (gqa_schedule.h)
-  long long total_tiles;  // KV tiles over all items
+  int head_items;      // Schedule (gqa_schedule.h): items processed whole first
+  int tail_splits;     //   pieces per remaining item
+  int n_units;         //   units dealt to the CTAs
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
   int withhold_q;      // test only: the producer never loads the first Q tile
@@ -47,10 +48,10 @@ struct MergeParams {
   __nv_bfloat16* out;
   float* lse;             // may be null
   int q_len;
-  int p0;
   int n_qtiles;
-  int grid;               // CTAs of the attention launch
-  long long total_tiles;
+  int head_items;
+  int tail_items;         // one merge block per tail item
+  int tail_splits;
 };
 
 size_t fwd_smem_bytes();

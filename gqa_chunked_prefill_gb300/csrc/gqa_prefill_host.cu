@@ -37,86 +37,93 @@ constexpr double kTileUs = 1.5;              // planning estimate per tile
 constexpr double kMergeBytesPerUs = 6.0e6;   // HBM bandwidth for the merge pass
 constexpr double kMergeLaunchUs = 4.0;
 constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
+constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16};
 
 Geometry geometry(int q_len, int kv_len) {
   return Geometry{q_len, kv_len - q_len, (q_len + kTokPerTile - 1) / kTokPerTile};
 }
 
-// Fills *plan for one schedule on `grid_cap` CTAs at most; returns the estimated time in us.
-double plan_schedule(int q_len, int kv_len, int num_sms, int grid_cap, int schedule,
+// Fills *plan for head_rounds whole rounds and S-way tail splits on `grid` CTAs
+// (S must not exceed the shortest item's tiles); returns the estimated time in us.
+double plan_schedule(const Geometry& geo, int num_sms, int grid, int head_rounds, int S,
                      gqa_prefill_plan* plan) {
-  const Geometry geo = geometry(q_len, kv_len);
   const int n_items = geo.n_qtiles * kKvHeads;
-  const int64_t W = total_tiles(geo);
-  int grid = schedule == kScheduleItems ? std::min(n_items, grid_cap)
-                                        : static_cast<int>(std::min<int64_t>(W, grid_cap));
-  grid = std::max(grid, 1);
-  // Busiest CTA and number of cut items, by walking every CTA's pieces.
-  int64_t makespan = 0;
-  int cut = 0;
-  for (int b = 0; b < grid; ++b) {
-    PieceIter it;
-    it.init(geo, schedule, grid, b, W);
-    Piece w;
-    int64_t load = 0;
-    while (it.next(w)) {
-      load += (w.n1 - w.n0) + kPieceOverheadTiles;
-      if (w.slot >= 0 && w.n0 == 0) ++cut;  // each cut item once, at its first piece
-    }
-    makespan = std::max(makespan, load);
+  const int head = std::min(head_rounds * grid, n_items);
+  const Schedule sc{head, S, head + (n_items - head) * S};
+  grid = std::max(1, std::min(grid, sc.n_units));
+  std::vector<int64_t> load(static_cast<size_t>(grid), 0);
+  int64_t total = 0;
+  for (int u = 0; u < sc.n_units; ++u) {
+    const int r = u / grid, x = u % grid;
+    const int b = (r & 1) ? grid - 1 - x : x;
+    const Piece w = unit_piece(geo, sc, u);
+    load[static_cast<size_t>(b)] += (w.n1 - w.n0) + kPieceOverheadTiles;
+    total += w.n1 - w.n0;
   }
+  const int tail = n_items - head;
   std::memset(plan, 0, sizeof(*plan));
   plan->num_sms = num_sms;
   plan->q_tiles = geo.n_qtiles;
   plan->n_items = n_items;
-  plan->schedule = schedule;
+  plan->head_rounds = head / grid;
+  plan->tail_items = tail;
+  plan->tail_splits = S;
+  plan->n_units = sc.n_units;
   plan->grid = grid;
-  plan->split_items = cut;
-  plan->kernels_per_call = cut > 0 ? 2 : 1;
+  plan->kernels_per_call = (S > 1 && tail > 0) ? 2 : 1;
   plan->variant = 1;
-  plan->total_tiles = W;
-  plan->workspace_bytes = cut > 0 ? int64_t{2} * grid * kRowsPerTile * kPartialRowBytes : 0;
-  plan->est_makespan_tiles = makespan;
-  double us = static_cast<double>(makespan) * kTileUs;
-  if (cut > 0) {
-    // Each cut item is read back in ~2-3 pieces and written once.
-    const double bytes = cut * static_cast<double>(kRowsPerTile) * (3.0 * kPartialRowBytes + 520.0);
+  plan->total_tiles = total;
+  plan->workspace_bytes =
+      (S > 1 && tail > 0) ? static_cast<int64_t>(tail) * S * kRowsPerTile * kPartialRowBytes : 0;
+  plan->est_makespan_tiles = *std::max_element(load.begin(), load.end());
+  double us = static_cast<double>(plan->est_makespan_tiles) * kTileUs;
+  if (plan->kernels_per_call == 2) {
+    const double bytes = tail * static_cast<double>(kRowsPerTile) * (S * kPartialRowBytes + 520.0);
     us += bytes / kMergeBytesPerUs + kMergeLaunchUs;
   }
   return us;
 }
 
-// Pure function of its arguments.
-void compute_plan(int q_len, int kv_len, int num_sms, int force_schedule, int force_grid,
+// Pure function of its arguments. Searches the number of whole rounds and the
+// tail split; a split must win by 2 % over the simpler plan to be taken.
+void compute_plan(int q_len, int kv_len, int num_sms, int force_splits, int force_grid,
                   gqa_prefill_plan* plan) {
-  const int cap = force_grid > 0 ? std::min(force_grid, num_sms) : num_sms;
-  if (force_schedule == 1) {
-    plan_schedule(q_len, kv_len, num_sms, cap, kScheduleItems, plan);
+  const Geometry geo = geometry(q_len, kv_len);
+  const int n_items = geo.n_qtiles * kKvHeads;
+  const int grid = std::max(1, force_grid > 0 ? std::min(force_grid, num_sms) : num_sms);
+  const int max_splits = std::max(1, item_tiles(geo, 0));  // the shortest item's tiles
+  const int full_rounds = n_items / grid;
+  if (force_splits > 0) {
+    plan_schedule(geo, num_sms, grid, full_rounds, std::min(force_splits, max_splits), plan);
     return;
   }
-  if (force_schedule == 2) {
-    plan_schedule(q_len, kv_len, num_sms, cap, kScheduleRanges, plan);
-    return;
+  double best = plan_schedule(geo, num_sms, grid, 0, 1, plan);  // whole items only
+  gqa_prefill_plan cand{};
+  for (int hr = full_rounds; hr >= 0; --hr) {
+    for (int S : kSplitCandidates) {
+      if (S == 1 || S > max_splits) continue;
+      const double us = plan_schedule(geo, num_sms, grid, hr, S, &cand);
+      if (us < 0.98 * best) {
+        best = us;
+        *plan = cand;
+      }
+    }
   }
-  gqa_prefill_plan whole{}, ranges{};
-  const double t_whole = plan_schedule(q_len, kv_len, num_sms, cap, kScheduleItems, &whole);
-  const double t_ranges = plan_schedule(q_len, kv_len, num_sms, cap, kScheduleRanges, &ranges);
-  *plan = t_ranges < 0.98 * t_whole ? ranges : whole;  // cutting items must win clearly
 }
 
 struct PlanKey {
-  int q_len, kv_len, num_sms, force_schedule, force_grid;
+  int q_len, kv_len, num_sms, force_splits, force_grid;
   bool operator<(const PlanKey& o) const {
-    return std::tie(q_len, kv_len, num_sms, force_schedule, force_grid) <
-           std::tie(o.q_len, o.kv_len, o.num_sms, o.force_schedule, o.force_grid);
+    return std::tie(q_len, kv_len, num_sms, force_splits, force_grid) <
+           std::tie(o.q_len, o.kv_len, o.num_sms, o.force_splits, o.force_grid);
   }
 };
 
-void cached_plan(int q_len, int kv_len, int num_sms, int force_schedule, int force_grid,
+void cached_plan(int q_len, int kv_len, int num_sms, int force_splits, int force_grid,
                  gqa_prefill_plan* plan) {
   static std::mutex mu;
   static std::map<PlanKey, gqa_prefill_plan> cache;
-  const PlanKey key{q_len, kv_len, num_sms, force_schedule, force_grid};
+  const PlanKey key{q_len, kv_len, num_sms, force_splits, force_grid};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -125,7 +132,7 @@ void cached_plan(int q_len, int kv_len, int num_sms, int force_schedule, int for
       return;
     }
   }
-  compute_plan(q_len, kv_len, num_sms, force_schedule, force_grid, plan);
+  compute_plan(q_len, kv_len, num_sms, force_splits, force_grid, plan);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache.emplace(key, *plan);
@@ -224,7 +231,7 @@ gqa_status run(const void* q, const void* k, const void* v, void* out, float* ls
   if ((st = device_state(&dev)) != GQA_OK) return st;
 
   gqa_prefill_plan plan{};
-  cached_plan(q_len, kv_len, dev->num_sms, opts ? opts->force_schedule : 0,
+  cached_plan(q_len, kv_len, dev->num_sms, opts ? opts->force_splits : 0,
               opts ? opts->force_grid : 0, &plan);
   if (plan_out) *plan_out = plan;
 
@@ -243,29 +250,32 @@ gqa_status run(const void* q, const void* k, const void* v, void* out, float* ls
   p.kv_len = kv_len;
   p.p0 = kv_len - q_len;
   p.n_qtiles = plan.q_tiles;
-  p.schedule = plan.schedule;
-  p.total_tiles = plan.total_tiles;
+  p.head_items = plan.head_rounds * plan.grid < plan.n_items ? plan.head_rounds * plan.grid
+                                                             : plan.n_items;
+  p.tail_splits = plan.tail_splits;
+  p.n_units = plan.n_units;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = (opts && opts->wait_timeout_us) ? 1000ull * opts->wait_timeout_us
                                                  : kDefaultTimeoutNs;
   p.withhold_q = (opts && opts->test_withhold_q) ? 1 : 0;
 
   void* ws = nullptr;
-  if (plan.split_items > 0) {
+  const size_t n_slots = static_cast<size_t>(plan.tail_items) * plan.tail_splits;
+  if (plan.kernels_per_call == 2) {
     if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(plan.workspace_bytes), dev->pool, stream) !=
         cudaSuccess)
       return GQA_ERR_CUDA;
     p.part_o = static_cast<float*>(ws);
-    p.part_lse = p.part_o + static_cast<size_t>(2) * plan.grid * kRowsPerTile * kHeadDim;
+    p.part_lse = p.part_o + n_slots * kRowsPerTile * kHeadDim;
   }
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   if (st == GQA_OK && launch_fwd(p, plan.grid, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   if (st == GQA_OK && ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) st = GQA_ERR_CUDA;
-  if (st == GQA_OK && plan.split_items > 0) {
-    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.p0, p.n_qtiles, plan.grid,
-                  plan.total_tiles};
+  if (st == GQA_OK && plan.kernels_per_call == 2) {
+    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.n_qtiles, p.head_items,
+                  plan.tail_items, plan.tail_splits};
     if (launch_merge(m, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   }
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) st = GQA_ERR_CUDA;
@@ -339,20 +349,23 @@ gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, f
   p.kv_len = kv_len;
   p.p0 = kv_len - q_len;
   p.n_qtiles = plan.q_tiles;
-  p.schedule = plan.schedule;
-  p.total_tiles = plan.total_tiles;
+  p.head_items = plan.head_rounds * plan.grid < plan.n_items ? plan.head_rounds * plan.grid
+                                                             : plan.n_items;
+  p.tail_splits = plan.tail_splits;
+  p.n_units = plan.n_units;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = kDefaultTimeoutNs;
-  if (plan.split_items > 0) {
+  if (plan.kernels_per_call == 2) {
     // Every partial row the merge reads is written by the attention kernel first,
     // so the scratch needs no clearing between calls.
     p.part_o = static_cast<float*>(dev->scratch);
-    p.part_lse = p.part_o + static_cast<size_t>(2) * plan.grid * kRowsPerTile * kHeadDim;
+    p.part_lse = p.part_o + static_cast<size_t>(plan.tail_items) * plan.tail_splits *
+                                kRowsPerTile * kHeadDim;
   }
   if (launch_fwd(p, plan.grid, stream) != cudaSuccess) return GQA_ERR_CUDA;
-  if (plan.split_items > 0) {
-    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.p0, p.n_qtiles, plan.grid,
-                  plan.total_tiles};
+  if (plan.kernels_per_call == 2) {
+    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.n_qtiles, p.head_items,
+                  plan.tail_items, plan.tail_splits};
     if (launch_merge(m, stream) != cudaSuccess) return GQA_ERR_CUDA;
   }
   return GQA_OK;
@@ -387,7 +400,7 @@ gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void
 }
 
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int num_sms, int force_schedule, int force_grid,
+                                 int num_sms, int force_splits, int force_grid,
                                  gqa_prefill_plan* plan) {
   if (!plan) return GQA_ERR_NULL;
   const gqa_status st =
@@ -396,7 +409,7 @@ gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_
   if (num_sms <= 0) return GQA_ERR_SHAPE;
   std::memset(plan, 0, sizeof(*plan));
   if (q_len == 0) return GQA_OK;
-  gqa::cached_plan(q_len, kv_len, num_sms, force_schedule, force_grid, plan);
+  gqa::cached_plan(q_len, kv_len, num_sms, force_splits, force_grid, plan);
   return GQA_OK;
 }
 

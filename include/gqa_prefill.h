@@ -74,9 +74,10 @@ gqa_status gqa_prefill_attn(const void* q, const void* k, const void* v, void* o
 
 /* Options for gqa_prefill_attn_ex (zero-initialise; zero fields mean "default"). */
 typedef struct gqa_prefill_opts {
-  int force_schedule;         /* 0: planner decides; 1: whole work items only (no
-                                 merge pass); 2: balanced KV-tile ranges per CTA,
-                                 items cut at range boundaries are merged        */
+  int force_splits;           /* 0: planner decides; S > 0: every full round of the
+                                 grid takes whole items and each remaining item is
+                                 split into S KV pieces (capped at the shortest
+                                 item's tile count; 1 = no split, no merge pass) */
   int force_grid;             /* > 0: use at most this many CTAs (tests use it to cut
                                  items into many pieces); 0: one CTA per SM       */
   uint32_t wait_timeout_us;   /* bound on any single device-side wait; 0 = 2 s      */
@@ -97,22 +98,24 @@ typedef struct gqa_prefill_opts {
  * What the planner chose (the route check: which kernel ran and how).
  * A work item is one 21-token query tile of one KV group (21 x 6 = 126 MMA
  * rows); it visits KV tiles of 128 keys up to the causal diagonal. Items are
- * ordered longest first. Schedule 0 deals whole items to the persistent CTAs;
- * schedule 1 gives every CTA an equal contiguous range of the items' KV tiles
- * laid end to end, and a second kernel merges the items cut at range
- * boundaries.
+ * ordered longest first and dealt to the persistent CTAs in a snake, whole
+ * items in the first head_rounds full rounds; each remaining (tail) item is
+ * split into tail_splits pieces of equal KV length, and a second kernel
+ * merges the pieces.
  */
 typedef struct gqa_prefill_plan {
   int num_sms;                /* SMs of the device                                    */
   int q_tiles;                /* ceil(q_len / 21)                                     */
   int n_items;                /* q_tiles * n_kv_heads                                 */
-  int schedule;               /* 0 = whole items, 1 = balanced KV-tile ranges         */
+  int head_rounds;            /* full rounds of whole items                           */
+  int tail_items;             /* items after those rounds                             */
+  int tail_splits;            /* KV pieces per tail item (1 = whole, no merge pass)   */
+  int n_units;                /* units dealt: head items + tail_items * tail_splits   */
   int grid;                   /* CTAs launched for the attention kernel               */
-  int split_items;            /* items cut by a range boundary (merged afterwards)    */
   int kernels_per_call;       /* launches per call: 1, or 2 with the merge kernel     */
   int variant;                /* 1 = tcgen05 1-CTA M=128 kernel                       */
   int64_t total_tiles;        /* KV tiles summed over all items                       */
-  int64_t workspace_bytes;    /* temporary FP32 partials of cut items (0 if none)     */
+  int64_t workspace_bytes;    /* temporary FP32 partials of the split items (or 0)    */
   int64_t est_makespan_tiles; /* planner's cost of the busiest CTA, in KV tiles       */
 } gqa_prefill_plan;
 
@@ -124,12 +127,12 @@ gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void
 
 /*
  * Host-only planning (no CUDA call): fills *plan for a device with `num_sms`
- * SMs exactly as gqa_prefill_attn_ex would with the same force_schedule and
+ * SMs exactly as gqa_prefill_attn_ex would with the same force_splits and
  * force_grid options (0 = planner decides). Validates shapes like the
  * attention call (pointers are not involved).
  */
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int num_sms, int force_schedule, int force_grid,
+                                 int num_sms, int force_splits, int force_grid,
                                  gqa_prefill_plan* plan);
 
 /*
@@ -158,7 +161,7 @@ gqa_status gqa_prefill_poll(void* stream, int* device_status);
  * The scratch array is GQA_NOALLOC_SCRATCH_BYTES (64 MiB) of device memory,
  * held on every GPU that loads the library until the process exits. The call
  * plans exactly like gqa_prefill_attn; when that plan's partials
- * (2 * grid * 128 * 257 * 4 bytes when items are cut, 0 otherwise)
+ * (tail_items * tail_splits * 128 * 257 * 4 bytes when items are split, else 0)
  * exceed the array, it returns GQA_ERR_SCRATCH and launches nothing.
  *
  * It calls no cudaMalloc, cudaFree or other allocating routine. Its first call

@@ -1,9 +1,12 @@
 // Host check of the work decomposition in gqa_schedule.h (compiled with g++ by
-// tests/test_schedule_cpu.py): the closed-form tile prefix and item lookup
-// against brute force, and, for both schedules and many grid sizes, that every
-// KV tile of every item is computed exactly once, partial slots are unique and
-// owned by their CTA, and the merge side finds exactly the slots the kernel
-// writes. Prints "checks=N bad=M" and exits non-zero on any mismatch.
+// tests/test_schedule_cpu.py). For many chunk shapes, grid sizes, numbers of
+// whole rounds and tail splits (never more splits than the shortest item has
+// KV tiles, as the planner guarantees) it checks that every KV tile of every
+// item is computed exactly once, that no unit is empty, that whole items and
+// only they write the output directly, that partial slots are exactly
+// 0 .. tail_items*S-1 with item j's pieces in slots j*S .. j*S+S-1 (what the
+// merge kernel reads), and that every unit is dealt to exactly one CTA.
+// Prints "checks=N bad=M" and exits non-zero on any mismatch.
 #include "gqa_schedule.h"
 
 #include <cstdio>
@@ -16,86 +19,64 @@ int main() {
   long long checks = 0;
   int bad = 0;
   const int qls[] = {1, 2, 5, 20, 21, 22, 42, 43, 127, 128, 129, 500, 512, 3072, 4096};
-  const int extras[] = {0, 1, 100, 127, 128, 129, 255, 1000, 4096, 12288, 28672};
-  const int grids[] = {1, 2, 3, 7, 64, 148, 152, 1000};
+  const int extras[] = {0, 1, 100, 127, 128, 129, 255, 1000, 4096, 28672};
+  const int grids[] = {1, 2, 3, 7, 64, 152, 1000};
+  const int splits[] = {1, 2, 3, 4, 7, 16};
   for (int ql : qls)
     for (int ex : extras) {
       const Geometry geo{ql, ex, (ql + 20) / 21};
-      std::vector<long long> start;
+      const int n_items = 4 * geo.n_qtiles;
       std::vector<int> nts;
-      long long acc = 0;
-      for (int r = 0; r < geo.n_qtiles; ++r)
-        for (int g = 0; g < 4; ++g) {
-          const int nt = item_tiles(geo, geo.n_qtiles - 1 - r);
-          start.push_back(acc);
-          nts.push_back(nt);
-          acc += nt;
-        }
-      const long long W = total_tiles(geo);
-      if (W != acc) {
-        printf("total mismatch q_len=%d p0=%d: %lld vs %lld\n", ql, ex, W, acc);
-        ++bad;
-      }
-      for (size_t i = 0; i < start.size(); ++i)
-        for (long long t = start[i]; t < start[i] + nts[i]; t += (nts[i] > 3 ? nts[i] / 3 : 1)) {
-          const ItemPos p = locate(geo, t);
-          ++checks;
-          if (static_cast<size_t>(4 * p.r + p.g) != i || p.start != start[i] || p.nt != nts[i]) {
-            if (++bad < 5) printf("locate mismatch q_len=%d p0=%d t=%lld\n", ql, ex, t);
-          }
-        }
-      for (int mode = 0; mode < 2; ++mode)
-        for (int G0 : grids) {
-          const int n_items = 4 * geo.n_qtiles;
-          const int G = mode == 0 ? (G0 < n_items ? G0 : n_items) : static_cast<int>(G0 < W ? G0 : W);
-          std::map<long long, int> cover;  // item * 100000 + tile -> times computed
-          std::map<int, int> slots;
-          for (int b = 0; b < G; ++b) {
-            PieceIter it;
-            it.init(geo, mode, G, b, W);
-            Piece w;
-            while (it.next(w)) {
-              const int item = 4 * (geo.n_qtiles - 1 - w.qt) + w.g;
-              if (w.n0 < 0 || w.n1 > nts[item] || w.n0 >= w.n1) {
-                ++bad;
-                printf("bad piece range\n");
+      for (int i = 0; i < n_items; ++i) nts.push_back(item_tiles(geo, geo.n_qtiles - 1 - i / 4));
+      const int shortest = item_tiles(geo, 0);
+      for (int G0 : grids)
+        for (int S : splits) {
+          if (S > shortest) continue;
+          const int max_rounds = n_items / G0;
+          for (int hr : {0, 1, max_rounds}) {
+            if (hr > max_rounds || (hr == 1 && max_rounds == 1 && hr != max_rounds)) continue;
+            const int head = hr * G0 < n_items ? hr * G0 : n_items;
+            const Schedule sc{head, S, head + (n_items - head) * S};
+            const int G = G0 < sc.n_units ? G0 : sc.n_units;
+            if (hr > 0 && G != G0) continue;  // whole rounds need a full grid
+            std::map<long long, int> cover;
+            std::map<int, int> slots;
+            int units_seen = 0;
+            for (int b = 0; b < G; ++b) {
+              PieceIter it;
+              it.init(geo, sc, G, b);
+              Piece w;
+              while (it.next(w)) {
+                ++units_seen;
+                const int item = 4 * (geo.n_qtiles - 1 - w.qt) + w.g;
+                if (w.n0 < 0 || w.n1 > nts[item] || w.n0 >= w.n1) { ++bad; printf("empty or bad range\n"); }
+                const bool whole = w.n0 == 0 && w.n1 == nts[item];
+                if (item < head && !(whole && w.slot < 0)) { ++bad; printf("head item not whole\n"); }
+                if (item >= head) {
+                  if (S == 1 && w.slot >= 0) { ++bad; printf("unsplit tail wrote a slot\n"); }
+                  if (S > 1) {
+                    const int j = item - head;
+                    if (w.slot < j * S || w.slot >= j * S + S) { ++bad; printf("slot outside item block\n"); }
+                    if (slots[w.slot]++) { ++bad; printf("slot reused\n"); }
+                  }
+                }
+                for (int n = w.n0; n < w.n1; ++n) cover[static_cast<long long>(item) * 100000 + n]++;
               }
-              const bool whole = w.n0 == 0 && w.n1 == nts[item];
-              if (whole != (w.slot < 0)) {
-                ++bad;
-                printf("slot / whole mismatch\n");
-              }
-              if (w.slot >= 0) {
-                if (slots[w.slot]++) { ++bad; printf("slot reused\n"); }
-                if (w.slot / 2 != b) { ++bad; printf("slot not owned by its CTA\n"); }
-              }
-              for (int n = w.n0; n < w.n1; ++n) cover[static_cast<long long>(item) * 100000 + n]++;
             }
-          }
-          for (size_t i = 0; i < nts.size(); ++i)
-            for (int n = 0; n < nts[i]; ++n) {
-              ++checks;
-              const int c = cover[static_cast<long long>(i) * 100000 + n];
-              if (c != 1 && ++bad < 10)
-                printf("coverage q_len=%d p0=%d mode=%d G=%d item=%zu tile=%d count=%d\n", ql, ex,
-                       mode, G, i, n, c);
-            }
-          if (mode == 1)
-            for (int m = 1; m < G; ++m) {  // the merge kernel's view of boundary m
-              const long long t = range_lo(W, G, m);
-              const ItemPos p = locate(geo, t);
-              if (t == p.start || range_lo(W, G, m - 1) > p.start) continue;
-              const int b_lo = m - 1, b_hi = range_owner(W, G, p.start + p.nt - 1);
-              if (range_lo(W, G, b_lo) > p.start || range_lo(W, G, b_hi) >= p.start + p.nt ||
-                  range_lo(W, G, b_hi + 1) < p.start + p.nt) {
-                ++bad;
-                printf("range owner mismatch\n");
-              }
-              for (int b = b_lo; b <= b_hi; ++b) {
+            if (units_seen != sc.n_units) { ++bad; printf("units dealt %d of %d\n", units_seen, sc.n_units); }
+            for (int i = 0; i < n_items; ++i)
+              for (int n = 0; n < nts[i]; ++n) {
                 ++checks;
-                if (!slots.count(b == b_lo ? 2 * b + 1 : 2 * b)) { ++bad; printf("merge slot missing\n"); }
+                const int c = cover[static_cast<long long>(i) * 100000 + n];
+                if (c != 1 && ++bad < 10)
+                  printf("coverage q_len=%d p0=%d G=%d S=%d hr=%d item=%d tile=%d count=%d\n", ql, ex,
+                         G, S, hr, i, n, c);
               }
+            if (S > 1 && static_cast<int>(slots.size()) != (n_items - head) * S) {
+              ++bad;
+              printf("slot count\n");
             }
+          }
         }
     }
   printf("checks=%lld bad=%d\n", checks, bad);

@@ -1,6 +1,6 @@
 """CPU-only checks of the C ABI: the library loads without a GPU, exports every
 function include/*.h declares, refuses bad calls before touching CUDA, and its
-host planner behaves (deterministic, grid within SM count, balanced ranges)."""
+host planner behaves (deterministic, grid within SM count, tail split balances)."""
 import ctypes
 import glob
 import os
@@ -69,40 +69,43 @@ def _total_tiles(q_len, kv_len):
 
 @pytest.mark.parametrize("q_len,kv_len", SHAPES)
 @pytest.mark.parametrize("sms", [148, 152])
-@pytest.mark.parametrize("force", [0, 1, 2])
+@pytest.mark.parametrize("force", [0, 1, 3])
 def test_planner_invariants(gqa, q_len, kv_len, sms, force):
-    _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_schedule=force)
+    _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_splits=force)
     q_tiles = -(-q_len // 21)
+    n = 4 * q_tiles
     W = _total_tiles(q_len, kv_len)
-    assert p["q_tiles"] == q_tiles and p["n_items"] == 4 * q_tiles and p["total_tiles"] == W
-    assert p["schedule"] in (0, 1) and (force == 0 or p["schedule"] == force - 1)
-    assert 1 <= p["grid"] <= sms
-    if p["schedule"] == 0:
-        assert p["grid"] == min(4 * q_tiles, sms) and p["split_items"] == 0
-    else:
-        assert p["grid"] == min(W, sms) and p["split_items"] <= p["grid"] - 1
-    assert p["kernels_per_call"] == (2 if p["split_items"] else 1)
-    assert p["workspace_bytes"] == (2 * p["grid"] * 128 * 257 * 4 if p["split_items"] else 0)
+    assert p["q_tiles"] == q_tiles and p["n_items"] == n and p["total_tiles"] == W
+    shortest = -(-(kv_len - q_len + min(21, q_len)) // 128)
+    assert 1 <= p["tail_splits"] <= max(shortest, 1)
+    if force:
+        assert p["tail_splits"] == min(force, shortest)
+    head = min(p["head_rounds"] * p["grid"], n)
+    assert p["tail_items"] == n - head
+    assert p["n_units"] == head + p["tail_items"] * p["tail_splits"]
+    assert 1 <= p["grid"] <= min(sms, p["n_units"])
+    split = p["tail_splits"] > 1 and p["tail_items"] > 0
+    assert p["kernels_per_call"] == (2 if split else 1)
+    assert p["workspace_bytes"] == (p["tail_items"] * p["tail_splits"] * 128 * 257 * 4 if split else 0)
     assert p["est_makespan_tiles"] * p["grid"] >= W  # the busiest CTA carries at least the mean
-    _, again = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_schedule=force)
+    _, again = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_splits=force)
     assert again == p
 
 
-def test_ranges_balance_long_chunks(gqa):
-    """On the long workloads the balanced ranges beat whole items by the tail they remove."""
+def test_split_tail_balances_long_chunks(gqa):
+    """On the long workloads splitting the last round beats whole items."""
     for q_len, kv_len in ((4096, 16384), (4096, 32768)):
-        _, whole = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, force_schedule=1)
-        _, ranges = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, force_schedule=2)
-        assert ranges["est_makespan_tiles"] < 0.95 * whole["est_makespan_tiles"]
-        mean = -(-ranges["total_tiles"] // 152)
-        assert ranges["est_makespan_tiles"] <= mean + 2 * 12  # within a few piece overheads
+        _, whole = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, force_splits=1)
+        _, auto = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152)
+        assert auto["tail_splits"] > 1 and auto["head_rounds"] >= 1
+        assert auto["est_makespan_tiles"] < 0.93 * whole["est_makespan_tiles"]
 
 
 def test_force_grid_caps_the_grid(gqa):
-    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_schedule=2, force_grid=3)
-    assert p["grid"] == 3 and p["split_items"] >= 1
-    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_schedule=1, force_grid=5)
-    assert p["grid"] == 5 and p["split_items"] == 0
+    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_splits=3, force_grid=5)
+    assert p["grid"] == 5 and p["head_rounds"] == 5 and p["tail_items"] == 3
+    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_splits=1, force_grid=5)
+    assert p["grid"] == 5 and p["kernels_per_call"] == 1
 
 
 def test_make_plan_validates(gqa):

@@ -24,16 +24,16 @@ def test_run_twice_bit_identical(cuda_device, name):
 
 
 @pytest.mark.parametrize("q_len,kv_len,t_star", [(100, 700, 40), (300, 300, 150), (512, 4096, 200)])
-@pytest.mark.parametrize("schedule,grid", [(0, 0), (2, 9)])
-def test_future_keys_leave_earlier_rows_bit_identical(cuda_device, q_len, kv_len, t_star, schedule,
+@pytest.mark.parametrize("splits,grid", [(0, 0), (3, 9)])
+def test_future_keys_leave_earlier_rows_bit_identical(cuda_device, q_len, kv_len, t_star, splits,
                                                       grid):
     q, k, v = make_qkv(q_len, kv_len, seed=q_len + kv_len)
-    o1, l1, _ = run_gpu(q, k, v, SCALE, force_schedule=schedule, force_grid=grid)
+    o1, l1, _ = run_gpu(q, k, v, SCALE, force_splits=splits, force_grid=grid)
     p_star = kv_len - q_len + t_star
     k2, v2 = k.clone(), v.clone()
     k2[p_star + 1:] = (k2[p_star + 1:].float() * 3.0 + 1.0).to(torch.bfloat16)
     v2[p_star + 1:] = (-v2[p_star + 1:].float() + 2.0).to(torch.bfloat16)
-    o2, l2, _ = run_gpu(q, k2, v2, SCALE, force_schedule=schedule, force_grid=grid)
+    o2, l2, _ = run_gpu(q, k2, v2, SCALE, force_splits=splits, force_grid=grid)
     assert torch.equal(o1[: t_star + 1], o2[: t_star + 1])
     assert torch.equal(l1[: t_star + 1], l2[: t_star + 1])
     assert not torch.equal(o1[t_star + 1:], o2[t_star + 1:])
@@ -43,10 +43,10 @@ def test_future_keys_leave_earlier_rows_bit_identical(cuda_device, q_len, kv_len
 def test_whole_and_cut_items_agree(cuda_device, name):
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
-    o1, l1, p1 = run_gpu(q, k, v, SCALE, force_schedule=1)
-    o2, l2, p2 = run_gpu(q, k, v, SCALE, force_schedule=2)
-    assert p1["schedule"] == 0 and p1["split_items"] == 0
-    assert p2["schedule"] == 1 and p2["split_items"] > 0 and p2["kernels_per_call"] == 2
+    o1, l1, p1 = run_gpu(q, k, v, SCALE, force_splits=1)
+    o2, l2, p2 = run_gpu(q, k, v, SCALE, force_splits=4)
+    assert p1["tail_splits"] == 1 and p1["kernels_per_call"] == 1
+    assert p2["tail_splits"] == 4 and p2["tail_items"] > 0 and p2["kernels_per_call"] == 2
     check_close(o2.double().cpu().numpy(), l2.double().cpu().numpy(),
                 o1.double().cpu().numpy(), l1.double().cpu().numpy(), "cut vs whole items")
 

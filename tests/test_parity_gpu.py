@@ -45,25 +45,26 @@ def test_small_shapes_every_element(cuda_device, q_len, kv_len):
 
 
 @pytest.mark.parametrize("q_len,kv_len", [(22, 1000), (129, 1000), (43, 257), (7, 700), (300, 300)])
-@pytest.mark.parametrize("grid", [1, 3, 7, 40])
-def test_balanced_ranges_every_element(cuda_device, q_len, kv_len, grid):
-    """Schedule 1 on few CTAs: items are cut into many pieces and merged."""
+@pytest.mark.parametrize("splits,grid", [(2, 0), (3, 0), (7, 0), (3, 5), (2, 11), (4, 1)])
+def test_split_tail_every_element(cuda_device, q_len, kv_len, splits, grid):
+    """Items split into KV pieces and merged: all items (grid >= items) or only the
+    items after whole rounds on a few CTAs (small grid)."""
     q, k, v = make_qkv(q_len, kv_len, seed=11 * q_len + kv_len)
-    out, lse, plan = run_gpu(q, k, v, SCALE, force_schedule=2, force_grid=grid)
-    assert plan["schedule"] == 1 and plan["grid"] <= grid
-    assert plan["kernels_per_call"] == (2 if plan["split_items"] > 0 else 1)
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_grid=grid)
+    assert plan["grid"] <= (grid or plan["num_sms"])
+    assert plan["kernels_per_call"] == (2 if plan["tail_splits"] > 1 and plan["tail_items"] else 1)
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
-                f"{q_len}x{kv_len} ranges on {grid} CTAs")
+                f"{q_len}x{kv_len} splits {splits} grid {grid}")
 
 
 @pytest.mark.parametrize("q_len,kv_len", [(129, 1000), (300, 300)])
 @pytest.mark.parametrize("grid", [1, 5])
 def test_whole_items_on_few_ctas(cuda_device, q_len, kv_len, grid):
-    """Schedule 0 with more items than CTAs: each CTA walks many items in turn."""
+    """No split, more items than CTAs: each CTA walks many whole items in turn."""
     q, k, v = make_qkv(q_len, kv_len, seed=13 * q_len + kv_len)
-    out, lse, plan = run_gpu(q, k, v, SCALE, force_schedule=1, force_grid=grid)
-    assert plan["schedule"] == 0 and plan["split_items"] == 0 and plan["kernels_per_call"] == 1
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=1, force_grid=grid)
+    assert plan["tail_splits"] == 1 and plan["kernels_per_call"] == 1 and plan["grid"] == grid
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
                 f"{q_len}x{kv_len} whole items on {grid} CTAs")

@@ -1,7 +1,8 @@
 """The work decomposition shared by the planner and the kernels, checked on the
 CPU: tests/schedule_cover_check.cpp includes csrc/gqa_schedule.h directly and
-brute-forces coverage (every KV tile of every item exactly once, unique partial
-slots, merge-side slot lookup) over many chunk shapes and grid sizes."""
+brute-forces coverage (every KV tile of every item exactly once, no empty unit,
+partial slots exactly where the merge kernel reads them) over many chunk shapes,
+grid sizes, numbers of whole rounds and tail splits."""
 import os
 import subprocess
 

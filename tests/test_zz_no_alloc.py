@@ -4,11 +4,11 @@ start-up, code that must not risk cudaFree's implicit synchronisation, hosts
 whose allocator belongs to another framework). It keeps split-KV partials in a
 64 MiB scratch array compiled into the library instead of allocating them.
 
-Checks, through the C ABI: on workloads whose plan cuts work items between
-CTAs (so the scratch really holds partials), two calls in a row each match the
-allocating entry point within the suite's tolerance; a call whose partials
-would not fit is refused with GQA_ERR_SCRATCH and writes nothing (on devices
-where such a plan exists). This file is collected last,
+Checks, through the C ABI: on workloads whose plan splits work items along
+the KV range (so the scratch really holds partials), two calls in a row each
+match the allocating entry point within the suite's tolerance; a call whose
+partials would not fit is refused with GQA_ERR_SCRATCH and writes nothing (on
+devices where such a plan exists). This file is collected last,
 and it also passes when run alone in a fresh process."""
 import pytest
 import torch
@@ -58,7 +58,8 @@ def test_noalloc_uses_scratch_on_a_split_plan(cuda_device):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     plans = [gqa.gqa_prefill_make_plan(WORKLOADS[n].q_len, WORKLOADS[n].kv_len, 24, 4, 256, sms)[1]
              for n in ("q512_kv4096_kbias", "q512_kv32768")]
-    assert any(p["split_items"] > 0 and 0 < p["workspace_bytes"] <= SCRATCH_BYTES for p in plans)
+    assert any(p["kernels_per_call"] == 2 and 0 < p["workspace_bytes"] <= SCRATCH_BYTES
+               for p in plans)
 
 
 def test_noalloc_refuses_partials_larger_than_scratch(cuda_device):
