@@ -51,8 +51,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # source it was measured on; reported as null once the source no longer matches.
 KNOWN_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the full launch:
-    # 1.44 GB read + 199.37 MB written (split partials included).
-    "q4096_kv32768": {"bytes": 1_639_370_000, "kernel_sha256": "87cfe400611558bc9b7686a1261e15b6cfb4349ea3c46e79dfe28fe263c0d3af"},
+    # 791.32 MB read + 52.07 MB written.
+    "q4096_kv32768": {"bytes": 843_390_000, "kernel_sha256": "7f11ab4734f9aeffc5e0afcd33220dcb737a297725ae88742ac957e609836c0f"},
 }
 
 
