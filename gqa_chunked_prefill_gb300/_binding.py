@@ -36,7 +36,8 @@ class PrefillOpts(ctypes.Structure):
     _fields_ = [("force_splits", ctypes.c_int), ("force_grid", ctypes.c_int),
                 ("wait_timeout_us", ctypes.c_uint32),
                 ("fwd_event_begin", ctypes.c_void_p), ("fwd_event_end", ctypes.c_void_p),
-                ("test_withhold_q", ctypes.c_int), ("reserved", ctypes.c_int * 2)]
+                ("test_withhold_q", ctypes.c_int), ("force_variant", ctypes.c_int),
+                ("reserved", ctypes.c_int * 1)]
 
 
 class PrefillPlan(ctypes.Structure):
@@ -64,7 +65,8 @@ lib.gqa_prefill_attn_ex.argtypes = _ATTN_ARGS + [ctypes.POINTER(PrefillOpts), ct
 lib.gqa_prefill_attn_ex.restype = _i
 lib.gqa_prefill_attn_noalloc.argtypes = _ATTN_ARGS
 lib.gqa_prefill_attn_noalloc.restype = _i
-lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                      ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan.restype = _i
 lib.gqa_prefill_poll.argtypes = [_vp, ctypes.POINTER(_i)]
 lib.gqa_prefill_poll.restype = _i
@@ -125,12 +127,13 @@ def gqa_prefill_attn_noalloc(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_h
 
 
 def gqa_prefill_attn_ex(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
-                        stream=None, force_splits=0, force_grid=0, wait_timeout_us=0,
-                        fwd_events=None, test_withhold_q=False, check=True):
+                        stream=None, force_splits=0, force_grid=0, force_variant=0,
+                        wait_timeout_us=0, fwd_events=None, test_withhold_q=False, check=True):
     """fwd_events: optional (begin, end) torch.cuda.Event pair recorded around the
     attention kernel itself (not the split merge)."""
     opts = PrefillOpts(force_splits=force_splits, force_grid=force_grid,
-                       wait_timeout_us=wait_timeout_us, test_withhold_q=1 if test_withhold_q else 0)
+                       wait_timeout_us=wait_timeout_us, test_withhold_q=1 if test_withhold_q else 0,
+                       force_variant=force_variant)
     if fwd_events is not None:
         opts.fwd_event_begin = fwd_events[0].cuda_event
         opts.fwd_event_end = fwd_events[1].cuda_event
@@ -144,10 +147,10 @@ def gqa_prefill_attn_ex(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
 
 
 def gqa_prefill_make_plan(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, num_sms,
-                          force_splits=0, force_grid=0, check=True):
+                          force_splits=0, force_grid=0, force_variant=0, check=True):
     plan = PrefillPlan()
     rc = lib.gqa_prefill_make_plan(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, num_sms,
-                                   force_splits, force_grid, ctypes.byref(plan))
+                                   force_splits, force_grid, force_variant, ctypes.byref(plan))
     if check:
         _check(rc)
     return rc, plan.as_dict()

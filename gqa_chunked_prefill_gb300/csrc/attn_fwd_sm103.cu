@@ -91,6 +91,8 @@ constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base up 
 
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
+constexpr uint32_t kIdescQK2 = ptx::idesc_bf16_f32(256, 128, false, false);  // CTA pair
+constexpr uint32_t kIdescPV2 = ptx::idesc_bf16_f32(256, 256, false, true);   // CTA pair
 
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
@@ -98,11 +100,19 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 __device__ int g_status_word = 0;
 
+// Bounded wait for the phase of `bar` with the given parity. In CTA pairs the
+// arrivals come from the other CTA too, so the wait acquires at cluster scope.
+template <bool kCluster>
+__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
+  return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+}
+
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const FwdParams& p) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (try_wait<kCluster>(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (try_wait<kCluster>(bar, parity)) return true;
     if ((spin & 31u) == 0 && ptx::globaltimer_ns() - t0 > p.timeout_ns) {
       atomicExch(p.status, static_cast<int>(GQA_ERR_DEVICE_TIMEOUT));
       return false;
@@ -110,6 +120,16 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Fw
   }
 }
 
+// kPair = false: one CTA per work item (21 tokens x 6 heads = 126 MMA rows).
+// kPair = true: a cluster of two CTAs per work item (42 tokens); CTA r holds
+// tokens 21r .. 21r+20 (its own 128 MMA rows), the pair's leader (r = 0)
+// issues cta_group::2 MMAs with M = 256, and each CTA loads half of every K
+// tile (64 keys) and half of every V tile (128 of the 256 columns), so each
+// SM streams and re-reads half the B operands of the one-CTA kernel. TMA
+// copies of both CTAs complete on the leader's barriers; MMA completions are
+// multicast to both CTAs; the peer's softmax warps arrive on the leader's
+// barriers remotely.
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -123,6 +143,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;  // position in the pair
+  const bool leader = rank == 0;
+  // Barriers the leader's MMA thread waits on, as seen from this CTA.
+  auto lbar = [&](uint32_t id) { return kPair ? ptx::map_to_cta(bar(id), 0) : bar(id); };
+  auto arrive_leader = [&](uint32_t id) {
+    if constexpr (kPair) ptx::mbar_arrive_cluster(lbar(id)); else ptx::mbar_arrive(bar(id));
+  };
+  auto commit = [&](uint32_t id) {
+    if constexpr (kPair) ptx::tc_commit_pair(bar(id)); else ptx::tc_commit(bar(id));
+  };
+  constexpr uint32_t kConsumers = (kPair ? 2 : 1) * 4 * 32;  // softmax threads per item
 
   // ---- set-up: barriers, idle Q rows, tensor memory -------------------------
   if (threadIdx.x == 0) {
@@ -133,12 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(kBarQFull), 1);
     ptx::mbar_init(bar(kBarQEmpty), 1);
     ptx::mbar_init(bar(kBarSFull), 1);
-    ptx::mbar_init(bar(kBarSFree), 4 * 32);
-    ptx::mbar_init(bar(kBarPFull0), 4 * 32);
-    ptx::mbar_init(bar(kBarPFull1), 4 * 32);
+    ptx::mbar_init(bar(kBarSFree), kConsumers);
+    ptx::mbar_init(bar(kBarPFull0), kConsumers);
+    ptx::mbar_init(bar(kBarPFull1), kConsumers);
     ptx::mbar_init(bar(kBarPvDone0), 1);
     ptx::mbar_init(bar(kBarPvDone1), 1);
-    ptx::mbar_init(bar(kBarOFree), 4 * 32);
+    ptx::mbar_init(bar(kBarOFree), kConsumers);
     ptx::mbar_init(bar(kBarDrain), 1);
     ptx::fence_mbar_init();
   }
@@ -152,17 +183,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::fence_proxy_async_smem();
   }
   if (warp == kMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (kPair) {
+      ptx::tmem_alloc_pair(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) ptx::cluster_sync();  // both CTAs' barriers exist before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const Geometry geo{p.q_len, p.p0, p.n_qtiles};
-  PieceIter pieces;  // this CTA's work, in order; each role walks its own copy
-  pieces.init(geo, Schedule{p.head_items, p.tail_splits, p.n_units}, static_cast<int>(gridDim.x),
-              static_cast<int>(blockIdx.x));
+  const int tpi = kPair ? 2 * kTokPerTile : kTokPerTile;  // tokens per work item
+  const Geometry geo{p.q_len, p.p0, p.n_qtiles, tpi};
+  const int n_workers = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
+  const int worker = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  PieceIter pieces;  // this CTA's (pair's) work, in order; each role walks its own copy
+  pieces.init(geo, Schedule{p.head_items, p.tail_splits, p.n_units}, n_workers, worker);
 
   if (warp == kTmaWarp) {
     // ======================= TMA producer ======================================
@@ -177,21 +216,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool q_issued = false;
       uint32_t q_parity = 0;
       bool ok = true;
-      auto next_stage = [&](int n, bool is_k, int g) -> bool {
-        // Two 32 KB stages per K tile (d halves) and per V tile (key halves).
-        for (int half = 0; half < 2; ++half) {
-          if (!wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
-          const uint32_t fb = bar(kBarFull + st);
+      auto load = [&](uint32_t dst, const CUtensorMap* map, uint32_t id, int c0, int c1, int c2,
+                      uint64_t pol) {
+        if constexpr (kPair) ptx::tma_load_3d_pair(dst, map, lbar(id), c0, c1, c2, pol);
+        else ptx::tma_load_3d(dst, map, bar(id), c0, c1, c2, pol);
+      };
+      // One K tile is two 32 KB stages (d halves) in the one-CTA kernel and one
+      // stage (this CTA's 64 keys) in a pair; likewise for V (key halves / this
+      // CTA's 128 columns).
+      auto next_tile = [&](int n, bool is_k, int g) -> bool {
+        for (int half = 0; half < (kPair ? 1 : 2); ++half) {
+          if (!wait_bar<kPair>(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
           const uint32_t dst = stage_smem + st * kStageBytes;
-          ptx::mbar_arrive_expect_tx(fb, kStageBytes);
-          if (is_k) {
-            for (int c = 0; c < 2; ++c)
-              ptx::tma_load_3d(dst + c * kKBoxBytes, &p.tmap_k, fb, 128 * half + 64 * c, g,
-                               n * kBlockN, pol_kv);
+          if (leader) ptx::mbar_arrive_expect_tx(bar(kBarFull + st), (kPair ? 2 : 1) * kStageBytes);
+          if constexpr (kPair) {
+            if (is_k) {
+              for (int c = 0; c < 4; ++c)
+                load(dst + c * 8192, &p.tmap_k, kBarFull + st, 64 * c, g,
+                     n * kBlockN + 64 * static_cast<int>(rank), pol_kv);
+            } else {
+              for (int c = 0; c < 2; ++c)
+                load(dst + c * 16384, &p.tmap_v, kBarFull + st, 128 * static_cast<int>(rank) + 64 * c,
+                     g, n * kBlockN, pol_kv);
+            }
           } else {
-            for (int c = 0; c < 4; ++c)
-              ptx::tma_load_3d(dst + c * kVBoxBytes, &p.tmap_v, fb, 64 * c, g,
-                               n * kBlockN + 64 * half, pol_kv);
+            if (is_k) {
+              for (int c = 0; c < 2; ++c)
+                load(dst + c * kKBoxBytes, &p.tmap_k, kBarFull + st, 128 * half + 64 * c, g,
+                     n * kBlockN, pol_kv);
+            } else {
+              for (int c = 0; c < 4; ++c)
+                load(dst + c * kVBoxBytes, &p.tmap_v, kBarFull + st, 64 * c, g,
+                     n * kBlockN + 64 * half, pol_kv);
+            }
           }
           issued_mask |= 1u << st;
           issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
@@ -202,40 +259,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k = 0;
       Piece w;
       while (ok && pieces.next(w)) {
-        if (k > 0 && !(ok = wait_bar(bar(kBarQEmpty), (k - 1) & 1, p))) break;
+        if (k > 0 && !(ok = wait_bar<kPair>(bar(kBarQEmpty), (k - 1) & 1, p))) break;
         if (!(p.withhold_q && k == 0)) {
-          ptx::mbar_arrive_expect_tx(bar(kBarQFull), 4 * kQBoxBytes);
+          if (leader) ptx::mbar_arrive_expect_tx(bar(kBarQFull), (kPair ? 2 : 1) * 4 * kQBoxBytes);
           for (int c = 0; c < 4; ++c)
-            ptx::tma_load_3d(q_smem + c * kQChunkBytes, &p.tmap_q, bar(kBarQFull), 64 * c,
-                             kGroup * w.g, kTokPerTile * w.qt, pol_q);
+            load(q_smem + c * kQChunkBytes, &p.tmap_q, kBarQFull, 64 * c, kGroup * w.g,
+                 tpi * w.qt + kTokPerTile * static_cast<int>(rank), pol_q);
           q_issued = true;
           q_parity = k & 1;
         }
         // Consumption order of the MMA warp: K0, K1, V0, K2, V1, ..., V(nt-1).
         const int nt = w.n1 - w.n0;
         for (int j = 0; j < nt && ok; ++j) {
-          ok = next_stage(w.n0 + j, true, w.g);
-          if (ok && j >= 1) ok = next_stage(w.n0 + j - 1, false, w.g);
+          ok = next_tile(w.n0 + j, true, w.g);
+          if (ok && j >= 1) ok = next_tile(w.n0 + j - 1, false, w.g);
         }
-        if (ok) ok = next_stage(w.n1 - 1, false, w.g);
+        if (ok) ok = next_tile(w.n1 - 1, false, w.g);
         ++k;
       }
-      // Every copy this warp issued must have landed before the CTA exits. On the
-      // normal path the consumers already waited for all of them (these return at
-      // once); after a time-out they may still be in flight.
-      for (int s = 0; s < kStages; ++s)
-        if (issued_mask & (1u << s)) wait_bar(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
-      if (q_issued) wait_bar(bar(kBarQFull), q_parity, p);
+      // Every copy issued must have landed before the CTA exits. On the normal
+      // path the MMA thread already waited for all of them (these return at
+      // once); after a time-out they may still be in flight. In a pair all
+      // copies complete on the leader's barriers, so the leader drains for both.
+      if (leader) {
+        for (int s = 0; s < kStages; ++s)
+          if (issued_mask & (1u << s)) wait_bar<kPair>(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
+        if (q_issued) wait_bar<kPair>(bar(kBarQFull), q_parity, p);
+      }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer ========================================
+    // ======================= MMA issuer (the pair's leader) ====================
     // Issue order per unit: QK_0, then for each tile j: QK_{j+1}, PV_j. QK_{j+1}
     // runs on the tensor pipe while the softmax of tile j is in flight.
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       const uint64_t q_desc0 = ptx::smem_desc(q_smem, 16, 1024, ptx::kSwizzle128B);
       const uint64_t k_desc0 = ptx::smem_desc(stage_smem, 16, 1024, ptx::kSwizzle128B);
-      const uint64_t v_desc0 = ptx::smem_desc(stage_smem, kVBoxBytes, 1024, ptx::kSwizzle128B);
+      const uint64_t v_desc0 =
+          ptx::smem_desc(stage_smem, kPair ? 16384u : kVBoxBytes, 1024, ptx::kSwizzle128B);
       uint32_t st = 0, phase = 0;
       uint32_t tile = 0;  // KV tiles this CTA has processed (global tile index T)
       bool ok = true;
@@ -243,35 +304,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       Piece w;
       while (ok && pieces.next(w)) {
         const int nt = w.n1 - w.n0;
-        if (!(ok = wait_bar(bar(kBarQFull), k & 1, p))) break;
+        if (!(ok = wait_bar<kPair>(bar(kBarQFull), k & 1, p))) break;
         ptx::tc_fence_after();
-        // S = Q K_j^T over d = 256: two stages (d halves) x 2 chunks x 4 k-steps of 16.
-        // Descriptors are built once; an offset below 256 KB only touches the
-        // 14-bit start-address field, so stepping through a tile is one add.
+        // S = Q K_j^T over d = 256 in k-steps of 16. Descriptors are built once;
+        // an offset below 256 KB only touches the 14-bit start-address field, so
+        // stepping through a tile is one add.
         auto issue_qk = [&](int j) -> bool {
           const uint32_t T = tile + j;
           // S may be overwritten once the softmax holds tile T-1's scores in registers.
-          if (T > 0 && !wait_bar(bar(kBarSFree), (T - 1) & 1u, p)) return false;
+          if (T > 0 && !wait_bar<kPair>(bar(kBarSFree), (T - 1) & 1u, p)) return false;
           ptx::tc_fence_after();
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
+          if constexpr (kPair) {
+            // One stage: this CTA's 64 keys as 4 boxes (64-wide d chunks, 8 KB apart).
+            if (!wait_bar<kPair>(bar(kBarFull + st), phase, p)) return false;
             ptx::tc_fence_after();
             const uint64_t kd = k_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < 4; ++c) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = q_desc0 + (((2 * half + c) * kQChunkBytes + 32 * kk) >> 4);
-                const uint64_t bd = kd + ((c * kKBoxBytes + 32 * kk) >> 4);
-                ptx::mma_ss(tmem + kTmemS, a, bd, kIdescQK, (half | c | kk) != 0);
+                const uint64_t a = q_desc0 + ((c * kQChunkBytes + 32 * kk) >> 4);
+                const uint64_t bd = kd + ((c * 8192 + 32 * kk) >> 4);
+                ptx::mma_ss_pair(tmem + kTmemS, a, bd, kIdescQK2, (c | kk) != 0);
               }
             }
-            ptx::tc_commit(bar(kBarEmpty + st));
+            commit(kBarEmpty + st);
             if (++st == kStages) { st = 0; phase ^= 1u; }
+          } else {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              if (!wait_bar<kPair>(bar(kBarFull + st), phase, p)) return false;
+              ptx::tc_fence_after();
+              const uint64_t kd = k_desc0 + ((st * kStageBytes) >> 4);
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t a = q_desc0 + (((2 * half + c) * kQChunkBytes + 32 * kk) >> 4);
+                  const uint64_t bd = kd + ((c * kKBoxBytes + 32 * kk) >> 4);
+                  ptx::mma_ss(tmem + kTmemS, a, bd, kIdescQK, (half | c | kk) != 0);
+                }
+              }
+              commit(kBarEmpty + st);
+              if (++st == kStages) { st = 0; phase ^= 1u; }
+            }
           }
-          ptx::tc_commit(bar(kBarSFull));
-          if (j == nt - 1) ptx::tc_commit(bar(kBarQEmpty));
+          commit(kBarSFull);
+          if (j == nt - 1) commit(kBarQEmpty);
           return true;
         };
         ok = issue_qk(0);
@@ -279,34 +358,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j + 1 < nt && !(ok = issue_qk(j + 1))) break;
           const uint32_t T = tile + j;
           const uint32_t b = T & 1u;
-          if (!(ok = wait_bar(bar(b ? kBarPFull1 : kBarPFull0), (T >> 1) & 1u, p))) break;
-          if (j == 0 && k > 0 && !(ok = wait_bar(bar(kBarOFree), (k - 1) & 1, p))) break;
+          if (!(ok = wait_bar<kPair>(bar(b ? kBarPFull1 : kBarPFull0), (T >> 1) & 1u, p))) break;
+          if (j == 0 && k > 0 && !(ok = wait_bar<kPair>(bar(kBarOFree), (k - 1) & 1, p))) break;
           ptx::tc_fence_after();
-          // O += P_j V_j: two stages (key halves) x 4 k-steps of 16 keys, N = 256.
-          for (int half = 0; half < 2 && ok; ++half) {
-            if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
+          // O += P_j V_j in k-steps of 16 keys, N = 256. V stages are MN-major:
+          // LBO = next 64-wide d chunk, SBO = next group of 8 keys.
+          if constexpr (kPair) {
+            // One stage: 128 keys x this CTA's 128 columns (2 boxes, 16 KB apart).
+            if (!(ok = wait_bar<kPair>(bar(kBarFull + st), phase, p))) break;
             ptx::tc_fence_after();
             const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              // V stage: 4 boxes (64-wide d chunks, 8 KB apart) of 64 keys x 128 B.
-              // MN-major B: LBO = next d chunk, SBO = next group of 8 keys.
+            for (int kk = 0; kk < 8; ++kk) {
               const uint64_t bd = vd + ((2048 * kk) >> 4);
-              const uint32_t a_tmem = tmem + kTmemP + 64u * b + 32u * half + 8u * kk;
-              ptx::mma_ts(tmem + kTmemO, a_tmem, bd, kIdescPV, (j | half | kk) != 0);
+              ptx::mma_ts_pair(tmem + kTmemO, tmem + kTmemP + 64u * b + 8u * kk, bd, kIdescPV2,
+                               (j | kk) != 0);
             }
-            ptx::tc_commit(bar(kBarEmpty + st));
+            commit(kBarEmpty + st);
             if (++st == kStages) { st = 0; phase ^= 1u; }
+          } else {
+            // Two stages (key halves) of 4 boxes (64-wide d chunks, 8 KB apart).
+            for (int half = 0; half < 2 && ok; ++half) {
+              if (!(ok = wait_bar<kPair>(bar(kBarFull + st), phase, p))) break;
+              ptx::tc_fence_after();
+              const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bd = vd + ((2048 * kk) >> 4);
+                const uint32_t a_tmem = tmem + kTmemP + 64u * b + 32u * half + 8u * kk;
+                ptx::mma_ts(tmem + kTmemO, a_tmem, bd, kIdescPV, (j | half | kk) != 0);
+              }
+              commit(kBarEmpty + st);
+              if (++st == kStages) { st = 0; phase ^= 1u; }
+            }
           }
           if (!ok) break;
-          ptx::tc_commit(bar(b ? kBarPvDone1 : kBarPvDone0));
+          commit(b ? kBarPvDone1 : kBarPvDone0);
         }
         tile += nt;
         ++k;
       }
       // Drain: every MMA issued above has completed once this barrier fires.
-      ptx::tc_commit(bar(kBarDrain));
-      wait_bar(bar(kBarDrain), 0, p);
+      commit(kBarDrain);
+      wait_bar<kPair>(bar(kBarDrain), 0, p);
     }
     __syncwarp();
   } else {
@@ -322,22 +416,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     Piece w;
     while (ok && pieces.next(w)) {
       const int nt = w.n1 - w.n0;
-      const int tok = kTokPerTile * w.qt + tl;
+      const int tok0 = tpi * w.qt + kTokPerTile * static_cast<int>(rank);  // this CTA's first token
+      const int tok = tok0 + tl;
       const bool valid = row < kTokPerTile * kGroup && tok < p.q_len;
-      const int pos = p.p0 + tok;                          // last key this row may see
-      const int tile_min_pos = p.p0 + kTokPerTile * w.qt;  // smallest such key in the tile
+      const int pos = p.p0 + tok;            // last key this row may see
+      const int tile_min_pos = p.p0 + tok0;  // smallest such key among this CTA's rows
       float m_ref = kNegInf;  // max used in the exponent (base-2, scaled)
       float l = 0.0f;         // running row sum of p
       for (int j = 0; j < nt; ++j) {
         const uint32_t T = tile + j;
         const uint32_t b = T & 1u;
-        ok = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull), T & 1u, p));
+        ok = __all_sync(0xffffffffu, wait_bar<kPair>(bar(kBarSFull), T & 1u, p));
         if (!ok) break;
         ptx::tc_fence_after();
         uint32_t sr[128];
         ptx::tmem_ld_x128(lane_addr + kTmemS, sr);  // includes tcgen05.wait::ld
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(kBarSFree));  // the next QK^T may overwrite S now
+        arrive_leader(kBarSFree);  // the next QK^T may overwrite S now
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
@@ -366,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (need) m_ref = m_new;
           l *= alpha;
           // O must hold PV_{j-1} (which read P[(T-1)&1], use (T-1)>>1) before it is rescaled.
-          ok = __all_sync(0xffffffffu, wait_bar(bar((T - 1) & 1u ? kBarPvDone1 : kBarPvDone0),
+          ok = __all_sync(0xffffffffu, wait_bar<kPair>(bar((T - 1) & 1u ? kBarPvDone1 : kBarPvDone0),
                                                 ((T - 1) >> 1) & 1u, p));
           if (!ok) break;
           ptx::tc_fence_after();
@@ -400,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += sum0 + sum1;
         if (T >= 2) {
           // P[b] was last read by PV_{T-2}: it must have completed before P[b] is rewritten.
-          ok = __all_sync(0xffffffffu, wait_bar(bar(b ? kBarPvDone1 : kBarPvDone0),
+          ok = __all_sync(0xffffffffu, wait_bar<kPair>(bar(b ? kBarPvDone1 : kBarPvDone0),
                                                 ((T - 2) >> 1) & 1u, p));
           if (!ok) break;
           ptx::tc_fence_after();
@@ -408,12 +503,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_st_x64(lane_addr + kTmemP + 64u * b, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(b ? kBarPFull1 : kBarPFull0));
+        arrive_leader(b ? kBarPFull1 : kBarPFull0);
       }
       if (!ok) break;
       // ---- epilogue: O / l -> out (or the split partial), LSE ----------------
       const uint32_t T_last = tile + nt - 1;
-      ok = __all_sync(0xffffffffu, wait_bar(bar(T_last & 1u ? kBarPvDone1 : kBarPvDone0),
+      ok = __all_sync(0xffffffffu, wait_bar<kPair>(bar(T_last & 1u ? kBarPvDone1 : kBarPvDone0),
                                             (T_last >> 1) & 1u, p));
       if (!ok) break;
       ptx::tc_fence_after();
@@ -440,8 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (valid && p.lse != nullptr) p.lse[qrow] = lse2 * kLn2;
       } else {
-        // A piece of a split item: normalised partial rows go to the piece's slot.
-        const size_t prow = static_cast<size_t>(w.slot) * kRowsPerTile + row;
+        // A piece of a split item: normalised partial rows go to the piece's slot
+        // (one 128-row block per CTA of the item).
+        const size_t prow =
+            (static_cast<size_t>(w.slot) * (kPair ? 2 : 1) + rank) * kRowsPerTile + row;
         float* dst = p.part_o + prow * kHeadDim;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
@@ -460,23 +557,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid) p.part_lse[prow] = lse2;
       }
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(kBarOFree));
+      arrive_leader(kBarOFree);
       tile += nt;
       ++k;
     }
   }
 
   // ---- teardown ----------------------------------------------------------------
+  // In a pair, neither CTA may leave (or free tensor memory) while the leader's
+  // MMAs or the peer's remote arrivals can still touch it.
   ptx::tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) ptx::cluster_sync();
   if (warp == kMmaWarp) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    if constexpr (kPair) ptx::tmem_dealloc_pair(tmem, kTmemCols);
+    else ptx::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 // Combine the S pieces of every split (tail) item: block j merges item
-// head_items + j from slots j*S .. j*S + S-1, in that fixed order:
+// head_items + j from slots j*S .. j*S + S-1 (each slot holds one 128-row block
+// per CTA of the item), in that fixed order:
 // lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s. One warp per row.
 __global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
   const int j = blockIdx.x;
@@ -484,18 +586,21 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
   const int qt = p.n_qtiles - 1 - item / 4;
   const int g = item % 4;
   const int S = p.tail_splits;
+  const int cpi = p.ctas_per_item;
   const int lane = threadIdx.x & 31;
-  for (int row = threadIdx.x >> 5; row < kTokPerTile * kGroup; row += 8) {
-    const int tok = kTokPerTile * qt + row / kGroup;
-    if (tok >= p.q_len) break;
+  for (int rr = threadIdx.x >> 5; rr < cpi * kTokPerTile * kGroup; rr += 8) {
+    const int r = rr / (kTokPerTile * kGroup);    // CTA of the item
+    const int row = rr % (kTokPerTile * kGroup);  // its MMA row
+    const int tok = kTokPerTile * (cpi * qt + r) + row / kGroup;
+    if (tok >= p.q_len) continue;
     float mx = kNegInf;
     for (int s = 0; s < S; ++s)
-      mx = fmaxf(mx, p.part_lse[static_cast<size_t>(j * S + s) * kRowsPerTile + row]);
+      mx = fmaxf(mx, p.part_lse[(static_cast<size_t>(j * S + s) * cpi + r) * kRowsPerTile + row]);
     const float m_use = (mx == kNegInf) ? 0.0f : mx;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float wsum = 0.0f;
     for (int s = 0; s < S; ++s) {
-      const size_t prow = static_cast<size_t>(j * S + s) * kRowsPerTile + row;
+      const size_t prow = (static_cast<size_t>(j * S + s) * cpi + r) * kRowsPerTile + row;
       const float w = ptx::ex2_approx(p.part_lse[prow] - m_use);
       wsum += w;
       const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * kHeadDim + 8 * lane);
@@ -521,13 +626,48 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
 size_t fwd_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t prepare_fwd_kernel() {
-  return cudaFuncSetAttribute(gqa_attn_fwd_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(gqa_attn_fwd_sm103_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kSmemAlloc));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gqa_attn_fwd_sm103_kernel<true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(kSmemAlloc));
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream) {
-  gqa_attn_fwd_sm103_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(p);
-  return cudaGetLastError();
+cudaError_t max_active_pairs(int* pairs) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true>, &cfg);
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, cudaStream_t stream) {
+  if (!pair) {
+    gqa_attn_fwd_sm103_kernel<false><<<grid, kThreads, kSmemAlloc, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);  // 2 CTAs per pair
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true>, p);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {

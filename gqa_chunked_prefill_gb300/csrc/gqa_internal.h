@@ -23,8 +23,8 @@ constexpr int kThreads = 192;  // 4 softmax warps, 1 TMA warp, 1 MMA warp
 
 struct FwdParams {
   CUtensorMap tmap_q;  // Q [q_len][24][256], box (64 d, 6 heads, 21 tokens), 128B swizzle
-  CUtensorMap tmap_k;  // K [kv_len][4][256], box (64 d, 1 head, 128 keys), 128B swizzle
-  CUtensorMap tmap_v;  // V [kv_len][4][256], box (64 d, 1 head, 64 keys), 128B swizzle
+  CUtensorMap tmap_k;  // K [kv_len][4][256], box (64 d, 1 head, 128 keys; 64 keys for pairs)
+  CUtensorMap tmap_v;  // V [kv_len][4][256], box (64 d, 1 head, 64 keys; 128 keys for pairs)
   __nv_bfloat16* out;  // [q_len][24][256]
   float* lse;          // [q_len][24] natural log, or null
   float* part_o;       // [tail pieces][128 rows][256] normalised partial O (tail_splits > 1)
@@ -33,7 +33,7 @@ struct FwdParams {
   int q_len;
   int kv_len;
   int p0;              // kv_len - q_len: position of the chunk's first token
-  int n_qtiles;        // ceil(q_len / 21)
+  int n_qtiles;        // ceil(q_len / tokens per item): 21, or 42 for CTA pairs
   int head_items;      // Schedule (gqa_schedule.h): items processed whole first
   int tail_splits;     //   pieces per remaining item
   int n_units;         //   units dealt to the CTAs
@@ -52,10 +52,13 @@ struct MergeParams {
   int head_items;
   int tail_items;         // one merge block per tail item
   int tail_splits;
+  int ctas_per_item;      // 1, or 2 for the CTA-pair kernel (42-token items)
 };
 
 size_t fwd_smem_bytes();
-cudaError_t launch_fwd(const FwdParams& p, int grid, cudaStream_t stream);
+// grid = CTAs; with pair = true the CTAs form clusters of two (grid even).
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, cudaStream_t stream);
+cudaError_t max_active_pairs(int* pairs);       // co-resident CTA pairs on this device
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t prepare_fwd_kernel();                // per-device one-time attributes
 cudaError_t status_word_address(int** ptr);      // device address of the status word

@@ -31,99 +31,131 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per device-side wa
 
 // ------------------------------------------------------------------ planner --
 // Cost model in units of one 128-key KV tile of one item (QK^T + PV of a
-// 128 x 128 x 256 block: ~1.3 us of tensor-core time on one SM at peak).
+// 128 x 128 x 256 block per CTA: ~1.3 us of tensor-core time on one SM at peak).
 constexpr int64_t kPieceOverheadTiles = 2;   // Q load, pipeline fill, epilogue
-constexpr double kTileUs = 1.5;              // planning estimate per tile
+constexpr double kTileUs = 1.5;              // planning estimate per tile, one-CTA kernel
+// Per tile of a CTA pair (the same work per SM as a one-CTA tile). Measured on
+// GB300: the pair kernel runs ~1.3x slower per tile than the one-CTA kernel
+// (e.g. 4096x32768: 2.51 ms vs 1.91 ms), so the planner only picks it when
+// forced or when its schedule is far better balanced.
+constexpr double kPairTileUs = 1.95;
 constexpr double kMergeBytesPerUs = 6.0e6;   // HBM bandwidth for the merge pass
 constexpr double kMergeLaunchUs = 4.0;
 constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
 constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16};
 
-Geometry geometry(int q_len, int kv_len) {
-  return Geometry{q_len, kv_len - q_len, (q_len + kTokPerTile - 1) / kTokPerTile};
+Geometry geometry(int q_len, int kv_len, int variant) {
+  const int tpi = variant == 2 ? 2 * kTokPerTile : kTokPerTile;
+  return Geometry{q_len, kv_len - q_len, (q_len + tpi - 1) / tpi, tpi};
 }
 
-// Fills *plan for head_rounds whole rounds and S-way tail splits on `grid` CTAs
-// (S must not exceed the shortest item's tiles); returns the estimated time in us.
-double plan_schedule(const Geometry& geo, int num_sms, int grid, int head_rounds, int S,
-                     gqa_prefill_plan* plan) {
+// Fills *plan for `variant` (1: one CTA per item, 2: a CTA pair per item) with
+// head_rounds whole rounds and S-way tail splits over `workers` CTAs (or
+// pairs); S must not exceed the shortest item's tiles. Returns the estimated
+// time in us.
+double plan_schedule(const Geometry& geo, int num_sms, int variant, int workers, int head_rounds,
+                     int S, gqa_prefill_plan* plan) {
   const int n_items = geo.n_qtiles * kKvHeads;
-  const int head = std::min(head_rounds * grid, n_items);
+  const int cpi = variant == 2 ? 2 : 1;
+  const int head = std::min(head_rounds * workers, n_items);
   const Schedule sc{head, S, head + (n_items - head) * S};
-  grid = std::max(1, std::min(grid, sc.n_units));
-  std::vector<int64_t> load(static_cast<size_t>(grid), 0);
+  workers = std::max(1, std::min(workers, sc.n_units));
+  std::vector<int64_t> load(static_cast<size_t>(workers), 0);
   int64_t total = 0;
   for (int u = 0; u < sc.n_units; ++u) {
-    const int r = u / grid, x = u % grid;
-    const int b = (r & 1) ? grid - 1 - x : x;
+    const int r = u / workers, x = u % workers;
+    const int b = (r & 1) ? workers - 1 - x : x;
     const Piece w = unit_piece(geo, sc, u);
     load[static_cast<size_t>(b)] += (w.n1 - w.n0) + kPieceOverheadTiles;
     total += w.n1 - w.n0;
   }
   const int tail = n_items - head;
+  const bool split = S > 1 && tail > 0;
   std::memset(plan, 0, sizeof(*plan));
   plan->num_sms = num_sms;
   plan->q_tiles = geo.n_qtiles;
   plan->n_items = n_items;
-  plan->head_rounds = head / grid;
+  plan->head_rounds = head / workers;
   plan->tail_items = tail;
   plan->tail_splits = S;
   plan->n_units = sc.n_units;
-  plan->grid = grid;
-  plan->kernels_per_call = (S > 1 && tail > 0) ? 2 : 1;
-  plan->variant = 1;
+  plan->grid = workers * cpi;
+  plan->kernels_per_call = split ? 2 : 1;
+  plan->variant = variant;
   plan->total_tiles = total;
   plan->workspace_bytes =
-      (S > 1 && tail > 0) ? static_cast<int64_t>(tail) * S * kRowsPerTile * kPartialRowBytes : 0;
+      split ? static_cast<int64_t>(tail) * S * cpi * kRowsPerTile * kPartialRowBytes : 0;
   plan->est_makespan_tiles = *std::max_element(load.begin(), load.end());
-  double us = static_cast<double>(plan->est_makespan_tiles) * kTileUs;
-  if (plan->kernels_per_call == 2) {
-    const double bytes = tail * static_cast<double>(kRowsPerTile) * (S * kPartialRowBytes + 520.0);
+  double us = static_cast<double>(plan->est_makespan_tiles) * (variant == 2 ? kPairTileUs : kTileUs);
+  if (split) {
+    const double bytes =
+        tail * static_cast<double>(cpi * kRowsPerTile) * (S * kPartialRowBytes + 520.0);
     us += bytes / kMergeBytesPerUs + kMergeLaunchUs;
   }
   return us;
 }
 
-// Pure function of its arguments. Searches the number of whole rounds and the
-// tail split; a split must win by 2 % over the simpler plan to be taken.
-void compute_plan(int q_len, int kv_len, int num_sms, int force_splits, int force_grid,
-                  gqa_prefill_plan* plan) {
-  const Geometry geo = geometry(q_len, kv_len);
+// Best plan of one variant: searches the number of whole rounds and the tail
+// split; a split must win by 2 % over the simpler plan to be taken.
+double best_plan_of(int q_len, int kv_len, int num_sms, int variant, int workers, int force_splits,
+                    gqa_prefill_plan* plan) {
+  const Geometry geo = geometry(q_len, kv_len, variant);
   const int n_items = geo.n_qtiles * kKvHeads;
-  const int grid = std::max(1, force_grid > 0 ? std::min(force_grid, num_sms) : num_sms);
   const int max_splits = std::max(1, item_tiles(geo, 0));  // the shortest item's tiles
-  const int full_rounds = n_items / grid;
-  if (force_splits > 0) {
-    plan_schedule(geo, num_sms, grid, full_rounds, std::min(force_splits, max_splits), plan);
-    return;
-  }
-  double best = plan_schedule(geo, num_sms, grid, 0, 1, plan);  // whole items only
+  const int full_rounds = n_items / workers;
+  if (force_splits > 0)
+    return plan_schedule(geo, num_sms, variant, workers, full_rounds,
+                         std::min(force_splits, max_splits), plan);
+  double best = plan_schedule(geo, num_sms, variant, workers, 0, 1, plan);  // whole items only
   gqa_prefill_plan cand{};
   for (int hr = full_rounds; hr >= 0; --hr) {
     for (int S : kSplitCandidates) {
       if (S == 1 || S > max_splits) continue;
-      const double us = plan_schedule(geo, num_sms, grid, hr, S, &cand);
+      const double us = plan_schedule(geo, num_sms, variant, workers, hr, S, &cand);
       if (us < 0.98 * best) {
         best = us;
         *plan = cand;
       }
     }
   }
+  return best;
+}
+
+// Pure function of its arguments. max_pairs: CTA pairs that can be resident at
+// once. force_grid caps the CTAs launched (a pair counts as two).
+void compute_plan(int q_len, int kv_len, int num_sms, int max_pairs, int force_splits,
+                  int force_grid, int force_variant, gqa_prefill_plan* plan) {
+  const int cap = force_grid > 0 ? std::min(force_grid, num_sms) : num_sms;
+  const int workers1 = std::max(1, cap);
+  const int workers2 = std::max(1, std::min(max_pairs, cap / 2));
+  if (force_variant == 1 || (force_variant == 0 && max_pairs < 1)) {
+    best_plan_of(q_len, kv_len, num_sms, 1, workers1, force_splits, plan);
+    return;
+  }
+  if (force_variant == 2) {
+    best_plan_of(q_len, kv_len, num_sms, 2, workers2, force_splits, plan);
+    return;
+  }
+  gqa_prefill_plan one{}, pair{};
+  const double t1 = best_plan_of(q_len, kv_len, num_sms, 1, workers1, force_splits, &one);
+  const double t2 = best_plan_of(q_len, kv_len, num_sms, 2, workers2, force_splits, &pair);
+  *plan = t2 < 0.98 * t1 ? pair : one;
 }
 
 struct PlanKey {
-  int q_len, kv_len, num_sms, force_splits, force_grid;
+  int q_len, kv_len, num_sms, max_pairs, force_splits, force_grid, force_variant;
   bool operator<(const PlanKey& o) const {
-    return std::tie(q_len, kv_len, num_sms, force_splits, force_grid) <
-           std::tie(o.q_len, o.kv_len, o.num_sms, o.force_splits, o.force_grid);
+    return std::tie(q_len, kv_len, num_sms, max_pairs, force_splits, force_grid, force_variant) <
+           std::tie(o.q_len, o.kv_len, o.num_sms, o.max_pairs, o.force_splits, o.force_grid,
+                    o.force_variant);
   }
 };
 
-void cached_plan(int q_len, int kv_len, int num_sms, int force_splits, int force_grid,
-                 gqa_prefill_plan* plan) {
+void cached_plan(int q_len, int kv_len, int num_sms, int max_pairs, int force_splits,
+                 int force_grid, int force_variant, gqa_prefill_plan* plan) {
   static std::mutex mu;
   static std::map<PlanKey, gqa_prefill_plan> cache;
-  const PlanKey key{q_len, kv_len, num_sms, force_splits, force_grid};
+  const PlanKey key{q_len, kv_len, num_sms, max_pairs, force_splits, force_grid, force_variant};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -132,7 +164,7 @@ void cached_plan(int q_len, int kv_len, int num_sms, int force_splits, int force
       return;
     }
   }
-  compute_plan(q_len, kv_len, num_sms, force_splits, force_grid, plan);
+  compute_plan(q_len, kv_len, num_sms, max_pairs, force_splits, force_grid, force_variant, plan);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache.emplace(key, *plan);
@@ -151,15 +183,66 @@ gqa_status validate_shape(int q_len, int kv_len, int n_q_heads, int n_kv_heads, 
 bool misaligned(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
 
 // ------------------------------------------------------------ device state --
-struct DeviceState {
+// Per-device facts both entry points need: SM count, co-resident CTA pairs and
+// the status word's device address. Set up once per device with it current; no
+// device memory is allocated here.
+struct DeviceInfo {
   std::once_flag once;
-  cudaError_t init_err = cudaSuccess;
-  bool supported = false;
+  gqa_status status = GQA_OK;
   int num_sms = 0;
-  int* status = nullptr;
+  int max_pairs = 0;
+  int* status_word = nullptr;
+};
+DeviceInfo g_info[kMaxDevices];
+
+gqa_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  DeviceInfo& s = g_info[dev];
+  std::call_once(s.once, [&s, dev] {
+    cudaDeviceProp prop{};
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) { s.status = GQA_ERR_CUDA; return; }
+    // The kernels are built for sm_103a only (tcgen05 / TMEM / TMA).
+    if (!(prop.major == 10 && prop.minor == 3)) { s.status = GQA_ERR_UNSUPPORTED; return; }
+    s.num_sms = prop.multiProcessorCount;
+    if (prepare_fwd_kernel() != cudaSuccess || status_word_address(&s.status_word) != cudaSuccess) {
+      s.status = GQA_ERR_CUDA;
+      return;
+    }
+    int pairs = 0;
+    if (max_active_pairs(&pairs) != cudaSuccess) pairs = 0;  // then the pair kernel is not used
+    s.max_pairs = std::min(pairs, s.num_sms / 2);
+  });
+  if (s.status != GQA_OK) return s.status;
+  *out = &s;
+  return GQA_OK;
+}
+
+// The stream-ordered pool that gqa_prefill_attn takes split partials from.
+struct DevicePool {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
   cudaMemPool_t pool = nullptr;
 };
-DeviceState g_dev[kMaxDevices];
+DevicePool g_pool[kMaxDevices];
+
+gqa_status device_pool(cudaMemPool_t* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  DevicePool& s = g_pool[dev];
+  std::call_once(s.once, [&s, dev] {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if ((s.err = cudaMemPoolCreate(&s.pool, &props)) != cudaSuccess) return;
+    uint64_t keep = UINT64_MAX;  // keep freed partial buffers cached in the pool
+    s.err = cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  });
+  if (s.err != cudaSuccess) return GQA_ERR_CUDA;
+  *out = s.pool;
+  return GQA_OK;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -175,33 +258,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-gqa_status device_state(DeviceState** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
-  DeviceState& s = g_dev[dev];
-  std::call_once(s.once, [&s, dev] {
-    cudaDeviceProp prop{};
-    if ((s.init_err = cudaGetDeviceProperties(&prop, dev)) != cudaSuccess) return;
-    // The kernels are built for sm_103a only (tcgen05 / TMEM / TMA).
-    s.supported = prop.major == 10 && prop.minor == 3;
-    s.num_sms = prop.multiProcessorCount;
-    if (!s.supported) return;
-    if ((s.init_err = prepare_fwd_kernel()) != cudaSuccess) return;
-    if ((s.init_err = status_word_address(&s.status)) != cudaSuccess) return;
-    cudaMemPoolProps props{};
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    if ((s.init_err = cudaMemPoolCreate(&s.pool, &props)) != cudaSuccess) return;
-    uint64_t keep = UINT64_MAX;  // keep freed partial buffers cached in the pool
-    s.init_err = cudaMemPoolSetAttribute(s.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-  });
-  if (s.init_err != cudaSuccess) return GQA_ERR_CUDA;
-  if (!s.supported) return GQA_ERR_UNSUPPORTED;
-  *out = &s;
-  return GQA_OK;
-}
-
 bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                uint32_t b0, uint32_t b1, uint32_t b2) {
   auto fn = encode_fn();
@@ -215,69 +271,87 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-gqa_status run(const void* q, const void* k, const void* v, void* out, float* lse, int q_len,
-               int kv_len, int n_q_heads, int n_kv_heads, int head_dim, float scale, void* stream_ptr,
-               const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out) {
+// Checks every argument; on success fills *plan (q_len == 0 gives an empty plan).
+gqa_status check_call(const void* q, const void* k, const void* v, const void* out,
+                      const float* lse, int q_len, int kv_len, int n_q_heads, int n_kv_heads,
+                      int head_dim, float scale) {
   gqa_status st = validate_shape(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
-  if (st != GQA_OK) return st;
-  if (q_len == 0) {
-    if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
-    return GQA_OK;  // empty chunk: nothing to compute, pointers may be NULL
-  }
+  if (st != GQA_OK || q_len == 0) return st;  // empty chunk: pointers may be NULL
   if (!q || !k || !v || !out) return GQA_ERR_NULL;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(lse))
     return GQA_ERR_ALIGN;
-  DeviceState* dev = nullptr;
-  if ((st = device_state(&dev)) != GQA_OK) return st;
+  return GQA_OK;
+}
 
-  gqa_prefill_plan plan{};
-  cached_plan(q_len, kv_len, dev->num_sms, opts ? opts->force_splits : 0,
-              opts ? opts->force_grid : 0, &plan);
-  if (plan_out) *plan_out = plan;
-
-  auto stream = static_cast<cudaStream_t>(stream_ptr);
+// Launches `plan` on `stream`; `ws` holds plan.workspace_bytes (or nothing).
+gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* k, const void* v,
+                       void* out, float* lse, int q_len, int kv_len, float scale, int* status_word,
+                       void* ws, const gqa_prefill_opts* opts, cudaStream_t stream) {
+  const bool pair = plan.variant == 2;
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   if (!encode_3d(&p.tmap_q, q, kHeadDim, kQHeads, static_cast<uint64_t>(q_len), 64, kGroup,
                  kTokPerTile) ||
-      !encode_3d(&p.tmap_k, k, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1, kBlockN) ||
-      !encode_3d(&p.tmap_v, v, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1, 64))
+      !encode_3d(&p.tmap_k, k, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1,
+                 pair ? 64 : kBlockN) ||
+      !encode_3d(&p.tmap_v, v, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1,
+                 pair ? kBlockN : 64))
     return GQA_ERR_CUDA;
+  const int workers = pair ? plan.grid / 2 : plan.grid;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  p.status = dev->status;
+  p.status = status_word;
   p.q_len = q_len;
   p.kv_len = kv_len;
   p.p0 = kv_len - q_len;
   p.n_qtiles = plan.q_tiles;
-  p.head_items = plan.head_rounds * plan.grid < plan.n_items ? plan.head_rounds * plan.grid
-                                                             : plan.n_items;
+  p.head_items = std::min(plan.head_rounds * workers, plan.n_items);
   p.tail_splits = plan.tail_splits;
   p.n_units = plan.n_units;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.timeout_ns = (opts && opts->wait_timeout_us) ? 1000ull * opts->wait_timeout_us
                                                  : kDefaultTimeoutNs;
   p.withhold_q = (opts && opts->test_withhold_q) ? 1 : 0;
-
-  void* ws = nullptr;
-  const size_t n_slots = static_cast<size_t>(plan.tail_items) * plan.tail_splits;
   if (plan.kernels_per_call == 2) {
-    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(plan.workspace_bytes), dev->pool, stream) !=
-        cudaSuccess)
-      return GQA_ERR_CUDA;
     p.part_o = static_cast<float*>(ws);
-    p.part_lse = p.part_o + n_slots * kRowsPerTile * kHeadDim;
+    p.part_lse = p.part_o + static_cast<size_t>(plan.tail_items) * plan.tail_splits *
+                                (pair ? 2 : 1) * kRowsPerTile * kHeadDim;
   }
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
-  if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) st = GQA_ERR_CUDA;
-  if (st == GQA_OK && launch_fwd(p, plan.grid, stream) != cudaSuccess) st = GQA_ERR_CUDA;
-  if (st == GQA_OK && ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) st = GQA_ERR_CUDA;
-  if (st == GQA_OK && plan.kernels_per_call == 2) {
+  if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return GQA_ERR_CUDA;
+  if (launch_fwd(p, plan.grid, pair, stream) != cudaSuccess) return GQA_ERR_CUDA;
+  if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return GQA_ERR_CUDA;
+  if (plan.kernels_per_call == 2) {
     MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.n_qtiles, p.head_items,
-                  plan.tail_items, plan.tail_splits};
-    if (launch_merge(m, stream) != cudaSuccess) st = GQA_ERR_CUDA;
+                  plan.tail_items, plan.tail_splits, pair ? 2 : 1};
+    if (launch_merge(m, stream) != cudaSuccess) return GQA_ERR_CUDA;
   }
+  return GQA_OK;
+}
+
+gqa_status run(const void* q, const void* k, const void* v, void* out, float* lse, int q_len,
+               int kv_len, int n_q_heads, int n_kv_heads, int head_dim, float scale, void* stream_ptr,
+               const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out) {
+  if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
+  gqa_status st = check_call(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
+  if (st != GQA_OK || q_len == 0) return st;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != GQA_OK) return st;
+  gqa_prefill_plan plan{};
+  cached_plan(q_len, kv_len, dev->num_sms, dev->max_pairs, opts ? opts->force_splits : 0,
+              opts ? opts->force_grid : 0, opts ? opts->force_variant : 0, &plan);
+  if (plan_out) *plan_out = plan;
+  auto stream = static_cast<cudaStream_t>(stream_ptr);
+  void* ws = nullptr;
+  if (plan.workspace_bytes > 0) {
+    cudaMemPool_t pool = nullptr;
+    if ((st = device_pool(&pool)) != GQA_OK) return st;
+    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(plan.workspace_bytes), pool, stream) !=
+        cudaSuccess)
+      return GQA_ERR_CUDA;
+  }
+  st = launch_plan(plan, q, k, v, out, lse, q_len, kv_len, scale, dev->status_word, ws, opts, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   return st;
 }
@@ -293,82 +367,39 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 struct NoAllocDeviceState {
   std::once_flag once;
   gqa_status status = GQA_OK;
-  int num_sms = 0;
-  int* status_word = nullptr;
   void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
 };
 NoAllocDeviceState g_noalloc_dev[kMaxDevices];
 
-gqa_status noalloc_device_state(NoAllocDeviceState** out) {
+gqa_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
   NoAllocDeviceState& s = g_noalloc_dev[dev];
-  std::call_once(s.once, [&s, dev] {
-    cudaDeviceProp prop{};
-    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) { s.status = GQA_ERR_CUDA; return; }
-    if (!(prop.major == 10 && prop.minor == 3)) { s.status = GQA_ERR_UNSUPPORTED; return; }
-    s.num_sms = prop.multiProcessorCount;
-    if (prepare_fwd_kernel() != cudaSuccess || status_word_address(&s.status_word) != cudaSuccess ||
-        cudaGetSymbolAddress(&s.scratch, g_noalloc_scratch) != cudaSuccess || s.scratch == nullptr) {
+  std::call_once(s.once, [&s] {
+    if (cudaGetSymbolAddress(&s.scratch, g_noalloc_scratch) != cudaSuccess || s.scratch == nullptr)
       s.status = GQA_ERR_CUDA;
-      return;
-    }
   });
   if (s.status != GQA_OK) return s.status;
-  *out = &s;
+  *out = s.scratch;
   return GQA_OK;
 }
 
 gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
                        int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, void* stream_ptr) {
-  gqa_status st = validate_shape(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
-  if (st != GQA_OK) return st;
-  if (q_len == 0) return GQA_OK;
-  if (!q || !k || !v || !out) return GQA_ERR_NULL;
-  if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(lse))
-    return GQA_ERR_ALIGN;
-  NoAllocDeviceState* dev = nullptr;
-  if ((st = noalloc_device_state(&dev)) != GQA_OK) return st;
+  gqa_status st = check_call(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
+  if (st != GQA_OK || q_len == 0) return st;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != GQA_OK) return st;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != GQA_OK) return st;
   gqa_prefill_plan plan{};
-  cached_plan(q_len, kv_len, dev->num_sms, 0, 0, &plan);
+  cached_plan(q_len, kv_len, dev->num_sms, dev->max_pairs, 0, 0, 0, &plan);
   if (static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes) return GQA_ERR_SCRATCH;
-
-  auto stream = static_cast<cudaStream_t>(stream_ptr);
-  FwdParams p;
-  std::memset(&p, 0, sizeof(p));
-  if (!encode_3d(&p.tmap_q, q, kHeadDim, kQHeads, static_cast<uint64_t>(q_len), 64, kGroup,
-                 kTokPerTile) ||
-      !encode_3d(&p.tmap_k, k, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1, kBlockN) ||
-      !encode_3d(&p.tmap_v, v, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1, 64))
-    return GQA_ERR_CUDA;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.lse = lse;
-  p.status = dev->status_word;
-  p.q_len = q_len;
-  p.kv_len = kv_len;
-  p.p0 = kv_len - q_len;
-  p.n_qtiles = plan.q_tiles;
-  p.head_items = plan.head_rounds * plan.grid < plan.n_items ? plan.head_rounds * plan.grid
-                                                             : plan.n_items;
-  p.tail_splits = plan.tail_splits;
-  p.n_units = plan.n_units;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.timeout_ns = kDefaultTimeoutNs;
-  if (plan.kernels_per_call == 2) {
-    // Every partial row the merge reads is written by the attention kernel first,
-    // so the scratch needs no clearing between calls.
-    p.part_o = static_cast<float*>(dev->scratch);
-    p.part_lse = p.part_o + static_cast<size_t>(plan.tail_items) * plan.tail_splits *
-                                kRowsPerTile * kHeadDim;
-  }
-  if (launch_fwd(p, plan.grid, stream) != cudaSuccess) return GQA_ERR_CUDA;
-  if (plan.kernels_per_call == 2) {
-    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.n_qtiles, p.head_items,
-                  plan.tail_items, plan.tail_splits};
-    if (launch_merge(m, stream) != cudaSuccess) return GQA_ERR_CUDA;
-  }
-  return GQA_OK;
+  // Every partial row the merge reads is written by the attention kernel first,
+  // so the scratch needs no clearing between calls.
+  return launch_plan(plan, q, k, v, out, lse, q_len, kv_len, scale, dev->status_word, scratch,
+                     nullptr, static_cast<cudaStream_t>(stream_ptr));
 }
 
 }  // namespace
@@ -400,7 +431,7 @@ gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void
 }
 
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int num_sms, int force_splits, int force_grid,
+                                 int num_sms, int force_splits, int force_grid, int force_variant,
                                  gqa_prefill_plan* plan) {
   if (!plan) return GQA_ERR_NULL;
   const gqa_status st =
@@ -409,22 +440,23 @@ gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_
   if (num_sms <= 0) return GQA_ERR_SHAPE;
   std::memset(plan, 0, sizeof(*plan));
   if (q_len == 0) return GQA_OK;
-  gqa::cached_plan(q_len, kv_len, num_sms, force_splits, force_grid, plan);
+  gqa::cached_plan(q_len, kv_len, num_sms, num_sms / 2, force_splits, force_grid, force_variant,
+                   plan);
   return GQA_OK;
 }
 
 gqa_status gqa_prefill_poll(void* stream, int* device_status) {
   if (!device_status) return GQA_ERR_NULL;
-  gqa::DeviceState* dev = nullptr;
-  const gqa_status st = gqa::device_state(&dev);
+  gqa::DeviceInfo* dev = nullptr;
+  const gqa_status st = gqa::device_info(&dev);
   if (st != GQA_OK) return st;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
   int value = 0;
-  if (cudaMemcpy(&value, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(&value, dev->status_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return GQA_ERR_CUDA;
   if (value != 0) {
     const int zero = 0;
-    if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    if (cudaMemcpy(dev->status_word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return GQA_ERR_CUDA;
   }
   *device_status = value;

@@ -1,8 +1,9 @@
 // Work decomposition of one call, shared by the host planner, the attention
 // kernel and the merge kernel (all three must agree unit for unit).
 //
-// An *item* is one 21-token query tile of one KV group: 126 packed MMA rows
-// that sweep KV tiles 0 .. nt-1 (128 keys each) up to the causal diagonal.
+// An *item* is one query tile of one KV group that sweeps KV tiles 0 .. nt-1
+// (128 keys each) up to the causal diagonal: 21 tokens (126 packed MMA rows)
+// for the one-CTA kernel, 42 tokens for the CTA-pair kernel (21 per CTA).
 // Items are ordered longest first — item i covers query tile
 // qt = n_qtiles - 1 - i/4 and KV group g = i%4 — so consecutive items have
 // (nearly) the same length.
@@ -27,14 +28,16 @@
 namespace gqa {
 
 struct Geometry {
-  int q_len;     // tokens in the chunk
-  int p0;        // kv_len - q_len: position of the chunk's first token
-  int n_qtiles;  // ceil(q_len / 21)
+  int q_len;         // tokens in the chunk
+  int p0;            // kv_len - q_len: position of the chunk's first token
+  int n_qtiles;      // ceil(q_len / tok_per_item)
+  int tok_per_item;  // 21 (one CTA per item) or 42 (a CTA pair per item)
 };
 
 // KV tiles an item of query tile qt visits: keys 0 .. p0 + last token of the tile.
 __host__ __device__ inline int item_tiles(const Geometry& geo, int qt) {
-  const int tok_end = (qt + 1) * 21 < geo.q_len ? (qt + 1) * 21 : geo.q_len;
+  const int end = (qt + 1) * geo.tok_per_item;
+  const int tok_end = end < geo.q_len ? end : geo.q_len;
   return (geo.p0 + tok_end + 127) / 128;
 }
 

@@ -91,7 +91,9 @@ typedef struct gqa_prefill_opts {
                                  GQA_ERR_DEVICE_TIMEOUT, drains its copies, frees
                                  tensor memory and returns (outputs undefined).
                                  Exercises the time-out path without faulting.     */
-  int reserved[2];
+  int force_variant;          /* 0: planner decides; 1: one CTA per 21-token item;
+                                 2: a CTA pair per 42-token item (cta_group::2 MMAs) */
+  int reserved[1];
 } gqa_prefill_opts;
 
 /*
@@ -105,7 +107,7 @@ typedef struct gqa_prefill_opts {
  */
 typedef struct gqa_prefill_plan {
   int num_sms;                /* SMs of the device                                    */
-  int q_tiles;                /* ceil(q_len / 21)                                     */
+  int q_tiles;                /* ceil(q_len / tokens per item)                        */
   int n_items;                /* q_tiles * n_kv_heads                                 */
   int head_rounds;            /* full rounds of whole items                           */
   int tail_items;             /* items after those rounds                             */
@@ -113,7 +115,9 @@ typedef struct gqa_prefill_plan {
   int n_units;                /* units dealt: head items + tail_items * tail_splits   */
   int grid;                   /* CTAs launched for the attention kernel               */
   int kernels_per_call;       /* launches per call: 1, or 2 with the merge kernel     */
-  int variant;                /* 1 = tcgen05 1-CTA M=128 kernel                       */
+  int variant;                /* 1 = one CTA per item (M = 128 MMAs, 21 tokens);
+                                 2 = a CTA pair per item (cta_group::2, M = 256, 42
+                                 tokens: each CTA streams half of every K/V tile)  */
   int64_t total_tiles;        /* KV tiles summed over all items                       */
   int64_t workspace_bytes;    /* temporary FP32 partials of the split items (or 0)    */
   int64_t est_makespan_tiles; /* planner's cost of the busiest CTA, in KV tiles       */
@@ -127,13 +131,13 @@ gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void
 
 /*
  * Host-only planning (no CUDA call): fills *plan for a device with `num_sms`
- * SMs exactly as gqa_prefill_attn_ex would with the same force_splits and
- * force_grid options (0 = planner decides). Validates shapes like the
- * attention call (pointers are not involved).
+ * SMs exactly as gqa_prefill_attn_ex would with the same force_* options
+ * (0 = planner decides), assuming num_sms/2 CTA pairs can be resident.
+ * Validates shapes like the attention call (pointers are not involved).
  */
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                                  int num_sms, int force_splits, int force_grid,
-                                 gqa_prefill_plan* plan);
+                                 int force_variant, gqa_prefill_plan* plan);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
@@ -161,7 +165,8 @@ gqa_status gqa_prefill_poll(void* stream, int* device_status);
  * The scratch array is GQA_NOALLOC_SCRATCH_BYTES (64 MiB) of device memory,
  * held on every GPU that loads the library until the process exits. The call
  * plans exactly like gqa_prefill_attn; when that plan's partials
- * (tail_items * tail_splits * 128 * 257 * 4 bytes when items are split, else 0)
+ * (tail_items * tail_splits * CTAs-per-item * 128 * 257 * 4 bytes when items are
+ * split, else 0)
  * exceed the array, it returns GQA_ERR_SCRATCH and launches nothing.
  *
  * It calls no cudaMalloc, cudaFree or other allocating routine. Its first call

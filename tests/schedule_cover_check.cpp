@@ -22,9 +22,10 @@ int main() {
   const int extras[] = {0, 1, 100, 127, 128, 129, 255, 1000, 4096, 28672};
   const int grids[] = {1, 2, 3, 7, 64, 152, 1000};
   const int splits[] = {1, 2, 3, 4, 7, 16};
+  for (int tpi : {21, 42})
   for (int ql : qls)
     for (int ex : extras) {
-      const Geometry geo{ql, ex, (ql + 20) / 21};
+      const Geometry geo{ql, ex, (ql + tpi - 1) / tpi, tpi};
       const int n_items = 4 * geo.n_qtiles;
       std::vector<int> nts;
       for (int i = 0; i < n_items; ++i) nts.push_back(item_tiles(geo, geo.n_qtiles - 1 - i / 4));

@@ -62,50 +62,66 @@ SHAPES = [(1, 1), (21, 21), (22, 5000), (128, 256), (512, 4096), (4096, 8192), (
           (3072, 16384), (4096, 32768), (512, 32768)]
 
 
-def _total_tiles(q_len, kv_len):
-    p0, nq = kv_len - q_len, -(-q_len // 21)
-    return sum(4 * (-(-(p0 + min(21 * (qt + 1), q_len)) // 128)) for qt in range(nq))
+def _total_tiles(q_len, kv_len, tpi=21):
+    p0, nq = kv_len - q_len, -(-q_len // tpi)
+    return sum(4 * (-(-(p0 + min(tpi * (qt + 1), q_len)) // 128)) for qt in range(nq))
 
 
 @pytest.mark.parametrize("q_len,kv_len", SHAPES)
 @pytest.mark.parametrize("sms", [148, 152])
 @pytest.mark.parametrize("force", [0, 1, 3])
-def test_planner_invariants(gqa, q_len, kv_len, sms, force):
-    _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_splits=force)
-    q_tiles = -(-q_len // 21)
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_planner_invariants(gqa, q_len, kv_len, sms, force, variant):
+    _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_splits=force,
+                                     force_variant=variant)
+    assert p["variant"] in (1, 2) and (variant == 0 or p["variant"] == variant)
+    cpi = p["variant"]  # CTAs per item
+    tpi = 21 * cpi
+    q_tiles = -(-q_len // tpi)
     n = 4 * q_tiles
-    W = _total_tiles(q_len, kv_len)
+    W = _total_tiles(q_len, kv_len, tpi)
     assert p["q_tiles"] == q_tiles and p["n_items"] == n and p["total_tiles"] == W
-    shortest = -(-(kv_len - q_len + min(21, q_len)) // 128)
+    shortest = -(-(kv_len - q_len + min(tpi, q_len)) // 128)
     assert 1 <= p["tail_splits"] <= max(shortest, 1)
     if force:
         assert p["tail_splits"] == min(force, shortest)
-    head = min(p["head_rounds"] * p["grid"], n)
+    assert p["grid"] % cpi == 0
+    workers = p["grid"] // cpi
+    head = min(p["head_rounds"] * workers, n)
     assert p["tail_items"] == n - head
     assert p["n_units"] == head + p["tail_items"] * p["tail_splits"]
-    assert 1 <= p["grid"] <= min(sms, p["n_units"])
+    assert 1 <= workers <= min(sms // cpi, p["n_units"])
     split = p["tail_splits"] > 1 and p["tail_items"] > 0
     assert p["kernels_per_call"] == (2 if split else 1)
-    assert p["workspace_bytes"] == (p["tail_items"] * p["tail_splits"] * 128 * 257 * 4 if split else 0)
-    assert p["est_makespan_tiles"] * p["grid"] >= W  # the busiest CTA carries at least the mean
-    _, again = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_splits=force)
+    assert p["workspace_bytes"] == (
+        p["tail_items"] * p["tail_splits"] * cpi * 128 * 257 * 4 if split else 0)
+    assert p["est_makespan_tiles"] * workers >= W  # the busiest worker carries at least the mean
+    _, again = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_splits=force,
+                                         force_variant=variant)
     assert again == p
 
 
 def test_split_tail_balances_long_chunks(gqa):
     """On the long workloads splitting the last round beats whole items."""
     for q_len, kv_len in ((4096, 16384), (4096, 32768)):
-        _, whole = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, force_splits=1)
-        _, auto = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152)
-        assert auto["tail_splits"] > 1 and auto["head_rounds"] >= 1
-        assert auto["est_makespan_tiles"] < 0.93 * whole["est_makespan_tiles"]
+        for v in (1, 2):
+            _, whole = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, force_splits=1,
+                                                 force_variant=v)
+            _, auto = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, force_variant=v)
+            assert auto["tail_splits"] > 1 and auto["head_rounds"] >= 1
+            assert auto["est_makespan_tiles"] < 0.95 * whole["est_makespan_tiles"]
 
 
 def test_force_grid_caps_the_grid(gqa):
-    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_splits=3, force_grid=5)
+    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_splits=3, force_grid=5,
+                                     force_variant=1)
     assert p["grid"] == 5 and p["head_rounds"] == 5 and p["tail_items"] == 3
-    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_splits=1, force_grid=5)
+    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_splits=1, force_grid=5,
+                                     force_variant=1)
     assert p["grid"] == 5 and p["kernels_per_call"] == 1
+    _, p = gqa.gqa_prefill_make_plan(129, 1000, 24, 4, 256, 152, force_splits=2, force_grid=6,
+                                     force_variant=2)
+    assert p["grid"] == 6 and p["variant"] == 2 and p["q_tiles"] == 4  # 3 pairs, 42-token items
 
 
 def test_make_plan_validates(gqa):

@@ -16,35 +16,39 @@ SCALE = 1.0 / 16.0
 
 
 @pytest.mark.parametrize("name", ["q512_kv4096_kbias", "q4096_kv8192", "q512_kv32768"])
-def test_run_twice_bit_identical(cuda_device, name):
+@pytest.mark.parametrize("variant", [1, 2])
+def test_run_twice_bit_identical(cuda_device, name, variant):
     q, k, v = make_workload(WORKLOADS[name])
-    o1, l1, _ = run_gpu(q, k, v, SCALE)
-    o2, l2, _ = run_gpu(q, k, v, SCALE)
+    o1, l1, _ = run_gpu(q, k, v, SCALE, force_variant=variant)
+    o2, l2, _ = run_gpu(q, k, v, SCALE, force_variant=variant)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 @pytest.mark.parametrize("q_len,kv_len,t_star", [(100, 700, 40), (300, 300, 150), (512, 4096, 200)])
-@pytest.mark.parametrize("splits,grid", [(0, 0), (3, 9)])
+@pytest.mark.parametrize("splits,grid,variant", [(0, 0, 1), (3, 9, 1), (0, 0, 2), (3, 10, 2)])
 def test_future_keys_leave_earlier_rows_bit_identical(cuda_device, q_len, kv_len, t_star, splits,
-                                                      grid):
+                                                      grid, variant):
     q, k, v = make_qkv(q_len, kv_len, seed=q_len + kv_len)
-    o1, l1, _ = run_gpu(q, k, v, SCALE, force_splits=splits, force_grid=grid)
+    o1, l1, _ = run_gpu(q, k, v, SCALE, force_splits=splits, force_grid=grid,
+                        force_variant=variant)
     p_star = kv_len - q_len + t_star
     k2, v2 = k.clone(), v.clone()
     k2[p_star + 1:] = (k2[p_star + 1:].float() * 3.0 + 1.0).to(torch.bfloat16)
     v2[p_star + 1:] = (-v2[p_star + 1:].float() + 2.0).to(torch.bfloat16)
-    o2, l2, _ = run_gpu(q, k2, v2, SCALE, force_splits=splits, force_grid=grid)
+    o2, l2, _ = run_gpu(q, k2, v2, SCALE, force_splits=splits, force_grid=grid,
+                        force_variant=variant)
     assert torch.equal(o1[: t_star + 1], o2[: t_star + 1])
     assert torch.equal(l1[: t_star + 1], l2[: t_star + 1])
     assert not torch.equal(o1[t_star + 1:], o2[t_star + 1:])
 
 
 @pytest.mark.parametrize("name", ["q512_kv4096_kbias", "q4096_kv8192"])
-def test_whole_and_cut_items_agree(cuda_device, name):
+@pytest.mark.parametrize("variant", [1, 2])
+def test_whole_and_cut_items_agree(cuda_device, name, variant):
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
-    o1, l1, p1 = run_gpu(q, k, v, SCALE, force_splits=1)
-    o2, l2, p2 = run_gpu(q, k, v, SCALE, force_splits=4)
+    o1, l1, p1 = run_gpu(q, k, v, SCALE, force_splits=1, force_variant=variant)
+    o2, l2, p2 = run_gpu(q, k, v, SCALE, force_splits=4, force_variant=variant)
     assert p1["tail_splits"] == 1 and p1["kernels_per_call"] == 1
     assert p2["tail_splits"] == 4 and p2["tail_items"] > 0 and p2["kernels_per_call"] == 2
     check_close(o2.double().cpu().numpy(), l2.double().cpu().numpy(),
@@ -57,8 +61,8 @@ def test_route_check_reports_planned_kernel(cuda_device):
     _, _, plan = run_gpu(q, k, v, SCALE)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     _, host_plan = gqa.gqa_prefill_make_plan(4096, 8192, 24, 4, 256, sms)
-    assert plan == host_plan
-    assert plan["variant"] == 1 and plan["num_sms"] == sms and plan["grid"] <= sms
+    assert plan == host_plan  # holds when every SM pair can be resident (true on this part)
+    assert plan["variant"] in (1, 2) and plan["num_sms"] == sms and plan["grid"] <= sms
 
 
 def test_empty_chunk_is_a_no_op(cuda_device):

@@ -35,23 +35,27 @@ CASES = sorted({(ql, _kv(ql, s)) for ql in Q_LENS for s in KV_EXTRA if _kv(ql, s
 
 
 @pytest.mark.parametrize("q_len,kv_len", CASES)
-def test_small_shapes_every_element(cuda_device, q_len, kv_len):
+@pytest.mark.parametrize("variant", [1, 2])
+def test_small_shapes_every_element(cuda_device, q_len, kv_len, variant):
     q, k, v = make_qkv(q_len, kv_len, seed=7 * q_len + kv_len)
-    out, lse, plan = run_gpu(q, k, v, SCALE)
-    assert plan["variant"] == 1 and plan["q_tiles"] == -(-q_len // 21)
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_variant=variant)
+    assert plan["variant"] == variant and plan["q_tiles"] == -(-q_len // (21 * variant))
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
                 f"{q_len}x{kv_len}")
 
 
 @pytest.mark.parametrize("q_len,kv_len", [(22, 1000), (129, 1000), (43, 257), (7, 700), (300, 300)])
-@pytest.mark.parametrize("splits,grid", [(2, 0), (3, 0), (7, 0), (3, 5), (2, 11), (4, 1)])
-def test_split_tail_every_element(cuda_device, q_len, kv_len, splits, grid):
+@pytest.mark.parametrize("splits,grid,variant", [(2, 0, 1), (3, 0, 1), (7, 0, 1), (3, 5, 1),
+                                                 (2, 11, 1), (4, 1, 1), (2, 0, 2), (3, 0, 2),
+                                                 (3, 6, 2), (2, 10, 2), (5, 2, 2)])
+def test_split_tail_every_element(cuda_device, q_len, kv_len, splits, grid, variant):
     """Items split into KV pieces and merged: all items (grid >= items) or only the
-    items after whole rounds on a few CTAs (small grid)."""
+    items after whole rounds on a few CTAs (small grid); one CTA or a CTA pair per item."""
     q, k, v = make_qkv(q_len, kv_len, seed=11 * q_len + kv_len)
-    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_grid=grid)
-    assert plan["grid"] <= (grid or plan["num_sms"])
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_grid=grid,
+                             force_variant=variant)
+    assert plan["grid"] <= (grid or plan["num_sms"]) and plan["variant"] == variant
     assert plan["kernels_per_call"] == (2 if plan["tail_splits"] > 1 and plan["tail_items"] else 1)
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
@@ -59,11 +63,12 @@ def test_split_tail_every_element(cuda_device, q_len, kv_len, splits, grid):
 
 
 @pytest.mark.parametrize("q_len,kv_len", [(129, 1000), (300, 300)])
-@pytest.mark.parametrize("grid", [1, 5])
-def test_whole_items_on_few_ctas(cuda_device, q_len, kv_len, grid):
-    """No split, more items than CTAs: each CTA walks many whole items in turn."""
+@pytest.mark.parametrize("grid,variant", [(1, 1), (5, 1), (2, 2), (6, 2)])
+def test_whole_items_on_few_ctas(cuda_device, q_len, kv_len, grid, variant):
+    """No split, more items than CTAs: each CTA (pair) walks many whole items in turn."""
     q, k, v = make_qkv(q_len, kv_len, seed=13 * q_len + kv_len)
-    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=1, force_grid=grid)
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=1, force_grid=grid,
+                             force_variant=variant)
     assert plan["tail_splits"] == 1 and plan["kernels_per_call"] == 1 and plan["grid"] == grid
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
@@ -71,10 +76,11 @@ def test_whole_items_on_few_ctas(cuda_device, q_len, kv_len, grid):
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
-def test_workload_full_size_sampled_rows(cuda_device, name):
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_workload_full_size_sampled_rows(cuda_device, name, variant):
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
-    out, lse, plan = run_gpu(q, k, v, w.scale)
+    out, lse, plan = run_gpu(q, k, v, w.scale, force_variant=variant)
     rows = sample_rows(w.q_len, w.n_q_heads, 1200 if w.q_len * w.kv_len > 4e6 else 4000, seed=5)
     ref_o, ref_l = oracle.attention(q, k, v, w.scale, rows=rows)
     got_o, got_l = gather_rows(out, lse, rows)
