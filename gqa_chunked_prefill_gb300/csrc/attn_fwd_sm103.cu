@@ -100,19 +100,12 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 __device__ int g_status_word = 0;
 
-// Bounded wait for the phase of `bar` with the given parity. In CTA pairs the
-// arrivals come from the other CTA too, so the wait acquires at cluster scope.
-template <bool kCluster>
-__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity) {
-  return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
-}
-
-template <bool kCluster = false>
+// Bounded wait for the phase of `bar` with the given parity.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const FwdParams& p) {
-  if (try_wait<kCluster>(bar, parity)) return true;
+  if (ptx::mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t spin = 1;; ++spin) {
-    if (try_wait<kCluster>(bar, parity)) return true;
+    if (ptx::mbar_try_wait(bar, parity)) return true;
     if ((spin & 31u) == 0 && ptx::globaltimer_ns() - t0 > p.timeout_ns) {
       atomicExch(p.status, static_cast<int>(GQA_ERR_DEVICE_TIMEOUT));
       return false;
@@ -226,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // CTA's 128 columns).
       auto next_tile = [&](int n, bool is_k, int g) -> bool {
         for (int half = 0; half < (kPair ? 1 : 2); ++half) {
-          if (!wait_bar<kPair>(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
+          if (!wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
           const uint32_t dst = stage_smem + st * kStageBytes;
           if (leader) ptx::mbar_arrive_expect_tx(bar(kBarFull + st), (kPair ? 2 : 1) * kStageBytes);
           if constexpr (kPair) {
@@ -259,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k = 0;
       Piece w;
       while (ok && pieces.next(w)) {
-        if (k > 0 && !(ok = wait_bar<kPair>(bar(kBarQEmpty), (k - 1) & 1, p))) break;
+        if (k > 0 && !(ok = wait_bar(bar(kBarQEmpty), (k - 1) & 1, p))) break;
         if (!(p.withhold_q && k == 0)) {
           if (leader) ptx::mbar_arrive_expect_tx(bar(kBarQFull), (kPair ? 2 : 1) * 4 * kQBoxBytes);
           for (int c = 0; c < 4; ++c)
@@ -283,8 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // copies complete on the leader's barriers, so the leader drains for both.
       if (leader) {
         for (int s = 0; s < kStages; ++s)
-          if (issued_mask & (1u << s)) wait_bar<kPair>(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
-        if (q_issued) wait_bar<kPair>(bar(kBarQFull), q_parity, p);
+          if (issued_mask & (1u << s)) wait_bar(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
+        if (q_issued) wait_bar(bar(kBarQFull), q_parity, p);
       }
     }
     __syncwarp();
@@ -304,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Piece w;
       while (ok && pieces.next(w)) {
         const int nt = w.n1 - w.n0;
-        if (!(ok = wait_bar<kPair>(bar(kBarQFull), k & 1, p))) break;
+        if (!(ok = wait_bar(bar(kBarQFull), k & 1, p))) break;
         ptx::tc_fence_after();
         // S = Q K_j^T over d = 256 in k-steps of 16. Descriptors are built once;
         // an offset below 256 KB only touches the 14-bit start-address field, so
@@ -312,11 +305,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto issue_qk = [&](int j) -> bool {
           const uint32_t T = tile + j;
           // S may be overwritten once the softmax holds tile T-1's scores in registers.
-          if (T > 0 && !wait_bar<kPair>(bar(kBarSFree), (T - 1) & 1u, p)) return false;
+          if (T > 0 && !wait_bar(bar(kBarSFree), (T - 1) & 1u, p)) return false;
           ptx::tc_fence_after();
           if constexpr (kPair) {
             // One stage: this CTA's 64 keys as 4 boxes (64-wide d chunks, 8 KB apart).
-            if (!wait_bar<kPair>(bar(kBarFull + st), phase, p)) return false;
+            if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
             ptx::tc_fence_after();
             const uint64_t kd = k_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
@@ -333,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-              if (!wait_bar<kPair>(bar(kBarFull + st), phase, p)) return false;
+              if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
               ptx::tc_fence_after();
               const uint64_t kd = k_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
@@ -358,14 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j + 1 < nt && !(ok = issue_qk(j + 1))) break;
           const uint32_t T = tile + j;
           const uint32_t b = T & 1u;
-          if (!(ok = wait_bar<kPair>(bar(b ? kBarPFull1 : kBarPFull0), (T >> 1) & 1u, p))) break;
-          if (j == 0 && k > 0 && !(ok = wait_bar<kPair>(bar(kBarOFree), (k - 1) & 1, p))) break;
+          if (!(ok = wait_bar(bar(b ? kBarPFull1 : kBarPFull0), (T >> 1) & 1u, p))) break;
+          if (j == 0 && k > 0 && !(ok = wait_bar(bar(kBarOFree), (k - 1) & 1, p))) break;
           ptx::tc_fence_after();
           // O += P_j V_j in k-steps of 16 keys, N = 256. V stages are MN-major:
           // LBO = next 64-wide d chunk, SBO = next group of 8 keys.
           if constexpr (kPair) {
             // One stage: 128 keys x this CTA's 128 columns (2 boxes, 16 KB apart).
-            if (!(ok = wait_bar<kPair>(bar(kBarFull + st), phase, p))) break;
+            if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
             ptx::tc_fence_after();
             const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
@@ -379,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             // Two stages (key halves) of 4 boxes (64-wide d chunks, 8 KB apart).
             for (int half = 0; half < 2 && ok; ++half) {
-              if (!(ok = wait_bar<kPair>(bar(kBarFull + st), phase, p))) break;
+              if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
               ptx::tc_fence_after();
               const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
@@ -400,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Drain: every MMA issued above has completed once this barrier fires.
       commit(kBarDrain);
-      wait_bar<kPair>(bar(kBarDrain), 0, p);
+      wait_bar(bar(kBarDrain), 0, p);
     }
     __syncwarp();
   } else {
@@ -426,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nt; ++j) {
         const uint32_t T = tile + j;
         const uint32_t b = T & 1u;
-        ok = __all_sync(0xffffffffu, wait_bar<kPair>(bar(kBarSFull), T & 1u, p));
+        ok = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull), T & 1u, p));
         if (!ok) break;
         ptx::tc_fence_after();
         uint32_t sr[128];
@@ -461,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (need) m_ref = m_new;
           l *= alpha;
           // O must hold PV_{j-1} (which read P[(T-1)&1], use (T-1)>>1) before it is rescaled.
-          ok = __all_sync(0xffffffffu, wait_bar<kPair>(bar((T - 1) & 1u ? kBarPvDone1 : kBarPvDone0),
+          ok = __all_sync(0xffffffffu, wait_bar(bar((T - 1) & 1u ? kBarPvDone1 : kBarPvDone0),
                                                 ((T - 1) >> 1) & 1u, p));
           if (!ok) break;
           ptx::tc_fence_after();
@@ -495,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += sum0 + sum1;
         if (T >= 2) {
           // P[b] was last read by PV_{T-2}: it must have completed before P[b] is rewritten.
-          ok = __all_sync(0xffffffffu, wait_bar<kPair>(bar(b ? kBarPvDone1 : kBarPvDone0),
+          ok = __all_sync(0xffffffffu, wait_bar(bar(b ? kBarPvDone1 : kBarPvDone0),
                                                 ((T - 2) >> 1) & 1u, p));
           if (!ok) break;
           ptx::tc_fence_after();
@@ -508,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       // ---- epilogue: O / l -> out (or the split partial), LSE ----------------
       const uint32_t T_last = tile + nt - 1;
-      ok = __all_sync(0xffffffffu, wait_bar<kPair>(bar(T_last & 1u ? kBarPvDone1 : kBarPvDone0),
+      ok = __all_sync(0xffffffffu, wait_bar(bar(T_last & 1u ? kBarPvDone1 : kBarPvDone0),
                                             (T_last >> 1) & 1u, p));
       if (!ok) break;
       ptx::tc_fence_after();
@@ -576,19 +569,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Combine the S pieces of every split (tail) item: block j merges item
-// head_items + j from slots j*S .. j*S + S-1 (each slot holds one 128-row block
-// per CTA of the item), in that fixed order:
+// Combine the S pieces of every split (tail) item: blocks (j, *) merge item
+// head_items + j, 32 rows each, from slots j*S .. j*S + S-1 (each slot holds one
+// 128-row block per CTA of the item), in that fixed order:
 // lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s. One warp per row.
+constexpr int kMergeRowsPerBlock = 32;  // 8 warps x 4 rows
+
 __global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
-  const int j = blockIdx.x;
+  const int j = blockIdx.x;                           // tail item
+  const int row_begin = blockIdx.y * kMergeRowsPerBlock;  // its rows, both CTAs of a pair
   const int item = p.head_items + j;
   const int qt = p.n_qtiles - 1 - item / 4;
   const int g = item % 4;
   const int S = p.tail_splits;
   const int cpi = p.ctas_per_item;
   const int lane = threadIdx.x & 31;
-  for (int rr = threadIdx.x >> 5; rr < cpi * kTokPerTile * kGroup; rr += 8) {
+  const int row_end = min(row_begin + kMergeRowsPerBlock, cpi * kTokPerTile * kGroup);
+  for (int rr = row_begin + (threadIdx.x >> 5); rr < row_end; rr += 8) {
     const int r = rr / (kTokPerTile * kGroup);    // CTA of the item
     const int row = rr % (kTokPerTile * kGroup);  // its MMA row
     const int tok = kTokPerTile * (cpi * qt + r) + row / kGroup;
@@ -672,7 +669,10 @@ cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, cudaStream_t str
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   if (p.tail_items < 1 || p.tail_splits < 2) return cudaSuccess;
-  merge_tail_kernel<<<p.tail_items, 256, 0, stream>>>(p);
+  const int rows = p.ctas_per_item * kTokPerTile * kGroup;
+  const dim3 grid(static_cast<unsigned>(p.tail_items),
+                  static_cast<unsigned>((rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock));
+  merge_tail_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -35,12 +35,11 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per device-side wa
 constexpr int64_t kPieceOverheadTiles = 2;   // Q load, pipeline fill, epilogue
 constexpr double kTileUs = 1.5;              // planning estimate per tile, one-CTA kernel
 // Per tile of a CTA pair (the same work per SM as a one-CTA tile). Measured on
-// GB300: the pair kernel runs ~1.3x slower per tile than the one-CTA kernel
-// (e.g. 4096x32768: 2.51 ms vs 1.91 ms), so the planner only picks it when
-// forced or when its schedule is far better balanced.
-constexpr double kPairTileUs = 1.95;
-constexpr double kMergeBytesPerUs = 6.0e6;   // HBM bandwidth for the merge pass
-constexpr double kMergeLaunchUs = 4.0;
+// GB300 the pair kernel is ~1.1x faster per tile (4096x32768: 1.75 ms vs
+// 1.92 ms; 3072x16384: 0.67 ms vs 0.74 ms): each SM streams half the operands.
+constexpr double kPairTileUs = 1.35;
+constexpr double kMergeBytesPerUs = 3.0e6;   // effective bandwidth of the merge pass
+constexpr double kMergeLaunchUs = 6.0;
 constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
 constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16};
 

@@ -13,7 +13,9 @@ from tests.gpu_helpers import check_close, run_gpu
 pytestmark = pytest.mark.gpu
 
 
-def test_withheld_q_times_out_and_context_survives(cuda_device):
+@pytest.mark.parametrize("variant", [1, 2])
+def test_withheld_q_times_out_and_context_survives(cuda_device, variant):
+    """variant 2 also covers a CTA pair giving up together (leader and peer)."""
     import gqa_chunked_prefill_gb300 as gqa
     assert gqa.gqa_prefill_poll() == 0
     q, k, v = make_qkv(100, 900, seed=5)
@@ -21,8 +23,9 @@ def test_withheld_q_times_out_and_context_survives(cuda_device):
     out = torch.zeros_like(qd)
     lse = torch.zeros(100, 24, device="cuda")
     rc, plan = gqa.gqa_prefill_attn_ex(qd, kd, vd, out, lse, 100, 900, 24, 4, 256, 1 / 16,
-                                       wait_timeout_us=50_000, test_withhold_q=True)
-    assert rc == 0  # launched; the failure is reported by the device
+                                       wait_timeout_us=50_000, test_withhold_q=True,
+                                       force_variant=variant)
+    assert rc == 0 and plan["variant"] == variant  # launched; the device reports the failure
     status = gqa.gqa_prefill_poll()
     assert status == gqa.GqaStatus.ERR_DEVICE_TIMEOUT
     assert gqa.gqa_prefill_poll() == 0  # polling clears the word
