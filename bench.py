@@ -38,7 +38,8 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from gqa_inputs import WORKLOADS, make_workload, sample_rows  # noqa: E402
+from gqa_inputs import (SERVING_PAGE_SIZE, WORKLOADS, make_paged_cache, make_workload,  # noqa: E402
+                        sample_rows)
 
 METRIC = "effective causal attention TFLOPS and % of GB300 BF16 tensor peak"
 UNIT = "TFLOP/s"
@@ -208,6 +209,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--page-size", type=int, default=SERVING_PAGE_SIZE,
+                    help="also time the paged-K/V entry point with this page size (0: skip)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -315,6 +318,45 @@ def main():
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_ev) / e2e_steps, pg, dev)
 
+    # ---- the same workload with K/V read from a paged cache ------------------------
+    paged = None
+    if args.page_size > 0:
+        kc_cpu, vc_cpu, table_cpu = make_paged_cache(k_cpu, v_cpu, args.page_size, seed=w.seed)
+        kc, vc, table = kc_cpu.to(dev), vc_cpu.to(dev), table_cpu.to(dev)
+
+        def pcall(events=None):
+            return gqa.gqa_prefill_attn_paged_ex(
+                q, kc, vc, table, kc.shape[0], args.page_size, out, lse, w.q_len, w.kv_len,
+                w.n_q_heads, w.n_kv_heads, w.head_dim, w.scale, stream=stream,
+                fwd_events=events)[1]
+
+        for _ in range(3):
+            flush.zero_()
+            pcall()
+        p_steps = min(args.steps, 100)
+        pev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(p_steps)]
+        for e in pev:
+            for x in e:
+                x.record(stream)
+        torch.cuda.synchronize(dev)
+        for i in range(p_steps):
+            flush.zero_()
+            s0, s1, f0, f1 = pev[i]
+            s0.record(stream)
+            pplan = pcall((f0, f1))
+            s1.record(stream)
+        torch.cuda.synchronize(dev)
+        if gqa.gqa_prefill_poll(stream) != 0:
+            raise RuntimeError("device-side error during the paged steps")
+        p_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b, _, _ in pev) / p_steps, pg, dev)
+        p_fwd = sum(a.elapsed_time(b) for _, _, a, b in pev) / p_steps
+        paged = {"page_size": args.page_size, "num_pages": int(kc.shape[0]),
+                 "block_table": "seeded permutation of the cache's pages; unused slots NaN",
+                 "steps": p_steps, "value": round(job_throughput(world, flops, p_ms), 2),
+                 "unit": UNIT, "ms_per_step": round(p_ms, 4), "kernel_ms": round(p_fwd, 4),
+                 "kernels_per_call": pplan["kernels_per_call"]}
+        del kc, vc, table
+
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -371,6 +413,7 @@ def main():
             "d2h_bytes_per_step": d2h,
         },
         "gpu_launches": args.steps * plan["kernels_per_call"],
+        "paged": paged,
         "clocks": clocks,
         "wall_s_timed_loop": round(wall, 4),
     }

@@ -24,6 +24,7 @@ class GqaStatus(enum.IntEnum):
     ERR_CUDA = 5
     ERR_DEVICE_TIMEOUT = 6
     ERR_SCRATCH = 7
+    ERR_PAGE_TABLE = 8
 
 
 class GqaError(RuntimeError):
@@ -65,6 +66,12 @@ lib.gqa_prefill_attn_ex.argtypes = _ATTN_ARGS + [ctypes.POINTER(PrefillOpts), ct
 lib.gqa_prefill_attn_ex.restype = _i
 lib.gqa_prefill_attn_noalloc.argtypes = _ATTN_ARGS
 lib.gqa_prefill_attn_noalloc.restype = _i
+_PAGED_ARGS = [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
+lib.gqa_prefill_attn_paged.argtypes = _PAGED_ARGS
+lib.gqa_prefill_attn_paged.restype = _i
+lib.gqa_prefill_attn_paged_ex.argtypes = _PAGED_ARGS + [ctypes.POINTER(PrefillOpts),
+                                                        ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_attn_paged_ex.restype = _i
 lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
                                       ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan.restype = _i
@@ -131,16 +138,51 @@ def gqa_prefill_attn_ex(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
                         wait_timeout_us=0, fwd_events=None, test_withhold_q=False, check=True):
     """fwd_events: optional (begin, end) torch.cuda.Event pair recorded around the
     attention kernel itself (not the split merge)."""
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
+                 test_withhold_q)
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_attn_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), q_len, kv_len,
+                                 n_q_heads, n_kv_heads, head_dim, scale, _stream(stream),
+                                 ctypes.byref(opts), ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, test_withhold_q):
     opts = PrefillOpts(force_splits=force_splits, force_grid=force_grid,
                        wait_timeout_us=wait_timeout_us, test_withhold_q=1 if test_withhold_q else 0,
                        force_variant=force_variant)
     if fwd_events is not None:
         opts.fwd_event_begin = fwd_events[0].cuda_event
         opts.fwd_event_end = fwd_events[1].cuda_event
+    return opts
+
+
+def gqa_prefill_attn_paged(q, k_cache, v_cache, block_table, num_pages, page_size, out, lse,
+                           q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale, stream=None,
+                           check=True) -> int:
+    """K/V from paged caches [num_pages, page_size, 4, 256]; block_table: int32 device
+    [ceil(kv_len / page_size)] (logical page -> physical page)."""
+    rc = lib.gqa_prefill_attn_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                    num_pages, page_size, _ptr(out), _ptr(lse), q_len, kv_len,
+                                    n_q_heads, n_kv_heads, head_dim, scale, _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_prefill_attn_paged_ex(q, k_cache, v_cache, block_table, num_pages, page_size, out, lse,
+                              q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale, stream=None,
+                              force_splits=0, force_grid=0, force_variant=0, wait_timeout_us=0,
+                              fwd_events=None, test_withhold_q=False, check=True):
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
+                 test_withhold_q)
     plan = PrefillPlan()
-    rc = lib.gqa_prefill_attn_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), q_len, kv_len,
-                                 n_q_heads, n_kv_heads, head_dim, scale, _stream(stream),
-                                 ctypes.byref(opts), ctypes.byref(plan))
+    rc = lib.gqa_prefill_attn_paged_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                       num_pages, page_size, _ptr(out), _ptr(lse), q_len, kv_len,
+                                       n_q_heads, n_kv_heads, head_dim, scale, _stream(stream),
+                                       ctypes.byref(opts), ctypes.byref(plan))
     if check:
         _check(rc)
     return rc, plan.as_dict()

@@ -42,6 +42,7 @@
 //    tensor memory and returns.
 
 #include "gqa_internal.h"
+#include "gqa_paged.h"
 #include "gqa_prefill.h"
 #include "gqa_schedule.h"
 #include "sm100_ptx.cuh"
@@ -113,6 +114,29 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Fw
   }
 }
 
+// Paged K/V: the V rows of the tile holding key kv_len-1 that lie past kv_len
+// come from the cache's last page and may hold anything. Their P is exactly 0,
+// but 0 * NaN is not, so they are zeroed before the PV reads the stage. The
+// producer loads that tile's V in 16-row boxes and boxes that start past
+// kv_len read TMA zero fill, so only rows [kv_len, next multiple of 16) remain.
+// `base`: the stage (this CTA's shared::cta address, or the peer's
+// shared::cluster address when `remote`); it holds `nb` boxes `box_bytes`
+// apart, each rows key0 .. key0+rows-1 of the tile in 128-byte rows (a whole
+// row stays in place under the 128-byte swizzle).
+__device__ __forceinline__ void zero_v_tail(uint32_t base, uint32_t box_bytes, int nb, int key0,
+                                            int rows, const FwdParams& p, bool remote) {
+  const int kr = p.kv_len - p.v_fix_tile * kBlockN;  // first key of the tile past kv_len
+  const int r_begin = max(kr, key0) - key0;
+  const int r_end = min((kr + 15) & ~15, key0 + rows) - key0;
+  for (int b = 0; b < nb; ++b)
+    for (int r = r_begin; r < r_end; ++r)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t a = base + b * box_bytes + r * 128 + c * 16;
+        if (remote) ptx::st_cluster_zero16(a); else ptx::st_shared_zero16(a);
+      }
+}
+
 // kPair = false: one CTA per work item (21 tokens x 6 heads = 126 MMA rows).
 // kPair = true: a cluster of two CTAs per work item (42 tokens); CTA r holds
 // tokens 21r .. 21r+20 (its own 128 MMA rows), the pair's leader (r = 0)
@@ -122,7 +146,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Fw
 // copies of both CTAs complete on the leader's barriers; MMA completions are
 // multicast to both CTAs; the peer's softmax warps arrive on the leader's
 // barriers remotely.
-template <bool kPair>
+template <bool kPair, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -202,6 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&p.tmap_q);
       ptx::prefetch_tmap(&p.tmap_k);
       ptx::prefetch_tmap(&p.tmap_v);
+      if constexpr (kPaged) {
+        ptx::prefetch_tmap(&p.tmap_k_sub);
+        ptx::prefetch_tmap(&p.tmap_v_sub);
+        ptx::prefetch_tmap(&p.tmap_v16);
+      }
       const uint64_t pol_kv = ptx::policy_evict_last();
       const uint64_t pol_q = ptx::policy_evict_first();
       uint32_t st = 0, phase = 0;
@@ -214,35 +243,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kPair) ptx::tma_load_3d_pair(dst, map, lbar(id), c0, c1, c2, pol);
         else ptx::tma_load_3d(dst, map, bar(id), c0, c1, c2, pol);
       };
+      // Block-table entries (paged K/V), the last one read kept in registers.
+      int cached_pg = -1, cached_entry = 0;
+      auto read_table = [&](int pg) -> int {
+        if (pg != cached_pg) {
+          cached_entry = __ldg(p.block_table + pg);
+          cached_pg = pg;
+        }
+        return cached_entry;
+      };
+      const PagedGeom pgeo{p.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
+      // TMA row coordinates of one box of `rows` keys starting at logical key
+      // r0: the key itself for dense K/V, the cache rows of gqa_paged.h otherwise.
+      auto map_run = [&](int r0, int rows, bool v_fix, PagedRun& run) {
+        if constexpr (kPaged) {
+          map_paged_run(pgeo, r0, rows, v_fix, read_table, run);
+          if (run.bad) atomicExch(p.status, static_cast<int>(GQA_ERR_PAGE_TABLE));
+        } else {
+          run.n = 0;
+          run.sub = rows;
+          run.row[0] = r0;
+        }
+      };
+      auto load_run = [&](uint32_t dst, const CUtensorMap* full, const CUtensorMap* sub_map,
+                          uint32_t id, int c0, int g, const PagedRun& run) {
+        if (run.n == 0) {
+          load(dst, full, id, c0, g, run.row[0], pol_kv);
+          return;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < run.n) load(dst + i * run.sub * 128, sub_map, id, c0, g, run.row[i], pol_kv);
+      };
       // One K tile is two 32 KB stages (d halves) in the one-CTA kernel and one
       // stage (this CTA's 64 keys) in a pair; likewise for V (key halves / this
-      // CTA's 128 columns).
+      // CTA's 128 columns). Boxes are 64 d wide (128-byte rows).
       auto next_tile = [&](int n, bool is_k, int g) -> bool {
+        const bool v_fix = kPaged && !is_k && n == p.v_fix_tile;
+        const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
+        const CUtensorMap* sub_map = is_k ? &p.tmap_k_sub : (v_fix ? &p.tmap_v16 : &p.tmap_v_sub);
         for (int half = 0; half < (kPair ? 1 : 2); ++half) {
           if (!wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
           const uint32_t dst = stage_smem + st * kStageBytes;
           if (leader) ptx::mbar_arrive_expect_tx(bar(kBarFull + st), (kPair ? 2 : 1) * kStageBytes);
+          // Box geometry: first key, keys per box, boxes (d chunks), their stride
+          // in shared memory, first d column.
+          int r0, rows, nb, c_base;
+          uint32_t stride;
           if constexpr (kPair) {
-            if (is_k) {
-              for (int c = 0; c < 4; ++c)
-                load(dst + c * 8192, &p.tmap_k, kBarFull + st, 64 * c, g,
-                     n * kBlockN + 64 * static_cast<int>(rank), pol_kv);
-            } else {
-              for (int c = 0; c < 2; ++c)
-                load(dst + c * 16384, &p.tmap_v, kBarFull + st, 128 * static_cast<int>(rank) + 64 * c,
-                     g, n * kBlockN, pol_kv);
-            }
+            r0 = n * kBlockN + (is_k ? 64 * static_cast<int>(rank) : 0);
+            rows = is_k ? 64 : 128;
+            nb = is_k ? 4 : 2;
+            stride = is_k ? 8192u : 16384u;
+            c_base = is_k ? 0 : 128 * static_cast<int>(rank);
           } else {
-            if (is_k) {
-              for (int c = 0; c < 2; ++c)
-                load(dst + c * kKBoxBytes, &p.tmap_k, kBarFull + st, 128 * half + 64 * c, g,
-                     n * kBlockN, pol_kv);
-            } else {
-              for (int c = 0; c < 4; ++c)
-                load(dst + c * kVBoxBytes, &p.tmap_v, kBarFull + st, 64 * c, g,
-                     n * kBlockN + 64 * half, pol_kv);
-            }
+            r0 = n * kBlockN + (is_k ? 0 : 64 * half);
+            rows = is_k ? 128 : 64;
+            nb = is_k ? 2 : 4;
+            stride = is_k ? kKBoxBytes : kVBoxBytes;
+            c_base = is_k ? 128 * half : 0;
           }
+          PagedRun run;
+          map_run(r0, rows, v_fix, run);
+          for (int c = 0; c < nb; ++c)
+            load_run(dst + c * stride, full, sub_map, kBarFull + st, c_base + 64 * c, g, run);
           issued_mask |= 1u << st;
           issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
           if (++st == kStages) { st = 0; phase ^= 1u; }
@@ -356,10 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           // O += P_j V_j in k-steps of 16 keys, N = 256. V stages are MN-major:
           // LBO = next 64-wide d chunk, SBO = next group of 8 keys.
+          const bool v_fix = kPaged && w.n0 + j == p.v_fix_tile;
           if constexpr (kPair) {
             // One stage: 128 keys x this CTA's 128 columns (2 boxes, 16 KB apart).
             if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
             ptx::tc_fence_after();
+            if (v_fix) {
+              zero_v_tail(stage_smem + st * kStageBytes, 16384u, 2, 0, 128, p, false);
+              zero_v_tail(ptx::map_to_cta(stage_smem + st * kStageBytes, 1), 16384u, 2, 0, 128, p,
+                          true);
+              ptx::fence_proxy_async_all();
+            }
             const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -374,6 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int half = 0; half < 2 && ok; ++half) {
               if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
               ptx::tc_fence_after();
+              if (v_fix) {
+                zero_v_tail(stage_smem + st * kStageBytes, kVBoxBytes, 4, 64 * half, 64, p, false);
+                ptx::fence_proxy_async_all();
+              }
               const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
@@ -623,48 +698,52 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
 size_t fwd_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t prepare_fwd_kernel() {
-  cudaError_t e = cudaFuncSetAttribute(gqa_attn_fwd_sm103_kernel<false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kSmemAlloc));
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gqa_attn_fwd_sm103_kernel<true>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmemAlloc));
-}
-
-cudaError_t max_active_pairs(int* pairs) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemAlloc;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true>, &cfg);
-}
-
-cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, cudaStream_t stream) {
-  if (!pair) {
-    gqa_attn_fwd_sm103_kernel<false><<<grid, kThreads, kSmemAlloc, stream>>>(p);
-    return cudaGetLastError();
+  const void* kernels[] = {
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true>)};
+  for (const void* f : kernels) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(kSmemAlloc));
+    if (e != cudaSuccess) return e;
   }
+  return cudaSuccess;
+}
+
+namespace {
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);  // 2 CTAs per pair
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true>, p);
+  return cfg;
+}
+}  // namespace
+
+cudaError_t max_active_pairs(int* pairs) {
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
+  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, false>, &cfg);
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, cudaStream_t stream) {
+  if (!pair) {
+    if (paged) gqa_attn_fwd_sm103_kernel<false, true><<<grid, kThreads, kSmemAlloc, stream>>>(p);
+    else gqa_attn_fwd_sm103_kernel<false, false><<<grid, kThreads, kSmemAlloc, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
+  return paged ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true>, p)
+               : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false>, p);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {

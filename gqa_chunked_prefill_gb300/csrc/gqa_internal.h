@@ -40,6 +40,18 @@ struct FwdParams {
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
   int withhold_q;      // test only: the producer never loads the first Q tile
+  // Paged K/V (kernels instantiated with kPaged only): tmap_k / tmap_v then span
+  // the whole cache [num_pages * page_size][4][256] and key j of the sequence is
+  // cache row block_table[j / page_size] * page_size + j % page_size.
+  CUtensorMap tmap_k_sub;    // box (64 d, 1 head, sub_rows keys): boxes that cross a page
+  CUtensorMap tmap_v_sub;
+  CUtensorMap tmap_v16;      // box (64 d, 1 head, 16 keys): V of the tile holding key kv_len-1
+  const int* block_table;    // [ceil(kv_len / page_size)] physical page of each logical page
+  int page_size;             // keys per page, a multiple of 16
+  int num_pages;             // pages in the cache
+  int sub_rows;              // gcd(page_size, 64)
+  int oob_row;               // num_pages * page_size: a row past the cache (TMA zero fill)
+  int v_fix_tile;            // KV tile holding key kv_len-1 if kv_len % 128 != 0, else -1
 };
 
 struct MergeParams {
@@ -57,7 +69,7 @@ struct MergeParams {
 
 size_t fwd_smem_bytes();
 // grid = CTAs; with pair = true the CTAs form clusters of two (grid even).
-cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, cudaStream_t stream);
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, cudaStream_t stream);
 cudaError_t max_active_pairs(int* pairs);       // co-resident CTA pairs on this device
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t prepare_fwd_kernel();                // per-device one-time attributes

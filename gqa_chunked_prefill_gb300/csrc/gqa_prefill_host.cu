@@ -282,20 +282,63 @@ gqa_status check_call(const void* q, const void* k, const void* v, const void* o
   return GQA_OK;
 }
 
+// K/V of a paged call: the caches span num_pages * page_size rows.
+struct PagedKV {
+  const int32_t* block_table;
+  int num_pages;
+  int page_size;
+};
+constexpr int64_t kMaxCacheRows = int64_t{1} << 30;  // TMA row coordinates stay far from 2^31
+
+gqa_status check_paged(const PagedKV& pkv, int q_len) {
+  if (pkv.page_size <= 0 || pkv.page_size % 16 != 0) return GQA_ERR_UNSUPPORTED;
+  if (pkv.num_pages < 1 || static_cast<int64_t>(pkv.num_pages) * pkv.page_size >= kMaxCacheRows)
+    return GQA_ERR_SHAPE;
+  if (q_len == 0) return GQA_OK;
+  if (!pkv.block_table) return GQA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(pkv.block_table) & 3u) != 0) return GQA_ERR_ALIGN;
+  return GQA_OK;
+}
+
+int gcd_int(int a, int b) {
+  while (b != 0) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
 // Launches `plan` on `stream`; `ws` holds plan.workspace_bytes (or nothing).
+// `pkv` is null for dense K/V; otherwise k and v are the paged caches.
 gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* k, const void* v,
-                       void* out, float* lse, int q_len, int kv_len, float scale, int* status_word,
-                       void* ws, const gqa_prefill_opts* opts, cudaStream_t stream) {
+                       const PagedKV* pkv, void* out, float* lse, int q_len, int kv_len,
+                       float scale, int* status_word, void* ws, const gqa_prefill_opts* opts,
+                       cudaStream_t stream) {
   const bool pair = plan.variant == 2;
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
+  const uint64_t kv_rows = pkv ? static_cast<uint64_t>(pkv->num_pages) * pkv->page_size
+                               : static_cast<uint64_t>(kv_len);
   if (!encode_3d(&p.tmap_q, q, kHeadDim, kQHeads, static_cast<uint64_t>(q_len), 64, kGroup,
                  kTokPerTile) ||
-      !encode_3d(&p.tmap_k, k, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1,
-                 pair ? 64 : kBlockN) ||
-      !encode_3d(&p.tmap_v, v, kHeadDim, kKvHeads, static_cast<uint64_t>(kv_len), 64, 1,
-                 pair ? kBlockN : 64))
+      !encode_3d(&p.tmap_k, k, kHeadDim, kKvHeads, kv_rows, 64, 1, pair ? 64 : kBlockN) ||
+      !encode_3d(&p.tmap_v, v, kHeadDim, kKvHeads, kv_rows, 64, 1, pair ? kBlockN : 64))
     return GQA_ERR_CUDA;
+  p.v_fix_tile = -1;
+  if (pkv) {
+    const int sub = gcd_int(pkv->page_size, 64);  // 16, 32 or 64: divides pages and boxes
+    if (!encode_3d(&p.tmap_k_sub, k, kHeadDim, kKvHeads, kv_rows, 64, 1, sub) ||
+        !encode_3d(&p.tmap_v_sub, v, kHeadDim, kKvHeads, kv_rows, 64, 1, sub) ||
+        !encode_3d(&p.tmap_v16, v, kHeadDim, kKvHeads, kv_rows, 64, 1, 16))
+      return GQA_ERR_CUDA;
+    p.block_table = pkv->block_table;
+    p.page_size = pkv->page_size;
+    p.num_pages = pkv->num_pages;
+    p.sub_rows = sub;
+    p.oob_row = static_cast<int>(kv_rows);
+    if (kv_len % kBlockN != 0) p.v_fix_tile = (kv_len - 1) / kBlockN;
+  }
   const int workers = pair ? plan.grid / 2 : plan.grid;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
@@ -319,7 +362,7 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* 
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return GQA_ERR_CUDA;
-  if (launch_fwd(p, plan.grid, pair, stream) != cudaSuccess) return GQA_ERR_CUDA;
+  if (launch_fwd(p, plan.grid, pair, pkv != nullptr, stream) != cudaSuccess) return GQA_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return GQA_ERR_CUDA;
   if (plan.kernels_per_call == 2) {
     MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.n_qtiles, p.head_items,
@@ -329,11 +372,13 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* 
   return GQA_OK;
 }
 
-gqa_status run(const void* q, const void* k, const void* v, void* out, float* lse, int q_len,
-               int kv_len, int n_q_heads, int n_kv_heads, int head_dim, float scale, void* stream_ptr,
-               const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out) {
+gqa_status run(const void* q, const void* k, const void* v, const PagedKV* pkv, void* out,
+               float* lse, int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
+               float scale, void* stream_ptr, const gqa_prefill_opts* opts,
+               gqa_prefill_plan* plan_out) {
   if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
   gqa_status st = check_call(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
+  if (st == GQA_OK && pkv) st = check_paged(*pkv, q_len);
   if (st != GQA_OK || q_len == 0) return st;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != GQA_OK) return st;
@@ -350,7 +395,8 @@ gqa_status run(const void* q, const void* k, const void* v, void* out, float* ls
         cudaSuccess)
       return GQA_ERR_CUDA;
   }
-  st = launch_plan(plan, q, k, v, out, lse, q_len, kv_len, scale, dev->status_word, ws, opts, stream);
+  st = launch_plan(plan, q, k, v, pkv, out, lse, q_len, kv_len, scale, dev->status_word, ws, opts,
+                   stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   return st;
 }
@@ -397,8 +443,8 @@ gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, f
   if (static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes) return GQA_ERR_SCRATCH;
   // Every partial row the merge reads is written by the attention kernel first,
   // so the scratch needs no clearing between calls.
-  return launch_plan(plan, q, k, v, out, lse, q_len, kv_len, scale, dev->status_word, scratch,
-                     nullptr, static_cast<cudaStream_t>(stream_ptr));
+  return launch_plan(plan, q, k, v, nullptr, out, lse, q_len, kv_len, scale, dev->status_word,
+                     scratch, nullptr, static_cast<cudaStream_t>(stream_ptr));
 }
 
 }  // namespace
@@ -417,16 +463,36 @@ gqa_status gqa_prefill_attn_noalloc(const void* q, const void* k, const void* v,
 gqa_status gqa_prefill_attn(const void* q, const void* k, const void* v, void* out, float* lse,
                             int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                             float scale, void* stream) {
-  return gqa::run(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale, stream,
-                  nullptr, nullptr);
+  return gqa::run(q, k, v, nullptr, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
+                  stream, nullptr, nullptr);
 }
 
 gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,
                                int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                                float scale, void* stream, const gqa_prefill_opts* opts,
                                gqa_prefill_plan* plan_out) {
-  return gqa::run(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale, stream,
-                  opts, plan_out);
+  return gqa::run(q, k, v, nullptr, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
+                  stream, opts, plan_out);
+}
+
+gqa_status gqa_prefill_attn_paged(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, int num_pages, int page_size,
+                                  void* out, float* lse, int q_len, int kv_len, int n_q_heads,
+                                  int n_kv_heads, int head_dim, float scale, void* stream) {
+  const gqa::PagedKV pkv{block_table, num_pages, page_size};
+  return gqa::run(q, k_cache, v_cache, &pkv, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
+                  head_dim, scale, stream, nullptr, nullptr);
+}
+
+gqa_status gqa_prefill_attn_paged_ex(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, int num_pages, int page_size,
+                                     void* out, float* lse, int q_len, int kv_len,
+                                     int n_q_heads, int n_kv_heads, int head_dim, float scale,
+                                     void* stream, const gqa_prefill_opts* opts,
+                                     gqa_prefill_plan* plan_out) {
+  const gqa::PagedKV pkv{block_table, num_pages, page_size};
+  return gqa::run(q, k_cache, v_cache, &pkv, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
+                  head_dim, scale, stream, opts, plan_out);
 }
 
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
@@ -466,15 +532,20 @@ const char* gqa_status_string(gqa_status status) {
   switch (status) {
     case GQA_OK: return "ok";
     case GQA_ERR_NULL: return "a required pointer is NULL";
-    case GQA_ERR_SHAPE: return "invalid sizes (need 0 <= q_len <= kv_len) or scale (finite, > 0)";
+    case GQA_ERR_SHAPE:
+      return "invalid sizes (need 0 <= q_len <= kv_len; paged: num_pages >= 1, "
+             "num_pages * page_size < 2^30) or scale (finite, > 0)";
     case GQA_ERR_UNSUPPORTED:
-      return "unsupported: needs 24 query heads, 4 KV heads, head_dim 256 on an sm_103 GPU";
+      return "unsupported: needs 24 query heads, 4 KV heads, head_dim 256 on an sm_103 GPU "
+             "(paged: page_size a positive multiple of 16)";
     case GQA_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
     case GQA_ERR_CUDA: return "a CUDA call failed";
     case GQA_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out; the kernel gave up";
     case GQA_ERR_SCRATCH:
       return "gqa_prefill_attn_noalloc: split partials exceed the 64 MiB static scratch "
              "(use a shorter chunk or gqa_prefill_attn)";
+    case GQA_ERR_PAGE_TABLE:
+      return "a block-table entry was outside [0, num_pages); that page was read as zeros";
   }
   return "unknown status";
 }

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 1
+#define GQA_PREFILL_ABI_VERSION 2
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -55,8 +55,10 @@ typedef enum gqa_status {
   GQA_ERR_ALIGN = 4,          /* a pointer is not 16-byte aligned                      */
   GQA_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed                     */
   GQA_ERR_DEVICE_TIMEOUT = 6, /* a device-side wait ran out of time (see _poll)        */
-  GQA_ERR_SCRATCH = 7         /* gqa_prefill_attn_noalloc: the call's split partials do
+  GQA_ERR_SCRATCH = 7,        /* gqa_prefill_attn_noalloc: the call's split partials do
                                  not fit the library's static scratch array            */
+  GQA_ERR_PAGE_TABLE = 8      /* device-side (see _poll): a paged call met a block-table
+                                 entry outside [0, num_pages); that page read as zeros */
 } gqa_status;
 
 /*
@@ -141,7 +143,7 @@ gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
- * word (0 or GQA_ERR_DEVICE_TIMEOUT) into *device_status. Returns GQA_ERR_CUDA
+ * word (0, GQA_ERR_DEVICE_TIMEOUT or GQA_ERR_PAGE_TABLE) into *device_status. Returns GQA_ERR_CUDA
  * if the synchronisation itself fails. The status word is shared by all
  * streams of the device: it reports any kernel of this library that gave up
  * since the previous poll.
@@ -182,6 +184,46 @@ gqa_status gqa_prefill_poll(void* stream, int* device_status);
 gqa_status gqa_prefill_attn_noalloc(const void* q, const void* k, const void* v, void* out,
                                     float* lse, int q_len, int kv_len, int n_q_heads,
                                     int n_kv_heads, int head_dim, float scale, void* stream);
+
+/*
+ * gqa_prefill_attn_paged — the same operation with K and V read from a paged
+ * cache instead of dense [kv_len, ...] arrays (gfx936 DCU上实现INT8 QK MMAC：
+ * 分页访存、Fragment映射与GQA适配, §3: a logical key token is found through the
+ * block table, which gives its physical block, and its slot inside that block;
+ * DCU使用技术报告（中篇）, §8: the serving engine's BF16 attention page holds 784
+ * tokens).
+ *
+ *   k_cache, v_cache : BF16 [num_pages, page_size, n_kv_heads, head_dim], dense
+ *   block_table      : int32 [ceil(kv_len / page_size)], DEVICE memory: logical
+ *                      key j (0 <= j < kv_len) of the sequence is row
+ *                      j % page_size of page block_table[j / page_size]
+ *
+ * q, out, lse, scale and the causal alignment are those of gqa_prefill_attn:
+ * the chunk's q_len tokens are the last q_len of the kv_len keys, whose K/V are
+ * already in the cache. Pages may be listed in any order and shared between
+ * sequences. Rows of the last page past kv_len may hold anything, NaN
+ * included: they never reach the output.
+ *
+ * Requirements (else an error, nothing launched): page_size a positive
+ * multiple of 16 (GQA_ERR_UNSUPPORTED); num_pages >= 1 and
+ * num_pages * page_size < 2^30 (TMA row coordinates are 32-bit; 2^30 rows
+ * would be 2 TiB per cache; GQA_ERR_SHAPE); block_table non-NULL and 4-byte aligned, the other pointers
+ * 16-byte aligned. The block table is read on the device: an entry outside
+ * [0, num_pages) is not followed — the page's keys and values are read as
+ * zeros and GQA_ERR_PAGE_TABLE is recorded in the status word (_poll).
+ */
+gqa_status gqa_prefill_attn_paged(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, int num_pages, int page_size,
+                                  void* out, float* lse, int q_len, int kv_len, int n_q_heads,
+                                  int n_kv_heads, int head_dim, float scale, void* stream);
+
+/* gqa_prefill_attn_paged with options and the plan (as gqa_prefill_attn_ex). */
+gqa_status gqa_prefill_attn_paged_ex(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, int num_pages, int page_size,
+                                     void* out, float* lse, int q_len, int kv_len,
+                                     int n_q_heads, int n_kv_heads, int head_dim, float scale,
+                                     void* stream, const gqa_prefill_opts* opts,
+                                     gqa_prefill_plan* plan_out);
 
 /* Static description of a status code (never NULL). */
 const char* gqa_status_string(gqa_status status);

@@ -5,6 +5,9 @@ benchmark's CPU-baseline leg are the only callers. The product package never
 imports this module, and this module never imports the product package; the
 two share nothing but the seeded inputs of ``gqa_inputs``.
 
+``paged_gather()`` reads one sequence's keys and values out of paged caches
+through its block table; ``paged_attention()`` is attention on what it returns.
+
 ``attention()`` runs the plain C++ definition in ``gqa_oracle.cpp`` (explicit
 full-row softmax in FP64, one std::thread per row at a time). ``restate_numpy``
 holds an independent numpy restatement used to cross-check it on tiny shapes.
@@ -111,3 +114,35 @@ def attention(q, k, v, scale: float, rows=None, n_threads: Optional[int] = None,
     if with_prob_sum:
         return out, lse, psum
     return out, lse
+
+
+def paged_gather(k_cache, v_cache, block_table, kv_len: int):
+    """K and V of one sequence, read out of paged caches.
+
+    Follows "gfx936 DCU上实现INT8 QK MMAC：分页访存、Fragment映射与GQA适配", §3: a
+    logical key token is looked up in the block table, which names its physical
+    block, and sits in that block at its slot. Here the slot of key j is
+    j mod page_size and its block is block_table[j div page_size].
+    k_cache, v_cache: [num_pages, page_size, Hkv, d]; block_table: integer
+    [>= ceil(kv_len / page_size)]. Returns (k, v) [kv_len, Hkv, d] in the
+    caches' dtype (torch in, torch out; numpy in, numpy out).
+    """
+    table = np.asarray(block_table.cpu().numpy() if isinstance(block_table, torch.Tensor)
+                       else block_table, dtype=np.int64)
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    j = np.arange(kv_len, dtype=np.int64)
+    block = table[j // page_size]
+    slot = j % page_size
+    if kv_len and (block.min() < 0 or block.max() >= num_pages):
+        raise ValueError("block table entry outside the cache")
+    if isinstance(k_cache, torch.Tensor):
+        bi, si = torch.from_numpy(block), torch.from_numpy(slot)
+        return k_cache[bi, si], v_cache[bi, si]
+    return k_cache[block, slot], v_cache[block, slot]
+
+
+def paged_attention(q, k_cache, v_cache, block_table, kv_len: int, scale: float, rows=None,
+                    n_threads: Optional[int] = None):
+    """``attention()`` of q over the sequence ``paged_gather()`` reads from the caches."""
+    k, v = paged_gather(k_cache, v_cache, block_table, kv_len)
+    return attention(q, k, v, scale, rows=rows, n_threads=n_threads)

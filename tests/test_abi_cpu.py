@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(gqa):
 
 
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 1
+    assert gqa.gqa_prefill_abi_version() == 2
 
 
 def test_refusals_before_any_cuda_call(gqa):
@@ -56,6 +56,36 @@ def test_refusals_before_any_cuda_call(gqa):
     assert f(None, None, None, None, None, 0, 0, 24, 4, 256, 0.0625) == S.OK  # empty chunk
     for s in S:
         assert isinstance(gqa.gqa_status_string(int(s)), str)
+
+
+def test_paged_refusals_before_any_cuda_call(gqa):
+    """Arguments: q, k_cache, v_cache, block_table, num_pages, page_size, out, lse,
+    q_len, kv_len, heads..., scale."""
+    S = gqa.GqaStatus
+    f = lambda *a: gqa.gqa_prefill_attn_paged(*a, stream=0, check=False)
+    ok = (16, 16, 16, 16, 4, 784, 16, None, 4, 8, 24, 4, 256, 0.0625)
+
+    def call(**kw):
+        names = ["q", "kc", "vc", "bt", "np", "ps", "out", "lse", "q_len", "kv_len", "hq", "hkv",
+                 "d", "scale"]
+        args = dict(zip(names, ok))
+        args.update(kw)
+        return f(*[args[n] for n in names])
+
+    assert call(ps=0) == S.ERR_UNSUPPORTED
+    assert call(ps=24) == S.ERR_UNSUPPORTED        # not a multiple of 16
+    assert call(ps=-16) == S.ERR_UNSUPPORTED
+    assert call(np=0) == S.ERR_SHAPE
+    assert call(np=1 << 26, ps=16) == S.ERR_SHAPE   # 2^30 cache rows
+    assert call(bt=None) == S.ERR_NULL
+    assert call(bt=18) == S.ERR_ALIGN               # int32 table: 4-byte alignment
+    assert call(kc=None) == S.ERR_NULL
+    assert call(vc=24) == S.ERR_ALIGN
+    assert call(kv_len=3) == S.ERR_SHAPE            # kv_len < q_len
+    assert call(hkv=8) == S.ERR_UNSUPPORTED
+    assert call(q=None, kc=None, vc=None, bt=None, out=None, q_len=0, kv_len=0) == S.OK
+    assert call(q=None, kc=None, vc=None, bt=None, out=None, q_len=0, kv_len=0, ps=8) == \
+        S.ERR_UNSUPPORTED
 
 
 SHAPES = [(1, 1), (21, 21), (22, 5000), (128, 256), (512, 4096), (4096, 8192), (4096, 16384),

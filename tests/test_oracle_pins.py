@@ -198,3 +198,48 @@ def test_stored_oracle_values_unchanged():
         assert abs(lse[i] - float(l[1])) < 1e-12
         for j, c in enumerate(cols):
             assert abs(out[i, c] - float(l[2 + j])) < 1e-12
+
+
+# --- paged K/V: the block-table gather --------------------------------------------
+
+def test_paged_gather_worked_example_by_hand():
+    """page_size 2, three pages whose slots hold 10*page + slot, block table [2, 0, 1]:
+    keys 0..4 live at (page 2, slot 0), (2, 1), (0, 0), (0, 1), (1, 0)."""
+    cache = np.zeros((3, 2, 1, 1))
+    for page in range(3):
+        for slot in range(2):
+            cache[page, slot, 0, 0] = 10 * page + slot
+    k, v = oracle.paged_gather(cache, -cache, [2, 0, 1], kv_len=5)
+    assert k[:, 0, 0].tolist() == [20, 21, 0, 1, 10]
+    assert v[:, 0, 0].tolist() == [-20, -21, 0, -1, -10]
+
+
+def test_paged_gather_repeated_page():
+    cache = np.arange(8, dtype=np.float64).reshape(2, 4, 1, 1)
+    k, _ = oracle.paged_gather(cache, cache, [1, 1], kv_len=7)
+    assert k[:, 0, 0].tolist() == [4, 5, 6, 7, 4, 5, 6]
+
+
+@pytest.mark.parametrize("kv_len,page_size", [(1, 16), (40, 16), (300, 48), (300, 784), (1000, 64)])
+def test_paged_gather_inverts_the_cache_scatter(kv_len, page_size):
+    """The input generator scatters logical pages to seeded physical pages and
+    fills every other slot with NaN; reading the sequence back through the
+    table must give the dense K/V bit for bit, and no NaN."""
+    from gqa_inputs import make_paged_cache
+    q, k, v = make_qkv(min(kv_len, 7), kv_len, 50 + kv_len)
+    kc, vc, table = make_paged_cache(k, v, page_size, seed=kv_len + page_size)
+    assert kc.shape[0] == -(-kv_len // page_size) + 3
+    assert torch.isnan(kc.float()).any()  # unused slots really are poisoned
+    k2, v2 = oracle.paged_gather(kc, vc, table, kv_len)
+    assert torch.equal(k2, k) and torch.equal(v2, v)
+    out_p, lse_p = oracle.paged_attention(q, kc, vc, table, kv_len, SCALE)
+    out_d, lse_d = oracle.attention(q, k, v, SCALE)
+    assert np.array_equal(out_p, out_d) and np.array_equal(lse_p, lse_d)
+
+
+def test_paged_gather_rejects_entries_outside_the_cache():
+    cache = np.zeros((2, 4, 1, 1))
+    with pytest.raises(ValueError):
+        oracle.paged_gather(cache, cache, [0, 2], kv_len=6)
+    with pytest.raises(ValueError):
+        oracle.paged_gather(cache, cache, [-1], kv_len=3)
