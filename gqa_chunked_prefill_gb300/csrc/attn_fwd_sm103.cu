@@ -56,8 +56,6 @@ constexpr uint32_t kQChunkBytes = 128 * 128;   // 128 rows x 64 bf16 (one 128B-s
 constexpr uint32_t kQBoxBytes = 126 * 128;     // the 21x6 rows one TMA box writes
 constexpr uint32_t kQBytes = 4 * kQChunkBytes;  // d = 256 -> 4 chunks
 constexpr uint32_t kStageBytes = 32768;
-constexpr uint32_t kKBoxBytes = 128 * 128;     // 128 keys x 64 d
-constexpr uint32_t kVBoxBytes = 64 * 128;      // 64 keys x 64 d
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O: 256 FP32 columns
@@ -117,24 +115,48 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Fw
 // Paged K/V: the V rows of the tile holding key kv_len-1 that lie past kv_len
 // come from the cache's last page and may hold anything. Their P is exactly 0,
 // but 0 * NaN is not, so they are zeroed before the PV reads the stage. The
-// producer loads that tile's V in 16-row boxes and boxes that start past
-// kv_len read TMA zero fill, so only rows [kv_len, next multiple of 16) remain.
+// producer loads that tile's V in 16-key pieces and pieces that start past
+// kv_len read TMA zero fill, so only keys [kv_len, next multiple of 16) remain.
 // `base`: the stage (this CTA's shared::cta address, or the peer's
-// shared::cluster address when `remote`); it holds `nb` boxes `box_bytes`
-// apart, each rows key0 .. key0+rows-1 of the tile in 128-byte rows (a whole
-// row stays in place under the 128-byte swizzle).
-__device__ __forceinline__ void zero_v_tail(uint32_t base, uint32_t box_bytes, int nb, int key0,
-                                            int rows, const FwdParams& p, bool remote) {
+// shared::cluster address when `remote`), holding keys key0 .. key0+rows-1 of
+// the tile in the paged stage layout: key r, chunk c at
+// (r / 8) * 1024 * nch + c * 1024 + (r % 8) * 128 (a 128-byte row stays in
+// place under the 128-byte swizzle). Out of line (rare: once per item that
+// reaches the last KV tile) so the MMA thread's loop stays small.
+__device__ __noinline__ void zero_v_tail(uint32_t base, int nch, int key0, int rows,
+                                         const FwdParams& p, bool remote) {
   const int kr = p.kv_len - p.v_fix_tile * kBlockN;  // first key of the tile past kv_len
   const int r_begin = max(kr, key0) - key0;
   const int r_end = min((kr + 15) & ~15, key0 + rows) - key0;
-  for (int b = 0; b < nb; ++b)
-    for (int r = r_begin; r < r_end; ++r)
+  for (int r = r_begin; r < r_end; ++r)
+    for (int c = 0; c < nch; ++c)
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t a = base + b * box_bytes + r * 128 + c * 16;
+      for (int u = 0; u < 8; ++u) {
+        const uint32_t a = base + (r >> 3) * 1024 * nch + c * 1024 + (r & 7) * 128 + u * 16;
         if (remote) ptx::st_cluster_zero16(a); else ptx::st_shared_zero16(a);
       }
+}
+
+// Paged K/V, the rare case: a box that crosses pages (or the V box of the tile
+// holding key kv_len-1) goes as pieces (gqa_paged.h), one 5-D copy per piece
+// covering all `nch` chunks (paged stage layout, see the kernel). `bar`: the
+// barrier the copies complete on (the pair leader's, mapped, for pairs). Out of
+// line so the producer's common loop stays small.
+template <bool kPair>
+__device__ __noinline__ void issue_paged_pieces(const FwdParams& p, const CUtensorMap* sub_map,
+                                                uint32_t dst, uint32_t bar, int r0, int rows,
+                                                int nch, int chunk0, int g, bool v_fix,
+                                                uint64_t pol) {
+  const PagedGeom pgeo{p.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
+  PagedRun run;
+  map_paged_run(pgeo, r0, rows, v_fix, [&](int pg) { return __ldg(p.block_table + pg); }, run);
+  if (run.bad) atomicExch(p.status, static_cast<int>(GQA_ERR_PAGE_TABLE));
+  for (int i = 0; i < run.n; ++i) {
+    // Piece i is 8-key groups [i*sub/8, (i+1)*sub/8) of the stage: contiguous.
+    const uint32_t d = dst + i * run.sub * nch * 128;
+    if constexpr (kPair) ptx::tma_load_5d_pair(d, sub_map, bar, 0, 0, chunk0, run.row[i] / 8, g, pol);
+    else ptx::tma_load_5d(d, sub_map, bar, 0, 0, chunk0, run.row[i] / 8, g, pol);
+  }
 }
 
 // kPair = false: one CTA per work item (21 tokens x 6 heads = 126 MMA rows).
@@ -171,6 +193,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (kPair) ptx::tc_commit_pair(bar(id)); else ptx::tc_commit(bar(id));
   };
   constexpr uint32_t kConsumers = (kPair ? 2 : 1) * 4 * 32;  // softmax threads per item
+  // Shared-memory layout of a K or V stage (its keys x nch 64-column chunks,
+  // 128-byte rows, 128B swizzle). Dense K/V: chunk-major, each chunk's keys
+  // contiguous (one 4-D copy per stage). Paged K/V: 8-key groups outermost with
+  // the chunks inside each group, so that a piece of whole groups — what a
+  // paged box that crosses a page is cut into — is contiguous and one 5-D
+  // copy. Both are uniform strides for the MMA descriptors: K rows 8 apart at
+  // kSboK, next chunk at kChunkK; V next chunk at kLboV, next 8 keys at kSboV.
+  constexpr uint32_t kNchK = kPair ? 4 : 2;      // chunks per K stage
+  constexpr uint32_t kNchV = kPair ? 2 : 4;      // chunks per V stage
+  constexpr uint32_t kRowsK = kPair ? 64 : 128;  // keys per K stage
+  constexpr uint32_t kRowsV = kPair ? 128 : 64;  // keys per V stage
+  constexpr uint32_t kChunkK = kPaged ? 1024u : kRowsK * 128u;
+  constexpr uint32_t kSboK = kPaged ? kNchK * 1024u : 1024u;
+  constexpr uint32_t kLboV = kPaged ? 1024u : kRowsV * 128u;
+  constexpr uint32_t kSboV = kPaged ? kNchV * 1024u : 1024u;
 
   // ---- set-up: barriers, idle Q rows, tensor memory -------------------------
   if (threadIdx.x == 0) {
@@ -243,41 +280,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kPair) ptx::tma_load_3d_pair(dst, map, lbar(id), c0, c1, c2, pol);
         else ptx::tma_load_3d(dst, map, bar(id), c0, c1, c2, pol);
       };
-      // Block-table entries (paged K/V), the last one read kept in registers.
-      int cached_pg = -1, cached_entry = 0;
-      auto read_table = [&](int pg) -> int {
-        if (pg != cached_pg) {
-          cached_entry = __ldg(p.block_table + pg);
-          cached_pg = pg;
-        }
-        return cached_entry;
-      };
-      const PagedGeom pgeo{p.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
-      // TMA row coordinates of one box of `rows` keys starting at logical key
-      // r0: the key itself for dense K/V, the cache rows of gqa_paged.h otherwise.
-      auto map_run = [&](int r0, int rows, bool v_fix, PagedRun& run) {
+      // A whole K/V box: 4-D (64 d, key, head, chunk) dense, 5-D (64 d, key % 8,
+      // chunk, key / 8, head) paged; both with the stage layout described above.
+      auto load_box = [&](uint32_t dst, const CUtensorMap* map, uint32_t id, int row, int g,
+                          int chunk0) {
         if constexpr (kPaged) {
-          map_paged_run(pgeo, r0, rows, v_fix, read_table, run);
-          if (run.bad) atomicExch(p.status, static_cast<int>(GQA_ERR_PAGE_TABLE));
+          if constexpr (kPair) ptx::tma_load_5d_pair(dst, map, lbar(id), 0, 0, chunk0, row / 8, g, pol_kv);
+          else ptx::tma_load_5d(dst, map, bar(id), 0, 0, chunk0, row / 8, g, pol_kv);
         } else {
-          run.n = 0;
-          run.sub = rows;
-          run.row[0] = r0;
+          if constexpr (kPair) ptx::tma_load_4d_pair(dst, map, lbar(id), 0, row, g, chunk0, pol_kv);
+          else ptx::tma_load_4d(dst, map, bar(id), 0, row, g, chunk0, pol_kv);
         }
       };
-      auto load_run = [&](uint32_t dst, const CUtensorMap* full, const CUtensorMap* sub_map,
-                          uint32_t id, int c0, int g, const PagedRun& run) {
-        if (run.n == 0) {
-          load(dst, full, id, c0, g, run.row[0], pol_kv);
-          return;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < run.n) load(dst + i * run.sub * 128, sub_map, id, c0, g, run.row[i], pol_kv);
-      };
+      // Block-table entries (paged K/V); the K and V streams each keep their
+      // last entry in registers (they run one tile apart).
+      int cached_pg[2] = {-1, -1}, cached_entry[2] = {0, 0};
+      const PagedGeom pgeo{p.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
       // One K tile is two 32 KB stages (d halves) in the one-CTA kernel and one
       // stage (this CTA's 64 keys) in a pair; likewise for V (key halves / this
-      // CTA's 128 columns). Boxes are 64 d wide (128-byte rows).
+      // CTA's 128 columns). A whole box is one copy; a paged box that crosses a
+      // page is one copy per piece.
       auto next_tile = [&](int n, bool is_k, int g) -> bool {
         const bool v_fix = kPaged && !is_k && n == p.v_fix_tile;
         const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
@@ -286,27 +308,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
           const uint32_t dst = stage_smem + st * kStageBytes;
           if (leader) ptx::mbar_arrive_expect_tx(bar(kBarFull + st), (kPair ? 2 : 1) * kStageBytes);
-          // Box geometry: first key, keys per box, boxes (d chunks), their stride
-          // in shared memory, first d column.
-          int r0, rows, nb, c_base;
-          uint32_t stride;
+          // Box geometry: first key, keys per box, chunks and their stride in
+          // shared memory, first chunk.
+          int r0, rows, nb, chunk0;
           if constexpr (kPair) {
             r0 = n * kBlockN + (is_k ? 64 * static_cast<int>(rank) : 0);
             rows = is_k ? 64 : 128;
             nb = is_k ? 4 : 2;
-            stride = is_k ? 8192u : 16384u;
-            c_base = is_k ? 0 : 128 * static_cast<int>(rank);
+            chunk0 = is_k ? 0 : 2 * static_cast<int>(rank);
           } else {
             r0 = n * kBlockN + (is_k ? 0 : 64 * half);
             rows = is_k ? 128 : 64;
             nb = is_k ? 2 : 4;
-            stride = is_k ? kKBoxBytes : kVBoxBytes;
-            c_base = is_k ? 128 * half : 0;
+            chunk0 = is_k ? 2 * half : 0;
           }
-          PagedRun run;
-          map_run(r0, rows, v_fix, run);
-          for (int c = 0; c < nb; ++c)
-            load_run(dst + c * stride, full, sub_map, kBarFull + st, c_base + 64 * c, g, run);
+          int row = r0;  // dense K/V: the box is the keys themselves
+          bool whole = true;
+          if constexpr (kPaged) {
+            const int sid = is_k ? 0 : 1;
+            auto read = [&](int pg) -> int {
+              if (pg != cached_pg[sid]) {
+                cached_entry[sid] = __ldg(p.block_table + pg);
+                cached_pg[sid] = pg;
+              }
+              return cached_entry[sid];
+            };
+            bool bad = false;
+            whole = paged_whole_box(pgeo, r0, rows, v_fix, read, &row, &bad);
+            if (bad) atomicExch(p.status, static_cast<int>(GQA_ERR_PAGE_TABLE));
+          }
+          if (whole) {
+            load_box(dst, full, kBarFull + st, row, g, chunk0);
+          } else if constexpr (kPaged) {
+            issue_paged_pieces<kPair>(p, sub_map, dst, kPair ? lbar(kBarFull + st) : bar(kBarFull + st),
+                                      r0, rows, nb, chunk0, g, v_fix, pol_kv);
+          }
           issued_mask |= 1u << st;
           issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
           if (++st == kStages) { st = 0; phase ^= 1u; }
@@ -351,9 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // runs on the tensor pipe while the softmax of tile j is in flight.
     if (lane == 0 && leader) {
       const uint64_t q_desc0 = ptx::smem_desc(q_smem, 16, 1024, ptx::kSwizzle128B);
-      const uint64_t k_desc0 = ptx::smem_desc(stage_smem, 16, 1024, ptx::kSwizzle128B);
-      const uint64_t v_desc0 =
-          ptx::smem_desc(stage_smem, kPair ? 16384u : kVBoxBytes, 1024, ptx::kSwizzle128B);
+      const uint64_t k_desc0 = ptx::smem_desc(stage_smem, 16, kSboK, ptx::kSwizzle128B);
+      const uint64_t v_desc0 = ptx::smem_desc(stage_smem, kLboV, kSboV, ptx::kSwizzle128B);
       uint32_t st = 0, phase = 0;
       uint32_t tile = 0;  // KV tiles this CTA has processed (global tile index T)
       bool ok = true;
@@ -372,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (T > 0 && !wait_bar(bar(kBarSFree), (T - 1) & 1u, p)) return false;
           ptx::tc_fence_after();
           if constexpr (kPair) {
-            // One stage: this CTA's 64 keys as 4 boxes (64-wide d chunks, 8 KB apart).
+            // One stage: this CTA's 64 keys x 4 chunks of 64 d.
             if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
             ptx::tc_fence_after();
             const uint64_t kd = k_desc0 + ((st * kStageBytes) >> 4);
@@ -381,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t a = q_desc0 + ((c * kQChunkBytes + 32 * kk) >> 4);
-                const uint64_t bd = kd + ((c * 8192 + 32 * kk) >> 4);
+                const uint64_t bd = kd + ((c * kChunkK + 32 * kk) >> 4);
                 ptx::mma_ss_pair(tmem + kTmemS, a, bd, kIdescQK2, (c | kk) != 0);
               }
             }
@@ -398,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                   const uint64_t a = q_desc0 + (((2 * half + c) * kQChunkBytes + 32 * kk) >> 4);
-                  const uint64_t bd = kd + ((c * kKBoxBytes + 32 * kk) >> 4);
+                  const uint64_t bd = kd + ((c * kChunkK + 32 * kk) >> 4);
                   ptx::mma_ss(tmem + kTmemS, a, bd, kIdescQK, (half | c | kk) != 0);
                 }
               }
@@ -419,40 +454,40 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j == 0 && k > 0 && !(ok = wait_bar(bar(kBarOFree), (k - 1) & 1, p))) break;
           ptx::tc_fence_after();
           // O += P_j V_j in k-steps of 16 keys, N = 256. V stages are MN-major:
-          // LBO = next 64-wide d chunk, SBO = next group of 8 keys.
+          // LBO = next 64-wide d chunk (kLboV), SBO = next group of 8 keys (kSboV).
           const bool v_fix = kPaged && w.n0 + j == p.v_fix_tile;
           if constexpr (kPair) {
-            // One stage: 128 keys x this CTA's 128 columns (2 boxes, 16 KB apart).
+            // One stage: 128 keys x this CTA's 2 chunks of 64 columns.
             if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
             ptx::tc_fence_after();
             if (v_fix) {
-              zero_v_tail(stage_smem + st * kStageBytes, 16384u, 2, 0, 128, p, false);
-              zero_v_tail(ptx::map_to_cta(stage_smem + st * kStageBytes, 1), 16384u, 2, 0, 128, p,
+              zero_v_tail(stage_smem + st * kStageBytes, kNchV, 0, kRowsV, p, false);
+              zero_v_tail(ptx::map_to_cta(stage_smem + st * kStageBytes, 1), kNchV, 0, kRowsV, p,
                           true);
               ptx::fence_proxy_async_all();
             }
             const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bd = vd + ((2048 * kk) >> 4);
+              const uint64_t bd = vd + ((2 * kSboV * kk) >> 4);  // 16 keys = two 8-key groups
               ptx::mma_ts_pair(tmem + kTmemO, tmem + kTmemP + 64u * b + 8u * kk, bd, kIdescPV2,
                                (j | kk) != 0);
             }
             commit(kBarEmpty + st);
             if (++st == kStages) { st = 0; phase ^= 1u; }
           } else {
-            // Two stages (key halves) of 4 boxes (64-wide d chunks, 8 KB apart).
+            // Two stages (key halves), each 64 keys x 4 chunks of 64 d.
             for (int half = 0; half < 2 && ok; ++half) {
               if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
               ptx::tc_fence_after();
               if (v_fix) {
-                zero_v_tail(stage_smem + st * kStageBytes, kVBoxBytes, 4, 64 * half, 64, p, false);
+                zero_v_tail(stage_smem + st * kStageBytes, kNchV, kRowsV * half, kRowsV, p, false);
                 ptx::fence_proxy_async_all();
               }
               const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bd = vd + ((2048 * kk) >> 4);
+                const uint64_t bd = vd + ((2 * kSboV * kk) >> 4);  // 16 keys = two 8-key groups
                 const uint32_t a_tmem = tmem + kTmemP + 64u * b + 32u * half + 8u * kk;
                 ptx::mma_ts(tmem + kTmemO, a_tmem, bd, kIdescPV, (j | half | kk) != 0);
               }

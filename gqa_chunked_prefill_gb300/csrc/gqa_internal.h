@@ -23,8 +23,12 @@ constexpr int kThreads = 192;  // 4 softmax warps, 1 TMA warp, 1 MMA warp
 
 struct FwdParams {
   CUtensorMap tmap_q;  // Q [q_len][24][256], box (64 d, 6 heads, 21 tokens), 128B swizzle
-  CUtensorMap tmap_k;  // K [kv_len][4][256], box (64 d, 1 head, 128 keys; 64 keys for pairs)
-  CUtensorMap tmap_v;  // V [kv_len][4][256], box (64 d, 1 head, 64 keys; 128 keys for pairs)
+  // K, V boxes of one stage (per CTA): K 128 keys x 2 chunks of 64 d (pairs: 64 x 4),
+  // V 64 keys x 4 chunks (pairs: 128 x 2). Dense K/V [kv_len][4][256]: 4-D maps
+  // (64 d, key, head, chunk); paged caches: 5-D maps (64 d, key % 8, chunk, key / 8,
+  // head) over all num_pages * page_size rows (stage layouts: attn_fwd_sm103.cu).
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
   __nv_bfloat16* out;  // [q_len][24][256]
   float* lse;          // [q_len][24] natural log, or null
   float* part_o;       // [tail pieces][128 rows][256] normalised partial O (tail_splits > 1)
@@ -40,12 +44,11 @@ struct FwdParams {
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
   int withhold_q;      // test only: the producer never loads the first Q tile
-  // Paged K/V (kernels instantiated with kPaged only): tmap_k / tmap_v then span
-  // the whole cache [num_pages * page_size][4][256] and key j of the sequence is
-  // cache row block_table[j / page_size] * page_size + j % page_size.
-  CUtensorMap tmap_k_sub;    // box (64 d, 1 head, sub_rows keys): boxes that cross a page
-  CUtensorMap tmap_v_sub;
-  CUtensorMap tmap_v16;      // box (64 d, 1 head, 16 keys): V of the tile holding key kv_len-1
+  // Paged K/V (kernels instantiated with kPaged only): key j of the sequence is
+  // cache row block_table[j / page_size] * page_size + j % page_size (gqa_paged.h).
+  CUtensorMap tmap_k_sub;    // 5-D, sub_rows keys x the stage's chunks: pieces of a box
+  CUtensorMap tmap_v_sub;    //   that crosses a page
+  CUtensorMap tmap_v16;      // 5-D, 16 keys: V of the tile holding key kv_len-1
   const int* block_table;    // [ceil(kv_len / page_size)] physical page of each logical page
   int page_size;             // keys per page, a multiple of 16
   int num_pages;             // pages in the cache

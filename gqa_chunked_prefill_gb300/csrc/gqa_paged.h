@@ -38,6 +38,25 @@ struct PagedRun {
   bool bad;    // a block-table entry outside [0, num_pages) was met (read as zeros)
 };
 
+// The common case of map_paged_run, kept apart so that a kernel can inline it
+// and call the rest out of line: true when the box is one copy — it starts at
+// or past kv_len (row = oob_row) or lies inside one page (row = its cache row,
+// or oob_row with *bad set if that page's entry is outside the cache).
+template <typename Read>
+__host__ __device__ inline bool paged_whole_box(const PagedGeom& g, int r0, int rows, bool v_fix,
+                                                Read&& read, int* row, bool* bad) {
+  *row = g.oob_row;
+  *bad = false;
+  if (r0 >= g.kv_len) return true;  // the whole box lies past the sequence: zero fill
+  const int pg0 = r0 / g.page_size;
+  const int off0 = r0 - pg0 * g.page_size;
+  if (v_fix || off0 + rows > g.page_size) return false;
+  const int e = read(pg0);
+  if (e >= 0 && e < g.num_pages) *row = e * g.page_size + off0;
+  else *bad = true;
+  return true;
+}
+
 // Maps the box of `rows` keys (64 or 128) that starts at logical key r0.
 // `read(pg)` returns block-table entry pg; it is called only for pages that
 // hold a key below kv_len.
@@ -46,17 +65,9 @@ __host__ __device__ inline void map_paged_run(const PagedGeom& g, int r0, int ro
                                               Read&& read, PagedRun& run) {
   run.n = 0;
   run.sub = rows;
-  run.bad = false;
-  run.row[0] = g.oob_row;
-  if (r0 >= g.kv_len) return;  // the whole box lies past the sequence: zero fill
+  if (paged_whole_box(g, r0, rows, v_fix, read, &run.row[0], &run.bad)) return;
   const int pg0 = r0 / g.page_size;
   const int off0 = r0 - pg0 * g.page_size;
-  if (!v_fix && off0 + rows <= g.page_size) {
-    const int e = read(pg0);
-    if (e >= 0 && e < g.num_pages) run.row[0] = e * g.page_size + off0;
-    else run.bad = true;
-    return;
-  }
   run.sub = v_fix ? 16 : g.sub_rows;
   run.n = rows / run.sub;
   int ent[8];

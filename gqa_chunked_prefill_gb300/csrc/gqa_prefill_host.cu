@@ -270,6 +270,47 @@ bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// K or V [rows][4 heads][256] as a 4-D tensor (64 d, row, head, 64-column
+// chunk) with the chunk outermost, so that one box of (64, box_rows, 1,
+// box_chunks) lands in shared memory chunk-major: chunk c's box_rows rows of
+// 128 bytes at c * box_rows * 128, as the MMA descriptors read them.
+bool encode_kv(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows,
+               uint32_t box_chunks) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {64, rows, static_cast<cuuint64_t>(kKvHeads), kHeadDim / 64};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kKvHeads) * kHeadDim * 2,  // next key
+                                 kHeadDim * 2,                                         // next head
+                                 64 * 2};                                              // next chunk
+  const cuuint32_t box[4] = {64, box_rows, 1, box_chunks};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A paged K or V cache [rows][4 heads][256] (rows a multiple of 16) as a 5-D
+// tensor (64 d, key % 8, 64-column chunk, key / 8, head): one box of (64, 8,
+// box_chunks, box_rows / 8, 1) lands in shared memory as 8-key groups, each
+// holding its box_chunks chunks of 8 rows x 128 bytes — the paged stage layout
+// of the attention kernel, in which a piece of whole 8-key groups is contiguous.
+bool encode_kv_paged(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows,
+                     uint32_t box_chunks) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(kKvHeads) * kHeadDim * 2;
+  const cuuint64_t dims[5] = {64, 8, kHeadDim / 64, rows / 8, static_cast<cuuint64_t>(kKvHeads)};
+  const cuuint64_t strides[4] = {row_bytes,       // next key in the group
+                                 64 * 2,          // next chunk
+                                 8 * row_bytes,   // next group of 8 keys
+                                 kHeadDim * 2};   // next head
+  const cuuint32_t box[5] = {64, 8, box_chunks, box_rows / 8, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Checks every argument; on success fills *plan (q_len == 0 gives an empty plan).
 gqa_status check_call(const void* q, const void* k, const void* v, const void* out,
                       const float* lse, int q_len, int kv_len, int n_q_heads, int n_kv_heads,
@@ -320,22 +361,30 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* 
   std::memset(&p, 0, sizeof(p));
   const uint64_t kv_rows = pkv ? static_cast<uint64_t>(pkv->num_pages) * pkv->page_size
                                : static_cast<uint64_t>(kv_len);
+  // K/V stages: one-CTA K 128 keys x 2 chunks, V 64 keys x 4 chunks; pairs
+  // K 64 x 4, V 128 x 2 (per CTA).
+  const uint32_t k_rows = pair ? 64 : kBlockN, k_chunks = pair ? 4 : 2;
+  const uint32_t v_rows = pair ? kBlockN : 64, v_chunks = pair ? 2 : 4;
   if (!encode_3d(&p.tmap_q, q, kHeadDim, kQHeads, static_cast<uint64_t>(q_len), 64, kGroup,
-                 kTokPerTile) ||
-      !encode_3d(&p.tmap_k, k, kHeadDim, kKvHeads, kv_rows, 64, 1, pair ? 64 : kBlockN) ||
-      !encode_3d(&p.tmap_v, v, kHeadDim, kKvHeads, kv_rows, 64, 1, pair ? kBlockN : 64))
+                 kTokPerTile))
     return GQA_ERR_CUDA;
   p.v_fix_tile = -1;
-  if (pkv) {
-    const int sub = gcd_int(pkv->page_size, 64);  // 16, 32 or 64: divides pages and boxes
-    if (!encode_3d(&p.tmap_k_sub, k, kHeadDim, kKvHeads, kv_rows, 64, 1, sub) ||
-        !encode_3d(&p.tmap_v_sub, v, kHeadDim, kKvHeads, kv_rows, 64, 1, sub) ||
-        !encode_3d(&p.tmap_v16, v, kHeadDim, kKvHeads, kv_rows, 64, 1, 16))
+  if (!pkv) {
+    if (!encode_kv(&p.tmap_k, k, kv_rows, k_rows, k_chunks) ||
+        !encode_kv(&p.tmap_v, v, kv_rows, v_rows, v_chunks))
+      return GQA_ERR_CUDA;
+  } else {
+    const uint32_t sub = static_cast<uint32_t>(gcd_int(pkv->page_size, 64));  // 16, 32 or 64
+    if (!encode_kv_paged(&p.tmap_k, k, kv_rows, k_rows, k_chunks) ||
+        !encode_kv_paged(&p.tmap_v, v, kv_rows, v_rows, v_chunks) ||
+        !encode_kv_paged(&p.tmap_k_sub, k, kv_rows, sub, k_chunks) ||
+        !encode_kv_paged(&p.tmap_v_sub, v, kv_rows, sub, v_chunks) ||
+        !encode_kv_paged(&p.tmap_v16, v, kv_rows, 16, v_chunks))
       return GQA_ERR_CUDA;
     p.block_table = pkv->block_table;
     p.page_size = pkv->page_size;
     p.num_pages = pkv->num_pages;
-    p.sub_rows = sub;
+    p.sub_rows = static_cast<int>(sub);
     p.oob_row = static_cast<int>(kv_rows);
     if (kv_len % kBlockN != 0) p.v_fix_tile = (kv_len - 1) / kBlockN;
   }
