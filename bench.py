@@ -52,8 +52,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # source it was measured on; reported as null once the source no longer matches.
 KNOWN_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the full launch:
-    # 791.91 MB read + 51.94 MB written.
-    "q4096_kv32768": {"bytes": 843_850_000, "kernel_sha256": "c316c13334216b03e1d2ef522c13b9e651c09aba2a2e95e1aa765a635504cb4e"},
+    # 794.00 MB read + 52.37 MB written.
+    "q4096_kv32768": {"bytes": 846_370_000, "kernel_sha256": "3d0f897a363fb3708a08df0bbed39ea6554842f8c962e50307c5a74fe2619e24"},
 }
 
 
