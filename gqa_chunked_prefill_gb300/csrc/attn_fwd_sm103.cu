@@ -681,12 +681,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Combine the S pieces of every split (tail) item: blocks (j, *) merge item
 // head_items + j, 32 rows each, from slots j*S .. j*S + S-1 (each slot holds one
-// 128-row block per CTA of the item), in that fixed order:
-// lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s. One warp per row.
+// 128-row block per CTA of the item):
+// lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s. One warp per row:
+// lane s reads piece s's LSE (32 pieces per pass), the warp reduces max and
+// sum by shuffles, then every lane accumulates its 8 columns over the pieces
+// in order s = 0, 1, ... with independent loads (unrolled), so a row costs a
+// few memory latencies, not S of them. Deterministic: fixed order throughout.
 constexpr int kMergeRowsPerBlock = 32;  // 8 warps x 4 rows
 
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
 __global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
-  const int j = blockIdx.x;                           // tail item
+  const int j = blockIdx.x;                               // tail item
   const int row_begin = blockIdx.y * kMergeRowsPerBlock;  // its rows, both CTAs of a pair
   const int item = p.head_items + j;
   const int qt = p.n_qtiles - 1 - item / 4;
@@ -700,20 +715,29 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
     const int row = rr % (kTokPerTile * kGroup);  // its MMA row
     const int tok = kTokPerTile * (cpi * qt + r) + row / kGroup;
     if (tok >= p.q_len) continue;
+    // Partial row of piece s: slot (j*S + s), CTA r, MMA row `row`.
+    auto prow = [&](int s) {
+      return (static_cast<size_t>(j * S + s) * cpi + r) * kRowsPerTile + row;
+    };
     float mx = kNegInf;
-    for (int s = 0; s < S; ++s)
-      mx = fmaxf(mx, p.part_lse[(static_cast<size_t>(j * S + s) * cpi + r) * kRowsPerTile + row]);
+    for (int s0 = 0; s0 < S; s0 += 32)
+      if (s0 + lane < S) mx = fmaxf(mx, p.part_lse[prow(s0 + lane)]);
+    mx = warp_max(mx);
     const float m_use = (mx == kNegInf) ? 0.0f : mx;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float wsum = 0.0f;
-    for (int s = 0; s < S; ++s) {
-      const size_t prow = (static_cast<size_t>(j * S + s) * cpi + r) * kRowsPerTile + row;
-      const float w = ptx::ex2_approx(p.part_lse[prow] - m_use);
-      wsum += w;
-      const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * kHeadDim + 8 * lane);
-      const float4 a = src[0], c = src[1];
-      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-      acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int n = min(32, S - s0);
+      const float w_lane = lane < n ? ptx::ex2_approx(p.part_lse[prow(s0 + lane)] - m_use) : 0.0f;
+      wsum += warp_sum(w_lane);
+#pragma unroll 8
+      for (int i = 0; i < n; ++i) {
+        const float w = __shfl_sync(0xffffffffu, w_lane, i);
+        const float4* src = reinterpret_cast<const float4*>(p.part_o + prow(s0 + i) * kHeadDim + 8 * lane);
+        const float4 a = src[0], c = src[1];
+        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+        acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+      }
     }
     const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
     uint4 o;

@@ -41,7 +41,7 @@ constexpr double kPairTileUs = 1.35;
 constexpr double kMergeBytesPerUs = 3.0e6;   // effective bandwidth of the merge pass
 constexpr double kMergeLaunchUs = 6.0;
 constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
-constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16};
+constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 24, 32};
 
 Geometry geometry(int q_len, int kv_len, int variant) {
   const int tpi = variant == 2 ? 2 * kTokPerTile : kTokPerTile;

@@ -114,3 +114,18 @@ def test_lse_may_be_null(cuda_device):
     out_a, _, _ = run_gpu(q, k, v, SCALE, with_lse=False)
     out_b, _, _ = run_gpu(q, k, v, SCALE, with_lse=True)
     assert torch.equal(out_a, out_b)
+
+
+@pytest.mark.parametrize("q_len", [1, 2, 3, 4])
+@pytest.mark.parametrize("kv_len", [4096, 32768])
+@pytest.mark.parametrize("splits,variant", [(0, 0), (32, 1), (24, 2), (5, 1)])
+def test_decode_shapes_every_element(cuda_device, q_len, kv_len, splits, variant):
+    """Decode-sized chunks (one to four new tokens, 6 to 24 live MMA rows) over a long
+    prefix: the whole KV range is cut into many pieces and merged."""
+    q, k, v = make_qkv(q_len, kv_len, seed=17 * q_len + kv_len)
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_variant=variant)
+    if splits:
+        assert plan["tail_splits"] == splits and plan["kernels_per_call"] == 2
+    ref_o, ref_l = oracle.attention(q, k, v, SCALE)
+    check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
+                f"decode {q_len}x{kv_len} S {splits}")
