@@ -66,7 +66,7 @@ def test_noalloc_refuses_partials_larger_than_scratch(cuda_device):
     import gqa_chunked_prefill_gb300 as gqa
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     big = None
-    for q_len, kv_len in ((4096, 32768), (4096, 16384), (2048, 65536), (4096, 65536)):
+    for q_len, kv_len in ((4096, 32768), (4096, 16384), (2048, 65536), (4096, 65536), (168, 262144)):
         _, plan = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms)
         if plan["workspace_bytes"] > SCRATCH_BYTES:
             big = (q_len, kv_len)
