@@ -72,6 +72,16 @@ lib.gqa_prefill_attn_paged.restype = _i
 lib.gqa_prefill_attn_paged_ex.argtypes = _PAGED_ARGS + [ctypes.POINTER(PrefillOpts),
                                                         ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_attn_paged_ex.restype = _i
+lib.gqa_quantize_q_fp8.argtypes = [_vp, _vp, _vp, _i, _i, _i, _vp]
+lib.gqa_quantize_q_fp8.restype = _i
+lib.gqa_quantize_k_fp8.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp]
+lib.gqa_quantize_k_fp8.restype = _i
+_FP8_ARGS = [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
+lib.gqa_prefill_attn_fp8qk.argtypes = _FP8_ARGS
+lib.gqa_prefill_attn_fp8qk.restype = _i
+lib.gqa_prefill_attn_fp8qk_ex.argtypes = _FP8_ARGS + [ctypes.POINTER(PrefillOpts),
+                                                      ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_attn_fp8qk_ex.restype = _i
 lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
                                       ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan.restype = _i
@@ -183,6 +193,53 @@ def gqa_prefill_attn_paged_ex(q, k_cache, v_cache, block_table, num_pages, page_
                                        num_pages, page_size, _ptr(out), _ptr(lse), q_len, kv_len,
                                        n_q_heads, n_kv_heads, head_dim, scale, _stream(stream),
                                        ctypes.byref(opts), ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def gqa_quantize_q_fp8(q, q_fp8, q_scale, q_len, n_q_heads, head_dim, stream=None,
+                       check=True) -> int:
+    """E4M3 codes [q_len, 24, 256] (uint8) and FP32 scales [q_len, 24] of BF16 q."""
+    rc = lib.gqa_quantize_q_fp8(_ptr(q), _ptr(q_fp8), _ptr(q_scale), q_len, n_q_heads, head_dim,
+                                _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_quantize_k_fp8(k, k_fp8, k_scale, kv_len, n_kv_heads, head_dim, k_scale_stride,
+                       stream=None, check=True) -> int:
+    """E4M3 codes [kv_len, 4, 256] (uint8) and FP32 scales [4, k_scale_stride] of BF16 k."""
+    rc = lib.gqa_quantize_k_fp8(_ptr(k), _ptr(k_fp8), _ptr(k_scale), kv_len, n_kv_heads,
+                                head_dim, k_scale_stride, _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_prefill_attn_fp8qk(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v, out, lse, q_len,
+                           kv_len, n_q_heads, n_kv_heads, head_dim, scale, stream=None,
+                           check=True) -> int:
+    rc = lib.gqa_prefill_attn_fp8qk(_ptr(q_fp8), _ptr(q_scale), _ptr(k_fp8), _ptr(k_scale),
+                                    k_scale_stride, _ptr(v), _ptr(out), _ptr(lse), q_len, kv_len,
+                                    n_q_heads, n_kv_heads, head_dim, scale, _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_prefill_attn_fp8qk_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v, out, lse, q_len,
+                              kv_len, n_q_heads, n_kv_heads, head_dim, scale, stream=None,
+                              force_splits=0, force_grid=0, force_variant=0, wait_timeout_us=0,
+                              fwd_events=None, test_withhold_q=False, check=True):
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
+                 test_withhold_q)
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_attn_fp8qk_ex(_ptr(q_fp8), _ptr(q_scale), _ptr(k_fp8), _ptr(k_scale),
+                                       k_scale_stride, _ptr(v), _ptr(out), _ptr(lse), q_len,
+                                       kv_len, n_q_heads, n_kv_heads, head_dim, scale,
+                                       _stream(stream), ctypes.byref(opts), ctypes.byref(plan))
     if check:
         _check(rc)
     return rc, plan.as_dict()

@@ -82,8 +82,15 @@ enum BarId : uint32_t {
   kBarPvDone1,
   kBarOFree,                    // epilogue finished reading O (128 arrivals)
   kBarDrain,                    // MMA warp's final drain
-  kNumBars
+  kBarScFull,                   // [kScSlots] FP8 QK^T: key scales of a tile loaded (TMA tx)
+  kBarScEmpty = kBarScFull + 8, // [kScSlots] this CTA's softmax done with them (128 arrivals)
+  kNumBars = kBarScEmpty + 8
 };
+// FP8 QK^T: Q codes take 2 of the 4 Q chunks; the key-scale ring (one 128-key
+// FP32 row per slot, consumed by the softmax warps) lives in the other half.
+constexpr int kScSlots = 8;
+constexpr uint32_t kScSlotBytes = 128 * 4;
+constexpr uint32_t kOffScales = kOffQ + 2 * kQChunkBytes;
 constexpr uint32_t kOffTmemSlot = kOffBars + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffTmemSlot + 16;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base up to 1024
@@ -92,6 +99,8 @@ constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
 constexpr uint32_t kIdescQK2 = ptx::idesc_bf16_f32(256, 128, false, false);  // CTA pair
 constexpr uint32_t kIdescPV2 = ptx::idesc_bf16_f32(256, 256, false, true);   // CTA pair
+constexpr uint32_t kIdescQK8 = ptx::idesc_e4m3_f32(128, 128);                 // FP8 QK^T
+constexpr uint32_t kIdescQK82 = ptx::idesc_e4m3_f32(256, 128);                // FP8, pair
 
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
@@ -168,7 +177,12 @@ __device__ __noinline__ void issue_paged_pieces(const FwdParams& p, const CUtens
 // copies of both CTAs complete on the leader's barriers; MMA completions are
 // multicast to both CTAs; the peer's softmax warps arrive on the leader's
 // barriers remotely.
-template <bool kPair, bool kPaged>
+//
+// kFp8 = true: quantised QK^T (gfx936 DCU上实现INT8 QK MMAC, §1): Q and K are E4M3
+// codes with one FP32 scale per query (token, head) and per key (token, KV
+// head); S = Q_q K_q^T is a kind::f8f6f4 MMA, and every score is restored as
+// S * s_q * s_k * scale before the softmax. PV stays BF16.
+template <bool kPair, bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -200,14 +214,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // paged box that crosses a page is cut into — is contiguous and one 5-D
   // copy. Both are uniform strides for the MMA descriptors: K rows 8 apart at
   // kSboK, next chunk at kChunkK; V next chunk at kLboV, next 8 keys at kSboV.
-  constexpr uint32_t kNchK = kPair ? 4 : 2;      // chunks per K stage
-  constexpr uint32_t kNchV = kPair ? 2 : 4;      // chunks per V stage
+  // Q and K rows hold 64 BF16 or 128 FP8 values per 128-byte chunk.
+  constexpr int kQChunks = kFp8 ? 2 : 4;
+  constexpr int kChunkElems = kFp8 ? 128 : 64;
+  constexpr int kKStagesPerTile = (kFp8 || kPair) ? 1 : 2;
+  constexpr uint32_t kNchK = kFp8 ? 2 : (kPair ? 4 : 2);  // chunks per K stage
+  constexpr uint32_t kNchV = kPair ? 2 : 4;               // chunks per V stage
   constexpr uint32_t kRowsK = kPair ? 64 : 128;  // keys per K stage
   constexpr uint32_t kRowsV = kPair ? 128 : 64;  // keys per V stage
   constexpr uint32_t kChunkK = kPaged ? 1024u : kRowsK * 128u;
   constexpr uint32_t kSboK = kPaged ? kNchK * 1024u : 1024u;
   constexpr uint32_t kLboV = kPaged ? 1024u : kRowsV * 128u;
   constexpr uint32_t kSboV = kPaged ? kNchV * 1024u : 1024u;
+  constexpr uint32_t kKStageBytes = kRowsK * kNchK * 128u;  // K bytes per stage per CTA
 
   // ---- set-up: barriers, idle Q rows, tensor memory -------------------------
   if (threadIdx.x == 0) {
@@ -225,11 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(kBarPvDone1), 1);
     ptx::mbar_init(bar(kBarOFree), kConsumers);
     ptx::mbar_init(bar(kBarDrain), 1);
+    if constexpr (kFp8) {
+      for (int i = 0; i < kScSlots; ++i) {
+        ptx::mbar_init(bar(kBarScFull + i), 1);
+        ptx::mbar_init(bar(kBarScEmpty + i), 4 * 32);  // this CTA's softmax threads
+      }
+    }
     ptx::fence_mbar_init();
   }
   if (warp < 4) {
     // Rows 126 and 127 of each Q chunk are never written by TMA: zero them once.
-    for (int i = threadIdx.x; i < 4 * 2 * 128 / 16; i += 128) {
+    for (int i = threadIdx.x; i < kQChunks * 2 * 128 / 16; i += 128) {
       const int chunk = i / 16, off = (i % 16) * 16;
       *reinterpret_cast<uint4*>(smem + kOffQ + chunk * kQChunkBytes + kQBoxBytes + off) =
           make_uint4(0, 0, 0, 0);
@@ -263,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&p.tmap_q);
       ptx::prefetch_tmap(&p.tmap_k);
       ptx::prefetch_tmap(&p.tmap_v);
+      if constexpr (kFp8) ptx::prefetch_tmap(&p.tmap_ks);
       if constexpr (kPaged) {
         ptx::prefetch_tmap(&p.tmap_k_sub);
         ptx::prefetch_tmap(&p.tmap_v_sub);
@@ -272,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_q = ptx::policy_evict_first();
       uint32_t st = 0, phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load issued / its phase
+      uint32_t sc_count = 0, sc_issued_mask = 0, sc_issued_parity = 0;  // FP8 key-scale ring
       bool q_issued = false;
       uint32_t q_parity = 0;
       bool ok = true;
@@ -304,23 +331,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool v_fix = kPaged && !is_k && n == p.v_fix_tile;
         const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
         const CUtensorMap* sub_map = is_k ? &p.tmap_k_sub : (v_fix ? &p.tmap_v16 : &p.tmap_v_sub);
-        for (int half = 0; half < (kPair ? 1 : 2); ++half) {
+        const int halves = is_k ? kKStagesPerTile : (kPair ? 1 : 2);
+        for (int half = 0; half < halves; ++half) {
           if (!wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
           const uint32_t dst = stage_smem + st * kStageBytes;
-          if (leader) ptx::mbar_arrive_expect_tx(bar(kBarFull + st), (kPair ? 2 : 1) * kStageBytes);
+          const uint32_t bytes = is_k ? kKStageBytes : kStageBytes;  // per CTA
+          if (leader) ptx::mbar_arrive_expect_tx(bar(kBarFull + st), (kPair ? 2 : 1) * bytes);
           // Box geometry: first key, keys per box, chunks and their stride in
           // shared memory, first chunk.
           int r0, rows, nb, chunk0;
           if constexpr (kPair) {
             r0 = n * kBlockN + (is_k ? 64 * static_cast<int>(rank) : 0);
             rows = is_k ? 64 : 128;
-            nb = is_k ? 4 : 2;
+            nb = is_k ? static_cast<int>(kNchK) : 2;
             chunk0 = is_k ? 0 : 2 * static_cast<int>(rank);
           } else {
             r0 = n * kBlockN + (is_k ? 0 : 64 * half);
             rows = is_k ? 128 : 64;
-            nb = is_k ? 2 : 4;
-            chunk0 = is_k ? 2 * half : 0;
+            nb = is_k ? static_cast<int>(kNchK) : 4;
+            chunk0 = is_k ? static_cast<int>(kNchK) * half : 0;
           }
           int row = r0;  // dense K/V: the box is the keys themselves
           bool whole = true;
@@ -347,6 +376,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
           if (++st == kStages) { st = 0; phase ^= 1u; }
         }
+        if constexpr (kFp8) {
+          if (is_k) {
+            // The tile's 128 key scales of group g, for this CTA's softmax warps
+            // (each CTA of a pair loads its own copy on its own barrier).
+            const uint32_t slot = sc_count % kScSlots, use = sc_count / kScSlots;
+            if (use > 0 && !wait_bar(bar(kBarScEmpty + slot), (use - 1) & 1u, p)) return false;
+            ptx::mbar_arrive_expect_tx(bar(kBarScFull + slot), kScSlotBytes);
+            ptx::tma_load_2d(base + kOffScales + slot * kScSlotBytes, &p.tmap_ks,
+                             bar(kBarScFull + slot), n * kBlockN, g, pol_kv);
+            sc_issued_mask |= 1u << slot;
+            sc_issued_parity = (sc_issued_parity & ~(1u << slot)) | ((use & 1u) << slot);
+            ++sc_count;
+          }
+        }
         return true;
       };
       int k = 0;
@@ -354,9 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && pieces.next(w)) {
         if (k > 0 && !(ok = wait_bar(bar(kBarQEmpty), (k - 1) & 1, p))) break;
         if (!(p.withhold_q && k == 0)) {
-          if (leader) ptx::mbar_arrive_expect_tx(bar(kBarQFull), (kPair ? 2 : 1) * 4 * kQBoxBytes);
-          for (int c = 0; c < 4; ++c)
-            load(q_smem + c * kQChunkBytes, &p.tmap_q, kBarQFull, 64 * c, kGroup * w.g,
+          if (leader)
+            ptx::mbar_arrive_expect_tx(bar(kBarQFull), (kPair ? 2 : 1) * kQChunks * kQBoxBytes);
+          for (int c = 0; c < kQChunks; ++c)
+            load(q_smem + c * kQChunkBytes, &p.tmap_q, kBarQFull, kChunkElems * c, kGroup * w.g,
                  tpi * w.qt + kTokPerTile * static_cast<int>(rank), pol_q);
           q_issued = true;
           q_parity = k & 1;
@@ -378,6 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s)
           if (issued_mask & (1u << s)) wait_bar(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
         if (q_issued) wait_bar(bar(kBarQFull), q_parity, p);
+      }
+      if constexpr (kFp8) {  // key scales complete on each CTA's own barriers
+        for (int s = 0; s < kScSlots; ++s)
+          if (sc_issued_mask & (1u << s))
+            wait_bar(bar(kBarScFull + s), (sc_issued_parity >> s) & 1u, p);
       }
     }
     __syncwarp();
@@ -406,40 +455,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S may be overwritten once the softmax holds tile T-1's scores in registers.
           if (T > 0 && !wait_bar(bar(kBarSFree), (T - 1) & 1u, p)) return false;
           ptx::tc_fence_after();
-          if constexpr (kPair) {
-            // One stage: this CTA's 64 keys x 4 chunks of 64 d.
+          // K arrives as kKStagesPerTile stages of kNchK 128-byte chunks (one-CTA
+          // BF16: two d halves; pairs and FP8: one stage); every MMA advances
+          // 32 bytes along d (16 BF16 or 32 FP8 values).
+#pragma unroll
+          for (int half = 0; half < kKStagesPerTile; ++half) {
             if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
             ptx::tc_fence_after();
             const uint64_t kd = k_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < static_cast<int>(kNchK); ++c) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = q_desc0 + ((c * kQChunkBytes + 32 * kk) >> 4);
+                const uint64_t a =
+                    q_desc0 + (((half * kNchK + c) * kQChunkBytes + 32 * kk) >> 4);
                 const uint64_t bd = kd + ((c * kChunkK + 32 * kk) >> 4);
-                ptx::mma_ss_pair(tmem + kTmemS, a, bd, kIdescQK2, (c | kk) != 0);
+                const uint32_t acc = (half | c | kk) != 0;
+                if constexpr (kFp8) {
+                  if constexpr (kPair) ptx::mma_ss_f8_pair(tmem + kTmemS, a, bd, kIdescQK82, acc);
+                  else ptx::mma_ss_f8(tmem + kTmemS, a, bd, kIdescQK8, acc);
+                } else {
+                  if constexpr (kPair) ptx::mma_ss_pair(tmem + kTmemS, a, bd, kIdescQK2, acc);
+                  else ptx::mma_ss(tmem + kTmemS, a, bd, kIdescQK, acc);
+                }
               }
             }
             commit(kBarEmpty + st);
             if (++st == kStages) { st = 0; phase ^= 1u; }
-          } else {
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
-              ptx::tc_fence_after();
-              const uint64_t kd = k_desc0 + ((st * kStageBytes) >> 4);
-#pragma unroll
-              for (int c = 0; c < 2; ++c) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t a = q_desc0 + (((2 * half + c) * kQChunkBytes + 32 * kk) >> 4);
-                  const uint64_t bd = kd + ((c * kChunkK + 32 * kk) >> 4);
-                  ptx::mma_ss(tmem + kTmemS, a, bd, kIdescQK, (half | c | kk) != 0);
-                }
-              }
-              commit(kBarEmpty + st);
-              if (++st == kStages) { st = 0; phase ^= 1u; }
-            }
           }
           commit(kBarSFull);
           if (j == nt - 1) commit(kBarQEmpty);
@@ -524,6 +566,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = row < kTokPerTile * kGroup && tok < p.q_len;
       const int pos = p.p0 + tok;            // last key this row may see
       const int tile_min_pos = p.p0 + tok0;  // smallest such key among this CTA's rows
+      // Score -> base-2 exponent factor: scale * log2(e), times the query's scale
+      // for FP8 QK^T (the key's scale is applied per column below).
+      float rowfac = sl2;
+      if constexpr (kFp8) {
+        if (valid) rowfac = sl2 * __ldg(p.q_scale + static_cast<size_t>(tok) * kQHeads + kGroup * w.g + hj);
+      }
       float m_ref = kNegInf;  // max used in the exponent (base-2, scaled)
       float l = 0.0f;         // running row sum of p
       for (int j = 0; j < nt; ++j) {
@@ -539,6 +587,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        if constexpr (kFp8) {
+          // Restore each key's scale before the softmax (the report's §1: scales
+          // change the relative probabilities, so they cannot wait until after).
+          const uint32_t slot = T % kScSlots;
+          ok = __all_sync(0xffffffffu, wait_bar(bar(kBarScFull + slot), (T / kScSlots) & 1u, p));
+          if (!ok) break;
+          const float4* ks = reinterpret_cast<const float4*>(smem + kOffScales + slot * kScSlotBytes);
+#pragma unroll
+          for (int c = 0; c < 128; c += 4) {
+            const float4 k4 = ks[c / 4];
+            float a0, a1, a2, a3;
+            ptx::f32x2_split(ptx::mul_f32x2(ptx::f32x2(s[c], s[c + 1]), ptx::f32x2(k4.x, k4.y)), a0, a1);
+            ptx::f32x2_split(ptx::mul_f32x2(ptx::f32x2(s[c + 2], s[c + 3]), ptx::f32x2(k4.z, k4.w)), a2, a3);
+            s[c] = a0;
+            s[c + 1] = a1;
+            s[c + 2] = a2;
+            s[c + 3] = a3;
+          }
+          ptx::mbar_arrive(bar(kBarScEmpty + slot));
+        }
         const int key0 = (w.n0 + j) * kBlockN;
         if (key0 + kBlockN - 1 > tile_min_pos) {
           // Diagonal tile: keys after this row's position are masked out.
@@ -554,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
           mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
         }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * rowfac;
         const float m_new = fmaxf(m_ref, m_tile);
         const bool need = m_new > m_ref + kRescaleThreshold;
         if (j == 0) {
@@ -581,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_use = (m_ref == kNegInf) ? 0.0f : m_ref;
         uint32_t pk[64];
         // p = 2^(s*scale*log2e - m): one packed FMA per pair, two ex2, one packed add.
-        const uint64_t scale2 = ptx::f32x2(sl2, sl2);
+        const uint64_t scale2 = ptx::f32x2(rowfac, rowfac);
         const uint64_t neg_m2 = ptx::f32x2(-m_use, -m_use);
         uint64_t sum2 = ptx::f32x2(0.0f, 0.0f);
 #pragma unroll
@@ -758,10 +826,12 @@ size_t fwd_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t prepare_fwd_kernel() {
   const void* kernels[] = {
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true>)};
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, false>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, false>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true, false>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true, false>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, true>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, true>)};
   for (const void* f : kernels) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(kSmemAlloc));
@@ -790,19 +860,24 @@ cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribut
 cudaError_t max_active_pairs(int* pairs) {
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
-  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, false>, &cfg);
+  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, false, false>, &cfg);
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, cudaStream_t stream) {
+// Paged K/V with FP8 QK^T is not instantiated (the host refuses it first).
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, bool fp8,
+                       cudaStream_t stream) {
+  if (paged && fp8) return cudaErrorInvalidValue;
   if (!pair) {
-    if (paged) gqa_attn_fwd_sm103_kernel<false, true><<<grid, kThreads, kSmemAlloc, stream>>>(p);
-    else gqa_attn_fwd_sm103_kernel<false, false><<<grid, kThreads, kSmemAlloc, stream>>>(p);
+    if (fp8) gqa_attn_fwd_sm103_kernel<false, false, true><<<grid, kThreads, kSmemAlloc, stream>>>(p);
+    else if (paged) gqa_attn_fwd_sm103_kernel<false, true, false><<<grid, kThreads, kSmemAlloc, stream>>>(p);
+    else gqa_attn_fwd_sm103_kernel<false, false, false><<<grid, kThreads, kSmemAlloc, stream>>>(p);
     return cudaGetLastError();
   }
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
-  return paged ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true>, p)
-               : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false>, p);
+  if (fp8) return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, true>, p);
+  return paged ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, false>, p)
+               : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, false>, p);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {

@@ -55,6 +55,10 @@ struct FwdParams {
   int sub_rows;              // gcd(page_size, 64)
   int oob_row;               // num_pages * page_size: a row past the cache (TMA zero fill)
   int v_fix_tile;            // KV tile holding key kv_len-1 if kv_len % 128 != 0, else -1
+  // FP8 QK^T (kernels instantiated with kFp8 only): tmap_q / tmap_k hold E4M3 codes
+  // (Q box (128, 6 heads, 21 tokens); K 4-D (128, key, head, chunk) with 2 chunks).
+  CUtensorMap tmap_ks;       // key scales FP32 [4][k_scale_stride], box (128 keys, 1 head)
+  const float* q_scale;      // [q_len][24] FP32 query scales
 };
 
 struct MergeParams {
@@ -72,7 +76,11 @@ struct MergeParams {
 
 size_t fwd_smem_bytes();
 // grid = CTAs; with pair = true the CTAs form clusters of two (grid even).
-cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, cudaStream_t stream);
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, bool fp8,
+                       cudaStream_t stream);
+// E4M3 codes and scales of rows x heads vectors of 256 BF16 values (quantize_fp8.cu).
+cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scale, int rows, int heads,
+                                int scale_stride, bool head_major, cudaStream_t stream);
 cudaError_t max_active_pairs(int* pairs);       // co-resident CTA pairs on this device
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t prepare_fwd_kernel();                // per-device one-time attributes

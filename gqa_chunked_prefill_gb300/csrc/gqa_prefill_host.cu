@@ -257,47 +257,58 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-               uint32_t b0, uint32_t b1, uint32_t b2) {
+// One tiled tensor map; dims/strides/box as cuTensorMapEncodeTiled takes them
+// (strides in bytes for dims 1..rank-1), unit element strides.
+bool encode(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+            const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+            CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};  // bytes, dims 1 and 2
-  const cuuint32_t box[3] = {b0, b1, b2};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// K or V [rows][4 heads][256] as a 4-D tensor (64 d, row, head, 64-column
-// chunk) with the chunk outermost, so that one box of (64, box_rows, 1,
-// box_chunks) lands in shared memory chunk-major: chunk c's box_rows rows of
+// Element type of the Q and K tensors: BF16 values, or E4M3 codes (one byte).
+struct Elem {
+  CUtensorMapDataType dtype;
+  uint32_t bytes;
+};
+constexpr Elem kBf16{CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2};
+constexpr Elem kE4m3{CU_TENSOR_MAP_DATA_TYPE_UINT8, 1};
+
+// Q [q_len][24][256]: box (one 128-byte chunk of d, 6 heads, 21 tokens).
+bool encode_q(CUtensorMap* map, const void* base, uint64_t q_len, Elem e) {
+  const cuuint64_t dims[3] = {kHeadDim, kQHeads, q_len};
+  const cuuint64_t strides[2] = {kHeadDim * e.bytes, static_cast<cuuint64_t>(kQHeads) * kHeadDim * e.bytes};
+  const cuuint32_t box[3] = {128 / e.bytes, static_cast<cuuint32_t>(kGroup), kTokPerTile};
+  return encode(map, e.dtype, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// K or V [rows][4 heads][256] as a 4-D tensor (one 128-byte chunk of d, row,
+// head, chunk) with the chunk outermost, so that one box of (chunk, box_rows,
+// 1, box_chunks) lands in shared memory chunk-major: chunk c's box_rows rows of
 // 128 bytes at c * box_rows * 128, as the MMA descriptors read them.
 bool encode_kv(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows,
-               uint32_t box_chunks) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[4] = {64, rows, static_cast<cuuint64_t>(kKvHeads), kHeadDim / 64};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kKvHeads) * kHeadDim * 2,  // next key
-                                 kHeadDim * 2,                                         // next head
-                                 64 * 2};                                              // next chunk
-  const cuuint32_t box[4] = {64, box_rows, 1, box_chunks};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               uint32_t box_chunks, Elem e) {
+  const cuuint64_t per_chunk = 128 / e.bytes;
+  const cuuint64_t dims[4] = {per_chunk, rows, static_cast<cuuint64_t>(kKvHeads),
+                              kHeadDim / per_chunk};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kKvHeads) * kHeadDim * e.bytes,  // key
+                                 kHeadDim * e.bytes,                                       // head
+                                 128};                                                     // chunk
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(per_chunk), box_rows, 1, box_chunks};
+  return encode(map, e.dtype, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// A paged K or V cache [rows][4 heads][256] (rows a multiple of 16) as a 5-D
-// tensor (64 d, key % 8, 64-column chunk, key / 8, head): one box of (64, 8,
+// A paged K or V cache [rows][4 heads][256] BF16 (rows a multiple of 16) as a
+// 5-D tensor (64 d, key % 8, 64-column chunk, key / 8, head): one box of (64, 8,
 // box_chunks, box_rows / 8, 1) lands in shared memory as 8-key groups, each
 // holding its box_chunks chunks of 8 rows x 128 bytes — the paged stage layout
 // of the attention kernel, in which a piece of whole 8-key groups is contiguous.
 bool encode_kv_paged(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows,
                      uint32_t box_chunks) {
-  auto fn = encode_fn();
-  if (!fn) return false;
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(kKvHeads) * kHeadDim * 2;
   const cuuint64_t dims[5] = {64, 8, kHeadDim / 64, rows / 8, static_cast<cuuint64_t>(kKvHeads)};
   const cuuint64_t strides[4] = {row_bytes,       // next key in the group
@@ -305,10 +316,18 @@ bool encode_kv_paged(CUtensorMap* map, const void* base, uint64_t rows, uint32_t
                                  8 * row_bytes,   // next group of 8 keys
                                  kHeadDim * 2};   // next head
   const cuuint32_t box[5] = {64, 8, box_chunks, box_rows / 8, 1};
-  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Key scales FP32 [4 heads][stride], box (128 keys, 1 head); keys past kv_len
+// read zeros.
+bool encode_key_scales(CUtensorMap* map, const float* base, uint64_t kv_len, uint64_t stride) {
+  const cuuint64_t dims[2] = {kv_len, static_cast<cuuint64_t>(kKvHeads)};
+  const cuuint64_t strides[1] = {stride * 4};
+  const cuuint32_t box[2] = {kBlockN, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Checks every argument; on success fills *plan (q_len == 0 gives an empty plan).
@@ -341,6 +360,24 @@ gqa_status check_paged(const PagedKV& pkv, int q_len) {
   return GQA_OK;
 }
 
+// Quantised-QK^T inputs of a call: q and k are E4M3 codes with these scales.
+struct Fp8Qk {
+  const float* q_scale;  // [q_len][24]
+  const float* k_scale;  // [4][k_scale_stride]
+  int k_scale_stride;
+};
+
+gqa_status check_fp8(const Fp8Qk& f8, int q_len, int kv_len) {
+  if (f8.k_scale_stride < kv_len || f8.k_scale_stride % 4 != 0 ||
+      static_cast<int64_t>(f8.k_scale_stride) * kKvHeads >= (int64_t{1} << 31))
+    return GQA_ERR_SHAPE;
+  if (q_len == 0) return GQA_OK;
+  if (!f8.q_scale || !f8.k_scale) return GQA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(f8.q_scale) & 3u) != 0 || misaligned(f8.k_scale))
+    return GQA_ERR_ALIGN;
+  return GQA_OK;
+}
+
 int gcd_int(int a, int b) {
   while (b != 0) {
     const int t = a % b;
@@ -351,27 +388,30 @@ int gcd_int(int a, int b) {
 }
 
 // Launches `plan` on `stream`; `ws` holds plan.workspace_bytes (or nothing).
-// `pkv` is null for dense K/V; otherwise k and v are the paged caches.
+// `pkv` is null for dense K/V, otherwise k and v are the paged caches; `f8` is
+// null for BF16 Q/K, otherwise q and k are E4M3 codes with its scales.
 gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* k, const void* v,
-                       const PagedKV* pkv, void* out, float* lse, int q_len, int kv_len,
-                       float scale, int* status_word, void* ws, const gqa_prefill_opts* opts,
-                       cudaStream_t stream) {
+                       const PagedKV* pkv, const Fp8Qk* f8, void* out, float* lse, int q_len,
+                       int kv_len, float scale, int* status_word, void* ws,
+                       const gqa_prefill_opts* opts, cudaStream_t stream) {
   const bool pair = plan.variant == 2;
+  if (pkv && f8) return GQA_ERR_UNSUPPORTED;
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   const uint64_t kv_rows = pkv ? static_cast<uint64_t>(pkv->num_pages) * pkv->page_size
                                : static_cast<uint64_t>(kv_len);
-  // K/V stages: one-CTA K 128 keys x 2 chunks, V 64 keys x 4 chunks; pairs
-  // K 64 x 4, V 128 x 2 (per CTA).
-  const uint32_t k_rows = pair ? 64 : kBlockN, k_chunks = pair ? 4 : 2;
+  const Elem qk = f8 ? kE4m3 : kBf16;
+  // K/V stages per CTA: one-CTA K 128 keys (BF16: 2 chunks per stage, 2 stages;
+  // FP8: all 2 chunks), V 64 keys x 4 chunks; pairs K 64 keys x all chunks,
+  // V 128 keys x 2 chunks.
+  const uint32_t k_rows = pair ? 64 : kBlockN;
+  const uint32_t k_chunks = f8 ? 2 : (pair ? 4 : 2);
   const uint32_t v_rows = pair ? kBlockN : 64, v_chunks = pair ? 2 : 4;
-  if (!encode_3d(&p.tmap_q, q, kHeadDim, kQHeads, static_cast<uint64_t>(q_len), 64, kGroup,
-                 kTokPerTile))
-    return GQA_ERR_CUDA;
+  if (!encode_q(&p.tmap_q, q, static_cast<uint64_t>(q_len), qk)) return GQA_ERR_CUDA;
   p.v_fix_tile = -1;
   if (!pkv) {
-    if (!encode_kv(&p.tmap_k, k, kv_rows, k_rows, k_chunks) ||
-        !encode_kv(&p.tmap_v, v, kv_rows, v_rows, v_chunks))
+    if (!encode_kv(&p.tmap_k, k, kv_rows, k_rows, k_chunks, qk) ||
+        !encode_kv(&p.tmap_v, v, kv_rows, v_rows, v_chunks, kBf16))
       return GQA_ERR_CUDA;
   } else {
     const uint32_t sub = static_cast<uint32_t>(gcd_int(pkv->page_size, 64));  // 16, 32 or 64
@@ -387,6 +427,12 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* 
     p.sub_rows = static_cast<int>(sub);
     p.oob_row = static_cast<int>(kv_rows);
     if (kv_len % kBlockN != 0) p.v_fix_tile = (kv_len - 1) / kBlockN;
+  }
+  if (f8) {
+    if (!encode_key_scales(&p.tmap_ks, f8->k_scale, static_cast<uint64_t>(kv_len),
+                           static_cast<uint64_t>(f8->k_scale_stride)))
+      return GQA_ERR_CUDA;
+    p.q_scale = f8->q_scale;
   }
   const int workers = pair ? plan.grid / 2 : plan.grid;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -411,7 +457,8 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* 
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return GQA_ERR_CUDA;
-  if (launch_fwd(p, plan.grid, pair, pkv != nullptr, stream) != cudaSuccess) return GQA_ERR_CUDA;
+  if (launch_fwd(p, plan.grid, pair, pkv != nullptr, f8 != nullptr, stream) != cudaSuccess)
+    return GQA_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return GQA_ERR_CUDA;
   if (plan.kernels_per_call == 2) {
     MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.n_qtiles, p.head_items,
@@ -421,13 +468,14 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* 
   return GQA_OK;
 }
 
-gqa_status run(const void* q, const void* k, const void* v, const PagedKV* pkv, void* out,
-               float* lse, int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-               float scale, void* stream_ptr, const gqa_prefill_opts* opts,
+gqa_status run(const void* q, const void* k, const void* v, const PagedKV* pkv, const Fp8Qk* f8,
+               void* out, float* lse, int q_len, int kv_len, int n_q_heads, int n_kv_heads,
+               int head_dim, float scale, void* stream_ptr, const gqa_prefill_opts* opts,
                gqa_prefill_plan* plan_out) {
   if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
   gqa_status st = check_call(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
   if (st == GQA_OK && pkv) st = check_paged(*pkv, q_len);
+  if (st == GQA_OK && f8) st = check_fp8(*f8, q_len, kv_len);
   if (st != GQA_OK || q_len == 0) return st;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != GQA_OK) return st;
@@ -444,8 +492,8 @@ gqa_status run(const void* q, const void* k, const void* v, const PagedKV* pkv, 
         cudaSuccess)
       return GQA_ERR_CUDA;
   }
-  st = launch_plan(plan, q, k, v, pkv, out, lse, q_len, kv_len, scale, dev->status_word, ws, opts,
-                   stream);
+  st = launch_plan(plan, q, k, v, pkv, f8, out, lse, q_len, kv_len, scale, dev->status_word, ws,
+                   opts, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   return st;
 }
@@ -492,8 +540,8 @@ gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, f
   if (static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes) return GQA_ERR_SCRATCH;
   // Every partial row the merge reads is written by the attention kernel first,
   // so the scratch needs no clearing between calls.
-  return launch_plan(plan, q, k, v, nullptr, out, lse, q_len, kv_len, scale, dev->status_word,
-                     scratch, nullptr, static_cast<cudaStream_t>(stream_ptr));
+  return launch_plan(plan, q, k, v, nullptr, nullptr, out, lse, q_len, kv_len, scale,
+                     dev->status_word, scratch, nullptr, static_cast<cudaStream_t>(stream_ptr));
 }
 
 }  // namespace
@@ -512,16 +560,16 @@ gqa_status gqa_prefill_attn_noalloc(const void* q, const void* k, const void* v,
 gqa_status gqa_prefill_attn(const void* q, const void* k, const void* v, void* out, float* lse,
                             int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                             float scale, void* stream) {
-  return gqa::run(q, k, v, nullptr, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
-                  stream, nullptr, nullptr);
+  return gqa::run(q, k, v, nullptr, nullptr, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
+                  head_dim, scale, stream, nullptr, nullptr);
 }
 
 gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,
                                int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                                float scale, void* stream, const gqa_prefill_opts* opts,
                                gqa_prefill_plan* plan_out) {
-  return gqa::run(q, k, v, nullptr, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
-                  stream, opts, plan_out);
+  return gqa::run(q, k, v, nullptr, nullptr, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
+                  head_dim, scale, stream, opts, plan_out);
 }
 
 gqa_status gqa_prefill_attn_paged(const void* q, const void* k_cache, const void* v_cache,
@@ -529,8 +577,8 @@ gqa_status gqa_prefill_attn_paged(const void* q, const void* k_cache, const void
                                   void* out, float* lse, int q_len, int kv_len, int n_q_heads,
                                   int n_kv_heads, int head_dim, float scale, void* stream) {
   const gqa::PagedKV pkv{block_table, num_pages, page_size};
-  return gqa::run(q, k_cache, v_cache, &pkv, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
-                  head_dim, scale, stream, nullptr, nullptr);
+  return gqa::run(q, k_cache, v_cache, &pkv, nullptr, out, lse, q_len, kv_len, n_q_heads,
+                  n_kv_heads, head_dim, scale, stream, nullptr, nullptr);
 }
 
 gqa_status gqa_prefill_attn_paged_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -540,7 +588,55 @@ gqa_status gqa_prefill_attn_paged_ex(const void* q, const void* k_cache, const v
                                      void* stream, const gqa_prefill_opts* opts,
                                      gqa_prefill_plan* plan_out) {
   const gqa::PagedKV pkv{block_table, num_pages, page_size};
-  return gqa::run(q, k_cache, v_cache, &pkv, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
+  return gqa::run(q, k_cache, v_cache, &pkv, nullptr, out, lse, q_len, kv_len, n_q_heads,
+                  n_kv_heads, head_dim, scale, stream, opts, plan_out);
+}
+
+gqa_status gqa_quantize_q_fp8(const void* q, void* q_fp8, float* q_scale, int q_len,
+                              int n_q_heads, int head_dim, void* stream) {
+  if (q_len < 0) return GQA_ERR_SHAPE;
+  if (n_q_heads != gqa::kQHeads || head_dim != gqa::kHeadDim) return GQA_ERR_UNSUPPORTED;
+  if (q_len == 0) return GQA_OK;
+  if (!q || !q_fp8 || !q_scale) return GQA_ERR_NULL;
+  if (gqa::misaligned(q) || gqa::misaligned(q_fp8) || (reinterpret_cast<uintptr_t>(q_scale) & 3u))
+    return GQA_ERR_ALIGN;
+  return gqa::launch_quantize_fp8(q, q_fp8, q_scale, q_len, gqa::kQHeads, 0, false,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
+gqa_status gqa_quantize_k_fp8(const void* k, void* k_fp8, float* k_scale, int kv_len,
+                              int n_kv_heads, int head_dim, int k_scale_stride, void* stream) {
+  if (kv_len < 0 || k_scale_stride < kv_len || k_scale_stride % 4 != 0 ||
+      static_cast<int64_t>(k_scale_stride) * gqa::kKvHeads >= (int64_t{1} << 31))
+    return GQA_ERR_SHAPE;
+  if (n_kv_heads != gqa::kKvHeads || head_dim != gqa::kHeadDim) return GQA_ERR_UNSUPPORTED;
+  if (kv_len == 0) return GQA_OK;
+  if (!k || !k_fp8 || !k_scale) return GQA_ERR_NULL;
+  if (gqa::misaligned(k) || gqa::misaligned(k_fp8) || gqa::misaligned(k_scale)) return GQA_ERR_ALIGN;
+  return gqa::launch_quantize_fp8(k, k_fp8, k_scale, kv_len, gqa::kKvHeads, k_scale_stride, true,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
+gqa_status gqa_prefill_attn_fp8qk(const void* q_fp8, const float* q_scale, const void* k_fp8,
+                                  const float* k_scale, int k_scale_stride, const void* v,
+                                  void* out, float* lse, int q_len, int kv_len, int n_q_heads,
+                                  int n_kv_heads, int head_dim, float scale, void* stream) {
+  const gqa::Fp8Qk f8{q_scale, k_scale, k_scale_stride};
+  return gqa::run(q_fp8, k_fp8, v, nullptr, &f8, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
+                  head_dim, scale, stream, nullptr, nullptr);
+}
+
+gqa_status gqa_prefill_attn_fp8qk_ex(const void* q_fp8, const float* q_scale, const void* k_fp8,
+                                     const float* k_scale, int k_scale_stride, const void* v,
+                                     void* out, float* lse, int q_len, int kv_len, int n_q_heads,
+                                     int n_kv_heads, int head_dim, float scale, void* stream,
+                                     const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out) {
+  const gqa::Fp8Qk f8{q_scale, k_scale, k_scale_stride};
+  return gqa::run(q_fp8, k_fp8, v, nullptr, &f8, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
                   head_dim, scale, stream, opts, plan_out);
 }
 
@@ -583,7 +679,8 @@ const char* gqa_status_string(gqa_status status) {
     case GQA_ERR_NULL: return "a required pointer is NULL";
     case GQA_ERR_SHAPE:
       return "invalid sizes (need 0 <= q_len <= kv_len; paged: num_pages >= 1, "
-             "num_pages * page_size < 2^30) or scale (finite, > 0)";
+             "num_pages * page_size < 2^30; FP8: k_scale_stride >= kv_len, a multiple of 4) "
+             "or scale (finite, > 0)";
     case GQA_ERR_UNSUPPORTED:
       return "unsupported: needs 24 query heads, 4 KV heads, head_dim 256 on an sm_103 GPU "
              "(paged: page_size a positive multiple of 16)";

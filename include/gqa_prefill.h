@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 2
+#define GQA_PREFILL_ABI_VERSION 3
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -224,6 +224,50 @@ gqa_status gqa_prefill_attn_paged_ex(const void* q, const void* k_cache, const v
                                      int n_q_heads, int n_kv_heads, int head_dim, float scale,
                                      void* stream, const gqa_prefill_opts* opts,
                                      gqa_prefill_plan* plan_out);
+
+/*
+ * Quantised QK^T (gfx936 DCU上实现INT8 QK MMAC：分页访存、Fragment映射与GQA适配, §1
+ * "INT8 QK的量化和Scale恢复" and §4 "Query量化只做一次"). The report quantises each
+ * query vector (token, query head) and each key vector (token, KV head) with
+ * one symmetric dynamic scale, multiplies the integer codes, and restores
+ * score = (code_q . code_k) * s_q * s_k * softmax_scale for every score BEFORE
+ * the softmax. Its codes are INT8 for gfx936's INT8 MMAC; on GB300 the native
+ * low-precision tensor path is FP8, so here the codes are E4M3:
+ *
+ *   s    = max_c |x[c]| / 448                  (FP32, IEEE round-to-nearest division)
+ *   code = E4M3(x[c] / s)                      (FP32 division, then round to nearest
+ *                                               even, saturating at +-448)
+ *   a vector of zeros gets s = 0 and codes 0.
+ *
+ * PV stays BF16 (V is not quantised), as does the output.
+ *
+ * gqa_quantize_q_fp8: q BF16 [q_len][24][256] -> q_fp8 E4M3 [q_len][24][256]
+ *   (one byte per value), q_scale FP32 [q_len][24]. Run once per chunk, before
+ *   attention (the report's producer-side quantisation).
+ * gqa_quantize_k_fp8: k BF16 [kv_len][4][256] -> k_fp8 E4M3 [kv_len][4][256],
+ *   k_scale FP32 [4][k_scale_stride] (head-major: key j of KV head g at
+ *   g * k_scale_stride + j), k_scale_stride >= kv_len and a multiple of 4 (so
+ *   every head's row starts on 16 bytes). Run when keys enter the cache.
+ * Both are asynchronous on `stream`; pointers 16-byte aligned (q_scale 4-byte).
+ *
+ * gqa_prefill_attn_fp8qk[_ex]: the attention of gqa_prefill_attn with Q and K
+ * given as those codes and scales; v, out, lse, scale, causal alignment, plan
+ * and options as gqa_prefill_attn[_ex]. The result is the attention of the
+ * DEQUANTISED query and keys (code * s) computed like the BF16 path.
+ */
+gqa_status gqa_quantize_q_fp8(const void* q, void* q_fp8, float* q_scale, int q_len,
+                              int n_q_heads, int head_dim, void* stream);
+gqa_status gqa_quantize_k_fp8(const void* k, void* k_fp8, float* k_scale, int kv_len,
+                              int n_kv_heads, int head_dim, int k_scale_stride, void* stream);
+gqa_status gqa_prefill_attn_fp8qk(const void* q_fp8, const float* q_scale, const void* k_fp8,
+                                  const float* k_scale, int k_scale_stride, const void* v,
+                                  void* out, float* lse, int q_len, int kv_len, int n_q_heads,
+                                  int n_kv_heads, int head_dim, float scale, void* stream);
+gqa_status gqa_prefill_attn_fp8qk_ex(const void* q_fp8, const float* q_scale, const void* k_fp8,
+                                     const float* k_scale, int k_scale_stride, const void* v,
+                                     void* out, float* lse, int q_len, int kv_len, int n_q_heads,
+                                     int n_kv_heads, int head_dim, float scale, void* stream,
+                                     const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out);
 
 /* Static description of a status code (never NULL). */
 const char* gqa_status_string(gqa_status status);

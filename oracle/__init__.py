@@ -146,3 +146,74 @@ def paged_attention(q, k_cache, v_cache, block_table, kv_len: int, scale: float,
     """``attention()`` of q over the sequence ``paged_gather()`` reads from the caches."""
     k, v = paged_gather(k_cache, v_cache, block_table, kv_len)
     return attention(q, k, v, scale, rows=rows, n_threads=n_threads)
+
+
+# --- quantised QK^T -------------------------------------------------------------
+#
+# "gfx936 DCU上实现INT8 QK MMAC：分页访存、Fragment映射与GQA适配", §1 and §4: each query
+# vector (token, query head) and each key vector (token, KV head) gets one
+# symmetric dynamic scale s = max|x| / qmax and codes x / s; scores are restored
+# as (code_q . code_k) * s_q * s_k * softmax_scale before the softmax. The codes
+# here are FP8 E4M3 (qmax 448) instead of the report's INT8 (qmax 127).
+
+def e4m3_values() -> np.ndarray:
+    """Value of every non-negative E4M3 code 0x00 .. 0x7E (0x7F is NaN).
+
+    E4M3: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits. Exponent
+    field 0 is subnormal (m/8 * 2^-6); otherwise (1 + m/8) * 2^(e - 7). There is
+    no infinity; 0x7E = 448 is the largest finite value.
+    """
+    vals = np.empty(127, np.float64)
+    for code in range(127):
+        e, m = code >> 3, code & 7
+        vals[code] = (m / 8.0) * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return vals
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Codes of FP32 values: round to nearest, ties to the even code, saturating at
+    +-448, sign kept (a negative value that rounds to zero gives 0x80)."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    vals = e4m3_values()
+    a = np.abs(x)
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, 126)  # first value >= a
+    lo = np.clip(hi - 1, 0, 126)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a >= vals[126], 126, code)  # saturate
+    return (code | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """FP64 value of E4M3 codes (0x7F / 0xFF, NaN, are not produced here)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    mag = e4m3_values()[np.minimum(c & 0x7F, 126)]
+    return np.where(c & 0x80, -mag, mag)
+
+
+def quantize_e4m3(x):
+    """Per-vector quantisation of [..., d] values: s = max|x| / 448 and codes of
+    x / s, both in FP32 with IEEE round-to-nearest division; a vector of zeros
+    gets s = 0 and codes 0. Returns (codes uint8 [..., d], scales float32 [...])."""
+    x32 = np.asarray(x.float().numpy() if isinstance(x, torch.Tensor) else x, dtype=np.float32)
+    amax = np.max(np.abs(x32), axis=-1)
+    s = (amax / np.float32(448.0)).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    codes = e4m3_encode((x32 / safe[..., None]).astype(np.float32))
+    codes = np.where((s > 0)[..., None], codes, np.uint8(0)).astype(np.uint8)
+    return codes, s
+
+
+def dequantize_e4m3(codes, scales) -> np.ndarray:
+    """code * s in FP64 (exact: a 4-bit-significand value times an FP32 scale)."""
+    return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[..., None]
+
+
+def fp8qk_attention(q_codes, q_scale, k_codes, k_scale, v, scale: float, rows=None,
+                    n_threads: Optional[int] = None):
+    """Attention of the dequantised query and keys (the quantised-QK^T result):
+    q_codes [q_len, Hq, d] with q_scale [q_len, Hq]; k_codes [kv_len, Hkv, d] with
+    k_scale [kv_len, Hkv] (token-major here); v as for ``attention``."""
+    return attention(dequantize_e4m3(q_codes, q_scale), dequantize_e4m3(k_codes, k_scale), v,
+                     scale, rows=rows, n_threads=n_threads)

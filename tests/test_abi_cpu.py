@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(gqa):
 
 
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 2
+    assert gqa.gqa_prefill_abi_version() == 3
 
 
 def test_refusals_before_any_cuda_call(gqa):
@@ -159,3 +159,39 @@ def test_make_plan_validates(gqa):
     assert gqa.gqa_prefill_make_plan(5, 4, 24, 4, 256, 148, check=False)[0] == S.ERR_SHAPE
     assert gqa.gqa_prefill_make_plan(5, 8, 24, 4, 256, 0, check=False)[0] == S.ERR_SHAPE
     assert gqa.gqa_prefill_make_plan(5, 8, 24, 2, 256, 148, check=False)[0] == S.ERR_UNSUPPORTED
+
+
+def test_fp8_refusals_before_any_cuda_call(gqa):
+    S = gqa.GqaStatus
+    qz = lambda *a: gqa.gqa_quantize_q_fp8(*a, stream=0, check=False)
+    kz = lambda *a: gqa.gqa_quantize_k_fp8(*a, stream=0, check=False)
+    assert qz(16, 16, 16, -1, 24, 256) == S.ERR_SHAPE
+    assert qz(16, 16, 16, 4, 32, 256) == S.ERR_UNSUPPORTED
+    assert qz(None, 16, 16, 4, 24, 256) == S.ERR_NULL
+    assert qz(16, 24, 16, 4, 24, 256) == S.ERR_ALIGN
+    assert qz(16, 16, 18, 4, 24, 256) == S.ERR_ALIGN   # q_scale: 4-byte alignment
+    assert qz(None, None, None, 0, 24, 256) == S.OK     # nothing to do
+    assert kz(16, 16, 16, 8, 4, 256, 6) == S.ERR_SHAPE  # stride not a multiple of 4
+    assert kz(16, 16, 16, 8, 4, 256, 4) == S.ERR_SHAPE  # stride < kv_len
+    assert kz(16, 16, 20, 8, 4, 256, 8) == S.ERR_ALIGN  # k_scale: 16-byte alignment
+    assert kz(16, 16, 16, 8, 2, 256, 8) == S.ERR_UNSUPPORTED
+    f = lambda *a: gqa.gqa_prefill_attn_fp8qk(*a, stream=0, check=False)
+    ok = dict(q=16, qs=16, k=16, ks=16, st=8, v=16, out=16, lse=None, q_len=4, kv_len=8, hq=24,
+              hkv=4, d=256, scale=0.0625)
+    names = list(ok)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(*[a[n] for n in names])
+
+    assert call(st=4) == S.ERR_SHAPE
+    assert call(st=10) == S.ERR_SHAPE
+    assert call(qs=None) == S.ERR_NULL
+    assert call(ks=None) == S.ERR_NULL
+    assert call(ks=20) == S.ERR_ALIGN
+    assert call(qs=18) == S.ERR_ALIGN
+    assert call(v=None) == S.ERR_NULL
+    assert call(hq=16) == S.ERR_UNSUPPORTED
+    assert call(q_len=9) == S.ERR_SHAPE
+    assert call(q=None, qs=None, k=None, ks=None, v=None, out=None, q_len=0, kv_len=0, st=0) == S.OK

@@ -1,0 +1,125 @@
+"""GPU parity of the quantised-QK^T path (E4M3 codes, per-vector scales).
+
+1. The quantise kernels give the oracle's codes and scales bit for bit (both
+   sides take every rounding decision in FP32: s = amax / 448, code = E4M3(x / s)).
+2. gqa_prefill_attn_fp8qk matches the FP64 oracle run on the dequantised query
+   and keys (the oracle quantises the same BF16 inputs itself) at the
+   acceptance tolerance of the BF16 path: products of E4M3 codes are exact in
+   FP32, and the scales are restored in FP32 before the softmax, so what is left
+   is the BF16 rounding of P and of the output, as in the BF16 path.
+3. The quantisation error itself (against unquantised attention) is reported by
+   a loose bound, not a parity claim.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gqa_inputs import WORKLOADS, make_qkv, make_workload, sample_rows
+from tests.gpu_helpers import check_close, gather_rows
+
+pytestmark = pytest.mark.gpu
+SCALE = 1.0 / 16.0
+
+
+def quantize_gpu(q, k):
+    """GPU codes/scales: q_fp8 [q_len,24,256] u8, q_scale [q_len,24], k_fp8 [kv_len,4,256] u8,
+    k_scale [4, stride] (head-major, stride = kv_len rounded up to 4)."""
+    import gqa_chunked_prefill_gb300 as gqa
+    dev = torch.device("cuda:0")
+    qd, kd = q.to(dev).contiguous(), k.to(dev).contiguous()
+    q_len, kv_len = qd.shape[0], kd.shape[0]
+    stride = max(4, -(-kv_len // 4) * 4)
+    q8 = torch.empty(qd.shape, dtype=torch.uint8, device=dev)
+    qs = torch.empty((q_len, 24), dtype=torch.float32, device=dev)
+    k8 = torch.empty(kd.shape, dtype=torch.uint8, device=dev)
+    ks = torch.full((4, stride), float("nan"), dtype=torch.float32, device=dev)
+    gqa.gqa_quantize_q_fp8(qd, q8, qs, q_len, 24, 256)
+    gqa.gqa_quantize_k_fp8(kd, k8, ks, kv_len, 4, 256, stride)
+    torch.cuda.synchronize()
+    return q8, qs, k8, ks, stride
+
+
+def run_fp8(q, k, v, scale, **force):
+    import gqa_chunked_prefill_gb300 as gqa
+    dev = torch.device("cuda:0")
+    q8, qs, k8, ks, stride = quantize_gpu(q, k)
+    vd = v.to(dev).contiguous()
+    q_len, kv_len = q.shape[0], k.shape[0]
+    out = torch.empty((q_len, 24, 256), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((q_len, 24), dtype=torch.float32, device=dev)
+    _, plan = gqa.gqa_prefill_attn_fp8qk_ex(q8, qs, k8, ks, stride, vd, out, lse, q_len, kv_len,
+                                            24, 4, 256, scale, **force)
+    torch.cuda.synchronize()
+    assert gqa.gqa_prefill_poll() == 0
+    return out, lse, plan
+
+
+def oracle_fp8(q, k, v, scale, rows=None):
+    qc, qs = oracle.quantize_e4m3(q)
+    kc, ks = oracle.quantize_e4m3(k)
+    return oracle.fp8qk_attention(qc, qs, kc, ks, v, scale, rows=rows)
+
+
+@pytest.mark.parametrize("q_len,kv_len", [(1, 1), (43, 300), (300, 1000), (7, 4097)])
+def test_quantize_kernels_match_oracle_bit_for_bit(cuda_device, q_len, kv_len):
+    q, k, _ = make_qkv(q_len, kv_len, seed=q_len + 7 * kv_len)
+    q = q.clone()
+    k = k.clone()
+    q[0, 3] = 0                                  # an all-zero vector: s = 0, codes 0
+    k[-1, 2] = 0
+    k[0, 1] = k[0, 1] * 1e-30                    # scale far below 1: tiny but normal
+    q[-1, 0, :128] = q[-1, 0, :128] * 1e-6       # half the vector in E4M3's subnormal range
+    q8, qs, k8, ks, _ = quantize_gpu(q, k)
+    qc, qsc = oracle.quantize_e4m3(q)
+    kc, ksc = oracle.quantize_e4m3(k)
+    assert np.array_equal(q8.cpu().numpy(), qc) and np.array_equal(qs.cpu().numpy(), qsc)
+    assert np.array_equal(k8.cpu().numpy(), kc)
+    assert np.array_equal(ks[:, :kv_len].cpu().numpy(), ksc.T)
+
+
+@pytest.mark.parametrize("q_len,kv_len", [(1, 1), (5, 300), (43, 300), (100, 100), (129, 1000),
+                                          (22, 2000)])
+@pytest.mark.parametrize("variant", [1, 2])
+def test_fp8qk_small_shapes_every_element(cuda_device, q_len, kv_len, variant):
+    q, k, v = make_qkv(q_len, kv_len, seed=5 * q_len + kv_len)
+    out, lse, plan = run_fp8(q, k, v, SCALE, force_variant=variant)
+    assert plan["variant"] == variant
+    ref_o, ref_l = oracle_fp8(q, k, v, SCALE)
+    check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
+                f"fp8 {q_len}x{kv_len}")
+
+
+@pytest.mark.parametrize("splits,grid,variant", [(3, 0, 1), (3, 5, 1), (2, 0, 2), (3, 6, 2),
+                                                 (32, 0, 1)])
+def test_fp8qk_split_tail_every_element(cuda_device, splits, grid, variant):
+    q, k, v = make_qkv(129, 1000, seed=31)
+    out, lse, _ = run_fp8(q, k, v, SCALE, force_splits=splits, force_grid=grid,
+                          force_variant=variant)
+    ref_o, ref_l = oracle_fp8(q, k, v, SCALE)
+    check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
+                f"fp8 split {splits} grid {grid}")
+
+
+@pytest.mark.parametrize("name", ["q4096_kv32768", "q512_kv4096_kbias", "q3072_kv16384"])
+@pytest.mark.parametrize("variant", [0, 1])
+def test_fp8qk_workload_full_size(cuda_device, name, variant):
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    out, lse, _ = run_fp8(q, k, v, w.scale, force_variant=variant)
+    rows = sample_rows(w.q_len, w.n_q_heads, 1200, seed=12)
+    ref_o, ref_l = oracle_fp8(q, k, v, w.scale, rows=rows)
+    got_o, got_l = gather_rows(out, lse, rows)
+    check_close(got_o, got_l, ref_o, ref_l, f"fp8 {name}")
+
+
+def test_fp8qk_quantisation_error_is_small_against_bf16_attention(cuda_device):
+    """Not parity: the method's own error. With N(0,1) data the E4M3 codes (3
+    mantissa bits, relative step 2^-3) perturb each score by about
+    2^-4 * scale * |q| |k| / sqrt(d); outputs stay within a few 1e-2."""
+    q, k, v = make_qkv(64, 2000, seed=77)
+    out, lse, _ = run_fp8(q, k, v, SCALE)
+    ref_o, ref_l = oracle.attention(q, k, v, SCALE)
+    err = np.abs(out.double().cpu().numpy() - ref_o)
+    assert err.mean() < 5e-3 and err.max() < 6e-2
+    assert np.abs(lse.double().cpu().numpy() - ref_l).max() < 5e-2

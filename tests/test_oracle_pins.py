@@ -243,3 +243,68 @@ def test_paged_gather_rejects_entries_outside_the_cache():
         oracle.paged_gather(cache, cache, [0, 2], kv_len=6)
     with pytest.raises(ValueError):
         oracle.paged_gather(cache, cache, [-1], kv_len=3)
+
+
+# --- quantised QK^T: E4M3 codes and per-vector scales -----------------------------
+
+def test_e4m3_values_follow_the_format():
+    v = oracle.e4m3_values()
+    assert v[0] == 0.0 and v[1] == 2.0 ** -9 and v[7] == 7 * 2.0 ** -9  # subnormals m/8 * 2^-6
+    assert v[8] == 2.0 ** -6 and v[0x38] == 1.0 and v[0x3F] == 1.875
+    assert v[0x7E] == 448.0 and v[0x7D] == 416.0
+    assert np.all(np.diff(v) > 0)
+
+
+def test_e4m3_every_code_round_trips():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    assert np.array_equal(oracle.e4m3_encode(oracle.e4m3_decode(codes).astype(np.float32)), codes)
+
+
+def test_e4m3_rounding_by_hand():
+    x = [448.0, 1.0, 2.0 ** -9, 2.0 ** -10, 1.0625, 1.1875, 1.125 + 2.0 ** -10, 470.0, 1e30,
+         -1.0, -1e-9, 3 * 2.0 ** -10]
+    # 2^-10 ties 0 / 2^-9 -> 0 (even); 1.0625 ties 1.0 / 1.125 -> 1.0 (code 0x38, even);
+    # 1.1875 ties 1.125 / 1.25 -> 1.25 (0x3A); just above 1.125 -> 0x39; beyond 448 -> 448;
+    # -1e-9 rounds to -0 (sign kept); 3*2^-10 ties 2^-9 / 2^-8 -> 2^-8 (code 0x02).
+    want = [0x7E, 0x38, 0x01, 0x00, 0x38, 0x3A, 0x39, 0x7E, 0x7E, 0xB8, 0x80, 0x02]
+    assert oracle.e4m3_encode(x).tolist() == want
+
+
+def test_e4m3_matches_library_cast():
+    x = (torch.randn(200000, generator=torch.Generator().manual_seed(3)) * 60).clamp(-447, 447)
+    lib = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x.numpy()), lib)
+
+
+def test_quantize_per_vector_scale_and_error_bound():
+    q, _, _ = make_qkv(9, 9, 44)
+    x = q.float().numpy()
+    x[3, 5] = 0.0  # one all-zero vector
+    codes, s = oracle.quantize_e4m3(x)
+    amax = np.abs(x).max(axis=-1)
+    assert s.dtype == np.float32 and np.array_equal(s, (amax / np.float32(448)).astype(np.float32))
+    assert np.all(codes[3, 5] == 0) and s[3, 5] == 0
+    dq = oracle.dequantize_e4m3(codes, s)
+    err = np.abs(dq - x)
+    # half a code spacing: 2^-4 relative in the normal range, 2^-10 * s among subnormals
+    bound = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * s[..., None].astype(np.float64)) * 1.0001
+    assert np.all(err <= bound)
+    # the largest element of every non-zero vector maps to +-448
+    nz = amax > 0
+    top = np.take_along_axis(oracle.e4m3_decode(codes), np.abs(x).argmax(-1)[..., None], -1)[..., 0]
+    assert np.all(np.abs(top[nz]) == 448.0)
+
+
+def test_fp8qk_attention_equals_attention_on_exact_codes():
+    """Integers with max |x| = 448 in every vector quantise exactly (s = 1): the
+    quantised path must then equal plain attention on those values."""
+    g = np.random.default_rng(9)
+    q = g.integers(-16, 17, (5, 24, 256)).astype(np.float64); q[..., 0] = 448
+    k = g.integers(-16, 17, (40, 4, 256)).astype(np.float64); k[..., 7] = -448
+    v = g.standard_normal((40, 4, 256))
+    qc, qs = oracle.quantize_e4m3(q)
+    kc, ks = oracle.quantize_e4m3(k)
+    assert np.all(qs == 1.0) and np.all(ks == 1.0)
+    out_a, lse_a = oracle.fp8qk_attention(qc, qs, kc, ks, v, 1e-5)
+    out_b, lse_b = oracle.attention(q, k, v, 1e-5)
+    assert np.array_equal(out_a, out_b) and np.array_equal(lse_a, lse_b)
