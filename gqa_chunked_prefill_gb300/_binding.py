@@ -82,6 +82,21 @@ lib.gqa_prefill_attn_fp8qk.restype = _i
 lib.gqa_prefill_attn_fp8qk_ex.argtypes = _FP8_ARGS + [ctypes.POINTER(PrefillOpts),
                                                       ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_attn_fp8qk_ex.restype = _i
+_VARLEN_ARGS = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]
+lib.gqa_prefill_attn_varlen.argtypes = _VARLEN_ARGS
+lib.gqa_prefill_attn_varlen.restype = _i
+lib.gqa_prefill_attn_varlen_ex.argtypes = _VARLEN_ARGS + [ctypes.POINTER(PrefillOpts),
+                                                          ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_attn_varlen_ex.restype = _i
+_PVARLEN_ARGS = [_vp, _vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]
+lib.gqa_prefill_attn_paged_varlen.argtypes = _PVARLEN_ARGS
+lib.gqa_prefill_attn_paged_varlen.restype = _i
+lib.gqa_prefill_attn_paged_varlen_ex.argtypes = _PVARLEN_ARGS + [ctypes.POINTER(PrefillOpts),
+                                                                 ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_attn_paged_varlen_ex.restype = _i
+lib.gqa_prefill_make_plan_varlen.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
+                                             ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_make_plan_varlen.restype = _i
 lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
                                       ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan.restype = _i
@@ -240,6 +255,90 @@ def gqa_prefill_attn_fp8qk_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v,
                                        k_scale_stride, _ptr(v), _ptr(out), _ptr(lse), q_len,
                                        kv_len, n_q_heads, n_kv_heads, head_dim, scale,
                                        _stream(stream), ctypes.byref(opts), ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def _host_i32(xs):
+    """A host int32 array (kept alive by the caller's reference) and its address."""
+    arr = (ctypes.c_int32 * len(xs))(*[int(x) for x in xs])
+    return arr, ctypes.addressof(arr)
+
+
+def gqa_prefill_attn_varlen_ex(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, n_q_heads,
+                               n_kv_heads, head_dim, scale, stream=None, force_splits=0,
+                               force_grid=0, force_variant=0, wait_timeout_us=0, fwd_events=None,
+                               check=True):
+    """cu_seqlens_q / cu_seqlens_k: HOST sequences of batch + 1 ints (lists or arrays)."""
+    cq, pq = _host_i32(cu_seqlens_q)
+    ck, pk = _host_i32(cu_seqlens_k)
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, False)
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_attn_varlen_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), pq, pk,
+                                        len(cu_seqlens_q) - 1, n_q_heads, n_kv_heads, head_dim,
+                                        scale, _stream(stream), ctypes.byref(opts),
+                                        ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def gqa_prefill_attn_varlen(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, n_q_heads, n_kv_heads,
+                            head_dim, scale, stream=None, check=True) -> int:
+    cq, pq = _host_i32(cu_seqlens_q)
+    ck, pk = _host_i32(cu_seqlens_k)
+    rc = lib.gqa_prefill_attn_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), pq, pk,
+                                     len(cu_seqlens_q) - 1, n_q_heads, n_kv_heads, head_dim,
+                                     scale, _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_prefill_attn_paged_varlen_ex(q, k_cache, v_cache, block_table, bt_stride, num_pages,
+                                     page_size, out, lse, cu_seqlens_q, kv_lens, n_q_heads,
+                                     n_kv_heads, head_dim, scale, stream=None, force_splits=0,
+                                     force_grid=0, force_variant=0, wait_timeout_us=0,
+                                     fwd_events=None, check=True):
+    """block_table: DEVICE int32 [batch, bt_stride]; cu_seqlens_q (batch + 1) and kv_lens
+    (batch): HOST ints."""
+    cq, pq = _host_i32(cu_seqlens_q)
+    kl, pk = _host_i32(kv_lens)
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, False)
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_attn_paged_varlen_ex(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), bt_stride, num_pages, page_size,
+        _ptr(out), _ptr(lse), pq, pk, len(kv_lens), n_q_heads, n_kv_heads, head_dim, scale,
+        _stream(stream), ctypes.byref(opts), ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def gqa_prefill_attn_paged_varlen(q, k_cache, v_cache, block_table, bt_stride, num_pages,
+                                  page_size, out, lse, cu_seqlens_q, kv_lens, n_q_heads,
+                                  n_kv_heads, head_dim, scale, stream=None, check=True) -> int:
+    cq, pq = _host_i32(cu_seqlens_q)
+    kl, pk = _host_i32(kv_lens)
+    rc = lib.gqa_prefill_attn_paged_varlen(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), bt_stride, num_pages, page_size,
+        _ptr(out), _ptr(lse), pq, pk, len(kv_lens), n_q_heads, n_kv_heads, head_dim, scale,
+        _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_prefill_make_plan_varlen(cu_seqlens_q, cu_seqlens_k, n_q_heads, n_kv_heads, head_dim,
+                                 num_sms, force_splits=0, force_grid=0, force_variant=0,
+                                 check=True):
+    cq, pq = _host_i32(cu_seqlens_q)
+    ck, pk = _host_i32(cu_seqlens_k)
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_make_plan_varlen(pq, pk, len(cu_seqlens_q) - 1, n_q_heads, n_kv_heads,
+                                          head_dim, num_sms, force_splits, force_grid,
+                                          force_variant, ctypes.byref(plan))
     if check:
         _check(rc)
     return rc, plan.as_dict()

@@ -128,13 +128,12 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Fw
 // kv_len read TMA zero fill, so only keys [kv_len, next multiple of 16) remain.
 // `base`: the stage (this CTA's shared::cta address, or the peer's
 // shared::cluster address when `remote`), holding keys key0 .. key0+rows-1 of
-// the tile in the paged stage layout: key r, chunk c at
+// the tile (kr: its first key past kv_len) in the paged stage layout: key r, chunk c at
 // (r / 8) * 1024 * nch + c * 1024 + (r % 8) * 128 (a 128-byte row stays in
 // place under the 128-byte swizzle). Out of line (rare: once per item that
 // reaches the last KV tile) so the MMA thread's loop stays small.
-__device__ __noinline__ void zero_v_tail(uint32_t base, int nch, int key0, int rows,
-                                         const FwdParams& p, bool remote) {
-  const int kr = p.kv_len - p.v_fix_tile * kBlockN;  // first key of the tile past kv_len
+__device__ __noinline__ void zero_v_tail(uint32_t base, int nch, int key0, int rows, int kr,
+                                         bool remote) {
   const int r_begin = max(kr, key0) - key0;
   const int r_end = min((kr + 15) & ~15, key0 + rows) - key0;
   for (int r = r_begin; r < r_end; ++r)
@@ -148,18 +147,19 @@ __device__ __noinline__ void zero_v_tail(uint32_t base, int nch, int key0, int r
 
 // Paged K/V, the rare case: a box that crosses pages (or the V box of the tile
 // holding key kv_len-1) goes as pieces (gqa_paged.h), one 5-D copy per piece
-// covering all `nch` chunks (paged stage layout, see the kernel). `bar`: the
-// barrier the copies complete on (the pair leader's, mapped, for pairs). Out of
-// line so the producer's common loop stays small.
+// covering all `nch` chunks (paged stage layout, see the kernel). `table`: the
+// sequence's block-table row; `bar`: the barrier the copies complete on (the
+// pair leader's, mapped, for pairs). Out of line so the producer's common loop
+// stays small.
 template <bool kPair>
-__device__ __noinline__ void issue_paged_pieces(const FwdParams& p, const CUtensorMap* sub_map,
+__device__ __noinline__ void issue_paged_pieces(const PagedGeom& pgeo, const int* table,
+                                                int* status, const CUtensorMap* sub_map,
                                                 uint32_t dst, uint32_t bar, int r0, int rows,
                                                 int nch, int chunk0, int g, bool v_fix,
                                                 uint64_t pol) {
-  const PagedGeom pgeo{p.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
   PagedRun run;
-  map_paged_run(pgeo, r0, rows, v_fix, [&](int pg) { return __ldg(p.block_table + pg); }, run);
-  if (run.bad) atomicExch(p.status, static_cast<int>(GQA_ERR_PAGE_TABLE));
+  map_paged_run(pgeo, r0, rows, v_fix, [&](int pg) { return __ldg(table + pg); }, run);
+  if (run.bad) atomicExch(status, static_cast<int>(GQA_ERR_PAGE_TABLE));
   for (int i = 0; i < run.n; ++i) {
     // Piece i is 8-key groups [i*sub/8, (i+1)*sub/8) of the stage: contiguous.
     const uint32_t d = dst + i * run.sub * nch * 128;
@@ -276,11 +276,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int tpi = kPair ? 2 * kTokPerTile : kTokPerTile;  // tokens per work item
-  const Geometry geo{p.q_len, p.p0, p.n_qtiles, tpi};
   const int n_workers = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
   const int worker = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   PieceIter pieces;  // this CTA's (pair's) work, in order; each role walks its own copy
-  pieces.init(geo, Schedule{p.head_items, p.tail_splits, p.n_units}, n_workers, worker);
+  pieces.init(&p.batch, Schedule{p.head_items, p.tail_splits, p.n_units}, n_workers, worker);
+  // KV tile holding key kv_len-1 of a sequence when it is partial (else -1).
+  auto v_fix_tile = [](const SeqGeo& sq) { return sq.kv_len % kBlockN ? (sq.kv_len - 1) / kBlockN : -1; };
 
   if (warp == kTmaWarp) {
     // ======================= TMA producer ======================================
@@ -320,15 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       // Block-table entries (paged K/V); the K and V streams each keep their
-      // last entry in registers (they run one tile apart).
+      // last entry in registers (they run one tile apart; both are reset when
+      // an item of another sequence starts).
       int cached_pg[2] = {-1, -1}, cached_entry[2] = {0, 0};
-      const PagedGeom pgeo{p.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
       // One K tile is two 32 KB stages (d halves) in the one-CTA kernel and one
       // stage (this CTA's 64 keys) in a pair; likewise for V (key halves / this
       // CTA's 128 columns). A whole box is one copy; a paged box that crosses a
       // page is one copy per piece.
-      auto next_tile = [&](int n, bool is_k, int g) -> bool {
-        const bool v_fix = kPaged && !is_k && n == p.v_fix_tile;
+      auto next_tile = [&](const SeqGeo& sq, int n, bool is_k, int g) -> bool {
+        const bool v_fix = kPaged && !is_k && n == v_fix_tile(sq);
         const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
         const CUtensorMap* sub_map = is_k ? &p.tmap_k_sub : (v_fix ? &p.tmap_v16 : &p.tmap_v_sub);
         const int halves = is_k ? kKStagesPerTile : (kPair ? 1 : 2);
@@ -351,27 +352,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             nb = is_k ? static_cast<int>(kNchK) : 4;
             chunk0 = is_k ? static_cast<int>(kNchK) * half : 0;
           }
-          int row = r0;  // dense K/V: the box is the keys themselves
+          int row = sq.kv_start + r0;  // dense K/V: the box is the keys themselves
           bool whole = true;
           if constexpr (kPaged) {
             const int sid = is_k ? 0 : 1;
+            const int* table = p.block_table + static_cast<size_t>(sq.src) * p.bt_stride;
             auto read = [&](int pg) -> int {
               if (pg != cached_pg[sid]) {
-                cached_entry[sid] = __ldg(p.block_table + pg);
+                cached_entry[sid] = __ldg(table + pg);
                 cached_pg[sid] = pg;
               }
               return cached_entry[sid];
             };
+            const PagedGeom pgeo{sq.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
             bool bad = false;
             whole = paged_whole_box(pgeo, r0, rows, v_fix, read, &row, &bad);
             if (bad) atomicExch(p.status, static_cast<int>(GQA_ERR_PAGE_TABLE));
+            if (!whole)
+              issue_paged_pieces<kPair>(pgeo, table, p.status, sub_map, dst,
+                                        kPair ? lbar(kBarFull + st) : bar(kBarFull + st), r0, rows,
+                                        nb, chunk0, g, v_fix, pol_kv);
           }
-          if (whole) {
-            load_box(dst, full, kBarFull + st, row, g, chunk0);
-          } else if constexpr (kPaged) {
-            issue_paged_pieces<kPair>(p, sub_map, dst, kPair ? lbar(kBarFull + st) : bar(kBarFull + st),
-                                      r0, rows, nb, chunk0, g, v_fix, pol_kv);
-          }
+          if (whole) load_box(dst, full, kBarFull + st, row, g, chunk0);
           issued_mask |= 1u << st;
           issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
           if (++st == kStages) { st = 0; phase ^= 1u; }
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (use > 0 && !wait_bar(bar(kBarScEmpty + slot), (use - 1) & 1u, p)) return false;
             ptx::mbar_arrive_expect_tx(bar(kBarScFull + slot), kScSlotBytes);
             ptx::tma_load_2d(base + kOffScales + slot * kScSlotBytes, &p.tmap_ks,
-                             bar(kBarScFull + slot), n * kBlockN, g, pol_kv);
+                             bar(kBarScFull + slot), sq.kv_start + n * kBlockN, g, pol_kv);
             sc_issued_mask |= 1u << slot;
             sc_issued_parity = (sc_issued_parity & ~(1u << slot)) | ((use & 1u) << slot);
             ++sc_count;
@@ -392,26 +394,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       };
-      int k = 0;
+      int k = 0, last_seq = -1;
       Piece w;
       while (ok && pieces.next(w)) {
+        const SeqGeo& sq = p.batch.seq[w.seq];
+        if constexpr (kPaged) {
+          if (w.seq != last_seq) cached_pg[0] = cached_pg[1] = -1;
+        }
+        last_seq = w.seq;
         if (k > 0 && !(ok = wait_bar(bar(kBarQEmpty), (k - 1) & 1, p))) break;
         if (!(p.withhold_q && k == 0)) {
           if (leader)
             ptx::mbar_arrive_expect_tx(bar(kBarQFull), (kPair ? 2 : 1) * kQChunks * kQBoxBytes);
           for (int c = 0; c < kQChunks; ++c)
             load(q_smem + c * kQChunkBytes, &p.tmap_q, kBarQFull, kChunkElems * c, kGroup * w.g,
-                 tpi * w.qt + kTokPerTile * static_cast<int>(rank), pol_q);
+                 sq.q_start + tpi * w.qt + kTokPerTile * static_cast<int>(rank), pol_q);
           q_issued = true;
           q_parity = k & 1;
         }
         // Consumption order of the MMA warp: K0, K1, V0, K2, V1, ..., V(nt-1).
         const int nt = w.n1 - w.n0;
         for (int j = 0; j < nt && ok; ++j) {
-          ok = next_tile(w.n0 + j, true, w.g);
-          if (ok && j >= 1) ok = next_tile(w.n0 + j - 1, false, w.g);
+          ok = next_tile(sq, w.n0 + j, true, w.g);
+          if (ok && j >= 1) ok = next_tile(sq, w.n0 + j - 1, false, w.g);
         }
-        if (ok) ok = next_tile(w.n1 - 1, false, w.g);
+        if (ok) ok = next_tile(sq, w.n1 - 1, false, w.g);
         ++k;
       }
       // Every copy issued must have landed before the CTA exits. On the normal
@@ -497,14 +504,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           // O += P_j V_j in k-steps of 16 keys, N = 256. V stages are MN-major:
           // LBO = next 64-wide d chunk (kLboV), SBO = next group of 8 keys (kSboV).
-          const bool v_fix = kPaged && w.n0 + j == p.v_fix_tile;
+          const int vfix_tile = kPaged ? v_fix_tile(p.batch.seq[w.seq]) : -1;
+          const bool v_fix = kPaged && w.n0 + j == vfix_tile;
+          const int kr = p.batch.seq[w.seq].kv_len - vfix_tile * kBlockN;  // used when v_fix
           if constexpr (kPair) {
             // One stage: 128 keys x this CTA's 2 chunks of 64 columns.
             if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
             ptx::tc_fence_after();
             if (v_fix) {
-              zero_v_tail(stage_smem + st * kStageBytes, kNchV, 0, kRowsV, p, false);
-              zero_v_tail(ptx::map_to_cta(stage_smem + st * kStageBytes, 1), kNchV, 0, kRowsV, p,
+              zero_v_tail(stage_smem + st * kStageBytes, kNchV, 0, kRowsV, kr, false);
+              zero_v_tail(ptx::map_to_cta(stage_smem + st * kStageBytes, 1), kNchV, 0, kRowsV, kr,
                           true);
               ptx::fence_proxy_async_all();
             }
@@ -523,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
               ptx::tc_fence_after();
               if (v_fix) {
-                zero_v_tail(stage_smem + st * kStageBytes, kNchV, kRowsV * half, kRowsV, p, false);
+                zero_v_tail(stage_smem + st * kStageBytes, kNchV, kRowsV * half, kRowsV, kr, false);
                 ptx::fence_proxy_async_all();
               }
               const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
@@ -561,16 +570,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     Piece w;
     while (ok && pieces.next(w)) {
       const int nt = w.n1 - w.n0;
+      const SeqGeo& sq = p.batch.seq[w.seq];
+      const int p0 = sq.kv_len - sq.q_len;   // position of the sequence's first new token
       const int tok0 = tpi * w.qt + kTokPerTile * static_cast<int>(rank);  // this CTA's first token
-      const int tok = tok0 + tl;
-      const bool valid = row < kTokPerTile * kGroup && tok < p.q_len;
-      const int pos = p.p0 + tok;            // last key this row may see
-      const int tile_min_pos = p.p0 + tok0;  // smallest such key among this CTA's rows
+      const int tok = tok0 + tl;             // token within the sequence
+      const bool valid = row < kTokPerTile * kGroup && tok < sq.q_len;
+      const int pos = p0 + tok;              // last key this row may see
+      const int tile_min_pos = p0 + tok0;    // smallest such key among this CTA's rows
+      const size_t qrow = static_cast<size_t>(sq.q_start + tok) * kQHeads + kGroup * w.g + hj;
       // Score -> base-2 exponent factor: scale * log2(e), times the query's scale
       // for FP8 QK^T (the key's scale is applied per column below).
       float rowfac = sl2;
       if constexpr (kFp8) {
-        if (valid) rowfac = sl2 * __ldg(p.q_scale + static_cast<size_t>(tok) * kQHeads + kGroup * w.g + hj);
+        if (valid) rowfac = sl2 * __ldg(p.q_scale + qrow);
       }
       float m_ref = kNegInf;  // max used in the exponent (base-2, scaled)
       float l = 0.0f;         // running row sum of p
@@ -685,7 +697,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
       const float lse2 = l > 0.0f ? m_ref + __log2f(l) : kNegInf;
-      const size_t qrow = static_cast<size_t>(tok) * kQHeads + kGroup * w.g + hj;
       if (w.slot < 0) {
         __nv_bfloat16* dst = p.out + qrow * kHeadDim;
 #pragma unroll 1
@@ -768,12 +779,12 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-__global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(256) merge_tail_kernel(const __grid_constant__ MergeParams p) {
   const int j = blockIdx.x;                               // tail item
   const int row_begin = blockIdx.y * kMergeRowsPerBlock;  // its rows, both CTAs of a pair
-  const int item = p.head_items + j;
-  const int qt = p.n_qtiles - 1 - item / 4;
-  const int g = item % 4;
+  int seq, qt, g;
+  item_of(p.batch, p.head_items + j, seq, qt, g);
+  const SeqGeo& sq = p.batch.seq[seq];
   const int S = p.tail_splits;
   const int cpi = p.ctas_per_item;
   const int lane = threadIdx.x & 31;
@@ -781,8 +792,8 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
   for (int rr = row_begin + (threadIdx.x >> 5); rr < row_end; rr += 8) {
     const int r = rr / (kTokPerTile * kGroup);    // CTA of the item
     const int row = rr % (kTokPerTile * kGroup);  // its MMA row
-    const int tok = kTokPerTile * (cpi * qt + r) + row / kGroup;
-    if (tok >= p.q_len) continue;
+    const int tok = kTokPerTile * (cpi * qt + r) + row / kGroup;  // token within the sequence
+    if (tok >= sq.q_len) continue;
     // Partial row of piece s: slot (j*S + s), CTA r, MMA row `row`.
     auto prow = [&](int s) {
       return (static_cast<size_t>(j * S + s) * cpi + r) * kRowsPerTile + row;
@@ -813,7 +824,7 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const MergeParams p) {
     o.y = ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv);
     o.z = ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv);
     o.w = ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    const size_t orow = static_cast<size_t>(tok) * kQHeads + kGroup * g + row % kGroup;
+    const size_t orow = static_cast<size_t>(sq.q_start + tok) * kQHeads + kGroup * g + row % kGroup;
     *reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 8 * lane) = o;
     if (lane == 0 && p.lse != nullptr)
       p.lse[orow] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;

@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "gqa_schedule.h"
+
 namespace gqa {
 
 // Fixed problem geometry (the only shape the library accepts).
@@ -34,10 +36,6 @@ struct FwdParams {
   float* part_o;       // [tail pieces][128 rows][256] normalised partial O (tail_splits > 1)
   float* part_lse;     // [tail pieces][128 rows] base-2 partial LSE        (tail_splits > 1)
   int* status;         // per-device status word
-  int q_len;
-  int kv_len;
-  int p0;              // kv_len - q_len: position of the chunk's first token
-  int n_qtiles;        // ceil(q_len / tokens per item): 21, or 42 for CTA pairs
   int head_items;      // Schedule (gqa_schedule.h): items processed whole first
   int tail_splits;     //   pieces per remaining item
   int n_units;         //   units dealt to the CTAs
@@ -49,16 +47,17 @@ struct FwdParams {
   CUtensorMap tmap_k_sub;    // 5-D, sub_rows keys x the stage's chunks: pieces of a box
   CUtensorMap tmap_v_sub;    //   that crosses a page
   CUtensorMap tmap_v16;      // 5-D, 16 keys: V of the tile holding key kv_len-1
-  const int* block_table;    // [ceil(kv_len / page_size)] physical page of each logical page
+  const int* block_table;    // sequence b's row at b * bt_stride: physical page of each
+  int bt_stride;             //   logical page (ceil(kv_len_b / page_size) used entries)
   int page_size;             // keys per page, a multiple of 16
   int num_pages;             // pages in the cache
   int sub_rows;              // gcd(page_size, 64)
   int oob_row;               // num_pages * page_size: a row past the cache (TMA zero fill)
-  int v_fix_tile;            // KV tile holding key kv_len-1 if kv_len % 128 != 0, else -1
   // FP8 QK^T (kernels instantiated with kFp8 only): tmap_q / tmap_k hold E4M3 codes
   // (Q box (128, 6 heads, 21 tokens); K 4-D (128, key, head, chunk) with 2 chunks).
   CUtensorMap tmap_ks;       // key scales FP32 [4][k_scale_stride], box (128 keys, 1 head)
-  const float* q_scale;      // [q_len][24] FP32 query scales
+  const float* q_scale;      // [total q rows][24] FP32 query scales
+  Batch batch;               // the call's sequences (gqa_schedule.h); kept last: it is large
 };
 
 struct MergeParams {
@@ -66,12 +65,11 @@ struct MergeParams {
   const float* part_lse;  // as FwdParams::part_lse
   __nv_bfloat16* out;
   float* lse;             // may be null
-  int q_len;
-  int n_qtiles;
   int head_items;
   int tail_items;         // one merge block per tail item
   int tail_splits;
   int ctas_per_item;      // 1, or 2 for the CTA-pair kernel (42-token items)
+  Batch batch;            // as FwdParams::batch
 };
 
 size_t fwd_smem_bytes();

@@ -26,6 +26,7 @@
 namespace gqa {
 namespace {
 
+static_assert(kMaxSeqs == GQA_MAX_SEQS, "the sequence table and the public limit must agree");
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per device-side wait
 
@@ -43,41 +44,89 @@ constexpr double kMergeLaunchUs = 6.0;
 constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
 constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 24, 32};
 
-Geometry geometry(int q_len, int kv_len, int variant) {
-  const int tpi = variant == 2 ? 2 * kTokPerTile : kTokPerTile;
-  return Geometry{q_len, kv_len - q_len, (q_len + tpi - 1) / tpi, tpi};
+// One sequence of a call as the caller gives it: its rows in the packed Q /
+// out / LSE and (dense K/V) K / V.
+struct SeqIn {
+  int q_start, q_len, kv_start, kv_len;
+};
+
+int tok_per_item(int variant) { return variant == 2 ? 2 * kTokPerTile : kTokPerTile; }
+
+// The call's sequence table for `variant`: empty sequences left out, the rest
+// ordered by their longest item (longest first; ties keep the caller's order),
+// with the items of the sequences before each one counted in item_begin.
+void build_batch(const std::vector<SeqIn>& in, int variant, Batch* b) {
+  const int tpi = tok_per_item(variant);
+  std::vector<int> idx;
+  std::vector<int> longest(in.size(), 0);
+  for (size_t i = 0; i < in.size(); ++i) {
+    if (in[i].q_len <= 0) continue;
+    idx.push_back(static_cast<int>(i));
+    const SeqGeo g{0, in[i].q_len, 0, in[i].kv_len, (in[i].q_len + tpi - 1) / tpi, 0, 0};
+    longest[i] = item_tiles(g, tpi, g.n_qtiles - 1);
+  }
+  std::stable_sort(idx.begin(), idx.end(), [&](int a, int c) { return longest[a] > longest[c]; });
+  b->n_seq = static_cast<int>(idx.size());
+  b->tok_per_item = tpi;
+  int items = 0;
+  for (size_t k = 0; k < idx.size(); ++k) {
+    const SeqIn& s = in[static_cast<size_t>(idx[k])];
+    const int n_qtiles = (s.q_len + tpi - 1) / tpi;
+    b->seq[k] = SeqGeo{s.q_start, s.q_len, s.kv_start, s.kv_len, n_qtiles, items, idx[k]};
+    items += kKvHeads * n_qtiles;
+  }
+  b->n_items = items;
+}
+
+// KV tiles of every item of the call, in the call's item order.
+std::vector<int> item_tile_counts(const Batch& b) {
+  std::vector<int> t(static_cast<size_t>(b.n_items));
+  for (int i = 0; i < b.n_items; ++i) {
+    int seq, qt, g;
+    item_of(b, i, seq, qt, g);
+    t[static_cast<size_t>(i)] = item_tiles(b.seq[seq], b.tok_per_item, qt);
+  }
+  return t;
 }
 
 // Fills *plan for `variant` (1: one CTA per item, 2: a CTA pair per item) with
 // head_rounds whole rounds and S-way tail splits over `workers` CTAs (or
-// pairs); S must not exceed the shortest item's tiles. Returns the estimated
+// pairs), simulating the snake deal of gqa_schedule.h over the items' tile
+// counts; S must not exceed the shortest item's tiles. Returns the estimated
 // time in us.
-double plan_schedule(const Geometry& geo, int num_sms, int variant, int workers, int head_rounds,
-                     int S, gqa_prefill_plan* plan) {
-  const int n_items = geo.n_qtiles * kKvHeads;
+double plan_schedule(const std::vector<int>& tiles, int q_tiles, int num_sms, int variant,
+                     int workers, int head_rounds, int S, gqa_prefill_plan* plan) {
+  const int n_items = static_cast<int>(tiles.size());
   const int cpi = variant == 2 ? 2 : 1;
   const int head = std::min(head_rounds * workers, n_items);
-  const Schedule sc{head, S, head + (n_items - head) * S};
-  workers = std::max(1, std::min(workers, sc.n_units));
+  const int n_units = head + (n_items - head) * S;
+  workers = std::max(1, std::min(workers, n_units));
   std::vector<int64_t> load(static_cast<size_t>(workers), 0);
   int64_t total = 0;
-  for (int u = 0; u < sc.n_units; ++u) {
+  for (int u = 0; u < n_units; ++u) {
     const int r = u / workers, x = u % workers;
     const int b = (r & 1) ? workers - 1 - x : x;
-    const Piece w = unit_piece(geo, sc, u);
-    load[static_cast<size_t>(b)] += (w.n1 - w.n0) + kPieceOverheadTiles;
-    total += w.n1 - w.n0;
+    int len;
+    if (u < head) {
+      len = tiles[static_cast<size_t>(u)];
+    } else {
+      const int t = u - head, s = t % S;
+      const int64_t nt = tiles[static_cast<size_t>(head + t / S)];
+      len = static_cast<int>((s + 1) * nt / S - s * nt / S);
+    }
+    load[static_cast<size_t>(b)] += len + kPieceOverheadTiles;
+    total += len;
   }
   const int tail = n_items - head;
   const bool split = S > 1 && tail > 0;
   std::memset(plan, 0, sizeof(*plan));
   plan->num_sms = num_sms;
-  plan->q_tiles = geo.n_qtiles;
+  plan->q_tiles = q_tiles;
   plan->n_items = n_items;
   plan->head_rounds = head / workers;
   plan->tail_items = tail;
   plan->tail_splits = S;
-  plan->n_units = sc.n_units;
+  plan->n_units = n_units;
   plan->grid = workers * cpi;
   plan->kernels_per_call = split ? 2 : 1;
   plan->variant = variant;
@@ -94,23 +143,29 @@ double plan_schedule(const Geometry& geo, int num_sms, int variant, int workers,
   return us;
 }
 
-// Best plan of one variant: searches the number of whole rounds and the tail
-// split; a split must win by 2 % over the simpler plan to be taken.
-double best_plan_of(int q_len, int kv_len, int num_sms, int variant, int workers, int force_splits,
-                    gqa_prefill_plan* plan) {
-  const Geometry geo = geometry(q_len, kv_len, variant);
-  const int n_items = geo.n_qtiles * kKvHeads;
-  const int max_splits = std::max(1, item_tiles(geo, 0));  // the shortest item's tiles
+// Best plan of one variant: searches the number of whole rounds (the last few
+// full rounds and none) and the tail split; a split must win by 2 % over the
+// simpler plan to be taken.
+double best_plan_of(const std::vector<SeqIn>& seqs, int num_sms, int variant, int workers,
+                    int force_splits, gqa_prefill_plan* plan) {
+  static thread_local Batch b;  // large: not on the stack
+  build_batch(seqs, variant, &b);
+  const std::vector<int> tiles = item_tile_counts(b);
+  int q_tiles = 0;
+  for (int i = 0; i < b.n_seq; ++i) q_tiles += b.seq[i].n_qtiles;
+  const int n_items = static_cast<int>(tiles.size());
+  const int max_splits = std::max(1, *std::min_element(tiles.begin(), tiles.end()));
   const int full_rounds = n_items / workers;
   if (force_splits > 0)
-    return plan_schedule(geo, num_sms, variant, workers, full_rounds,
+    return plan_schedule(tiles, q_tiles, num_sms, variant, workers, full_rounds,
                          std::min(force_splits, max_splits), plan);
-  double best = plan_schedule(geo, num_sms, variant, workers, 0, 1, plan);  // whole items only
+  double best = plan_schedule(tiles, q_tiles, num_sms, variant, workers, 0, 1, plan);
   gqa_prefill_plan cand{};
   for (int hr = full_rounds; hr >= 0; --hr) {
+    if (hr < full_rounds - 3 && hr != 0) continue;
     for (int S : kSplitCandidates) {
       if (S == 1 || S > max_splits) continue;
-      const double us = plan_schedule(geo, num_sms, variant, workers, hr, S, &cand);
+      const double us = plan_schedule(tiles, q_tiles, num_sms, variant, workers, hr, S, &cand);
       if (us < 0.98 * best) {
         best = us;
         *plan = cand;
@@ -120,41 +175,39 @@ double best_plan_of(int q_len, int kv_len, int num_sms, int variant, int workers
   return best;
 }
 
-// Pure function of its arguments. max_pairs: CTA pairs that can be resident at
-// once. force_grid caps the CTAs launched (a pair counts as two).
-void compute_plan(int q_len, int kv_len, int num_sms, int max_pairs, int force_splits,
+// Pure function of its arguments (seqs: at least one non-empty sequence).
+// max_pairs: CTA pairs that can be resident at once. force_grid caps the CTAs
+// launched (a pair counts as two).
+void compute_plan(const std::vector<SeqIn>& seqs, int num_sms, int max_pairs, int force_splits,
                   int force_grid, int force_variant, gqa_prefill_plan* plan) {
   const int cap = force_grid > 0 ? std::min(force_grid, num_sms) : num_sms;
   const int workers1 = std::max(1, cap);
   const int workers2 = std::max(1, std::min(max_pairs, cap / 2));
   if (force_variant == 1 || (force_variant == 0 && max_pairs < 1)) {
-    best_plan_of(q_len, kv_len, num_sms, 1, workers1, force_splits, plan);
+    best_plan_of(seqs, num_sms, 1, workers1, force_splits, plan);
     return;
   }
   if (force_variant == 2) {
-    best_plan_of(q_len, kv_len, num_sms, 2, workers2, force_splits, plan);
+    best_plan_of(seqs, num_sms, 2, workers2, force_splits, plan);
     return;
   }
   gqa_prefill_plan one{}, pair{};
-  const double t1 = best_plan_of(q_len, kv_len, num_sms, 1, workers1, force_splits, &one);
-  const double t2 = best_plan_of(q_len, kv_len, num_sms, 2, workers2, force_splits, &pair);
+  const double t1 = best_plan_of(seqs, num_sms, 1, workers1, force_splits, &one);
+  const double t2 = best_plan_of(seqs, num_sms, 2, workers2, force_splits, &pair);
   *plan = t2 < 0.98 * t1 ? pair : one;
 }
 
-struct PlanKey {
-  int q_len, kv_len, num_sms, max_pairs, force_splits, force_grid, force_variant;
-  bool operator<(const PlanKey& o) const {
-    return std::tie(q_len, kv_len, num_sms, max_pairs, force_splits, force_grid, force_variant) <
-           std::tie(o.q_len, o.kv_len, o.num_sms, o.max_pairs, o.force_splits, o.force_grid,
-                    o.force_variant);
-  }
-};
-
-void cached_plan(int q_len, int kv_len, int num_sms, int max_pairs, int force_splits,
+// Plans keyed by everything they depend on: the device, the options and the
+// (q_len, kv_len) of every sequence in the caller's order.
+void cached_plan(const std::vector<SeqIn>& seqs, int num_sms, int max_pairs, int force_splits,
                  int force_grid, int force_variant, gqa_prefill_plan* plan) {
   static std::mutex mu;
-  static std::map<PlanKey, gqa_prefill_plan> cache;
-  const PlanKey key{q_len, kv_len, num_sms, max_pairs, force_splits, force_grid, force_variant};
+  static std::map<std::vector<int>, gqa_prefill_plan> cache;
+  std::vector<int> key{num_sms, max_pairs, force_splits, force_grid, force_variant};
+  for (const SeqIn& s : seqs) {
+    key.push_back(s.q_len);
+    key.push_back(s.kv_len);
+  }
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -163,23 +216,46 @@ void cached_plan(int q_len, int kv_len, int num_sms, int max_pairs, int force_sp
       return;
     }
   }
-  compute_plan(q_len, kv_len, num_sms, max_pairs, force_splits, force_grid, force_variant, plan);
+  compute_plan(seqs, num_sms, max_pairs, force_splits, force_grid, force_variant, plan);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
-  cache.emplace(key, *plan);
+  cache.emplace(std::move(key), *plan);
 }
 
 // --------------------------------------------------------------- validation --
-gqa_status validate_shape(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                          float scale) {
-  if (q_len < 0 || kv_len < q_len) return GQA_ERR_SHAPE;
+
+bool misaligned(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
+
+gqa_status validate_heads(int n_q_heads, int n_kv_heads, int head_dim, float scale) {
   if (!(std::isfinite(scale) && scale > 0.0f)) return GQA_ERR_SHAPE;
   if (n_q_heads != kQHeads || n_kv_heads != kKvHeads || head_dim != kHeadDim)
     return GQA_ERR_UNSUPPORTED;
   return GQA_OK;
 }
 
-bool misaligned(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; }
+// Sequences of a batched call from the caller's HOST arrays: query rows
+// cu_q[b] .. cu_q[b+1]-1 and, with dense K/V, key rows cu_k[b] .. cu_k[b+1]-1;
+// with paged K/V (cu_k null) kv_lens[b] keys through block-table row b.
+gqa_status batch_from_host(const int32_t* cu_q, const int32_t* cu_k, const int32_t* kv_lens,
+                           int batch, std::vector<SeqIn>* seqs, int* total_q, int64_t* total_kv) {
+  if (batch < 0) return GQA_ERR_SHAPE;
+  if (batch > kMaxSeqs) return GQA_ERR_UNSUPPORTED;
+  seqs->clear();
+  *total_q = 0;
+  *total_kv = 0;
+  if (batch == 0) return GQA_OK;
+  if (!cu_q || (!cu_k && !kv_lens)) return GQA_ERR_NULL;
+  if (cu_q[0] != 0 || (cu_k && cu_k[0] != 0)) return GQA_ERR_SHAPE;
+  for (int b = 0; b < batch; ++b) {
+    const int q_len = cu_q[b + 1] - cu_q[b];
+    const int kv_len = cu_k ? cu_k[b + 1] - cu_k[b] : kv_lens[b];
+    if (cu_q[b + 1] < cu_q[b] || kv_len < 0 || q_len > kv_len) return GQA_ERR_SHAPE;
+    seqs->push_back(SeqIn{cu_q[b], q_len, cu_k ? cu_k[b] : 0, kv_len});
+  }
+  *total_q = cu_q[batch];
+  *total_kv = cu_k ? cu_k[batch] : 0;
+  return GQA_OK;
+}
 
 // ------------------------------------------------------------ device state --
 // Per-device facts both entry points need: SM count, co-resident CTA pairs and
@@ -330,31 +406,33 @@ bool encode_key_scales(CUtensorMap* map, const float* base, uint64_t kv_len, uin
                 CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Checks every argument; on success fills *plan (q_len == 0 gives an empty plan).
-gqa_status check_call(const void* q, const void* k, const void* v, const void* out,
-                      const float* lse, int q_len, int kv_len, int n_q_heads, int n_kv_heads,
-                      int head_dim, float scale) {
-  gqa_status st = validate_shape(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
-  if (st != GQA_OK || q_len == 0) return st;  // empty chunk: pointers may be NULL
+// Pointers of a call that has work to do (with none, they may be NULL).
+gqa_status check_pointers(const void* q, const void* k, const void* v, const void* out,
+                          const float* lse) {
   if (!q || !k || !v || !out) return GQA_ERR_NULL;
   if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out) || misaligned(lse))
     return GQA_ERR_ALIGN;
   return GQA_OK;
 }
 
-// K/V of a paged call: the caches span num_pages * page_size rows.
+// K/V of a paged call: the caches span num_pages * page_size rows; sequence
+// b's block-table row starts at b * bt_stride.
 struct PagedKV {
   const int32_t* block_table;
+  int bt_stride;
   int num_pages;
   int page_size;
 };
 constexpr int64_t kMaxCacheRows = int64_t{1} << 30;  // TMA row coordinates stay far from 2^31
 
-gqa_status check_paged(const PagedKV& pkv, int q_len) {
+gqa_status check_paged(const PagedKV& pkv, const std::vector<SeqIn>& seqs, bool work) {
   if (pkv.page_size <= 0 || pkv.page_size % 16 != 0) return GQA_ERR_UNSUPPORTED;
   if (pkv.num_pages < 1 || static_cast<int64_t>(pkv.num_pages) * pkv.page_size >= kMaxCacheRows)
     return GQA_ERR_SHAPE;
-  if (q_len == 0) return GQA_OK;
+  for (const SeqIn& s : seqs)  // every row must hold the sequence's pages
+    if (seqs.size() > 1 && (s.kv_len + pkv.page_size - 1) / pkv.page_size > pkv.bt_stride)
+      return GQA_ERR_SHAPE;
+  if (!work) return GQA_OK;
   if (!pkv.block_table) return GQA_ERR_NULL;
   if ((reinterpret_cast<uintptr_t>(pkv.block_table) & 3u) != 0) return GQA_ERR_ALIGN;
   return GQA_OK;
@@ -367,11 +445,11 @@ struct Fp8Qk {
   int k_scale_stride;
 };
 
-gqa_status check_fp8(const Fp8Qk& f8, int q_len, int kv_len) {
-  if (f8.k_scale_stride < kv_len || f8.k_scale_stride % 4 != 0 ||
+gqa_status check_fp8(const Fp8Qk& f8, int64_t key_rows, bool work) {
+  if (f8.k_scale_stride < key_rows || f8.k_scale_stride % 4 != 0 ||
       static_cast<int64_t>(f8.k_scale_stride) * kKvHeads >= (int64_t{1} << 31))
     return GQA_ERR_SHAPE;
-  if (q_len == 0) return GQA_OK;
+  if (!work) return GQA_OK;
   if (!f8.q_scale || !f8.k_scale) return GQA_ERR_NULL;
   if ((reinterpret_cast<uintptr_t>(f8.q_scale) & 3u) != 0 || misaligned(f8.k_scale))
     return GQA_ERR_ALIGN;
@@ -387,65 +465,73 @@ int gcd_int(int a, int b) {
   return a;
 }
 
+// Tensors and options of one call.
+struct CallIO {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  const PagedKV* pkv;  // null: dense K/V; else k and v are the paged caches
+  const Fp8Qk* f8;     // null: BF16 Q/K; else q and k are E4M3 codes with these scales
+  float scale;
+};
+
 // Launches `plan` on `stream`; `ws` holds plan.workspace_bytes (or nothing).
-// `pkv` is null for dense K/V, otherwise k and v are the paged caches; `f8` is
-// null for BF16 Q/K, otherwise q and k are E4M3 codes with its scales.
-gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* k, const void* v,
-                       const PagedKV* pkv, const Fp8Qk* f8, void* out, float* lse, int q_len,
-                       int kv_len, float scale, int* status_word, void* ws,
-                       const gqa_prefill_opts* opts, cudaStream_t stream) {
+// total_q / total_kv: rows of the packed Q and (dense) K/V.
+gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
+                       const std::vector<SeqIn>& seqs, int total_q, int64_t total_kv,
+                       int* status_word, void* ws, const gqa_prefill_opts* opts,
+                       cudaStream_t stream) {
   const bool pair = plan.variant == 2;
-  if (pkv && f8) return GQA_ERR_UNSUPPORTED;
-  FwdParams p;
+  if (io.pkv && io.f8) return GQA_ERR_UNSUPPORTED;
+  static thread_local FwdParams p;  // ~5 KB with the sequence table: not on the stack
   std::memset(&p, 0, sizeof(p));
-  const uint64_t kv_rows = pkv ? static_cast<uint64_t>(pkv->num_pages) * pkv->page_size
-                               : static_cast<uint64_t>(kv_len);
-  const Elem qk = f8 ? kE4m3 : kBf16;
+  const uint64_t kv_rows = io.pkv ? static_cast<uint64_t>(io.pkv->num_pages) * io.pkv->page_size
+                                  : static_cast<uint64_t>(total_kv);
+  const Elem qk = io.f8 ? kE4m3 : kBf16;
   // K/V stages per CTA: one-CTA K 128 keys (BF16: 2 chunks per stage, 2 stages;
   // FP8: all 2 chunks), V 64 keys x 4 chunks; pairs K 64 keys x all chunks,
   // V 128 keys x 2 chunks.
   const uint32_t k_rows = pair ? 64 : kBlockN;
-  const uint32_t k_chunks = f8 ? 2 : (pair ? 4 : 2);
+  const uint32_t k_chunks = io.f8 ? 2 : (pair ? 4 : 2);
   const uint32_t v_rows = pair ? kBlockN : 64, v_chunks = pair ? 2 : 4;
-  if (!encode_q(&p.tmap_q, q, static_cast<uint64_t>(q_len), qk)) return GQA_ERR_CUDA;
-  p.v_fix_tile = -1;
-  if (!pkv) {
-    if (!encode_kv(&p.tmap_k, k, kv_rows, k_rows, k_chunks, qk) ||
-        !encode_kv(&p.tmap_v, v, kv_rows, v_rows, v_chunks, kBf16))
+  if (!encode_q(&p.tmap_q, io.q, static_cast<uint64_t>(total_q), qk)) return GQA_ERR_CUDA;
+  if (!io.pkv) {
+    if (!encode_kv(&p.tmap_k, io.k, kv_rows, k_rows, k_chunks, qk) ||
+        !encode_kv(&p.tmap_v, io.v, kv_rows, v_rows, v_chunks, kBf16))
       return GQA_ERR_CUDA;
   } else {
-    const uint32_t sub = static_cast<uint32_t>(gcd_int(pkv->page_size, 64));  // 16, 32 or 64
-    if (!encode_kv_paged(&p.tmap_k, k, kv_rows, k_rows, k_chunks) ||
-        !encode_kv_paged(&p.tmap_v, v, kv_rows, v_rows, v_chunks) ||
-        !encode_kv_paged(&p.tmap_k_sub, k, kv_rows, sub, k_chunks) ||
-        !encode_kv_paged(&p.tmap_v_sub, v, kv_rows, sub, v_chunks) ||
-        !encode_kv_paged(&p.tmap_v16, v, kv_rows, 16, v_chunks))
+    const PagedKV& pkv = *io.pkv;
+    const uint32_t sub = static_cast<uint32_t>(gcd_int(pkv.page_size, 64));  // 16, 32 or 64
+    if (!encode_kv_paged(&p.tmap_k, io.k, kv_rows, k_rows, k_chunks) ||
+        !encode_kv_paged(&p.tmap_v, io.v, kv_rows, v_rows, v_chunks) ||
+        !encode_kv_paged(&p.tmap_k_sub, io.k, kv_rows, sub, k_chunks) ||
+        !encode_kv_paged(&p.tmap_v_sub, io.v, kv_rows, sub, v_chunks) ||
+        !encode_kv_paged(&p.tmap_v16, io.v, kv_rows, 16, v_chunks))
       return GQA_ERR_CUDA;
-    p.block_table = pkv->block_table;
-    p.page_size = pkv->page_size;
-    p.num_pages = pkv->num_pages;
+    p.block_table = pkv.block_table;
+    p.bt_stride = pkv.bt_stride;
+    p.page_size = pkv.page_size;
+    p.num_pages = pkv.num_pages;
     p.sub_rows = static_cast<int>(sub);
     p.oob_row = static_cast<int>(kv_rows);
-    if (kv_len % kBlockN != 0) p.v_fix_tile = (kv_len - 1) / kBlockN;
   }
-  if (f8) {
-    if (!encode_key_scales(&p.tmap_ks, f8->k_scale, static_cast<uint64_t>(kv_len),
-                           static_cast<uint64_t>(f8->k_scale_stride)))
+  if (io.f8) {
+    if (!encode_key_scales(&p.tmap_ks, io.f8->k_scale, static_cast<uint64_t>(total_kv),
+                           static_cast<uint64_t>(io.f8->k_scale_stride)))
       return GQA_ERR_CUDA;
-    p.q_scale = f8->q_scale;
+    p.q_scale = io.f8->q_scale;
   }
+  build_batch(seqs, plan.variant, &p.batch);
   const int workers = pair ? plan.grid / 2 : plan.grid;
-  p.out = static_cast<__nv_bfloat16*>(out);
-  p.lse = lse;
+  p.out = static_cast<__nv_bfloat16*>(io.out);
+  p.lse = io.lse;
   p.status = status_word;
-  p.q_len = q_len;
-  p.kv_len = kv_len;
-  p.p0 = kv_len - q_len;
-  p.n_qtiles = plan.q_tiles;
   p.head_items = std::min(plan.head_rounds * workers, plan.n_items);
   p.tail_splits = plan.tail_splits;
   p.n_units = plan.n_units;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale_log2 = io.scale * 1.4426950408889634f;
   p.timeout_ns = (opts && opts->wait_timeout_us) ? 1000ull * opts->wait_timeout_us
                                                  : kDefaultTimeoutNs;
   p.withhold_q = (opts && opts->test_withhold_q) ? 1 : 0;
@@ -457,30 +543,41 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const void* q, const void* 
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return GQA_ERR_CUDA;
-  if (launch_fwd(p, plan.grid, pair, pkv != nullptr, f8 != nullptr, stream) != cudaSuccess)
+  if (launch_fwd(p, plan.grid, pair, io.pkv != nullptr, io.f8 != nullptr, stream) != cudaSuccess)
     return GQA_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return GQA_ERR_CUDA;
   if (plan.kernels_per_call == 2) {
-    MergeParams m{p.part_o, p.part_lse, p.out, lse, q_len, p.n_qtiles, p.head_items,
-                  plan.tail_items, plan.tail_splits, pair ? 2 : 1};
+    static thread_local MergeParams m;
+    m.part_o = p.part_o;
+    m.part_lse = p.part_lse;
+    m.out = p.out;
+    m.lse = io.lse;
+    m.head_items = p.head_items;
+    m.tail_items = plan.tail_items;
+    m.tail_splits = plan.tail_splits;
+    m.ctas_per_item = pair ? 2 : 1;
+    m.batch = p.batch;
     if (launch_merge(m, stream) != cudaSuccess) return GQA_ERR_CUDA;
   }
   return GQA_OK;
 }
 
-gqa_status run(const void* q, const void* k, const void* v, const PagedKV* pkv, const Fp8Qk* f8,
-               void* out, float* lse, int q_len, int kv_len, int n_q_heads, int n_kv_heads,
-               int head_dim, float scale, void* stream_ptr, const gqa_prefill_opts* opts,
-               gqa_prefill_plan* plan_out) {
+// Every entry point but the allocation-free one: check, plan, take split
+// partials from the pool, launch.
+gqa_status run(const CallIO& io, const std::vector<SeqIn>& seqs, int total_q, int64_t total_kv,
+               int n_q_heads, int n_kv_heads, int head_dim, void* stream_ptr,
+               const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out) {
   if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
-  gqa_status st = check_call(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
-  if (st == GQA_OK && pkv) st = check_paged(*pkv, q_len);
-  if (st == GQA_OK && f8) st = check_fp8(*f8, q_len, kv_len);
-  if (st != GQA_OK || q_len == 0) return st;
+  gqa_status st = validate_heads(n_q_heads, n_kv_heads, head_dim, io.scale);
+  const bool work = total_q > 0;
+  if (st == GQA_OK && work) st = check_pointers(io.q, io.k, io.v, io.out, io.lse);
+  if (st == GQA_OK && io.pkv) st = check_paged(*io.pkv, seqs, work);
+  if (st == GQA_OK && io.f8) st = check_fp8(*io.f8, total_kv, work);
+  if (st != GQA_OK || !work) return st;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != GQA_OK) return st;
   gqa_prefill_plan plan{};
-  cached_plan(q_len, kv_len, dev->num_sms, dev->max_pairs, opts ? opts->force_splits : 0,
+  cached_plan(seqs, dev->num_sms, dev->max_pairs, opts ? opts->force_splits : 0,
               opts ? opts->force_grid : 0, opts ? opts->force_variant : 0, &plan);
   if (plan_out) *plan_out = plan;
   auto stream = static_cast<cudaStream_t>(stream_ptr);
@@ -492,10 +589,19 @@ gqa_status run(const void* q, const void* k, const void* v, const PagedKV* pkv, 
         cudaSuccess)
       return GQA_ERR_CUDA;
   }
-  st = launch_plan(plan, q, k, v, pkv, f8, out, lse, q_len, kv_len, scale, dev->status_word, ws,
-                   opts, stream);
+  st = launch_plan(plan, io, seqs, total_q, total_kv, dev->status_word, ws, opts, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   return st;
+}
+
+// One sequence: q_len tokens at the end of kv_len keys (the non-batched calls).
+gqa_status run_one(const CallIO& io, int q_len, int kv_len, int n_q_heads, int n_kv_heads,
+                   int head_dim, void* stream, const gqa_prefill_opts* opts,
+                   gqa_prefill_plan* plan_out) {
+  if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
+  if (q_len < 0 || kv_len < q_len) return GQA_ERR_SHAPE;
+  const std::vector<SeqIn> seqs{SeqIn{0, q_len, 0, kv_len}};
+  return run(io, seqs, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
 }
 
 // ---------------------------------------------------- allocation-free variant --
@@ -529,19 +635,23 @@ gqa_status noalloc_scratch(void** out) {
 gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
                        int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                        float scale, void* stream_ptr) {
-  gqa_status st = check_call(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale);
+  if (q_len < 0 || kv_len < q_len) return GQA_ERR_SHAPE;
+  gqa_status st = validate_heads(n_q_heads, n_kv_heads, head_dim, scale);
   if (st != GQA_OK || q_len == 0) return st;
+  if ((st = check_pointers(q, k, v, out, lse)) != GQA_OK) return st;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != GQA_OK) return st;
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != GQA_OK) return st;
+  const std::vector<SeqIn> seqs{SeqIn{0, q_len, 0, kv_len}};
   gqa_prefill_plan plan{};
-  cached_plan(q_len, kv_len, dev->num_sms, dev->max_pairs, 0, 0, 0, &plan);
+  cached_plan(seqs, dev->num_sms, dev->max_pairs, 0, 0, 0, &plan);
   if (static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes) return GQA_ERR_SCRATCH;
   // Every partial row the merge reads is written by the attention kernel first,
   // so the scratch needs no clearing between calls.
-  return launch_plan(plan, q, k, v, nullptr, nullptr, out, lse, q_len, kv_len, scale,
-                     dev->status_word, scratch, nullptr, static_cast<cudaStream_t>(stream_ptr));
+  const CallIO io{q, k, v, out, lse, nullptr, nullptr, scale};
+  return launch_plan(plan, io, seqs, q_len, kv_len, dev->status_word, scratch, nullptr,
+                     static_cast<cudaStream_t>(stream_ptr));
 }
 
 }  // namespace
@@ -560,25 +670,26 @@ gqa_status gqa_prefill_attn_noalloc(const void* q, const void* k, const void* v,
 gqa_status gqa_prefill_attn(const void* q, const void* k, const void* v, void* out, float* lse,
                             int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                             float scale, void* stream) {
-  return gqa::run(q, k, v, nullptr, nullptr, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
-                  head_dim, scale, stream, nullptr, nullptr);
+  const gqa::CallIO io{q, k, v, out, lse, nullptr, nullptr, scale};
+  return gqa::run_one(io, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, stream, nullptr,
+                      nullptr);
 }
 
 gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void* out, float* lse,
                                int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                                float scale, void* stream, const gqa_prefill_opts* opts,
                                gqa_prefill_plan* plan_out) {
-  return gqa::run(q, k, v, nullptr, nullptr, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
-                  head_dim, scale, stream, opts, plan_out);
+  const gqa::CallIO io{q, k, v, out, lse, nullptr, nullptr, scale};
+  return gqa::run_one(io, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
 }
 
 gqa_status gqa_prefill_attn_paged(const void* q, const void* k_cache, const void* v_cache,
                                   const int32_t* block_table, int num_pages, int page_size,
                                   void* out, float* lse, int q_len, int kv_len, int n_q_heads,
                                   int n_kv_heads, int head_dim, float scale, void* stream) {
-  const gqa::PagedKV pkv{block_table, num_pages, page_size};
-  return gqa::run(q, k_cache, v_cache, &pkv, nullptr, out, lse, q_len, kv_len, n_q_heads,
-                  n_kv_heads, head_dim, scale, stream, nullptr, nullptr);
+  return gqa_prefill_attn_paged_ex(q, k_cache, v_cache, block_table, num_pages, page_size, out,
+                                   lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
+                                   stream, nullptr, nullptr);
 }
 
 gqa_status gqa_prefill_attn_paged_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -587,9 +698,71 @@ gqa_status gqa_prefill_attn_paged_ex(const void* q, const void* k_cache, const v
                                      int n_q_heads, int n_kv_heads, int head_dim, float scale,
                                      void* stream, const gqa_prefill_opts* opts,
                                      gqa_prefill_plan* plan_out) {
-  const gqa::PagedKV pkv{block_table, num_pages, page_size};
-  return gqa::run(q, k_cache, v_cache, &pkv, nullptr, out, lse, q_len, kv_len, n_q_heads,
-                  n_kv_heads, head_dim, scale, stream, opts, plan_out);
+  const gqa::PagedKV pkv{block_table, 0, num_pages, page_size};
+  const gqa::CallIO io{q, k_cache, v_cache, out, lse, &pkv, nullptr, scale};
+  return gqa::run_one(io, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
+}
+
+gqa_status gqa_prefill_attn_varlen_ex(const void* q, const void* k, const void* v, void* out,
+                                      float* lse, const int32_t* cu_seqlens_q,
+                                      const int32_t* cu_seqlens_k, int batch, int n_q_heads,
+                                      int n_kv_heads, int head_dim, float scale, void* stream,
+                                      const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out) {
+  if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
+  if (batch > 0 && !cu_seqlens_k) return GQA_ERR_NULL;
+  std::vector<gqa::SeqIn> seqs;
+  int total_q = 0;
+  int64_t total_kv = 0;
+  const gqa_status st = gqa::batch_from_host(cu_seqlens_q, cu_seqlens_k, nullptr, batch, &seqs,
+                                             &total_q, &total_kv);
+  if (st != GQA_OK) return st;
+  const gqa::CallIO io{q, k, v, out, lse, nullptr, nullptr, scale};
+  return gqa::run(io, seqs, total_q, total_kv, n_q_heads, n_kv_heads, head_dim, stream, opts,
+                  plan_out);
+}
+
+gqa_status gqa_prefill_attn_varlen(const void* q, const void* k, const void* v, void* out,
+                                   float* lse, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int batch, int n_q_heads,
+                                   int n_kv_heads, int head_dim, float scale, void* stream) {
+  return gqa_prefill_attn_varlen_ex(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, batch,
+                                    n_q_heads, n_kv_heads, head_dim, scale, stream, nullptr,
+                                    nullptr);
+}
+
+gqa_status gqa_prefill_attn_paged_varlen_ex(const void* q, const void* k_cache,
+                                            const void* v_cache, const int32_t* block_table,
+                                            int bt_stride, int num_pages, int page_size,
+                                            void* out, float* lse,
+                                            const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                            int batch, int n_q_heads, int n_kv_heads,
+                                            int head_dim, float scale, void* stream,
+                                            const gqa_prefill_opts* opts,
+                                            gqa_prefill_plan* plan_out) {
+  if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
+  if (batch > 0 && !kv_lens) return GQA_ERR_NULL;
+  if (bt_stride < 0) return GQA_ERR_SHAPE;
+  std::vector<gqa::SeqIn> seqs;
+  int total_q = 0;
+  int64_t total_kv = 0;
+  const gqa_status st =
+      gqa::batch_from_host(cu_seqlens_q, nullptr, kv_lens, batch, &seqs, &total_q, &total_kv);
+  if (st != GQA_OK) return st;
+  const gqa::PagedKV pkv{block_table, bt_stride, num_pages, page_size};
+  const gqa::CallIO io{q, k_cache, v_cache, out, lse, &pkv, nullptr, scale};
+  return gqa::run(io, seqs, total_q, 0, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
+}
+
+gqa_status gqa_prefill_attn_paged_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, int bt_stride, int num_pages,
+                                         int page_size, void* out, float* lse,
+                                         const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                         int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                         float scale, void* stream) {
+  return gqa_prefill_attn_paged_varlen_ex(q, k_cache, v_cache, block_table, bt_stride, num_pages,
+                                          page_size, out, lse, cu_seqlens_q, kv_lens, batch,
+                                          n_q_heads, n_kv_heads, head_dim, scale, stream, nullptr,
+                                          nullptr);
 }
 
 gqa_status gqa_quantize_q_fp8(const void* q, void* q_fp8, float* q_scale, int q_len,
@@ -626,8 +799,9 @@ gqa_status gqa_prefill_attn_fp8qk(const void* q_fp8, const float* q_scale, const
                                   void* out, float* lse, int q_len, int kv_len, int n_q_heads,
                                   int n_kv_heads, int head_dim, float scale, void* stream) {
   const gqa::Fp8Qk f8{q_scale, k_scale, k_scale_stride};
-  return gqa::run(q_fp8, k_fp8, v, nullptr, &f8, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
-                  head_dim, scale, stream, nullptr, nullptr);
+  const gqa::CallIO io{q_fp8, k_fp8, v, out, lse, nullptr, &f8, scale};
+  return gqa::run_one(io, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, stream, nullptr,
+                      nullptr);
 }
 
 gqa_status gqa_prefill_attn_fp8qk_ex(const void* q_fp8, const float* q_scale, const void* k_fp8,
@@ -636,22 +810,38 @@ gqa_status gqa_prefill_attn_fp8qk_ex(const void* q_fp8, const float* q_scale, co
                                      int n_kv_heads, int head_dim, float scale, void* stream,
                                      const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out) {
   const gqa::Fp8Qk f8{q_scale, k_scale, k_scale_stride};
-  return gqa::run(q_fp8, k_fp8, v, nullptr, &f8, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
-                  head_dim, scale, stream, opts, plan_out);
+  const gqa::CallIO io{q_fp8, k_fp8, v, out, lse, nullptr, &f8, scale};
+  return gqa::run_one(io, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
 }
 
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                                  int num_sms, int force_splits, int force_grid, int force_variant,
                                  gqa_prefill_plan* plan) {
   if (!plan) return GQA_ERR_NULL;
-  const gqa_status st =
-      gqa::validate_shape(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, 1.0f / 16.0f);
-  if (st != GQA_OK) return st;
-  if (num_sms <= 0) return GQA_ERR_SHAPE;
+  const int32_t cu_q[2] = {0, q_len}, cu_k[2] = {0, kv_len};
+  if (q_len < 0 || kv_len < q_len) return GQA_ERR_SHAPE;
+  return gqa_prefill_make_plan_varlen(cu_q, cu_k, 1, n_q_heads, n_kv_heads, head_dim, num_sms,
+                                      force_splits, force_grid, force_variant, plan);
+}
+
+gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                        int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                        int num_sms, int force_splits, int force_grid,
+                                        int force_variant, gqa_prefill_plan* plan) {
+  if (!plan) return GQA_ERR_NULL;
   std::memset(plan, 0, sizeof(*plan));
-  if (q_len == 0) return GQA_OK;
-  gqa::cached_plan(q_len, kv_len, num_sms, num_sms / 2, force_splits, force_grid, force_variant,
-                   plan);
+  std::vector<gqa::SeqIn> seqs;
+  int total_q = 0;
+  int64_t total_kv = 0;
+  if (batch > 0 && !cu_seqlens_k) return GQA_ERR_NULL;
+  gqa_status st = gqa::batch_from_host(cu_seqlens_q, cu_seqlens_k, nullptr, batch, &seqs,
+                                       &total_q, &total_kv);
+  if (st != GQA_OK) return st;
+  if ((st = gqa::validate_heads(n_q_heads, n_kv_heads, head_dim, 1.0f / 16.0f)) != GQA_OK)
+    return st;
+  if (num_sms <= 0) return GQA_ERR_SHAPE;
+  if (total_q == 0) return GQA_OK;
+  gqa::cached_plan(seqs, num_sms, num_sms / 2, force_splits, force_grid, force_variant, plan);
   return GQA_OK;
 }
 

@@ -1,12 +1,19 @@
 // Work decomposition of one call, shared by the host planner, the attention
 // kernel and the merge kernel (all three must agree unit for unit).
 //
-// An *item* is one query tile of one KV group that sweeps KV tiles 0 .. nt-1
-// (128 keys each) up to the causal diagonal: 21 tokens (126 packed MMA rows)
-// for the one-CTA kernel, 42 tokens for the CTA-pair kernel (21 per CTA).
-// Items are ordered longest first — item i covers query tile
-// qt = n_qtiles - 1 - i/4 and KV group g = i%4 — so consecutive items have
-// (nearly) the same length.
+// A call holds one or more sequences (up to kMaxSeqs). In each, the q_len new
+// tokens are the last q_len of its kv_len keys (bottom-right causal
+// alignment); its rows sit at q_start of the packed Q / out / LSE and, for
+// dense K/V, at kv_start of the packed K / V.
+//
+// An *item* is one query tile of one KV group of one sequence that sweeps KV
+// tiles 0 .. nt-1 (128 keys each) up to the causal diagonal: 21 tokens (126
+// packed MMA rows) for the one-CTA kernel, 42 tokens for the CTA-pair kernel
+// (21 per CTA). A sequence's items are ordered longest first — item li covers
+// query tile qt = n_qtiles - 1 - li/4 and KV group g = li%4 — and the host
+// orders the sequences by their longest item, so the call's item list runs
+// (nearly) longest first; item i belongs to the last sequence whose
+// item_begin <= i.
 //
 // Work units are dealt to the G persistent CTAs in a snake: in round r, unit
 // r*G + x goes to CTA x (r even) or G-1-x (r odd). The first head_items =
@@ -17,28 +24,40 @@
 // combines the S slots of every tail item.
 //
 // Why this shape: in every round all CTAs sweep the KV range of items of
-// equal length from the same starting key in lockstep, so the K/V tiles in
-// flight at any moment are few and stay in L2 even when the whole K/V does
-// not fit; only the last, partial round is cut into pieces so that it spreads
-// over all CTAs (and its pieces with the same s are aligned as well).
+// (nearly) equal length from the same starting key in lockstep, so the K/V
+// tiles in flight at any moment are few and stay in L2 even when the whole
+// K/V does not fit; only the last, partial round is cut into pieces so that it
+// spreads over all CTAs (and its pieces with the same s are aligned as well).
 #pragma once
 
 #include <cstdint>
 
 namespace gqa {
 
-struct Geometry {
-  int q_len;         // tokens in the chunk
-  int p0;            // kv_len - q_len: position of the chunk's first token
-  int n_qtiles;      // ceil(q_len / tok_per_item)
+constexpr int kMaxSeqs = 128;  // sequences per call
+
+struct SeqGeo {
+  int q_start;     // first row of the sequence in the packed Q / out / LSE
+  int q_len;       // its new tokens (> 0: the host leaves empty sequences out)
+  int kv_start;    // first key row in the packed K / V (dense K/V; 0 when paged)
+  int kv_len;      // its keys, q_len of them the new tokens' own
+  int n_qtiles;    // ceil(q_len / tok_per_item)
+  int item_begin;  // items of the sequences before it in the call's order
+  int src;         // its index in the caller's batch (block-table row of paged K/V)
+};
+
+struct Batch {
+  int n_seq;
   int tok_per_item;  // 21 (one CTA per item) or 42 (a CTA pair per item)
+  int n_items;       // items of the whole call
+  SeqGeo seq[kMaxSeqs];
 };
 
 // KV tiles an item of query tile qt visits: keys 0 .. p0 + last token of the tile.
-__host__ __device__ inline int item_tiles(const Geometry& geo, int qt) {
-  const int end = (qt + 1) * geo.tok_per_item;
-  const int tok_end = end < geo.q_len ? end : geo.q_len;
-  return (geo.p0 + tok_end + 127) / 128;
+__host__ __device__ inline int item_tiles(const SeqGeo& s, int tpi, int qt) {
+  const int end = (qt + 1) * tpi;
+  const int tok_end = end < s.q_len ? end : s.q_len;
+  return (s.kv_len - s.q_len + tok_end + 127) / 128;
 }
 
 struct Schedule {
@@ -47,13 +66,27 @@ struct Schedule {
   int n_units;      // head_items + (n_items - head_items) * S
 };
 
-// One unit of work: tiles [n0, n1) of item (qt, g). slot < 0: the unit is a
-// whole item and writes the output directly; otherwise it writes partial slot `slot`.
+// Item i of the call: its sequence, query tile and KV group.
+__host__ __device__ inline void item_of(const Batch& b, int i, int& seq, int& qt, int& g) {
+  int lo = 0, hi = b.n_seq - 1;  // the last sequence with item_begin <= i
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (b.seq[mid].item_begin <= i) lo = mid;
+    else hi = mid - 1;
+  }
+  seq = lo;
+  const int li = i - b.seq[lo].item_begin;
+  qt = b.seq[lo].n_qtiles - 1 - li / 4;
+  g = li % 4;
+}
+
+// One unit of work: tiles [n0, n1) of item (seq, qt, g). slot < 0: the unit is
+// a whole item and writes the output directly; otherwise it writes partial slot `slot`.
 struct Piece {
-  int qt, g, n0, n1, slot;
+  int seq, qt, g, n0, n1, slot;
 };
 
-__host__ __device__ inline Piece unit_piece(const Geometry& geo, const Schedule& sc, int u) {
+__host__ __device__ inline Piece unit_piece(const Batch& b, const Schedule& sc, int u) {
   Piece w;
   int item, s = 0;
   if (u < sc.head_items) {
@@ -63,9 +96,8 @@ __host__ __device__ inline Piece unit_piece(const Geometry& geo, const Schedule&
     item = sc.head_items + t / sc.tail_splits;
     s = t % sc.tail_splits;
   }
-  w.qt = geo.n_qtiles - 1 - item / 4;
-  w.g = item % 4;
-  const int nt = item_tiles(geo, w.qt);
+  item_of(b, item, w.seq, w.qt, w.g);
+  const int nt = item_tiles(b.seq[w.seq], b.tok_per_item, w.qt);
   if (u < sc.head_items || sc.tail_splits == 1) {
     w.n0 = 0;
     w.n1 = nt;
@@ -80,23 +112,23 @@ __host__ __device__ inline Piece unit_piece(const Geometry& geo, const Schedule&
 
 // Iterates one CTA's units in order; every role of the CTA runs its own copy.
 struct PieceIter {
-  Geometry geo;
+  const Batch* b;
   Schedule sc;
-  int G, b, round;
+  int G, x, round;
 
-  __host__ __device__ inline void init(const Geometry& g_, const Schedule& s_, int G_, int b_) {
-    geo = g_;
+  __host__ __device__ inline void init(const Batch* b_, const Schedule& s_, int G_, int x_) {
+    b = b_;
     sc = s_;
     G = G_;
-    b = b_;
+    x = x_;
     round = 0;
   }
 
   __host__ __device__ inline bool next(Piece& w) {
-    const int u = round * G + ((round & 1) ? (G - 1 - b) : b);
+    const int u = round * G + ((round & 1) ? (G - 1 - x) : x);
     if (u >= sc.n_units) return false;
     ++round;
-    w = unit_piece(geo, sc, u);  // never empty: the planner keeps S <= every tail item's tiles
+    w = unit_piece(*b, sc, u);  // never empty: the planner keeps S <= every item's tiles
     return true;
   }
 };

@@ -106,6 +106,49 @@ def make_paged_cache(k: torch.Tensor, v: torch.Tensor, page_size: int, seed: int
     return k_cache, v_cache, table
 
 
+def make_varlen(lens, seed: int):
+    """A batch of sequences packed end to end. lens: [(q_len, kv_len), ...].
+    Returns (q [sum q_len, 24, 256], k, v [sum kv_len, 4, 256] CPU BF16,
+    cu_seqlens_q, cu_seqlens_k as lists of batch + 1 ints). Each sequence is drawn
+    by make_qkv with seed + its index."""
+    qs, ks, vs, cu_q, cu_k = [], [], [], [0], [0]
+    for i, (ql, kl) in enumerate(lens):
+        q, k, v = make_qkv(ql, kl, seed + i)
+        qs.append(q), ks.append(k), vs.append(v)
+        cu_q.append(cu_q[-1] + ql)
+        cu_k.append(cu_k[-1] + kl)
+    return torch.cat(qs), torch.cat(ks), torch.cat(vs), cu_q, cu_k
+
+
+def make_paged_batch(k: torch.Tensor, v: torch.Tensor, cu_k, page_size: int, seed: int, *,
+                     extra_pages: int = 5, fill: float = float("nan"), pad: int = 1 << 30):
+    """Scatter every sequence of a packed batch into ONE shared paged cache.
+
+    Pages go to distinct physical pages in a seeded random order across all
+    sequences; unused slots hold ``fill``. Returns (k_cache, v_cache
+    [num_pages, page_size, Hkv, d], block_table int32 [batch, bt_stride] whose
+    unused entries hold ``pad``, kv_lens list)."""
+    kv_lens = [cu_k[i + 1] - cu_k[i] for i in range(len(cu_k) - 1)]
+    n_pages = [-(-kl // page_size) for kl in kv_lens]
+    bt_stride = max(max(n_pages), 1)
+    num_pages = sum(n_pages) + extra_pages
+    g = torch.Generator("cpu").manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g).tolist()
+    k_cache = torch.full((num_pages, page_size) + tuple(k.shape[1:]), fill, dtype=k.dtype)
+    v_cache = torch.full((num_pages, page_size) + tuple(v.shape[1:]), fill, dtype=v.dtype)
+    table = torch.full((len(kv_lens), bt_stride), pad, dtype=torch.int32)
+    nxt = 0
+    for b, kl in enumerate(kv_lens):
+        for i in range(n_pages[b]):
+            phys = perm[nxt]
+            nxt += 1
+            table[b, i] = phys
+            lo, hi = cu_k[b] + i * page_size, min(cu_k[b] + (i + 1) * page_size, cu_k[b + 1])
+            k_cache[phys, : hi - lo] = k[lo:hi]
+            v_cache[phys, : hi - lo] = v[lo:hi]
+    return k_cache, v_cache, table, kv_lens
+
+
 def sample_rows(q_len: int, n_q_heads: int, n: int, seed: int) -> torch.Tensor:
     """A fixed, stratified set of (token, head) row ids ``t*n_q_heads + h``.
 

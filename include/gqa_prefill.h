@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 3
+#define GQA_PREFILL_ABI_VERSION 4
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -109,7 +109,7 @@ typedef struct gqa_prefill_opts {
  */
 typedef struct gqa_prefill_plan {
   int num_sms;                /* SMs of the device                                    */
-  int q_tiles;                /* ceil(q_len / tokens per item)                        */
+  int q_tiles;                /* ceil(q_len / tokens per item), summed over sequences */
   int n_items;                /* q_tiles * n_kv_heads                                 */
   int head_rounds;            /* full rounds of whole items                           */
   int tail_items;             /* items after those rounds                             */
@@ -224,6 +224,60 @@ gqa_status gqa_prefill_attn_paged_ex(const void* q, const void* k_cache, const v
                                      int n_q_heads, int n_kv_heads, int head_dim, float scale,
                                      void* stream, const gqa_prefill_opts* opts,
                                      gqa_prefill_plan* plan_out);
+
+/*
+ * Batched (varlen) calls: up to GQA_MAX_SEQS sequences of a serving batch in
+ * one launch. Each sequence is a chunk exactly as in gqa_prefill_attn: its
+ * q_len new tokens are the last q_len of its kv_len keys (the pages restrict
+ * their kernel to one sequence, DCU使用技术报告（中篇）, §2; batching the chunks
+ * of several requests is the step beside it in a server). Work items of all
+ * sequences share the persistent grid; the plan is made on the host from the
+ * real lengths, so the length arrays are HOST memory (a serving scheduler
+ * knows them there) and are read during the call only.
+ *
+ * gqa_prefill_attn_varlen: packed tensors
+ *   q, out   : [total_q,  24, 256] BF16; lse [total_q, 24] FP32 (may be NULL)
+ *   k, v     : [total_kv,  4, 256] BF16
+ *   cu_seqlens_q, cu_seqlens_k : HOST int32 [batch + 1], starting at 0 and
+ *     non-decreasing: sequence b owns query rows cu_seqlens_q[b] ..
+ *     cu_seqlens_q[b+1]-1 and key rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1,
+ *     with q_len_b <= kv_len_b. Empty sequences are allowed.
+ * gqa_prefill_attn_paged_varlen: q / out / lse packed as above; K/V caches as
+ *   gqa_prefill_attn_paged; block_table DEVICE int32 [batch][bt_stride]
+ *   (bt_stride >= every sequence's ceil(kv_len_b / page_size)); kv_lens HOST
+ *   int32 [batch].
+ * batch > GQA_MAX_SEQS returns GQA_ERR_UNSUPPORTED (split the batch).
+ */
+#define GQA_MAX_SEQS 128
+gqa_status gqa_prefill_attn_varlen(const void* q, const void* k, const void* v, void* out,
+                                   float* lse, const int32_t* cu_seqlens_q,
+                                   const int32_t* cu_seqlens_k, int batch, int n_q_heads,
+                                   int n_kv_heads, int head_dim, float scale, void* stream);
+gqa_status gqa_prefill_attn_varlen_ex(const void* q, const void* k, const void* v, void* out,
+                                      float* lse, const int32_t* cu_seqlens_q,
+                                      const int32_t* cu_seqlens_k, int batch, int n_q_heads,
+                                      int n_kv_heads, int head_dim, float scale, void* stream,
+                                      const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out);
+gqa_status gqa_prefill_attn_paged_varlen(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, int bt_stride, int num_pages,
+                                         int page_size, void* out, float* lse,
+                                         const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                         int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                         float scale, void* stream);
+gqa_status gqa_prefill_attn_paged_varlen_ex(const void* q, const void* k_cache,
+                                            const void* v_cache, const int32_t* block_table,
+                                            int bt_stride, int num_pages, int page_size,
+                                            void* out, float* lse,
+                                            const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                            int batch, int n_q_heads, int n_kv_heads,
+                                            int head_dim, float scale, void* stream,
+                                            const gqa_prefill_opts* opts,
+                                            gqa_prefill_plan* plan_out);
+/* Host-only planning of a dense batched call (as gqa_prefill_make_plan). */
+gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                        int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                        int num_sms, int force_splits, int force_grid,
+                                        int force_variant, gqa_prefill_plan* plan);
 
 /*
  * Quantised QK^T (gfx936 DCU上实现INT8 QK MMAC：分页访存、Fragment映射与GQA适配, §1

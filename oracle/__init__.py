@@ -7,6 +7,9 @@ two share nothing but the seeded inputs of ``gqa_inputs``.
 
 ``paged_gather()`` reads one sequence's keys and values out of paged caches
 through its block table; ``paged_attention()`` is attention on what it returns.
+``varlen_attention()`` / ``paged_varlen_attention()`` apply the definition to
+each sequence of a packed batch. ``quantize_e4m3()`` and ``fp8qk_attention()``
+define the quantised-QK^T path.
 
 ``attention()`` runs the plain C++ definition in ``gqa_oracle.cpp`` (explicit
 full-row softmax in FP64, one std::thread per row at a time). ``restate_numpy``
@@ -146,6 +149,46 @@ def paged_attention(q, k_cache, v_cache, block_table, kv_len: int, scale: float,
     """``attention()`` of q over the sequence ``paged_gather()`` reads from the caches."""
     k, v = paged_gather(k_cache, v_cache, block_table, kv_len)
     return attention(q, k, v, scale, rows=rows, n_threads=n_threads)
+
+
+# --- batches of sequences ------------------------------------------------------
+
+def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float,
+                     n_threads: Optional[int] = None):
+    """A batch packed end to end: sequence b is query rows cu_q[b] .. cu_q[b+1]-1
+    and keys cu_k[b] .. cu_k[b+1]-1, each its own chunk-at-the-end attention
+    (the single-sequence definition, applied per sequence; nothing crosses
+    sequences). Returns (out [total_q, Hq, d], lse [total_q, Hq]) FP64."""
+    q64, k64, v64 = _f64(q), _f64(k), _f64(v)
+    out = np.zeros(q64.shape, np.float64)
+    lse = np.zeros(q64.shape[:2], np.float64)
+    for b in range(len(cu_seqlens_q) - 1):
+        q0, q1 = cu_seqlens_q[b], cu_seqlens_q[b + 1]
+        k0, k1 = cu_seqlens_k[b], cu_seqlens_k[b + 1]
+        if q1 == q0:
+            continue
+        o, l = attention(q64[q0:q1], k64[k0:k1], v64[k0:k1], scale, n_threads=n_threads)
+        out[q0:q1], lse[q0:q1] = o, l
+    return out, lse
+
+
+def paged_varlen_attention(q, k_cache, v_cache, block_table, cu_seqlens_q, kv_lens, scale: float,
+                           n_threads: Optional[int] = None):
+    """Batch with K/V in one paged cache: sequence b reads its kv_lens[b] keys
+    through block-table row b (``paged_gather``)."""
+    q64 = _f64(q)
+    out = np.zeros(q64.shape, np.float64)
+    lse = np.zeros(q64.shape[:2], np.float64)
+    table = np.asarray(block_table.cpu().numpy() if isinstance(block_table, torch.Tensor)
+                       else block_table)
+    for b in range(len(kv_lens)):
+        q0, q1 = cu_seqlens_q[b], cu_seqlens_q[b + 1]
+        if q1 == q0:
+            continue
+        k, v = paged_gather(k_cache, v_cache, table[b], kv_lens[b])
+        o, l = attention(q64[q0:q1], k, v, scale, n_threads=n_threads)
+        out[q0:q1], lse[q0:q1] = o, l
+    return out, lse
 
 
 # --- quantised QK^T -------------------------------------------------------------

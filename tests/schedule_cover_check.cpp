@@ -1,5 +1,6 @@
 // Host check of the work decomposition in gqa_schedule.h (compiled with g++ by
-// tests/test_schedule_cpu.py). For many chunk shapes, grid sizes, numbers of
+// tests/test_schedule_cpu.py). For many chunk shapes and seeded batches of
+// several sequences (item numbering inverted by item_of), grid sizes, numbers of
 // whole rounds and tail splits (never more splits than the shortest item has
 // KV tiles, as the planner guarantees) it checks that every KV tile of every
 // item is computed exactly once, that no unit is empty, that whole items and
@@ -9,77 +10,137 @@
 // Prints "checks=N bad=M" and exits non-zero on any mismatch.
 #include "gqa_schedule.h"
 
+#include <cstdint>
 #include <cstdio>
 #include <map>
+#include <utility>
 #include <vector>
 
 using namespace gqa;
 
+namespace {
+
+long long checks = 0;
+int bad = 0;
+
+uint32_t lcg(uint32_t& s) {
+  s = s * 1664525u + 1013904223u;
+  return s >> 8;
+}
+
+// A call's sequence table (any order: coverage must not depend on it).
+void make_batch(const std::vector<std::pair<int, int>>& lens, int tpi, Batch& b) {
+  b.n_seq = 0;
+  b.tok_per_item = tpi;
+  int items = 0, q_start = 0, kv_start = 0;
+  for (size_t i = 0; i < lens.size(); ++i) {
+    const int ql = lens[i].first, kl = lens[i].second;
+    if (ql > 0) {
+      const int nq = (ql + tpi - 1) / tpi;
+      b.seq[b.n_seq++] = SeqGeo{q_start, ql, kv_start, kl, nq, items, static_cast<int>(i)};
+      items += 4 * nq;
+    }
+    q_start += ql;
+    kv_start += kl;
+  }
+  b.n_items = items;
+}
+
+void check_batch(const Batch& b, const int* grids, int n_grids, const int* splits, int n_splits) {
+  const int n_items = b.n_items;
+  std::vector<int> nts(static_cast<size_t>(n_items));
+  int shortest = 1 << 30;
+  for (int i = 0; i < n_items; ++i) {  // item_of must invert item numbering
+    int seq, qt, g;
+    item_of(b, i, seq, qt, g);
+    const SeqGeo& s = b.seq[seq];
+    const int li = 4 * (s.n_qtiles - 1 - qt) + g;
+    if (s.item_begin + li != i || qt < 0 || qt >= s.n_qtiles) { ++bad; printf("item_of\n"); }
+    nts[static_cast<size_t>(i)] = item_tiles(s, b.tok_per_item, qt);
+    if (nts[static_cast<size_t>(i)] < shortest) shortest = nts[static_cast<size_t>(i)];
+  }
+  for (int gi = 0; gi < n_grids; ++gi)
+    for (int si = 0; si < n_splits; ++si) {
+      const int G0 = grids[gi], S = splits[si];
+      if (S > shortest) continue;
+      const int max_rounds = n_items / G0;
+      for (int hr : {0, 1, max_rounds}) {
+        if (hr > max_rounds) continue;
+        const int head = hr * G0 < n_items ? hr * G0 : n_items;
+        const Schedule sc{head, S, head + (n_items - head) * S};
+        const int G = G0 < sc.n_units ? G0 : sc.n_units;
+        if (hr > 0 && G != G0) continue;  // whole rounds need a full grid
+        std::map<long long, int> cover;
+        std::map<int, int> slots;
+        int units_seen = 0;
+        for (int x = 0; x < G; ++x) {
+          PieceIter it;
+          it.init(&b, sc, G, x);
+          Piece w;
+          while (it.next(w)) {
+            ++units_seen;
+            const SeqGeo& s = b.seq[w.seq];
+            const int item = s.item_begin + 4 * (s.n_qtiles - 1 - w.qt) + w.g;
+            if (w.n0 < 0 || w.n1 > nts[item] || w.n0 >= w.n1) { ++bad; printf("empty or bad range\n"); }
+            const bool whole = w.n0 == 0 && w.n1 == nts[item];
+            if (item < head && !(whole && w.slot < 0)) { ++bad; printf("head item not whole\n"); }
+            if (item >= head) {
+              if (S == 1 && w.slot >= 0) { ++bad; printf("unsplit tail wrote a slot\n"); }
+              if (S > 1) {
+                const int j = item - head;
+                if (w.slot < j * S || w.slot >= j * S + S) { ++bad; printf("slot outside item block\n"); }
+                if (slots[w.slot]++) { ++bad; printf("slot reused\n"); }
+              }
+            }
+            for (int n = w.n0; n < w.n1; ++n) cover[static_cast<long long>(item) * 100000 + n]++;
+          }
+        }
+        if (units_seen != sc.n_units) { ++bad; printf("units dealt %d of %d\n", units_seen, sc.n_units); }
+        for (int i = 0; i < n_items; ++i)
+          for (int n = 0; n < nts[static_cast<size_t>(i)]; ++n) {
+            ++checks;
+            const int c = cover[static_cast<long long>(i) * 100000 + n];
+            if (c != 1 && ++bad < 10)
+              printf("coverage seqs=%d G=%d S=%d hr=%d item=%d tile=%d count=%d\n", b.n_seq, G, S,
+                     hr, i, n, c);
+          }
+        if (S > 1 && static_cast<int>(slots.size()) != (n_items - head) * S) {
+          ++bad;
+          printf("slot count\n");
+        }
+      }
+    }
+}
+
+}  // namespace
+
 int main() {
-  long long checks = 0;
-  int bad = 0;
+  static Batch b;
   const int qls[] = {1, 2, 5, 20, 21, 22, 42, 43, 127, 128, 129, 500, 512, 3072, 4096};
   const int extras[] = {0, 1, 100, 127, 128, 129, 255, 1000, 4096, 28672};
   const int grids[] = {1, 2, 3, 7, 64, 152, 1000};
   const int splits[] = {1, 2, 3, 4, 7, 16};
+  // One sequence: every chunk shape of the workloads and around the tile edges.
   for (int tpi : {21, 42})
-  for (int ql : qls)
-    for (int ex : extras) {
-      const Geometry geo{ql, ex, (ql + tpi - 1) / tpi, tpi};
-      const int n_items = 4 * geo.n_qtiles;
-      std::vector<int> nts;
-      for (int i = 0; i < n_items; ++i) nts.push_back(item_tiles(geo, geo.n_qtiles - 1 - i / 4));
-      const int shortest = item_tiles(geo, 0);
-      for (int G0 : grids)
-        for (int S : splits) {
-          if (S > shortest) continue;
-          const int max_rounds = n_items / G0;
-          for (int hr : {0, 1, max_rounds}) {
-            if (hr > max_rounds || (hr == 1 && max_rounds == 1 && hr != max_rounds)) continue;
-            const int head = hr * G0 < n_items ? hr * G0 : n_items;
-            const Schedule sc{head, S, head + (n_items - head) * S};
-            const int G = G0 < sc.n_units ? G0 : sc.n_units;
-            if (hr > 0 && G != G0) continue;  // whole rounds need a full grid
-            std::map<long long, int> cover;
-            std::map<int, int> slots;
-            int units_seen = 0;
-            for (int b = 0; b < G; ++b) {
-              PieceIter it;
-              it.init(geo, sc, G, b);
-              Piece w;
-              while (it.next(w)) {
-                ++units_seen;
-                const int item = 4 * (geo.n_qtiles - 1 - w.qt) + w.g;
-                if (w.n0 < 0 || w.n1 > nts[item] || w.n0 >= w.n1) { ++bad; printf("empty or bad range\n"); }
-                const bool whole = w.n0 == 0 && w.n1 == nts[item];
-                if (item < head && !(whole && w.slot < 0)) { ++bad; printf("head item not whole\n"); }
-                if (item >= head) {
-                  if (S == 1 && w.slot >= 0) { ++bad; printf("unsplit tail wrote a slot\n"); }
-                  if (S > 1) {
-                    const int j = item - head;
-                    if (w.slot < j * S || w.slot >= j * S + S) { ++bad; printf("slot outside item block\n"); }
-                    if (slots[w.slot]++) { ++bad; printf("slot reused\n"); }
-                  }
-                }
-                for (int n = w.n0; n < w.n1; ++n) cover[static_cast<long long>(item) * 100000 + n]++;
-              }
-            }
-            if (units_seen != sc.n_units) { ++bad; printf("units dealt %d of %d\n", units_seen, sc.n_units); }
-            for (int i = 0; i < n_items; ++i)
-              for (int n = 0; n < nts[i]; ++n) {
-                ++checks;
-                const int c = cover[static_cast<long long>(i) * 100000 + n];
-                if (c != 1 && ++bad < 10)
-                  printf("coverage q_len=%d p0=%d G=%d S=%d hr=%d item=%d tile=%d count=%d\n", ql, ex,
-                         G, S, hr, i, n, c);
-              }
-            if (S > 1 && static_cast<int>(slots.size()) != (n_items - head) * S) {
-              ++bad;
-              printf("slot count\n");
-            }
-          }
-        }
+    for (int ql : qls)
+      for (int ex : extras) {
+        make_batch({{ql, ql + ex}}, tpi, b);
+        check_batch(b, grids, 7, splits, 6);
+      }
+  // Batches of 2 to 12 sequences (some empty), seeded.
+  uint32_t seed = 12345;
+  for (int t = 0; t < 300; ++t) {
+    const int n = 2 + static_cast<int>(lcg(seed) % 11);
+    std::vector<std::pair<int, int>> lens;
+    for (int i = 0; i < n; ++i) {
+      const int ql = (lcg(seed) % 5 == 0) ? 0 : 1 + static_cast<int>(lcg(seed) % 600);
+      const int kl = ql + static_cast<int>(lcg(seed) % 3000);
+      lens.push_back({ql, kl > 0 ? kl : 1});
     }
+    make_batch(lens, (t & 1) ? 42 : 21, b);
+    if (b.n_items == 0) continue;
+    check_batch(b, grids, 7, splits, 6);
+  }
   printf("checks=%lld bad=%d\n", checks, bad);
   return bad != 0;
 }

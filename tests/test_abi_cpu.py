@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(gqa):
 
 
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 3
+    assert gqa.gqa_prefill_abi_version() == 4
 
 
 def test_refusals_before_any_cuda_call(gqa):
@@ -195,3 +195,50 @@ def test_fp8_refusals_before_any_cuda_call(gqa):
     assert call(hq=16) == S.ERR_UNSUPPORTED
     assert call(q_len=9) == S.ERR_SHAPE
     assert call(q=None, qs=None, k=None, ks=None, v=None, out=None, q_len=0, kv_len=0, st=0) == S.OK
+
+
+def test_varlen_refusals_before_any_cuda_call(gqa):
+    S = gqa.GqaStatus
+    f = lambda cq, ck, **kw: gqa.gqa_prefill_attn_varlen(
+        kw.get("q", 16), 16, 16, kw.get("out", 16), None, cq, ck, 24, kw.get("hkv", 4), 256,
+        0.0625, stream=0, check=False)
+    assert f([1, 4], [0, 8]) == S.ERR_SHAPE          # must start at 0
+    assert f([0, 4, 3], [0, 8, 16]) == S.ERR_SHAPE   # decreasing
+    assert f([0, 9], [0, 8]) == S.ERR_SHAPE          # q_len > kv_len
+    assert f([0, 4], [0, 8], hkv=2) == S.ERR_UNSUPPORTED
+    assert f([0, 4], [0, 8], q=None) == S.ERR_NULL
+    assert f([0, 4], [0, 8], out=24) == S.ERR_ALIGN
+    assert f([0] * 130, [0] * 130) == S.ERR_UNSUPPORTED   # 129 sequences > GQA_MAX_SEQS
+    assert f([0, 0, 0], [0, 5, 9], q=None, out=None) == S.OK  # no query rows: nothing to do
+    pf = lambda bt_stride, kv_lens: gqa.gqa_prefill_attn_paged_varlen(
+        16, 16, 16, 16, bt_stride, 10, 16, 16, None, [0, 2, 4], kv_lens, 24, 4, 256, 0.0625,
+        stream=0, check=False)
+    assert pf(2, [40, 20]) == S.ERR_SHAPE             # 40 keys need 3 pages per table row
+    assert pf(3, [40, 1]) == S.ERR_SHAPE              # second sequence: q_len 2 > kv_len 1
+
+
+@pytest.mark.parametrize("lens", [[(4096, 32768)], [(43, 300), (1, 4096), (0, 50), (129, 1000)],
+                                  [(1, 1000)] * 40, [(512, 4096), (300, 20000), (2000, 2000)],
+                                  [(21, 21)] * 128])
+@pytest.mark.parametrize("variant", [0, 1, 2])
+def test_varlen_plan_invariants(gqa, lens, variant):
+    cu_q, cu_k = [0], [0]
+    for ql, kl in lens:
+        cu_q.append(cu_q[-1] + ql)
+        cu_k.append(cu_k[-1] + kl)
+    rc, p = gqa.gqa_prefill_make_plan_varlen(cu_q, cu_k, 24, 4, 256, 152, force_variant=variant)
+    assert rc == 0
+    tpi = 42 if p["variant"] == 2 else 21
+    n_items = sum(4 * -(-ql // tpi) for ql, _ in lens)
+    tiles = 0
+    for ql, kl in lens:
+        for qt in range(-(-ql // tpi)):
+            tok_end = min((qt + 1) * tpi, ql)
+            tiles += 4 * ((kl - ql + tok_end + 127) // 128)
+    assert p["n_items"] == n_items and p["total_tiles"] == tiles
+    assert p["grid"] <= 152
+    assert p["n_units"] == (p["n_items"] - p["tail_items"]) + p["tail_items"] * p["tail_splits"]
+    if len(lens) == 1:
+        _, single = gqa.gqa_prefill_make_plan(lens[0][0], lens[0][1], 24, 4, 256, 152,
+                                              force_variant=variant)
+        assert single == p

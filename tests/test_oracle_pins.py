@@ -308,3 +308,53 @@ def test_fp8qk_attention_equals_attention_on_exact_codes():
     out_a, lse_a = oracle.fp8qk_attention(qc, qs, kc, ks, v, 1e-5)
     out_b, lse_b = oracle.attention(q, k, v, 1e-5)
     assert np.array_equal(out_a, out_b) and np.array_equal(lse_a, lse_b)
+
+
+# --- batches of sequences ---------------------------------------------------------
+
+def test_varlen_single_sequence_is_attention():
+    q, k, v = make_qkv(9, 40, 61)
+    o1, l1 = oracle.varlen_attention(q, k, v, [0, 9], [0, 40], SCALE)
+    o2, l2 = oracle.attention(q, k, v, SCALE)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_varlen_sequences_do_not_see_each_other():
+    from gqa_inputs import make_varlen
+    q, k, v, cu_q, cu_k = make_varlen([(5, 30), (0, 7), (8, 8), (3, 50)], 70)
+    out, lse = oracle.varlen_attention(q, k, v, cu_q, cu_k, SCALE)
+    k2, v2 = k.clone(), v.clone()
+    k2[cu_k[2]:cu_k[3]] = 3.0  # change only sequence 2's keys and values
+    v2[cu_k[2]:cu_k[3]] = -1.0
+    out2, lse2 = oracle.varlen_attention(q, k2, v2, cu_q, cu_k, SCALE)
+    rows2 = slice(cu_q[2], cu_q[3])
+    keep = np.ones(out.shape[0], bool)
+    keep[rows2] = False
+    assert np.array_equal(out[keep], out2[keep]) and np.array_equal(lse[keep], lse2[keep])
+    assert not np.array_equal(out[rows2], out2[rows2])
+
+
+def test_varlen_matches_library_per_sequence_bottom_right_masks():
+    from gqa_inputs import make_varlen
+    q, k, v, cu_q, cu_k = make_varlen([(4, 20), (6, 6), (1, 33)], 80)
+    out, _ = oracle.varlen_attention(q, k, v, cu_q, cu_k, SCALE)
+    for b in range(3):
+        qb = q[cu_q[b]:cu_q[b + 1]].double().numpy()
+        kb = k[cu_k[b]:cu_k[b + 1]].double().numpy()
+        vb = v[cu_k[b]:cu_k[b + 1]].double().numpy()
+        ql, kl = qb.shape[0], kb.shape[0]
+        mask = torch.ones(ql, kl, dtype=torch.bool).tril(diagonal=kl - ql)
+        np.testing.assert_allclose(out[cu_q[b]:cu_q[b + 1]], _sdpa(qb, kb, vb, SCALE, mask=mask),
+                                   rtol=1e-10, atol=1e-12)
+
+
+def test_paged_batch_scatter_is_read_back_exactly():
+    from gqa_inputs import make_paged_batch, make_varlen
+    q, k, v, cu_q, cu_k = make_varlen([(3, 100), (0, 17), (5, 5), (2, 260)], 90)
+    kc, vc, table, kv_lens = make_paged_batch(k, v, cu_k, 48, seed=91)
+    for b, kl in enumerate(kv_lens):
+        kb, vb = oracle.paged_gather(kc, vc, table[b], kl)
+        assert torch.equal(kb, k[cu_k[b]:cu_k[b + 1]]) and torch.equal(vb, v[cu_k[b]:cu_k[b + 1]])
+    o1, l1 = oracle.paged_varlen_attention(q, kc, vc, table, cu_q, kv_lens, SCALE)
+    o2, l2 = oracle.varlen_attention(q, k, v, cu_q, cu_k, SCALE)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
