@@ -38,12 +38,15 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from gqa_inputs import (SERVING_PAGE_SIZE, WORKLOADS, make_paged_cache, make_workload,  # noqa: E402
-                        sample_rows)
+from gqa_inputs import (SERVING_PAGE_SIZE, WORKLOADS, make_paged_cache, make_varlen,  # noqa: E402
+                        make_workload, sample_rows)
 
 METRIC = "effective causal attention TFLOPS and % of GB300 BF16 tensor peak"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "q4096_kv32768"
+# The batched leg: a 4096-token chunked-prefill step shared by 8 requests, 512 new
+# tokens each, over prefixes of 0, 4096, ..., 28672 keys.
+VARLEN_BATCH = [(512, 512 + 4096 * i) for i in range(8)]
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 
@@ -212,6 +215,7 @@ def main():
     ap.add_argument("--page-size", type=int, default=SERVING_PAGE_SIZE,
                     help="also time the paged-K/V entry point with this page size (0: skip)")
     ap.add_argument("--no-fp8", action="store_true", help="skip the quantised-QK^T leg")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the batched (varlen) leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -415,6 +419,55 @@ def main():
                        "PV in BF16. Step = the attention call; Q/K quantisation timed apart."}
         del q8, k8
 
+    # ---- a batched step: the 4096-token chunk budget split over 8 requests ----------
+    varlen = None
+    if not args.no_varlen:
+        lens = VARLEN_BATCH
+        vq, vk, vv, cu_q, cu_k = make_varlen(lens, seed=w.seed + 7)
+        vq, vk, vv = vq.to(dev), vk.to(dev), vv.to(dev)
+        vout = torch.empty_like(vq)
+        vlse = torch.empty((vq.shape[0], w.n_q_heads), dtype=torch.float32, device=dev)
+        v_flops = sum(4 * w.head_dim * w.n_q_heads * (ql * (kl - ql) + ql * (ql + 1) // 2)
+                      for ql, kl in lens)
+
+        def vcall():
+            gqa.gqa_prefill_attn_varlen(vq, vk, vv, vout, vlse, cu_q, cu_k, w.n_q_heads,
+                                        w.n_kv_heads, w.head_dim, w.scale, stream=stream)
+
+        def separate():
+            for b in range(len(lens)):
+                gqa.gqa_prefill_attn(vq[cu_q[b]:], vk[cu_k[b]:], vv[cu_k[b]:], vout[cu_q[b]:],
+                                     vlse[cu_q[b]:], lens[b][0], lens[b][1], w.n_q_heads,
+                                     w.n_kv_heads, w.head_dim, w.scale, stream)
+
+        def timed_plain(fn, n):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(n)]
+            for fn_ in (fn, fn, fn):
+                flush.zero_()
+                fn_()
+            torch.cuda.synchronize(dev)
+            for a, b in evs:
+                flush.zero_()
+                a.record(stream)
+                fn()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            return sum(a.elapsed_time(b) for a, b in evs) / n
+
+        n_v = min(args.steps, 100)
+        v_ms = max_over_ranks(timed_plain(vcall, n_v), pg, dev)
+        s_ms = max_over_ranks(timed_plain(separate, n_v), pg, dev)
+        if gqa.gqa_prefill_poll(stream) != 0:
+            raise RuntimeError("device-side error during the varlen steps")
+        varlen = {"batch": [list(x) for x in lens], "steps": n_v,
+                  "effective_gflop_per_step": round(v_flops / 1e9, 2),
+                  "value": round(job_throughput(world, v_flops, v_ms), 2), "unit": UNIT,
+                  "ms_per_step": round(v_ms, 4), "separate_calls_ms": round(s_ms, 4),
+                  "note": "one gqa_prefill_attn_varlen call vs one gqa_prefill_attn call per "
+                          "sequence, same data"}
+        del vq, vk, vv
+
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -481,6 +534,7 @@ def main():
         "gpu_launches": args.steps * plan["kernels_per_call"],
         "paged": paged,
         "fp8qk": fp8,
+        "varlen": varlen,
         "clocks": clocks,
         "wall_s_timed_loop": round(wall, 4),
     }
