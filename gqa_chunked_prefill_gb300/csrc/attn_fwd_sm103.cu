@@ -228,6 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kSboV = kPaged ? kNchV * 1024u : 1024u;
   constexpr uint32_t kKStageBytes = kRowsK * kNchK * 128u;  // K bytes per stage per CTA
 
+  // The stream's next kernel (the split merge, or the caller's) may be
+  // scheduled now; it waits for this grid to finish before touching memory.
+  ptx::griddep_launch_dependents();
+
   // ---- set-up: barriers, idle Q rows, tensor memory -------------------------
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -275,6 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (kPair) ptx::cluster_sync();  // both CTAs' barriers exist before any remote use
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Everything above touched only this CTA's own on-chip state; from here on
+  // global memory is read and written, so the previous kernel of the stream
+  // must have completed (programmatic dependent launch overlaps the set-up).
+  ptx::griddep_wait();
   const int tpi = kPair ? 2 * kTokPerTile : kTokPerTile;  // tokens per work item
   const int n_workers = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
   const int worker = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
@@ -780,6 +788,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 __global__ void __launch_bounds__(256) merge_tail_kernel(const __grid_constant__ MergeParams p) {
+  ptx::griddep_wait();  // launched early (programmatic dependent launch): the pieces must be done
   const int j = blockIdx.x;                               // tail item
   const int row_begin = blockIdx.y * kMergeRowsPerBlock;  // its rows, both CTAs of a pair
   int seq, qt, g;
@@ -852,25 +861,36 @@ cudaError_t prepare_fwd_kernel() {
 }
 
 namespace {
-cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+// Launch configuration with programmatic dependent launch allowed (the kernels
+// wait with griddepcontrol.wait before touching global memory) and, for CTA
+// pairs, clusters of two.
+cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, bool pair,
+                                 cudaStream_t stream, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);  // 2 CTAs per pair
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.numAttrs = 1;
+  if (pair) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attr;
   return cfg;
 }
 }  // namespace
 
 cudaError_t max_active_pairs(int* pairs) {
-  cudaLaunchAttribute attr[1];
-  const cudaLaunchConfig_t cfg = pair_config(2, nullptr, attr);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config(dim3(2), dim3(kThreads), kSmemAlloc, true, nullptr, attr);
+  cfg.attrs = attr + 1;  // occupancy of the cluster shape only
+  cfg.numAttrs = 1;
   return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, false, false>, &cfg);
 }
 
@@ -878,17 +898,17 @@ cudaError_t max_active_pairs(int* pairs) {
 cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, bool fp8,
                        cudaStream_t stream) {
   if (paged && fp8) return cudaErrorInvalidValue;
-  if (!pair) {
-    if (fp8) gqa_attn_fwd_sm103_kernel<false, false, true><<<grid, kThreads, kSmemAlloc, stream>>>(p);
-    else if (paged) gqa_attn_fwd_sm103_kernel<false, true, false><<<grid, kThreads, kSmemAlloc, stream>>>(p);
-    else gqa_attn_fwd_sm103_kernel<false, false, false><<<grid, kThreads, kSmemAlloc, stream>>>(p);
-    return cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = launch_config(dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                                               kSmemAlloc, pair, stream, attr);
+  if (pair) {
+    if (fp8) return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, true>, p);
+    return paged ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, false>, p)
+                 : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, false>, p);
   }
-  cudaLaunchAttribute attr[1];
-  const cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
-  if (fp8) return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, true>, p);
-  return paged ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, false>, p)
-               : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, false>, p);
+  if (fp8) return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, true>, p);
+  return paged ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, false>, p)
+               : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, false>, p);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
@@ -896,8 +916,9 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int rows = p.ctas_per_item * kTokPerTile * kGroup;
   const dim3 grid(static_cast<unsigned>(p.tail_items),
                   static_cast<unsigned>((rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock));
-  merge_tail_kernel<<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = launch_config(grid, dim3(256), 0, false, stream, attr);
+  return cudaLaunchKernelEx(&cfg, merge_tail_kernel, p);
 }
 
 cudaError_t status_word_address(int** ptr) {
