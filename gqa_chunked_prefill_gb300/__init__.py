@@ -8,6 +8,7 @@ from ._binding import (GqaError, GqaStatus, gqa_prefill_abi_version, gqa_prefill
                        gqa_prefill_attn_ex, gqa_prefill_attn_noalloc, gqa_prefill_attn_paged,
                        gqa_prefill_attn_paged_ex, gqa_prefill_attn_fp8qk, gqa_prefill_attn_fp8qk_ex,
                        gqa_prefill_attn_paged_varlen, gqa_prefill_attn_paged_varlen_ex,
+                       gqa_prefill_attn_fp8qk_varlen_ex, gqa_prefill_attn_paged_fp8qk_varlen_ex,
                        gqa_prefill_attn_varlen, gqa_prefill_attn_varlen_ex, gqa_prefill_make_plan,
                        gqa_prefill_make_plan_varlen, gqa_prefill_poll, gqa_quantize_k_fp8,
                        gqa_quantize_q_fp8, gqa_status_string, lib)

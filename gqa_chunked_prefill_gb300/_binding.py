@@ -97,6 +97,15 @@ lib.gqa_prefill_attn_paged_varlen_ex.restype = _i
 lib.gqa_prefill_make_plan_varlen.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
                                              ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan_varlen.restype = _i
+lib.gqa_prefill_attn_fp8qk_varlen_ex.argtypes = [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp,
+                                                 _i, _i, _i, _i, _f, _vp,
+                                                 ctypes.POINTER(PrefillOpts),
+                                                 ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_attn_fp8qk_varlen_ex.restype = _i
+lib.gqa_prefill_attn_paged_fp8qk_varlen_ex.argtypes = [
+    _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp,
+    ctypes.POINTER(PrefillOpts), ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_attn_paged_fp8qk_varlen_ex.restype = _i
 lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
                                       ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan.restype = _i
@@ -328,6 +337,44 @@ def gqa_prefill_attn_paged_varlen(q, k_cache, v_cache, block_table, bt_stride, n
     if check:
         _check(rc)
     return rc
+
+
+def gqa_prefill_attn_fp8qk_varlen_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v, out, lse,
+                                     cu_seqlens_q, cu_seqlens_k, n_q_heads, n_kv_heads, head_dim,
+                                     scale, stream=None, force_splits=0, force_grid=0,
+                                     force_variant=0, wait_timeout_us=0, fwd_events=None,
+                                     check=True):
+    cq, pq = _host_i32(cu_seqlens_q)
+    ck, pk = _host_i32(cu_seqlens_k)
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, False)
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_attn_fp8qk_varlen_ex(
+        _ptr(q_fp8), _ptr(q_scale), _ptr(k_fp8), _ptr(k_scale), k_scale_stride, _ptr(v),
+        _ptr(out), _ptr(lse), pq, pk, len(cu_seqlens_q) - 1, n_q_heads, n_kv_heads, head_dim,
+        scale, _stream(stream), ctypes.byref(opts), ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def gqa_prefill_attn_paged_fp8qk_varlen_ex(q_fp8, q_scale, k_cache_fp8, k_scale, k_scale_stride,
+                                           v_cache, block_table, bt_stride, num_pages, page_size,
+                                           out, lse, cu_seqlens_q, kv_lens, n_q_heads, n_kv_heads,
+                                           head_dim, scale, stream=None, force_splits=0,
+                                           force_grid=0, force_variant=0, wait_timeout_us=0,
+                                           fwd_events=None, check=True):
+    cq, pq = _host_i32(cu_seqlens_q)
+    kl, pk = _host_i32(kv_lens)
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, False)
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_attn_paged_fp8qk_varlen_ex(
+        _ptr(q_fp8), _ptr(q_scale), _ptr(k_cache_fp8), _ptr(k_scale), k_scale_stride,
+        _ptr(v_cache), _ptr(block_table), bt_stride, num_pages, page_size, _ptr(out), _ptr(lse),
+        pq, pk, len(kv_lens), n_q_heads, n_kv_heads, head_dim, scale, _stream(stream),
+        ctypes.byref(opts), ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
 
 
 def gqa_prefill_make_plan_varlen(cu_seqlens_q, cu_seqlens_k, n_q_heads, n_kv_heads, head_dim,

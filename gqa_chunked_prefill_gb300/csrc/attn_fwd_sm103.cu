@@ -168,6 +168,18 @@ __device__ __noinline__ void issue_paged_pieces(const PagedGeom& pgeo, const int
   }
 }
 
+// Paged FP8 K: the 128 key scales of a tile that crosses pages, as pieces of
+// sub_rows keys (one 2-D copy each, piece i at dst + i * sub_rows * 4 bytes).
+// Out of line, like issue_paged_pieces.
+__device__ __noinline__ void issue_paged_scale_pieces(const PagedGeom& pgeo, const int* table,
+                                                      const CUtensorMap* map, uint32_t dst,
+                                                      uint32_t bar, int r0, int g, uint64_t pol) {
+  PagedRun run;
+  map_paged_run(pgeo, r0, kBlockN, false, [&](int pg) { return __ldg(table + pg); }, run);
+  for (int i = 0; i < run.n; ++i)
+    ptx::tma_load_2d(dst + i * run.sub * 4, map, bar, run.row[i], g, pol);
+}
+
 // kPair = false: one CTA per work item (21 tokens x 6 heads = 126 MMA rows).
 // kPair = true: a cluster of two CTAs per work item (42 tokens); CTA r holds
 // tokens 21r .. 21r+20 (its own 128 MMA rows), the pair's leader (r = 0)
@@ -298,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&p.tmap_k);
       ptx::prefetch_tmap(&p.tmap_v);
       if constexpr (kFp8) ptx::prefetch_tmap(&p.tmap_ks);
+      if constexpr (kFp8 && kPaged) ptx::prefetch_tmap(&p.tmap_ks_sub);
       if constexpr (kPaged) {
         ptx::prefetch_tmap(&p.tmap_k_sub);
         ptx::prefetch_tmap(&p.tmap_v_sub);
@@ -393,8 +406,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t slot = sc_count % kScSlots, use = sc_count / kScSlots;
             if (use > 0 && !wait_bar(bar(kBarScEmpty + slot), (use - 1) & 1u, p)) return false;
             ptx::mbar_arrive_expect_tx(bar(kBarScFull + slot), kScSlotBytes);
-            ptx::tma_load_2d(base + kOffScales + slot * kScSlotBytes, &p.tmap_ks,
-                             bar(kBarScFull + slot), sq.kv_start + n * kBlockN, g, pol_kv);
+            const uint32_t sdst = base + kOffScales + slot * kScSlotBytes;
+            int srow = sq.kv_start + n * kBlockN;
+            bool swhole = true;
+            if constexpr (kPaged) {  // the scales sit beside the cache rows: same page mapping
+              const int* table = p.block_table + static_cast<size_t>(sq.src) * p.bt_stride;
+              const PagedGeom pgeo{sq.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
+              auto read = [&](int pg) -> int {
+                if (pg != cached_pg[0]) {
+                  cached_entry[0] = __ldg(table + pg);
+                  cached_pg[0] = pg;
+                }
+                return cached_entry[0];
+              };
+              bool bad = false;
+              swhole = paged_whole_box(pgeo, n * kBlockN, kBlockN, false, read, &srow, &bad);
+              if (!swhole)
+                issue_paged_scale_pieces(pgeo, table, &p.tmap_ks_sub, sdst, bar(kBarScFull + slot),
+                                         n * kBlockN, g, pol_kv);
+            }
+            if (swhole) ptx::tma_load_2d(sdst, &p.tmap_ks, bar(kBarScFull + slot), srow, g, pol_kv);
             sc_issued_mask |= 1u << slot;
             sc_issued_parity = (sc_issued_parity & ~(1u << slot)) | ((use & 1u) << slot);
             ++sc_count;
@@ -851,7 +882,9 @@ cudaError_t prepare_fwd_kernel() {
       reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true, false>),
       reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true, false>),
       reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, true>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, true>)};
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, true>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true, true>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true, true>)};
   for (const void* f : kernels) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(kSmemAlloc));
@@ -894,21 +927,22 @@ cudaError_t max_active_pairs(int* pairs) {
   return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, false, false>, &cfg);
 }
 
-// Paged K/V with FP8 QK^T is not instantiated (the host refuses it first).
 cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, bool fp8,
                        cudaStream_t stream) {
-  if (paged && fp8) return cudaErrorInvalidValue;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = launch_config(dim3(static_cast<unsigned>(grid)), dim3(kThreads),
                                                kSmemAlloc, pair, stream, attr);
-  if (pair) {
-    if (fp8) return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, true>, p);
-    return paged ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, false>, p)
-                 : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, false>, p);
+  const int which = (pair ? 4 : 0) | (paged ? 2 : 0) | (fp8 ? 1 : 0);
+  switch (which) {
+    case 0: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, false>, p);
+    case 1: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, true>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, false>, p);
+    case 3: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, true>, p);
+    case 4: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, false>, p);
+    case 5: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, true>, p);
+    case 6: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, false>, p);
+    default: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, true>, p);
   }
-  if (fp8) return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, true>, p);
-  return paged ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, false>, p)
-               : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, false>, p);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {

@@ -378,30 +378,33 @@ bool encode_kv(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_r
   return encode(map, e.dtype, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// A paged K or V cache [rows][4 heads][256] BF16 (rows a multiple of 16) as a
-// 5-D tensor (64 d, key % 8, 64-column chunk, key / 8, head): one box of (64, 8,
-// box_chunks, box_rows / 8, 1) lands in shared memory as 8-key groups, each
-// holding its box_chunks chunks of 8 rows x 128 bytes — the paged stage layout
-// of the attention kernel, in which a piece of whole 8-key groups is contiguous.
+// A paged K or V cache [rows][4 heads][256] (rows a multiple of 16; BF16 values
+// or E4M3 codes) as a 5-D tensor (one 128-byte chunk of d, key % 8, chunk,
+// key / 8, head): one box of (chunk, 8, box_chunks, box_rows / 8, 1) lands in
+// shared memory as 8-key groups, each holding its box_chunks chunks of 8 rows x
+// 128 bytes — the paged stage layout of the attention kernel, in which a piece
+// of whole 8-key groups is contiguous.
 bool encode_kv_paged(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows,
-                     uint32_t box_chunks) {
-  const cuuint64_t row_bytes = static_cast<cuuint64_t>(kKvHeads) * kHeadDim * 2;
-  const cuuint64_t dims[5] = {64, 8, kHeadDim / 64, rows / 8, static_cast<cuuint64_t>(kKvHeads)};
-  const cuuint64_t strides[4] = {row_bytes,       // next key in the group
-                                 64 * 2,          // next chunk
-                                 8 * row_bytes,   // next group of 8 keys
-                                 kHeadDim * 2};   // next head
-  const cuuint32_t box[5] = {64, 8, box_chunks, box_rows / 8, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box,
-                CU_TENSOR_MAP_SWIZZLE_128B);
+                     uint32_t box_chunks, Elem e = kBf16) {
+  const cuuint64_t per_chunk = 128 / e.bytes;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(kKvHeads) * kHeadDim * e.bytes;
+  const cuuint64_t dims[5] = {per_chunk, 8, kHeadDim / per_chunk, rows / 8,
+                              static_cast<cuuint64_t>(kKvHeads)};
+  const cuuint64_t strides[4] = {row_bytes,            // next key in the group
+                                 128,                  // next chunk
+                                 8 * row_bytes,        // next group of 8 keys
+                                 kHeadDim * e.bytes};  // next head
+  const cuuint32_t box[5] = {static_cast<cuuint32_t>(per_chunk), 8, box_chunks, box_rows / 8, 1};
+  return encode(map, e.dtype, 5, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Key scales FP32 [4 heads][stride], box (128 keys, 1 head); keys past kv_len
 // read zeros.
-bool encode_key_scales(CUtensorMap* map, const float* base, uint64_t kv_len, uint64_t stride) {
+bool encode_key_scales(CUtensorMap* map, const float* base, uint64_t kv_len, uint64_t stride,
+                       uint32_t box_keys = kBlockN) {
   const cuuint64_t dims[2] = {kv_len, static_cast<cuuint64_t>(kKvHeads)};
   const cuuint64_t strides[1] = {stride * 4};
-  const cuuint32_t box[2] = {kBlockN, 1};
+  const cuuint32_t box[2] = {box_keys, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_NONE);
 }
@@ -484,7 +487,6 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
                        int* status_word, void* ws, const gqa_prefill_opts* opts,
                        cudaStream_t stream) {
   const bool pair = plan.variant == 2;
-  if (io.pkv && io.f8) return GQA_ERR_UNSUPPORTED;
   static thread_local FwdParams p;  // ~5 KB with the sequence table: not on the stack
   std::memset(&p, 0, sizeof(p));
   const uint64_t kv_rows = io.pkv ? static_cast<uint64_t>(io.pkv->num_pages) * io.pkv->page_size
@@ -504,9 +506,9 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
   } else {
     const PagedKV& pkv = *io.pkv;
     const uint32_t sub = static_cast<uint32_t>(gcd_int(pkv.page_size, 64));  // 16, 32 or 64
-    if (!encode_kv_paged(&p.tmap_k, io.k, kv_rows, k_rows, k_chunks) ||
+    if (!encode_kv_paged(&p.tmap_k, io.k, kv_rows, k_rows, k_chunks, qk) ||
         !encode_kv_paged(&p.tmap_v, io.v, kv_rows, v_rows, v_chunks) ||
-        !encode_kv_paged(&p.tmap_k_sub, io.k, kv_rows, sub, k_chunks) ||
+        !encode_kv_paged(&p.tmap_k_sub, io.k, kv_rows, sub, k_chunks, qk) ||
         !encode_kv_paged(&p.tmap_v_sub, io.v, kv_rows, sub, v_chunks) ||
         !encode_kv_paged(&p.tmap_v16, io.v, kv_rows, 16, v_chunks))
       return GQA_ERR_CUDA;
@@ -518,8 +520,12 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
     p.oob_row = static_cast<int>(kv_rows);
   }
   if (io.f8) {
-    if (!encode_key_scales(&p.tmap_ks, io.f8->k_scale, static_cast<uint64_t>(total_kv),
-                           static_cast<uint64_t>(io.f8->k_scale_stride)))
+    // One scale per key row of K: the packed keys, or every row of the paged cache.
+    const uint64_t scale_rows = io.pkv ? kv_rows : static_cast<uint64_t>(total_kv);
+    const uint64_t stride = static_cast<uint64_t>(io.f8->k_scale_stride);
+    if (!encode_key_scales(&p.tmap_ks, io.f8->k_scale, scale_rows, stride) ||
+        (io.pkv && !encode_key_scales(&p.tmap_ks_sub, io.f8->k_scale, scale_rows, stride,
+                                      static_cast<uint32_t>(p.sub_rows))))
       return GQA_ERR_CUDA;
     p.q_scale = io.f8->q_scale;
   }
@@ -572,7 +578,10 @@ gqa_status run(const CallIO& io, const std::vector<SeqIn>& seqs, int total_q, in
   const bool work = total_q > 0;
   if (st == GQA_OK && work) st = check_pointers(io.q, io.k, io.v, io.out, io.lse);
   if (st == GQA_OK && io.pkv) st = check_paged(*io.pkv, seqs, work);
-  if (st == GQA_OK && io.f8) st = check_fp8(*io.f8, total_kv, work);
+  if (st == GQA_OK && io.f8)
+    st = check_fp8(*io.f8, io.pkv ? static_cast<int64_t>(io.pkv->num_pages) * io.pkv->page_size
+                                  : total_kv,
+                   work);
   if (st != GQA_OK || !work) return st;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != GQA_OK) return st;
@@ -812,6 +821,49 @@ gqa_status gqa_prefill_attn_fp8qk_ex(const void* q_fp8, const float* q_scale, co
   const gqa::Fp8Qk f8{q_scale, k_scale, k_scale_stride};
   const gqa::CallIO io{q_fp8, k_fp8, v, out, lse, nullptr, &f8, scale};
   return gqa::run_one(io, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
+}
+
+gqa_status gqa_prefill_attn_fp8qk_varlen_ex(const void* q_fp8, const float* q_scale,
+                                            const void* k_fp8, const float* k_scale,
+                                            int k_scale_stride, const void* v, void* out,
+                                            float* lse, const int32_t* cu_seqlens_q,
+                                            const int32_t* cu_seqlens_k, int batch, int n_q_heads,
+                                            int n_kv_heads, int head_dim, float scale,
+                                            void* stream, const gqa_prefill_opts* opts,
+                                            gqa_prefill_plan* plan_out) {
+  if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
+  if (batch > 0 && !cu_seqlens_k) return GQA_ERR_NULL;
+  std::vector<gqa::SeqIn> seqs;
+  int total_q = 0;
+  int64_t total_kv = 0;
+  const gqa_status st = gqa::batch_from_host(cu_seqlens_q, cu_seqlens_k, nullptr, batch, &seqs,
+                                             &total_q, &total_kv);
+  if (st != GQA_OK) return st;
+  const gqa::Fp8Qk f8{q_scale, k_scale, k_scale_stride};
+  const gqa::CallIO io{q_fp8, k_fp8, v, out, lse, nullptr, &f8, scale};
+  return gqa::run(io, seqs, total_q, total_kv, n_q_heads, n_kv_heads, head_dim, stream, opts,
+                  plan_out);
+}
+
+gqa_status gqa_prefill_attn_paged_fp8qk_varlen_ex(
+    const void* q_fp8, const float* q_scale, const void* k_cache_fp8, const float* k_scale,
+    int k_scale_stride, const void* v_cache, const int32_t* block_table, int bt_stride,
+    int num_pages, int page_size, void* out, float* lse, const int32_t* cu_seqlens_q,
+    const int32_t* kv_lens, int batch, int n_q_heads, int n_kv_heads, int head_dim, float scale,
+    void* stream, const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out) {
+  if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
+  if (batch > 0 && !kv_lens) return GQA_ERR_NULL;
+  if (bt_stride < 0) return GQA_ERR_SHAPE;
+  std::vector<gqa::SeqIn> seqs;
+  int total_q = 0;
+  int64_t total_kv = 0;
+  const gqa_status st =
+      gqa::batch_from_host(cu_seqlens_q, nullptr, kv_lens, batch, &seqs, &total_q, &total_kv);
+  if (st != GQA_OK) return st;
+  const gqa::PagedKV pkv{block_table, bt_stride, num_pages, page_size};
+  const gqa::Fp8Qk f8{q_scale, k_scale, k_scale_stride};
+  const gqa::CallIO io{q_fp8, k_cache_fp8, v_cache, out, lse, &pkv, &f8, scale};
+  return gqa::run(io, seqs, total_q, 0, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
 }
 
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 4
+#define GQA_PREFILL_ABI_VERSION 5
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -322,6 +322,34 @@ gqa_status gqa_prefill_attn_fp8qk_ex(const void* q_fp8, const float* q_scale, co
                                      void* out, float* lse, int q_len, int kv_len, int n_q_heads,
                                      int n_kv_heads, int head_dim, float scale, void* stream,
                                      const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out);
+
+/*
+ * Quantised QK^T for batched calls, dense or paged (the report's production
+ * path reads its quantised K from a paged cache, gfx936 DCU上实现INT8 QK MMAC, §3).
+ * q_fp8 / q_scale packed [total_q][24][256] / [total_q][24]; V and out as the
+ * BF16 batched calls.
+ *  - dense: k_fp8 packed [total_kv][4][256], k_scale [4][k_scale_stride] with
+ *    k_scale_stride >= total_kv (gqa_quantize_k_fp8 over the packed keys).
+ *  - paged: k_cache_fp8 [num_pages][page_size][4][256] E4M3 codes, k_scale
+ *    [4][k_scale_stride] holding the scale of every CACHE ROW (row = page *
+ *    page_size + slot), k_scale_stride >= num_pages * page_size, a multiple of
+ *    4 (gqa_quantize_k_fp8 over the cache viewed as [num_pages * page_size][4][256]
+ *    writes exactly this); v_cache BF16 as gqa_prefill_attn_paged.
+ */
+gqa_status gqa_prefill_attn_fp8qk_varlen_ex(const void* q_fp8, const float* q_scale,
+                                            const void* k_fp8, const float* k_scale,
+                                            int k_scale_stride, const void* v, void* out,
+                                            float* lse, const int32_t* cu_seqlens_q,
+                                            const int32_t* cu_seqlens_k, int batch, int n_q_heads,
+                                            int n_kv_heads, int head_dim, float scale,
+                                            void* stream, const gqa_prefill_opts* opts,
+                                            gqa_prefill_plan* plan_out);
+gqa_status gqa_prefill_attn_paged_fp8qk_varlen_ex(
+    const void* q_fp8, const float* q_scale, const void* k_cache_fp8, const float* k_scale,
+    int k_scale_stride, const void* v_cache, const int32_t* block_table, int bt_stride,
+    int num_pages, int page_size, void* out, float* lse, const int32_t* cu_seqlens_q,
+    const int32_t* kv_lens, int batch, int n_q_heads, int n_kv_heads, int head_dim, float scale,
+    void* stream, const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out);
 
 /* Static description of a status code (never NULL). */
 const char* gqa_status_string(gqa_status status);

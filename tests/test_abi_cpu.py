@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(gqa):
 
 
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 4
+    assert gqa.gqa_prefill_abi_version() == 5
 
 
 def test_refusals_before_any_cuda_call(gqa):

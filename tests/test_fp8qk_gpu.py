@@ -123,3 +123,61 @@ def test_fp8qk_quantisation_error_is_small_against_bf16_attention(cuda_device):
     err = np.abs(out.double().cpu().numpy() - ref_o)
     assert err.mean() < 5e-3 and err.max() < 6e-2
     assert np.abs(lse.double().cpu().numpy() - ref_l).max() < 5e-2
+
+
+# --- quantised QK^T in batched calls, dense and paged -----------------------------
+
+def _fp8_batch_inputs(lens, seed):
+    from gqa_inputs import make_varlen
+    return make_varlen(lens, seed)
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_fp8qk_varlen_every_element(cuda_device, variant):
+    import gqa_chunked_prefill_gb300 as gqa
+    q, k, v, cu_q, cu_k = _fp8_batch_inputs([(43, 300), (1, 2000), (0, 9), (129, 1000)], 810)
+    q8, qs, k8, ks, stride = quantize_gpu(q, k)
+    dev = torch.device("cuda:0")
+    out = torch.empty((q.shape[0], 24, 256), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((q.shape[0], 24), dtype=torch.float32, device=dev)
+    gqa.gqa_prefill_attn_fp8qk_varlen_ex(q8, qs, k8, ks, stride, v.to(dev), out, lse, cu_q, cu_k,
+                                         24, 4, 256, SCALE, force_variant=variant)
+    torch.cuda.synchronize()
+    assert gqa.gqa_prefill_poll() == 0
+    qc, qsc = oracle.quantize_e4m3(q)
+    kc, ksc = oracle.quantize_e4m3(k)
+    ref_o, ref_l = oracle.varlen_attention(oracle.dequantize_e4m3(qc, qsc),
+                                           oracle.dequantize_e4m3(kc, ksc), v, cu_q, cu_k, SCALE)
+    check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l, "fp8 varlen")
+
+
+@pytest.mark.parametrize("page_size", [16, 784])
+@pytest.mark.parametrize("variant", [1, 2])
+def test_paged_fp8qk_varlen_matches_dense(cuda_device, page_size, variant):
+    """The paged FP8 batch (K codes and scales quantised in place over the whole
+    cache, unused slots NaN) equals the dense FP8 batch bit for bit."""
+    import gqa_chunked_prefill_gb300 as gqa
+    from gqa_inputs import make_paged_batch
+    q, k, v, cu_q, cu_k = _fp8_batch_inputs([(43, 300), (1, 2000), (0, 9), (129, 1000), (5, 5)], 820)
+    kc, vc, table, kv_lens = make_paged_batch(k, v, cu_k, page_size, seed=821)
+    dev = torch.device("cuda:0")
+    rows = kc.shape[0] * page_size
+    stride = -(-rows // 4) * 4
+    kc8 = torch.empty(kc.shape, dtype=torch.uint8, device=dev)
+    kcs = torch.empty((4, stride), dtype=torch.float32, device=dev)
+    gqa.gqa_quantize_k_fp8(kc.to(dev), kc8, kcs, rows, 4, 256, stride)
+    q8, qs, k8, ks, dstride = quantize_gpu(q, k)
+    out_p = torch.empty((q.shape[0], 24, 256), dtype=torch.bfloat16, device=dev)
+    lse_p = torch.empty((q.shape[0], 24), dtype=torch.float32, device=dev)
+    _, plan_p = gqa.gqa_prefill_attn_paged_fp8qk_varlen_ex(
+        q8, qs, kc8, kcs, stride, vc.to(dev), table.to(dev), table.shape[1], kc.shape[0],
+        page_size, out_p, lse_p, cu_q, kv_lens, 24, 4, 256, SCALE, force_variant=variant)
+    out_d = torch.empty_like(out_p)
+    lse_d = torch.empty_like(lse_p)
+    _, plan_d = gqa.gqa_prefill_attn_fp8qk_varlen_ex(q8, qs, k8, ks, dstride, v.to(dev), out_d,
+                                                     lse_d, cu_q, cu_k, 24, 4, 256, SCALE,
+                                                     force_variant=variant)
+    torch.cuda.synchronize()
+    assert gqa.gqa_prefill_poll() == 0
+    assert plan_p == plan_d
+    assert torch.equal(out_p, out_d) and torch.equal(lse_p, lse_d)
