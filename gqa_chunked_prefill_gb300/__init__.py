@@ -11,7 +11,8 @@ from ._binding import (GqaError, GqaStatus, gqa_prefill_abi_version, gqa_prefill
                        gqa_prefill_attn_fp8qk_varlen_ex, gqa_prefill_attn_paged_fp8qk_varlen_ex,
                        gqa_prefill_attn_varlen, gqa_prefill_attn_varlen_ex, gqa_prefill_make_plan,
                        gqa_prefill_make_plan_varlen, gqa_prefill_poll, gqa_quantize_k_fp8,
-                       gqa_quantize_q_fp8, gqa_status_string, lib)
+                       gqa_quantize_k_fp8_varlen, gqa_quantize_q_fp8, gqa_status_string,
+                       key_scale_columns, lib)
 
 N_Q_HEADS, N_KV_HEADS, HEAD_DIM = 24, 4, 256
 

@@ -97,6 +97,8 @@ lib.gqa_prefill_attn_paged_varlen_ex.restype = _i
 lib.gqa_prefill_make_plan_varlen.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
                                              ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan_varlen.restype = _i
+lib.gqa_quantize_k_fp8_varlen.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
+lib.gqa_quantize_k_fp8_varlen.restype = _i
 lib.gqa_prefill_attn_fp8qk_varlen_ex.argtypes = [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp,
                                                  _i, _i, _i, _i, _f, _vp,
                                                  ctypes.POINTER(PrefillOpts),
@@ -334,6 +336,27 @@ def gqa_prefill_attn_paged_varlen(q, k_cache, v_cache, block_table, bt_stride, n
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), bt_stride, num_pages, page_size,
         _ptr(out), _ptr(lse), pq, pk, len(kv_lens), n_q_heads, n_kv_heads, head_dim, scale,
         _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def key_scale_columns(cu_seqlens_k):
+    """Where gqa_quantize_k_fp8_varlen puts each sequence's key scales: column
+    sum of the earlier kv_len rounded up to 4; returns (starts, columns used)."""
+    starts, col = [], 0
+    for b in range(len(cu_seqlens_k) - 1):
+        starts.append(col)
+        col += -(-(cu_seqlens_k[b + 1] - cu_seqlens_k[b]) // 4) * 4
+    return starts, col
+
+
+def gqa_quantize_k_fp8_varlen(k, k_fp8, k_scale, cu_seqlens_k, n_kv_heads, head_dim,
+                              k_scale_stride, stream=None, check=True) -> int:
+    ck, pk = _host_i32(cu_seqlens_k)
+    rc = lib.gqa_quantize_k_fp8_varlen(_ptr(k), _ptr(k_fp8), _ptr(k_scale), pk,
+                                       len(cu_seqlens_k) - 1, n_kv_heads, head_dim,
+                                       k_scale_stride, _stream(stream))
     if check:
         _check(rc)
     return rc

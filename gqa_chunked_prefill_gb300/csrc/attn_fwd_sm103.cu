@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (use > 0 && !wait_bar(bar(kBarScEmpty + slot), (use - 1) & 1u, p)) return false;
             ptx::mbar_arrive_expect_tx(bar(kBarScFull + slot), kScSlotBytes);
             const uint32_t sdst = base + kOffScales + slot * kScSlotBytes;
-            int srow = sq.kv_start + n * kBlockN;
+            int srow = sq.ks_start + n * kBlockN;  // a multiple of 4 (16-byte TMA start)
             bool swhole = true;
             if constexpr (kPaged) {  // the scales sit beside the cache rows: same page mapping
               const int* table = p.block_table + static_cast<size_t>(sq.src) * p.bt_stride;

@@ -78,9 +78,17 @@ size_t fwd_smem_bytes();
 // grid = CTAs; with pair = true the CTAs form clusters of two (grid even).
 cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, bool fp8,
                        cudaStream_t stream);
+// Scale column of each key row for head-major key scales: sequence b of a packed
+// batch (rows row_begin[b] .. row_begin[b+1]-1) starts at column col_begin[b].
+struct ScaleColumns {
+  int n_seq;  // 1: column = row
+  int row_begin[kMaxSeqs + 1];
+  int col_begin[kMaxSeqs];
+};
 // E4M3 codes and scales of rows x heads vectors of 256 BF16 values (quantize_fp8.cu).
 cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scale, int rows, int heads,
-                                int scale_stride, bool head_major, cudaStream_t stream);
+                                int scale_stride, bool head_major, const ScaleColumns& cols,
+                                cudaStream_t stream);
 cudaError_t max_active_pairs(int* pairs);       // co-resident CTA pairs on this device
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t prepare_fwd_kernel();                // per-device one-time attributes

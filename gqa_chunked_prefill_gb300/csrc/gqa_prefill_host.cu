@@ -48,7 +48,20 @@ constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 24, 32};
 // out / LSE and (dense K/V) K / V.
 struct SeqIn {
   int q_start, q_len, kv_start, kv_len;
+  int ks_start;  // FP8 QK^T, dense K: first key-scale column (see key_scale_starts)
 };
+
+// Key-scale columns of a dense FP8 batch: sequence b's scales start at the sum of
+// its predecessors' kv_len, each rounded up to a multiple of 4, so that every
+// tile's scales start on 16 bytes (a TMA requirement). Returns the columns used.
+int64_t key_scale_starts(std::vector<SeqIn>* seqs) {
+  int64_t col = 0;
+  for (SeqIn& s : *seqs) {
+    s.ks_start = static_cast<int>(col);
+    col += (static_cast<int64_t>(s.kv_len) + 3) / 4 * 4;
+  }
+  return col;
+}
 
 int tok_per_item(int variant) { return variant == 2 ? 2 * kTokPerTile : kTokPerTile; }
 
@@ -62,7 +75,7 @@ void build_batch(const std::vector<SeqIn>& in, int variant, Batch* b) {
   for (size_t i = 0; i < in.size(); ++i) {
     if (in[i].q_len <= 0) continue;
     idx.push_back(static_cast<int>(i));
-    const SeqGeo g{0, in[i].q_len, 0, in[i].kv_len, (in[i].q_len + tpi - 1) / tpi, 0, 0};
+    const SeqGeo g{0, in[i].q_len, 0, in[i].kv_len, (in[i].q_len + tpi - 1) / tpi, 0, 0, 0};
     longest[i] = item_tiles(g, tpi, g.n_qtiles - 1);
   }
   std::stable_sort(idx.begin(), idx.end(), [&](int a, int c) { return longest[a] > longest[c]; });
@@ -72,7 +85,8 @@ void build_batch(const std::vector<SeqIn>& in, int variant, Batch* b) {
   for (size_t k = 0; k < idx.size(); ++k) {
     const SeqIn& s = in[static_cast<size_t>(idx[k])];
     const int n_qtiles = (s.q_len + tpi - 1) / tpi;
-    b->seq[k] = SeqGeo{s.q_start, s.q_len, s.kv_start, s.kv_len, n_qtiles, items, idx[k]};
+    b->seq[k] = SeqGeo{s.q_start, s.q_len, s.kv_start, s.kv_len, n_qtiles, items, idx[k],
+                       s.ks_start};
     items += kKvHeads * n_qtiles;
   }
   b->n_items = items;
@@ -250,7 +264,7 @@ gqa_status batch_from_host(const int32_t* cu_q, const int32_t* cu_k, const int32
     const int q_len = cu_q[b + 1] - cu_q[b];
     const int kv_len = cu_k ? cu_k[b + 1] - cu_k[b] : kv_lens[b];
     if (cu_q[b + 1] < cu_q[b] || kv_len < 0 || q_len > kv_len) return GQA_ERR_SHAPE;
-    seqs->push_back(SeqIn{cu_q[b], q_len, cu_k ? cu_k[b] : 0, kv_len});
+    seqs->push_back(SeqIn{cu_q[b], q_len, cu_k ? cu_k[b] : 0, kv_len, 0});
   }
   *total_q = cu_q[batch];
   *total_kv = cu_k ? cu_k[batch] : 0;
@@ -520,8 +534,16 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
     p.oob_row = static_cast<int>(kv_rows);
   }
   if (io.f8) {
-    // One scale per key row of K: the packed keys, or every row of the paged cache.
-    const uint64_t scale_rows = io.pkv ? kv_rows : static_cast<uint64_t>(total_kv);
+    // One scale per key row of K: the packed keys (each sequence from a column that
+    // is a multiple of 4), or every row of the paged cache.
+    uint64_t scale_rows = kv_rows;
+    if (!io.pkv) {
+      scale_rows = 0;
+      for (const SeqIn& sq : seqs) {
+        if (sq.ks_start % 4 != 0) return GQA_ERR_ALIGN;  // every TMA start on 16 bytes
+        scale_rows = std::max<uint64_t>(scale_rows, static_cast<uint64_t>(sq.ks_start) + sq.kv_len);
+      }
+    }
     const uint64_t stride = static_cast<uint64_t>(io.f8->k_scale_stride);
     if (!encode_key_scales(&p.tmap_ks, io.f8->k_scale, scale_rows, stride) ||
         (io.pkv && !encode_key_scales(&p.tmap_ks_sub, io.f8->k_scale, scale_rows, stride,
@@ -578,11 +600,23 @@ gqa_status run(const CallIO& io, const std::vector<SeqIn>& seqs, int total_q, in
   const bool work = total_q > 0;
   if (st == GQA_OK && work) st = check_pointers(io.q, io.k, io.v, io.out, io.lse);
   if (st == GQA_OK && io.pkv) st = check_paged(*io.pkv, seqs, work);
-  if (st == GQA_OK && io.f8)
-    st = check_fp8(*io.f8, io.pkv ? static_cast<int64_t>(io.pkv->num_pages) * io.pkv->page_size
-                                  : total_kv,
-                   work);
+  if (st == GQA_OK && io.f8) {
+    int64_t scale_cols = static_cast<int64_t>(io.pkv ? io.pkv->num_pages : 0) *
+                         (io.pkv ? io.pkv->page_size : 0);
+    if (!io.pkv) {  // dense: every sequence's scales start on a multiple of 4
+      std::vector<SeqIn> tmp = seqs;
+      scale_cols = key_scale_starts(&tmp);
+    }
+    st = check_fp8(*io.f8, scale_cols, work);
+  }
   if (st != GQA_OK || !work) return st;
+  std::vector<SeqIn> fp8_seqs;
+  const std::vector<SeqIn>* use = &seqs;
+  if (io.f8 && !io.pkv) {
+    fp8_seqs = seqs;
+    key_scale_starts(&fp8_seqs);
+    use = &fp8_seqs;
+  }
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != GQA_OK) return st;
   gqa_prefill_plan plan{};
@@ -598,7 +632,7 @@ gqa_status run(const CallIO& io, const std::vector<SeqIn>& seqs, int total_q, in
         cudaSuccess)
       return GQA_ERR_CUDA;
   }
-  st = launch_plan(plan, io, seqs, total_q, total_kv, dev->status_word, ws, opts, stream);
+  st = launch_plan(plan, io, *use, total_q, total_kv, dev->status_word, ws, opts, stream);
   if (ws && cudaFreeAsync(ws, stream) != cudaSuccess) st = GQA_ERR_CUDA;
   return st;
 }
@@ -609,7 +643,7 @@ gqa_status run_one(const CallIO& io, int q_len, int kv_len, int n_q_heads, int n
                    gqa_prefill_plan* plan_out) {
   if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
   if (q_len < 0 || kv_len < q_len) return GQA_ERR_SHAPE;
-  const std::vector<SeqIn> seqs{SeqIn{0, q_len, 0, kv_len}};
+  const std::vector<SeqIn> seqs{SeqIn{0, q_len, 0, kv_len, 0}};
   return run(io, seqs, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
 }
 
@@ -652,7 +686,7 @@ gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, f
   if ((st = device_info(&dev)) != GQA_OK) return st;
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != GQA_OK) return st;
-  const std::vector<SeqIn> seqs{SeqIn{0, q_len, 0, kv_len}};
+  const std::vector<SeqIn> seqs{SeqIn{0, q_len, 0, kv_len, 0}};
   gqa_prefill_plan plan{};
   cached_plan(seqs, dev->num_sms, dev->max_pairs, 0, 0, 0, &plan);
   if (static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes) return GQA_ERR_SCRATCH;
@@ -774,6 +808,15 @@ gqa_status gqa_prefill_attn_paged_varlen(const void* q, const void* k_cache, con
                                           nullptr);
 }
 
+namespace {
+gqa::ScaleColumns one_sequence() {
+  gqa::ScaleColumns c;
+  std::memset(&c, 0, sizeof(c));
+  c.n_seq = 1;
+  return c;
+}
+}  // namespace
+
 gqa_status gqa_quantize_q_fp8(const void* q, void* q_fp8, float* q_scale, int q_len,
                               int n_q_heads, int head_dim, void* stream) {
   if (q_len < 0) return GQA_ERR_SHAPE;
@@ -783,7 +826,7 @@ gqa_status gqa_quantize_q_fp8(const void* q, void* q_fp8, float* q_scale, int q_
   if (gqa::misaligned(q) || gqa::misaligned(q_fp8) || (reinterpret_cast<uintptr_t>(q_scale) & 3u))
     return GQA_ERR_ALIGN;
   return gqa::launch_quantize_fp8(q, q_fp8, q_scale, q_len, gqa::kQHeads, 0, false,
-                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+                                  one_sequence(), static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? GQA_OK
              : GQA_ERR_CUDA;
 }
@@ -798,6 +841,40 @@ gqa_status gqa_quantize_k_fp8(const void* k, void* k_fp8, float* k_scale, int kv
   if (!k || !k_fp8 || !k_scale) return GQA_ERR_NULL;
   if (gqa::misaligned(k) || gqa::misaligned(k_fp8) || gqa::misaligned(k_scale)) return GQA_ERR_ALIGN;
   return gqa::launch_quantize_fp8(k, k_fp8, k_scale, kv_len, gqa::kKvHeads, k_scale_stride, true,
+                                  one_sequence(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
+gqa_status gqa_quantize_k_fp8_varlen(const void* k, void* k_fp8, float* k_scale,
+                                     const int32_t* cu_seqlens_k, int batch, int n_kv_heads,
+                                     int head_dim, int k_scale_stride, void* stream) {
+  if (batch < 0) return GQA_ERR_SHAPE;
+  if (batch > gqa::kMaxSeqs) return GQA_ERR_UNSUPPORTED;
+  if (n_kv_heads != gqa::kKvHeads || head_dim != gqa::kHeadDim) return GQA_ERR_UNSUPPORTED;
+  if (batch == 0) return GQA_OK;
+  if (!cu_seqlens_k) return GQA_ERR_NULL;
+  if (cu_seqlens_k[0] != 0) return GQA_ERR_SHAPE;
+  static thread_local gqa::ScaleColumns cols;
+  std::memset(&cols, 0, sizeof(cols));
+  cols.n_seq = batch;
+  int64_t col = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int kv_len = cu_seqlens_k[b + 1] - cu_seqlens_k[b];
+    if (kv_len < 0) return GQA_ERR_SHAPE;
+    cols.row_begin[b] = cu_seqlens_k[b];
+    cols.col_begin[b] = static_cast<int>(col);
+    col += (static_cast<int64_t>(kv_len) + 3) / 4 * 4;  // as the attention kernel reads them
+  }
+  cols.row_begin[batch] = cu_seqlens_k[batch];
+  const int rows = cu_seqlens_k[batch];
+  if (k_scale_stride < col || k_scale_stride % 4 != 0 ||
+      static_cast<int64_t>(k_scale_stride) * gqa::kKvHeads >= (int64_t{1} << 31))
+    return GQA_ERR_SHAPE;
+  if (rows == 0) return GQA_OK;
+  if (!k || !k_fp8 || !k_scale) return GQA_ERR_NULL;
+  if (gqa::misaligned(k) || gqa::misaligned(k_fp8) || gqa::misaligned(k_scale)) return GQA_ERR_ALIGN;
+  return gqa::launch_quantize_fp8(k, k_fp8, k_scale, rows, gqa::kKvHeads, k_scale_stride, true, cols,
                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? GQA_OK
              : GQA_ERR_CUDA;

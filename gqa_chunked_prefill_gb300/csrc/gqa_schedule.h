@@ -44,6 +44,8 @@ struct SeqGeo {
   int n_qtiles;    // ceil(q_len / tok_per_item)
   int item_begin;  // items of the sequences before it in the call's order
   int src;         // its index in the caller's batch (block-table row of paged K/V)
+  int ks_start;    // FP8 QK^T with dense K: column of its first key in the key-scale rows
+                   //   (a multiple of 4: TMA needs 16-byte-aligned starts)
 };
 
 struct Batch {

@@ -9,6 +9,11 @@
 // are E4M3 (qmax 448, round to nearest even, saturating); Q is quantised once,
 // before attention, like the report's producer-side Q quantisation (§4).
 //
+// Key scales are stored head-major, [4][stride]; in a batch packed end to end,
+// sequence b's scales start at column col_begin[b] (a multiple of 4, so that
+// the attention kernel's TMA copies of them start on 16 bytes) instead of at
+// its first key row.
+//
 // Every rounding decision is taken in FP32 exactly as written: s = amax / 448
 // and x / s are IEEE round-to-nearest divisions (no reciprocal), then one
 // RNE conversion to E4M3. A vector of zeros gets s = 0 and codes 0.
@@ -28,7 +33,7 @@ constexpr int kVecPerBlock = 8;  // 8 warps
 __global__ void __launch_bounds__(256)
     quantize_fp8_kernel(const __nv_bfloat16* __restrict__ x, uint8_t* __restrict__ codes,
                         float* __restrict__ scale, int n_vec, int heads, int scale_stride,
-                        int head_major) {
+                        int head_major, const __grid_constant__ ScaleColumns cols) {
   const int vec = blockIdx.x * kVecPerBlock + static_cast<int>(threadIdx.x >> 5);
   if (vec >= n_vec) return;  // whole warps leave together
   const int lane = threadIdx.x & 31;
@@ -58,7 +63,17 @@ __global__ void __launch_bounds__(256)
       make_uint2(packed[0], packed[1]);
   if (lane == 0) {
     const int row = vec / heads, h = vec - (vec / heads) * heads;
-    scale[head_major ? static_cast<size_t>(h) * scale_stride + row
+    int col = row;  // head-major: the scale column of this row (sequences start on 4)
+    if (head_major && cols.n_seq > 1) {
+      int lo = 0, hi = cols.n_seq - 1;  // the last sequence starting at or before `row`
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cols.row_begin[mid] <= row) lo = mid;
+        else hi = mid - 1;
+      }
+      col = cols.col_begin[lo] + row - cols.row_begin[lo];
+    }
+    scale[head_major ? static_cast<size_t>(h) * scale_stride + col
                      : static_cast<size_t>(row) * heads + h] = s;
   }
 }
@@ -66,13 +81,14 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scale, int rows, int heads,
-                                int scale_stride, bool head_major, cudaStream_t stream) {
+                                int scale_stride, bool head_major, const ScaleColumns& cols,
+                                cudaStream_t stream) {
   const int n_vec = rows * heads;
   if (n_vec == 0) return cudaSuccess;
   const int blocks = (n_vec + kVecPerBlock - 1) / kVecPerBlock;
   quantize_fp8_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x),
                                                    static_cast<uint8_t*>(codes), scale, n_vec,
-                                                   heads, scale_stride, head_major ? 1 : 0);
+                                                   heads, scale_stride, head_major ? 1 : 0, cols);
   return cudaGetLastError();
 }
 

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 5
+#define GQA_PREFILL_ABI_VERSION 6
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -328,14 +328,20 @@ gqa_status gqa_prefill_attn_fp8qk_ex(const void* q_fp8, const float* q_scale, co
  * path reads its quantised K from a paged cache, gfx936 DCU上实现INT8 QK MMAC, §3).
  * q_fp8 / q_scale packed [total_q][24][256] / [total_q][24]; V and out as the
  * BF16 batched calls.
- *  - dense: k_fp8 packed [total_kv][4][256], k_scale [4][k_scale_stride] with
- *    k_scale_stride >= total_kv (gqa_quantize_k_fp8 over the packed keys).
+ *  - dense: k_fp8 packed [total_kv][4][256]; k_scale [4][k_scale_stride] where
+ *    sequence b's scales start at column sum_{i<b} roundup4(kv_len_i) (every
+ *    sequence starts on 16 bytes, as the kernel's TMA copies of them must);
+ *    k_scale_stride >= sum_b roundup4(kv_len_b), a multiple of 4.
+ *    gqa_quantize_k_fp8_varlen writes exactly this layout.
  *  - paged: k_cache_fp8 [num_pages][page_size][4][256] E4M3 codes, k_scale
  *    [4][k_scale_stride] holding the scale of every CACHE ROW (row = page *
  *    page_size + slot), k_scale_stride >= num_pages * page_size, a multiple of
  *    4 (gqa_quantize_k_fp8 over the cache viewed as [num_pages * page_size][4][256]
  *    writes exactly this); v_cache BF16 as gqa_prefill_attn_paged.
  */
+gqa_status gqa_quantize_k_fp8_varlen(const void* k, void* k_fp8, float* k_scale,
+                                     const int32_t* cu_seqlens_k, int batch, int n_kv_heads,
+                                     int head_dim, int k_scale_stride, void* stream);
 gqa_status gqa_prefill_attn_fp8qk_varlen_ex(const void* q_fp8, const float* q_scale,
                                             const void* k_fp8, const float* k_scale,
                                             int k_scale_stride, const void* v, void* out,

@@ -37,7 +37,7 @@ void make_batch(const std::vector<std::pair<int, int>>& lens, int tpi, Batch& b)
     const int ql = lens[i].first, kl = lens[i].second;
     if (ql > 0) {
       const int nq = (ql + tpi - 1) / tpi;
-      b.seq[b.n_seq++] = SeqGeo{q_start, ql, kv_start, kl, nq, items, static_cast<int>(i)};
+      b.seq[b.n_seq++] = SeqGeo{q_start, ql, kv_start, kl, nq, items, static_cast<int>(i), 0};
       items += 4 * nq;
     }
     q_start += ql;

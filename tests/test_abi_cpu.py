@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(gqa):
 
 
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 5
+    assert gqa.gqa_prefill_abi_version() == 6
 
 
 def test_refusals_before_any_cuda_call(gqa):
@@ -242,3 +242,19 @@ def test_varlen_plan_invariants(gqa, lens, variant):
         _, single = gqa.gqa_prefill_make_plan(lens[0][0], lens[0][1], 24, 4, 256, 152,
                                               force_variant=variant)
         assert single == p
+
+
+def test_batched_key_quantisation_refusals(gqa):
+    S = gqa.GqaStatus
+    f = lambda cu_k, stride, **kw: gqa.gqa_quantize_k_fp8_varlen(
+        kw.get("k", 16), 16, kw.get("ks", 16), cu_k, kw.get("hkv", 4), 256, stride, stream=0,
+        check=False)
+    assert gqa.key_scale_columns([0, 5, 12]) == ([0, 8], 16)
+    assert f([0, 5, 12], 12) == S.ERR_SHAPE   # the two sequences need 8 + 8 columns
+    assert f([0, 5, 12], 18) == S.ERR_SHAPE   # stride not a multiple of 4
+    assert f([1, 5], 8) == S.ERR_SHAPE
+    assert f([0, 5, 4], 16) == S.ERR_SHAPE    # decreasing
+    assert f([0, 5], 8, hkv=2) == S.ERR_UNSUPPORTED
+    assert f([0, 5], 8, ks=20) == S.ERR_ALIGN
+    assert f([0, 5], 8, k=None) == S.ERR_NULL
+    assert f([0, 0, 0], 0, k=None, ks=None) == S.OK

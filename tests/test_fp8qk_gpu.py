@@ -132,11 +132,42 @@ def _fp8_batch_inputs(lens, seed):
     return make_varlen(lens, seed)
 
 
+def quantize_batch_gpu(q, k, cu_k):
+    """GPU codes/scales of a packed batch; key scales in the batched layout (each
+    sequence from a column that is a multiple of 4)."""
+    import gqa_chunked_prefill_gb300 as gqa
+    dev = torch.device("cuda:0")
+    qd, kd = q.to(dev).contiguous(), k.to(dev).contiguous()
+    starts, cols = gqa.key_scale_columns(cu_k)
+    stride = max(4, cols)
+    q8 = torch.empty(qd.shape, dtype=torch.uint8, device=dev)
+    qs = torch.empty((qd.shape[0], 24), dtype=torch.float32, device=dev)
+    k8 = torch.empty(kd.shape, dtype=torch.uint8, device=dev)
+    ks = torch.full((4, stride), float("nan"), dtype=torch.float32, device=dev)
+    gqa.gqa_quantize_q_fp8(qd, q8, qs, qd.shape[0], 24, 256)
+    gqa.gqa_quantize_k_fp8_varlen(kd, k8, ks, cu_k, 4, 256, stride)
+    torch.cuda.synchronize()
+    return q8, qs, k8, ks, stride, starts
+
+
+def test_batched_key_scales_land_in_their_columns(cuda_device):
+    q, k, v, cu_q, cu_k = _fp8_batch_inputs([(3, 5), (2, 7), (0, 1), (4, 9)], 800)
+    _, _, k8, ks, _, starts = quantize_batch_gpu(q, k, cu_k)
+    kc, ksc = oracle.quantize_e4m3(k)
+    assert np.array_equal(k8.cpu().numpy(), kc)
+    for b in range(4):
+        n = cu_k[b + 1] - cu_k[b]
+        got = ks[:, starts[b]:starts[b] + n].cpu().numpy()
+        assert np.array_equal(got, ksc[cu_k[b]:cu_k[b + 1]].T), f"sequence {b}"
+    assert starts == [0, 8, 16, 20]
+
+
 @pytest.mark.parametrize("variant", [1, 2])
 def test_fp8qk_varlen_every_element(cuda_device, variant):
     import gqa_chunked_prefill_gb300 as gqa
-    q, k, v, cu_q, cu_k = _fp8_batch_inputs([(43, 300), (1, 2000), (0, 9), (129, 1000)], 810)
-    q8, qs, k8, ks, stride = quantize_gpu(q, k)
+    q, k, v, cu_q, cu_k = _fp8_batch_inputs([(43, 300), (1, 2000), (0, 9), (129, 1001), (2, 3)],
+                                            810)
+    q8, qs, k8, ks, stride, _ = quantize_batch_gpu(q, k, cu_k)
     dev = torch.device("cuda:0")
     out = torch.empty((q.shape[0], 24, 256), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((q.shape[0], 24), dtype=torch.float32, device=dev)
@@ -166,7 +197,7 @@ def test_paged_fp8qk_varlen_matches_dense(cuda_device, page_size, variant):
     kc8 = torch.empty(kc.shape, dtype=torch.uint8, device=dev)
     kcs = torch.empty((4, stride), dtype=torch.float32, device=dev)
     gqa.gqa_quantize_k_fp8(kc.to(dev), kc8, kcs, rows, 4, 256, stride)
-    q8, qs, k8, ks, dstride = quantize_gpu(q, k)
+    q8, qs, k8, ks, dstride, _ = quantize_batch_gpu(q, k, cu_k)
     out_p = torch.empty((q.shape[0], 24, 256), dtype=torch.bfloat16, device=dev)
     lse_p = torch.empty((q.shape[0], 24), dtype=torch.float32, device=dev)
     _, plan_p = gqa.gqa_prefill_attn_paged_fp8qk_varlen_ex(
