@@ -168,16 +168,35 @@ __device__ __noinline__ void issue_paged_pieces(const PagedGeom& pgeo, const int
   }
 }
 
-// Paged FP8 K: the 128 key scales of a tile that crosses pages, as pieces of
-// sub_rows keys (one 2-D copy each, piece i at dst + i * sub_rows * 4 bytes).
-// Out of line, like issue_paged_pieces.
-__device__ __noinline__ void issue_paged_scale_pieces(const PagedGeom& pgeo, const int* table,
-                                                      const CUtensorMap* map, uint32_t dst,
-                                                      uint32_t bar, int r0, int g, uint64_t pol) {
+// Paged FP8 K: the 128 key scales of tile key r0.. of head g into a ring slot.
+// The scales sit in head-major rows beside the cache rows, so the same page
+// mapping applies: one run inside a page, else pieces of sub_rows keys. Each is
+// a 1-D bulk copy (16-byte alignment; a tensor copy would need its shared
+// destination on 128 bytes, which 16-key pieces are not). Pieces past the
+// cache or on a bad table entry are not copied but zeroed, and only the bytes
+// actually copied are expected on `bar`; this thread's arrive (after the
+// zeroing) is the slot's one arrival. Out of line, like issue_paged_pieces.
+__device__ __noinline__ void issue_paged_scales(const PagedGeom& pgeo, const int* table,
+                                                int* status, const float* scale_row,
+                                                uint32_t dst, uint32_t bar, int r0,
+                                                uint64_t pol) {
   PagedRun run;
   map_paged_run(pgeo, r0, kBlockN, false, [&](int pg) { return __ldg(table + pg); }, run);
-  for (int i = 0; i < run.n; ++i)
-    ptx::tma_load_2d(dst + i * run.sub * 4, map, bar, run.row[i], g, pol);
+  if (run.bad) atomicExch(status, static_cast<int>(GQA_ERR_PAGE_TABLE));
+  const int n = run.n == 0 ? 1 : run.n;
+  const int keys = run.n == 0 ? kBlockN : run.sub;
+  uint32_t bytes = 0;
+  for (int i = 0; i < n; ++i) {
+    if (run.row[i] < pgeo.oob_row) {
+      bytes += keys * 4;
+    } else {
+      for (int c = 0; c < keys; c += 4) ptx::st_shared_zero16(dst + (i * keys + c) * 4);
+    }
+  }
+  ptx::mbar_arrive_expect_tx(bar, bytes);
+  for (int i = 0; i < n; ++i)
+    if (run.row[i] < pgeo.oob_row)
+      ptx::bulk_load(dst + i * keys * 4, scale_row + run.row[i], keys * 4, bar, pol);
 }
 
 // kPair = false: one CTA per work item (21 tokens x 6 heads = 126 MMA rows).
@@ -310,7 +329,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::prefetch_tmap(&p.tmap_k);
       ptx::prefetch_tmap(&p.tmap_v);
       if constexpr (kFp8) ptx::prefetch_tmap(&p.tmap_ks);
-      if constexpr (kFp8 && kPaged) ptx::prefetch_tmap(&p.tmap_ks_sub);
       if constexpr (kPaged) {
         ptx::prefetch_tmap(&p.tmap_k_sub);
         ptx::prefetch_tmap(&p.tmap_v_sub);
@@ -405,27 +423,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (each CTA of a pair loads its own copy on its own barrier).
             const uint32_t slot = sc_count % kScSlots, use = sc_count / kScSlots;
             if (use > 0 && !wait_bar(bar(kBarScEmpty + slot), (use - 1) & 1u, p)) return false;
-            ptx::mbar_arrive_expect_tx(bar(kBarScFull + slot), kScSlotBytes);
             const uint32_t sdst = base + kOffScales + slot * kScSlotBytes;
-            int srow = sq.ks_start + n * kBlockN;  // a multiple of 4 (16-byte TMA start)
-            bool swhole = true;
             if constexpr (kPaged) {  // the scales sit beside the cache rows: same page mapping
               const int* table = p.block_table + static_cast<size_t>(sq.src) * p.bt_stride;
               const PagedGeom pgeo{sq.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
-              auto read = [&](int pg) -> int {
-                if (pg != cached_pg[0]) {
-                  cached_entry[0] = __ldg(table + pg);
-                  cached_pg[0] = pg;
-                }
-                return cached_entry[0];
-              };
-              bool bad = false;
-              swhole = paged_whole_box(pgeo, n * kBlockN, kBlockN, false, read, &srow, &bad);
-              if (!swhole)
-                issue_paged_scale_pieces(pgeo, table, &p.tmap_ks_sub, sdst, bar(kBarScFull + slot),
-                                         n * kBlockN, g, pol_kv);
+              issue_paged_scales(pgeo, table, p.status,
+                                 p.k_scale + static_cast<size_t>(g) * p.k_scale_stride, sdst,
+                                 bar(kBarScFull + slot), n * kBlockN, pol_kv);
+            } else {
+              ptx::mbar_arrive_expect_tx(bar(kBarScFull + slot), kScSlotBytes);
+              ptx::tma_load_2d(sdst, &p.tmap_ks, bar(kBarScFull + slot),
+                               sq.ks_start + n * kBlockN, g, pol_kv);  // x: a multiple of 4
             }
-            if (swhole) ptx::tma_load_2d(sdst, &p.tmap_ks, bar(kBarScFull + slot), srow, g, pol_kv);
             sc_issued_mask |= 1u << slot;
             sc_issued_parity = (sc_issued_parity & ~(1u << slot)) | ((use & 1u) << slot);
             ++sc_count;

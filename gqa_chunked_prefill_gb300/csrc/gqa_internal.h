@@ -55,9 +55,9 @@ struct FwdParams {
   int oob_row;               // num_pages * page_size: a row past the cache (TMA zero fill)
   // FP8 QK^T (kernels instantiated with kFp8 only): tmap_q / tmap_k hold E4M3 codes
   // (Q box (128, 6 heads, 21 tokens); K 4-D (128, key, head, chunk) with 2 chunks).
-  CUtensorMap tmap_ks;       // key scales FP32 [4][k_scale_stride], box (128 keys, 1 head);
-                             //   paged: one per cache row, [4][k_scale_stride >= cache rows]
-  CUtensorMap tmap_ks_sub;   // paged: box (sub_rows keys, 1 head) for tiles that cross pages
+  CUtensorMap tmap_ks;       // dense: key scales FP32 [4][k_scale_stride], box (128 keys, 1 head)
+  const float* k_scale;      // paged: one scale per cache row, [4][k_scale_stride], read by
+  int k_scale_stride;        //   1-D bulk copies (16-key pieces are 64 bytes)
   const float* q_scale;      // [total q rows][24] FP32 query scales
   Batch batch;               // the call's sequences (gqa_schedule.h); kept last: it is large
 };

@@ -414,11 +414,10 @@ bool encode_kv_paged(CUtensorMap* map, const void* base, uint64_t rows, uint32_t
 
 // Key scales FP32 [4 heads][stride], box (128 keys, 1 head); keys past kv_len
 // read zeros.
-bool encode_key_scales(CUtensorMap* map, const float* base, uint64_t kv_len, uint64_t stride,
-                       uint32_t box_keys = kBlockN) {
+bool encode_key_scales(CUtensorMap* map, const float* base, uint64_t kv_len, uint64_t stride) {
   const cuuint64_t dims[2] = {kv_len, static_cast<cuuint64_t>(kKvHeads)};
   const cuuint64_t strides[1] = {stride * 4};
-  const cuuint32_t box[2] = {box_keys, 1};
+  const cuuint32_t box[2] = {kBlockN, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box,
                 CU_TENSOR_MAP_SWIZZLE_NONE);
 }
@@ -545,10 +544,10 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
       }
     }
     const uint64_t stride = static_cast<uint64_t>(io.f8->k_scale_stride);
-    if (!encode_key_scales(&p.tmap_ks, io.f8->k_scale, scale_rows, stride) ||
-        (io.pkv && !encode_key_scales(&p.tmap_ks_sub, io.f8->k_scale, scale_rows, stride,
-                                      static_cast<uint32_t>(p.sub_rows))))
+    if (!io.pkv && !encode_key_scales(&p.tmap_ks, io.f8->k_scale, scale_rows, stride))
       return GQA_ERR_CUDA;
+    p.k_scale = io.f8->k_scale;
+    p.k_scale_stride = io.f8->k_scale_stride;
     p.q_scale = io.f8->q_scale;
   }
   build_batch(seqs, plan.variant, &p.batch);
