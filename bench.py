@@ -38,8 +38,8 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from gqa_inputs import (SERVING_PAGE_SIZE, WORKLOADS, make_paged_cache, make_varlen,  # noqa: E402
-                        make_workload, sample_rows)
+from gqa_inputs import (SERVING_PAGE_SIZE, WORKLOADS, make_paged_cache, make_qkv,  # noqa: E402
+                        make_varlen, make_workload, sample_rows)
 
 METRIC = "effective causal attention TFLOPS and % of GB300 BF16 tensor peak"
 UNIT = "TFLOP/s"
@@ -216,6 +216,7 @@ def main():
                     help="also time the paged-K/V entry point with this page size (0: skip)")
     ap.add_argument("--no-fp8", action="store_true", help="skip the quantised-QK^T leg")
     ap.add_argument("--no-varlen", action="store_true", help="skip the batched (varlen) leg")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode leg")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -468,6 +469,42 @@ def main():
                           "sequence, same data"}
         del vq, vk, vv
 
+    # ---- decode: one new token over the workload's prefix (HBM-bound) ------------------
+    decode = None
+    if not args.no_decode:
+        d_len = 1
+        dq, dk, dv = (t.to(dev) for t in make_qkv(d_len, w.kv_len, w.seed + 11))
+        dout = torch.empty_like(dq)
+        dlse = torch.empty((d_len, w.n_q_heads), dtype=torch.float32, device=dev)
+
+        def dcall():
+            gqa.gqa_prefill_attn(dq, dk, dv, dout, dlse, d_len, w.kv_len, w.n_q_heads,
+                                 w.n_kv_heads, w.head_dim, w.scale, stream)
+
+        for _ in range(3):
+            flush.zero_()
+            dcall()
+        d_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(50)]
+        torch.cuda.synchronize(dev)
+        for a, b in d_ev:
+            flush.zero_()
+            a.record(stream)
+            dcall()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        d_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in d_ev) / len(d_ev), pg, dev)
+        kv_bytes = 2 * w.kv_len * w.n_kv_heads * w.head_dim * 2
+        hbm = float(load_peaks()[0].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        gbs = kv_bytes / (d_ms * 1e-3) / 1e9
+        decode = {"q_len": d_len, "kv_len": w.kv_len, "steps": len(d_ev),
+                  "us_per_call": round(d_ms * 1e3, 2), "unit": "GB/s",
+                  "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
+                               "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                               "algorithmic_bytes": kv_bytes},
+                  "note": "K + V read once per call (the bound); L2 flushed before each call"}
+        del dq, dk, dv
+
     if rank != 0:
         if pg:
             pg.destroy_process_group()
@@ -535,6 +572,7 @@ def main():
         "paged": paged,
         "fp8qk": fp8,
         "varlen": varlen,
+        "decode": decode,
         "clocks": clocks,
         "wall_s_timed_loop": round(wall, 4),
     }
