@@ -494,11 +494,27 @@ def main():
             b.record(stream)
         torch.cuda.synchronize(dev)
         d_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in d_ev) / len(d_ev), pg, dev)
+        # the same call replayed from a CUDA graph (how a serving loop issues decode steps)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            dcall()
+        torch.cuda.synchronize(dev)
+        g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(50)]
+        for a, b in g_ev:
+            flush.zero_()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        dg_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in g_ev) / len(g_ev), pg, dev)
+        del graph
         kv_bytes = 2 * w.kv_len * w.n_kv_heads * w.head_dim * 2
         hbm = float(load_peaks()[0].get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
         gbs = kv_bytes / (d_ms * 1e-3) / 1e9
         decode = {"q_len": d_len, "kv_len": w.kv_len, "steps": len(d_ev),
-                  "us_per_call": round(d_ms * 1e3, 2), "unit": "GB/s",
+                  "us_per_call": round(d_ms * 1e3, 2),
+                  "us_per_graph_replay": round(dg_ms * 1e3, 2), "unit": "GB/s",
                   "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm,
                                "unit": "GB/s", "frac": round(gbs / hbm, 4),
                                "algorithmic_bytes": kv_bytes},

@@ -280,11 +280,12 @@ def _host_i32(xs):
 def gqa_prefill_attn_varlen_ex(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, n_q_heads,
                                n_kv_heads, head_dim, scale, stream=None, force_splits=0,
                                force_grid=0, force_variant=0, wait_timeout_us=0, fwd_events=None,
-                               check=True):
+                               test_withhold_q=False, check=True):
     """cu_seqlens_q / cu_seqlens_k: HOST sequences of batch + 1 ints (lists or arrays)."""
     cq, pq = _host_i32(cu_seqlens_q)
     ck, pk = _host_i32(cu_seqlens_k)
-    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, False)
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_varlen_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), pq, pk,
                                         len(cu_seqlens_q) - 1, n_q_heads, n_kv_heads, head_dim,
@@ -311,12 +312,13 @@ def gqa_prefill_attn_paged_varlen_ex(q, k_cache, v_cache, block_table, bt_stride
                                      page_size, out, lse, cu_seqlens_q, kv_lens, n_q_heads,
                                      n_kv_heads, head_dim, scale, stream=None, force_splits=0,
                                      force_grid=0, force_variant=0, wait_timeout_us=0,
-                                     fwd_events=None, check=True):
+                                     fwd_events=None, test_withhold_q=False, check=True):
     """block_table: DEVICE int32 [batch, bt_stride]; cu_seqlens_q (batch + 1) and kv_lens
     (batch): HOST ints."""
     cq, pq = _host_i32(cu_seqlens_q)
     kl, pk = _host_i32(kv_lens)
-    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, False)
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_paged_varlen_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), bt_stride, num_pages, page_size,
@@ -366,10 +368,11 @@ def gqa_prefill_attn_fp8qk_varlen_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_str
                                      cu_seqlens_q, cu_seqlens_k, n_q_heads, n_kv_heads, head_dim,
                                      scale, stream=None, force_splits=0, force_grid=0,
                                      force_variant=0, wait_timeout_us=0, fwd_events=None,
-                                     check=True):
+                                     test_withhold_q=False, check=True):
     cq, pq = _host_i32(cu_seqlens_q)
     ck, pk = _host_i32(cu_seqlens_k)
-    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, False)
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_fp8qk_varlen_ex(
         _ptr(q_fp8), _ptr(q_scale), _ptr(k_fp8), _ptr(k_scale), k_scale_stride, _ptr(v),
@@ -385,10 +388,11 @@ def gqa_prefill_attn_paged_fp8qk_varlen_ex(q_fp8, q_scale, k_cache_fp8, k_scale,
                                            out, lse, cu_seqlens_q, kv_lens, n_q_heads, n_kv_heads,
                                            head_dim, scale, stream=None, force_splits=0,
                                            force_grid=0, force_variant=0, wait_timeout_us=0,
-                                           fwd_events=None, check=True):
+                                           fwd_events=None, test_withhold_q=False, check=True):
     cq, pq = _host_i32(cu_seqlens_q)
     kl, pk = _host_i32(kv_lens)
-    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, False)
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_paged_fp8qk_varlen_ex(
         _ptr(q_fp8), _ptr(q_scale), _ptr(k_cache_fp8), _ptr(k_scale), k_scale_stride,
