@@ -477,9 +477,9 @@ def main():
         dout = torch.empty_like(dq)
         dlse = torch.empty((d_len, w.n_q_heads), dtype=torch.float32, device=dev)
 
-        def dcall():
+        def dcall(st=None):
             gqa.gqa_prefill_attn(dq, dk, dv, dout, dlse, d_len, w.kv_len, w.n_q_heads,
-                                 w.n_kv_heads, w.head_dim, w.scale, stream)
+                                 w.n_kv_heads, w.head_dim, w.scale, st or stream)
 
         for _ in range(3):
             flush.zero_()
@@ -496,8 +496,9 @@ def main():
         d_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in d_ev) / len(d_ev), pg, dev)
         # the same call replayed from a CUDA graph (how a serving loop issues decode steps)
         graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            dcall()
+        side = torch.cuda.Stream(dev)  # graphs are captured off the default stream
+        with torch.cuda.graph(graph, stream=side):
+            dcall(side)
         torch.cuda.synchronize(dev)
         g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(50)]
