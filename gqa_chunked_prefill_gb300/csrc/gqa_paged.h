@@ -21,6 +21,14 @@
 // table is never read past its ceil(kv_len / page_size) entries.
 #pragma once
 
+// Unroll hint for the CUDA compiler only (the host brute-force check builds
+// this header with a plain C++ compiler).
+#if defined(__CUDACC__)
+#define GQA_UNROLL _Pragma("unroll")
+#else
+#define GQA_UNROLL
+#endif
+
 namespace gqa {
 
 struct PagedGeom {
@@ -73,7 +81,7 @@ __host__ __device__ inline void map_paged_run(const PagedGeom& g, int r0, int ro
   int ent[8];
   unsigned live = 0;  // pieces that start below kv_len
   int pg = pg0, off = off0;
-#pragma unroll
+  GQA_UNROLL
   for (int i = 0; i < 8; ++i) {  // independent block-table reads, issued together
     run.row[i] = off;
     ent[i] = 0;
@@ -87,7 +95,7 @@ __host__ __device__ inline void map_paged_run(const PagedGeom& g, int r0, int ro
       ++pg;
     }
   }
-#pragma unroll
+  GQA_UNROLL
   for (int i = 0; i < 8; ++i) {
     const bool is_live = (live >> i) & 1u;
     const bool in_cache = ent[i] >= 0 && ent[i] < g.num_pages;
