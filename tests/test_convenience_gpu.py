@@ -1,0 +1,42 @@
+"""The convenience wrappers of the package (output allocation and argument
+marshalling only) give exactly what the entry points they wrap give."""
+import pytest
+import torch
+
+from gqa_inputs import make_paged_batch, make_qkv, make_varlen
+
+pytestmark = pytest.mark.gpu
+SCALE = 1.0 / 16.0
+
+
+def test_wrappers_match_entry_points(cuda_device):
+    import gqa_chunked_prefill_gb300 as gqa
+    lens = [(43, 300), (1, 2000), (129, 1001)]
+    q, k, v, cu_q, cu_k = (x.cuda() if hasattr(x, "cuda") else x for x in make_varlen(lens, 77))
+    o1, l1 = gqa.attention_varlen(q, k, v, cu_q, cu_k, SCALE)
+    o2 = torch.empty_like(q)
+    l2 = torch.empty_like(l1)
+    gqa.gqa_prefill_attn_varlen(q, k, v, o2, l2, cu_q, cu_k, 24, 4, 256, SCALE)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+    kc, vc, table, kv_lens = make_paged_batch(k.cpu(), v.cpu(), cu_k, 784, seed=78)
+    o3, l3 = gqa.attention_paged(q, kc.cuda(), vc.cuda(), table.cuda(), kv_lens, cu_q, SCALE)
+    assert torch.equal(o3, o1) and torch.equal(l3, l1)
+
+    q8, qs = gqa.quantize_fp8(q)
+    k8, ks = gqa.quantize_fp8(k, cu_k)
+    o4, l4 = gqa.attention_fp8qk(q8, qs, k8, ks, v, cu_q, cu_k, SCALE)
+    o5 = torch.empty_like(q)
+    l5 = torch.empty_like(l1)
+    gqa.gqa_prefill_attn_fp8qk_varlen_ex(q8, qs, k8, ks, ks.shape[1], v, o5, l5, cu_q, cu_k, 24, 4,
+                                         256, SCALE)
+    assert torch.equal(o4, o5) and torch.equal(l4, l5)
+
+    qs1, ks1, vs1 = (t.cuda() for t in make_qkv(50, 400, seed=79))
+    o6, l6 = gqa.attention(qs1, ks1, vs1, SCALE)
+    tbl = torch.arange(1, dtype=torch.int32, device="cuda")
+    o7, l7 = gqa.attention_paged(qs1, ks1.reshape(1, 400, 4, 256), vs1.reshape(1, 400, 4, 256),
+                                 tbl, 400, scale=SCALE)
+    torch.cuda.synchronize()
+    assert gqa.gqa_prefill_poll() == 0
+    assert torch.equal(o6, o7) and torch.equal(l6, l7)
