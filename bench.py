@@ -306,34 +306,63 @@ def main():
     warm_ms = statistics.median(a.elapsed_time(b) for a, b in w_ev)
 
     # ---- end to end through the public call with host buffers ----------------------
-    e2e_steps = min(args.steps, 10)
+    # Every step uploads its Q, K, V from pinned host memory, runs the call and
+    # downloads out and LSE. Steps alternate between two device buffer sets, with
+    # uploads and downloads on their own streams, so that step i+1's uploads and
+    # step i-1's downloads overlap step i's attention, as a serving loop would
+    # issue them; every step still moves all its bytes inside the timed region.
+    e2e_steps = min(args.steps, 20)
     pin = lambda t: t.pin_memory()
     hq, hk, hv = pin(q_cpu), pin(k_cpu), pin(v_cpu)
     ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     h2d = (hq.numel() + hk.numel() + hv.numel()) * 2
     d2h = ho.numel() * 2 + hl.numel() * 4
+    sets = [(q, k, v, out, lse),
+            tuple(torch.empty_like(t) for t in (q, k, v, out, lse))]
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        gqa.gqa_prefill_attn(q, k, v, out, lse, w.q_len, w.kv_len, w.n_q_heads, w.n_kv_heads,
-                             w.head_dim, w.scale, stream)
-        ho.copy_(out, non_blocking=True)
-        hl.copy_(lse, non_blocking=True)
+    def e2e_run(n):
+        ev = lambda: torch.cuda.Event()
+        uploaded, computed, downloaded = ([ev() for _ in range(n)] for _ in range(3))
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    e2e_step()
-    torch.cuda.synchronize(dev)
-    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(e2e_steps)]
-    for a, b in e_ev:
-        flush.zero_()
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e_ev) / e2e_steps, pg, dev)
+        def upload(i):
+            bq, bk, bv = sets[i % 2][:3]
+            if i >= 2:
+                h2d_s.wait_event(computed[i - 2])  # that set's Q/K/V are no longer read
+            with torch.cuda.stream(h2d_s):
+                bq.copy_(hq, non_blocking=True)
+                bk.copy_(hk, non_blocking=True)
+                bv.copy_(hv, non_blocking=True)
+            uploaded[i].record(h2d_s)
+
+        start.record(stream)
+        h2d_s.wait_event(start)
+        d2h_s.wait_event(start)
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            bq, bk, bv, bo, bl = sets[i % 2]
+            stream.wait_event(uploaded[i])
+            if i >= 2:
+                stream.wait_event(downloaded[i - 2])  # that set's out/LSE were read back
+            gqa.gqa_prefill_attn(bq, bk, bv, bo, bl, w.q_len, w.kv_len, w.n_q_heads,
+                                 w.n_kv_heads, w.head_dim, w.scale, stream)
+            computed[i].record(stream)
+            d2h_s.wait_event(computed[i])
+            with torch.cuda.stream(d2h_s):
+                ho.copy_(bo, non_blocking=True)
+                hl.copy_(bl, non_blocking=True)
+            downloaded[i].record(d2h_s)
+        stream.wait_event(downloaded[n - 1])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        return start.elapsed_time(end) / n
+
+    e2e_run(2)
+    e2e_ms = max_over_ranks(e2e_run(e2e_steps), pg, dev)
 
     # ---- the same workload with K/V read from a paged cache ------------------------
     paged = None
@@ -600,6 +629,9 @@ def main():
             "ms_per_step": round(e2e_ms, 4),
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
+            "steps": e2e_steps,
+            "note": "uploads / call / downloads pipelined over two device buffer sets and three "
+                    "streams; no L2 flush (each step's uploads stream 184 MB through L2)",
         },
         "gpu_launches": args.steps * plan["kernels_per_call"],
         "paged": paged,
