@@ -4,7 +4,7 @@ A C-ABI CUDA library (libgqa_prefill.so, declared in include/gqa_prefill.h)
 plus this thin binding. ``attention()`` is the convenience call on torch CUDA
 tensors; the ``gqa_prefill_*`` functions mirror the C entry points one to one.
 """
-from ._binding import (GqaError, GqaStatus, gqa_prefill_abi_version, gqa_prefill_attn,  # noqa: F401
+from ._binding import (FORCE_BALANCED_TAIL, GqaError, GqaStatus, gqa_prefill_abi_version, gqa_prefill_attn,  # noqa: F401
                        gqa_prefill_attn_ex, gqa_prefill_attn_noalloc, gqa_prefill_attn_paged,
                        gqa_prefill_attn_paged_ex, gqa_prefill_attn_fp8qk, gqa_prefill_attn_fp8qk_ex,
                        gqa_prefill_attn_paged_varlen, gqa_prefill_attn_paged_varlen_ex,

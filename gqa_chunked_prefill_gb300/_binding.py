@@ -119,6 +119,10 @@ lib.gqa_prefill_abi_version.argtypes = []
 lib.gqa_prefill_abi_version.restype = _i
 
 
+# force_splits value that asks for the balanced tail (GQA_FORCE_BALANCED_TAIL).
+FORCE_BALANCED_TAIL = -1
+
+
 def _ptr(x):
     if x is None:
         return None

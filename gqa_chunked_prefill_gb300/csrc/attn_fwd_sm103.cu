@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_workers = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
   const int worker = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
   PieceIter pieces;  // this CTA's (pair's) work, in order; each role walks its own copy
-  pieces.init(&p.batch, Schedule{p.head_items, p.tail_splits, p.n_units}, n_workers, worker);
+  pieces.init(&p.batch, p.tail.v, Schedule{p.head_items, p.tail_splits, p.n_units, p.n_tail},
+              n_workers, worker);
   // KV tile holding key kv_len-1 of a sequence when it is partial (else -1).
   auto v_fix_tile = [](const SeqGeo& sq) { return sq.kv_len % kBlockN ? (sq.kv_len - 1) / kBlockN : -1; };
 
@@ -806,15 +807,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Combine the S pieces of every split (tail) item: blocks (j, *) merge item
-// head_items + j, 32 rows each, from slots j*S .. j*S + S-1 (each slot holds one
-// 128-row block per CTA of the item):
+// Combine the pieces of every split (tail) item: blocks (j, *) merge tail item
+// j (item head_items + j), 8 rows each. Its n pieces are read in KV order from
+// their slots (each slot holds one 128-row block per CTA of the item): uniform
+// tail, piece s in slot j*S + s; balanced tail, the workers' slots that
+// balanced_item_pieces / balanced_slot name (an item that no worker boundary
+// cuts was written whole by the attention kernel: its blocks return at once).
 // lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s. One warp per row:
 // lane s reads piece s's LSE (32 pieces per pass), the warp reduces max and
 // sum by shuffles, then every lane accumulates its 8 columns over the pieces
 // in order s = 0, 1, ... with independent loads (unrolled), so a row costs a
-// few memory latencies, not S of them. Deterministic: fixed order throughout.
-constexpr int kMergeRowsPerBlock = 32;  // 8 warps x 4 rows
+// few memory latencies, not n of them; with one row per warp every row of the
+// call is in flight at once. Deterministic: fixed order throughout.
+constexpr int kMergeRowsPerBlock = 8;  // 8 warps x 1 row
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -829,55 +834,62 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 __global__ void __launch_bounds__(256) merge_tail_kernel(const __grid_constant__ MergeParams p) {
   ptx::griddep_wait();  // launched early (programmatic dependent launch): the pieces must be done
-  const int j = blockIdx.x;                               // tail item
-  const int row_begin = blockIdx.y * kMergeRowsPerBlock;  // its rows, both CTAs of a pair
+  const int j = blockIdx.x;  // tail item
+  const bool balanced = p.tail_splits == 0;
+  int n = p.tail_splits, x_lo = 0;
+  if (balanced) {
+    balanced_item_pieces(p.tail.v, p.tail_items, p.workers, j, x_lo, n);
+    if (n < 2) return;  // not split: written by the attention kernel
+  }
   int seq, qt, g;
   item_of(p.batch, p.head_items + j, seq, qt, g);
   const SeqGeo& sq = p.batch.seq[seq];
-  const int S = p.tail_splits;
   const int cpi = p.ctas_per_item;
   const int lane = threadIdx.x & 31;
-  const int row_end = min(row_begin + kMergeRowsPerBlock, cpi * kTokPerTile * kGroup);
-  for (int rr = row_begin + (threadIdx.x >> 5); rr < row_end; rr += 8) {
-    const int r = rr / (kTokPerTile * kGroup);    // CTA of the item
-    const int row = rr % (kTokPerTile * kGroup);  // its MMA row
-    const int tok = kTokPerTile * (cpi * qt + r) + row / kGroup;  // token within the sequence
-    if (tok >= sq.q_len) continue;
-    // Partial row of piece s: slot (j*S + s), CTA r, MMA row `row`.
-    auto prow = [&](int s) {
-      return (static_cast<size_t>(j * S + s) * cpi + r) * kRowsPerTile + row;
-    };
-    float mx = kNegInf;
-    for (int s0 = 0; s0 < S; s0 += 32)
-      if (s0 + lane < S) mx = fmaxf(mx, p.part_lse[prow(s0 + lane)]);
-    mx = warp_max(mx);
-    const float m_use = (mx == kNegInf) ? 0.0f : mx;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    float wsum = 0.0f;
-    for (int s0 = 0; s0 < S; s0 += 32) {
-      const int n = min(32, S - s0);
-      const float w_lane = lane < n ? ptx::ex2_approx(p.part_lse[prow(s0 + lane)] - m_use) : 0.0f;
-      wsum += warp_sum(w_lane);
+  const int rr = blockIdx.y * kMergeRowsPerBlock + static_cast<int>(threadIdx.x >> 5);
+  if (rr >= cpi * kTokPerTile * kGroup) return;
+  const int r = rr / (kTokPerTile * kGroup);    // CTA of the item
+  const int row = rr % (kTokPerTile * kGroup);  // its MMA row
+  const int tok = kTokPerTile * (cpi * qt + r) + row / kGroup;  // token within the sequence
+  if (tok >= sq.q_len) return;
+  // Partial row of piece s: its slot, CTA r, MMA row `row`.
+  auto prow = [&](int s) {
+    const int slot = balanced ? balanced_slot(p.tail.v, p.tail_items, p.workers, j, x_lo, s)
+                              : j * n + s;
+    return (static_cast<size_t>(slot) * cpi + r) * kRowsPerTile + row;
+  };
+  float mx = kNegInf;
+  for (int s0 = 0; s0 < n; s0 += 32)
+    if (s0 + lane < n) mx = fmaxf(mx, p.part_lse[prow(s0 + lane)]);
+  mx = warp_max(mx);
+  const float m_use = (mx == kNegInf) ? 0.0f : mx;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float wsum = 0.0f;
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    const int m = min(32, n - s0);
+    const float w_lane = lane < m ? ptx::ex2_approx(p.part_lse[prow(s0 + lane)] - m_use) : 0.0f;
+    const unsigned long long my_row = lane < m ? prow(s0 + lane) : 0;
+    wsum += warp_sum(w_lane);
 #pragma unroll 8
-      for (int i = 0; i < n; ++i) {
-        const float w = __shfl_sync(0xffffffffu, w_lane, i);
-        const float4* src = reinterpret_cast<const float4*>(p.part_o + prow(s0 + i) * kHeadDim + 8 * lane);
-        const float4 a = src[0], c = src[1];
-        acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-        acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
-      }
+    for (int i = 0; i < m; ++i) {
+      const float w = __shfl_sync(0xffffffffu, w_lane, i);
+      const unsigned long long pr = __shfl_sync(0xffffffffu, my_row, i);
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + pr * kHeadDim + 8 * lane);
+      const float4 a = src[0], c = src[1];
+      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+      acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
     }
-    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-    uint4 o;
-    o.x = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    o.y = ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    o.z = ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    o.w = ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    const size_t orow = static_cast<size_t>(sq.q_start + tok) * kQHeads + kGroup * g + row % kGroup;
-    *reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 8 * lane) = o;
-    if (lane == 0 && p.lse != nullptr)
-      p.lse[orow] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;
   }
+  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+  uint4 o;
+  o.x = ptx::pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  o.y = ptx::pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  o.z = ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  o.w = ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  const size_t orow = static_cast<size_t>(sq.q_start + tok) * kQHeads + kGroup * g + row % kGroup;
+  *reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 8 * lane) = o;
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[orow] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;
 }
 
 }  // namespace
@@ -955,7 +967,7 @@ cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, bool
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
-  if (p.tail_items < 1 || p.tail_splits < 2) return cudaSuccess;
+  if (p.tail_items < 1 || p.tail_splits == 1) return cudaSuccess;
   const int rows = p.ctas_per_item * kTokPerTile * kGroup;
   const dim3 grid(static_cast<unsigned>(p.tail_items),
                   static_cast<unsigned>((rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock));

@@ -33,12 +33,13 @@ struct FwdParams {
   CUtensorMap tmap_v;
   __nv_bfloat16* out;  // [q_len][24][256]
   float* lse;          // [q_len][24] natural log, or null
-  float* part_o;       // [tail pieces][128 rows][256] normalised partial O (tail_splits > 1)
-  float* part_lse;     // [tail pieces][128 rows] base-2 partial LSE        (tail_splits > 1)
+  float* part_o;       // [slots][128 rows][256] normalised partial O of split pieces
+  float* part_lse;     // [slots][128 rows] base-2 partial LSE (slots: gqa_schedule.h)
   int* status;         // per-device status word
   int head_items;      // Schedule (gqa_schedule.h): items processed whole first
-  int tail_splits;     //   pieces per remaining item
-  int n_units;         //   units dealt to the CTAs
+  int tail_splits;     //   pieces per remaining item (0: balanced tail)
+  int n_units;         //   units dealt to the CTAs (uniform tail)
+  int n_tail;          //   tail items (balanced tail)
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
   int withhold_q;      // test only: the producer never loads the first Q tile
@@ -59,6 +60,7 @@ struct FwdParams {
   const float* k_scale;      // paged: one scale per cache row, [4][k_scale_stride], read by
   int k_scale_stride;        //   1-D bulk copies (16-key pieces are 64 bytes)
   const float* q_scale;      // [total q rows][24] FP32 query scales
+  TailPrefix tail;           // balanced tail: tile prefix sums of the tail items
   Batch batch;               // the call's sequences (gqa_schedule.h); kept last: it is large
 };
 
@@ -68,9 +70,11 @@ struct MergeParams {
   __nv_bfloat16* out;
   float* lse;             // may be null
   int head_items;
-  int tail_items;         // one merge block per tail item
-  int tail_splits;
+  int tail_items;         // one merge block column per tail item
+  int tail_splits;        // S > 1 (uniform), or 0 (balanced: pieces from `tail`)
+  int workers;            // balanced: the attention grid's CTAs (or pairs)
   int ctas_per_item;      // 1, or 2 for the CTA-pair kernel (42-token items)
+  TailPrefix tail;        // as FwdParams::tail
   Batch batch;            // as FwdParams::batch
 };
 

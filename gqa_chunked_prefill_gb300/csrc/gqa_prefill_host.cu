@@ -43,6 +43,7 @@ constexpr double kMergeBytesPerUs = 3.0e6;   // effective bandwidth of the merge
 constexpr double kMergeLaunchUs = 6.0;
 constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
 constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 24, 32};
+constexpr int kForceBalanced = GQA_FORCE_BALANCED_TAIL;  // force_splits value: balanced tail
 
 // One sequence of a call as the caller gives it: its rows in the packed Q /
 // out / LSE and (dense K/V) K / V.
@@ -157,9 +158,79 @@ double plan_schedule(const std::vector<int>& tiles, int q_tiles, int num_sms, in
   return us;
 }
 
+// Fills *plan for `variant` with head_rounds whole rounds and a balanced tail
+// (gqa_schedule.h): every worker takes an equal share of the remaining items'
+// tiles, cut at item boundaries. Returns the estimated time in us, or a
+// negative value when the tail does not fit the balanced form (no tail item,
+// more than kMaxBalancedTail of them, fewer tiles than workers, or 2^31 tiles
+// and more). Without whole rounds the grid shrinks to the tail's tile count.
+double plan_balanced(const std::vector<int>& tiles, int q_tiles, int num_sms, int variant,
+                     int workers, int head_rounds, gqa_prefill_plan* plan) {
+  const int n_items = static_cast<int>(tiles.size());
+  const int cpi = variant == 2 ? 2 : 1;
+  const int head = std::min(head_rounds * workers, n_items);
+  const int n_tail = n_items - head;
+  if (n_tail < 1 || n_tail > kMaxBalancedTail) return -1.0;
+  std::vector<int64_t> prefix(static_cast<size_t>(n_tail) + 1, 0);
+  for (int k = 0; k < n_tail; ++k)
+    prefix[static_cast<size_t>(k) + 1] = prefix[static_cast<size_t>(k)] + tiles[static_cast<size_t>(head + k)];
+  const int64_t W = prefix[static_cast<size_t>(n_tail)];
+  if (head == 0) workers = static_cast<int>(std::min<int64_t>(workers, W));
+  if (W < workers || W > INT32_MAX) return -1.0;
+  std::vector<int64_t> load(static_cast<size_t>(workers), 0);
+  int64_t total = W;
+  for (int u = 0; u < head; ++u) {  // whole rounds: the snake deal
+    const int r = u / workers, x = u % workers;
+    const int b = (r & 1) ? workers - 1 - x : x;
+    load[static_cast<size_t>(b)] += tiles[static_cast<size_t>(u)] + kPieceOverheadTiles;
+    total += tiles[static_cast<size_t>(u)];
+  }
+  int pieces = 0, partial = 0, split_items = 0;
+  int k = 0;
+  for (int x = 0; x < workers; ++x) {
+    const int64_t a = x * W / workers, e = (x + 1) * W / workers;
+    load[static_cast<size_t>(x)] += e - a;
+    while (prefix[static_cast<size_t>(k) + 1] <= a) ++k;
+    for (int64_t pos = a; pos < e; ++k) {
+      const int64_t s = prefix[static_cast<size_t>(k)], f = prefix[static_cast<size_t>(k) + 1];
+      const int64_t stop = std::min(e, f);
+      ++pieces;
+      if (pos != s || stop != f) ++partial;
+      if (pos == s && stop != f) ++split_items;  // counted once: at the item's first piece
+      load[static_cast<size_t>(x)] += kPieceOverheadTiles;
+      pos = stop;
+      if (stop < f) break;  // the item continues in the next worker's range
+    }
+  }
+  std::memset(plan, 0, sizeof(*plan));
+  plan->num_sms = num_sms;
+  plan->q_tiles = q_tiles;
+  plan->n_items = n_items;
+  plan->head_rounds = head / workers;
+  plan->tail_items = n_tail;
+  plan->tail_splits = 0;
+  plan->n_units = head + pieces;
+  plan->grid = workers * cpi;
+  plan->kernels_per_call = split_items > 0 ? 2 : 1;
+  plan->variant = variant;
+  plan->total_tiles = total;
+  plan->workspace_bytes =
+      split_items > 0 ? 2 * static_cast<int64_t>(workers) * cpi * kRowsPerTile * kPartialRowBytes : 0;
+  plan->est_makespan_tiles = *std::max_element(load.begin(), load.end());
+  double us = static_cast<double>(plan->est_makespan_tiles) * (variant == 2 ? kPairTileUs : kTileUs);
+  if (split_items > 0) {
+    const double bytes = static_cast<double>(cpi * kRowsPerTile) *
+                         (split_items * 520.0 + partial * static_cast<double>(kPartialRowBytes));
+    us += bytes / kMergeBytesPerUs + kMergeLaunchUs;
+  }
+  return us;
+}
+
 // Best plan of one variant: searches the number of whole rounds (the last few
-// full rounds and none) and the tail split; a split must win by 2 % over the
-// simpler plan to be taken.
+// full rounds and none) and the tail's cut (uniform S-way splits or the
+// balanced tail); a split must win by 2 % over the simpler plan to be taken.
+// force_splits: S > 0 forces the uniform cut with S pieces, kForceBalanced the
+// balanced tail (the best number of whole rounds for it, if any fits).
 double best_plan_of(const std::vector<SeqIn>& seqs, int num_sms, int variant, int workers,
                     int force_splits, gqa_prefill_plan* plan) {
   static thread_local Batch b;  // large: not on the stack
@@ -175,6 +246,17 @@ double best_plan_of(const std::vector<SeqIn>& seqs, int num_sms, int variant, in
                          std::min(force_splits, max_splits), plan);
   double best = plan_schedule(tiles, q_tiles, num_sms, variant, workers, 0, 1, plan);
   gqa_prefill_plan cand{};
+  if (force_splits == kForceBalanced) {
+    double best_b = -1.0;
+    for (int hr = full_rounds; hr >= 0; --hr) {
+      const double us = plan_balanced(tiles, q_tiles, num_sms, variant, workers, hr, &cand);
+      if (us >= 0.0 && (best_b < 0.0 || us < best_b)) {
+        best_b = us;
+        *plan = cand;
+      }
+    }
+    return best_b >= 0.0 ? best_b : best;
+  }
   for (int hr = full_rounds; hr >= 0; --hr) {
     if (hr < full_rounds - 3 && hr != 0) continue;
     for (int S : kSplitCandidates) {
@@ -184,6 +266,11 @@ double best_plan_of(const std::vector<SeqIn>& seqs, int num_sms, int variant, in
         best = us;
         *plan = cand;
       }
+    }
+    const double us = plan_balanced(tiles, q_tiles, num_sms, variant, workers, hr, &cand);
+    if (us >= 0.0 && us < 0.98 * best) {
+      best = us;
+      *plan = cand;
     }
   }
   return best;
@@ -558,14 +645,27 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
   p.head_items = std::min(plan.head_rounds * workers, plan.n_items);
   p.tail_splits = plan.tail_splits;
   p.n_units = plan.n_units;
+  p.n_tail = 0;
+  if (plan.tail_splits == 0) {  // balanced tail: tile prefix sums of the tail items
+    p.n_tail = plan.n_items - p.head_items;
+    p.tail.v[0] = 0;
+    for (int k = 0; k < p.n_tail; ++k) {
+      int seq, qt, g;
+      item_of(p.batch, p.head_items + k, seq, qt, g);
+      p.tail.v[k + 1] = p.tail.v[k] + item_tiles(p.batch.seq[seq], p.batch.tok_per_item, qt);
+    }
+  }
   p.scale_log2 = io.scale * 1.4426950408889634f;
   p.timeout_ns = (opts && opts->wait_timeout_us) ? 1000ull * opts->wait_timeout_us
                                                  : kDefaultTimeoutNs;
   p.withhold_q = (opts && opts->test_withhold_q) ? 1 : 0;
   if (plan.kernels_per_call == 2) {
+    // Partial slots: tail_items * S (uniform tail) or two per worker (balanced).
+    const size_t slots = plan.tail_splits > 0
+                             ? static_cast<size_t>(plan.tail_items) * plan.tail_splits
+                             : 2 * static_cast<size_t>(workers);
     p.part_o = static_cast<float*>(ws);
-    p.part_lse = p.part_o + static_cast<size_t>(plan.tail_items) * plan.tail_splits *
-                                (pair ? 2 : 1) * kRowsPerTile * kHeadDim;
+    p.part_lse = p.part_o + slots * (pair ? 2 : 1) * kRowsPerTile * kHeadDim;
   }
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
@@ -582,7 +682,9 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
     m.head_items = p.head_items;
     m.tail_items = plan.tail_items;
     m.tail_splits = plan.tail_splits;
+    m.workers = workers;
     m.ctas_per_item = pair ? 2 : 1;
+    m.tail = p.tail;
     m.batch = p.batch;
     if (launch_merge(m, stream) != cudaSuccess) return GQA_ERR_CUDA;
   }

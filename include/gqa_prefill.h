@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 6
+#define GQA_PREFILL_ABI_VERSION 7
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -74,12 +74,19 @@ gqa_status gqa_prefill_attn(const void* q, const void* k, const void* v, void* o
                             int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
                             float scale, void* stream);
 
+/* gqa_prefill_opts.force_splits (and the make_plan calls' force_splits): cut the
+   tail in the balanced form (see gqa_prefill_plan). */
+#define GQA_FORCE_BALANCED_TAIL (-1)
+
 /* Options for gqa_prefill_attn_ex (zero-initialise; zero fields mean "default"). */
 typedef struct gqa_prefill_opts {
   int force_splits;           /* 0: planner decides; S > 0: every full round of the
                                  grid takes whole items and each remaining item is
                                  split into S KV pieces (capped at the shortest
-                                 item's tile count; 1 = no split, no merge pass) */
+                                 item's tile count; 1 = no split, no merge pass);
+                                 GQA_FORCE_BALANCED_TAIL: the balanced tail (the
+                                 planner's best number of whole rounds for it), or
+                                 the planner's choice where no tail fits it      */
   int force_grid;             /* > 0: use at most this many CTAs (tests use it to cut
                                  items into many pieces); 0: one CTA per SM       */
   uint32_t wait_timeout_us;   /* bound on any single device-side wait; 0 = 2 s      */
@@ -103,9 +110,11 @@ typedef struct gqa_prefill_opts {
  * A work item is one 21-token query tile of one KV group (21 x 6 = 126 MMA
  * rows); it visits KV tiles of 128 keys up to the causal diagonal. Items are
  * ordered longest first and dealt to the persistent CTAs in a snake, whole
- * items in the first head_rounds full rounds; each remaining (tail) item is
- * split into tail_splits pieces of equal KV length, and a second kernel
- * merges the pieces.
+ * items in the first head_rounds full rounds. The remaining (tail) items are
+ * cut in one of two ways: uniform, each split into tail_splits pieces of equal
+ * KV length; or balanced (tail_splits == 0), their tiles laid end to end and
+ * every CTA (pair) taking an equal share, cut at item boundaries. A second
+ * kernel merges the pieces of every split item.
  */
 typedef struct gqa_prefill_plan {
   int num_sms;                /* SMs of the device                                    */
@@ -113,15 +122,19 @@ typedef struct gqa_prefill_plan {
   int n_items;                /* q_tiles * n_kv_heads                                 */
   int head_rounds;            /* full rounds of whole items                           */
   int tail_items;             /* items after those rounds                             */
-  int tail_splits;            /* KV pieces per tail item (1 = whole, no merge pass)   */
-  int n_units;                /* units dealt: head items + tail_items * tail_splits   */
+  int tail_splits;            /* KV pieces per tail item (1 = whole, no merge pass);
+                                 0 = balanced tail                                    */
+  int n_units;                /* pieces computed: head items + tail_items * tail_splits
+                                 (balanced: head items + the tail's pieces)          */
   int grid;                   /* CTAs launched for the attention kernel               */
   int kernels_per_call;       /* launches per call: 1, or 2 with the merge kernel     */
   int variant;                /* 1 = one CTA per item (M = 128 MMAs, 21 tokens);
                                  2 = a CTA pair per item (cta_group::2, M = 256, 42
                                  tokens: each CTA streams half of every K/V tile)  */
   int64_t total_tiles;        /* KV tiles summed over all items                       */
-  int64_t workspace_bytes;    /* temporary FP32 partials of the split items (or 0)    */
+  int64_t workspace_bytes;    /* temporary FP32 partials of the split items (or 0):
+                                 tail_items * tail_splits slots, or 2 per CTA (pair)
+                                 of a balanced tail, of 128 rows x 257 floats per CTA */
   int64_t est_makespan_tiles; /* planner's cost of the busiest CTA, in KV tiles       */
 } gqa_prefill_plan;
 

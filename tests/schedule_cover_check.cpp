@@ -7,6 +7,10 @@
 // only they write the output directly, that partial slots are exactly
 // 0 .. tail_items*S-1 with item j's pieces in slots j*S .. j*S+S-1 (what the
 // merge kernel reads), and that every unit is dealt to exactly one CTA.
+// The balanced tail (S = 0) is checked the same way, and against the merge
+// kernel's view of it: for every tail item, balanced_item_pieces /
+// balanced_slot must name exactly the workers and slots that wrote its pieces,
+// in KV order, and an item they call unsplit must have been written whole.
 // Prints "checks=N bad=M" and exits non-zero on any mismatch.
 #include "gqa_schedule.h"
 
@@ -46,10 +50,14 @@ void make_batch(const std::vector<std::pair<int, int>>& lens, int tpi, Batch& b)
   b.n_items = items;
 }
 
+void check_balanced(const Batch& b, const std::vector<int>& nts, const std::vector<long long>& off,
+                    const int* grids, int n_grids);
+
 void check_batch(const Batch& b, const int* grids, int n_grids, const int* splits, int n_splits) {
   const int n_items = b.n_items;
   std::vector<int> nts(static_cast<size_t>(n_items));
   int shortest = 1 << 30;
+  std::vector<long long> off(static_cast<size_t>(n_items) + 1, 0);  // first tile of each item
   for (int i = 0; i < n_items; ++i) {  // item_of must invert item numbering
     int seq, qt, g;
     item_of(b, i, seq, qt, g);
@@ -57,6 +65,7 @@ void check_batch(const Batch& b, const int* grids, int n_grids, const int* split
     const int li = 4 * (s.n_qtiles - 1 - qt) + g;
     if (s.item_begin + li != i || qt < 0 || qt >= s.n_qtiles) { ++bad; printf("item_of\n"); }
     nts[static_cast<size_t>(i)] = item_tiles(s, b.tok_per_item, qt);
+    off[static_cast<size_t>(i) + 1] = off[static_cast<size_t>(i)] + nts[static_cast<size_t>(i)];
     if (nts[static_cast<size_t>(i)] < shortest) shortest = nts[static_cast<size_t>(i)];
   }
   for (int gi = 0; gi < n_grids; ++gi)
@@ -67,15 +76,15 @@ void check_batch(const Batch& b, const int* grids, int n_grids, const int* split
       for (int hr : {0, 1, max_rounds}) {
         if (hr > max_rounds) continue;
         const int head = hr * G0 < n_items ? hr * G0 : n_items;
-        const Schedule sc{head, S, head + (n_items - head) * S};
+        const Schedule sc{head, S, head + (n_items - head) * S, 0};
         const int G = G0 < sc.n_units ? G0 : sc.n_units;
         if (hr > 0 && G != G0) continue;  // whole rounds need a full grid
-        std::map<long long, int> cover;
+        std::vector<int> cover(static_cast<size_t>(off[static_cast<size_t>(n_items)]), 0);
         std::map<int, int> slots;
         int units_seen = 0;
         for (int x = 0; x < G; ++x) {
           PieceIter it;
-          it.init(&b, sc, G, x);
+          it.init(&b, nullptr, sc, G, x);
           Piece w;
           while (it.next(w)) {
             ++units_seen;
@@ -92,14 +101,14 @@ void check_batch(const Batch& b, const int* grids, int n_grids, const int* split
                 if (slots[w.slot]++) { ++bad; printf("slot reused\n"); }
               }
             }
-            for (int n = w.n0; n < w.n1; ++n) cover[static_cast<long long>(item) * 100000 + n]++;
+            for (int n = w.n0; n < w.n1; ++n) cover[static_cast<size_t>(off[static_cast<size_t>(item)] + n)]++;
           }
         }
         if (units_seen != sc.n_units) { ++bad; printf("units dealt %d of %d\n", units_seen, sc.n_units); }
         for (int i = 0; i < n_items; ++i)
           for (int n = 0; n < nts[static_cast<size_t>(i)]; ++n) {
             ++checks;
-            const int c = cover[static_cast<long long>(i) * 100000 + n];
+            const int c = cover[static_cast<size_t>(off[static_cast<size_t>(i)] + n)];
             if (c != 1 && ++bad < 10)
               printf("coverage seqs=%d G=%d S=%d hr=%d item=%d tile=%d count=%d\n", b.n_seq, G, S,
                      hr, i, n, c);
@@ -110,6 +119,80 @@ void check_batch(const Batch& b, const int* grids, int n_grids, const int* split
         }
       }
     }
+  check_balanced(b, nts, off, grids, n_grids);
+}
+
+struct Emitted {
+  int x, n0, n1, slot;
+};
+
+void check_balanced(const Batch& b, const std::vector<int>& nts, const std::vector<long long>& off,
+                    const int* grids, int n_grids) {
+  static TailPrefix tp;
+  const int n_items = b.n_items;
+  for (int gi = 0; gi < n_grids; ++gi) {
+    const int max_rounds = n_items / grids[gi];
+    for (int hr : {0, 1, max_rounds}) {
+      if (hr > max_rounds) continue;
+      int G = grids[gi];
+      const int head = hr * G < n_items ? hr * G : n_items;
+      const int n_tail = n_items - head;
+      if (n_tail < 1 || n_tail > kMaxBalancedTail) continue;
+      tp.v[0] = 0;
+      for (int k = 0; k < n_tail; ++k) tp.v[k + 1] = tp.v[k] + nts[static_cast<size_t>(head + k)];
+      const long long W = tp.v[n_tail];
+      if (hr == 0 && W < G) G = static_cast<int>(W);  // the planner shrinks the grid
+      if (W < G) continue;
+      const Schedule sc{head, 0, 0, n_tail};
+      std::vector<int> cover(static_cast<size_t>(off[static_cast<size_t>(n_items)]), 0);
+      std::map<int, int> slots;
+      std::vector<std::vector<Emitted>> by_item(static_cast<size_t>(n_tail));
+      for (int x = 0; x < G; ++x) {
+        PieceIter it;
+        it.init(&b, tp.v, sc, G, x);
+        Piece w;
+        int partial_pieces = 0;
+        while (it.next(w)) {
+          const SeqGeo& s = b.seq[w.seq];
+          const int item = s.item_begin + 4 * (s.n_qtiles - 1 - w.qt) + w.g;
+          const int nt = nts[static_cast<size_t>(item)];
+          if (w.n0 < 0 || w.n1 > nt || w.n0 >= w.n1) { ++bad; printf("balanced: bad range\n"); }
+          const bool whole = w.n0 == 0 && w.n1 == nt;
+          if (whole != (w.slot < 0)) { ++bad; printf("balanced: whole <-> no slot\n"); }
+          if (item < head && !whole) { ++bad; printf("balanced: head item not whole\n"); }
+          if (w.slot >= 0) {
+            ++partial_pieces;
+            if (w.slot != 2 * x && w.slot != 2 * x + 1) { ++bad; printf("balanced: foreign slot\n"); }
+            if (slots[w.slot]++) { ++bad; printf("balanced: slot reused\n"); }
+          }
+          if (item >= head) by_item[static_cast<size_t>(item - head)].push_back({x, w.n0, w.n1, w.slot});
+          for (int n = w.n0; n < w.n1; ++n) cover[static_cast<size_t>(off[static_cast<size_t>(item)] + n)]++;
+        }
+        if (partial_pieces > 2) { ++bad; printf("balanced: more than two partial pieces\n"); }
+      }
+      for (int i = 0; i < n_items; ++i)
+        for (int n = 0; n < nts[static_cast<size_t>(i)]; ++n) {
+          ++checks;
+          if (cover[static_cast<size_t>(off[static_cast<size_t>(i)] + n)] != 1 && ++bad < 10)
+            printf("balanced coverage G=%d hr=%d item=%d tile=%d\n", G, hr, i, n);
+        }
+      for (int k = 0; k < n_tail; ++k) {  // what the merge kernel reads
+        int x_lo = 0, n = 0;
+        balanced_item_pieces(tp.v, n_tail, G, k, x_lo, n);
+        const std::vector<Emitted>& e = by_item[static_cast<size_t>(k)];
+        ++checks;
+        if (static_cast<int>(e.size()) != n) { ++bad; printf("balanced: piece count %d vs %d\n", static_cast<int>(e.size()), n); continue; }
+        if (n == 1 && e[0].slot >= 0) { ++bad; printf("balanced: unsplit item wrote a slot\n"); }
+        int next = 0;
+        for (int i = 0; i < n; ++i) {
+          if (e[static_cast<size_t>(i)].x != x_lo + i || e[static_cast<size_t>(i)].n0 != next) { ++bad; printf("balanced: piece order\n"); }
+          if (n > 1 && e[static_cast<size_t>(i)].slot != balanced_slot(tp.v, n_tail, G, k, x_lo, i)) { ++bad; printf("balanced: merge slot\n"); }
+          next = e[static_cast<size_t>(i)].n1;
+        }
+        if (next != nts[static_cast<size_t>(head + k)]) { ++bad; printf("balanced: item not complete\n"); }
+      }
+    }
+  }
 }
 
 }  // namespace

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(gqa):
 
 
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 6
+    assert gqa.gqa_prefill_abi_version() == 7
 
 
 def test_refusals_before_any_cuda_call(gqa):
@@ -97,9 +97,32 @@ def _total_tiles(q_len, kv_len, tpi=21):
     return sum(4 * (-(-(p0 + min(tpi * (qt + 1), q_len)) // 128)) for qt in range(nq))
 
 
+def _item_tiles(q_len, kv_len, tpi):
+    """KV tiles of every item of one sequence in the call's order: query tiles
+    from the last to the first, the 4 KV groups of each."""
+    p0, nq = kv_len - q_len, -(-q_len // tpi)
+    return [-(-(p0 + min(tpi * (qt + 1), q_len)) // 128) for qt in reversed(range(nq))
+            for _ in range(4)]
+
+
+def _balanced_cut(tail_tiles, G):
+    """Pieces and split items when G workers take equal shares [x*W/G, (x+1)*W/G)
+    of the tail's tiles laid end to end."""
+    W = sum(tail_tiles)
+    starts = [0]
+    for t in tail_tiles:
+        starts.append(starts[-1] + t)
+    bounds = [x * W // G for x in range(G + 1)]
+    pieces = sum(sum(1 for k in range(len(tail_tiles))
+                     if starts[k] < bounds[x + 1] and starts[k + 1] > bounds[x]) for x in range(G))
+    split = sum(1 for k in range(len(tail_tiles))
+                if any(starts[k] < b < starts[k + 1] for b in bounds))
+    return pieces, split
+
+
 @pytest.mark.parametrize("q_len,kv_len", SHAPES)
 @pytest.mark.parametrize("sms", [148, 152])
-@pytest.mark.parametrize("force", [0, 1, 3])
+@pytest.mark.parametrize("force", [0, 1, 3, -1])
 @pytest.mark.parametrize("variant", [0, 1, 2])
 def test_planner_invariants(gqa, q_len, kv_len, sms, force, variant):
     _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_splits=force,
@@ -112,19 +135,29 @@ def test_planner_invariants(gqa, q_len, kv_len, sms, force, variant):
     W = _total_tiles(q_len, kv_len, tpi)
     assert p["q_tiles"] == q_tiles and p["n_items"] == n and p["total_tiles"] == W
     shortest = -(-(kv_len - q_len + min(tpi, q_len)) // 128)
-    assert 1 <= p["tail_splits"] <= max(shortest, 1)
-    if force:
-        assert p["tail_splits"] == min(force, shortest)
     assert p["grid"] % cpi == 0
     workers = p["grid"] // cpi
     head = min(p["head_rounds"] * workers, n)
     assert p["tail_items"] == n - head
-    assert p["n_units"] == head + p["tail_items"] * p["tail_splits"]
-    assert 1 <= workers <= min(sms // cpi, p["n_units"])
-    split = p["tail_splits"] > 1 and p["tail_items"] > 0
-    assert p["kernels_per_call"] == (2 if split else 1)
-    assert p["workspace_bytes"] == (
-        p["tail_items"] * p["tail_splits"] * cpi * 128 * 257 * 4 if split else 0)
+    if p["tail_splits"] == 0:  # balanced tail
+        assert force in (0, -1)
+        tail = _item_tiles(q_len, kv_len, tpi)[head:]
+        assert 1 <= len(tail) <= 512 and sum(tail) >= workers
+        assert 1 <= workers <= sms // cpi
+        pieces, split = _balanced_cut(tail, workers)
+        assert p["n_units"] == head + pieces
+        assert p["kernels_per_call"] == (2 if split else 1)
+        assert p["workspace_bytes"] == (2 * workers * cpi * 128 * 257 * 4 if split else 0)
+    else:
+        assert 1 <= p["tail_splits"] <= max(shortest, 1)
+        if force > 0:
+            assert p["tail_splits"] == min(force, shortest)
+        assert p["n_units"] == head + p["tail_items"] * p["tail_splits"]
+        assert 1 <= workers <= min(sms // cpi, p["n_units"])
+        split = p["tail_splits"] > 1 and p["tail_items"] > 0
+        assert p["kernels_per_call"] == (2 if split else 1)
+        assert p["workspace_bytes"] == (
+            p["tail_items"] * p["tail_splits"] * cpi * 128 * 257 * 4 if split else 0)
     assert p["est_makespan_tiles"] * workers >= W  # the busiest worker carries at least the mean
     _, again = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_splits=force,
                                          force_variant=variant)
@@ -237,7 +270,11 @@ def test_varlen_plan_invariants(gqa, lens, variant):
             tiles += 4 * ((kl - ql + tok_end + 127) // 128)
     assert p["n_items"] == n_items and p["total_tiles"] == tiles
     assert p["grid"] <= 152
-    assert p["n_units"] == (p["n_items"] - p["tail_items"]) + p["tail_items"] * p["tail_splits"]
+    if p["tail_splits"] > 0:
+        assert p["n_units"] == (p["n_items"] - p["tail_items"]) + p["tail_items"] * p["tail_splits"]
+    else:  # balanced tail: every item at least once, at most two extra pieces per worker
+        workers = p["grid"] // (2 if p["variant"] == 2 else 1)
+        assert p["n_items"] <= p["n_units"] <= p["n_items"] + 2 * workers
     if len(lens) == 1:
         _, single = gqa.gqa_prefill_make_plan(lens[0][0], lens[0][1], 24, 4, 256, 152,
                                               force_variant=variant)

@@ -49,7 +49,8 @@ def check_replay(fn, inputs, outputs, new_inputs, stream):
     assert gqa.gqa_prefill_poll() == 0
 
 
-@pytest.mark.parametrize("q_len,kv_len,splits", [(300, 1000, 3), (1, 4096, 16), (129, 129, 1)])
+@pytest.mark.parametrize("q_len,kv_len,splits", [(300, 1000, 3), (1, 4096, 16), (129, 129, 1),
+                                                 (300, 1000, -1), (1, 4096, -1)])
 def test_dense_call_in_a_graph(cuda_device, q_len, kv_len, splits):
     import gqa_chunked_prefill_gb300 as gqa
     s = torch.cuda.Stream()

@@ -91,7 +91,7 @@ def test_fp8qk_small_shapes_every_element(cuda_device, q_len, kv_len, variant):
 
 
 @pytest.mark.parametrize("splits,grid,variant", [(3, 0, 1), (3, 5, 1), (2, 0, 2), (3, 6, 2),
-                                                 (32, 0, 1)])
+                                                 (32, 0, 1), (-1, 0, 1), (-1, 6, 2)])
 def test_fp8qk_split_tail_every_element(cuda_device, splits, grid, variant):
     q, k, v = make_qkv(129, 1000, seed=31)
     out, lse, _ = run_fp8(q, k, v, SCALE, force_splits=splits, force_grid=grid,

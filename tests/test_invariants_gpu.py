@@ -25,7 +25,8 @@ def test_run_twice_bit_identical(cuda_device, name, variant):
 
 
 @pytest.mark.parametrize("q_len,kv_len,t_star", [(100, 700, 40), (300, 300, 150), (512, 4096, 200)])
-@pytest.mark.parametrize("splits,grid,variant", [(0, 0, 1), (3, 9, 1), (0, 0, 2), (3, 10, 2)])
+@pytest.mark.parametrize("splits,grid,variant", [(0, 0, 1), (3, 9, 1), (0, 0, 2), (3, 10, 2),
+                                                 (-1, 0, 1), (-1, 10, 2)])
 def test_future_keys_leave_earlier_rows_bit_identical(cuda_device, q_len, kv_len, t_star, splits,
                                                       grid, variant):
     q, k, v = make_qkv(q_len, kv_len, seed=q_len + kv_len)

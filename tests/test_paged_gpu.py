@@ -71,7 +71,8 @@ def test_paged_small_shapes_every_element(cuda_device, page_size, q_len, kv_len,
 
 
 @pytest.mark.parametrize("page_size", [16, SERVING_PAGE_SIZE])
-@pytest.mark.parametrize("splits,grid,variant", [(3, 0, 1), (3, 5, 1), (2, 0, 2), (3, 6, 2)])
+@pytest.mark.parametrize("splits,grid,variant", [(3, 0, 1), (3, 5, 1), (2, 0, 2), (3, 6, 2),
+                                                 (-1, 0, 1), (-1, 5, 1), (-1, 0, 2), (-1, 6, 2)])
 def test_paged_split_tail_every_element(cuda_device, page_size, splits, grid, variant):
     q, k, v = make_qkv(129, 1000, seed=91)
     plan = check_paged(q, k, v, page_size, seed=92, what=f"split {splits} grid {grid}",

@@ -62,6 +62,27 @@ def test_split_tail_every_element(cuda_device, q_len, kv_len, splits, grid, vari
                 f"{q_len}x{kv_len} splits {splits} grid {grid}")
 
 
+BALANCED = -1  # force_splits value of the balanced tail (GQA_FORCE_BALANCED_TAIL)
+
+
+@pytest.mark.parametrize("q_len,kv_len", [(22, 1000), (129, 1000), (43, 257), (7, 700), (300, 300),
+                                          (1, 129), (512, 4096)])
+@pytest.mark.parametrize("grid,variant", [(0, 1), (0, 2), (5, 1), (3, 1), (6, 2), (10, 2), (152, 1),
+                                          (38, 1), (76, 2)])
+def test_balanced_tail_every_element(cuda_device, q_len, kv_len, grid, variant):
+    """The balanced tail: the tail items' tiles laid end to end and cut into equal
+    shares, one per CTA (pair), whole rounds first where they fit; items cut at
+    any tile, pieces merged from per-worker slots."""
+    q, k, v = make_qkv(q_len, kv_len, seed=19 * q_len + kv_len)
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=BALANCED, force_grid=grid,
+                             force_variant=variant)
+    assert plan["variant"] == variant and plan["grid"] <= (grid or plan["num_sms"])
+    assert plan["tail_splits"] == 0
+    ref_o, ref_l = oracle.attention(q, k, v, SCALE)
+    check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
+                f"{q_len}x{kv_len} balanced grid {grid}")
+
+
 @pytest.mark.parametrize("q_len,kv_len", [(129, 1000), (300, 300)])
 @pytest.mark.parametrize("grid,variant", [(1, 1), (5, 1), (2, 2), (6, 2)])
 def test_whole_items_on_few_ctas(cuda_device, q_len, kv_len, grid, variant):
@@ -76,11 +97,11 @@ def test_whole_items_on_few_ctas(cuda_device, q_len, kv_len, grid, variant):
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
-@pytest.mark.parametrize("variant", [0, 1, 2])
-def test_workload_full_size_sampled_rows(cuda_device, name, variant):
+@pytest.mark.parametrize("variant,splits", [(0, 0), (1, 0), (2, 0), (2, -1)])
+def test_workload_full_size_sampled_rows(cuda_device, name, variant, splits):
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
-    out, lse, plan = run_gpu(q, k, v, w.scale, force_variant=variant)
+    out, lse, plan = run_gpu(q, k, v, w.scale, force_variant=variant, force_splits=splits)
     rows = sample_rows(w.q_len, w.n_q_heads, 1200 if w.q_len * w.kv_len > 4e6 else 4000, seed=5)
     ref_o, ref_l = oracle.attention(q, k, v, w.scale, rows=rows)
     got_o, got_l = gather_rows(out, lse, rows)
@@ -118,14 +139,16 @@ def test_lse_may_be_null(cuda_device):
 
 @pytest.mark.parametrize("q_len", [1, 2, 3, 4])
 @pytest.mark.parametrize("kv_len", [4096, 32768])
-@pytest.mark.parametrize("splits,variant", [(0, 0), (32, 1), (24, 2), (5, 1)])
+@pytest.mark.parametrize("splits,variant", [(0, 0), (32, 1), (24, 2), (5, 1), (-1, 1), (-1, 2)])
 def test_decode_shapes_every_element(cuda_device, q_len, kv_len, splits, variant):
     """Decode-sized chunks (one to four new tokens, 6 to 24 live MMA rows) over a long
     prefix: the whole KV range is cut into many pieces and merged."""
     q, k, v = make_qkv(q_len, kv_len, seed=17 * q_len + kv_len)
     out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_variant=variant)
-    if splits:
+    if splits > 0:
         assert plan["tail_splits"] == splits and plan["kernels_per_call"] == 2
+    if splits < 0:
+        assert plan["tail_splits"] == 0 and plan["kernels_per_call"] == 2
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
                 f"decode {q_len}x{kv_len} S {splits}")
