@@ -213,6 +213,31 @@ __device__ __noinline__ void issue_paged_scales(const PagedGeom& pgeo, const int
 // codes with one FP32 scale per query (token, head) and per key (token, KV
 // head); S = Q_q K_q^T is a kind::f8f6f4 MMA, and every score is restored as
 // S * s_q * s_k * scale before the softmax. PV stays BF16.
+// Transpose of an 8 x 8 matrix of 16-byte quads held by a group of 8 lanes
+// (aligned: lanes 8i .. 8i+7), lane j holding row j: afterwards lane j holds
+// column j, e[s] = old e[j] of lane s. Three butterfly stages; in stage m the
+// lanes whose bit m is set trade their quads i (bit m clear) for their
+// partner's quads i | m. Used by the epilogue so that each store instruction
+// of a group writes 128 contiguous bytes of one output row.
+__device__ __forceinline__ void transpose8_quads(uint4 (&e)[8], int j) {
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool up = (j & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i & m) continue;
+      const uint4 send = up ? e[i] : e[i | m];
+      uint4 recv;
+      recv.x = __shfl_xor_sync(0xffffffffu, send.x, m);
+      recv.y = __shfl_xor_sync(0xffffffffu, send.y, m);
+      recv.z = __shfl_xor_sync(0xffffffffu, send.z, m);
+      recv.w = __shfl_xor_sync(0xffffffffu, send.w, m);
+      if (up) e[i] = recv;
+      else e[i | m] = recv;
+    }
+  }
+}
+
 template <bool kPair, bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
@@ -746,46 +771,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
       const float lse2 = l > 0.0f ? m_ref + __log2f(l) : kNegInf;
+      // Stores go out through groups of 8 lanes: after transpose8_quads each lane
+      // of a group holds one 16-byte quad of each of the group's 8 rows, so every
+      // store instruction writes 128 contiguous bytes of 4 rows instead of 16
+      // bytes of 32 rows (the output rows are 512 bytes, partial rows 1 KB apart).
+      const int gl = lane & 7;                    // lane within its group of 8
+      const int grow0 = warp * 32 + (lane & ~7);  // MMA row of the group's lane 0
+      auto group_row = [&](int s_, int& tok_s) -> bool {
+        const int r = grow0 + s_;
+        tok_s = tok0 + r / kGroup;
+        return r < kTokPerTile * kGroup && tok_s < sq.q_len;
+      };
       if (w.slot < 0) {
-        __nv_bfloat16* dst = p.out + qrow * kHeadDim;
+        size_t off[8];  // element offset of each group row in `out`
+        uint32_t vmask = 0;
+#pragma unroll
+        for (int s_ = 0; s_ < 8; ++s_) {
+          int tok_s;
+          const bool v_ = group_row(s_, tok_s);
+          const int hj_s = (grow0 + s_) % kGroup;
+          off[s_] = (static_cast<size_t>(sq.q_start + tok_s) * kQHeads + kGroup * w.g + hj_s) * kHeadDim;
+          vmask |= (v_ ? 1u : 0u) << s_;
+        }
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t o[32];
-          ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
-          if (valid) {
-            uint32_t pk[16];
+        for (int c = 0; c < 256; c += 64) {
+          uint4 e[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              pk[e] = ptx::pack_bf16x2(__uint_as_float(o[2 * e]) * inv_l,
-                                       __uint_as_float(o[2 * e + 1]) * inv_l);
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+          for (int h = 0; h < 2; ++h) {
+            uint32_t o[32];
+            ptx::tmem_ld_x32(lane_addr + kTmemO + c + 32 * h, o);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            for (int q4 = 0; q4 < 4; ++q4)
+              e[4 * h + q4] = make_uint4(
+                  ptx::pack_bf16x2(__uint_as_float(o[8 * q4]) * inv_l, __uint_as_float(o[8 * q4 + 1]) * inv_l),
+                  ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv_l, __uint_as_float(o[8 * q4 + 3]) * inv_l),
+                  ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv_l, __uint_as_float(o[8 * q4 + 5]) * inv_l),
+                  ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv_l, __uint_as_float(o[8 * q4 + 7]) * inv_l));
           }
+          transpose8_quads(e, gl);
+#pragma unroll
+          for (int s_ = 0; s_ < 8; ++s_)
+            if (vmask & (1u << s_))
+              *reinterpret_cast<uint4*>(p.out + off[s_] + c + 8 * gl) = e[s_];
         }
         if (valid && p.lse != nullptr) p.lse[qrow] = lse2 * kLn2;
       } else {
         // A piece of a split item: normalised partial rows go to the piece's slot
         // (one 128-row block per CTA of the item).
-        const size_t prow =
-            (static_cast<size_t>(w.slot) * (kPair ? 2 : 1) + rank) * kRowsPerTile + row;
-        float* dst = p.part_o + prow * kHeadDim;
+        const size_t slot_row0 =
+            (static_cast<size_t>(w.slot) * (kPair ? 2 : 1) + rank) * kRowsPerTile;
+        uint32_t vmask = 0;
+#pragma unroll
+        for (int s_ = 0; s_ < 8; ++s_) {
+          int tok_s;
+          vmask |= (group_row(s_, tok_s) ? 1u : 0u) << s_;
+        }
+        float* base = p.part_o + (slot_row0 + grow0) * kHeadDim;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
           uint32_t o[32];
           ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
-          if (valid) {
-            float4* d4 = reinterpret_cast<float4*>(dst + c);
+          uint4 e[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              d4[e] = make_float4(__uint_as_float(o[4 * e]) * inv_l,
-                                  __uint_as_float(o[4 * e + 1]) * inv_l,
-                                  __uint_as_float(o[4 * e + 2]) * inv_l,
-                                  __uint_as_float(o[4 * e + 3]) * inv_l);
-          }
+          for (int q4 = 0; q4 < 8; ++q4)
+            e[q4] = make_uint4(__float_as_uint(__uint_as_float(o[4 * q4]) * inv_l),
+                               __float_as_uint(__uint_as_float(o[4 * q4 + 1]) * inv_l),
+                               __float_as_uint(__uint_as_float(o[4 * q4 + 2]) * inv_l),
+                               __float_as_uint(__uint_as_float(o[4 * q4 + 3]) * inv_l));
+          transpose8_quads(e, gl);
+#pragma unroll
+          for (int s_ = 0; s_ < 8; ++s_)
+            if (vmask & (1u << s_))
+              *reinterpret_cast<uint4*>(base + static_cast<size_t>(s_) * kHeadDim + c + 4 * gl) = e[s_];
         }
-        if (valid) p.part_lse[prow] = lse2;
+        if (valid) p.part_lse[slot_row0 + row] = lse2;
       }
       ptx::tc_fence_before();
       arrive_leader(kBarOFree);
