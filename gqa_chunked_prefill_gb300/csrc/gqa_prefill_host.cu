@@ -39,8 +39,8 @@ constexpr double kTileUs = 1.5;              // planning estimate per tile, one-
 // GB300 the pair kernel is ~1.1x faster per tile (4096x32768: 1.75 ms vs
 // 1.92 ms; 3072x16384: 0.67 ms vs 0.74 ms): each SM streams half the operands.
 constexpr double kPairTileUs = 1.35;
-constexpr double kMergeBytesPerUs = 3.0e6;   // effective bandwidth of the merge pass
-constexpr double kMergeLaunchUs = 6.0;
+constexpr double kMergeBytesPerUs = 6.0e6;   // effective bandwidth of the merge pass (partials in L2)
+constexpr double kMergeLaunchUs = 3.0;       // its launch, mostly hidden by programmatic launch
 constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
 constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 24, 32};
 constexpr int kForceBalanced = GQA_FORCE_BALANCED_TAIL;  // force_splits value: balanced tail
@@ -266,11 +266,6 @@ double best_plan_of(const std::vector<SeqIn>& seqs, int num_sms, int variant, in
         best = us;
         *plan = cand;
       }
-    }
-    const double us = plan_balanced(tiles, q_tiles, num_sms, variant, workers, hr, &cand);
-    if (us >= 0.0 && us < 0.98 * best) {
-      best = us;
-      *plan = cand;
     }
   }
   return best;
