@@ -533,15 +533,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stepping through a tile is one add.
         auto issue_qk = [&](int j) -> bool {
           const uint32_t T = tile + j;
+          // K arrives as kKStagesPerTile stages of kNchK 128-byte chunks (one-CTA
+          // BF16: two d halves; pairs and FP8: one stage); every MMA advances
+          // 32 bytes along d (16 BF16 or 32 FP8 values). The first K stage is waited
+          // for before s_free: it has usually landed long before, and the wait for
+          // the softmax is then the last thing between S being free and the MMAs.
+          if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
           // S may be overwritten once the softmax holds tile T-1's scores in registers.
           if (T > 0 && !wait_bar(bar(kBarSFree), (T - 1) & 1u, p)) return false;
           ptx::tc_fence_after();
-          // K arrives as kKStagesPerTile stages of kNchK 128-byte chunks (one-CTA
-          // BF16: two d halves; pairs and FP8: one stage); every MMA advances
-          // 32 bytes along d (16 BF16 or 32 FP8 values).
 #pragma unroll
           for (int half = 0; half < kKStagesPerTile; ++half) {
-            if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
+            if (half > 0 && !wait_bar(bar(kBarFull + st), phase, p)) return false;
             ptx::tc_fence_after();
             const uint64_t kd = k_desc0 + ((st * kStageBytes) >> 4);
 #pragma unroll
@@ -573,6 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j + 1 < nt && !(ok = issue_qk(j + 1))) break;
           const uint32_t T = tile + j;
           const uint32_t b = T & 1u;
+          // The (first) V stage before P, for the same reason as K before s_free.
+          if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
           if (!(ok = wait_bar(bar(b ? kBarPFull1 : kBarPFull0), (T >> 1) & 1u, p))) break;
           if (j == 0 && k > 0 && !(ok = wait_bar(bar(kBarOFree), (k - 1) & 1, p))) break;
           ptx::tc_fence_after();
@@ -582,8 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool v_fix = kPaged && w.n0 + j == vfix_tile;
           const int kr = p.batch.seq[w.seq].kv_len - vfix_tile * kBlockN;  // used when v_fix
           if constexpr (kPair) {
-            // One stage: 128 keys x this CTA's 2 chunks of 64 columns.
-            if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
+            // One stage: 128 keys x this CTA's 2 chunks of 64 columns (waited for above).
             ptx::tc_fence_after();
             if (v_fix) {
               zero_v_tail(stage_smem + st * kStageBytes, kNchV, 0, kRowsV, kr, false);
@@ -603,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             // Two stages (key halves), each 64 keys x 4 chunks of 64 d.
             for (int half = 0; half < 2 && ok; ++half) {
-              if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
+              if (half > 0 && !(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
               ptx::tc_fence_after();
               if (v_fix) {
                 zero_v_tail(stage_smem + st * kStageBytes, kNchV, kRowsV * half, kRowsV, kr, false);
