@@ -12,7 +12,10 @@ import ctypes
 import enum
 import os
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgqa_prefill.so")
+# GQA_PREFILL_LIB selects another build of the same library, e.g. the bounds-checked
+# libgqa_prefill_checked.so next to this file (the tests run the parity suite on it).
+_LIB_PATH = os.environ.get("GQA_PREFILL_LIB") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libgqa_prefill.so")
 
 
 class GqaStatus(enum.IntEnum):
@@ -25,6 +28,7 @@ class GqaStatus(enum.IntEnum):
     ERR_DEVICE_TIMEOUT = 6
     ERR_SCRATCH = 7
     ERR_PAGE_TABLE = 8
+    ERR_BOUNDS = 9
 
 
 class GqaError(RuntimeError):

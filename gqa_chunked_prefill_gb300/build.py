@@ -17,8 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libgqa_prefill.so")
-BUILD_DIR = os.path.join(PKG, "_build", platform.machine())
-STAMP = LIB + ".arch"
+CHECKED_LIB = os.path.join(PKG, "libgqa_prefill_checked.so")  # built with GQA_CHECK_BOUNDS
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -41,21 +40,28 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _arch_matches() -> bool:
+def _arch_matches(stamp: str) -> bool:
     try:
-        return open(STAMP).read().strip() == platform.machine()
+        return open(stamp).read().strip() == platform.machine()
     except OSError:
         return False
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    force = force or not _arch_matches()
+def build(force: bool = False, verbose: bool = False, extra_flags=(), check_bounds: bool = False) -> str:
+    """libgqa_prefill.so, or with check_bounds the bounds-checked libgqa_prefill_checked.so
+    (same sources and ABI; every epilogue store and merge access checks its row)."""
+    lib = CHECKED_LIB if check_bounds else LIB
+    build_dir = os.path.join(PKG, "_build", platform.machine() + ("-checked" if check_bounds else ""))
+    stamp = lib + ".arch"
+    if check_bounds:
+        extra_flags = list(extra_flags) + ["-DGQA_CHECK_BOUNDS=1"]
+    os.makedirs(build_dir, exist_ok=True)
+    force = force or not _arch_matches(stamp)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     objs, jobs = [], []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             jobs.append([nvcc(), *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj])
@@ -69,12 +75,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, len(jobs))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        run([nvcc(), *ARCH, "-shared", "-o", LIB + ".tmp", *objs])
-        os.replace(LIB + ".tmp", LIB)
-        with open(STAMP, "w") as f:
+    if force or jobs or _stale(lib, objs):
+        run([nvcc(), *ARCH, "-shared", "-o", lib + ".tmp", *objs])
+        os.replace(lib + ".tmp", lib)
+        with open(stamp, "w") as f:
             f.write(platform.machine())
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

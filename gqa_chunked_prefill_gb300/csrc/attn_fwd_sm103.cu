@@ -108,6 +108,22 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 __device__ int g_status_word = 0;
 
+// Bounds-checked build (compiled with -DGQA_CHECK_BOUNDS, libgqa_prefill_checked.so):
+// every global store of the epilogue and every read and write of the merge pass
+// checks its row against the buffer's extent first; a row outside records
+// GQA_ERR_BOUNDS in the status word and the access is skipped. (No device assert,
+// no trap: the substitute for a memory checker, which this kernel's tests run under.)
+#ifdef GQA_CHECK_BOUNDS
+constexpr bool kCheckBounds = true;
+#else
+constexpr bool kCheckBounds = false;
+#endif
+__device__ __forceinline__ bool row_ok(long long r, long long rows, int* status) {
+  if (!kCheckBounds || (r >= 0 && r < rows)) return true;
+  atomicExch(status, static_cast<int>(GQA_ERR_BOUNDS));
+  return false;
+}
+
 // Bounded wait for the phase of `bar` with the given parity.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const FwdParams& p) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -815,10 +831,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           transpose8_quads(e, gl);
 #pragma unroll
           for (int s_ = 0; s_ < 8; ++s_)
-            if (vmask & (1u << s_))
+            if ((vmask & (1u << s_)) &&
+                row_ok(static_cast<long long>(off[s_] / kHeadDim), p.out_rows, p.status))
               *reinterpret_cast<uint4*>(p.out + off[s_] + c + 8 * gl) = e[s_];
         }
-        if (valid && p.lse != nullptr) p.lse[qrow] = lse2 * kLn2;
+        if (valid && p.lse != nullptr && row_ok(static_cast<long long>(qrow), p.out_rows, p.status))
+          p.lse[qrow] = lse2 * kLn2;
       } else {
         // A piece of a split item: normalised partial rows go to the piece's slot
         // (one 128-row block per CTA of the item).
@@ -845,10 +863,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           transpose8_quads(e, gl);
 #pragma unroll
           for (int s_ = 0; s_ < 8; ++s_)
-            if (vmask & (1u << s_))
+            if ((vmask & (1u << s_)) &&
+                row_ok(static_cast<long long>(slot_row0 + grow0 + s_), p.part_rows, p.status))
               *reinterpret_cast<uint4*>(base + static_cast<size_t>(s_) * kHeadDim + c + 4 * gl) = e[s_];
         }
-        if (valid) p.part_lse[slot_row0 + row] = lse2;
+        if (valid && row_ok(static_cast<long long>(slot_row0 + row), p.part_rows, p.status))
+          p.part_lse[slot_row0 + row] = lse2;
       }
       ptx::tc_fence_before();
       arrive_leader(kBarOFree);
@@ -921,6 +941,12 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const __grid_constant__
                               : j * n + s;
     return (static_cast<size_t>(slot) * cpi + r) * kRowsPerTile + row;
   };
+  if constexpr (kCheckBounds) {  // every partial row this warp will read
+    bool rows_ok = true;
+    for (int s0 = 0; s0 < n; s0 += 32)
+      if (s0 + lane < n) rows_ok &= row_ok(static_cast<long long>(prow(s0 + lane)), p.part_rows, p.status);
+    if (!__all_sync(0xffffffffu, rows_ok)) return;
+  }
   float mx = kNegInf;
   for (int s0 = 0; s0 < n; s0 += 32)
     if (s0 + lane < n) mx = fmaxf(mx, p.part_lse[prow(s0 + lane)]);
@@ -950,6 +976,7 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const __grid_constant__
   o.z = ptx::pack_bf16x2(acc[4] * inv, acc[5] * inv);
   o.w = ptx::pack_bf16x2(acc[6] * inv, acc[7] * inv);
   const size_t orow = static_cast<size_t>(sq.q_start + tok) * kQHeads + kGroup * g + row % kGroup;
+  if (!row_ok(static_cast<long long>(orow), p.out_rows, p.status)) return;
   *reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 8 * lane) = o;
   if (lane == 0 && p.lse != nullptr)
     p.lse[orow] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;

@@ -36,6 +36,8 @@ struct FwdParams {
   float* part_o;       // [slots][128 rows][256] normalised partial O of split pieces
   float* part_lse;     // [slots][128 rows] base-2 partial LSE (slots: gqa_schedule.h)
   int* status;         // per-device status word
+  long long out_rows;  // rows of 256 values in out / entries of lse (bounds-checked build)
+  long long part_rows; // rows in part_o / part_lse (bounds-checked build)
   int head_items;      // Schedule (gqa_schedule.h): items processed whole first
   int tail_splits;     //   pieces per remaining item (0: balanced tail)
   int n_units;         //   units dealt to the CTAs (uniform tail)
@@ -69,6 +71,9 @@ struct MergeParams {
   const float* part_lse;  // as FwdParams::part_lse
   __nv_bfloat16* out;
   float* lse;             // may be null
+  int* status;            // per-device status word
+  long long out_rows;     // as FwdParams (bounds-checked build)
+  long long part_rows;
   int head_items;
   int tail_items;         // one merge block column per tail item
   int tail_splits;        // S > 1 (uniform), or 0 (balanced: pieces from `tail`)

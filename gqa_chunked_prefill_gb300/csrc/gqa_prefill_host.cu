@@ -637,6 +637,8 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
   p.out = static_cast<__nv_bfloat16*>(io.out);
   p.lse = io.lse;
   p.status = status_word;
+  p.out_rows = static_cast<long long>(total_q) * kQHeads;
+  p.part_rows = 0;
   p.head_items = std::min(plan.head_rounds * workers, plan.n_items);
   p.tail_splits = plan.tail_splits;
   p.n_units = plan.n_units;
@@ -661,6 +663,7 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
                              : 2 * static_cast<size_t>(workers);
     p.part_o = static_cast<float*>(ws);
     p.part_lse = p.part_o + slots * (pair ? 2 : 1) * kRowsPerTile * kHeadDim;
+    p.part_rows = static_cast<long long>(slots) * (pair ? 2 : 1) * kRowsPerTile;
   }
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
@@ -674,6 +677,9 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
     m.part_lse = p.part_lse;
     m.out = p.out;
     m.lse = io.lse;
+    m.status = p.status;
+    m.out_rows = p.out_rows;
+    m.part_rows = p.part_rows;
     m.head_items = p.head_items;
     m.tail_items = plan.tail_items;
     m.tail_splits = plan.tail_splits;
@@ -1107,6 +1113,9 @@ const char* gqa_status_string(gqa_status status) {
              "(use a shorter chunk or gqa_prefill_attn)";
     case GQA_ERR_PAGE_TABLE:
       return "a block-table entry was outside [0, num_pages); that page was read as zeros";
+    case GQA_ERR_BOUNDS:
+      return "bounds-checked build: an output, LSE or partial-row index fell outside its buffer "
+             "(the access was skipped)";
   }
   return "unknown status";
 }

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 7
+#define GQA_PREFILL_ABI_VERSION 8
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -57,8 +57,11 @@ typedef enum gqa_status {
   GQA_ERR_DEVICE_TIMEOUT = 6, /* a device-side wait ran out of time (see _poll)        */
   GQA_ERR_SCRATCH = 7,        /* gqa_prefill_attn_noalloc: the call's split partials do
                                  not fit the library's static scratch array            */
-  GQA_ERR_PAGE_TABLE = 8      /* device-side (see _poll): a paged call met a block-table
+  GQA_ERR_PAGE_TABLE = 8,     /* device-side (see _poll): a paged call met a block-table
                                  entry outside [0, num_pages); that page read as zeros */
+  GQA_ERR_BOUNDS = 9          /* device-side, bounds-checked build only (libgqa_prefill_checked.so,
+                                 see _poll): an output, LSE or split-partial index fell outside
+                                 its buffer; the access was skipped                     */
 } gqa_status;
 
 /*

@@ -36,8 +36,21 @@ def test_every_declared_symbol_is_exported(gqa):
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
 
+def test_bounds_checked_build_exports_the_same_abi(gqa):
+    """build() also makes libgqa_prefill_checked.so (every epilogue store and merge
+    access bounds-checked): same symbols, same ABI version, same status strings."""
+    path = os.path.join(ROOT, "gqa_chunked_prefill_gb300", "libgqa_prefill_checked.so")
+    lib = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} not exported by the bounds-checked build"
+    lib.gqa_prefill_abi_version.restype = ctypes.c_int
+    assert lib.gqa_prefill_abi_version() == gqa.gqa_prefill_abi_version()
+    lib.gqa_status_string.restype = ctypes.c_char_p
+    assert b"bounds" in lib.gqa_status_string(int(gqa.GqaStatus.ERR_BOUNDS))
+
+
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 7
+    assert gqa.gqa_prefill_abi_version() == 8
 
 
 def test_refusals_before_any_cuda_call(gqa):
