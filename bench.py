@@ -452,12 +452,45 @@ def main():
         if gqa.gqa_prefill_poll(stream) != 0:
             raise RuntimeError("device-side error during the FP8 steps")
         f_ms = max_over_ranks(f_ms, pg, dev)
-        qq_ms, _ = timed(lambda: quant_q(), 20)
-        qk_ms, _ = timed(lambda: quant_k(), 20)
+        # The quantisers are HBM-bound: timed on rotating copies of Q and K (each set of
+        # copies over 4x L2, so every call reads cold input) with no flush, whose dirty
+        # lines would share HBM with them.
+        def rotating_us(make_call, nbytes):
+            n_rot = max(2, min(D_ROTATE, -(-4 * L2_BYTES // nbytes) + 1))
+            calls = [make_call(r) for r in range(n_rot)]
+            for c in calls:
+                c()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(40)]
+            torch.cuda.synchronize(dev)
+            for i, (a, b) in enumerate(ev):
+                a.record(stream)
+                calls[i % n_rot]()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            return sum(a.elapsed_time(b) for a, b in ev) / len(ev), n_rot
+
+        def q_copy_call(r):
+            src = q if r == 0 else q.clone()
+            return lambda: gqa.gqa_quantize_q_fp8(src, q8, qs, w.q_len, w.n_q_heads, w.head_dim,
+                                                  stream=stream)
+
+        def k_copy_call(r):
+            src = k if r == 0 else k.clone()
+            return lambda: gqa.gqa_quantize_k_fp8(src, k8, ks, w.kv_len, w.n_kv_heads,
+                                                  w.head_dim, stride, stream=stream)
+
+        qq_ms, q_rot = rotating_us(q_copy_call, q.numel() * 2)
+        qk_ms, k_rot = rotating_us(k_copy_call, k.numel() * 2)
+        q_bytes = q.numel() * 3 + w.q_len * w.n_q_heads * 4   # BF16 in, E4M3 codes + scales out
+        k_bytes = k.numel() * 3 + w.kv_len * w.n_kv_heads * 4
         fp8 = {"steps": f_steps, "value": round(job_throughput(world, flops, f_ms), 2),
                "unit": UNIT, "ms_per_step": round(f_ms, 4), "kernel_ms": round(f_fwd, 4),
                "kernels_per_call": fplan["kernels_per_call"],
                "quantize_q_us": round(qq_ms * 1e3, 1), "quantize_k_us": round(qk_ms * 1e3, 1),
+               "quantize_gbs": {"q": round(q_bytes / (qq_ms * 1e-3) / 1e9, 1),
+                                "k": round(k_bytes / (qk_ms * 1e-3) / 1e9, 1),
+                                "note": f"rotating {q_rot} Q / {k_rot} K copies, no flush"},
                "note": "QK^T on E4M3 codes (kind::f8f6f4), scales restored before the softmax; "
                        "PV in BF16. Step = the attention call; Q/K quantisation timed apart."}
         del q8, k8

@@ -78,6 +78,49 @@ def test_quantize_kernels_match_oracle_bit_for_bit(cuda_device, q_len, kv_len):
     assert np.array_equal(ks[:, :kv_len].cpu().numpy(), ksc.T)
 
 
+def _e4m3_boundary_vectors(rows, heads, seed):
+    """Vectors whose quotients x / s sit on or next to E4M3 rounding boundaries: each
+    holds 448 (so amax = 448 and s = 1 exactly: x / s = x) and otherwise values at the
+    midpoints between neighbouring E4M3 numbers (ties, rounded to even), one BF16 step
+    either side of them, the boundary of E4M3's subnormal range and the halfway point
+    below its least code; then the same vectors scaled by 2^k and by 3 (s no longer a
+    power of two: quotients land next to the boundaries instead of on them)."""
+    g = torch.Generator().manual_seed(seed)
+    vals = []
+    for e in range(-6, 9):                      # normal E4M3: midpoints (1 + (2m+1)/16) 2^e
+        for m in range(8):
+            vals.append((1 + (2 * m + 1) / 16) * 2.0 ** e)
+    for m in range(8):                          # subnormal E4M3: midpoints (2m+1) 2^-10
+        vals.append((2 * m + 1) * 2.0 ** -10)
+    vals += [2.0 ** -6, 2.0 ** -10, 2.0 ** -11, 448.0, 464.0]
+    base = torch.tensor(vals, dtype=torch.float32)
+    near = torch.cat([base, torch.nextafter(base.bfloat16().float(), torch.tensor(0.0)),
+                      torch.nextafter(base.bfloat16().float(), torch.tensor(1e9))])
+    x = torch.empty(rows, heads, 256)
+    for r in range(rows):
+        for h in range(heads):
+            idx = torch.randint(0, near.numel(), (255,), generator=g)
+            sign = torch.where(torch.rand(255, generator=g) < 0.5, -1.0, 1.0)
+            x[r, h, 0] = 448.0
+            x[r, h, 1:] = near[idx] * sign
+    scaled = [x, x * 2.0 ** -5, x * 2.0 ** 7, x * 3.0, x / 3.0]
+    return torch.cat(scaled).clamp(-3e38, 3e38).to(torch.bfloat16)
+
+
+def test_quantize_codes_at_e4m3_rounding_boundaries(cuda_device):
+    """The kernels take x / s through a reciprocal and fall back to the division near
+    E4M3 rounding boundaries: on inputs built around those boundaries the codes and
+    scales must still equal the oracle's (IEEE divisions) bit for bit."""
+    q = _e4m3_boundary_vectors(8, 24, seed=91)
+    k = _e4m3_boundary_vectors(8, 4, seed=92)
+    q8, qs, k8, ks, _ = quantize_gpu(q, k)
+    qc, qsc = oracle.quantize_e4m3(q)
+    kc, ksc = oracle.quantize_e4m3(k)
+    assert np.array_equal(q8.cpu().numpy(), qc) and np.array_equal(qs.cpu().numpy(), qsc)
+    assert np.array_equal(k8.cpu().numpy(), kc)
+    assert np.array_equal(ks[:, :k.shape[0]].cpu().numpy(), ksc.T)
+
+
 @pytest.mark.parametrize("q_len,kv_len", [(1, 1), (5, 300), (43, 300), (100, 100), (129, 1000),
                                           (22, 2000)])
 @pytest.mark.parametrize("variant", [1, 2])
