@@ -36,10 +36,13 @@
 //    rounds; the items of the last, partial round are split along KV into
 //    equal pieces so that they spread over all CTAs (gqa_schedule.h). Each
 //    piece writes a normalised FP32 partial plus its base-2 LSE, and
-//    merge_tail_kernel combines them.
+//    merge_tail_kernel (a warp per row) or, for items of 16 pieces or more,
+//    merge_wide_kernel (a block per row) combines them.
 //  * Every mbarrier wait is bounded: on time-out the kernel records
 //    GQA_ERR_DEVICE_TIMEOUT, waits for its own TMA copies in flight, frees its
 //    tensor memory and returns.
+
+#include <algorithm>
 
 #include "gqa_internal.h"
 #include "gqa_paged.h"
@@ -982,6 +985,92 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const __grid_constant__
     p.lse[orow] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;
 }
 
+// The same merge for calls whose items have many pieces (decode-sized chunks cut
+// into 16 or more KV pieces, on the uniform or the balanced tail): one block per row, its 8 warps taking the
+// pieces s = w, w + 8, ... (so each warp's loads are few and all in flight), their
+// weighted partial sums combined through shared memory in warp order (fixed order:
+// deterministic). Blocks (j, r): tail item j, row r of the item's rows.
+constexpr int kWideWarps = 8;
+constexpr int kWideMergePieces = 16;  // items with this many pieces or more use it
+
+__global__ void __launch_bounds__(kWideWarps * 32)
+    merge_wide_kernel(const __grid_constant__ MergeParams p) {
+  __shared__ float part[kWideWarps][kHeadDim];
+  __shared__ float part_w[kWideWarps];
+  ptx::griddep_wait();
+  const int j = blockIdx.x;
+  const bool balanced = p.tail_splits == 0;
+  int n = p.tail_splits, x_lo = 0;
+  if (balanced) {
+    balanced_item_pieces(p.tail.v, p.tail_items, p.workers, j, x_lo, n);
+    if (n < 2) return;
+  }
+  int seq, qt, g;
+  item_of(p.batch, p.head_items + j, seq, qt, g);
+  const SeqGeo& sq = p.batch.seq[seq];
+  const int cpi = p.ctas_per_item;
+  const int rr = blockIdx.y;
+  if (rr >= cpi * kTokPerTile * kGroup) return;
+  const int r = rr / (kTokPerTile * kGroup);
+  const int row = rr % (kTokPerTile * kGroup);
+  const int tok = kTokPerTile * (cpi * qt + r) + row / kGroup;
+  if (tok >= sq.q_len) return;  // the whole block leaves together
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto prow = [&](int s) {
+    const int slot = balanced ? balanced_slot(p.tail.v, p.tail_items, p.workers, j, x_lo, s)
+                              : j * n + s;
+    return (static_cast<size_t>(slot) * cpi + r) * kRowsPerTile + row;
+  };
+  if constexpr (kCheckBounds) {
+    bool rows_ok = true;
+    for (int s = threadIdx.x; s < n; s += kWideWarps * 32)
+      rows_ok &= row_ok(static_cast<long long>(prow(s)), p.part_rows, p.status);
+    if (!__syncthreads_and(rows_ok)) return;
+  }
+  // Every warp finds the row's maximum piece LSE itself (n loads across the lanes).
+  float mx = kNegInf;
+  for (int s0 = 0; s0 < n; s0 += 32)
+    if (s0 + lane < n) mx = fmaxf(mx, p.part_lse[prow(s0 + lane)]);
+  mx = warp_max(mx);
+  const float m_use = (mx == kNegInf) ? 0.0f : mx;
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float wsum = 0.0f;
+#pragma unroll 4
+  for (int s = warp; s < n; s += kWideWarps) {
+    const size_t pr = prow(s);
+    const float w = ptx::ex2_approx(p.part_lse[pr] - m_use);
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + pr * kHeadDim + 8 * lane);
+    const float4 a = src[0], c = src[1];
+    wsum += w;
+    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+    acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) part[warp][8 * lane + e] = acc[e];
+  if (lane == 0) part_w[warp] = wsum;
+  __syncthreads();
+  if (warp != 0) return;
+  float tot[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float wtot = 0.0f;
+#pragma unroll
+  for (int q = 0; q < kWideWarps; ++q) {
+    wtot += part_w[q];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tot[e] += part[q][8 * lane + e];
+  }
+  const float inv = wtot > 0.0f ? 1.0f / wtot : 0.0f;
+  uint4 o;
+  o.x = ptx::pack_bf16x2(tot[0] * inv, tot[1] * inv);
+  o.y = ptx::pack_bf16x2(tot[2] * inv, tot[3] * inv);
+  o.z = ptx::pack_bf16x2(tot[4] * inv, tot[5] * inv);
+  o.w = ptx::pack_bf16x2(tot[6] * inv, tot[7] * inv);
+  const size_t orow = static_cast<size_t>(sq.q_start + tok) * kQHeads + kGroup * g + row % kGroup;
+  if (!row_ok(static_cast<long long>(orow), p.out_rows, p.status)) return;
+  *reinterpret_cast<uint4*>(p.out + orow * kHeadDim + 8 * lane) = o;
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[orow] = wtot > 0.0f ? (m_use + __log2f(wtot)) * kLn2 : kNegInf;
+}
+
 }  // namespace
 
 size_t fwd_smem_bytes() { return kSmemAlloc; }
@@ -1058,10 +1147,23 @@ cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, bool
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   if (p.tail_items < 1 || p.tail_splits == 1) return cudaSuccess;
-  const int rows = p.ctas_per_item * kTokPerTile * kGroup;
+  // Merged row rr of an item holds token 21 * (ctas_per_item * qt + rr / 126) + (rr % 126) / 6
+  // = tok_per_item * qt + rr / 6 >= rr / 6, so only rows rr < 6 * (longest chunk) can be live:
+  // a decode-sized call launches 6 to 24 rows per item, not 126 or 252.
+  int max_q = 0;
+  for (int i = 0; i < p.batch.n_seq; ++i) max_q = std::max(max_q, p.batch.seq[i].q_len);
+  const int rows = std::min(p.ctas_per_item * kTokPerTile * kGroup, kGroup * max_q);
+  if (rows < 1) return cudaSuccess;
+  cudaLaunchAttribute attr[2];
+  // Pieces per tail item: S, or for the balanced tail about workers / items + 1.
+  const int pieces = p.tail_splits > 0 ? p.tail_splits : p.workers / p.tail_items + 1;
+  if (pieces >= kWideMergePieces) {  // many pieces per item: a block per row
+    const dim3 grid(static_cast<unsigned>(p.tail_items), static_cast<unsigned>(rows));
+    const cudaLaunchConfig_t cfg = launch_config(grid, dim3(kWideWarps * 32), 0, false, stream, attr);
+    return cudaLaunchKernelEx(&cfg, merge_wide_kernel, p);
+  }
   const dim3 grid(static_cast<unsigned>(p.tail_items),
                   static_cast<unsigned>((rows + kMergeRowsPerBlock - 1) / kMergeRowsPerBlock));
-  cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = launch_config(grid, dim3(256), 0, false, stream, attr);
   return cudaLaunchKernelEx(&cfg, merge_tail_kernel, p);
 }

@@ -62,6 +62,23 @@ def test_split_tail_every_element(cuda_device, q_len, kv_len, splits, grid, vari
                 f"{q_len}x{kv_len} splits {splits} grid {grid}")
 
 
+@pytest.mark.parametrize("q_len,kv_len", [(22, 4096), (129, 2200), (300, 4096)])
+@pytest.mark.parametrize("splits,grid,variant", [(16, 0, 1), (31, 0, 1), (17, 9, 1), (16, 0, 2),
+                                                 (20, 6, 2)])
+def test_many_pieces_every_element(cuda_device, q_len, kv_len, splits, grid, variant):
+    """16 or more KV pieces per item: the merge takes a block per output row, its
+    warps each combining a subset of the pieces (the decode-sized merge)."""
+    q, k, v = make_qkv(q_len, kv_len, seed=23 * q_len + kv_len)
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_grid=grid,
+                             force_variant=variant)
+    # S is capped at the fewest KV tiles of an item (17 for 129x2200)
+    assert plan["tail_items"] > 0 and 16 <= plan["tail_splits"] <= splits
+    assert plan["kernels_per_call"] == 2
+    ref_o, ref_l = oracle.attention(q, k, v, SCALE)
+    check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
+                f"{q_len}x{kv_len} splits {splits} grid {grid}")
+
+
 BALANCED = -1  # force_splits value of the balanced tail (GQA_FORCE_BALANCED_TAIL)
 
 
