@@ -379,7 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&p.tmap_v_sub);
         ptx::prefetch_tmap(&p.tmap_v16);
       }
-      const uint64_t pol_kv = ptx::policy_evict_last();
+      // K/V tiles stay in L2 for the other items that read them; in decode-sized
+      // calls no other item does, and they go first.
+      const uint64_t pol_kv = p.kv_read_once ? ptx::policy_evict_first() : ptx::policy_evict_last();
       const uint64_t pol_q = ptx::policy_evict_first();
       uint32_t st = 0, phase = 0;
       uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load issued / its phase

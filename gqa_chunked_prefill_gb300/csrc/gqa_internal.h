@@ -45,6 +45,7 @@ struct FwdParams {
   float scale_log2;    // scale * log2(e)
   unsigned long long timeout_ns;
   int withhold_q;      // test only: the producer never loads the first Q tile
+  int kv_read_once;    // no KV tile is read by two items (decode-sized chunks)
   // Paged K/V (kernels instantiated with kPaged only): key j of the sequence is
   // cache row block_table[j / page_size] * page_size + j % page_size (gqa_paged.h).
   CUtensorMap tmap_k_sub;    // 5-D, sub_rows keys x the stage's chunks: pieces of a box

@@ -656,6 +656,11 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
   p.timeout_ns = (opts && opts->wait_timeout_us) ? 1000ull * opts->wait_timeout_us
                                                  : kDefaultTimeoutNs;
   p.withhold_q = (opts && opts->test_withhold_q) ? 1 : 0;
+  // Every chunk within one query tile of an item: each KV tile of a sequence and
+  // group belongs to exactly one item, so no tile is read twice.
+  p.kv_read_once = 1;
+  for (const SeqIn& sq : seqs)
+    if (sq.q_len > p.batch.tok_per_item) p.kv_read_once = 0;
   if (plan.kernels_per_call == 2) {
     // Partial slots: tail_items * S (uniform tail) or two per worker (balanced).
     const size_t slots = plan.tail_splits > 0
