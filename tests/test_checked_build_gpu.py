@@ -7,7 +7,7 @@ access. The GPU parity tests assert the status word is 0 after every call, so
 running them on this build (in a child process that loads it through
 GQA_PREFILL_LIB) checks both the results and that no access left its buffer: dense
 shapes with ragged tails, forced uniform and balanced split tails, decode shapes,
-and paged, batched and FP8 calls."""
+items cut into 16 or more pieces (the block-per-row merge), and paged, batched and FP8 calls."""
 import os
 import subprocess
 import sys
@@ -22,8 +22,8 @@ def test_parity_suite_on_the_bounds_checked_build(cuda_device):
     lib = os.path.join(ROOT, "gqa_chunked_prefill_gb300", "libgqa_prefill_checked.so")
     assert os.path.exists(lib), "build() makes the bounds-checked library"
     env = dict(os.environ, GQA_PREFILL_LIB=lib)
-    sel = ("small_shapes or split_tail or balanced or whole_items or decode or paged or varlen "
-           "or fp8")
+    sel = ("small_shapes or split_tail or balanced or whole_items or decode or many_pieces or paged "
+           "or varlen or fp8")
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu", "-k", sel,
                         "-p", "no:cacheprovider",
                         "tests/test_parity_gpu.py", "tests/test_paged_gpu.py",
