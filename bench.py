@@ -190,6 +190,26 @@ def oracle_sample(w, q, k, v, target_s: float, seed: int = 17):
 
 
 # ----------------------------------------------------------------------------- ranks
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the architecture)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def max_over_ranks(value: float, dist=None, device=None) -> float:
     """MAX of a per-rank number over all ranks (identity when not distributed)."""
     if dist is None:
@@ -702,7 +722,7 @@ def main():
     if not args.no_cpu_baseline:
         tf, cores, desc, _, _ = oracle_sample(w, q_cpu, k_cpu, v_cpu, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(tf, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": desc}
+                                "cpu_model": cpu_model(), "sample": desc}
     print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
@@ -749,7 +769,7 @@ def run_reference(args, w, flops, world, rank):
                    "effective_gflop_per_step": round(flops / 1e9, 2),
                    "note": "ms_per_step extrapolates the sampled rate to the whole workload"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": desc},
+                         "cpu_model": cpu_model(), "sample": desc},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

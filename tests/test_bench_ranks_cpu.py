@@ -47,3 +47,9 @@ def test_single_rank_identity():
     import bench
     assert bench.max_over_ranks(2.5) == 2.5
     assert abs(bench.job_throughput(1, 2 * 10 ** 12, 4.0) - 500.0) < 1e-9
+
+
+def test_cpu_model_is_named():
+    import bench
+    name = bench.cpu_model()
+    assert isinstance(name, str) and name.strip()
