@@ -308,3 +308,14 @@ def test_batched_key_quantisation_refusals(gqa):
     assert f([0, 5], 8, ks=20) == S.ERR_ALIGN
     assert f([0, 5], 8, k=None) == S.ERR_NULL
     assert f([0, 0, 0], 0, k=None, ks=None) == S.OK
+
+
+@pytest.mark.parametrize("q_len,kv_len,splits", [(1, 32768, 32), (4, 32768, 32), (2, 16384, 32),
+                                                 (1, 131072, 32), (1, 4096, 16)])
+def test_decode_plans_keep_the_measured_split_counts(gqa, q_len, kv_len, splits):
+    """Decode-sized chunks: one CTA per 21-token item, each item's KV range cut into the
+    split count that measured fastest on GB300 in sweeps of forced counts (16 to 38 and the
+    balanced tail), one CTA per piece."""
+    _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152)
+    assert p["variant"] == 1 and p["head_rounds"] == 0 and p["tail_items"] == 4
+    assert p["tail_splits"] == splits and p["grid"] == 4 * splits and p["kernels_per_call"] == 2
