@@ -319,3 +319,15 @@ def test_decode_plans_keep_the_measured_split_counts(gqa, q_len, kv_len, splits)
     _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152)
     assert p["variant"] == 1 and p["head_rounds"] == 0 and p["tail_items"] == 4
     assert p["tail_splits"] == splits and p["grid"] == 4 * splits and p["kernels_per_call"] == 2
+
+
+@pytest.mark.parametrize("q_len,kv_len,plan", [
+    (128, 256, (2, 0, 16, 1, 32)), (512, 4096, (2, 0, 52, 1, 104)),
+    (4096, 8192, (2, 5, 12, 5, 152)), (4096, 16384, (2, 5, 12, 3, 152)),
+    (3072, 16384, (2, 0, 296, 1, 152)), (512, 32768, (1, 0, 100, 3, 152)),
+    (4096, 32768, (2, 5, 12, 5, 152))])
+def test_workload_plans_are_the_measured_ones(gqa, q_len, kv_len, plan):
+    """The seven workloads' plans (variant, whole rounds, tail items, splits, grid) on 152
+    SMs: the ones the measured figures were taken with."""
+    _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152)
+    assert (p["variant"], p["head_rounds"], p["tail_items"], p["tail_splits"], p["grid"]) == plan
