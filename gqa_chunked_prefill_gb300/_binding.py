@@ -98,7 +98,7 @@ lib.gqa_prefill_attn_paged_varlen.restype = _i
 lib.gqa_prefill_attn_paged_varlen_ex.argtypes = _PVARLEN_ARGS + [ctypes.POINTER(PrefillOpts),
                                                                  ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_attn_paged_varlen_ex.restype = _i
-lib.gqa_prefill_make_plan_varlen.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
+lib.gqa_prefill_make_plan_varlen.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                              ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan_varlen.restype = _i
 lib.gqa_quantize_k_fp8_varlen.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
@@ -112,9 +112,11 @@ lib.gqa_prefill_attn_paged_fp8qk_varlen_ex.argtypes = [
     _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _vp,
     ctypes.POINTER(PrefillOpts), ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_attn_paged_fp8qk_varlen_ex.restype = _i
-lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
+lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                       ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan.restype = _i
+lib.gqa_prefill_device_info.argtypes = [ctypes.POINTER(_i), ctypes.POINTER(_i)]
+lib.gqa_prefill_device_info.restype = _i
 lib.gqa_prefill_poll.argtypes = [_vp, ctypes.POINTER(_i)]
 lib.gqa_prefill_poll.restype = _i
 lib.gqa_status_string.argtypes = [_i]
@@ -413,13 +415,13 @@ def gqa_prefill_attn_paged_fp8qk_varlen_ex(q_fp8, q_scale, k_cache_fp8, k_scale,
 
 
 def gqa_prefill_make_plan_varlen(cu_seqlens_q, cu_seqlens_k, n_q_heads, n_kv_heads, head_dim,
-                                 num_sms, force_splits=0, force_grid=0, force_variant=0,
-                                 check=True):
+                                 num_sms, max_pairs=-1, force_splits=0, force_grid=0,
+                                 force_variant=0, check=True):
     cq, pq = _host_i32(cu_seqlens_q)
     ck, pk = _host_i32(cu_seqlens_k)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_make_plan_varlen(pq, pk, len(cu_seqlens_q) - 1, n_q_heads, n_kv_heads,
-                                          head_dim, num_sms, force_splits, force_grid,
+                                          head_dim, num_sms, max_pairs, force_splits, force_grid,
                                           force_variant, ctypes.byref(plan))
     if check:
         _check(rc)
@@ -427,13 +429,24 @@ def gqa_prefill_make_plan_varlen(cu_seqlens_q, cu_seqlens_k, n_q_heads, n_kv_hea
 
 
 def gqa_prefill_make_plan(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, num_sms,
-                          force_splits=0, force_grid=0, force_variant=0, check=True):
+                          max_pairs=-1, force_splits=0, force_grid=0, force_variant=0,
+                          check=True):
+    """max_pairs < 0: num_sms / 2 co-resident CTA pairs (gqa_prefill_device_info gives
+    the current device's number)."""
     plan = PrefillPlan()
     rc = lib.gqa_prefill_make_plan(q_len, kv_len, n_q_heads, n_kv_heads, head_dim, num_sms,
-                                   force_splits, force_grid, force_variant, ctypes.byref(plan))
+                                   max_pairs, force_splits, force_grid, force_variant,
+                                   ctypes.byref(plan))
     if check:
         _check(rc)
     return rc, plan.as_dict()
+
+
+def gqa_prefill_device_info():
+    """(num_sms, max_pairs) the planner uses on the current device."""
+    sms, pairs = _i(0), _i(0)
+    _check(lib.gqa_prefill_device_info(ctypes.byref(sms), ctypes.byref(pairs)))
+    return sms.value, pairs.value
 
 
 def gqa_prefill_poll(stream=None) -> int:

@@ -762,23 +762,24 @@ gqa_status run_one(const CallIO& io, int q_len, int kv_len, int n_q_heads, int n
 constexpr size_t kNoAllocScratchBytes = GQA_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-struct NoAllocDeviceState {
-  std::once_flag once;
-  gqa_status status = GQA_OK;
-  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
-};
-NoAllocDeviceState g_noalloc_dev[kMaxDevices];
+// The lookup is retried until it succeeds: a failed first attempt (say, one made
+// while the stream was being captured) does not disable the entry point.
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};  // device address of g_noalloc_scratch per device
 
 gqa_status noalloc_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
-  NoAllocDeviceState& s = g_noalloc_dev[dev];
-  std::call_once(s.once, [&s] {
-    if (cudaGetSymbolAddress(&s.scratch, g_noalloc_scratch) != cudaSuccess || s.scratch == nullptr)
-      s.status = GQA_ERR_CUDA;
-  });
-  if (s.status != GQA_OK) return s.status;
-  *out = s.scratch;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || a == nullptr) {
+      cudaGetLastError();  // do not leave the failure for the caller's next CUDA call
+      return GQA_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = a;
+  }
+  *out = g_noalloc_addr[dev];
   return GQA_OK;
 }
 
@@ -1051,19 +1052,29 @@ gqa_status gqa_prefill_attn_paged_fp8qk_varlen_ex(
 }
 
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int num_sms, int force_splits, int force_grid, int force_variant,
-                                 gqa_prefill_plan* plan) {
+                                 int num_sms, int max_pairs, int force_splits, int force_grid,
+                                 int force_variant, gqa_prefill_plan* plan) {
   if (!plan) return GQA_ERR_NULL;
   const int32_t cu_q[2] = {0, q_len}, cu_k[2] = {0, kv_len};
   if (q_len < 0 || kv_len < q_len) return GQA_ERR_SHAPE;
   return gqa_prefill_make_plan_varlen(cu_q, cu_k, 1, n_q_heads, n_kv_heads, head_dim, num_sms,
-                                      force_splits, force_grid, force_variant, plan);
+                                      max_pairs, force_splits, force_grid, force_variant, plan);
+}
+
+gqa_status gqa_prefill_device_info(int* num_sms, int* max_pairs) {
+  gqa::DeviceInfo* dev = nullptr;
+  const gqa_status st = gqa::device_info(&dev);
+  if (st != GQA_OK) return st;
+  if (num_sms) *num_sms = dev->num_sms;
+  if (max_pairs) *max_pairs = dev->max_pairs;
+  return GQA_OK;
 }
 
 gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                                         int batch, int n_q_heads, int n_kv_heads, int head_dim,
-                                        int num_sms, int force_splits, int force_grid,
-                                        int force_variant, gqa_prefill_plan* plan) {
+                                        int num_sms, int max_pairs, int force_splits,
+                                        int force_grid, int force_variant,
+                                        gqa_prefill_plan* plan) {
   if (!plan) return GQA_ERR_NULL;
   std::memset(plan, 0, sizeof(*plan));
   std::vector<gqa::SeqIn> seqs;
@@ -1077,7 +1088,9 @@ gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32
     return st;
   if (num_sms <= 0) return GQA_ERR_SHAPE;
   if (total_q == 0) return GQA_OK;
-  gqa::cached_plan(seqs, num_sms, num_sms / 2, force_splits, force_grid, force_variant, plan);
+  // The attention calls plan with min(occupancy pairs, num_sms / 2) (device_info).
+  const int pairs = max_pairs < 0 ? num_sms / 2 : std::min(max_pairs, num_sms / 2);
+  gqa::cached_plan(seqs, num_sms, pairs, force_splits, force_grid, force_variant, plan);
   return GQA_OK;
 }
 

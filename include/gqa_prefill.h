@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 8
+#define GQA_PREFILL_ABI_VERSION 9
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -149,13 +149,27 @@ gqa_status gqa_prefill_attn_ex(const void* q, const void* k, const void* v, void
 
 /*
  * Host-only planning (no CUDA call): fills *plan for a device with `num_sms`
- * SMs exactly as gqa_prefill_attn_ex would with the same force_* options
- * (0 = planner decides), assuming num_sms/2 CTA pairs can be resident.
- * Validates shapes like the attention call (pointers are not involved).
+ * SMs of which `max_pairs` CTA pairs of the pair kernel can be resident at
+ * once, exactly as gqa_prefill_attn_ex would with the same force_* options
+ * (0 = planner decides). max_pairs < 0 assumes num_sms / 2; larger values are
+ * capped there; 0 plans without the pair kernel. gqa_prefill_device_info gives
+ * both numbers for the current device, so a plan made from them is the plan
+ * the attention call runs there. Validates shapes like the attention call
+ * (pointers are not involved).
  */
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,
-                                 int num_sms, int force_splits, int force_grid,
+                                 int num_sms, int max_pairs, int force_splits, int force_grid,
                                  int force_variant, gqa_prefill_plan* plan);
+
+/*
+ * The planner's inputs on the CURRENT device, as the attention calls use them:
+ * its SM count and the number of CTA pairs of the pair kernel that can be
+ * resident at once (cudaOccupancyMaxActiveClusters, at most num_sms / 2; 0 if
+ * the pair kernel cannot run). Does the library's one-time per-device set-up on
+ * first use (make that first call outside any stream capture). Either pointer
+ * may be NULL. GQA_ERR_UNSUPPORTED on a device that is not sm_103.
+ */
+gqa_status gqa_prefill_device_info(int* num_sms, int* max_pairs);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status
@@ -292,8 +306,8 @@ gqa_status gqa_prefill_attn_paged_varlen_ex(const void* q, const void* k_cache,
 /* Host-only planning of a dense batched call (as gqa_prefill_make_plan). */
 gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
                                         int batch, int n_q_heads, int n_kv_heads, int head_dim,
-                                        int num_sms, int force_splits, int force_grid,
-                                        int force_variant, gqa_prefill_plan* plan);
+                                        int num_sms, int max_pairs, int force_splits,
+                                        int force_grid, int force_variant, gqa_prefill_plan* plan);
 
 /*
  * Quantised QK^T (gfx936 DCU上实现INT8 QK MMAC：分页访存、Fragment映射与GQA适配, §1

@@ -51,3 +51,47 @@ def gather_rows(out: torch.Tensor, lse, rows):
     o = out.reshape(-1, d).index_select(0, r).double().cpu().numpy()
     l = lse.reshape(-1).index_select(0, r).double().cpu().numpy() if lse is not None else None
     return o, l
+
+
+TOK_PER_TILE = 21  # tokens of one 128-row MMA tile (21 tokens x 6 heads)
+GROUP = 6          # query heads per KV head
+
+
+def item_cover_rows(q_len: int, n_q_heads: int = 24, extra=None) -> np.ndarray:
+    """Row ids t*Hq + h that touch every work item of a call, whatever its kernel variant.
+
+    A work item is one query tile (21 tokens, or 42 for a CTA pair = two 21-token
+    tiles) of one KV group (6 query heads). For every 21-token tile i and group g
+    this takes the tile's first token and its last token (the last sees every KV
+    tile of the item, so it depends on every KV piece of a split item), with the
+    head inside the group rotating with i so all six heads of a group appear.
+    ``extra`` (row ids) is merged in. Returns sorted unique int64 row ids."""
+    rows = []
+    n_tiles = -(-q_len // TOK_PER_TILE)
+    for i in range(n_tiles):
+        first = TOK_PER_TILE * i
+        last = min(first + TOK_PER_TILE - 1, q_len - 1)
+        for g in range(n_q_heads // GROUP):
+            rows.append(first * n_q_heads + GROUP * g + i % GROUP)
+            rows.append(last * n_q_heads + GROUP * g + (i + 3) % GROUP)
+    if extra is not None:
+        rows.extend(int(r) for r in np.asarray(extra).reshape(-1))
+    return np.unique(np.asarray(rows, dtype=np.int64))
+
+
+def unchecked_items(rows, q_len: int, tok_per_item: int, n_q_heads: int = 24):
+    """Items (query tile of tok_per_item tokens, KV group) that the sampled rows do
+    not check: no row at all, or no row of the item's last token (the one row
+    that every KV piece of a split item contributes to). Returns a list of
+    (tile, group); empty means every item and every piece is compared."""
+    rows = np.asarray(rows, dtype=np.int64)
+    tok, head = rows // n_q_heads, rows % n_q_heads
+    n_tiles = -(-q_len // tok_per_item)
+    seen = np.zeros((n_tiles, n_q_heads // GROUP), bool)
+    seen_last = np.zeros_like(seen)
+    seen[tok // tok_per_item, head // GROUP] = True
+    last_tok = np.minimum((tok // tok_per_item + 1) * tok_per_item, q_len) - 1
+    is_last = tok == last_tok
+    seen_last[tok[is_last] // tok_per_item, head[is_last] // GROUP] = True
+    bad = np.argwhere(~(seen & seen_last))
+    return [tuple(int(x) for x in b) for b in bad]

@@ -50,7 +50,7 @@ def test_bounds_checked_build_exports_the_same_abi(gqa):
 
 
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 8
+    assert gqa.gqa_prefill_abi_version() == 9
 
 
 def test_refusals_before_any_cuda_call(gqa):
@@ -331,3 +331,18 @@ def test_workload_plans_are_the_measured_ones(gqa, q_len, kv_len, plan):
     SMs: the ones the measured figures were taken with."""
     _, p = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152)
     assert (p["variant"], p["head_rounds"], p["tail_items"], p["tail_splits"], p["grid"]) == plan
+
+
+def test_make_plan_respects_the_resident_pair_count(gqa):
+    """max_pairs caps the CTA-pair grid; 0 plans without the pair kernel; a negative
+    value assumes num_sms / 2 (the same plan as passing num_sms / 2)."""
+    for q_len, kv_len in ((4096, 32768), (512, 4096), (3072, 16384), (1, 32768)):
+        _, p_none = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, max_pairs=0)
+        assert p_none["variant"] == 1
+        _, p_few = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, max_pairs=10,
+                                             force_variant=2)
+        assert p_few["variant"] == 2 and p_few["grid"] <= 20
+        _, p_def = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152)
+        _, p_half = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, max_pairs=76)
+        _, p_big = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, 152, max_pairs=1000)
+        assert p_def == p_half == p_big

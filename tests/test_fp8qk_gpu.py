@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from gqa_inputs import WORKLOADS, make_qkv, make_workload, sample_rows
-from tests.gpu_helpers import check_close, gather_rows
+from tests.gpu_helpers import check_close, gather_rows, item_cover_rows, unchecked_items
 
 pytestmark = pytest.mark.gpu
 SCALE = 1.0 / 16.0
@@ -108,9 +108,11 @@ def _e4m3_boundary_vectors(rows, heads, seed):
 
 
 def test_quantize_codes_at_e4m3_rounding_boundaries(cuda_device):
-    """The kernels take x / s through a reciprocal and fall back to the division near
-    E4M3 rounding boundaries: on inputs built around those boundaries the codes and
-    scales must still equal the oracle's (IEEE divisions) bit for bit."""
+    """The kernels divide each value by its vector's scale with an IEEE
+    round-to-nearest division, then round to E4M3: on inputs built around E4M3
+    rounding boundaries (midpoints between codes, their BF16 neighbours, the
+    subnormal range, saturation) the codes and scales must equal the oracle's bit
+    for bit."""
     q = _e4m3_boundary_vectors(8, 24, seed=91)
     k = _e4m3_boundary_vectors(8, 4, seed=92)
     q8, qs, k8, ks, _ = quantize_gpu(q, k)
@@ -149,8 +151,9 @@ def test_fp8qk_split_tail_every_element(cuda_device, splits, grid, variant):
 def test_fp8qk_workload_full_size(cuda_device, name, variant):
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
-    out, lse, _ = run_fp8(q, k, v, w.scale, force_variant=variant)
-    rows = sample_rows(w.q_len, w.n_q_heads, 1200, seed=12)
+    out, lse, plan = run_fp8(q, k, v, w.scale, force_variant=variant)
+    rows = item_cover_rows(w.q_len, w.n_q_heads, sample_rows(w.q_len, w.n_q_heads, 1200, seed=12))
+    assert unchecked_items(rows, w.q_len, 21 * plan["variant"]) == []
     ref_o, ref_l = oracle_fp8(q, k, v, w.scale, rows=rows)
     got_o, got_l = gather_rows(out, lse, rows)
     check_close(got_o, got_l, ref_o, ref_l, f"fp8 {name}")

@@ -14,7 +14,7 @@ import torch
 import oracle
 from gqa_inputs import (SERVING_PAGE_SIZE, WORKLOADS, make_paged_cache, make_qkv, make_workload,
                         sample_rows)
-from tests.gpu_helpers import check_close, gather_rows, run_gpu
+from tests.gpu_helpers import check_close, gather_rows, item_cover_rows, run_gpu, unchecked_items
 
 pytestmark = pytest.mark.gpu
 SCALE = 1.0 / 16.0
@@ -93,8 +93,9 @@ def test_one_page_longer_than_the_sequence(cuda_device):
 def test_paged_workload_full_size(cuda_device, name, page_size):
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
-    rows = sample_rows(w.q_len, w.n_q_heads, 1200, seed=8)
-    check_paged(q, k, v, page_size, seed=w.seed, what=f"{name} page {page_size}", rows=rows)
+    rows = item_cover_rows(w.q_len, w.n_q_heads, sample_rows(w.q_len, w.n_q_heads, 1200, seed=8))
+    plan = check_paged(q, k, v, page_size, seed=w.seed, what=f"{name} page {page_size}", rows=rows)
+    assert unchecked_items(rows, w.q_len, 21 * plan["variant"]) == []
 
 
 @pytest.mark.parametrize("bad", ["past_end", "negative"])

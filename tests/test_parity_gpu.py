@@ -5,8 +5,10 @@ query tiles and 128-key KV tiles with ragged tails (q_len not a multiple of 21,
 kv_len not a multiple of 128), tiles straddling the causal diagonal, and the
 single-token/single-key degenerate cases. The seven workload shapes run at full
 size in the same launch configuration as the benchmark and are compared on a
-fixed stratified sample of rows (first, last and middle tokens, every head,
-seeded random rows).
+row sample that checks every work item: the first and last token of every
+21-token query tile in every KV group (the last token depends on every KV piece
+of a split item), plus a stratified random sample; an assertion counts the items
+(one-CTA and CTA-pair tiling) the sample leaves unchecked and requires none.
 """
 import numpy as np
 import pytest
@@ -14,7 +16,7 @@ import torch
 
 import oracle
 from gqa_inputs import WORKLOADS, make_qkv, make_workload, sample_rows
-from tests.gpu_helpers import check_close, gather_rows, run_gpu
+from tests.gpu_helpers import check_close, gather_rows, item_cover_rows, run_gpu, unchecked_items
 
 pytestmark = pytest.mark.gpu
 SCALE = 1.0 / 16.0
@@ -115,11 +117,16 @@ def test_whole_items_on_few_ctas(cuda_device, q_len, kv_len, grid, variant):
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
 @pytest.mark.parametrize("variant,splits", [(0, 0), (1, 0), (2, 0), (2, -1)])
-def test_workload_full_size_sampled_rows(cuda_device, name, variant, splits):
+def test_workload_full_size_every_item(cuda_device, name, variant, splits):
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
     out, lse, plan = run_gpu(q, k, v, w.scale, force_variant=variant, force_splits=splits)
-    rows = sample_rows(w.q_len, w.n_q_heads, 1200 if w.q_len * w.kv_len > 4e6 else 4000, seed=5)
+    rows = item_cover_rows(w.q_len, w.n_q_heads,
+                           sample_rows(w.q_len, w.n_q_heads,
+                                       1200 if w.q_len * w.kv_len > 4e6 else 4000, seed=5))
+    tpi = 21 * plan["variant"]
+    assert unchecked_items(rows, w.q_len, tpi) == [], "items without a compared row"
+    assert plan["n_items"] == 4 * -(-w.q_len // tpi)
     ref_o, ref_l = oracle.attention(q, k, v, w.scale, rows=rows)
     got_o, got_l = gather_rows(out, lse, rows)
     check_close(got_o, got_l, ref_o, ref_l, name)
