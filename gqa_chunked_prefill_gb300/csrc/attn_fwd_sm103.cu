@@ -85,6 +85,9 @@ enum BarId : uint32_t {
   kBarPvDone1,
   kBarOFree,                    // epilogue finished reading O (128 arrivals)
   kBarDrain,                    // MMA warp's final drain
+  kBarMerge0,                   // [2] fused split merge: partial rows staged (bulk-copy tx)
+  kBarMerge1,
+  kBarPartDone,                 // fused split merge: this CTA's partial rows stored (128 arrivals)
   kBarScFull,                   // [kScSlots] FP8 QK^T: key scales of a tile loaded (TMA tx)
   kBarScEmpty = kBarScFull + 8, // [kScSlots] this CTA's softmax done with them (128 arrivals)
   kNumBars = kBarScEmpty + 8
@@ -95,7 +98,16 @@ constexpr int kScSlots = 8;
 constexpr uint32_t kScSlotBytes = 128 * 4;
 constexpr uint32_t kOffScales = kOffQ + 2 * kQChunkBytes;
 constexpr uint32_t kOffTmemSlot = kOffBars + kNumBars * 8;
-constexpr uint32_t kSmemUsed = kOffTmemSlot + 16;
+constexpr uint32_t kOffAbort = kOffTmemSlot + 4;       // a role gave up (time-out): no merges
+constexpr uint32_t kOffMergeBits = kOffTmemSlot + 16;  // split pieces this CTA completed last
+constexpr uint32_t kSmemUsed = kOffMergeBits + kMaxFusedSplitPieces / 8;
+// Fused split merge, run after the CTA's last piece when the Q region and the
+// stage ring are free: two staging buffers of partial rows, every piece's
+// weight for every row, and the rows' inverse weight sums.
+constexpr uint32_t kMergeBufBytes = 96 * 1024;
+constexpr uint32_t kOffMergeWts = 2 * kMergeBufBytes;            // float [48 pieces][126 rows]
+constexpr uint32_t kOffMergeInv = kOffMergeWts + 48 * 128 * 4;   // float [128]
+static_assert(kOffMergeInv + 128 * 4 <= kOffBars, "merge staging overlaps the barriers");
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base up to 1024
 
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false, false);
@@ -140,28 +152,50 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Fw
   }
 }
 
-// Paged K/V: the V rows of the tile holding key kv_len-1 that lie past kv_len
-// come from the cache's last page and may hold anything. Their P is exactly 0,
-// but 0 * NaN is not, so they are zeroed before the PV reads the stage. The
-// producer loads that tile's V in 16-key pieces and pieces that start past
-// kv_len read TMA zero fill, so only keys [kv_len, next multiple of 16) remain.
-// `base`: the stage (this CTA's shared::cta address, or the peer's
-// shared::cluster address when `remote`), holding keys key0 .. key0+rows-1 of
-// the tile (kr: its first key past kv_len) in the paged stage layout: key r, chunk c at
-// (r / 8) * 1024 * nch + c * 1024 + (r % 8) * 128 (a 128-byte row stays in
-// place under the 128-byte swizzle). Out of line (rare: once per item that
-// reaches the last KV tile) so the MMA thread's loop stays small.
-__device__ __noinline__ void zero_v_tail(uint32_t base, int nch, int key0, int rows, int kr,
-                                         bool remote) {
+// The V rows of the tile holding key kv_len-1 that lie past kv_len may hold
+// anything: in a paged cache, the last page's unused slots; in a dense batch, the
+// next sequence's values. Their P is exactly 0, but 0 * NaN is not, so they are
+// zeroed before the PV reads the stage. The producer loads that tile's V in
+// 16-key pieces and pieces that start past kv_len read TMA zero fill, so only
+// keys [kv_len, next multiple of 16) remain. `base`: the stage (this CTA's
+// shared::cta address, or the peer's shared::cluster address when `remote`),
+// holding keys key0 .. key0+rows-1 of the tile (kr: its first key past kv_len);
+// key r, chunk c at (r / 8) * sbo + c * lbo + (r % 8) * 128 (the stage layout's
+// strides; a 128-byte row stays in place under the 128-byte swizzle). Out of
+// line (rare: once per item that reaches the last KV tile) so the MMA thread's
+// loop stays small.
+__device__ __noinline__ void zero_v_tail(uint32_t base, int nch, uint32_t sbo, uint32_t lbo,
+                                         int key0, int rows, int kr, bool remote) {
   const int r_begin = max(kr, key0) - key0;
   const int r_end = min((kr + 15) & ~15, key0 + rows) - key0;
   for (int r = r_begin; r < r_end; ++r)
     for (int c = 0; c < nch; ++c)
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const uint32_t a = base + (r >> 3) * 1024 * nch + c * 1024 + (r & 7) * 128 + u * 16;
+        const uint32_t a = base + (r >> 3) * sbo + c * lbo + (r & 7) * 128 + u * 16;
         if (remote) ptx::st_cluster_zero16(a); else ptx::st_shared_zero16(a);
       }
+}
+
+// Dense batch: the V box of the tile holding key kv_len-1 of a sequence, as
+// 16-key pieces of one 64-column chunk each (4-D map, box (64, 16, 1, 1)):
+// pieces that start past the sequence's kv_len keys read row oob_row, past the
+// tensor (TMA zero fill), so that no value of the next sequence lands in the
+// stage but the < 16 rows zero_v_tail clears. `r0`: first key of the box within
+// the sequence; the stage is chunk-major with `rows` keys per chunk.
+template <bool kPair>
+__device__ __noinline__ void issue_dense_v_pieces(const CUtensorMap* map16, uint32_t dst,
+                                                  uint32_t bar, int kv_start, int kv_len,
+                                                  int oob_row, int r0, int rows, int nch,
+                                                  int chunk0, int g, uint64_t pol) {
+  for (int c = 0; c < nch; ++c)
+    for (int i = 0; i < rows / 16; ++i) {
+      const int key = r0 + 16 * i;
+      const int row = key < kv_len ? kv_start + key : oob_row;
+      const uint32_t d = dst + c * rows * 128 + i * 16 * 128;
+      if constexpr (kPair) ptx::tma_load_4d_pair(d, map16, bar, 0, row, g, chunk0 + c, pol);
+      else ptx::tma_load_4d(d, map16, bar, 0, row, g, chunk0 + c, pol);
+    }
 }
 
 // Paged K/V, the rare case: a box that crosses pages (or the V box of the tile
@@ -257,6 +291,200 @@ __device__ __forceinline__ void transpose8_quads(uint4 (&e)[8], int j) {
   }
 }
 
+// Fused split merge, step 1 (one thread per piece, once the piece's 128 threads
+// have stored their partial rows): set this piece's flag to the call's tag and
+// tell whether every piece of the item has set its own. The release fence
+// publishes the CTA's partial rows before the flag (the other threads' stores
+// are ordered before it by the CTA barrier this thread waited on; the fence is
+// cumulative). Between the flag store and the loads of the other flags sits a
+// sequentially consistent fence, so of any pieces that finish together at least
+// one sees all the flags set; of those, the one that claims the item merges it.
+// A flag left by an earlier call holds 0 (cleared by its merger) or that call's
+// tag. No load waits for another CTA; the piece count is at most 48.
+__device__ __noinline__ bool flag_piece_done(const FwdParams& p, const Schedule& sc, int G, int j,
+                                             int slot, uint32_t rank, int cpi) {
+  unsigned long long* flags = p.merge_flag;
+  const unsigned long long tag = p.call_tag;
+  ptx::fence_acq_rel_gpu();
+  ptx::st_relaxed_gpu_u64(flags + static_cast<size_t>(slot) * cpi + rank, tag);
+  ptx::fence_sc_gpu();
+  int x_lo;
+  const int n = tail_item_pieces(sc, p.tail.v, G, j, x_lo);
+  bool all = true;
+#pragma unroll 8
+  for (int s = 0; s < n; ++s)
+    all &= ptx::ld_relaxed_gpu_u64(flags + static_cast<size_t>(tail_piece_slot(sc, p.tail.v, G, j,
+                                                                               x_lo, s)) * cpi +
+                                   rank) == tag;
+  if (!all) return false;
+  // Pieces that finish together may all see every flag set: they race for the
+  // item's claim word (first piece's flag slot + the flag area's second half),
+  // and only the one whose CAS installs the tag merges. The merger clears it.
+  unsigned long long* claim = flags + p.merge_claim_offset +
+                              static_cast<size_t>(tail_piece_slot(sc, p.tail.v, G, j, x_lo, 0)) *
+                                  cpi + rank;
+  const unsigned long long seen = ptx::ld_relaxed_gpu_u64(claim);
+  if (seen == tag || atomicCAS(claim, seen, tag) != seen) return false;
+  ptx::fence_acq_rel_gpu();  // acquire: the other pieces' rows are visible
+  return true;
+}
+
+// Fused split merge, step 2 (all threads of the CTA, after its last piece): rows
+// of rank `rank` of tail item j, merged from its n pieces' partials in KV order:
+// lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s (fixed order, so the
+// result does not depend on which CTA merges). First every piece's LSE of every
+// live row is loaded at once (n * rows <= 48 * 126 values, spread over the
+// threads) and turned into weights in shared memory; the partial rows then go
+// through two 96 KB staging buffers by bulk copies (one thread copies chunk c+1
+// while all threads reduce chunk c), in one of two shapes: row chunks (all
+// pieces' rows [r0, r0 + rc), for items of many rows: a few large copies) or,
+// when the rows are few (decode-sized chunks) and the pieces many, piece chunks
+// (all rows of pieces [s0, s0 + g), accumulated in registers). `mphase` holds the
+// two staging barriers' parities across calls. Returns false if a wait gave up.
+__device__ __noinline__ bool merge_item(const FwdParams& p, const Schedule& sc, int G, int j,
+                                        uint32_t rank, int cpi, uint8_t* smem, uint32_t sbase,
+                                        uint32_t bar0, uint32_t& mphase) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  int seq, qt, g;
+  item_of(p.batch, sc.head_items + j, seq, qt, g);
+  const SeqGeo& sq = p.batch.seq[seq];
+  const int tok0 = p.batch.tok_per_item * qt + kTokPerTile * static_cast<int>(rank);
+  const int rows = min(kTokPerTile * kGroup, kGroup * (sq.q_len - tok0));
+  if (rows <= 0) return true;
+  int x_lo;
+  const int n = tail_item_pieces(sc, p.tail.v, G, j, x_lo);
+  if (n > kMaxFusedItemPieces) {  // the planner never fuses such items
+    atomicExch(p.status, static_cast<int>(GQA_ERR_BOUNDS));
+    return true;
+  }
+  float* wsm = reinterpret_cast<float*>(smem + kOffMergeWts);  // [n][rows] LSE, then weights
+  float* inv = reinterpret_cast<float*>(smem + kOffMergeInv);  // [rows]
+  auto prow0 = [&](int s) {  // first partial row of piece s for this CTA's rows
+    return (static_cast<size_t>(tail_piece_slot(sc, p.tail.v, G, j, x_lo, s)) * cpi + rank) *
+           kRowsPerTile;
+  };
+  auto out_row = [&](int r) {
+    return static_cast<size_t>(sq.q_start + tok0 + r / kGroup) * kQHeads + kGroup * g + r % kGroup;
+  };
+  // Staging plan: row chunks of rc rows (all n pieces), or piece chunks of gp pieces.
+  const bool by_piece = rows <= 24 && n * rows > 96;
+  const int rc = by_piece ? rows : max(1, min(rows, 96 / n));
+  const int gp = by_piece ? max(1, 96 / rows) : n;
+  const int chunks = by_piece ? (n + gp - 1) / gp : (rows + rc - 1) / rc;
+  auto issue = [&](int c) {  // thread 0: chunk c into buffer c & 1
+    const int b = c & 1;
+    const uint32_t dst = sbase + b * kMergeBufBytes;
+    const int s0 = by_piece ? c * gp : 0, s1 = by_piece ? min(n, s0 + gp) : n;
+    const int r0 = by_piece ? 0 : c * rc, nr = by_piece ? rows : min(rc, rows - r0);
+    ptx::fence_proxy_async_global();  // the pieces' generic-proxy stores, seen via the flags
+    ptx::fence_proxy_async_smem();    // earlier generic reads of this buffer come first
+    const uint64_t pol = ptx::policy_evict_first();
+    uint32_t bytes = 0;
+    for (int s = s0; s < s1; ++s)
+      if (row_ok(static_cast<long long>(prow0(s) + r0 + nr - 1), p.part_rows, p.status))
+        bytes += nr * 1024u;
+    ptx::mbar_arrive_expect_tx(bar0 + 8u * b, bytes);
+    for (int s = s0; s < s1; ++s) {
+      const size_t pr = prow0(s) + r0;
+      if (!kCheckBounds || static_cast<long long>(pr + nr - 1) < p.part_rows)
+        ptx::bulk_load(dst + (s - s0) * nr * 1024u, p.part_o + pr * kHeadDim, nr * 1024u,
+                       bar0 + 8u * b, pol);
+    }
+  };
+  if (tid == 0) issue(0);
+  // Every piece's LSE of every live row (independent loads, a few per thread).
+  for (int i0 = tid; i0 < n * rows; i0 += 4 * nthr) {
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * nthr;
+      v[u] = i < n * rows ? __ldcg(p.part_lse + prow0(i / rows) + i % rows) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i0 + u * nthr < n * rows) wsm[i0 + u * nthr] = v[u];
+  }
+  __syncthreads();
+  if (tid < rows) {  // the row's weights 2^{lse_s - max} (in place), their sum, its LSE
+    float mx = kNegInf;
+    for (int s = 0; s < n; ++s) mx = fmaxf(mx, wsm[s * rows + tid]);
+    const float m_use = (mx == kNegInf) ? 0.0f : mx;
+    float wsum = 0.0f;
+    for (int s = 0; s < n; ++s) {
+      const float w = ptx::ex2_approx(wsm[s * rows + tid] - m_use);
+      wsm[s * rows + tid] = w;
+      wsum += w;
+    }
+    inv[tid] = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+    const size_t orow = out_row(tid);
+    if (p.lse != nullptr && row_ok(static_cast<long long>(orow), p.out_rows, p.status))
+      p.lse[orow] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;
+  }
+  __syncthreads();
+  auto store = [&](int r, int q4, float4 acc) {
+    const float iv = inv[r];
+    const size_t orow = out_row(r);
+    if (row_ok(static_cast<long long>(orow), p.out_rows, p.status)) {
+      uint2 o;
+      o.x = ptx::pack_bf16x2(acc.x * iv, acc.y * iv);
+      o.y = ptx::pack_bf16x2(acc.z * iv, acc.w * iv);
+      *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * q4) = o;
+    }
+  };
+  constexpr int kAccQuads = 8;  // piece chunks: rows <= 24, so rows * 64 quads <= 8 per thread
+  float4 acc[kAccQuads];
+#pragma unroll
+  for (int k = 0; k < kAccQuads; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  bool ok = true;
+  for (int c = 0; c < chunks; ++c) {
+    const int b = c & 1;
+    if (tid == 0 && c + 1 < chunks) issue(c + 1);  // buffer b ^ 1 was freed by chunk c - 1
+    ok = __syncthreads_and(ok && wait_bar(bar0 + 8u * b, (mphase >> b) & 1u, p)) != 0;
+    mphase ^= 1u << b;
+    if (!ok) return false;
+    const uint32_t buf = sbase + b * kMergeBufBytes;
+    if (by_piece) {
+      const int s0 = c * gp, s1 = min(n, s0 + gp);
+#pragma unroll
+      for (int k = 0; k < kAccQuads; ++k) {
+        const int idx = tid + k * nthr;
+        if (idx >= rows * 64) break;
+        const int r = idx >> 6, q4 = idx & 63;
+        for (int s = s0; s < s1; ++s) {
+          const float w = wsm[s * rows + r];
+          const float4 v = ptx::ld_shared_f4(buf + ((s - s0) * rows + r) * 1024u + q4 * 16u);
+          acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
+        }
+      }
+    } else {
+      const int r0 = c * rc, nr = min(rc, rows - r0);
+      for (int idx = tid; idx < nr * 64; idx += nthr) {
+        const int t = idx >> 6, q4 = idx & 63;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < n; ++s) {
+          const float w = wsm[s * rows + r0 + t];
+          const float4 v = ptx::ld_shared_f4(buf + (s * nr + t) * 1024u + q4 * 16u);
+          a.x += w * v.x; a.y += w * v.y; a.z += w * v.z; a.w += w * v.w;
+        }
+        store(r0 + t, q4, a);
+      }
+    }
+    __syncthreads();  // buffer b is free again
+  }
+  if (by_piece) {
+#pragma unroll
+    for (int k = 0; k < kAccQuads; ++k) {
+      const int idx = tid + k * nthr;
+      if (idx < rows * 64) store(idx >> 6, idx & 63, acc[k]);
+    }
+  }
+  // Clear the item's flags and claim (for the next call that gets this memory).
+  for (int s = tid; s < n; s += nthr)
+    ptx::st_relaxed_gpu_u64(p.merge_flag + prow0(s) / kRowsPerTile, 0ull);
+  if (tid == 0) ptx::st_relaxed_gpu_u64(p.merge_flag + p.merge_claim_offset + prow0(0) / kRowsPerTile, 0ull);
+  return true;
+}
+
 template <bool kPair, bool kPaged, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
@@ -323,6 +551,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(kBarPvDone1), 1);
     ptx::mbar_init(bar(kBarOFree), kConsumers);
     ptx::mbar_init(bar(kBarDrain), 1);
+    ptx::mbar_init(bar(kBarMerge0), 1);
+    ptx::mbar_init(bar(kBarMerge1), 1);
+    ptx::mbar_init(bar(kBarPartDone), 4 * 32);
     if constexpr (kFp8) {
       for (int i = 0; i < kScSlots; ++i) {
         ptx::mbar_init(bar(kBarScFull + i), 1);
@@ -331,6 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::fence_mbar_init();
   }
+  uint32_t* merge_bits = reinterpret_cast<uint32_t*>(smem + kOffMergeBits);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  if (threadIdx.x < kMaxFusedSplitPieces / 32) merge_bits[threadIdx.x] = 0;
+  if (threadIdx.x == 0) *abort_flag = 0;
   if (warp < 4) {
     // Rows 126 and 127 of each Q chunk are never written by TMA: zero them once.
     for (int i = threadIdx.x; i < kQChunks * 2 * 128 / 16; i += 128) {
@@ -361,9 +596,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tpi = kPair ? 2 * kTokPerTile : kTokPerTile;  // tokens per work item
   const int n_workers = kPair ? static_cast<int>(gridDim.x) / 2 : static_cast<int>(gridDim.x);
   const int worker = kPair ? static_cast<int>(blockIdx.x) / 2 : static_cast<int>(blockIdx.x);
+  const Schedule sched{p.head_items, p.tail_splits, p.n_units, p.n_tail};
   PieceIter pieces;  // this CTA's (pair's) work, in order; each role walks its own copy
-  pieces.init(&p.batch, p.tail.v, Schedule{p.head_items, p.tail_splits, p.n_units, p.n_tail},
-              n_workers, worker);
+  pieces.init(&p.batch, p.tail.v, sched, n_workers, worker);
   // KV tile holding key kv_len-1 of a sequence when it is partial (else -1).
   auto v_fix_tile = [](const SeqGeo& sq) { return sq.kv_len % kBlockN ? (sq.kv_len - 1) / kBlockN : -1; };
 
@@ -415,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // CTA's 128 columns). A whole box is one copy; a paged box that crosses a
       // page is one copy per piece.
       auto next_tile = [&](const SeqGeo& sq, int n, bool is_k, int g) -> bool {
-        const bool v_fix = kPaged && !is_k && n == v_fix_tile(sq);
+        const bool v_fix = (kPaged || p.dense_vfix) && !is_k && n == v_fix_tile(sq);
         const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
         const CUtensorMap* sub_map = is_k ? &p.tmap_k_sub : (v_fix ? &p.tmap_v16 : &p.tmap_v_sub);
         const int halves = is_k ? kKStagesPerTile : (kPair ? 1 : 2);
@@ -459,7 +694,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         kPair ? lbar(kBarFull + st) : bar(kBarFull + st), r0, rows,
                                         nb, chunk0, g, v_fix, pol_kv);
           }
-          if (whole) load_box(dst, full, kBarFull + st, row, g, chunk0);
+          if (!kPaged && v_fix)
+            issue_dense_v_pieces<kPair>(&p.tmap_v16, dst, kPair ? lbar(kBarFull + st) : bar(kBarFull + st),
+                                        sq.kv_start, sq.kv_len, p.oob_row, r0, rows, nb, chunk0, g,
+                                        pol_kv);
+          else if (whole)
+            load_box(dst, full, kBarFull + st, row, g, chunk0);
           issued_mask |= 1u << st;
           issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
           if (++st == kStages) { st = 0; phase ^= 1u; }
@@ -516,6 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = next_tile(sq, w.n1 - 1, false, w.g);
         ++k;
       }
+      if (!ok) *abort_flag = 1;
       // Every copy issued must have landed before the CTA exits. On the normal
       // path the MMA thread already waited for all of them (these return at
       // once); after a time-out they may still be in flight. In a pair all
@@ -604,16 +845,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           // O += P_j V_j in k-steps of 16 keys, N = 256. V stages are MN-major:
           // LBO = next 64-wide d chunk (kLboV), SBO = next group of 8 keys (kSboV).
-          const int vfix_tile = kPaged ? v_fix_tile(p.batch.seq[w.seq]) : -1;
-          const bool v_fix = kPaged && w.n0 + j == vfix_tile;
+          const int vfix_tile = (kPaged || p.dense_vfix) ? v_fix_tile(p.batch.seq[w.seq]) : -1;
+          const bool v_fix = (kPaged || p.dense_vfix) && w.n0 + j == vfix_tile;
           const int kr = p.batch.seq[w.seq].kv_len - vfix_tile * kBlockN;  // used when v_fix
           if constexpr (kPair) {
             // One stage: 128 keys x this CTA's 2 chunks of 64 columns (waited for above).
             ptx::tc_fence_after();
             if (v_fix) {
-              zero_v_tail(stage_smem + st * kStageBytes, kNchV, 0, kRowsV, kr, false);
-              zero_v_tail(ptx::map_to_cta(stage_smem + st * kStageBytes, 1), kNchV, 0, kRowsV, kr,
-                          true);
+              zero_v_tail(stage_smem + st * kStageBytes, kNchV, kSboV, kLboV, 0, kRowsV, kr, false);
+              zero_v_tail(ptx::map_to_cta(stage_smem + st * kStageBytes, 1), kNchV, kSboV, kLboV, 0,
+                          kRowsV, kr, true);
               ptx::fence_proxy_async_all();
             }
             const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
@@ -631,7 +872,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (half > 0 && !(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
               ptx::tc_fence_after();
               if (v_fix) {
-                zero_v_tail(stage_smem + st * kStageBytes, kNchV, kRowsV * half, kRowsV, kr, false);
+                zero_v_tail(stage_smem + st * kStageBytes, kNchV, kSboV, kLboV, kRowsV * half, kRowsV,
+                            kr, false);
                 ptx::fence_proxy_async_all();
               }
               const uint64_t vd = v_desc0 + ((st * kStageBytes) >> 4);
@@ -651,6 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile += nt;
         ++k;
       }
+      if (!ok) *abort_flag = 1;
       // Drain: every MMA issued above has completed once this barrier fires.
       commit(kBarDrain);
       wait_bar(bar(kBarDrain), 0, p);
@@ -665,6 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t tile = 0;
     int k = 0;
+    int split_k = 0;  // split pieces done so far (their bit in merge_bits)
     bool ok = true;
     Piece w;
     while (ok && pieces.next(w)) {
@@ -877,9 +1121,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       arrive_leader(kBarOFree);
+      if (w.slot >= 0 && p.fused_merge) {
+        // Flag the piece done once all 128 threads have stored their partial rows
+        // (they arrive; thread 0 waits, with the usual time limit, then publishes
+        // them all with its release fence); a CTA that finds the item's flags all
+        // set merges it after its last piece.
+        ptx::mbar_arrive(bar(kBarPartDone));
+        if (row == 0 && wait_bar(bar(kBarPartDone), split_k & 1, p) &&
+            flag_piece_done(p, sched, n_workers, w.tail, w.slot, rank, kPair ? 2 : 1) &&
+            split_k < kMaxFusedSplitPieces)
+          merge_bits[split_k >> 5] |= 1u << (split_k & 31);
+      }
+      if (w.slot >= 0) ++split_k;
       tile += nt;
       ++k;
     }
+    if (!ok) *abort_flag = 1;
   }
 
   // ---- teardown ----------------------------------------------------------------
@@ -893,6 +1150,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (kPair) ptx::tmem_dealloc_pair(tmem, kTmemCols);
     else ptx::tmem_dealloc(tmem, kTmemCols);
   }
+  // ---- fused split merge: the items whose last piece this CTA completed --------
+  // Every copy into shared memory has landed (the roles drained them), so the Q
+  // region and the stage ring stage the partial rows. Skipped after a time-out.
+  if (p.fused_merge) {
+    __syncthreads();
+    if (*abort_flag == 0) {
+      PieceIter again;
+      again.init(&p.batch, p.tail.v, sched, n_workers, worker);
+      uint32_t mphase = 0;
+      int sk = 0;
+      Piece w;
+      while (again.next(w)) {
+        if (w.slot < 0) continue;
+        const bool mine = sk < kMaxFusedSplitPieces && (merge_bits[sk >> 5] >> (sk & 31)) & 1u;
+        ++sk;
+        if (mine && !merge_item(p, sched, n_workers, w.tail, rank, kPair ? 2 : 1, smem, base,
+                                bar(kBarMerge0), mphase))
+          break;
+      }
+    }
+  }
 }
 
 // Combine the pieces of every split (tail) item: blocks (j, *) merge tail item
@@ -901,13 +1179,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // tail, piece s in slot j*S + s; balanced tail, the workers' slots that
 // balanced_item_pieces / balanced_slot name (an item that no worker boundary
 // cuts was written whole by the attention kernel: its blocks return at once).
-// lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s. One warp per row:
-// lane s reads piece s's LSE (32 pieces per pass), the warp reduces max and
-// sum by shuffles, then every lane accumulates its 8 columns over the pieces
-// in order s = 0, 1, ... with independent loads (unrolled), so a row costs a
-// few memory latencies, not n of them; with one row per warp every row of the
-// call is in flight at once. Deterministic: fixed order throughout.
+// lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s. One warp per row,
+// every lane holding 8 columns: the loads of the first 4 pieces' columns and of
+// every piece's LSE (lane s: piece s) go out together, so a row of up to 4
+// pieces costs one memory round trip (registers stay under 64, four blocks per
+// SM); the warp reduces max and sum by shuffles
+// and accumulates the pieces in order s = 0, 1, ... (deterministic). With one
+// row per warp every row of the call is in flight at once.
 constexpr int kMergeRowsPerBlock = 8;  // 8 warps x 1 row
+constexpr int kMergeBatch = 4;         // pieces whose columns a lane loads at once
 
 __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
@@ -920,7 +1200,27 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-__global__ void __launch_bounds__(256) merge_tail_kernel(const __grid_constant__ MergeParams p) {
+// Every piece's LSE of one row, read by the lanes of a warp (lane s: piece s, 32
+// per pass): returns the row's maximum and, in *l0, the lane's LSE of pass 0.
+template <typename RowOf>
+__device__ __forceinline__ float row_lse_max(const float* part_lse, int n, int lane, RowOf prow,
+                                             float* l0) {
+  *l0 = lane < n ? __ldcg(part_lse + prow(lane)) : kNegInf;
+  float mx = *l0;
+  for (int s0 = 32; s0 < n; s0 += 32)
+    if (s0 + lane < n) mx = fmaxf(mx, __ldcg(part_lse + prow(s0 + lane)));
+  return warp_max(mx);
+}
+
+// Weight 2^{lse_s - m} of piece s (lane-uniform s): from lane s's LSE for s < 32.
+template <typename RowOf>
+__device__ __forceinline__ float piece_weight(const float* part_lse, int s, float l0, float m,
+                                              RowOf prow) {
+  const float l = s < 32 ? __shfl_sync(0xffffffffu, l0, s) : __ldcg(part_lse + prow(s));
+  return ptx::ex2_approx(l - m);
+}
+
+__global__ void __launch_bounds__(256, 4) merge_tail_kernel(const __grid_constant__ MergeParams p) {
   ptx::griddep_wait();  // launched early (programmatic dependent launch): the pieces must be done
   const int j = blockIdx.x;  // tail item
   const bool balanced = p.tail_splits == 0;
@@ -952,26 +1252,39 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const __grid_constant__
       if (s0 + lane < n) rows_ok &= row_ok(static_cast<long long>(prow(s0 + lane)), p.part_rows, p.status);
     if (!__all_sync(0xffffffffu, rows_ok)) return;
   }
-  float mx = kNegInf;
-  for (int s0 = 0; s0 < n; s0 += 32)
-    if (s0 + lane < n) mx = fmaxf(mx, p.part_lse[prow(s0 + lane)]);
-  mx = warp_max(mx);
+  auto cols = [&](int s) {
+    return reinterpret_cast<const float4*>(p.part_o + prow(s) * kHeadDim + 8 * lane);
+  };
+  float4 va[kMergeBatch], vb[kMergeBatch];
+#pragma unroll
+  for (int i = 0; i < kMergeBatch; ++i)
+    if (i < n) {
+      va[i] = __ldcg(cols(i));
+      vb[i] = __ldcg(cols(i) + 1);
+    }
+  float l0;
+  const float mx = row_lse_max(p.part_lse, n, lane, prow, &l0);
   const float m_use = (mx == kNegInf) ? 0.0f : mx;
+  float wsum = warp_sum(lane < n ? ptx::ex2_approx(l0 - m_use) : 0.0f);
+  for (int s0 = 32; s0 < n; s0 += 32)
+    wsum += warp_sum(s0 + lane < n ? ptx::ex2_approx(__ldcg(p.part_lse + prow(s0 + lane)) - m_use)
+                                   : 0.0f);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  float wsum = 0.0f;
-  for (int s0 = 0; s0 < n; s0 += 32) {
-    const int m = min(32, n - s0);
-    const float w_lane = lane < m ? ptx::ex2_approx(p.part_lse[prow(s0 + lane)] - m_use) : 0.0f;
-    const unsigned long long my_row = lane < m ? prow(s0 + lane) : 0;
-    wsum += warp_sum(w_lane);
-#pragma unroll 8
-    for (int i = 0; i < m; ++i) {
-      const float w = __shfl_sync(0xffffffffu, w_lane, i);
-      const unsigned long long pr = __shfl_sync(0xffffffffu, my_row, i);
-      const float4* src = reinterpret_cast<const float4*>(p.part_o + pr * kHeadDim + 8 * lane);
-      const float4 a = src[0], c = src[1];
-      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-      acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+  for (int s0 = 0; s0 < n; s0 += kMergeBatch) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int i = 0; i < kMergeBatch; ++i)
+        if (s0 + i < n) {
+          va[i] = __ldcg(cols(s0 + i));
+          vb[i] = __ldcg(cols(s0 + i) + 1);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kMergeBatch; ++i) {
+      if (s0 + i >= n) break;
+      const float w = piece_weight(p.part_lse, s0 + i, l0, m_use, prow);
+      acc[0] += w * va[i].x; acc[1] += w * va[i].y; acc[2] += w * va[i].z; acc[3] += w * va[i].w;
+      acc[4] += w * vb[i].x; acc[5] += w * vb[i].y; acc[6] += w * vb[i].z; acc[7] += w * vb[i].w;
     }
   }
   const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
@@ -988,12 +1301,15 @@ __global__ void __launch_bounds__(256) merge_tail_kernel(const __grid_constant__
 }
 
 // The same merge for calls whose items have many pieces (decode-sized chunks cut
-// into 16 or more KV pieces, on the uniform or the balanced tail): one block per row, its 8 warps taking the
-// pieces s = w, w + 8, ... (so each warp's loads are few and all in flight), their
-// weighted partial sums combined through shared memory in warp order (fixed order:
-// deterministic). Blocks (j, r): tail item j, row r of the item's rows.
+// into 16 or more KV pieces, on the uniform or the balanced tail): one block per
+// row, its 8 warps taking the pieces s = w, w + 8, ... (each warp loads its first
+// 6 pieces' columns together with every piece's LSE, one round trip for up to
+// 48 pieces), their weighted partial sums combined through shared memory in warp
+// order (fixed order: deterministic). Blocks (j, r): tail item j, row r of the
+// item's rows.
 constexpr int kWideWarps = 8;
 constexpr int kWideMergePieces = 16;  // items with this many pieces or more use it
+constexpr int kWideBatch = 6;         // pieces per warp whose columns load at once
 
 __global__ void __launch_bounds__(kWideWarps * 32)
     merge_wide_kernel(const __grid_constant__ MergeParams p) {
@@ -1029,23 +1345,44 @@ __global__ void __launch_bounds__(kWideWarps * 32)
       rows_ok &= row_ok(static_cast<long long>(prow(s)), p.part_rows, p.status);
     if (!__syncthreads_and(rows_ok)) return;
   }
+  auto cols = [&](int s) {
+    return reinterpret_cast<const float4*>(p.part_o + prow(s) * kHeadDim + 8 * lane);
+  };
+  float4 va[kWideBatch], vb[kWideBatch];
+#pragma unroll
+  for (int i = 0; i < kWideBatch; ++i) {
+    const int s = warp + kWideWarps * i;
+    if (s < n) {
+      va[i] = __ldcg(cols(s));
+      vb[i] = __ldcg(cols(s) + 1);
+    }
+  }
   // Every warp finds the row's maximum piece LSE itself (n loads across the lanes).
-  float mx = kNegInf;
-  for (int s0 = 0; s0 < n; s0 += 32)
-    if (s0 + lane < n) mx = fmaxf(mx, p.part_lse[prow(s0 + lane)]);
-  mx = warp_max(mx);
+  float l0;
+  const float mx = row_lse_max(p.part_lse, n, lane, prow, &l0);
   const float m_use = (mx == kNegInf) ? 0.0f : mx;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   float wsum = 0.0f;
-#pragma unroll 4
-  for (int s = warp; s < n; s += kWideWarps) {
-    const size_t pr = prow(s);
-    const float w = ptx::ex2_approx(p.part_lse[pr] - m_use);
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + pr * kHeadDim + 8 * lane);
-    const float4 a = src[0], c = src[1];
-    wsum += w;
-    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-    acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+  for (int b0 = 0; warp + kWideWarps * b0 < n; b0 += kWideBatch) {
+    if (b0 > 0) {
+#pragma unroll
+      for (int i = 0; i < kWideBatch; ++i) {
+        const int s = warp + kWideWarps * (b0 + i);
+        if (s < n) {
+          va[i] = __ldcg(cols(s));
+          vb[i] = __ldcg(cols(s) + 1);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kWideBatch; ++i) {
+      const int s = warp + kWideWarps * (b0 + i);
+      if (s >= n) break;
+      const float w = piece_weight(p.part_lse, s, l0, m_use, prow);
+      wsum += w;
+      acc[0] += w * va[i].x; acc[1] += w * va[i].y; acc[2] += w * va[i].z; acc[3] += w * va[i].w;
+      acc[4] += w * vb[i].x; acc[5] += w * vb[i].y; acc[6] += w * vb[i].z; acc[7] += w * vb[i].w;
+    }
   }
 #pragma unroll
   for (int e = 0; e < 8; ++e) part[warp][8 * lane + e] = acc[e];

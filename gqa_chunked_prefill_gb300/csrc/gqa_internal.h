@@ -50,19 +50,33 @@ struct FwdParams {
   // cache row block_table[j / page_size] * page_size + j % page_size (gqa_paged.h).
   CUtensorMap tmap_k_sub;    // 5-D, sub_rows keys x the stage's chunks: pieces of a box
   CUtensorMap tmap_v_sub;    //   that crosses a page
-  CUtensorMap tmap_v16;      // 5-D, 16 keys: V of the tile holding key kv_len-1
+  CUtensorMap tmap_v16;      // 16 keys: V of the tile holding key kv_len-1 (paged: 5-D, all
+                             //   the stage's chunks; dense batch: 4-D, one chunk)
   const int* block_table;    // sequence b's row at b * bt_stride: physical page of each
   int bt_stride;             //   logical page (ceil(kv_len_b / page_size) used entries)
   int page_size;             // keys per page, a multiple of 16
   int num_pages;             // pages in the cache
   int sub_rows;              // gcd(page_size, 64)
-  int oob_row;               // num_pages * page_size: a row past the cache (TMA zero fill)
+  int oob_row;               // a row past the cache (num_pages * page_size) or, for a dense
+                             //   batch, past the packed K/V (total keys): TMA zero fill
+  int dense_vfix;            // dense batch of several sequences: V of each sequence's last
+                             //   KV tile goes in 16-key pieces, keys past it zeroed
   // FP8 QK^T (kernels instantiated with kFp8 only): tmap_q / tmap_k hold E4M3 codes
   // (Q box (128, 6 heads, 21 tokens); K 4-D (128, key, head, chunk) with 2 chunks).
   CUtensorMap tmap_ks;       // dense: key scales FP32 [4][k_scale_stride], box (128 keys, 1 head)
   const float* k_scale;      // paged: one scale per cache row, [4][k_scale_stride], read by
   int k_scale_stride;        //   1-D bulk copies (16-key pieces are 64 bytes)
   const float* q_scale;      // [total q rows][24] FP32 query scales
+  // Split merge inside the attention kernel (fused_merge != 0). Every split piece,
+  // once its partial rows are stored, sets its flag merge_flag[slot * CTAs per
+  // item + rank] to call_tag and then reads its item's other flags; a piece that
+  // finds them all equal to call_tag (flags left by another call hold another tag
+  // or 0) merges the item's rows of its rank after its last piece, and clears the
+  // flags. No CTA ever waits for another.
+  unsigned long long* merge_flag;  // [slots * cpi] flags, then [slots * cpi] claim words
+  long long merge_claim_offset;    // slots * cpi
+  unsigned long long call_tag;     // nonzero, new for every call
+  int fused_merge;
   TailPrefix tail;           // balanced tail: tile prefix sums of the tail items
   Batch batch;               // the call's sequences (gqa_schedule.h); kept last: it is large
 };
@@ -100,6 +114,13 @@ cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scale, int ro
                                 int scale_stride, bool head_major, const ScaleColumns& cols,
                                 cudaStream_t stream);
 cudaError_t max_active_pairs(int* pairs);       // co-resident CTA pairs on this device
+// Split pieces one CTA (pair) may count for the fused merge: it remembers which
+// items it completed in a bitset of this many bits (the planner keeps every
+// worker's split pieces below it, else it plans the separate merge pass).
+constexpr int kMaxFusedSplitPieces = 2048;
+// Pieces of one item the fused merge takes (their LSEs for all rows are staged in
+// shared memory at once); items cut into more use the separate merge pass.
+constexpr int kMaxFusedItemPieces = 48;
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t prepare_fwd_kernel();                // per-device one-time attributes
 cudaError_t status_word_address(int** ptr);      // device address of the status word

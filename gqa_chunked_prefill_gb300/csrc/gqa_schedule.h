@@ -29,8 +29,11 @@
 //    the output; of the others, the CTA's first piece writes slot 2x and its
 //    last piece slot 2x+1 (a range holds at most those two partial pieces).
 //    Every CTA gets the same number of tiles, whatever the tail's item count.
-// The merge pass (merge_tail_kernel, or merge_wide_kernel for items of 16 or more
-// pieces) then combines the pieces of every split tail item.
+// The pieces of every split tail item are then combined, either inside the
+// attention kernel by the CTA that completes the item's last piece (the "fused"
+// merge: each piece counts itself done on a per-item counter after storing its
+// partial; no CTA waits for another) or by a separate merge pass
+// (merge_tail_kernel, or merge_wide_kernel for items of 16 or more pieces).
 //
 // Why this shape: in every round all CTAs sweep the KV range of items of
 // (nearly) equal length from the same starting key in lockstep, so the K/V
@@ -140,10 +143,28 @@ __host__ __device__ inline void item_of(const Batch& b, int i, int& seq, int& qt
 }
 
 // One unit of work: tiles [n0, n1) of item (seq, qt, g). slot < 0: the unit is
-// a whole item and writes the output directly; otherwise it writes partial slot `slot`.
+// a whole item and writes the output directly; otherwise it writes partial slot
+// `slot`. tail: the item's index among the tail items (item - head_items), or -1
+// for an item of the whole rounds.
 struct Piece {
-  int seq, qt, g, n0, n1, slot;
+  int seq, qt, g, n0, n1, slot, tail;
 };
+
+// Pieces of tail item j and where piece s (KV order) wrote its partial, for
+// either cut (S = sc.tail_splits; S == 0: balanced, from the prefix sums v over
+// G workers). n < 2: the item was not split.
+__host__ __device__ inline int tail_item_pieces(const Schedule& sc, const int* v, int G, int j,
+                                                int& x_lo) {
+  x_lo = 0;
+  if (sc.tail_splits > 0) return sc.tail_splits;
+  int n;
+  balanced_item_pieces(v, sc.n_tail, G, j, x_lo, n);
+  return n;
+}
+__host__ __device__ inline int tail_piece_slot(const Schedule& sc, const int* v, int G, int j,
+                                               int x_lo, int s) {
+  return sc.tail_splits > 0 ? j * sc.tail_splits + s : balanced_slot(v, sc.n_tail, G, j, x_lo, s);
+}
 
 __host__ __device__ inline Piece unit_piece(const Batch& b, const Schedule& sc, int u) {
   Piece w;
@@ -156,6 +177,7 @@ __host__ __device__ inline Piece unit_piece(const Batch& b, const Schedule& sc, 
     s = t % sc.tail_splits;
   }
   item_of(b, item, w.seq, w.qt, w.g);
+  w.tail = u < sc.head_items ? -1 : item - sc.head_items;
   const int nt = item_tiles(b.seq[w.seq], b.tok_per_item, w.qt);
   if (u < sc.head_items || sc.tail_splits == 1) {
     w.n0 = 0;
@@ -209,6 +231,7 @@ struct PieceIter {
     const long long s = tail[k], e = tail[k + 1];
     const long long stop = end < e ? end : e;
     item_of(*b, sc.head_items + k, w.seq, w.qt, w.g);
+    w.tail = k;
     w.n0 = static_cast<int>(pos - s);
     w.n1 = static_cast<int>(stop - s);
     w.slot = (pos == s && stop == e) ? -1 : 2 * x + (pos == begin ? 0 : 1);

@@ -73,8 +73,10 @@ def test_varlen_split_tails_every_element(cuda_device, splits, grid, variant):
     out, lse, plan = run_varlen(q, k, v, cu_q, cu_k, force_splits=splits, force_grid=grid,
                                 force_variant=variant)
     # A balanced tail on a small grid may find worker boundaries on item boundaries
-    # (nothing split, one launch); on the full grid it cuts items.
-    assert plan["kernels_per_call"] == 2 or (splits < 0 and grid > 0)
+    # (nothing split, no workspace); on the full grid it cuts items.
+    assert plan["workspace_bytes"] > 0 or (splits < 0 and grid > 0)
+    assert plan["kernels_per_call"] == (2 if plan["workspace_bytes"] and not plan["fused_merge"]
+                                        else 1)
     assert (plan["tail_splits"] == 0) == (splits < 0)
     ref_o, ref_l = oracle.varlen_attention(q, k, v, cu_q, cu_k, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
@@ -112,3 +114,32 @@ def test_largest_batch(cuda_device):
     out, lse, plan = run_varlen(q, k, v, cu_q, cu_k)
     ref_o, ref_l = oracle.varlen_attention(q, k, v, cu_q, cu_k, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l, "128 seqs")
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("splits", [0, 3, -1])
+@pytest.mark.parametrize("poison", [float("nan"), float("inf")])
+def test_a_sequences_values_do_not_reach_its_neighbours(cuda_device, variant, splits, poison):
+    """Sequences are independent (the single-sequence definition, applied per
+    sequence): one sequence whose Q, K and V hold Inf or NaN leaves every other
+    sequence's output and LSE bit-identical to the clean run. K/V lengths are not
+    multiples of the 128-key tile, so the last tile of each sequence reaches into the
+    next sequence's rows."""
+    lens = [(43, 300), (5, 1000), (129, 1001), (22, 22), (7, 700), (1, 33)]
+    q, k, v, cu_q, cu_k = make_varlen(lens, seed=900)
+    force = dict(force_variant=variant, force_splits=splits)
+    out_c, lse_c, _ = run_varlen(q, k, v, cu_q, cu_k, **force)
+    ref_o, ref_l = oracle.varlen_attention(q, k, v, cu_q, cu_k, SCALE)
+    check_close(out_c.double().cpu().numpy(), lse_c.double().cpu().numpy(), ref_o, ref_l, "clean")
+    for bad in range(len(lens)):
+        q2, k2, v2 = q.clone(), k.clone(), v.clone()
+        q2[cu_q[bad]:cu_q[bad + 1]] = poison
+        k2[cu_k[bad]:cu_k[bad + 1]] = poison
+        v2[cu_k[bad]:cu_k[bad + 1]] = poison
+        out_p, lse_p, _ = run_varlen(q2, k2, v2, cu_q, cu_k, **force)
+        for b in range(len(lens)):
+            if b == bad:
+                continue
+            r = slice(cu_q[b], cu_q[b + 1])
+            assert torch.equal(out_p[r], out_c[r]), f"sequence {b} changed when {bad} was poisoned"
+            assert torch.equal(lse_p[r], lse_c[r]), f"sequence {b} LSE changed ({bad} poisoned)"

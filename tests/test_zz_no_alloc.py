@@ -58,7 +58,7 @@ def test_noalloc_uses_scratch_on_a_split_plan(cuda_device):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     plans = [gqa.gqa_prefill_make_plan(WORKLOADS[n].q_len, WORKLOADS[n].kv_len, 24, 4, 256, sms)[1]
              for n in ("q512_kv4096_kbias", "q512_kv32768")]
-    assert any(p["kernels_per_call"] == 2 and 0 < p["workspace_bytes"] <= SCRATCH_BYTES
+    assert any(p["tail_splits"] != 1 and 0 < p["workspace_bytes"] <= SCRATCH_BYTES
                for p in plans)
 
 
