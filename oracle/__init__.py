@@ -9,7 +9,9 @@ two share nothing but the seeded inputs of ``gqa_inputs``.
 through its block table; ``paged_attention()`` is attention on what it returns.
 ``varlen_attention()`` / ``paged_varlen_attention()`` apply the definition to
 each sequence of a packed batch. ``quantize_e4m3()`` and ``fp8qk_attention()``
-define the quantised-QK^T path.
+define the quantised-QK^T path; ``quantize_v_e4m3()``, ``fp8pv_attention()``
+and ``fp8pv_p_bound()`` the quantised PV (per-channel V scales, P rounded to
+E4M3, and the bound on what that rounding can change).
 
 ``attention()`` runs the plain C++ definition in ``gqa_oracle.cpp`` (explicit
 full-row softmax in FP64, one std::thread per row at a time). ``restate_numpy``
@@ -260,3 +262,79 @@ def fp8qk_attention(q_codes, q_scale, k_codes, k_scale, v, scale: float, rows=No
     k_scale [kv_len, Hkv] (token-major here); v as for ``attention``."""
     return attention(dequantize_e4m3(q_codes, q_scale), dequantize_e4m3(k_codes, k_scale), v,
                      scale, rows=rows, n_threads=n_threads)
+
+
+# --- quantised PV ----------------------------------------------------------------
+#
+# The same report's final submission also multiplies P by V in 8 bits ("INT8 PV")
+# without saying how V or P are scaled. The reading here, for GB300's FP8 tensor
+# path: V gets one symmetric scale per (KV head, channel) over the call's keys,
+# s_v = max_j |v[j,g,c]| / 448 with codes E4M3(v / s_v) (the rule of
+# quantize_e4m3, applied along the key axis), so that the scale multiplies a
+# column of P.V after the product; P is rounded to E4M3 as the MMA operand, while
+# the softmax normaliser keeps the exact probabilities. The result below is the
+# plain definition the method approximates: attention of the dequantised Q, K
+# and V with exact probabilities; fp8pv_p_bound bounds what rounding P can change.
+
+def quantize_v_e4m3(v):
+    """Per (KV head, channel) quantisation of v [kv_len, Hkv, d]: the kv_len values of
+    channel c of KV head g form one vector (quantize_e4m3's rule). Returns (codes
+    uint8 [kv_len, Hkv, d], scales float32 [Hkv, d])."""
+    v32 = np.asarray(v.float().numpy() if isinstance(v, torch.Tensor) else v, dtype=np.float32)
+    codes_t, s = quantize_e4m3(np.ascontiguousarray(v32.transpose(1, 2, 0)))
+    return np.ascontiguousarray(codes_t.transpose(2, 0, 1)), s
+
+
+def dequantize_v_e4m3(codes, scales) -> np.ndarray:
+    """codes [kv_len, Hkv, d] times the channel scales [Hkv, d], in FP64 (exact)."""
+    return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[None, :, :]
+
+
+def fp8pv_attention(q_codes, q_scale, k_codes, k_scale, v_codes, v_scale, scale: float,
+                    rows=None, n_threads: Optional[int] = None):
+    """The quantised QK^T and PV result: attention of the dequantised query, keys
+    and values (FP64, exact probabilities). q: codes [q_len, Hq, d] + scales
+    [q_len, Hq]; k: codes [kv_len, Hkv, d] + scales [kv_len, Hkv]; v: codes
+    [kv_len, Hkv, d] + channel scales [Hkv, d]."""
+    return attention(dequantize_e4m3(q_codes, q_scale), dequantize_e4m3(k_codes, k_scale),
+                     dequantize_v_e4m3(v_codes, v_scale), scale, rows=rows, n_threads=n_threads)
+
+
+E4M3_P_REL = 2.0 ** -4    # half a unit in the last place of a normal E4M3 value, relative
+E4M3_P_FLOOR = 2.0 ** -16  # half the subnormal step 2^-10 of P stored as 2^6 * p, p <= 4
+
+
+def fp8pv_p_bound(q, k, v, scale: float, rows=None, chunk: int = 256) -> np.ndarray:
+    """Per-element bound on how far rounding the probabilities to E4M3 moves the
+    output, for q [q_len, Hq, d], k, v [kv_len, Hkv, d] (FP64 values: the
+    dequantised inputs), rows as in ``attention``:
+
+        B[t, h, c] = sum_j (2^-4 p_j + 2^-16) |v[j, g, c]| / sum_j p_j,
+        p_j = exp(s_j - max_i s_i)  over the visible keys j of row (t, h).
+
+    Why: the kernel stores each probability as P = 2^6 * 2^(x_j - m), m a running
+    maximum at most 2 (log2 units) below the row maximum seen so far, so P <= 256
+    fits E4M3 unsaturated; rounding P moves it by at most 2^-4 P (normal range)
+    or 2^-10 (subnormal). In the final normalisation the first term becomes
+    2^-4 times the exact softmax weight and the second at most 2^-16 / sum_j p_j,
+    since the normaliser taken against a maximum m <= max_i x_i is at least the
+    one taken against the maximum itself."""
+    q64, k64, v64 = _f64(q), _f64(k), _f64(v)
+    q_len, hq, d = q64.shape
+    kv_len, hkv, _ = k64.shape
+    group = hq // hkv
+    p0 = kv_len - q_len
+    ids = np.arange(q_len * hq) if rows is None else np.asarray(
+        rows.numpy() if isinstance(rows, torch.Tensor) else rows, dtype=np.int64)
+    out = np.empty((len(ids), d), np.float64)
+    for a in range(0, len(ids), chunk):
+        blk = ids[a:a + chunk]
+        t, h = blk // hq, blk % hq
+        for g in np.unique(h // group):
+            sel = np.nonzero(h // group == g)[0]
+            s = scale * q64[t[sel], h[sel]] @ k64[:, g].T            # [rows, kv_len]
+            s[np.arange(kv_len)[None, :] > (p0 + t[sel])[:, None]] = -np.inf
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            w = E4M3_P_REL * p + np.where(np.isfinite(s), E4M3_P_FLOOR, 0.0)
+            out[a + sel] = (w @ np.abs(v64[:, g])) / p.sum(axis=1, keepdims=True)
+    return out if rows is not None else out.reshape(q_len, hq, d)

@@ -358,3 +358,160 @@ def test_paged_batch_scatter_is_read_back_exactly():
     o1, l1 = oracle.paged_varlen_attention(q, kc, vc, table, cu_q, kv_lens, SCALE)
     o2, l2 = oracle.varlen_attention(q, k, v, cu_q, cu_k, SCALE)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# --- quantised PV ---------------------------------------------------------------
+
+def test_v_channel_scales_and_codes_by_hand():
+    """Channel c of KV head g over all keys is one vector: its scale is its largest
+    magnitude / 448 and each value's code is E4M3(v / s). Worked by hand on a
+    3-key, 1-head, 2-channel V (channel 1 is all zeros: scale 0, codes 0)."""
+    v = np.zeros((3, 1, 2), np.float32)
+    v[:, 0, 0] = [1.0, -2.0, 0.5]          # max |v| = 2: s = 2 / 448 = 1 / 224
+    codes, s = oracle.quantize_v_e4m3(v)
+    assert s.shape == (1, 2) and s[0, 0] == np.float32(2.0) / np.float32(448.0) and s[0, 1] == 0
+    # 1 / s = 224 (E4M3 224 = 1.75 * 2^7: e=14, m=6 -> 0x76); -2 / s = -448 (0xFE);
+    # 0.5 / s = 112 (1.75 * 2^6: 0x6E)
+    assert list(codes[:, 0, 0]) == [0x76, 0xFE, 0x6E]
+    assert list(codes[:, 0, 1]) == [0, 0, 0]
+    np.testing.assert_array_equal(oracle.dequantize_v_e4m3(codes, s)[:, 0, 0],
+                                  np.array([224.0, -448.0, 112.0]) * float(s[0, 0]))
+
+
+def test_v_quantisation_is_the_vector_rule_along_keys():
+    """The V rule is quantize_e4m3 applied to each (head, channel) column over keys,
+    not to each key's 256 values: transposing first gives the same codes."""
+    v = rand64((37, 4, 256), 71).astype(np.float32)
+    codes, s = oracle.quantize_v_e4m3(v)
+    for g in range(4):
+        for c in (0, 17, 255):
+            cc, ss = oracle.quantize_e4m3(v[:, g, c][None, :])
+            np.testing.assert_array_equal(codes[:, g, c], cc[0])
+            assert s[g, c] == ss[0] == np.float32(np.abs(v[:, g, c]).max()) / np.float32(448.0)
+    per_key, _ = oracle.quantize_e4m3(v)  # the Q/K rule would differ
+    assert not np.array_equal(per_key, codes)
+
+
+def test_fp8pv_attention_equals_attention_on_exact_codes():
+    """Values that are already codes times a power-of-two channel scale (each
+    channel reaching +-448 times its scale) survive quantisation exactly, so the
+    quantised-PV result is plain attention on them."""
+    rng = np.random.default_rng(5)
+    q_len, kv_len = 6, 40
+    q = rand64((q_len, 24, 256), 1)
+    k = rand64((kv_len, 4, 256), 2)
+    vals = oracle.e4m3_values()
+    cv = rng.choice(vals, size=(kv_len, 4, 256)) * rng.choice([-1.0, 1.0], size=(kv_len, 4, 256))
+    cv[0] = 448.0  # every channel reaches the largest code
+    v = cv * (2.0 ** rng.integers(-8, 3, size=(1, 4, 256)))
+    vc, vs = oracle.quantize_v_e4m3(v)
+    np.testing.assert_array_equal(oracle.dequantize_v_e4m3(vc, vs), v)
+    qc, qs = oracle.quantize_e4m3(q)
+    kc, ks = oracle.quantize_e4m3(k)
+    got_o, got_l = oracle.fp8pv_attention(qc, qs, kc, ks, vc, vs, SCALE)
+    ref_o, ref_l = oracle.attention(oracle.dequantize_e4m3(qc, qs), oracle.dequantize_e4m3(kc, ks),
+                                    v, SCALE)
+    np.testing.assert_array_equal(got_o, ref_o)
+    np.testing.assert_array_equal(got_l, ref_l)
+
+
+def test_power_of_two_channel_scale_scales_the_output_column():
+    """Scaling one V channel by 2^k leaves its codes alone, multiplies its scale by
+    2^k and the output column by exactly 2^k; the other columns do not move."""
+    q, k, v = (t.double().numpy() for t in make_qkv(9, 50, seed=61))
+    vc, vs = oracle.quantize_v_e4m3(v)
+    v2 = v.copy()
+    v2[:, 2, 77] *= 2.0 ** 5
+    vc2, vs2 = oracle.quantize_v_e4m3(v2)
+    np.testing.assert_array_equal(vc2, vc)
+    assert vs2[2, 77] == vs[2, 77] * 32 and np.array_equal(np.delete(vs2.ravel(), 2 * 256 + 77),
+                                                           np.delete(vs.ravel(), 2 * 256 + 77))
+    qc, qs = oracle.quantize_e4m3(q)
+    kc, ks = oracle.quantize_e4m3(k)
+    o1, _ = oracle.fp8pv_attention(qc, qs, kc, ks, vc, vs, SCALE)
+    o2, _ = oracle.fp8pv_attention(qc, qs, kc, ks, vc2, vs2, SCALE)
+    np.testing.assert_array_equal(o2[:, 12:18, 77], o1[:, 12:18, 77] * 32)  # heads of group 2
+    mask = np.ones(o1.shape, bool)
+    mask[:, 12:18, 77] = False
+    np.testing.assert_array_equal(o2[mask], o1[mask])
+
+
+def _online_p_rounding(q, k, v, scale, t, h, rng, tile=16, threshold=2.0, pscale=6.0):
+    """Brute force of the method's PV for one row: keys in tiles, a running maximum
+    (log2 units) raised only when it grows by more than `threshold`, P stored as
+    E4M3(2^(x - m + pscale)), O and the row sum rescaled when m moves."""
+    kv_len = k.shape[0]
+    p_last = kv_len - q.shape[0] + t
+    g = h // (q.shape[1] // k.shape[1])
+    x = scale * (k[:p_last + 1, g] @ q[t, h]) / math.log(2.0)
+    m, o, l = -np.inf, np.zeros(v.shape[2]), 0.0
+    for a in range(0, p_last + 1, tile):
+        xt = x[a:a + tile]
+        if xt.max() > m + threshold:
+            m_new = xt.max() + rng.uniform(-threshold, 0)  # any reference at most `threshold` low
+            m_new = max(m_new, xt.max() - threshold)
+            if np.isfinite(m):
+                o *= 2.0 ** (m - m_new)
+                l *= 2.0 ** (m - m_new)
+            m = m_new
+        pf = 2.0 ** (xt - m + pscale)
+        pq = oracle.e4m3_decode(oracle.e4m3_encode(pf.astype(np.float32)))
+        o += pq @ v[a:a + len(xt), g]
+        l += pf.sum()
+    return o / l
+
+
+def test_p_rounding_stays_within_the_bound():
+    """The E4M3 rounding of P, simulated key by key with running maxima anywhere in
+    the allowed band, never moves an output element by more than fp8pv_p_bound;
+    and the bound is not slack by orders of magnitude (the worst case uses a good
+    part of it)."""
+    rng = np.random.default_rng(9)
+    q, k, v = (t.double().numpy() for t in make_qkv(5, 300, seed=62))
+    k[100:110] *= 4.0  # a few large scores: peaked rows and rescales
+    rows = np.array([0, 24 * 2 + 7, 24 * 4 + 23])
+    ref_o, _ = oracle.attention(q, k, v, SCALE, rows=rows)
+    bound = oracle.fp8pv_p_bound(q, k, v, SCALE, rows=rows)
+    worst = 0.0
+    for i, r in enumerate(rows):
+        for _ in range(3):
+            got = _online_p_rounding(q, k, v, SCALE, r // 24, r % 24, rng)
+            err = np.abs(got - ref_o[i])
+            assert np.all(err <= bound[i] * (1 + 1e-9)), (r, (err / bound[i]).max())
+            worst = max(worst, (err / bound[i]).max())
+    assert worst > 0.05
+
+
+def test_p_bound_by_hand():
+    """Two visible keys with scores 0 and ln(1/2) (p = 1, 1/2), one channel with
+    v = (1, -3): B = ((2^-4 + 2^-16) * 1 + (2^-4 / 2 + 2^-16) * 3) / 1.5."""
+    q = np.zeros((1, 1, 1))
+    q[0, 0, 0] = 1.0
+    k = np.array([[[0.0]], [[math.log(0.5)]]])
+    v = np.array([[[1.0]], [[-3.0]]])
+    b = oracle.fp8pv_p_bound(q, k, v, 1.0)
+    want = ((2 ** -4 + 2 ** -16) * 1 + (2 ** -5 + 2 ** -16) * 3) / 1.5
+    assert abs(b[0, 0, 0] - want) < 1e-15
+
+
+def test_p_bound_needs_its_subnormal_term():
+    """One dominant key and 200000 keys whose stored P (2^6 * p) is 0.45 * 2^-9,
+    below half the smallest E4M3 subnormal: they all round to zero although they
+    carry most of the row's mass. The bound holds; its relative term alone (what
+    a normal-range-only analysis would give) does not."""
+    kv_len = 200001
+    q = np.zeros((1, 1, 8))
+    q[0, 0, 0] = 1.0
+    k = np.zeros((kv_len, 1, 8))
+    k[1:, 0, 0] = (math.log2(0.45) - 9 - 6) * math.log(2.0)  # 2^6 * p = 0.45 * 2^-9
+    v = np.ones((kv_len, 1, 8))
+    v[:, 0, 1:] = np.linspace(0.5, 2.0, 7)
+    ref_o, _ = oracle.attention(q, k, v, 1.0)
+    got = _online_p_rounding(q, k, v, 1.0, 0, 0, np.random.default_rng(3), tile=kv_len,
+                             threshold=0.0)
+    err = np.abs(got - ref_o[0, 0])
+    bound = oracle.fp8pv_p_bound(q, k, v, 1.0)[0, 0]
+    assert np.all(err <= bound)
+    p = np.exp(k[:, 0, 0] - k[:, 0, 0].max())
+    rel_only = (oracle.E4M3_P_REL * p @ v[:, 0]) / p.sum()
+    assert np.all(err > 5 * rel_only)
