@@ -116,6 +116,14 @@ lib.gqa_prefill_make_plan.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                       ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan.restype = _i
 lib.gqa_prefill_device_info.argtypes = [ctypes.POINTER(_i), ctypes.POINTER(_i)]
+lib.gqa_quantize_v_fp8.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _vp]
+lib.gqa_quantize_v_fp8.restype = _i
+_FP8PV_ARGS = [_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
+lib.gqa_prefill_attn_fp8qkpv.argtypes = _FP8PV_ARGS
+lib.gqa_prefill_attn_fp8qkpv.restype = _i
+lib.gqa_prefill_attn_fp8qkpv_ex.argtypes = _FP8PV_ARGS + [ctypes.POINTER(PrefillOpts),
+                                                          ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_attn_fp8qkpv_ex.restype = _i
 lib.gqa_prefill_device_info.restype = _i
 lib.gqa_prefill_poll.argtypes = [_vp, ctypes.POINTER(_i)]
 lib.gqa_prefill_poll.restype = _i
@@ -279,6 +287,47 @@ def gqa_prefill_attn_fp8qk_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v,
                                        k_scale_stride, _ptr(v), _ptr(out), _ptr(lse), q_len,
                                        kv_len, n_q_heads, n_kv_heads, head_dim, scale,
                                        _stream(stream), ctypes.byref(opts), ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def gqa_quantize_v_fp8(v, v_fp8t, v_scale, kv_len, n_kv_heads, head_dim, v_stride, stream=None,
+                       check=True) -> int:
+    """E4M3 codes of BF16 v [kv_len, 4, 256], transposed to [4, 256, v_stride] (uint8),
+    and per-(KV head, channel) FP32 scales [4, 256]."""
+    rc = lib.gqa_quantize_v_fp8(_ptr(v), _ptr(v_fp8t), _ptr(v_scale), kv_len, n_kv_heads,
+                                head_dim, v_stride, _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_prefill_attn_fp8qkpv(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v_fp8t, v_scale,
+                             v_stride, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim,
+                             scale, stream=None, check=True) -> int:
+    rc = lib.gqa_prefill_attn_fp8qkpv(_ptr(q_fp8), _ptr(q_scale), _ptr(k_fp8), _ptr(k_scale),
+                                      k_scale_stride, _ptr(v_fp8t), _ptr(v_scale), v_stride,
+                                      _ptr(out), _ptr(lse), q_len, kv_len, n_q_heads, n_kv_heads,
+                                      head_dim, scale, _stream(stream))
+    if check:
+        _check(rc)
+    return rc
+
+
+def gqa_prefill_attn_fp8qkpv_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v_fp8t, v_scale,
+                                v_stride, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
+                                head_dim, scale, stream=None, force_splits=0, force_grid=0,
+                                force_variant=0, wait_timeout_us=0, fwd_events=None,
+                                test_withhold_q=False, merge_mode=0, check=True):
+    opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
+                 test_withhold_q, merge_mode)
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_attn_fp8qkpv_ex(_ptr(q_fp8), _ptr(q_scale), _ptr(k_fp8), _ptr(k_scale),
+                                         k_scale_stride, _ptr(v_fp8t), _ptr(v_scale), v_stride,
+                                         _ptr(out), _ptr(lse), q_len, kv_len, n_q_heads,
+                                         n_kv_heads, head_dim, scale, _stream(stream),
+                                         ctypes.byref(opts), ctypes.byref(plan))
     if check:
         _check(rc)
     return rc, plan.as_dict()

@@ -116,9 +116,16 @@ constexpr uint32_t kIdescQK2 = ptx::idesc_bf16_f32(256, 128, false, false);  // 
 constexpr uint32_t kIdescPV2 = ptx::idesc_bf16_f32(256, 256, false, true);   // CTA pair
 constexpr uint32_t kIdescQK8 = ptx::idesc_e4m3_f32(128, 128);                 // FP8 QK^T
 constexpr uint32_t kIdescQK82 = ptx::idesc_e4m3_f32(256, 128);                // FP8, pair
+constexpr uint32_t kIdescPV8 = ptx::idesc_e4m3_f32(128, 256);                 // FP8 PV
+constexpr uint32_t kIdescPV82 = ptx::idesc_e4m3_f32(256, 256);                // FP8 PV, pair
 
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
+// Quantised PV: P is stored as the E4M3 code of 2^6 * p with the running maximum
+// at most 2 below the row's maximum so far (p <= 4): 2^6 * p <= 256 < 448, and
+// probabilities down to 2^-12 of the maximum stay in E4M3's normal range.
+constexpr float kRescaleThresholdPv = 2.0f;
+constexpr float kPScaleLog2Pv = 6.0f;
 constexpr float kLn2 = 0.693147180559945309f;
 
 __device__ int g_status_word = 0;
@@ -262,7 +269,13 @@ __device__ __noinline__ void issue_paged_scales(const PagedGeom& pgeo, const int
 // multicast to both CTAs; the peer's softmax warps arrive on the leader's
 // barriers remotely.
 //
-// kFp8 = true: quantised QK^T (gfx936 DCU上实现INT8 QK MMAC, §1): Q and K are E4M3
+// kFp8 = 2: also quantised PV (the same report's final submission): V arrives as
+// E4M3 codes transposed per channel ([head][channel][key], one scale per
+// channel), P is rounded to E4M3 as 2^6 * p, O += P V is a kind::f8f6f4 MMA with
+// P from tensor memory and V K-major, and the epilogue multiplies column c of O
+// by channel c's scale. Dense K/V, one sequence.
+//
+// kFp8 = 1: quantised QK^T (gfx936 DCU上实现INT8 QK MMAC, §1): Q and K are E4M3
 // codes with one FP32 scale per query (token, head) and per key (token, KV
 // head); S = Q_q K_q^T is a kind::f8f6f4 MMA, and every score is restored as
 // S * s_q * s_k * scale before the softmax. PV stays BF16.
@@ -485,9 +498,11 @@ __device__ __noinline__ bool merge_item(const FwdParams& p, const Schedule& sc, 
   return true;
 }
 
-template <bool kPair, bool kPaged, bool kFp8>
+template <bool kPair, bool kPaged, int kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
+  static_assert(kFp8 != 2 || !kPaged, "quantised PV reads dense V");
+  constexpr bool kFp8Pv = kFp8 == 2;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -530,6 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kLboV = kPaged ? 1024u : kRowsV * 128u;
   constexpr uint32_t kSboV = kPaged ? kNchV * 1024u : 1024u;
   constexpr uint32_t kKStageBytes = kRowsK * kNchK * 128u;  // K bytes per stage per CTA
+  // Quantised PV: a V tile is one stage of 128-byte rows of 128 key codes, one row
+  // per channel (256, or this CTA's 128 in a pair): K-major, SBO = 8 rows.
+  constexpr uint32_t kVStageBytesPv = kPair ? 16384u : 32768u;
 
   // The stream's next kernel (the split merge, or the caller's) may be
   // scheduled now; it waits for this grid to finish before touching memory.
@@ -653,11 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool v_fix = (kPaged || p.dense_vfix) && !is_k && n == v_fix_tile(sq);
         const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
         const CUtensorMap* sub_map = is_k ? &p.tmap_k_sub : (v_fix ? &p.tmap_v16 : &p.tmap_v_sub);
-        const int halves = is_k ? kKStagesPerTile : (kPair ? 1 : 2);
+        const int halves = is_k ? kKStagesPerTile : ((kPair || kFp8Pv) ? 1 : 2);
         for (int half = 0; half < halves; ++half) {
           if (!wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
           const uint32_t dst = stage_smem + st * kStageBytes;
-          const uint32_t bytes = is_k ? kKStageBytes : kStageBytes;  // per CTA
+          const uint32_t bytes = is_k ? kKStageBytes : (kFp8Pv ? kVStageBytesPv : kStageBytes);
           if (leader) ptx::mbar_arrive_expect_tx(bar(kBarFull + st), (kPair ? 2 : 1) * bytes);
           // Box geometry: first key, keys per box, chunks and their stride in
           // shared memory, first chunk.
@@ -694,7 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         kPair ? lbar(kBarFull + st) : bar(kBarFull + st), r0, rows,
                                         nb, chunk0, g, v_fix, pol_kv);
           }
-          if (!kPaged && v_fix)
+          if (kFp8Pv && !is_k)  // one box (128 keys, 256 or 128 channels, head g)
+            load(dst, &p.tmap_v, kBarFull + st, sq.kv_start + n * kBlockN,
+                 kPair ? 128 * static_cast<int>(rank) : 0, g, pol_kv);
+          else if (!kPaged && v_fix)
             issue_dense_v_pieces<kPair>(&p.tmap_v16, dst, kPair ? lbar(kBarFull + st) : bar(kBarFull + st),
                                         sq.kv_start, sq.kv_len, p.oob_row, r0, rows, nb, chunk0, g,
                                         pol_kv);
@@ -848,7 +869,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int vfix_tile = (kPaged || p.dense_vfix) ? v_fix_tile(p.batch.seq[w.seq]) : -1;
           const bool v_fix = (kPaged || p.dense_vfix) && w.n0 + j == vfix_tile;
           const int kr = p.batch.seq[w.seq].kv_len - vfix_tile * kBlockN;  // used when v_fix
-          if constexpr (kPair) {
+          if constexpr (kFp8Pv) {
+            // One stage: (this CTA's) channel rows of 128 key codes, K-major; P as E4M3
+            // in tensor memory (4 codes per column: 8 columns per 32-key k-step).
+            ptx::tc_fence_after();
+            const uint64_t vd = k_desc0 + ((st * kStageBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t a_tmem = tmem + kTmemP + 64u * b + 8u * kk;
+              if constexpr (kPair)
+                ptx::mma_ts_f8_pair(tmem + kTmemO, a_tmem, vd + ((32 * kk) >> 4), kIdescPV82,
+                                    (j | kk) != 0);
+              else
+                ptx::mma_ts_f8(tmem + kTmemO, a_tmem, vd + ((32 * kk) >> 4), kIdescPV8,
+                               (j | kk) != 0);
+            }
+            commit(kBarEmpty + st);
+            if (++st == kStages) { st = 0; phase ^= 1u; }
+          } else if constexpr (kPair) {
             // One stage: 128 keys x this CTA's 2 chunks of 64 columns (waited for above).
             ptx::tc_fence_after();
             if (v_fix) {
@@ -925,7 +963,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // for FP8 QK^T (the key's scale is applied per column below).
       float rowfac = sl2;
       if constexpr (kFp8) {
-        if (valid) rowfac = sl2 * __ldg(p.q_scale + qrow);
+        // A query vector of zeros has scale 0 and codes 0: its scores are all 0. The
+        // factor stays positive so that masked keys (-inf) stay -inf, not -inf * 0.
+        if (valid) rowfac = sl2 * fmaxf(__ldg(p.q_scale + qrow), 1e-30f);
       }
       float m_ref = kNegInf;  // max used in the exponent (base-2, scaled)
       float l = 0.0f;         // running row sum of p
@@ -969,17 +1009,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (key0 + c > pos) s[c] = kNegInf;
         }
+        // Row maximum: s[0..3], then s[4..123] eight at a time, then s[124..127].
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int c = 4; c < 128; c += 8) {
+        for (int c = 4; c < 124; c += 8) {
           mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
           mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
           mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
           mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
         }
+        mx0 = fmaxf(mx0, s[124]);
+        mx1 = fmaxf(mx1, s[125]);
+        mx2 = fmaxf(mx2, s[126]);
+        mx3 = fmaxf(mx3, s[127]);
         const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * rowfac;
         const float m_new = fmaxf(m_ref, m_tile);
-        const bool need = m_new > m_ref + kRescaleThreshold;
+        const bool need = m_new > m_ref + (kFp8Pv ? kRescaleThresholdPv : kRescaleThreshold);
         if (j == 0) {
           if (need) m_ref = m_new;  // O is overwritten by this unit's first PV
         } else if (__any_sync(0xffffffffu, need)) {
@@ -1002,10 +1047,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_st_wait();
         }
         const float m_use = (m_ref == kNegInf) ? 0.0f : m_ref;
-        uint32_t pk[64];
+        // BF16 P: two values per tensor-memory column; E4M3 P (quantised PV): four.
+        uint32_t pk[kFp8Pv ? 32 : 64];
         // p = 2^(s*scale*log2e - m): one packed FMA per pair, two ex2, one packed add.
         const uint64_t scale2 = ptx::f32x2(rowfac, rowfac);
-        const uint64_t neg_m2 = ptx::f32x2(-m_use, -m_use);
+        const float pofs = kFp8Pv ? kPScaleLog2Pv - m_use : -m_use;
+        const uint64_t neg_m2 = ptx::f32x2(pofs, pofs);
         uint64_t sum2 = ptx::f32x2(0.0f, 0.0f);
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
@@ -1014,7 +1061,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float e0 = ptx::ex2_approx(x0);
           const float e1 = ptx::ex2_approx(x1);
           sum2 = ptx::add_f32x2(sum2, ptx::f32x2(e0, e1));
-          pk[c] = ptx::pack_bf16x2(e0, e1);
+          if constexpr (kFp8Pv) {
+            const uint32_t h = ptx::cvt_e4m3x2(e0, e1);
+            pk[c >> 1] = (c & 1) ? (pk[c >> 1] | (h << 16)) : h;
+          } else {
+            pk[c] = ptx::pack_bf16x2(e0, e1);
+          }
         }
         float sum0, sum1;
         ptx::f32x2_split(sum2, sum0, sum1);
@@ -1026,7 +1078,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ptx::tc_fence_after();
         }
-        ptx::tmem_st_x64(lane_addr + kTmemP + 64u * b, pk);
+        if constexpr (kFp8Pv) ptx::tmem_st_x32(lane_addr + kTmemP + 64u * b, pk);
+        else ptx::tmem_st_x64(lane_addr + kTmemP + 64u * b, pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         arrive_leader(b ? kBarPFull1 : kBarPFull0);
@@ -1039,7 +1092,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-      const float lse2 = l > 0.0f ? m_ref + __log2f(l) : kNegInf;
+      // (Quantised PV: l sums 2^6 p, so the scale's exponent comes off.)
+      const float lse2 = l > 0.0f ? m_ref + __log2f(l) - (kFp8Pv ? kPScaleLog2Pv : 0.0f) : kNegInf;
+      // Output column factor: 1/l, times the channel's V scale for quantised PV.
+      auto col_factors = [&](int col0, float (&f)[32]) {
+        if constexpr (kFp8Pv) {
+          const float4* sv = reinterpret_cast<const float4*>(p.v_scale + kHeadDim * w.g + col0);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 x = __ldg(sv + i);
+            f[4 * i] = x.x * inv_l; f[4 * i + 1] = x.y * inv_l;
+            f[4 * i + 2] = x.z * inv_l; f[4 * i + 3] = x.w * inv_l;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = inv_l;
+        }
+      };
       // Stores go out through groups of 8 lanes: after transpose8_quads each lane
       // of a group holds one 16-byte quad of each of the group's 8 rows, so every
       // store instruction writes 128 contiguous bytes of 4 rows instead of 16
@@ -1069,13 +1138,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int h = 0; h < 2; ++h) {
             uint32_t o[32];
             ptx::tmem_ld_x32(lane_addr + kTmemO + c + 32 * h, o);
+            float f[32];
+            col_factors(c + 32 * h, f);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int i = 8 * q4;
               e[4 * h + q4] = make_uint4(
-                  ptx::pack_bf16x2(__uint_as_float(o[8 * q4]) * inv_l, __uint_as_float(o[8 * q4 + 1]) * inv_l),
-                  ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv_l, __uint_as_float(o[8 * q4 + 3]) * inv_l),
-                  ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv_l, __uint_as_float(o[8 * q4 + 5]) * inv_l),
-                  ptx::pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv_l, __uint_as_float(o[8 * q4 + 7]) * inv_l));
+                  ptx::pack_bf16x2(__uint_as_float(o[i]) * f[i], __uint_as_float(o[i + 1]) * f[i + 1]),
+                  ptx::pack_bf16x2(__uint_as_float(o[i + 2]) * f[i + 2], __uint_as_float(o[i + 3]) * f[i + 3]),
+                  ptx::pack_bf16x2(__uint_as_float(o[i + 4]) * f[i + 4], __uint_as_float(o[i + 5]) * f[i + 5]),
+                  ptx::pack_bf16x2(__uint_as_float(o[i + 6]) * f[i + 6], __uint_as_float(o[i + 7]) * f[i + 7]));
+            }
           }
           transpose8_quads(e, gl);
 #pragma unroll
@@ -1102,13 +1175,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 256; c += 32) {
           uint32_t o[32];
           ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
+          float f[32];
+          col_factors(c, f);
           uint4 e[8];
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4)
-            e[q4] = make_uint4(__float_as_uint(__uint_as_float(o[4 * q4]) * inv_l),
-                               __float_as_uint(__uint_as_float(o[4 * q4 + 1]) * inv_l),
-                               __float_as_uint(__uint_as_float(o[4 * q4 + 2]) * inv_l),
-                               __float_as_uint(__uint_as_float(o[4 * q4 + 3]) * inv_l));
+            e[q4] = make_uint4(__float_as_uint(__uint_as_float(o[4 * q4]) * f[4 * q4]),
+                               __float_as_uint(__uint_as_float(o[4 * q4 + 1]) * f[4 * q4 + 1]),
+                               __float_as_uint(__uint_as_float(o[4 * q4 + 2]) * f[4 * q4 + 2]),
+                               __float_as_uint(__uint_as_float(o[4 * q4 + 3]) * f[4 * q4 + 3]));
           transpose8_quads(e, gl);
 #pragma unroll
           for (int s_ = 0; s_ < 8; ++s_)
@@ -1416,14 +1491,16 @@ size_t fwd_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t prepare_fwd_kernel() {
   const void* kernels[] = {
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, false>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, false>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true, false>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true, false>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, true>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, true>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true, true>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true, true>)};
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, 2>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, 2>)};
   for (const void* f : kernels) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(kSmemAlloc));
@@ -1463,24 +1540,27 @@ cudaError_t max_active_pairs(int* pairs) {
   cudaLaunchConfig_t cfg = launch_config(dim3(2), dim3(kThreads), kSmemAlloc, true, nullptr, attr);
   cfg.attrs = attr + 1;  // occupancy of the cluster shape only
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, false, false>, &cfg);
+  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, false, 0>, &cfg);
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, bool fp8,
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, int fp8,
                        cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = launch_config(dim3(static_cast<unsigned>(grid)), dim3(kThreads),
                                                kSmemAlloc, pair, stream, attr);
+  if (fp8 == 2)  // quantised QK^T and PV (dense K/V)
+    return pair ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, 2>, p)
+                : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, 2>, p);
   const int which = (pair ? 4 : 0) | (paged ? 2 : 0) | (fp8 ? 1 : 0);
   switch (which) {
-    case 0: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, false>, p);
-    case 1: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, true>, p);
-    case 2: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, false>, p);
-    case 3: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, true>, p);
-    case 4: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, false>, p);
-    case 5: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, true>, p);
-    case 6: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, false>, p);
-    default: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, true>, p);
+    case 0: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, 0>, p);
+    case 1: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, 1>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, 0>, p);
+    case 3: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, 1>, p);
+    case 4: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, 0>, p);
+    case 5: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, 1>, p);
+    case 6: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, 0>, p);
+    default: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, 1>, p);
   }
 }
 

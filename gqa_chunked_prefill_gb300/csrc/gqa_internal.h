@@ -67,6 +67,10 @@ struct FwdParams {
   const float* k_scale;      // paged: one scale per cache row, [4][k_scale_stride], read by
   int k_scale_stride;        //   1-D bulk copies (16-key pieces are 64 bytes)
   const float* q_scale;      // [total q rows][24] FP32 query scales
+  // Quantised PV (kernels instantiated with kFp8 = 2): tmap_v holds V's E4M3 codes
+  // transposed, [4 heads][256 channels][v_stride keys] bytes, 3-D (key, channel,
+  // head), box (128 keys, 256 channels or a pair CTA's 128, 1 head), 128B swizzle.
+  const float* v_scale;      // [4][256] FP32 per-channel scales of V
   // Split merge inside the attention kernel (fused_merge != 0). Every split piece,
   // once its partial rows are stored, sets its flag merge_flag[slot * CTAs per
   // item + rank] to call_tag and then reads its item's other flags; a piece that
@@ -100,7 +104,8 @@ struct MergeParams {
 
 size_t fwd_smem_bytes();
 // grid = CTAs; with pair = true the CTAs form clusters of two (grid even).
-cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, bool fp8,
+// fp8: 0 BF16, 1 E4M3 QK^T, 2 E4M3 QK^T and PV (dense K/V only).
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, int fp8,
                        cudaStream_t stream);
 // Scale column of each key row for head-major key scales: sequence b of a packed
 // batch (rows row_begin[b] .. row_begin[b+1]-1) starts at column col_begin[b].
@@ -113,6 +118,10 @@ struct ScaleColumns {
 cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scale, int rows, int heads,
                                 int scale_stride, bool head_major, const ScaleColumns& cols,
                                 cudaStream_t stream);
+// E4M3 codes of V transposed to [4][256][v_stride] and per-(head, channel) scales
+// [4][256] (quantize_fp8.cu).
+cudaError_t launch_quantize_v_fp8(const void* v, void* codes, float* scale, int kv_len,
+                                  int v_stride, cudaStream_t stream);
 cudaError_t max_active_pairs(int* pairs);       // co-resident CTA pairs on this device
 // Split pieces one CTA (pair) may count for the fused merge: it remembers which
 // items it completed in a bitset of this many bits (the planner keeps every

@@ -651,20 +651,39 @@ gqa_status check_paged(const PagedKV& pkv, const std::vector<SeqIn>& seqs, bool 
   return GQA_OK;
 }
 
-// Quantised-QK^T inputs of a call: q and k are E4M3 codes with these scales.
+// Quantised-QK^T inputs of a call: q and k are E4M3 codes with these scales;
+// with v_scale set, v is also E4M3 codes, transposed ([4][256][v_stride]).
 struct Fp8Qk {
   const float* q_scale;  // [q_len][24]
   const float* k_scale;  // [4][k_scale_stride]
   int k_scale_stride;
+  const float* v_scale = nullptr;  // [4][256] per-channel scales (quantised PV)
+  int v_stride = 0;                // bytes between channel rows of the V codes
 };
 
-gqa_status check_fp8(const Fp8Qk& f8, int64_t key_rows, bool work) {
+// V codes of the quantised PV, [4 heads][256 channels][v_stride keys] bytes, as a
+// 3-D tensor (key, channel, head) of kv_len keys (keys past it read zeros); box
+// (128 keys, box_ch channels, 1 head) lands as box_ch rows of 128 bytes (K-major).
+bool encode_v_codes(CUtensorMap* map, const void* base, uint64_t kv_len, uint64_t v_stride,
+                    uint32_t box_ch) {
+  const cuuint64_t dims[3] = {kv_len, kHeadDim, static_cast<cuuint64_t>(kKvHeads)};
+  const cuuint64_t strides[2] = {v_stride, v_stride * kHeadDim};
+  const cuuint32_t box[3] = {kBlockN, box_ch, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box,
+                CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+gqa_status check_fp8(const Fp8Qk& f8, int64_t key_rows, bool work, bool pv) {
   if (f8.k_scale_stride < key_rows || f8.k_scale_stride % 4 != 0 ||
       static_cast<int64_t>(f8.k_scale_stride) * kKvHeads >= (int64_t{1} << 31))
     return GQA_ERR_SHAPE;
+  if (pv && (f8.v_stride < key_rows || f8.v_stride % 16 != 0 ||
+             static_cast<int64_t>(f8.v_stride) * kHeadDim * kKvHeads >= (int64_t{1} << 40)))
+    return GQA_ERR_SHAPE;
   if (!work) return GQA_OK;
-  if (!f8.q_scale || !f8.k_scale) return GQA_ERR_NULL;
-  if ((reinterpret_cast<uintptr_t>(f8.q_scale) & 3u) != 0 || misaligned(f8.k_scale))
+  if (!f8.q_scale || !f8.k_scale || (pv && !f8.v_scale)) return GQA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(f8.q_scale) & 3u) != 0 || misaligned(f8.k_scale) ||
+      (pv && misaligned(f8.v_scale)))
     return GQA_ERR_ALIGN;
   return GQA_OK;
 }
@@ -720,10 +739,13 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
   const uint32_t k_rows = pair ? 64 : kBlockN;
   const uint32_t k_chunks = io.f8 ? 2 : (pair ? 4 : 2);
   const uint32_t v_rows = pair ? kBlockN : 64, v_chunks = pair ? 2 : 4;
+  const bool fp8_pv = io.f8 && io.f8->v_scale;
   if (!encode_q(&p.tmap_q, io.q, static_cast<uint64_t>(total_q), qk)) return GQA_ERR_CUDA;
   if (!io.pkv) {
     if (!encode_kv(&p.tmap_k, io.k, kv_rows, k_rows, k_chunks, qk) ||
-        !encode_kv(&p.tmap_v, io.v, kv_rows, v_rows, v_chunks, kBf16))
+        !(fp8_pv ? encode_v_codes(&p.tmap_v, io.v, kv_rows,
+                                  static_cast<uint64_t>(io.f8->v_stride), pair ? 128 : 256)
+                 : encode_kv(&p.tmap_v, io.v, kv_rows, v_rows, v_chunks, kBf16)))
       return GQA_ERR_CUDA;
     if (seqs.size() > 1) {
       // A box past a sequence's last key would read the next sequence's values:
@@ -765,6 +787,7 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
     p.k_scale = io.f8->k_scale;
     p.k_scale_stride = io.f8->k_scale_stride;
     p.q_scale = io.f8->q_scale;
+    p.v_scale = io.f8->v_scale;
   }
   build_batch(seqs, plan.variant, &p.batch);
   const int workers = pair ? plan.grid / 2 : plan.grid;
@@ -812,7 +835,8 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return GQA_ERR_CUDA;
-  if (launch_fwd(p, plan.grid, pair, io.pkv != nullptr, io.f8 != nullptr, stream) != cudaSuccess)
+  if (launch_fwd(p, plan.grid, pair, io.pkv != nullptr, io.f8 ? (fp8_pv ? 2 : 1) : 0, stream) !=
+      cudaSuccess)
     return GQA_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return GQA_ERR_CUDA;
   if (plan.kernels_per_call == 2) {  // the separate merge pass
@@ -845,6 +869,8 @@ gqa_status run(const CallIO& io, const std::vector<SeqIn>& seqs, int total_q, in
   gqa_status st = validate_heads(n_q_heads, n_kv_heads, head_dim, io.scale);
   const bool work = total_q > 0;
   if (st == GQA_OK && work) st = check_pointers(io.q, io.k, io.v, io.out, io.lse);
+  if (st == GQA_OK && work && io.f8 && io.f8->v_scale && io.f8->v_stride % 16 != 0)
+    st = GQA_ERR_SHAPE;
   if (st == GQA_OK && io.pkv) st = check_paged(*io.pkv, seqs, work);
   if (st == GQA_OK && io.f8) {
     int64_t scale_cols = static_cast<int64_t>(io.pkv ? io.pkv->num_pages : 0) *
@@ -853,7 +879,9 @@ gqa_status run(const CallIO& io, const std::vector<SeqIn>& seqs, int total_q, in
       std::vector<SeqIn> tmp = seqs;
       scale_cols = key_scale_starts(&tmp);
     }
-    st = check_fp8(*io.f8, scale_cols, work);
+    st = check_fp8(*io.f8, scale_cols, work, io.f8->v_scale != nullptr);
+    // Quantised PV: one sequence, dense K/V (V's channel scales span the call's keys).
+    if (st == GQA_OK && io.f8->v_scale && (io.pkv || seqs.size() != 1)) st = GQA_ERR_UNSUPPORTED;
   }
   if (st != GQA_OK || !work) return st;
   std::vector<SeqIn> fp8_seqs;
@@ -1189,6 +1217,49 @@ gqa_status gqa_prefill_attn_paged_fp8qk_varlen_ex(
   const gqa::Fp8Qk f8{q_scale, k_scale, k_scale_stride};
   const gqa::CallIO io{q_fp8, k_cache_fp8, v_cache, out, lse, &pkv, &f8, scale};
   return gqa::run(io, seqs, total_q, 0, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
+}
+
+gqa_status gqa_quantize_v_fp8(const void* v, void* v_fp8t, float* v_scale, int kv_len,
+                              int n_kv_heads, int head_dim, int v_stride, void* stream) {
+  if (kv_len < 0 || v_stride < kv_len || v_stride % 16 != 0 ||
+      static_cast<int64_t>(v_stride) * gqa::kHeadDim * gqa::kKvHeads >= (int64_t{1} << 40))
+    return GQA_ERR_SHAPE;
+  if (n_kv_heads != gqa::kKvHeads || head_dim != gqa::kHeadDim) return GQA_ERR_UNSUPPORTED;
+  if (kv_len == 0) return GQA_OK;
+  if (!v || !v_fp8t || !v_scale) return GQA_ERR_NULL;
+  if (gqa::misaligned(v) || gqa::misaligned(v_fp8t) || gqa::misaligned(v_scale)) return GQA_ERR_ALIGN;
+  return gqa::launch_quantize_v_fp8(v, v_fp8t, v_scale, kv_len, v_stride,
+                                    static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GQA_OK
+             : GQA_ERR_CUDA;
+}
+
+gqa_status gqa_prefill_attn_fp8qkpv_ex(const void* q_fp8, const float* q_scale, const void* k_fp8,
+                                       const float* k_scale, int k_scale_stride,
+                                       const void* v_fp8t, const float* v_scale, int v_stride,
+                                       void* out, float* lse, int q_len, int kv_len,
+                                       int n_q_heads, int n_kv_heads, int head_dim, float scale,
+                                       void* stream, const gqa_prefill_opts* opts,
+                                       gqa_prefill_plan* plan_out) {
+  gqa::Fp8Qk f8{q_scale, k_scale, k_scale_stride};
+  f8.v_scale = v_scale;
+  f8.v_stride = v_stride;
+  if (!v_scale && q_len > 0) {
+    if (plan_out) std::memset(plan_out, 0, sizeof(*plan_out));
+    return GQA_ERR_NULL;
+  }
+  const gqa::CallIO io{q_fp8, k_fp8, v_fp8t, out, lse, nullptr, &f8, scale};
+  return gqa::run_one(io, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, stream, opts, plan_out);
+}
+
+gqa_status gqa_prefill_attn_fp8qkpv(const void* q_fp8, const float* q_scale, const void* k_fp8,
+                                    const float* k_scale, int k_scale_stride, const void* v_fp8t,
+                                    const float* v_scale, int v_stride, void* out, float* lse,
+                                    int q_len, int kv_len, int n_q_heads, int n_kv_heads,
+                                    int head_dim, float scale, void* stream) {
+  return gqa_prefill_attn_fp8qkpv_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v_fp8t,
+                                     v_scale, v_stride, out, lse, q_len, kv_len, n_q_heads,
+                                     n_kv_heads, head_dim, scale, stream, nullptr, nullptr);
 }
 
 gqa_status gqa_prefill_make_plan(int q_len, int kv_len, int n_q_heads, int n_kv_heads, int head_dim,

@@ -78,7 +78,105 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Per-channel quantisation of V for the quantised PV (same report's final
+// submission multiplies P by V in 8 bits; the scaling is not given). Reading:
+// channel c of KV head g over all kv_len keys is one vector, with s = max_j
+// |v[j][g][c]| / 448 and codes E4M3(v / s) under the rounding rules above. The
+// codes are stored transposed, [g][c][key] with a row stride of v_stride
+// bytes, so that a 128-key tile of V is a K-major operand (one 128-byte row of
+// keys per channel) for the kind::f8f6f4 MMA; the scale multiplies column c of
+// P.V after the product.
+//
+// Three passes: (1) amax: block b reduces keys [b*kAmaxKeys, ...) for all 1024
+// (head, channel) pairs, a thread per 4 channels (8 bytes of each key row:
+// coalesced 2 KB rows), then one atomicMax on the float bits per channel (|v|
+// >= 0, so the bits order like the values) into v_scale, cleared before;
+// (2) encode: a block per (128 keys, 32 channels) tile reads the tile's key
+// rows (64 bytes each), divides by s = amax / 448, and writes 32 channel rows
+// of 128 codes through shared memory; (3) v_scale = amax / 448 in place.
+constexpr int kAmaxKeys = 64;
+
+__global__ void __launch_bounds__(256) v_amax_kernel(const __nv_bfloat16* __restrict__ v,
+                                                     unsigned int* __restrict__ amax_bits,
+                                                     int kv_len) {
+  const int c4 = threadIdx.x;  // channels 4*c4 .. 4*c4+3 of the 1024 (head-major)
+  const int k0 = blockIdx.x * kAmaxKeys, k1 = min(kv_len, k0 + kAmaxKeys);
+  float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int j = k0; j < k1; ++j) {
+    const uint2 raw = reinterpret_cast<const uint2*>(v + static_cast<size_t>(j) * kKvHeads * kHeadDim)[c4];
+    m[0] = fmaxf(m[0], fabsf(__uint_as_float(raw.x << 16)));
+    m[1] = fmaxf(m[1], fabsf(__uint_as_float(raw.x & 0xffff0000u)));
+    m[2] = fmaxf(m[2], fabsf(__uint_as_float(raw.y << 16)));
+    m[3] = fmaxf(m[3], fabsf(__uint_as_float(raw.y & 0xffff0000u)));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) atomicMax(amax_bits + 4 * c4 + i, __float_as_uint(m[i]));
+}
+
+__global__ void __launch_bounds__(256) v_encode_kernel(const __nv_bfloat16* __restrict__ v,
+                                                       const unsigned int* __restrict__ amax_bits,
+                                                       uint8_t* __restrict__ codes, int kv_len,
+                                                       int v_stride) {
+  __shared__ uint8_t tile[32][128 + 16];  // [channel][key], rows padded against bank conflicts
+  const int key0 = blockIdx.x * 128;
+  const int ch0 = blockIdx.y * 32;  // of the 1024 (head, channel) pairs
+  // Read: 128 key rows of 32 channels (64 bytes): thread t takes key t/2, channels
+  // 16*(t%2) .. +15, for keys key0 .. key0+127.
+  const int t = threadIdx.x;
+  const int kr = t >> 1, half = t & 1;
+  const int key = key0 + kr;
+  if (key < kv_len) {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        v + static_cast<size_t>(key) * kKvHeads * kHeadDim + ch0 + 16 * half);
+    const uint4 a = src[0], b = src[1];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = 16 * half + 2 * i + h;
+        const float x = __uint_as_float(h ? (w[i] & 0xffff0000u) : (w[i] << 16));
+        const float s = __fdiv_rn(__uint_as_float(amax_bits[ch0 + c]), kE4m3Max);
+        tile[c][kr] = s > 0.0f ? static_cast<uint8_t>(ptx::cvt_e4m3x2(__fdiv_rn(x, s), 0.0f) & 0xffu)
+                               : 0;
+      }
+    }
+  }
+  __syncthreads();
+  // Write: 32 channel rows of up to 128 codes; thread t: channel t/8, 16 keys.
+  const int c = t >> 3, part = t & 7;
+  const int g = (ch0 + c) / kHeadDim, d = (ch0 + c) % kHeadDim;
+  const int kk = key0 + 16 * part;
+  if (kk < kv_len) {
+    uint8_t* dst = codes + (static_cast<size_t>(g) * kHeadDim + d) * v_stride + kk;
+    if (kk + 16 <= kv_len) {
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&tile[c][16 * part]);
+    } else {
+      for (int i = 0; i < kv_len - kk; ++i) dst[i] = tile[c][16 * part + i];
+    }
+  }
+}
+
+__global__ void v_scale_kernel(float* __restrict__ scale) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < kKvHeads * kHeadDim) scale[i] = __fdiv_rn(scale[i], kE4m3Max);  // amax bits -> s
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_v_fp8(const void* v, void* codes, float* scale, int kv_len,
+                                  int v_stride, cudaStream_t stream) {
+  if (kv_len == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(scale, 0, kKvHeads * kHeadDim * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  auto* amax = reinterpret_cast<unsigned int*>(scale);
+  v_amax_kernel<<<(kv_len + kAmaxKeys - 1) / kAmaxKeys, 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(v), amax, kv_len);
+  v_encode_kernel<<<dim3((kv_len + 127) / 128, kKvHeads * kHeadDim / 32), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(v), amax, static_cast<uint8_t*>(codes), kv_len, v_stride);
+  v_scale_kernel<<<(kKvHeads * kHeadDim + 255) / 256, 256, 0, stream>>>(scale);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scale, int rows, int heads,
                                 int scale_stride, bool head_major, const ScaleColumns& cols,

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 9
+#define GQA_PREFILL_ABI_VERSION 10
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -405,6 +405,45 @@ gqa_status gqa_prefill_attn_paged_fp8qk_varlen_ex(
     int num_pages, int page_size, void* out, float* lse, const int32_t* cu_seqlens_q,
     const int32_t* kv_lens, int batch, int n_q_heads, int n_kv_heads, int head_dim, float scale,
     void* stream, const gqa_prefill_opts* opts, gqa_prefill_plan* plan_out);
+
+/*
+ * Quantised PV (the INT8 QK MMAC page, §6: the final submission multiplied P by V
+ * in 8 bits as well, without saying how V or P are scaled). Reading for GB300's
+ * FP8 tensor path:
+ *   - V gets one symmetric scale per (KV head, channel) over the call's kv_len
+ *     keys: s_v[g][c] = max_j |v[j][g][c]| / 448, codes E4M3(v / s_v) (the
+ *     rounding rules of gqa_quantize_q_fp8, along the key axis); the scale
+ *     multiplies column c of P.V after the product;
+ *   - P is rounded to E4M3 as the MMA operand (stored as 2^6 * p, p at most 4
+ *     times the running maximum, so it never saturates), while the softmax
+ *     normaliser and the LSE keep the FP32 probabilities.
+ * The result approximates the attention of the DEQUANTISED query, keys and
+ * values; rounding P moves an output element by at most
+ * sum_j (2^-4 p_j + 2^-16) |v_j| / sum_j p_j (p_j = exp(s_j - max s)).
+ *
+ * gqa_quantize_v_fp8: v BF16 [kv_len][4][256] -> v_fp8t E4M3 [4][256][v_stride]
+ *   (channel rows of key codes, TRANSPOSED so that a 128-key tile is a K-major
+ *   MMA operand; v_stride >= kv_len, a multiple of 16; entries past kv_len are
+ *   not written), v_scale FP32 [4][256]. Asynchronous on `stream` (a memset and
+ *   three small kernels). All of one call's keys share the channel scales.
+ * gqa_prefill_attn_fp8qkpv[_ex]: gqa_prefill_attn_fp8qk with V given as those
+ *   codes and scales. One sequence, dense K/V (GQA_ERR_UNSUPPORTED otherwise);
+ *   out, lse, options and plan as gqa_prefill_attn_fp8qk[_ex].
+ */
+gqa_status gqa_quantize_v_fp8(const void* v, void* v_fp8t, float* v_scale, int kv_len,
+                              int n_kv_heads, int head_dim, int v_stride, void* stream);
+gqa_status gqa_prefill_attn_fp8qkpv(const void* q_fp8, const float* q_scale, const void* k_fp8,
+                                    const float* k_scale, int k_scale_stride, const void* v_fp8t,
+                                    const float* v_scale, int v_stride, void* out, float* lse,
+                                    int q_len, int kv_len, int n_q_heads, int n_kv_heads,
+                                    int head_dim, float scale, void* stream);
+gqa_status gqa_prefill_attn_fp8qkpv_ex(const void* q_fp8, const float* q_scale, const void* k_fp8,
+                                       const float* k_scale, int k_scale_stride,
+                                       const void* v_fp8t, const float* v_scale, int v_stride,
+                                       void* out, float* lse, int q_len, int kv_len,
+                                       int n_q_heads, int n_kv_heads, int head_dim, float scale,
+                                       void* stream, const gqa_prefill_opts* opts,
+                                       gqa_prefill_plan* plan_out);
 
 /* Static description of a status code (never NULL). */
 const char* gqa_status_string(gqa_status status);

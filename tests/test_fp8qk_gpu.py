@@ -258,3 +258,21 @@ def test_paged_fp8qk_varlen_matches_dense(cuda_device, page_size, variant):
     assert gqa.gqa_prefill_poll() == 0
     assert plan_p == plan_d
     assert torch.equal(out_p, out_d) and torch.equal(lse_p, lse_d)
+
+
+@pytest.mark.parametrize("variant", [1, 2])
+def test_fp8qk_zero_query_gives_the_mean_of_visible_v(cuda_device, variant):
+    """A query of zeros quantises to scale 0 and codes 0: all its scores are 0, so
+    its output is the mean of the visible V rows and its LSE ln(visible keys). (Its
+    masked keys must stay at -inf: a zero factor must not turn them into NaN.)"""
+    q, k, v = make_qkv(30, 500, seed=43)
+    q[::3] = 0
+    out, lse, _ = run_fp8(q, k, v, SCALE, force_variant=variant)
+    ref_o, ref_l = oracle_fp8(q, k, v, SCALE)
+    check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
+                "fp8 zero query")
+    vv = v.double().numpy()
+    for t in (0, 3, 27):
+        want = np.repeat(vv[:470 + t + 1].mean(axis=0), 6, axis=0)
+        assert np.allclose(out[t].double().cpu().numpy(), want, rtol=2 ** -8, atol=1e-4)
+        assert np.allclose(lse[t].cpu().numpy(), np.log(470 + t + 1), atol=1e-5)
