@@ -553,7 +553,7 @@ def main():
         del kc, vc, table
 
     # ---- the same workload with quantised QK^T (E4M3 codes + per-vector scales) ------
-    fp8 = None
+    fp8 = fp8pv = None
     if not args.no_fp8:
         stride = -(-w.kv_len // 4) * 4
         q8 = torch.empty(q.shape, dtype=torch.uint8, device=dev)
@@ -631,6 +631,38 @@ def main():
         qk_ms, k_rot = rotating_us(k_copy_call, k.numel() * 2)
         q_bytes = q.numel() * 3 + w.q_len * w.n_q_heads * 4   # BF16 in, E4M3 codes + scales out
         k_bytes = k.numel() * 3 + w.kv_len * w.n_kv_heads * 4
+        # quantised PV as well: E4M3 V (per-channel scales, codes transposed) and E4M3 P
+        vstride = -(-w.kv_len // 16) * 16
+        v8 = torch.empty((w.n_kv_heads, w.head_dim, vstride), dtype=torch.uint8, device=dev)
+        vs8 = torch.empty((w.n_kv_heads, w.head_dim), dtype=torch.float32, device=dev)
+        gqa.gqa_quantize_v_fp8(v, v8, vs8, w.kv_len, w.n_kv_heads, w.head_dim, vstride,
+                               stream=stream)
+
+        def pvcall(events=None):
+            return gqa.gqa_prefill_attn_fp8qkpv_ex(
+                q8, qs, k8, ks, stride, v8, vs8, vstride, out, lse, w.q_len, w.kv_len,
+                w.n_q_heads, w.n_kv_heads, w.head_dim, w.scale, stream=stream,
+                fwd_events=events)[1]
+
+        for _ in range(3):
+            flush.zero_()
+            pvplan = pvcall()
+        pv_ms, pv_fwd = timed(pvcall, f_steps, with_fwd=True)
+        if gqa.gqa_prefill_poll(stream) != 0:
+            raise RuntimeError("device-side error during the FP8 PV steps")
+        pv_ms = max_over_ranks(pv_ms, pg, dev)
+        qv_ms, v_rot = rotating_us(
+            lambda r: (lambda src=(v if r == 0 else v.clone()): gqa.gqa_quantize_v_fp8(
+                src, v8, vs8, w.kv_len, w.n_kv_heads, w.head_dim, vstride, stream=stream)),
+            v.numel() * 2)
+        fp8pv = {"steps": f_steps, "value": round(job_throughput(world, flops, pv_ms), 2),
+                 "unit": UNIT, "ms_per_step": round(pv_ms, 4), "kernel_ms": round(pv_fwd, 4),
+                 "kernels_per_call": pvplan["kernels_per_call"],
+                 "quantize_v_us": round(qv_ms * 1e3, 1),
+                 "note": "QK^T and PV on E4M3 (kind::f8f6f4): Q, K per-vector scales, V "
+                         "per-(KV head, channel) scales, P rounded to E4M3; V quantisation "
+                         f"timed apart on {v_rot} rotating copies"}
+        del v8
         fp8 = {"steps": f_steps, "value": round(job_throughput(world, flops, f_ms), 2),
                "unit": UNIT, "ms_per_step": round(f_ms, 4), "kernel_ms": round(f_fwd, 4),
                "kernels_per_call": fplan["kernels_per_call"],
@@ -786,6 +818,13 @@ def main():
         fp8["roofline"] = {"bound": "tensor", "achieved": round(f_ach, 2), "peak": round(mixed, 1),
                            "unit": "TFLOP/s", "frac": round(f_ach / mixed, 4),
                            "peak_source": f"{peak_kind} bf16_tflops: QK^T at 2x, PV at 1x"}
+    if fp8pv:
+        # both halves at the FP8 rate: measured BF16 x 2 (the nominal FP8:BF16 ratio)
+        pv_ach = flops / (fp8pv["kernel_ms"] * 1e-3) / 1e12
+        fp8pv["roofline"] = {"bound": "tensor", "achieved": round(pv_ach, 2),
+                             "peak": round(2.0 * peak, 1), "unit": "TFLOP/s",
+                             "frac": round(pv_ach / (2.0 * peak), 4),
+                             "peak_source": f"{peak_kind} bf16_tflops x 2 (QK^T and PV in E4M3)"}
     known = KNOWN_TRAFFIC.get(w.name)
     traffic = known["bytes"] if known and known["kernel_sha256"] == kernel_source_sha() else None
 
@@ -842,6 +881,7 @@ def main():
         "gpu_launches": args.steps * plan["kernels_per_call"],
         "paged": paged,
         "fp8qk": fp8,
+        "fp8qkpv": fp8pv,
         "varlen": varlen,
         "decode": decode,
         "clocks": clocks,

@@ -42,7 +42,7 @@ class PrefillOpts(ctypes.Structure):
                 ("wait_timeout_us", ctypes.c_uint32),
                 ("fwd_event_begin", ctypes.c_void_p), ("fwd_event_end", ctypes.c_void_p),
                 ("test_withhold_q", ctypes.c_int), ("force_variant", ctypes.c_int),
-                ("merge_mode", ctypes.c_int)]
+                ("reserved", ctypes.c_int * 1)]
 
 
 class PrefillPlan(ctypes.Structure):
@@ -50,7 +50,7 @@ class PrefillPlan(ctypes.Structure):
                 ("head_rounds", ctypes.c_int), ("tail_items", ctypes.c_int),
                 ("tail_splits", ctypes.c_int), ("n_units", ctypes.c_int), ("grid", ctypes.c_int),
                 ("kernels_per_call", ctypes.c_int), ("variant", ctypes.c_int),
-                ("fused_merge", ctypes.c_int), ("total_tiles", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("total_tiles", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
                 ("est_makespan_tiles", ctypes.c_int64)]
 
     def as_dict(self):
@@ -189,11 +189,11 @@ def gqa_prefill_attn_noalloc(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_h
 
 def gqa_prefill_attn_ex(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale,
                         stream=None, force_splits=0, force_grid=0, force_variant=0,
-                        wait_timeout_us=0, fwd_events=None, test_withhold_q=False, merge_mode=0, check=True):
+                        wait_timeout_us=0, fwd_events=None, test_withhold_q=False, check=True):
     """fwd_events: optional (begin, end) torch.cuda.Event pair recorded around the
     attention kernel itself (not the split merge)."""
     opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
-                 test_withhold_q, merge_mode)
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), q_len, kv_len,
                                  n_q_heads, n_kv_heads, head_dim, scale, _stream(stream),
@@ -203,13 +203,10 @@ def gqa_prefill_attn_ex(q, k, v, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
     return rc, plan.as_dict()
 
 
-def _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, test_withhold_q,
-          merge_mode=0):
-    """merge_mode: 0 planner, 1 split items merged inside the attention kernel, 2 by a
-    separate merge kernel."""
+def _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events, test_withhold_q):
     opts = PrefillOpts(force_splits=force_splits, force_grid=force_grid,
                        wait_timeout_us=wait_timeout_us, test_withhold_q=1 if test_withhold_q else 0,
-                       force_variant=force_variant, merge_mode=merge_mode)
+                       force_variant=force_variant)
     if fwd_events is not None:
         opts.fwd_event_begin = fwd_events[0].cuda_event
         opts.fwd_event_end = fwd_events[1].cuda_event
@@ -232,9 +229,9 @@ def gqa_prefill_attn_paged(q, k_cache, v_cache, block_table, num_pages, page_siz
 def gqa_prefill_attn_paged_ex(q, k_cache, v_cache, block_table, num_pages, page_size, out, lse,
                               q_len, kv_len, n_q_heads, n_kv_heads, head_dim, scale, stream=None,
                               force_splits=0, force_grid=0, force_variant=0, wait_timeout_us=0,
-                              fwd_events=None, test_withhold_q=False, merge_mode=0, check=True):
+                              fwd_events=None, test_withhold_q=False, check=True):
     opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
-                 test_withhold_q, merge_mode)
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_paged_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                        num_pages, page_size, _ptr(out), _ptr(lse), q_len, kv_len,
@@ -279,9 +276,9 @@ def gqa_prefill_attn_fp8qk(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v, ou
 def gqa_prefill_attn_fp8qk_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, v, out, lse, q_len,
                               kv_len, n_q_heads, n_kv_heads, head_dim, scale, stream=None,
                               force_splits=0, force_grid=0, force_variant=0, wait_timeout_us=0,
-                              fwd_events=None, test_withhold_q=False, merge_mode=0, check=True):
+                              fwd_events=None, test_withhold_q=False, check=True):
     opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
-                 test_withhold_q, merge_mode)
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_fp8qk_ex(_ptr(q_fp8), _ptr(q_scale), _ptr(k_fp8), _ptr(k_scale),
                                        k_scale_stride, _ptr(v), _ptr(out), _ptr(lse), q_len,
@@ -319,9 +316,9 @@ def gqa_prefill_attn_fp8qkpv_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_stride, 
                                 v_stride, out, lse, q_len, kv_len, n_q_heads, n_kv_heads,
                                 head_dim, scale, stream=None, force_splits=0, force_grid=0,
                                 force_variant=0, wait_timeout_us=0, fwd_events=None,
-                                test_withhold_q=False, merge_mode=0, check=True):
+                                test_withhold_q=False, check=True):
     opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
-                 test_withhold_q, merge_mode)
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_fp8qkpv_ex(_ptr(q_fp8), _ptr(q_scale), _ptr(k_fp8), _ptr(k_scale),
                                          k_scale_stride, _ptr(v_fp8t), _ptr(v_scale), v_stride,
@@ -342,12 +339,12 @@ def _host_i32(xs):
 def gqa_prefill_attn_varlen_ex(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k, n_q_heads,
                                n_kv_heads, head_dim, scale, stream=None, force_splits=0,
                                force_grid=0, force_variant=0, wait_timeout_us=0, fwd_events=None,
-                               test_withhold_q=False, merge_mode=0, check=True):
+                               test_withhold_q=False, check=True):
     """cu_seqlens_q / cu_seqlens_k: HOST sequences of batch + 1 ints (lists or arrays)."""
     cq, pq = _host_i32(cu_seqlens_q)
     ck, pk = _host_i32(cu_seqlens_k)
     opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
-                 test_withhold_q, merge_mode)
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_varlen_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), pq, pk,
                                         len(cu_seqlens_q) - 1, n_q_heads, n_kv_heads, head_dim,
@@ -374,13 +371,13 @@ def gqa_prefill_attn_paged_varlen_ex(q, k_cache, v_cache, block_table, bt_stride
                                      page_size, out, lse, cu_seqlens_q, kv_lens, n_q_heads,
                                      n_kv_heads, head_dim, scale, stream=None, force_splits=0,
                                      force_grid=0, force_variant=0, wait_timeout_us=0,
-                                     fwd_events=None, test_withhold_q=False, merge_mode=0, check=True):
+                                     fwd_events=None, test_withhold_q=False, check=True):
     """block_table: DEVICE int32 [batch, bt_stride]; cu_seqlens_q (batch + 1) and kv_lens
     (batch): HOST ints."""
     cq, pq = _host_i32(cu_seqlens_q)
     kl, pk = _host_i32(kv_lens)
     opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
-                 test_withhold_q, merge_mode)
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_paged_varlen_ex(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), bt_stride, num_pages, page_size,
@@ -430,11 +427,11 @@ def gqa_prefill_attn_fp8qk_varlen_ex(q_fp8, q_scale, k_fp8, k_scale, k_scale_str
                                      cu_seqlens_q, cu_seqlens_k, n_q_heads, n_kv_heads, head_dim,
                                      scale, stream=None, force_splits=0, force_grid=0,
                                      force_variant=0, wait_timeout_us=0, fwd_events=None,
-                                     test_withhold_q=False, merge_mode=0, check=True):
+                                     test_withhold_q=False, check=True):
     cq, pq = _host_i32(cu_seqlens_q)
     ck, pk = _host_i32(cu_seqlens_k)
     opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
-                 test_withhold_q, merge_mode)
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_fp8qk_varlen_ex(
         _ptr(q_fp8), _ptr(q_scale), _ptr(k_fp8), _ptr(k_scale), k_scale_stride, _ptr(v),
@@ -450,11 +447,11 @@ def gqa_prefill_attn_paged_fp8qk_varlen_ex(q_fp8, q_scale, k_cache_fp8, k_scale,
                                            out, lse, cu_seqlens_q, kv_lens, n_q_heads, n_kv_heads,
                                            head_dim, scale, stream=None, force_splits=0,
                                            force_grid=0, force_variant=0, wait_timeout_us=0,
-                                           fwd_events=None, test_withhold_q=False, merge_mode=0, check=True):
+                                           fwd_events=None, test_withhold_q=False, check=True):
     cq, pq = _host_i32(cu_seqlens_q)
     kl, pk = _host_i32(kv_lens)
     opts = _opts(force_splits, force_grid, force_variant, wait_timeout_us, fwd_events,
-                 test_withhold_q, merge_mode)
+                 test_withhold_q)
     plan = PrefillPlan()
     rc = lib.gqa_prefill_attn_paged_fp8qk_varlen_ex(
         _ptr(q_fp8), _ptr(q_scale), _ptr(k_cache_fp8), _ptr(k_scale), k_scale_stride,

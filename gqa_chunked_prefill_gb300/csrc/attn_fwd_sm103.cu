@@ -85,9 +85,6 @@ enum BarId : uint32_t {
   kBarPvDone1,
   kBarOFree,                    // epilogue finished reading O (128 arrivals)
   kBarDrain,                    // MMA warp's final drain
-  kBarMerge0,                   // [2] fused split merge: partial rows staged (bulk-copy tx)
-  kBarMerge1,
-  kBarPartDone,                 // fused split merge: this CTA's partial rows stored (128 arrivals)
   kBarScFull,                   // [kScSlots] FP8 QK^T: key scales of a tile loaded (TMA tx)
   kBarScEmpty = kBarScFull + 8, // [kScSlots] this CTA's softmax done with them (128 arrivals)
   kNumBars = kBarScEmpty + 8
@@ -98,16 +95,7 @@ constexpr int kScSlots = 8;
 constexpr uint32_t kScSlotBytes = 128 * 4;
 constexpr uint32_t kOffScales = kOffQ + 2 * kQChunkBytes;
 constexpr uint32_t kOffTmemSlot = kOffBars + kNumBars * 8;
-constexpr uint32_t kOffAbort = kOffTmemSlot + 4;       // a role gave up (time-out): no merges
-constexpr uint32_t kOffMergeBits = kOffTmemSlot + 16;  // split pieces this CTA completed last
-constexpr uint32_t kSmemUsed = kOffMergeBits + kMaxFusedSplitPieces / 8;
-// Fused split merge, run after the CTA's last piece when the Q region and the
-// stage ring are free: two staging buffers of partial rows, every piece's
-// weight for every row, and the rows' inverse weight sums.
-constexpr uint32_t kMergeBufBytes = 96 * 1024;
-constexpr uint32_t kOffMergeWts = 2 * kMergeBufBytes;            // float [48 pieces][126 rows]
-constexpr uint32_t kOffMergeInv = kOffMergeWts + 48 * 128 * 4;   // float [128]
-static_assert(kOffMergeInv + 128 * 4 <= kOffBars, "merge staging overlaps the barriers");
+constexpr uint32_t kSmemUsed = kOffTmemSlot + 16;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base up to 1024
 
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false, false);
@@ -304,204 +292,15 @@ __device__ __forceinline__ void transpose8_quads(uint4 (&e)[8], int j) {
   }
 }
 
-// Fused split merge, step 1 (one thread per piece, once the piece's 128 threads
-// have stored their partial rows): set this piece's flag to the call's tag and
-// tell whether every piece of the item has set its own. The release fence
-// publishes the CTA's partial rows before the flag (the other threads' stores
-// are ordered before it by the CTA barrier this thread waited on; the fence is
-// cumulative). Between the flag store and the loads of the other flags sits a
-// sequentially consistent fence, so of any pieces that finish together at least
-// one sees all the flags set; of those, the one that claims the item merges it.
-// A flag left by an earlier call holds 0 (cleared by its merger) or that call's
-// tag. No load waits for another CTA; the piece count is at most 48.
-__device__ __noinline__ bool flag_piece_done(const FwdParams& p, const Schedule& sc, int G, int j,
-                                             int slot, uint32_t rank, int cpi) {
-  unsigned long long* flags = p.merge_flag;
-  const unsigned long long tag = p.call_tag;
-  ptx::fence_acq_rel_gpu();
-  ptx::st_relaxed_gpu_u64(flags + static_cast<size_t>(slot) * cpi + rank, tag);
-  ptx::fence_sc_gpu();
-  int x_lo;
-  const int n = tail_item_pieces(sc, p.tail.v, G, j, x_lo);
-  bool all = true;
-#pragma unroll 8
-  for (int s = 0; s < n; ++s)
-    all &= ptx::ld_relaxed_gpu_u64(flags + static_cast<size_t>(tail_piece_slot(sc, p.tail.v, G, j,
-                                                                               x_lo, s)) * cpi +
-                                   rank) == tag;
-  if (!all) return false;
-  // Pieces that finish together may all see every flag set: they race for the
-  // item's claim word (first piece's flag slot + the flag area's second half),
-  // and only the one whose CAS installs the tag merges. The merger clears it.
-  unsigned long long* claim = flags + p.merge_claim_offset +
-                              static_cast<size_t>(tail_piece_slot(sc, p.tail.v, G, j, x_lo, 0)) *
-                                  cpi + rank;
-  const unsigned long long seen = ptx::ld_relaxed_gpu_u64(claim);
-  if (seen == tag || atomicCAS(claim, seen, tag) != seen) return false;
-  ptx::fence_acq_rel_gpu();  // acquire: the other pieces' rows are visible
-  return true;
-}
-
-// Fused split merge, step 2 (all threads of the CTA, after its last piece): rows
-// of rank `rank` of tail item j, merged from its n pieces' partials in KV order:
-// lse = log2 sum_s 2^{lse_s}, out = sum_s 2^{lse_s - lse} O_s (fixed order, so the
-// result does not depend on which CTA merges). First every piece's LSE of every
-// live row is loaded at once (n * rows <= 48 * 126 values, spread over the
-// threads) and turned into weights in shared memory; the partial rows then go
-// through two 96 KB staging buffers by bulk copies (one thread copies chunk c+1
-// while all threads reduce chunk c), in one of two shapes: row chunks (all
-// pieces' rows [r0, r0 + rc), for items of many rows: a few large copies) or,
-// when the rows are few (decode-sized chunks) and the pieces many, piece chunks
-// (all rows of pieces [s0, s0 + g), accumulated in registers). `mphase` holds the
-// two staging barriers' parities across calls. Returns false if a wait gave up.
-__device__ __noinline__ bool merge_item(const FwdParams& p, const Schedule& sc, int G, int j,
-                                        uint32_t rank, int cpi, uint8_t* smem, uint32_t sbase,
-                                        uint32_t bar0, uint32_t& mphase) {
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  int seq, qt, g;
-  item_of(p.batch, sc.head_items + j, seq, qt, g);
-  const SeqGeo& sq = p.batch.seq[seq];
-  const int tok0 = p.batch.tok_per_item * qt + kTokPerTile * static_cast<int>(rank);
-  const int rows = min(kTokPerTile * kGroup, kGroup * (sq.q_len - tok0));
-  if (rows <= 0) return true;
-  int x_lo;
-  const int n = tail_item_pieces(sc, p.tail.v, G, j, x_lo);
-  if (n > kMaxFusedItemPieces) {  // the planner never fuses such items
-    atomicExch(p.status, static_cast<int>(GQA_ERR_BOUNDS));
-    return true;
-  }
-  float* wsm = reinterpret_cast<float*>(smem + kOffMergeWts);  // [n][rows] LSE, then weights
-  float* inv = reinterpret_cast<float*>(smem + kOffMergeInv);  // [rows]
-  auto prow0 = [&](int s) {  // first partial row of piece s for this CTA's rows
-    return (static_cast<size_t>(tail_piece_slot(sc, p.tail.v, G, j, x_lo, s)) * cpi + rank) *
-           kRowsPerTile;
-  };
-  auto out_row = [&](int r) {
-    return static_cast<size_t>(sq.q_start + tok0 + r / kGroup) * kQHeads + kGroup * g + r % kGroup;
-  };
-  // Staging plan: row chunks of rc rows (all n pieces), or piece chunks of gp pieces.
-  const bool by_piece = rows <= 24 && n * rows > 96;
-  const int rc = by_piece ? rows : max(1, min(rows, 96 / n));
-  const int gp = by_piece ? max(1, 96 / rows) : n;
-  const int chunks = by_piece ? (n + gp - 1) / gp : (rows + rc - 1) / rc;
-  auto issue = [&](int c) {  // thread 0: chunk c into buffer c & 1
-    const int b = c & 1;
-    const uint32_t dst = sbase + b * kMergeBufBytes;
-    const int s0 = by_piece ? c * gp : 0, s1 = by_piece ? min(n, s0 + gp) : n;
-    const int r0 = by_piece ? 0 : c * rc, nr = by_piece ? rows : min(rc, rows - r0);
-    ptx::fence_proxy_async_global();  // the pieces' generic-proxy stores, seen via the flags
-    ptx::fence_proxy_async_smem();    // earlier generic reads of this buffer come first
-    const uint64_t pol = ptx::policy_evict_first();
-    uint32_t bytes = 0;
-    for (int s = s0; s < s1; ++s)
-      if (row_ok(static_cast<long long>(prow0(s) + r0 + nr - 1), p.part_rows, p.status))
-        bytes += nr * 1024u;
-    ptx::mbar_arrive_expect_tx(bar0 + 8u * b, bytes);
-    for (int s = s0; s < s1; ++s) {
-      const size_t pr = prow0(s) + r0;
-      if (!kCheckBounds || static_cast<long long>(pr + nr - 1) < p.part_rows)
-        ptx::bulk_load(dst + (s - s0) * nr * 1024u, p.part_o + pr * kHeadDim, nr * 1024u,
-                       bar0 + 8u * b, pol);
-    }
-  };
-  if (tid == 0) issue(0);
-  // Every piece's LSE of every live row (independent loads, a few per thread).
-  for (int i0 = tid; i0 < n * rows; i0 += 4 * nthr) {
-    float v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * nthr;
-      v[u] = i < n * rows ? __ldcg(p.part_lse + prow0(i / rows) + i % rows) : 0.0f;
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (i0 + u * nthr < n * rows) wsm[i0 + u * nthr] = v[u];
-  }
-  __syncthreads();
-  if (tid < rows) {  // the row's weights 2^{lse_s - max} (in place), their sum, its LSE
-    float mx = kNegInf;
-    for (int s = 0; s < n; ++s) mx = fmaxf(mx, wsm[s * rows + tid]);
-    const float m_use = (mx == kNegInf) ? 0.0f : mx;
-    float wsum = 0.0f;
-    for (int s = 0; s < n; ++s) {
-      const float w = ptx::ex2_approx(wsm[s * rows + tid] - m_use);
-      wsm[s * rows + tid] = w;
-      wsum += w;
-    }
-    inv[tid] = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-    const size_t orow = out_row(tid);
-    if (p.lse != nullptr && row_ok(static_cast<long long>(orow), p.out_rows, p.status))
-      p.lse[orow] = wsum > 0.0f ? (m_use + __log2f(wsum)) * kLn2 : kNegInf;
-  }
-  __syncthreads();
-  auto store = [&](int r, int q4, float4 acc) {
-    const float iv = inv[r];
-    const size_t orow = out_row(r);
-    if (row_ok(static_cast<long long>(orow), p.out_rows, p.status)) {
-      uint2 o;
-      o.x = ptx::pack_bf16x2(acc.x * iv, acc.y * iv);
-      o.y = ptx::pack_bf16x2(acc.z * iv, acc.w * iv);
-      *reinterpret_cast<uint2*>(p.out + orow * kHeadDim + 4 * q4) = o;
-    }
-  };
-  constexpr int kAccQuads = 8;  // piece chunks: rows <= 24, so rows * 64 quads <= 8 per thread
-  float4 acc[kAccQuads];
-#pragma unroll
-  for (int k = 0; k < kAccQuads; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  bool ok = true;
-  for (int c = 0; c < chunks; ++c) {
-    const int b = c & 1;
-    if (tid == 0 && c + 1 < chunks) issue(c + 1);  // buffer b ^ 1 was freed by chunk c - 1
-    ok = __syncthreads_and(ok && wait_bar(bar0 + 8u * b, (mphase >> b) & 1u, p)) != 0;
-    mphase ^= 1u << b;
-    if (!ok) return false;
-    const uint32_t buf = sbase + b * kMergeBufBytes;
-    if (by_piece) {
-      const int s0 = c * gp, s1 = min(n, s0 + gp);
-#pragma unroll
-      for (int k = 0; k < kAccQuads; ++k) {
-        const int idx = tid + k * nthr;
-        if (idx >= rows * 64) break;
-        const int r = idx >> 6, q4 = idx & 63;
-        for (int s = s0; s < s1; ++s) {
-          const float w = wsm[s * rows + r];
-          const float4 v = ptx::ld_shared_f4(buf + ((s - s0) * rows + r) * 1024u + q4 * 16u);
-          acc[k].x += w * v.x; acc[k].y += w * v.y; acc[k].z += w * v.z; acc[k].w += w * v.w;
-        }
-      }
-    } else {
-      const int r0 = c * rc, nr = min(rc, rows - r0);
-      for (int idx = tid; idx < nr * 64; idx += nthr) {
-        const int t = idx >> 6, q4 = idx & 63;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < n; ++s) {
-          const float w = wsm[s * rows + r0 + t];
-          const float4 v = ptx::ld_shared_f4(buf + (s * nr + t) * 1024u + q4 * 16u);
-          a.x += w * v.x; a.y += w * v.y; a.z += w * v.z; a.w += w * v.w;
-        }
-        store(r0 + t, q4, a);
-      }
-    }
-    __syncthreads();  // buffer b is free again
-  }
-  if (by_piece) {
-#pragma unroll
-    for (int k = 0; k < kAccQuads; ++k) {
-      const int idx = tid + k * nthr;
-      if (idx < rows * 64) store(idx >> 6, idx & 63, acc[k]);
-    }
-  }
-  // Clear the item's flags and claim (for the next call that gets this memory).
-  for (int s = tid; s < n; s += nthr)
-    ptx::st_relaxed_gpu_u64(p.merge_flag + prow0(s) / kRowsPerTile, 0ull);
-  if (tid == 0) ptx::st_relaxed_gpu_u64(p.merge_flag + p.merge_claim_offset + prow0(0) / kRowsPerTile, 0ull);
-  return true;
-}
-
-template <bool kPair, bool kPaged, int kFp8>
+// kKv: 0 dense K/V of one sequence; 1 paged K/V; 2 dense K/V of a batch of
+// sequences packed end to end (the V box of a sequence's last tile goes in 16-key
+// pieces so that the next sequence's values never reach it).
+template <bool kPair, int kKv, int kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
-  static_assert(kFp8 != 2 || !kPaged, "quantised PV reads dense V");
+  constexpr bool kPaged = kKv == 1;
+  constexpr bool kDenseBatch = kKv == 2;
+  static_assert(kFp8 != 2 || kKv == 0, "quantised PV reads the dense V of one sequence");
   constexpr bool kFp8Pv = kFp8 == 2;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
@@ -569,9 +368,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(kBarPvDone1), 1);
     ptx::mbar_init(bar(kBarOFree), kConsumers);
     ptx::mbar_init(bar(kBarDrain), 1);
-    ptx::mbar_init(bar(kBarMerge0), 1);
-    ptx::mbar_init(bar(kBarMerge1), 1);
-    ptx::mbar_init(bar(kBarPartDone), 4 * 32);
     if constexpr (kFp8) {
       for (int i = 0; i < kScSlots; ++i) {
         ptx::mbar_init(bar(kBarScFull + i), 1);
@@ -580,10 +376,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::fence_mbar_init();
   }
-  uint32_t* merge_bits = reinterpret_cast<uint32_t*>(smem + kOffMergeBits);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
-  if (threadIdx.x < kMaxFusedSplitPieces / 32) merge_bits[threadIdx.x] = 0;
-  if (threadIdx.x == 0) *abort_flag = 0;
   if (warp < 4) {
     // Rows 126 and 127 of each Q chunk are never written by TMA: zero them once.
     for (int i = threadIdx.x; i < kQChunks * 2 * 128 / 16; i += 128) {
@@ -668,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // CTA's 128 columns). A whole box is one copy; a paged box that crosses a
       // page is one copy per piece.
       auto next_tile = [&](const SeqGeo& sq, int n, bool is_k, int g) -> bool {
-        const bool v_fix = (kPaged || p.dense_vfix) && !is_k && n == v_fix_tile(sq);
+        const bool v_fix = (kPaged || kDenseBatch) && !is_k && n == v_fix_tile(sq);
         const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
         const CUtensorMap* sub_map = is_k ? &p.tmap_k_sub : (v_fix ? &p.tmap_v16 : &p.tmap_v_sub);
         const int halves = is_k ? kKStagesPerTile : ((kPair || kFp8Pv) ? 1 : 2);
@@ -715,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kFp8Pv && !is_k)  // one box (128 keys, 256 or 128 channels, head g)
             load(dst, &p.tmap_v, kBarFull + st, sq.kv_start + n * kBlockN,
                  kPair ? 128 * static_cast<int>(rank) : 0, g, pol_kv);
-          else if (!kPaged && v_fix)
+          else if (kDenseBatch && v_fix)
             issue_dense_v_pieces<kPair>(&p.tmap_v16, dst, kPair ? lbar(kBarFull + st) : bar(kBarFull + st),
                                         sq.kv_start, sq.kv_len, p.oob_row, r0, rows, nb, chunk0, g,
                                         pol_kv);
@@ -777,7 +569,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = next_tile(sq, w.n1 - 1, false, w.g);
         ++k;
       }
-      if (!ok) *abort_flag = 1;
       // Every copy issued must have landed before the CTA exits. On the normal
       // path the MMA thread already waited for all of them (these return at
       // once); after a time-out they may still be in flight. In a pair all
@@ -866,8 +657,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tc_fence_after();
           // O += P_j V_j in k-steps of 16 keys, N = 256. V stages are MN-major:
           // LBO = next 64-wide d chunk (kLboV), SBO = next group of 8 keys (kSboV).
-          const int vfix_tile = (kPaged || p.dense_vfix) ? v_fix_tile(p.batch.seq[w.seq]) : -1;
-          const bool v_fix = (kPaged || p.dense_vfix) && w.n0 + j == vfix_tile;
+          const int vfix_tile = (kPaged || kDenseBatch) ? v_fix_tile(p.batch.seq[w.seq]) : -1;
+          const bool v_fix = (kPaged || kDenseBatch) && w.n0 + j == vfix_tile;
           const int kr = p.batch.seq[w.seq].kv_len - vfix_tile * kBlockN;  // used when v_fix
           if constexpr (kFp8Pv) {
             // One stage: (this CTA's) channel rows of 128 key codes, K-major; P as E4M3
@@ -931,7 +722,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tile += nt;
         ++k;
       }
-      if (!ok) *abort_flag = 1;
       // Drain: every MMA issued above has completed once this barrier fires.
       commit(kBarDrain);
       wait_bar(bar(kBarDrain), 0, p);
@@ -946,7 +736,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t tile = 0;
     int k = 0;
-    int split_k = 0;  // split pieces done so far (their bit in merge_bits)
     bool ok = true;
     Piece w;
     while (ok && pieces.next(w)) {
@@ -1009,19 +798,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (key0 + c > pos) s[c] = kNegInf;
         }
-        // Row maximum: s[0..3], then s[4..123] eight at a time, then s[124..127].
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // Row maximum: four running maxima over s[0..127], eight scores a step.
+        float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
 #pragma unroll
-        for (int c = 4; c < 124; c += 8) {
+        for (int c = 0; c < 128; c += 8) {
           mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
           mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
           mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
           mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
         }
-        mx0 = fmaxf(mx0, s[124]);
-        mx1 = fmaxf(mx1, s[125]);
-        mx2 = fmaxf(mx2, s[126]);
-        mx3 = fmaxf(mx3, s[127]);
         const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * rowfac;
         const float m_new = fmaxf(m_ref, m_tile);
         const bool need = m_new > m_ref + (kFp8Pv ? kRescaleThresholdPv : kRescaleThreshold);
@@ -1196,22 +981,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       arrive_leader(kBarOFree);
-      if (w.slot >= 0 && p.fused_merge) {
-        // Flag the piece done once all 128 threads have stored their partial rows
-        // (they arrive; thread 0 waits, with the usual time limit, then publishes
-        // them all with its release fence); a CTA that finds the item's flags all
-        // set merges it after its last piece.
-        ptx::mbar_arrive(bar(kBarPartDone));
-        if (row == 0 && wait_bar(bar(kBarPartDone), split_k & 1, p) &&
-            flag_piece_done(p, sched, n_workers, w.tail, w.slot, rank, kPair ? 2 : 1) &&
-            split_k < kMaxFusedSplitPieces)
-          merge_bits[split_k >> 5] |= 1u << (split_k & 31);
-      }
-      if (w.slot >= 0) ++split_k;
       tile += nt;
       ++k;
     }
-    if (!ok) *abort_flag = 1;
   }
 
   // ---- teardown ----------------------------------------------------------------
@@ -1224,27 +996,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     if constexpr (kPair) ptx::tmem_dealloc_pair(tmem, kTmemCols);
     else ptx::tmem_dealloc(tmem, kTmemCols);
-  }
-  // ---- fused split merge: the items whose last piece this CTA completed --------
-  // Every copy into shared memory has landed (the roles drained them), so the Q
-  // region and the stage ring stage the partial rows. Skipped after a time-out.
-  if (p.fused_merge) {
-    __syncthreads();
-    if (*abort_flag == 0) {
-      PieceIter again;
-      again.init(&p.batch, p.tail.v, sched, n_workers, worker);
-      uint32_t mphase = 0;
-      int sk = 0;
-      Piece w;
-      while (again.next(w)) {
-        if (w.slot < 0) continue;
-        const bool mine = sk < kMaxFusedSplitPieces && (merge_bits[sk >> 5] >> (sk & 31)) & 1u;
-        ++sk;
-        if (mine && !merge_item(p, sched, n_workers, w.tail, rank, kPair ? 2 : 1, smem, base,
-                                bar(kBarMerge0), mphase))
-          break;
-      }
-    }
   }
 }
 
@@ -1491,16 +1242,20 @@ size_t fwd_smem_bytes() { return kSmemAlloc; }
 
 cudaError_t prepare_fwd_kernel() {
   const void* kernels[] = {
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, 0>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, 0>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true, 0>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true, 0>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, 1>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, 1>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, true, 1>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, true, 1>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, false, 2>),
-      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, false, 2>)};
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, 0, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, 0, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, 1, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, 1, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, 2, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, 2, 0>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, 0, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, 0, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, 1, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, 1, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, 2, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, 2, 1>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<false, 0, 2>),
+      reinterpret_cast<const void*>(gqa_attn_fwd_sm103_kernel<true, 0, 2>)};
   for (const void* f : kernels) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(kSmemAlloc));
@@ -1540,28 +1295,28 @@ cudaError_t max_active_pairs(int* pairs) {
   cudaLaunchConfig_t cfg = launch_config(dim3(2), dim3(kThreads), kSmemAlloc, true, nullptr, attr);
   cfg.attrs = attr + 1;  // occupancy of the cluster shape only
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, false, 0>, &cfg);
+  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, 0, 0>, &cfg);
 }
 
-cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, int fp8,
+template <bool kPair>
+cudaError_t launch_fwd_of(const cudaLaunchConfig_t& cfg, const FwdParams& p, int kv, int fp8) {
+  if (fp8 == 2) return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<kPair, 0, 2>, p);
+  switch (kv * 2 + fp8) {
+    case 0: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<kPair, 0, 0>, p);
+    case 1: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<kPair, 0, 1>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<kPair, 1, 0>, p);
+    case 3: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<kPair, 1, 1>, p);
+    case 4: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<kPair, 2, 0>, p);
+    default: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<kPair, 2, 1>, p);
+  }
+}
+
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, int kv, int fp8,
                        cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = launch_config(dim3(static_cast<unsigned>(grid)), dim3(kThreads),
                                                kSmemAlloc, pair, stream, attr);
-  if (fp8 == 2)  // quantised QK^T and PV (dense K/V)
-    return pair ? cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, 2>, p)
-                : cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, 2>, p);
-  const int which = (pair ? 4 : 0) | (paged ? 2 : 0) | (fp8 ? 1 : 0);
-  switch (which) {
-    case 0: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, 0>, p);
-    case 1: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, false, 1>, p);
-    case 2: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, 0>, p);
-    case 3: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<false, true, 1>, p);
-    case 4: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, 0>, p);
-    case 5: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, false, 1>, p);
-    case 6: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, 0>, p);
-    default: return cudaLaunchKernelEx(&cfg, gqa_attn_fwd_sm103_kernel<true, true, 1>, p);
-  }
+  return pair ? launch_fwd_of<true>(cfg, p, kv, fp8) : launch_fwd_of<false>(cfg, p, kv, fp8);
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {

@@ -59,8 +59,6 @@ struct FwdParams {
   int sub_rows;              // gcd(page_size, 64)
   int oob_row;               // a row past the cache (num_pages * page_size) or, for a dense
                              //   batch, past the packed K/V (total keys): TMA zero fill
-  int dense_vfix;            // dense batch of several sequences: V of each sequence's last
-                             //   KV tile goes in 16-key pieces, keys past it zeroed
   // FP8 QK^T (kernels instantiated with kFp8 only): tmap_q / tmap_k hold E4M3 codes
   // (Q box (128, 6 heads, 21 tokens); K 4-D (128, key, head, chunk) with 2 chunks).
   CUtensorMap tmap_ks;       // dense: key scales FP32 [4][k_scale_stride], box (128 keys, 1 head)
@@ -71,16 +69,6 @@ struct FwdParams {
   // transposed, [4 heads][256 channels][v_stride keys] bytes, 3-D (key, channel,
   // head), box (128 keys, 256 channels or a pair CTA's 128, 1 head), 128B swizzle.
   const float* v_scale;      // [4][256] FP32 per-channel scales of V
-  // Split merge inside the attention kernel (fused_merge != 0). Every split piece,
-  // once its partial rows are stored, sets its flag merge_flag[slot * CTAs per
-  // item + rank] to call_tag and then reads its item's other flags; a piece that
-  // finds them all equal to call_tag (flags left by another call hold another tag
-  // or 0) merges the item's rows of its rank after its last piece, and clears the
-  // flags. No CTA ever waits for another.
-  unsigned long long* merge_flag;  // [slots * cpi] flags, then [slots * cpi] claim words
-  long long merge_claim_offset;    // slots * cpi
-  unsigned long long call_tag;     // nonzero, new for every call
-  int fused_merge;
   TailPrefix tail;           // balanced tail: tile prefix sums of the tail items
   Batch batch;               // the call's sequences (gqa_schedule.h); kept last: it is large
 };
@@ -104,8 +92,9 @@ struct MergeParams {
 
 size_t fwd_smem_bytes();
 // grid = CTAs; with pair = true the CTAs form clusters of two (grid even).
-// fp8: 0 BF16, 1 E4M3 QK^T, 2 E4M3 QK^T and PV (dense K/V only).
-cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, bool paged, int fp8,
+// kv: 0 dense K/V of one sequence, 1 paged K/V, 2 dense K/V of a batch;
+// fp8: 0 BF16, 1 E4M3 QK^T, 2 E4M3 QK^T and PV (dense K/V of one sequence).
+cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, int kv, int fp8,
                        cudaStream_t stream);
 // Scale column of each key row for head-major key scales: sequence b of a packed
 // batch (rows row_begin[b] .. row_begin[b+1]-1) starts at column col_begin[b].
@@ -123,13 +112,7 @@ cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scale, int ro
 cudaError_t launch_quantize_v_fp8(const void* v, void* codes, float* scale, int kv_len,
                                   int v_stride, cudaStream_t stream);
 cudaError_t max_active_pairs(int* pairs);       // co-resident CTA pairs on this device
-// Split pieces one CTA (pair) may count for the fused merge: it remembers which
-// items it completed in a bitset of this many bits (the planner keeps every
-// worker's split pieces below it, else it plans the separate merge pass).
-constexpr int kMaxFusedSplitPieces = 2048;
-// Pieces of one item the fused merge takes (their LSEs for all rows are staged in
-// shared memory at once); items cut into more use the separate merge pass.
-constexpr int kMaxFusedItemPieces = 48;
+
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t prepare_fwd_kernel();                // per-device one-time attributes
 cudaError_t status_word_address(int** ptr);      // device address of the status word

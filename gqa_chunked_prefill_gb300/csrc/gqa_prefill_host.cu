@@ -9,8 +9,6 @@
 // tensor maps, allocate split partials in stream order, and launch.
 
 #include <algorithm>
-#include <atomic>
-#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -43,12 +41,6 @@ constexpr double kTileUs = 1.5;              // planning estimate per tile, one-
 constexpr double kPairTileUs = 1.35;
 constexpr double kMergeBytesPerUs = 6.0e6;   // effective bandwidth of the merge pass (partials in L2)
 constexpr double kMergeLaunchUs = 3.0;       // its launch, mostly hidden by programmatic launch
-// Merge inside the attention kernel: one CTA loads an item's LSEs, stages its
-// partial rows from L2 into shared memory with bulk copies (96 KB chunks) and
-// reduces them after its last piece.
-constexpr double kFusedMergeBytesPerUs = 1.5e5;  // per CTA
-constexpr double kFusedMergeCopyUs = 0.1;        // per bulk copy issued
-constexpr double kFusedMergeFixedUs = 2.0;       // flags, LSE loads, staging latency
 constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
 constexpr int kSplitCandidates[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16, 24, 32};
 constexpr int kForceBalanced = GQA_FORCE_BALANCED_TAIL;  // force_splits value: balanced tail
@@ -112,84 +104,19 @@ std::vector<int> item_tile_counts(const Batch& b) {
   return t;
 }
 
-// Live MMA rows of the busiest CTA of every item (6 per token, at most 126).
-std::vector<int> item_live_rows(const Batch& b) {
-  std::vector<int> r(static_cast<size_t>(b.n_items));
-  for (int i = 0; i < b.n_items; ++i) {
-    int seq, qt, g;
-    item_of(b, i, seq, qt, g);
-    const int tokens = std::min(b.tok_per_item, b.seq[seq].q_len - qt * b.tok_per_item);
-    r[static_cast<size_t>(i)] = kGroup * std::min(kTokPerTile, tokens);
-  }
-  return r;
-}
-
-// The two ways to merge split items, costed on one simulated schedule: `load`
-// (per worker, in tiles, overheads included), `last` (per split item, the
-// worker whose piece ends last: it merges the item when the merge runs inside
-// the attention kernel), `merge_tiles` (that merge's cost, in tiles) and
-// `sep_us` (the separate merge pass). Records the choice in *plan and returns
-// the estimated time in us. merge_mode: 0 cheaper, 1 inside the kernel when
-// every worker's split pieces fit its bitset, 2 separate.
-double choose_merge(std::vector<int64_t> load, const std::vector<int>& last,
-                    const std::vector<int64_t>& merge_tiles, int max_split_pieces,
-                    int max_item_pieces, int64_t slots, double tile_us, double sep_us,
-                    int merge_mode, gqa_prefill_plan* plan) {
-  const double plain = static_cast<double>(*std::max_element(load.begin(), load.end()));
-  for (size_t i = 0; i < last.size(); ++i) load[static_cast<size_t>(last[i])] += merge_tiles[i];
-  const double fused = static_cast<double>(*std::max_element(load.begin(), load.end())) * tile_us;
-  const double separate = plain * tile_us + sep_us;
-  const bool fits =
-      max_split_pieces <= kMaxFusedSplitPieces && max_item_pieces <= kMaxFusedItemPieces;
-  // Measured on GB300, the merge inside the kernel never beat the separate pass:
-  // one CTA pulls an item's partials from L2 at ~35 GB/s and pays the flag,
-  // LSE and staging round trips (~8 us) after its last piece, while the
-  // separate pass spreads the rows over the whole GPU behind a programmatic
-  // launch. So it runs only when a caller asks for it (merge_mode 1).
-  (void)fused;
-  (void)separate;
-  const bool use = !last.empty() && fits && merge_mode == 1;
-  plan->fused_merge = use ? 1 : 0;
-  if (use) {
-    plan->kernels_per_call = 1;
-    plan->workspace_bytes += 2 * slots * (plan->variant == 2 ? 2 : 1) * 8;  // flags, claims
-  }
-  return last.empty() ? plain * tile_us : (use ? fused : separate);
-}
-
-// Merge inside the kernel: cost of one item of `pieces` pieces whose busiest CTA
-// has `rows` live MMA rows, in tiles of the variant. The copies follow the
-// kernel's staging: row chunks of 96/pieces rows, or for few rows and many pieces
-// one copy per piece.
-int64_t fused_merge_tiles(int pieces, int rows, double tile_us) {
-  const bool by_piece = rows <= 24 && pieces * rows > 96;
-  const int rc = std::max(1, std::min(rows, 96 / pieces));
-  const int copies = by_piece ? pieces : pieces * ((rows + rc - 1) / rc);
-  const double us = pieces * static_cast<double>(rows) * kPartialRowBytes / kFusedMergeBytesPerUs +
-                    copies * kFusedMergeCopyUs + kFusedMergeFixedUs;
-  return static_cast<int64_t>(std::ceil(us / tile_us));
-}
-
 // Fills *plan for `variant` (1: one CTA per item, 2: a CTA pair per item) with
 // head_rounds whole rounds and S-way tail splits over `workers` CTAs (or
 // pairs), simulating the snake deal of gqa_schedule.h over the items' tile
-// counts; S must not exceed the shortest item's tiles. rows[i]: live MMA rows
-// of item i's busiest CTA. Returns the estimated time in us.
-double plan_schedule(const std::vector<int>& tiles, const std::vector<int>& rows, int q_tiles,
-                     int num_sms, int variant, int workers, int head_rounds, int S, int merge_mode,
-                     gqa_prefill_plan* plan) {
+// counts; S must not exceed the shortest item's tiles. Returns the estimated
+// time in us.
+double plan_schedule(const std::vector<int>& tiles, int q_tiles, int num_sms, int variant,
+                     int workers, int head_rounds, int S, gqa_prefill_plan* plan) {
   const int n_items = static_cast<int>(tiles.size());
   const int cpi = variant == 2 ? 2 : 1;
   const int head = std::min(head_rounds * workers, n_items);
   const int n_units = head + (n_items - head) * S;
   workers = std::max(1, std::min(workers, n_units));
   std::vector<int64_t> load(static_cast<size_t>(workers), 0);
-  const int tail = n_items - head;
-  const bool split = S > 1 && tail > 0;
-  const double tile_us = variant == 2 ? kPairTileUs : kTileUs;
-  std::vector<int> last(split ? static_cast<size_t>(tail) : 0, 0);
-  std::vector<int64_t> last_end(last.size(), -1), merge_tiles(last.size(), 0);
-  std::vector<int> split_pieces(static_cast<size_t>(workers), 0);
   int64_t total = 0;
   for (int u = 0; u < n_units; ++u) {
     const int r = u / workers, x = u % workers;
@@ -204,17 +131,9 @@ double plan_schedule(const std::vector<int>& tiles, const std::vector<int>& rows
     }
     load[static_cast<size_t>(b)] += len + kPieceOverheadTiles;
     total += len;
-    if (split && u >= head) {  // who ends each split item last (it merges in-kernel)
-      const size_t i = static_cast<size_t>((u - head) / S);
-      ++split_pieces[static_cast<size_t>(b)];
-      if (load[static_cast<size_t>(b)] > last_end[i]) {
-        last_end[i] = load[static_cast<size_t>(b)];
-        last[i] = b;
-      }
-    }
   }
-  for (size_t i = 0; i < last.size(); ++i)
-    merge_tiles[i] = fused_merge_tiles(S, rows[static_cast<size_t>(head) + i], tile_us);
+  const int tail = n_items - head;
+  const bool split = S > 1 && tail > 0;
   std::memset(plan, 0, sizeof(*plan));
   plan->num_sms = num_sms;
   plan->q_tiles = q_tiles;
@@ -230,15 +149,13 @@ double plan_schedule(const std::vector<int>& tiles, const std::vector<int>& rows
   plan->workspace_bytes =
       split ? static_cast<int64_t>(tail) * S * cpi * kRowsPerTile * kPartialRowBytes : 0;
   plan->est_makespan_tiles = *std::max_element(load.begin(), load.end());
-  double sep_us = 0.0;
+  double us = static_cast<double>(plan->est_makespan_tiles) * (variant == 2 ? kPairTileUs : kTileUs);
   if (split) {
     const double bytes =
         tail * static_cast<double>(cpi * kRowsPerTile) * (S * kPartialRowBytes + 520.0);
-    sep_us = bytes / kMergeBytesPerUs + kMergeLaunchUs;
+    us += bytes / kMergeBytesPerUs + kMergeLaunchUs;
   }
-  return choose_merge(load, last, merge_tiles,
-                      *std::max_element(split_pieces.begin(), split_pieces.end()), S,
-                      static_cast<int64_t>(tail) * S, tile_us, sep_us, merge_mode, plan);
+  return us;
 }
 
 // Fills *plan for `variant` with head_rounds whole rounds and a balanced tail
@@ -247,9 +164,8 @@ double plan_schedule(const std::vector<int>& tiles, const std::vector<int>& rows
 // negative value when the tail does not fit the balanced form (no tail item,
 // more than kMaxBalancedTail of them, fewer tiles than workers, or 2^31 tiles
 // and more). Without whole rounds the grid shrinks to the tail's tile count.
-double plan_balanced(const std::vector<int>& tiles, const std::vector<int>& rows, int q_tiles,
-                     int num_sms, int variant, int workers, int head_rounds, int merge_mode,
-                     gqa_prefill_plan* plan) {
+double plan_balanced(const std::vector<int>& tiles, int q_tiles, int num_sms, int variant,
+                     int workers, int head_rounds, gqa_prefill_plan* plan) {
   const int n_items = static_cast<int>(tiles.size());
   const int cpi = variant == 2 ? 2 : 1;
   const int head = std::min(head_rounds * workers, n_items);
@@ -271,43 +187,20 @@ double plan_balanced(const std::vector<int>& tiles, const std::vector<int>& rows
   }
   int pieces = 0, partial = 0, split_items = 0;
   int k = 0;
-  // Per tail item: its pieces, and the worker whose piece of it ends last.
-  const size_t nt_ = static_cast<size_t>(n_tail);
-  std::vector<int> item_pieces(nt_, 0), item_last(nt_, 0);
-  std::vector<int64_t> item_end(nt_, -1);
-  std::vector<int> split_pieces(static_cast<size_t>(workers), 0);
   for (int x = 0; x < workers; ++x) {
     const int64_t a = x * W / workers, e = (x + 1) * W / workers;
-    const size_t xs = static_cast<size_t>(x);
+    load[static_cast<size_t>(x)] += e - a;
     while (prefix[static_cast<size_t>(k) + 1] <= a) ++k;
     for (int64_t pos = a; pos < e; ++k) {
       const int64_t s = prefix[static_cast<size_t>(k)], f = prefix[static_cast<size_t>(k) + 1];
       const int64_t stop = std::min(e, f);
       ++pieces;
-      if (pos != s || stop != f) {
-        ++partial;
-        ++split_pieces[xs];
-      }
+      if (pos != s || stop != f) ++partial;
       if (pos == s && stop != f) ++split_items;  // counted once: at the item's first piece
-      load[xs] += (stop - pos) + kPieceOverheadTiles;
-      const size_t ks = static_cast<size_t>(k);
-      ++item_pieces[ks];
-      if (load[xs] > item_end[ks]) {
-        item_end[ks] = load[xs];
-        item_last[ks] = x;
-      }
+      load[static_cast<size_t>(x)] += kPieceOverheadTiles;
       pos = stop;
       if (stop < f) break;  // the item continues in the next worker's range
     }
-  }
-  const double tile_us = variant == 2 ? kPairTileUs : kTileUs;
-  std::vector<int> last;
-  std::vector<int64_t> merge_tiles;
-  for (size_t i = 0; i < nt_; ++i) {
-    if (item_pieces[i] < 2) continue;
-    last.push_back(item_last[i]);
-    merge_tiles.push_back(
-        fused_merge_tiles(item_pieces[i], rows[static_cast<size_t>(head) + i], tile_us));
   }
   std::memset(plan, 0, sizeof(*plan));
   plan->num_sms = num_sms;
@@ -324,16 +217,13 @@ double plan_balanced(const std::vector<int>& tiles, const std::vector<int>& rows
   plan->workspace_bytes =
       split_items > 0 ? 2 * static_cast<int64_t>(workers) * cpi * kRowsPerTile * kPartialRowBytes : 0;
   plan->est_makespan_tiles = *std::max_element(load.begin(), load.end());
-  double sep_us = 0.0;
+  double us = static_cast<double>(plan->est_makespan_tiles) * (variant == 2 ? kPairTileUs : kTileUs);
   if (split_items > 0) {
     const double bytes = static_cast<double>(cpi * kRowsPerTile) *
                          (split_items * 520.0 + partial * static_cast<double>(kPartialRowBytes));
-    sep_us = bytes / kMergeBytesPerUs + kMergeLaunchUs;
+    us += bytes / kMergeBytesPerUs + kMergeLaunchUs;
   }
-  return choose_merge(load, last, merge_tiles,
-                      *std::max_element(split_pieces.begin(), split_pieces.end()),
-                      *std::max_element(item_pieces.begin(), item_pieces.end()),
-                      2 * static_cast<int64_t>(workers), tile_us, sep_us, merge_mode, plan);
+  return us;
 }
 
 // Best plan of one variant: searches the number of whole rounds (the last few
@@ -342,27 +232,24 @@ double plan_balanced(const std::vector<int>& tiles, const std::vector<int>& rows
 // force_splits: S > 0 forces the uniform cut with S pieces, kForceBalanced the
 // balanced tail (the best number of whole rounds for it, if any fits).
 double best_plan_of(const std::vector<SeqIn>& seqs, int num_sms, int variant, int workers,
-                    int force_splits, int merge_mode, gqa_prefill_plan* plan) {
+                    int force_splits, gqa_prefill_plan* plan) {
   static thread_local Batch b;  // large: not on the stack
   build_batch(seqs, variant, &b);
   const std::vector<int> tiles = item_tile_counts(b);
-  const std::vector<int> rows = item_live_rows(b);
   int q_tiles = 0;
   for (int i = 0; i < b.n_seq; ++i) q_tiles += b.seq[i].n_qtiles;
   const int n_items = static_cast<int>(tiles.size());
   const int max_splits = std::max(1, *std::min_element(tiles.begin(), tiles.end()));
   const int full_rounds = n_items / workers;
   if (force_splits > 0)
-    return plan_schedule(tiles, rows, q_tiles, num_sms, variant, workers, full_rounds,
-                         std::min(force_splits, max_splits), merge_mode, plan);
-  double best = plan_schedule(tiles, rows, q_tiles, num_sms, variant, workers, 0, 1, merge_mode,
-                              plan);
+    return plan_schedule(tiles, q_tiles, num_sms, variant, workers, full_rounds,
+                         std::min(force_splits, max_splits), plan);
+  double best = plan_schedule(tiles, q_tiles, num_sms, variant, workers, 0, 1, plan);
   gqa_prefill_plan cand{};
   if (force_splits == kForceBalanced) {
     double best_b = -1.0;
     for (int hr = full_rounds; hr >= 0; --hr) {
-      const double us =
-          plan_balanced(tiles, rows, q_tiles, num_sms, variant, workers, hr, merge_mode, &cand);
+      const double us = plan_balanced(tiles, q_tiles, num_sms, variant, workers, hr, &cand);
       if (us >= 0.0 && (best_b < 0.0 || us < best_b)) {
         best_b = us;
         *plan = cand;
@@ -374,8 +261,7 @@ double best_plan_of(const std::vector<SeqIn>& seqs, int num_sms, int variant, in
     if (hr < full_rounds - 3 && hr != 0) continue;
     for (int S : kSplitCandidates) {
       if (S == 1 || S > max_splits) continue;
-      const double us =
-          plan_schedule(tiles, rows, q_tiles, num_sms, variant, workers, hr, S, merge_mode, &cand);
+      const double us = plan_schedule(tiles, q_tiles, num_sms, variant, workers, hr, S, &cand);
       if (us < 0.98 * best) {
         best = us;
         *plan = cand;
@@ -389,31 +275,31 @@ double best_plan_of(const std::vector<SeqIn>& seqs, int num_sms, int variant, in
 // max_pairs: CTA pairs that can be resident at once. force_grid caps the CTAs
 // launched (a pair counts as two).
 void compute_plan(const std::vector<SeqIn>& seqs, int num_sms, int max_pairs, int force_splits,
-                  int force_grid, int force_variant, int merge_mode, gqa_prefill_plan* plan) {
+                  int force_grid, int force_variant, gqa_prefill_plan* plan) {
   const int cap = force_grid > 0 ? std::min(force_grid, num_sms) : num_sms;
   const int workers1 = std::max(1, cap);
   const int workers2 = std::max(1, std::min(max_pairs, cap / 2));
   if (force_variant == 1 || (force_variant == 0 && max_pairs < 1)) {
-    best_plan_of(seqs, num_sms, 1, workers1, force_splits, merge_mode, plan);
+    best_plan_of(seqs, num_sms, 1, workers1, force_splits, plan);
     return;
   }
   if (force_variant == 2) {
-    best_plan_of(seqs, num_sms, 2, workers2, force_splits, merge_mode, plan);
+    best_plan_of(seqs, num_sms, 2, workers2, force_splits, plan);
     return;
   }
   gqa_prefill_plan one{}, pair{};
-  const double t1 = best_plan_of(seqs, num_sms, 1, workers1, force_splits, merge_mode, &one);
-  const double t2 = best_plan_of(seqs, num_sms, 2, workers2, force_splits, merge_mode, &pair);
+  const double t1 = best_plan_of(seqs, num_sms, 1, workers1, force_splits, &one);
+  const double t2 = best_plan_of(seqs, num_sms, 2, workers2, force_splits, &pair);
   *plan = t2 < 0.98 * t1 ? pair : one;
 }
 
 // Plans keyed by everything they depend on: the device, the options and the
 // (q_len, kv_len) of every sequence in the caller's order.
 void cached_plan(const std::vector<SeqIn>& seqs, int num_sms, int max_pairs, int force_splits,
-                 int force_grid, int force_variant, int merge_mode, gqa_prefill_plan* plan) {
+                 int force_grid, int force_variant, gqa_prefill_plan* plan) {
   static std::mutex mu;
   static std::map<std::vector<int>, gqa_prefill_plan> cache;
-  std::vector<int> key{num_sms, max_pairs, force_splits, force_grid, force_variant, merge_mode};
+  std::vector<int> key{num_sms, max_pairs, force_splits, force_grid, force_variant};
   for (const SeqIn& s : seqs) {
     key.push_back(s.q_len);
     key.push_back(s.kv_len);
@@ -426,8 +312,7 @@ void cached_plan(const std::vector<SeqIn>& seqs, int num_sms, int max_pairs, int
       return;
     }
   }
-  compute_plan(seqs, num_sms, max_pairs, force_splits, force_grid, force_variant, merge_mode,
-               plan);
+  compute_plan(seqs, num_sms, max_pairs, force_splits, force_grid, force_variant, plan);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache.emplace(std::move(key), *plan);
@@ -709,18 +594,6 @@ struct CallIO {
   float scale;
 };
 
-// Tag of a call's fused-merge counter words: nonzero, below 2^48, never the
-// same twice in a row for the same memory (a process-wide sequence from a
-// clock-seeded start, so that a counter word left by another process's call in
-// recycled memory does not carry the same tag).
-unsigned long long next_call_tag() {
-  static std::atomic<unsigned long long> seq{static_cast<unsigned long long>(
-      std::chrono::steady_clock::now().time_since_epoch().count())};
-  constexpr unsigned long long kMask = (1ull << 48) - 1;
-  unsigned long long t = seq.fetch_add(1) & kMask;
-  return t == 0 ? 1 : t;
-}
-
 // Launches `plan` on `stream`; `ws` holds plan.workspace_bytes (or nothing).
 // total_q / total_kv: rows of the packed Q and (dense) K/V.
 gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
@@ -752,7 +625,6 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
       // that tile's V goes in 16-key pieces (see the kernel's issue_dense_v_pieces).
       if (!encode_kv(&p.tmap_v16, io.v, kv_rows, 16, 1, kBf16)) return GQA_ERR_CUDA;
       p.oob_row = static_cast<int>(kv_rows);
-      p.dense_vfix = 1;
     }
   } else {
     const PagedKV& pkv = *io.pkv;
@@ -819,24 +691,19 @@ gqa_status launch_plan(const gqa_prefill_plan& plan, const CallIO& io,
   for (const SeqIn& sq : seqs)
     if (sq.q_len > p.batch.tok_per_item) p.kv_read_once = 0;
   if (plan.workspace_bytes > 0) {
-    // Partial slots: tail_items * S (uniform tail) or two per worker (balanced),
-    // then (merge inside the kernel) one flag and one claim word per slot and CTA.
+    // Partial slots: tail_items * S (uniform tail) or two per worker (balanced).
     const size_t slots = plan.tail_splits > 0
                              ? static_cast<size_t>(plan.tail_items) * plan.tail_splits
                              : 2 * static_cast<size_t>(workers);
     p.part_o = static_cast<float*>(ws);
     p.part_lse = p.part_o + slots * (pair ? 2 : 1) * kRowsPerTile * kHeadDim;
     p.part_rows = static_cast<long long>(slots) * (pair ? 2 : 1) * kRowsPerTile;
-    p.merge_flag = reinterpret_cast<unsigned long long*>(p.part_lse + p.part_rows);
-    p.merge_claim_offset = p.part_rows / kRowsPerTile;
   }
-  p.fused_merge = plan.fused_merge;
-  p.call_tag = next_call_tag();
   auto ev_begin = static_cast<cudaEvent_t>(opts ? opts->fwd_event_begin : nullptr);
   auto ev_end = static_cast<cudaEvent_t>(opts ? opts->fwd_event_end : nullptr);
   if (ev_begin && cudaEventRecord(ev_begin, stream) != cudaSuccess) return GQA_ERR_CUDA;
-  if (launch_fwd(p, plan.grid, pair, io.pkv != nullptr, io.f8 ? (fp8_pv ? 2 : 1) : 0, stream) !=
-      cudaSuccess)
+  const int kv_mode = io.pkv ? 1 : (seqs.size() > 1 ? 2 : 0);
+  if (launch_fwd(p, plan.grid, pair, kv_mode, io.f8 ? (fp8_pv ? 2 : 1) : 0, stream) != cudaSuccess)
     return GQA_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, stream) != cudaSuccess) return GQA_ERR_CUDA;
   if (plan.kernels_per_call == 2) {  // the separate merge pass
@@ -895,8 +762,7 @@ gqa_status run(const CallIO& io, const std::vector<SeqIn>& seqs, int total_q, in
   if ((st = device_info(&dev)) != GQA_OK) return st;
   gqa_prefill_plan plan{};
   cached_plan(seqs, dev->num_sms, dev->max_pairs, opts ? opts->force_splits : 0,
-              opts ? opts->force_grid : 0, opts ? opts->force_variant : 0,
-              opts ? opts->merge_mode : 0, &plan);
+              opts ? opts->force_grid : 0, opts ? opts->force_variant : 0, &plan);
   if (plan_out) *plan_out = plan;
   auto stream = static_cast<cudaStream_t>(stream_ptr);
   void* ws = nullptr;
@@ -964,7 +830,7 @@ gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, f
   if ((st = noalloc_scratch(&scratch)) != GQA_OK) return st;
   const std::vector<SeqIn> seqs{SeqIn{0, q_len, 0, kv_len, 0}};
   gqa_prefill_plan plan{};
-  cached_plan(seqs, dev->num_sms, dev->max_pairs, 0, 0, 0, 0, &plan);
+  cached_plan(seqs, dev->num_sms, dev->max_pairs, 0, 0, 0, &plan);
   if (static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes) return GQA_ERR_SCRATCH;
   // Every partial row the merge reads is written by the attention kernel first,
   // so the scratch needs no clearing between calls.
@@ -1301,7 +1167,7 @@ gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32
   if (total_q == 0) return GQA_OK;
   // The attention calls plan with min(occupancy pairs, num_sms / 2) (device_info).
   const int pairs = max_pairs < 0 ? num_sms / 2 : std::min(max_pairs, num_sms / 2);
-  gqa::cached_plan(seqs, num_sms, pairs, force_splits, force_grid, force_variant, 0, plan);
+  gqa::cached_plan(seqs, num_sms, pairs, force_splits, force_grid, force_variant, plan);
   return GQA_OK;
 }
 

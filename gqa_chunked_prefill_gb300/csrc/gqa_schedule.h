@@ -29,11 +29,8 @@
 //    the output; of the others, the CTA's first piece writes slot 2x and its
 //    last piece slot 2x+1 (a range holds at most those two partial pieces).
 //    Every CTA gets the same number of tiles, whatever the tail's item count.
-// The pieces of every split tail item are then combined, either inside the
-// attention kernel by the CTA that completes the item's last piece (the "fused"
-// merge: each piece counts itself done on a per-item counter after storing its
-// partial; no CTA waits for another) or by a separate merge pass
-// (merge_tail_kernel, or merge_wide_kernel for items of 16 or more pieces).
+// The merge pass (merge_tail_kernel, or merge_wide_kernel for items of 16 or more
+// pieces) then combines the pieces of every split tail item.
 //
 // Why this shape: in every round all CTAs sweep the KV range of items of
 // (nearly) equal length from the same starting key in lockstep, so the K/V

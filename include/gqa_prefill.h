@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 10
+#define GQA_PREFILL_ABI_VERSION 11
 
 typedef enum gqa_status {
   GQA_OK = 0,
@@ -105,12 +105,7 @@ typedef struct gqa_prefill_opts {
                                  Exercises the time-out path without faulting.     */
   int force_variant;          /* 0: planner decides; 1: one CTA per 21-token item;
                                  2: a CTA pair per 42-token item (cta_group::2 MMAs) */
-  int merge_mode;             /* split items only. 0 or 2: a separate merge kernel
-                                 (measured faster on GB300); 1: merge inside the
-                                 attention kernel (a CTA that completes an item's
-                                 last piece merges it after its own last piece; one
-                                 launch per call), where the plan fits it (at most
-                                 48 pieces per item, 2048 split pieces per CTA)    */
+  int reserved[1];
 } gqa_prefill_opts;
 
 /*
@@ -121,10 +116,8 @@ typedef struct gqa_prefill_opts {
  * items in the first head_rounds full rounds. The remaining (tail) items are
  * cut in one of two ways: uniform, each split into tail_splits pieces of equal
  * KV length; or balanced (tail_splits == 0), their tiles laid end to end and
- * every CTA (pair) taking an equal share, cut at item boundaries. The pieces
- * of every split item are merged either inside the attention kernel, by the
- * CTA (pair) that completes the item's last piece (fused_merge = 1; no CTA
- * waits for another), or by a second kernel (fused_merge = 0).
+ * every CTA (pair) taking an equal share, cut at item boundaries. A second
+ * kernel merges the pieces of every split item.
  */
 typedef struct gqa_prefill_plan {
   int num_sms;                /* SMs of the device                                    */
@@ -141,18 +134,13 @@ typedef struct gqa_prefill_plan {
   int variant;                /* 1 = one CTA per item (M = 128 MMAs, 21 tokens);
                                  2 = a CTA pair per item (cta_group::2, M = 256, 42
                                  tokens: each CTA streams half of every K/V tile)  */
-  int fused_merge;            /* 1 = split items are merged inside the attention
-                                 kernel (kernels_per_call 1); 0 = no split items, or
-                                 a separate merge kernel                           */
   int64_t total_tiles;        /* KV tiles summed over all items                       */
   int64_t workspace_bytes;    /* temporary device memory of the split items (or 0):
                                  FP32 partials, 128 rows x 257 floats per CTA of an
                                  item (cpi = 1, or 2 for the CTA pair) per slot, in
                                  tail_items * tail_splits slots (uniform tail) or 2
                                  slots per worker (balanced tail: workers = grid /
-                                 cpi), i.e. slots * cpi * 128 * 1028 bytes; with
-                                 fused_merge, plus an 8-byte flag and an 8-byte
-                                 claim word per slot and CTA (slots * cpi * 16)    */
+                                 cpi), i.e. slots * cpi * 128 * 1028 bytes         */
   int64_t est_makespan_tiles; /* planner's cost of the busiest CTA, in KV tiles       */
 } gqa_prefill_plan;
 
@@ -214,17 +202,15 @@ gqa_status gqa_prefill_poll(void* stream, int* device_status);
  * plans exactly like gqa_prefill_attn; when that plan's workspace_bytes (see
  * gqa_prefill_plan: for a uniform tail tail_items * tail_splits * cpi * 128 *
  * 1028 bytes, for a balanced tail 2 * workers * cpi * 128 * 1028 bytes — at
- * most about 40 MB on 152 SMs — plus slots * cpi * 16 bytes of flags when
- * the merge runs inside the kernel; cpi = 2 for CTA-pair plans) exceed the
- * array, it returns GQA_ERR_SCRATCH and launches nothing.
+ * most about 40 MB on 152 SMs; cpi = 2 for CTA-pair plans) exceed the array,
+ * it returns GQA_ERR_SCRATCH and launches nothing.
  *
  * It calls no cudaMalloc, cudaFree or other allocating routine. Its first call
  * on each device does a one-time set-up with that device current (device
  * check, kernel attributes, and cudaGetSymbolAddress of the scratch array and
  * the status word); make that first call before any stream capture. Every
  * call shares the one array and it keeps the last call's contents (nothing in
- * it needs to start at zero: every partial row is written before it is read,
- * and the merge flags carry a per-call tag, so a stale flag does not count):
+ * it needs to start at zero: every partial row is written before it is read):
  * calls whose work overlaps on the GPU — on
  * different streams, or in different threads without ordering between them —
  * race on it and give undefined results. Serialise such calls.

@@ -13,7 +13,7 @@ ATOL, RTOL, MEAN_TOL, LSE_TOL = 1e-2, 1e-2, 2e-3, 1e-3
 
 
 def run_gpu(q, k, v, scale, force_splits=0, force_grid=0, force_variant=0, with_lse=True,
-            stream=None, merge_mode=0):
+            stream=None):
     """q, k, v: CPU or CUDA bf16. Returns (out bf16 CUDA, lse fp32 CUDA or None, plan)."""
     import gqa_chunked_prefill_gb300 as gqa
     dev = torch.device("cuda:0")
@@ -24,8 +24,7 @@ def run_gpu(q, k, v, scale, force_splits=0, force_grid=0, force_variant=0, with_
     lse = torch.empty((q_len, hq), dtype=torch.float32, device=dev) if with_lse else None
     _, plan = gqa.gqa_prefill_attn_ex(qd, kd, vd, out, lse, q_len, kv_len, hq, hkv, d, scale,
                                       stream=stream, force_splits=force_splits,
-                                      force_grid=force_grid, force_variant=force_variant,
-                                      merge_mode=merge_mode)
+                                      force_grid=force_grid, force_variant=force_variant)
     torch.cuda.synchronize()
     assert gqa.gqa_prefill_poll() == 0, "device-side wait timed out"
     return out, lse, plan

@@ -50,7 +50,7 @@ def test_bounds_checked_build_exports_the_same_abi(gqa):
 
 
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 10
+    assert gqa.gqa_prefill_abi_version() == 11
 
 
 def test_refusals_before_any_cuda_call(gqa):
@@ -159,10 +159,8 @@ def test_planner_invariants(gqa, q_len, kv_len, sms, force, variant):
         assert 1 <= workers <= sms // cpi
         pieces, split = _balanced_cut(tail, workers)
         assert p["n_units"] == head + pieces
-        assert p["fused_merge"] in ((0, 1) if split else (0,))
-        assert p["kernels_per_call"] == (2 if split and not p["fused_merge"] else 1)
-        assert p["workspace_bytes"] == (2 * workers * cpi * 128 * 257 * 4 if split else 0) + (
-            2 * 2 * workers * cpi * 8 if p["fused_merge"] else 0)
+        assert p["kernels_per_call"] == (2 if split else 1)
+        assert p["workspace_bytes"] == (2 * workers * cpi * 128 * 257 * 4 if split else 0)
     else:
         assert 1 <= p["tail_splits"] <= max(shortest, 1)
         if force > 0:
@@ -170,11 +168,9 @@ def test_planner_invariants(gqa, q_len, kv_len, sms, force, variant):
         assert p["n_units"] == head + p["tail_items"] * p["tail_splits"]
         assert 1 <= workers <= min(sms // cpi, p["n_units"])
         split = p["tail_splits"] > 1 and p["tail_items"] > 0
-        assert p["fused_merge"] in ((0, 1) if split else (0,))
-        assert p["kernels_per_call"] == (2 if split and not p["fused_merge"] else 1)
+        assert p["kernels_per_call"] == (2 if split else 1)
         assert p["workspace_bytes"] == (
-            p["tail_items"] * p["tail_splits"] * cpi * 128 * 257 * 4 if split else 0) + (
-            2 * p["tail_items"] * p["tail_splits"] * cpi * 8 if p["fused_merge"] else 0)
+            p["tail_items"] * p["tail_splits"] * cpi * 128 * 257 * 4 if split else 0)
     assert p["est_makespan_tiles"] * workers >= W  # the busiest worker carries at least the mean
     _, again = gqa.gqa_prefill_make_plan(q_len, kv_len, 24, 4, 256, sms, force_splits=force,
                                          force_variant=variant)

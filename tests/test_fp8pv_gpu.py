@@ -103,13 +103,12 @@ def test_fp8pv_small_shapes_every_element(cuda_device, q_len, kv_len, variant):
         assert np.all(np.abs(got[0] - want) <= 2.0 ** -8 * np.abs(want) + 1e-7)
 
 
-@pytest.mark.parametrize("splits,grid,variant,merge", [(3, 0, 1, 0), (3, 5, 1, 1), (2, 0, 2, 0),
-                                                       (3, 6, 2, 1), (32, 0, 1, 0), (-1, 0, 1, 1),
-                                                       (-1, 6, 2, 0)])
-def test_fp8pv_split_tail_every_element(cuda_device, splits, grid, variant, merge):
+@pytest.mark.parametrize("splits,grid,variant", [(3, 0, 1), (3, 5, 1), (2, 0, 2), (3, 6, 2),
+                                                 (32, 0, 1), (-1, 0, 1), (-1, 6, 2)])
+def test_fp8pv_split_tail_every_element(cuda_device, splits, grid, variant):
     q, k, v = make_qkv(129, 1000, seed=37)
     out, lse, _ = run_fp8pv(q, k, v, SCALE, force_splits=splits, force_grid=grid,
-                            force_variant=variant, merge_mode=merge)
+                            force_variant=variant)
     ref_o, ref_l, bound = oracle_fp8pv(q, k, v, SCALE)
     check_pv(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l, bound,
              f"fp8pv split {splits} grid {grid}")

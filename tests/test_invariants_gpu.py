@@ -15,21 +15,6 @@ pytestmark = pytest.mark.gpu
 SCALE = 1.0 / 16.0
 
 
-@pytest.mark.parametrize("name,splits", [("q512_kv4096_kbias", 3), ("q512_kv4096_kbias", -1),
-                                         ("q4096_kv8192", 4), ("q512_kv32768", -1)])
-@pytest.mark.parametrize("variant", [1, 2])
-def test_merge_inside_the_kernel_is_bit_stable(cuda_device, name, splits, variant):
-    """Which CTA completes a split item, and so merges it, changes from run to run; the
-    merge's arithmetic (fixed piece order) does not, so the bits do not either."""
-    w = WORKLOADS[name]
-    q, k, v = make_workload(w)
-    runs = [run_gpu(q, k, v, w.scale, force_splits=splits, force_variant=variant, merge_mode=1)
-            for _ in range(3)]
-    assert runs[0][2]["fused_merge"] == 1
-    for o, l, _ in runs[1:]:
-        assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1])
-
-
 @pytest.mark.parametrize("name", list(WORKLOADS))
 @pytest.mark.parametrize("variant", [0, 1, 2])
 def test_run_twice_bit_identical(cuda_device, name, variant):
@@ -65,15 +50,13 @@ def test_future_keys_leave_earlier_rows_bit_identical(cuda_device, q_len, kv_len
 
 @pytest.mark.parametrize("name", ["q512_kv4096_kbias", "q4096_kv8192"])
 @pytest.mark.parametrize("variant", [1, 2])
-@pytest.mark.parametrize("merge", [1, 2])
-def test_whole_and_cut_items_agree(cuda_device, name, variant, merge):
+def test_whole_and_cut_items_agree(cuda_device, name, variant):
     w = WORKLOADS[name]
     q, k, v = make_workload(w)
     o1, l1, p1 = run_gpu(q, k, v, SCALE, force_splits=1, force_variant=variant)
-    o2, l2, p2 = run_gpu(q, k, v, SCALE, force_splits=4, force_variant=variant, merge_mode=merge)
+    o2, l2, p2 = run_gpu(q, k, v, SCALE, force_splits=4, force_variant=variant)
     assert p1["tail_splits"] == 1 and p1["kernels_per_call"] == 1
-    assert p2["tail_splits"] == 4 and p2["tail_items"] > 0
-    assert p2["fused_merge"] == (merge == 1) and p2["kernels_per_call"] == merge
+    assert p2["tail_splits"] == 4 and p2["tail_items"] > 0 and p2["kernels_per_call"] == 2
     check_close(o2.double().cpu().numpy(), l2.double().cpu().numpy(),
                 o1.double().cpu().numpy(), l1.double().cpu().numpy(), "cut vs whole items")
 

@@ -47,31 +47,18 @@ def test_small_shapes_every_element(cuda_device, q_len, kv_len, variant):
                 f"{q_len}x{kv_len}")
 
 
-MERGES = [1, 2]  # merge_mode: inside the attention kernel / a separate merge kernel
-
-
-def check_merge_route(plan, merge_mode):
-    """The plan merged split items the way merge_mode asked (where it split any)."""
-    split = plan["workspace_bytes"] > 0
-    assert plan["fused_merge"] == (1 if split and merge_mode == 1 else 0)
-    assert plan["kernels_per_call"] == (2 if split and merge_mode == 2 else 1)
-
-
 @pytest.mark.parametrize("q_len,kv_len", [(22, 1000), (129, 1000), (43, 257), (7, 700), (300, 300)])
 @pytest.mark.parametrize("splits,grid,variant", [(2, 0, 1), (3, 0, 1), (7, 0, 1), (3, 5, 1),
                                                  (2, 11, 1), (4, 1, 1), (2, 0, 2), (3, 0, 2),
                                                  (3, 6, 2), (2, 10, 2), (5, 2, 2)])
-@pytest.mark.parametrize("merge", MERGES)
-def test_split_tail_every_element(cuda_device, q_len, kv_len, splits, grid, variant, merge):
+def test_split_tail_every_element(cuda_device, q_len, kv_len, splits, grid, variant):
     """Items split into KV pieces and merged: all items (grid >= items) or only the
-    items after whole rounds on a few CTAs (small grid); one CTA or a CTA pair per item;
-    merged inside the attention kernel or by the separate pass."""
+    items after whole rounds on a few CTAs (small grid); one CTA or a CTA pair per item."""
     q, k, v = make_qkv(q_len, kv_len, seed=11 * q_len + kv_len)
     out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_grid=grid,
-                             force_variant=variant, merge_mode=merge)
+                             force_variant=variant)
     assert plan["grid"] <= (grid or plan["num_sms"]) and plan["variant"] == variant
-    assert (plan["workspace_bytes"] > 0) == (plan["tail_splits"] > 1 and plan["tail_items"] > 0)
-    check_merge_route(plan, merge)
+    assert plan["kernels_per_call"] == (2 if plan["tail_splits"] > 1 and plan["tail_items"] else 1)
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
                 f"{q_len}x{kv_len} splits {splits} grid {grid}")
@@ -80,17 +67,15 @@ def test_split_tail_every_element(cuda_device, q_len, kv_len, splits, grid, vari
 @pytest.mark.parametrize("q_len,kv_len", [(22, 4096), (129, 2200), (300, 4096)])
 @pytest.mark.parametrize("splits,grid,variant", [(16, 0, 1), (31, 0, 1), (17, 9, 1), (16, 0, 2),
                                                  (20, 6, 2)])
-@pytest.mark.parametrize("merge", MERGES)
-def test_many_pieces_every_element(cuda_device, q_len, kv_len, splits, grid, variant, merge):
-    """16 or more KV pieces per item: the separate merge takes a block per output row,
-    its warps each combining a subset of the pieces (the decode-sized merge); the
-    in-kernel merge stages a few rows of every piece per chunk."""
+def test_many_pieces_every_element(cuda_device, q_len, kv_len, splits, grid, variant):
+    """16 or more KV pieces per item: the merge takes a block per output row, its
+    warps each combining a subset of the pieces (the decode-sized merge)."""
     q, k, v = make_qkv(q_len, kv_len, seed=23 * q_len + kv_len)
     out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_grid=grid,
-                             force_variant=variant, merge_mode=merge)
+                             force_variant=variant)
     # S is capped at the fewest KV tiles of an item (17 for 129x2200)
     assert plan["tail_items"] > 0 and 16 <= plan["tail_splits"] <= splits
-    check_merge_route(plan, merge)
+    assert plan["kernels_per_call"] == 2
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
                 f"{q_len}x{kv_len} splits {splits} grid {grid}")
@@ -103,15 +88,13 @@ BALANCED = -1  # force_splits value of the balanced tail (GQA_FORCE_BALANCED_TAI
                                           (1, 129), (512, 4096)])
 @pytest.mark.parametrize("grid,variant", [(0, 1), (0, 2), (5, 1), (3, 1), (6, 2), (10, 2), (152, 1),
                                           (38, 1), (76, 2)])
-@pytest.mark.parametrize("merge", MERGES)
-def test_balanced_tail_every_element(cuda_device, q_len, kv_len, grid, variant, merge):
+def test_balanced_tail_every_element(cuda_device, q_len, kv_len, grid, variant):
     """The balanced tail: the tail items' tiles laid end to end and cut into equal
     shares, one per CTA (pair), whole rounds first where they fit; items cut at
     any tile, pieces merged from per-worker slots."""
     q, k, v = make_qkv(q_len, kv_len, seed=19 * q_len + kv_len)
     out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=BALANCED, force_grid=grid,
-                             force_variant=variant, merge_mode=merge)
-    check_merge_route(plan, merge)
+                             force_variant=variant)
     assert plan["variant"] == variant and plan["grid"] <= (grid or plan["num_sms"])
     assert plan["tail_splits"] == 0
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
@@ -181,19 +164,15 @@ def test_lse_may_be_null(cuda_device):
 @pytest.mark.parametrize("q_len", [1, 2, 3, 4])
 @pytest.mark.parametrize("kv_len", [4096, 32768])
 @pytest.mark.parametrize("splits,variant", [(0, 0), (32, 1), (24, 2), (5, 1), (-1, 1), (-1, 2)])
-@pytest.mark.parametrize("merge", [0] + MERGES)
-def test_decode_shapes_every_element(cuda_device, q_len, kv_len, splits, variant, merge):
+def test_decode_shapes_every_element(cuda_device, q_len, kv_len, splits, variant):
     """Decode-sized chunks (one to four new tokens, 6 to 24 live MMA rows) over a long
     prefix: the whole KV range is cut into many pieces and merged."""
     q, k, v = make_qkv(q_len, kv_len, seed=17 * q_len + kv_len)
-    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_variant=variant,
-                             merge_mode=merge)
+    out, lse, plan = run_gpu(q, k, v, SCALE, force_splits=splits, force_variant=variant)
     if splits > 0:
-        assert plan["tail_splits"] == splits
+        assert plan["tail_splits"] == splits and plan["kernels_per_call"] == 2
     if splits < 0:
-        assert plan["tail_splits"] == 0
-    if splits != 0 and merge:
-        check_merge_route(plan, merge)
+        assert plan["tail_splits"] == 0 and plan["kernels_per_call"] == 2
     ref_o, ref_l = oracle.attention(q, k, v, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
                 f"decode {q_len}x{kv_len} S {splits}")

@@ -75,8 +75,7 @@ def test_varlen_split_tails_every_element(cuda_device, splits, grid, variant):
     # A balanced tail on a small grid may find worker boundaries on item boundaries
     # (nothing split, no workspace); on the full grid it cuts items.
     assert plan["workspace_bytes"] > 0 or (splits < 0 and grid > 0)
-    assert plan["kernels_per_call"] == (2 if plan["workspace_bytes"] and not plan["fused_merge"]
-                                        else 1)
+    assert plan["kernels_per_call"] == (2 if plan["workspace_bytes"] else 1)
     assert (plan["tail_splits"] == 0) == (splits < 0)
     ref_o, ref_l = oracle.varlen_attention(q, k, v, cu_q, cu_k, SCALE)
     check_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_l,
