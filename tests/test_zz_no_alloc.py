@@ -8,8 +8,9 @@ Checks, through the C ABI: on workloads whose plan splits work items along
 the KV range (so the scratch really holds partials), two calls in a row each
 match the allocating entry point within the suite's tolerance; a call whose
 partials would not fit is refused with GQA_ERR_SCRATCH and writes nothing (on
-devices where such a plan exists). This file is collected last,
-and it also passes when run alone in a fresh process."""
+devices where such a plan exists); and calls with growing split partials leave
+the device's free memory unchanged. This file is collected last, and it also
+passes when run alone in a fresh process."""
 import pytest
 import torch
 
@@ -82,3 +83,54 @@ def test_noalloc_refuses_partials_larger_than_scratch(cuda_device):
     assert rc == gqa.GqaStatus.ERR_SCRATCH
     torch.cuda.synchronize()
     assert torch.all(out == 3.0)
+
+
+_NO_ALLOC_CHILD = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+import gqa_chunked_prefill_gb300 as gqa
+from gqa_inputs import make_qkv
+dev = torch.device("cuda:0")
+cases = [(129, 1000), (512, 4096), (512, 32768)]  # split plans, growing partials
+sms, pairs = gqa.gqa_prefill_device_info()
+ws = [gqa.gqa_prefill_make_plan(a, b, 24, 4, 256, sms, max_pairs=pairs)[1]["workspace_bytes"]
+      for a, b in cases]
+assert 0 < ws[0] < ws[-1], ws
+bufs = []
+for q_len, kv_len in cases:
+    q, k, v = (t.to(dev) for t in make_qkv(q_len, kv_len, seed=q_len))
+    out = torch.empty_like(q)
+    lse = torch.empty((q_len, 24), dtype=torch.float32, device=dev)
+    bufs.append((q, k, v, out, lse, q_len, kv_len))
+torch.cuda.synchronize()
+q, k, v, out, lse, q_len, kv_len = bufs[0]
+gqa.gqa_prefill_attn_noalloc(q, k, v, out, lse, q_len, kv_len, 24, 4, 256, 1 / 16)  # set-up
+torch.cuda.synchronize()
+free0 = torch.cuda.mem_get_info()[0]
+for q, k, v, out, lse, q_len, kv_len in bufs:
+    for _ in range(2):
+        gqa.gqa_prefill_attn_noalloc(q, k, v, out, lse, q_len, kv_len, 24, 4, 256, 1 / 16)
+torch.cuda.synchronize()
+free1 = torch.cuda.mem_get_info()[0]
+assert gqa.gqa_prefill_poll() == 0
+print("free", free0, free1, "workspace", ws)
+assert free1 == free0, (free0, free1)
+"""
+
+
+def test_noalloc_allocates_no_device_memory(cuda_device):
+    """The promise itself: in a fresh process (no earlier call has grown any pool;
+    every kernel loaded up front), after one warm-up call that does the one-time
+    set-up, calls whose split partials grow from the smallest to the largest of
+    three plans leave the device's free memory exactly unchanged. A version that
+    took the partials from an allocator would have to grow it for the larger plans."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    # Eager module loading: every kernel of the library is resident before the
+    # measurement, so a first launch cannot take device memory for its code.
+    env = dict(os.environ, CUDA_MODULE_LOADING="EAGER")
+    r = subprocess.run([sys.executable, "-c", _NO_ALLOC_CHILD, root], capture_output=True,
+                       text=True, timeout=600, env=env)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-3000:]
