@@ -610,6 +610,10 @@ def main():
             ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(40)]
             torch.cuda.synchronize(dev)
+            # A call takes tens of microseconds, about what the host needs to issue one:
+            # the host queues all of them while the GPU spins (~5 ms), so no event pair
+            # holds GPU idle time waiting for the next launch.
+            torch.cuda._sleep(10_000_000)
             for i, (a, b) in enumerate(ev):
                 a.record(stream)
                 calls[i % n_rot]()

@@ -23,9 +23,13 @@
 //    the PV that read it has completed (pv_done[b]). tcgen05 only orders
 //    consecutive MMAs that share accumulator and shape, so these two barriers
 //    are what makes the S -> QK^T and P -> PV reuse safe.
-//  * Warp specialisation: warp 4 issues TMA, warp 5 issues MMAs (one thread),
-//    warps 0-3 run the softmax with one thread per MMA row (tensor-memory lane),
-//    so row max and row sum need no cross-thread reduction.
+//  * Warp specialisation: one warp issues TMA, one issues MMAs (one thread), and
+//    the softmax warps take the MMA rows (tensor-memory lanes). BF16 QK^T: warps
+//    0-3, one thread per row, so row max and row sum need no cross-thread
+//    reduction. Quantised PV, where the softmax (not the tensor core) sets the
+//    pace: warps 0-7, two threads per row on 64 keys of each tile each, which
+//    trade the row's tile maximum through shared memory; two warps per
+//    scheduler hide each other's latencies.
 //  * Online softmax in base 2 with the scale folded into one FMA. O is only
 //    rescaled when a row's running max grows by more than 2^8; otherwise the
 //    stale max is kept, which is exact after the final division by the row sum.
@@ -65,9 +69,6 @@ constexpr uint32_t kTmemO = 0;    // O: 256 FP32 columns
 constexpr uint32_t kTmemS = 256;  // S: 128 FP32 columns
 constexpr uint32_t kTmemP = 384;  // P buffer b: 64 columns of packed BF16 pairs at kTmemP + 64*b
 
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
-
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffStages = kOffQ + kQBytes;
@@ -86,17 +87,24 @@ enum BarId : uint32_t {
   kBarOFree,                    // epilogue finished reading O (128 arrivals)
   kBarDrain,                    // MMA warp's final drain
   kBarScFull,                   // [kScSlots] FP8 QK^T: key scales of a tile loaded (TMA tx)
-  kBarScEmpty = kBarScFull + 8, // [kScSlots] this CTA's softmax done with them (128 arrivals)
-  kNumBars = kBarScEmpty + 8
+  kBarScEmpty = kBarScFull + 8, // [kScSlots] this CTA's softmax done with them (all its softmax threads)
+  kBarXch = kBarScEmpty + 8,    // [4] FP8: the two softmax threads of each row of a 32-row
+                                //   quarter traded a value (64 arrivals)
+  kNumBars = kBarXch + 4
 };
 // FP8 QK^T: Q codes take 2 of the 4 Q chunks; the key-scale ring (one 128-key
 // FP32 row per slot, consumed by the softmax warps) lives in the other half.
 constexpr int kScSlots = 8;
 constexpr uint32_t kScSlotBytes = 128 * 4;
 constexpr uint32_t kOffScales = kOffQ + 2 * kQChunkBytes;
+// FP8: the values the two softmax threads of a row trade (two slots x two
+// halves x 128 rows of FP32), after the key-scale ring.
+constexpr uint32_t kOffXch = kOffScales + kScSlots * kScSlotBytes;
+static_assert(kOffXch + 2 * 2 * 128 * 4 <= kOffQ + kQBytes, "exchange slots fit beside the FP8 Q codes");
 constexpr uint32_t kOffTmemSlot = kOffBars + kNumBars * 8;
 constexpr uint32_t kSmemUsed = kOffTmemSlot + 16;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;  // room to align the base up to 1024
+static_assert(kSmemAlloc <= 227 * 1024, "dynamic shared memory of one CTA on sm_103a");
 
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
@@ -267,6 +275,20 @@ __device__ __noinline__ void issue_paged_scales(const PagedGeom& pgeo, const int
 // codes with one FP32 scale per query (token, head) and per key (token, KV
 // head); S = Q_q K_q^T is a kind::f8f6f4 MMA, and every score is restored as
 // S * s_q * s_k * scale before the softmax. PV stays BF16.
+// Tensor-memory load / store of one thread's N consecutive 32-bit columns.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N == 64 || N == 128, "64 or 128 columns");
+  if constexpr (N == 64) ptx::tmem_ld_x64(taddr, r); else ptx::tmem_ld_x128(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
+  static_assert(N == 16 || N == 32 || N == 64, "16, 32 or 64 columns");
+  if constexpr (N == 16) ptx::tmem_st_x16(taddr, r);
+  else if constexpr (N == 32) ptx::tmem_st_x32(taddr, r);
+  else ptx::tmem_st_x64(taddr, r);
+}
+
 // Transpose of an 8 x 8 matrix of 16-byte quads held by a group of 8 lanes
 // (aligned: lanes 8i .. 8i+7), lane j holding row j: afterwards lane j holds
 // column j, e[s] = old e[j] of lane s. Three butterfly stages; in stage m the
@@ -296,12 +318,21 @@ __device__ __forceinline__ void transpose8_quads(uint4 (&e)[8], int j) {
 // sequences packed end to end (the V box of a sequence's last tile goes in 16-key
 // pieces so that the next sequence's values never reach it).
 template <bool kPair, int kKv, int kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(fwd_threads(kFp8), 1)
     gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
   constexpr bool kPaged = kKv == 1;
   constexpr bool kDenseBatch = kKv == 2;
   static_assert(kFp8 != 2 || kKv == 0, "quantised PV reads the dense V of one sequence");
   constexpr bool kFp8Pv = kFp8 == 2;
+  // Warp roles: softmax warps 0 .. kSmWarps-1, then the TMA warp and the MMA warp.
+  // With 8 softmax warps, warps q and q + 4 share the MMA rows (tensor-memory
+  // lanes) 32q .. 32q+31 and take keys 0-63 and 64-127 of every tile.
+  constexpr int kSmWarps = fwd_softmax_warps(kFp8);
+  constexpr int kTmaWarp = kSmWarps;
+  constexpr int kMmaWarp = kSmWarps + 1;
+  constexpr int kHalves = kSmWarps / 4;  // softmax threads per MMA row
+  constexpr int kCols = 128 / kHalves;   // scores of a tile per softmax thread
+  static_assert(kHalves == 1 || kFp8 == 2, "the split softmax uses the exchange slots of the FP8 layout");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -323,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto commit = [&](uint32_t id) {
     if constexpr (kPair) ptx::tc_commit_pair(bar(id)); else ptx::tc_commit(bar(id));
   };
-  constexpr uint32_t kConsumers = (kPair ? 2 : 1) * 4 * 32;  // softmax threads per item
+  constexpr uint32_t kConsumers = (kPair ? 2 : 1) * kSmWarps * 32;  // softmax threads per item
   // Shared-memory layout of a K or V stage (its keys x nch 64-column chunks,
   // 128-byte rows, 128B swizzle). Dense K/V: chunk-major, each chunk's keys
   // contiguous (one 4-D copy per stage). Paged K/V: 8-key groups outermost with
@@ -371,9 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (kFp8) {
       for (int i = 0; i < kScSlots; ++i) {
         ptx::mbar_init(bar(kBarScFull + i), 1);
-        ptx::mbar_init(bar(kBarScEmpty + i), 4 * 32);  // this CTA's softmax threads
+        ptx::mbar_init(bar(kBarScEmpty + i), kSmWarps * 32);  // this CTA's softmax threads
       }
     }
+    if constexpr (kHalves == 2)
+      for (int i = 0; i < 4; ++i) ptx::mbar_init(bar(kBarXch + i), 2 * 32);
     ptx::fence_mbar_init();
   }
   if (warp < 4) {
@@ -728,9 +761,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ======================= softmax + correction + epilogue (warps 0-3) =======
-    const int row = threadIdx.x;  // MMA row == tensor-memory lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // ======================= softmax + correction + epilogue (softmax warps) ===
+    // Warp w owns MMA rows 32 (w % 4) .. +31 (a warp reaches only its quarter of
+    // the tensor-memory lanes). With two threads per row, half hf = w / 4 takes
+    // keys 64 hf .. 64 hf + 63 of every tile and columns 128 hf .. 128 hf + 127
+    // of O; the two trade the row's tile maximum and, at the end, its sum.
+    const int qw = warp & 3;
+    const int hf = kHalves == 2 ? warp >> 2 : 0;
+    const int row = qw * 32 + lane;  // MMA row == tensor-memory lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    const int kc0 = kCols * hf;                 // this thread's first key of a tile
+    const int oc0 = (kHeadDim / kHalves) * hf;  // ... and first column of O
+    // Trade of one value between the two threads of a row through shared memory:
+    // slot xph & 1, then phase xph of the quarter's barrier (both threads trade in
+    // the same order, so their counts agree; a slot is rewritten two trades later,
+    // after the partner's next arrival, so its read of this one is done).
+    uint32_t xph = 0;
+    float* const xch = reinterpret_cast<float*>(smem + kOffXch);
+    auto trade = [&](float v, float& other) -> bool {
+      float* const slot = xch + (xph & 1u) * 256;
+      slot[hf * 128 + row] = v;
+      ptx::mbar_arrive(bar(kBarXch + qw));
+      const bool good = __all_sync(0xffffffffu, wait_bar(bar(kBarXch + qw), xph & 1u, p));
+      other = slot[(hf ^ 1) * 128 + row];
+      ++xph;
+      return good;
+    };
     const int tl = row / kGroup;
     const int hj = row - tl * kGroup;
     const float sl2 = p.scale_log2;
@@ -764,22 +820,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, wait_bar(bar(kBarSFull), T & 1u, p));
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t sr[128];
-        ptx::tmem_ld_x128(lane_addr + kTmemS, sr);  // includes tcgen05.wait::ld
+        uint32_t sr[kCols];
+        tmem_ld_n(lane_addr + kTmemS + kc0, sr);  // includes tcgen05.wait::ld
         ptx::tc_fence_before();
         arrive_leader(kBarSFree);  // the next QK^T may overwrite S now
-        float s[128];
+        float s[kCols];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        for (int c = 0; c < kCols; ++c) s[c] = __uint_as_float(sr[c]);
         if constexpr (kFp8) {
           // Restore each key's scale before the softmax (the report's §1: scales
           // change the relative probabilities, so they cannot wait until after).
           const uint32_t slot = T % kScSlots;
           ok = __all_sync(0xffffffffu, wait_bar(bar(kBarScFull + slot), (T / kScSlots) & 1u, p));
           if (!ok) break;
-          const float4* ks = reinterpret_cast<const float4*>(smem + kOffScales + slot * kScSlotBytes);
+          const float4* ks =
+              reinterpret_cast<const float4*>(smem + kOffScales + slot * kScSlotBytes) + kc0 / 4;
 #pragma unroll
-          for (int c = 0; c < 128; c += 4) {
+          for (int c = 0; c < kCols; c += 4) {
             const float4 k4 = ks[c / 4];
             float a0, a1, a2, a3;
             ptx::f32x2_split(ptx::mul_f32x2(ptx::f32x2(s[c], s[c + 1]), ptx::f32x2(k4.x, k4.y)), a0, a1);
@@ -791,23 +848,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::mbar_arrive(bar(kBarScEmpty + slot));
         }
-        const int key0 = (w.n0 + j) * kBlockN;
-        if (key0 + kBlockN - 1 > tile_min_pos) {
+        const int key0 = (w.n0 + j) * kBlockN + kc0;  // key of s[0]
+        if (key0 + kCols - 1 > tile_min_pos) {
           // Diagonal tile: keys after this row's position are masked out.
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
+          for (int c = 0; c < kCols; ++c)
             if (key0 + c > pos) s[c] = kNegInf;
         }
-        // Row maximum: four running maxima over s[0..127], eight scores a step.
+        // Row maximum: four running maxima over s[], eight scores a step.
         float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
 #pragma unroll
-        for (int c = 0; c < 128; c += 8) {
+        for (int c = 0; c < kCols; c += 8) {
           mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
           mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
           mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
           mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
         }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * rowfac;
+        // (rowfac > 0: scaling each half's maximum gives the scaled row maximum exactly.)
+        float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * rowfac;
+        if constexpr (kHalves == 2) {
+          float m_other;
+          ok = trade(m_tile, m_other);
+          if (!ok) break;
+          m_tile = fmaxf(m_tile, m_other);
+        }
         const float m_new = fmaxf(m_ref, m_tile);
         const bool need = m_new > m_ref + (kFp8Pv ? kRescaleThresholdPv : kRescaleThreshold);
         if (j == 0) {
@@ -822,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ptx::tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 256; c += 32) {
+          for (int c = oc0; c < oc0 + kHeadDim / kHalves; c += 32) {
             uint32_t o[32];
             ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
 #pragma unroll
@@ -833,14 +897,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float m_use = (m_ref == kNegInf) ? 0.0f : m_ref;
         // BF16 P: two values per tensor-memory column; E4M3 P (quantised PV): four.
-        uint32_t pk[kFp8Pv ? 32 : 64];
+        uint32_t pk[kFp8Pv ? kCols / 4 : kCols / 2];
         // p = 2^(s*scale*log2e - m): one packed FMA per pair, two ex2, one packed add.
         const uint64_t scale2 = ptx::f32x2(rowfac, rowfac);
         const float pofs = kFp8Pv ? kPScaleLog2Pv - m_use : -m_use;
         const uint64_t neg_m2 = ptx::f32x2(pofs, pofs);
         uint64_t sum2 = ptx::f32x2(0.0f, 0.0f);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < kCols / 2; ++c) {
           float x0, x1;
           ptx::f32x2_split(ptx::fma_f32x2(ptx::f32x2(s[2 * c], s[2 * c + 1]), scale2, neg_m2), x0, x1);
           const float e0 = ptx::ex2_approx(x0);
@@ -863,8 +927,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ptx::tc_fence_after();
         }
-        if constexpr (kFp8Pv) ptx::tmem_st_x32(lane_addr + kTmemP + 64u * b, pk);
-        else ptx::tmem_st_x64(lane_addr + kTmemP + 64u * b, pk);
+        // Key k of the tile sits in P column k / 2 (BF16) or k / 4 (E4M3).
+        tmem_st_n(lane_addr + kTmemP + 64u * b + (kFp8Pv ? kc0 / 4 : kc0 / 2), pk);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         arrive_leader(b ? kBarPFull1 : kBarPFull0);
@@ -876,6 +940,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             (T_last >> 1) & 1u, p));
       if (!ok) break;
       ptx::tc_fence_after();
+      if constexpr (kHalves == 2) {  // the row sum: both halves' (IEEE + commutes: the same in both)
+        float l_other;
+        ok = trade(l, l_other);
+        if (!ok) break;
+        l += l_other;
+      }
       const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
       // (Quantised PV: l sums 2^6 p, so the scale's exponent comes off.)
       const float lse2 = l > 0.0f ? m_ref + __log2f(l) - (kFp8Pv ? kPScaleLog2Pv : 0.0f) : kNegInf;
@@ -899,7 +969,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // store instruction writes 128 contiguous bytes of 4 rows instead of 16
       // bytes of 32 rows (the output rows are 512 bytes, partial rows 1 KB apart).
       const int gl = lane & 7;                    // lane within its group of 8
-      const int grow0 = warp * 32 + (lane & ~7);  // MMA row of the group's lane 0
+      const int grow0 = qw * 32 + (lane & ~7);  // MMA row of the group's lane 0
       auto group_row = [&](int s_, int& tok_s) -> bool {
         const int r = grow0 + s_;
         tok_s = tok0 + r / kGroup;
@@ -917,7 +987,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           vmask |= (v_ ? 1u : 0u) << s_;
         }
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 64) {
+        for (int c = oc0; c < oc0 + kHeadDim / kHalves; c += 64) {
           uint4 e[8];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -942,7 +1012,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 row_ok(static_cast<long long>(off[s_] / kHeadDim), p.out_rows, p.status))
               *reinterpret_cast<uint4*>(p.out + off[s_] + c + 8 * gl) = e[s_];
         }
-        if (valid && p.lse != nullptr && row_ok(static_cast<long long>(qrow), p.out_rows, p.status))
+        if (hf == 0 && valid && p.lse != nullptr &&
+            row_ok(static_cast<long long>(qrow), p.out_rows, p.status))
           p.lse[qrow] = lse2 * kLn2;
       } else {
         // A piece of a split item: normalised partial rows go to the piece's slot
@@ -957,7 +1028,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float* base = p.part_o + (slot_row0 + grow0) * kHeadDim;
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
+        for (int c = oc0; c < oc0 + kHeadDim / kHalves; c += 32) {
           uint32_t o[32];
           ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
           float f[32];
@@ -976,7 +1047,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 row_ok(static_cast<long long>(slot_row0 + grow0 + s_), p.part_rows, p.status))
               *reinterpret_cast<uint4*>(base + static_cast<size_t>(s_) * kHeadDim + c + 4 * gl) = e[s_];
         }
-        if (valid && row_ok(static_cast<long long>(slot_row0 + row), p.part_rows, p.status))
+        if (hf == 0 && valid && row_ok(static_cast<long long>(slot_row0 + row), p.part_rows, p.status))
           p.part_lse[slot_row0 + row] = lse2;
       }
       ptx::tc_fence_before();
@@ -1291,11 +1362,22 @@ cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, bool pair,
 }  // namespace
 
 cudaError_t max_active_pairs(int* pairs) {
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = launch_config(dim3(2), dim3(kThreads), kSmemAlloc, true, nullptr, attr);
-  cfg.attrs = attr + 1;  // occupancy of the cluster shape only
-  cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(pairs, gqa_attn_fwd_sm103_kernel<true, 0, 0>, &cfg);
+  // The smaller of the 4- and 8-softmax-warp pair kernels' counts (block sizes differ).
+  int n[2] = {0, 0};
+  for (int i = 0; i < 2; ++i) {
+    const int fp8 = 2 * i;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg =
+        launch_config(dim3(2), dim3(fwd_threads(fp8)), kSmemAlloc, true, nullptr, attr);
+    cfg.attrs = attr + 1;  // occupancy of the cluster shape only
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(
+        n + i, fp8 ? gqa_attn_fwd_sm103_kernel<true, 0, 2> : gqa_attn_fwd_sm103_kernel<true, 0, 0>,
+        &cfg);
+    if (e != cudaSuccess) return e;
+  }
+  *pairs = std::min(n[0], n[1]);
+  return cudaSuccess;
 }
 
 template <bool kPair>
@@ -1314,7 +1396,7 @@ cudaError_t launch_fwd_of(const cudaLaunchConfig_t& cfg, const FwdParams& p, int
 cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, int kv, int fp8,
                        cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = launch_config(dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+  const cudaLaunchConfig_t cfg = launch_config(dim3(static_cast<unsigned>(grid)), dim3(fwd_threads(fp8)),
                                                kSmemAlloc, pair, stream, attr);
   return pair ? launch_fwd_of<true>(cfg, p, kv, fp8) : launch_fwd_of<false>(cfg, p, kv, fp8);
 }

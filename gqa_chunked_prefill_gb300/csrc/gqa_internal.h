@@ -21,7 +21,11 @@ constexpr int kTokPerTile = 21;
 constexpr int kRowsPerTile = 128;
 constexpr int kBlockN = 128;  // keys per KV tile
 
-constexpr int kThreads = 192;  // 4 softmax warps, 1 TMA warp, 1 MMA warp
+// Softmax warps of the attention kernel (fp8: 0 BF16, 1 FP8 QK^T, 2 FP8 QK^T and
+// PV): 4, one thread per MMA row; with quantised PV 8, two threads per row on 64
+// of a tile's 128 scores each. Then one TMA warp and one MMA warp.
+constexpr int fwd_softmax_warps(int fp8) { return fp8 == 2 ? 8 : 4; }
+constexpr int fwd_threads(int fp8) { return (fwd_softmax_warps(fp8) + 2) * 32; }
 
 struct FwdParams {
   CUtensorMap tmap_q;  // Q [q_len][24][256], box (64 d, 6 heads, 21 tokens), 128B swizzle
@@ -103,10 +107,11 @@ struct ScaleColumns {
   int row_begin[kMaxSeqs + 1];
   int col_begin[kMaxSeqs];
 };
-// E4M3 codes and scales of rows x heads vectors of 256 BF16 values (quantize_fp8.cu).
+// E4M3 codes and scales of rows x heads vectors of 256 BF16 values (quantize_fp8.cu);
+// num_sms sizes the persistent grid.
 cudaError_t launch_quantize_fp8(const void* x, void* codes, float* scale, int rows, int heads,
                                 int scale_stride, bool head_major, const ScaleColumns& cols,
-                                cudaStream_t stream);
+                                int num_sms, cudaStream_t stream);
 // E4M3 codes of V transposed to [4][256][v_stride] and per-(head, channel) scales
 // [4][256] (quantize_fp8.cu).
 cudaError_t launch_quantize_v_fp8(const void* v, void* codes, float* scale, int kv_len,

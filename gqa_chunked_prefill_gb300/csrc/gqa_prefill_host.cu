@@ -967,8 +967,11 @@ gqa_status gqa_quantize_q_fp8(const void* q, void* q_fp8, float* q_scale, int q_
   if (!q || !q_fp8 || !q_scale) return GQA_ERR_NULL;
   if (gqa::misaligned(q) || gqa::misaligned(q_fp8) || (reinterpret_cast<uintptr_t>(q_scale) & 3u))
     return GQA_ERR_ALIGN;
+  gqa::DeviceInfo* di = nullptr;
+  if (const gqa_status st = gqa::device_info(&di); st != GQA_OK) return st;
   return gqa::launch_quantize_fp8(q, q_fp8, q_scale, q_len, gqa::kQHeads, 0, false,
-                                  one_sequence(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+                                  one_sequence(), di->num_sms,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? GQA_OK
              : GQA_ERR_CUDA;
 }
@@ -982,8 +985,11 @@ gqa_status gqa_quantize_k_fp8(const void* k, void* k_fp8, float* k_scale, int kv
   if (kv_len == 0) return GQA_OK;
   if (!k || !k_fp8 || !k_scale) return GQA_ERR_NULL;
   if (gqa::misaligned(k) || gqa::misaligned(k_fp8) || gqa::misaligned(k_scale)) return GQA_ERR_ALIGN;
+  gqa::DeviceInfo* di = nullptr;
+  if (const gqa_status st = gqa::device_info(&di); st != GQA_OK) return st;
   return gqa::launch_quantize_fp8(k, k_fp8, k_scale, kv_len, gqa::kKvHeads, k_scale_stride, true,
-                                  one_sequence(), static_cast<cudaStream_t>(stream)) == cudaSuccess
+                                  one_sequence(), di->num_sms,
+                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? GQA_OK
              : GQA_ERR_CUDA;
 }
@@ -1016,8 +1022,10 @@ gqa_status gqa_quantize_k_fp8_varlen(const void* k, void* k_fp8, float* k_scale,
   if (rows == 0) return GQA_OK;
   if (!k || !k_fp8 || !k_scale) return GQA_ERR_NULL;
   if (gqa::misaligned(k) || gqa::misaligned(k_fp8) || gqa::misaligned(k_scale)) return GQA_ERR_ALIGN;
+  gqa::DeviceInfo* di = nullptr;
+  if (const gqa_status st = gqa::device_info(&di); st != GQA_OK) return st;
   return gqa::launch_quantize_fp8(k, k_fp8, k_scale, rows, gqa::kKvHeads, k_scale_stride, true, cols,
-                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+                                  di->num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? GQA_OK
              : GQA_ERR_CUDA;
 }
