@@ -85,7 +85,7 @@ enum BarId : uint32_t {
   kBarPvDone0,                  // [2] the PV that read P[b] completed (MMA commit)
   kBarPvDone1,
   kBarOFree,                    // epilogue finished reading O (128 arrivals)
-  kBarDrain,                    // MMA warp's final drain
+  kBarDrain,                    // the MMA threads' final drain (2 commits)
   kBarScFull,                   // [kScSlots] FP8 QK^T: key scales of a tile loaded (TMA tx)
   kBarScEmpty = kBarScFull + 8, // [kScSlots] this CTA's softmax done with them (all its softmax threads)
   kBarXch = kBarScEmpty + 8,    // [4] FP8: the two softmax threads of each row of a 32-row
@@ -324,12 +324,13 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
   constexpr bool kDenseBatch = kKv == 2;
   static_assert(kFp8 != 2 || kKv == 0, "quantised PV reads the dense V of one sequence");
   constexpr bool kFp8Pv = kFp8 == 2;
-  // Warp roles: softmax warps 0 .. kSmWarps-1, then the TMA warp and the MMA warp.
+  // Warp roles: softmax warps 0 .. kSmWarps-1, then the TMA warp and the two MMA warps.
   // With 8 softmax warps, warps q and q + 4 share the MMA rows (tensor-memory
   // lanes) 32q .. 32q+31 and take keys 0-63 and 64-127 of every tile.
   constexpr int kSmWarps = fwd_softmax_warps(kFp8);
   constexpr int kTmaWarp = kSmWarps;
-  constexpr int kMmaWarp = kSmWarps + 1;
+  constexpr int kMmaWarp = kSmWarps + 1;  // QK^T issuer; allocates tensor memory
+  constexpr int kPvWarp = kSmWarps + 2;   // PV issuer
   constexpr int kHalves = kSmWarps / 4;  // softmax threads per MMA row
   constexpr int kCols = 128 / kHalves;   // scores of a tile per softmax thread
   static_assert(kHalves == 1 || kFp8 == 2, "the split softmax uses the exchange slots of the FP8 layout");
@@ -366,6 +367,16 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
   constexpr int kQChunks = kFp8 ? 2 : 4;
   constexpr int kChunkElems = kFp8 ? 128 : 64;
   constexpr int kKStagesPerTile = (kFp8 || kPair) ? 1 : 2;
+  constexpr int kVStagesPerTile = (kPair || kFp8Pv) ? 1 : 2;
+  // The 5 stages form two rings, each filled in order by the producer and read in
+  // order by one MMA thread: K stages 0 .. kStagesK-1 (QK^T thread), V stages
+  // kStagesK .. 4 (PV thread). (With one ring read by both threads, a thread could
+  // wait on a stage whose previous fill, for the other thread, was still in
+  // flight, and take that stage's older phase for the one it waits for.)
+  constexpr uint32_t kStagesK = kKStagesPerTile == 2 ? 3 : 2;  // 1.5 or 2 K tiles
+  constexpr uint32_t kStagesV = kStages - kStagesK;
+  static_assert(kStagesK >= kKStagesPerTile + 1 && kStagesV >= kVStagesPerTile,
+                "each ring holds more than one tile's K, and at least one tile's V");
   constexpr uint32_t kNchK = kFp8 ? 2 : (kPair ? 4 : 2);  // chunks per K stage
   constexpr uint32_t kNchV = kPair ? 2 : 4;               // chunks per V stage
   constexpr uint32_t kRowsK = kPair ? 64 : 128;  // keys per K stage
@@ -398,7 +409,7 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
     ptx::mbar_init(bar(kBarPvDone0), 1);
     ptx::mbar_init(bar(kBarPvDone1), 1);
     ptx::mbar_init(bar(kBarOFree), kConsumers);
-    ptx::mbar_init(bar(kBarDrain), 1);
+    ptx::mbar_init(bar(kBarDrain), 2);  // both MMA threads commit
     if constexpr (kFp8) {
       for (int i = 0; i < kScSlots; ++i) {
         ptx::mbar_init(bar(kBarScFull + i), 1);
@@ -461,7 +472,7 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
       // calls no other item does, and they go first.
       const uint64_t pol_kv = p.kv_read_once ? ptx::policy_evict_first() : ptx::policy_evict_last();
       const uint64_t pol_q = ptx::policy_evict_first();
-      uint32_t st = 0, phase = 0;
+      uint32_t kst = 0, kph = 0, vst = kStagesK, vph = 0;  // next stage and phase of each ring
       uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load issued / its phase
       uint32_t sc_count = 0, sc_issued_mask = 0, sc_issued_parity = 0;  // FP8 key-scale ring
       bool q_issued = false;
@@ -496,8 +507,10 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
         const bool v_fix = (kPaged || kDenseBatch) && !is_k && n == v_fix_tile(sq);
         const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
         const CUtensorMap* sub_map = is_k ? &p.tmap_k_sub : (v_fix ? &p.tmap_v16 : &p.tmap_v_sub);
-        const int halves = is_k ? kKStagesPerTile : ((kPair || kFp8Pv) ? 1 : 2);
+        const int halves = is_k ? kKStagesPerTile : kVStagesPerTile;
         for (int half = 0; half < halves; ++half) {
+          uint32_t& st = is_k ? kst : vst;
+          uint32_t& phase = is_k ? kph : vph;
           if (!wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
           const uint32_t dst = stage_smem + st * kStageBytes;
           const uint32_t bytes = is_k ? kKStageBytes : (kFp8Pv ? kVStageBytesPv : kStageBytes);
@@ -548,7 +561,8 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
             load_box(dst, full, kBarFull + st, row, g, chunk0);
           issued_mask |= 1u << st;
           issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
-          if (++st == kStages) { st = 0; phase ^= 1u; }
+          if (is_k) { if (++st == kStagesK) { st = 0; phase ^= 1u; } }
+          else if (++st == kStages) { st = kStagesK; phase ^= 1u; }
         }
         if constexpr (kFp8) {
           if (is_k) {
@@ -618,23 +632,34 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer (the pair's leader) ====================
-    // Issue order per unit: QK_0, then for each tile j: QK_{j+1}, PV_j. QK_{j+1}
-    // runs on the tensor pipe while the softmax of tile j is in flight.
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ======================= MMA issuers (the pair's leader) ===================
+    // Two threads issue the MMAs: lane 0 of warp kMmaWarp the QK^T groups (QK_j
+    // once the softmax holds S_{j-1}), lane 0 of warp kPvWarp the PV groups (PV_j
+    // once P_j is written). A thread's first shared-memory access after a run of
+    // tcgen05.mma (its next barrier wait) stalls for ~250 cycles while the tensor
+    // pipe holds only a couple of its MMAs; with one issuing thread every such
+    // wait between two groups left the pipe idle (per-tile traces: ~2 x 230
+    // cycles of a 2,580-cycle BF16 tile). With two, one thread's MMAs keep the
+    // pipe fed while the other waits. Each thread reads its own ring of K or V
+    // stages in order; a commit tracks the MMAs of the committing thread only.
     if (lane == 0 && leader) {
+      const bool is_qk = warp == kMmaWarp;
       const uint64_t q_desc0 = ptx::smem_desc(q_smem, 16, 1024, ptx::kSwizzle128B);
       const uint64_t k_desc0 = ptx::smem_desc(stage_smem, 16, kSboK, ptx::kSwizzle128B);
       const uint64_t v_desc0 = ptx::smem_desc(stage_smem, kLboV, kSboV, ptx::kSwizzle128B);
-      uint32_t st = 0, phase = 0;
+      // This thread's ring: stage st (absolute index), phase.
+      const uint32_t ring0 = is_qk ? 0u : kStagesK, ring_end = is_qk ? kStagesK : kStages;
+      uint32_t st = ring0, phase = 0;
+      auto next_stage = [&] {
+        if (++st == ring_end) { st = ring0; phase ^= 1u; }
+      };
       uint32_t tile = 0;  // KV tiles this CTA has processed (global tile index T)
       bool ok = true;
       int k = 0;
       Piece w;
       while (ok && pieces.next(w)) {
         const int nt = w.n1 - w.n0;
-        if (!(ok = wait_bar(bar(kBarQFull), k & 1, p))) break;
-        ptx::tc_fence_after();
         // S = Q K_j^T over d = 256 in k-steps of 16. Descriptors are built once;
         // an offset below 256 KB only touches the 14-bit start-address field, so
         // stepping through a tile is one add.
@@ -672,21 +697,19 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
               }
             }
             commit(kBarEmpty + st);
-            if (++st == kStages) { st = 0; phase ^= 1u; }
+            next_stage();
           }
           commit(kBarSFull);
           if (j == nt - 1) commit(kBarQEmpty);
           return true;
         };
-        ok = issue_qk(0);
-        for (int j = 0; j < nt && ok; ++j) {
-          if (j + 1 < nt && !(ok = issue_qk(j + 1))) break;
+        auto issue_pv = [&](int j) -> bool {
           const uint32_t T = tile + j;
           const uint32_t b = T & 1u;
           // The (first) V stage before P, for the same reason as K before s_free.
-          if (!(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
-          if (!(ok = wait_bar(bar(b ? kBarPFull1 : kBarPFull0), (T >> 1) & 1u, p))) break;
-          if (j == 0 && k > 0 && !(ok = wait_bar(bar(kBarOFree), (k - 1) & 1, p))) break;
+          if (!wait_bar(bar(kBarFull + st), phase, p)) return false;
+          if (!wait_bar(bar(b ? kBarPFull1 : kBarPFull0), (T >> 1) & 1u, p)) return false;
+          if (j == 0 && k > 0 && !wait_bar(bar(kBarOFree), (k - 1) & 1, p)) return false;
           ptx::tc_fence_after();
           // O += P_j V_j in k-steps of 16 keys, N = 256. V stages are MN-major:
           // LBO = next 64-wide d chunk (kLboV), SBO = next group of 8 keys (kSboV).
@@ -709,7 +732,7 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
                                (j | kk) != 0);
             }
             commit(kBarEmpty + st);
-            if (++st == kStages) { st = 0; phase ^= 1u; }
+            next_stage();
           } else if constexpr (kPair) {
             // One stage: 128 keys x this CTA's 2 chunks of 64 columns (waited for above).
             ptx::tc_fence_after();
@@ -727,11 +750,11 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
                                (j | kk) != 0);
             }
             commit(kBarEmpty + st);
-            if (++st == kStages) { st = 0; phase ^= 1u; }
+            next_stage();
           } else {
             // Two stages (key halves), each 64 keys x 4 chunks of 64 d.
-            for (int half = 0; half < 2 && ok; ++half) {
-              if (half > 0 && !(ok = wait_bar(bar(kBarFull + st), phase, p))) break;
+            for (int half = 0; half < 2; ++half) {
+              if (half > 0 && !wait_bar(bar(kBarFull + st), phase, p)) return false;
               ptx::tc_fence_after();
               if (v_fix) {
                 zero_v_tail(stage_smem + st * kStageBytes, kNchV, kSboV, kLboV, kRowsV * half, kRowsV,
@@ -746,16 +769,24 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
                 ptx::mma_ts(tmem + kTmemO, a_tmem, bd, kIdescPV, (j | half | kk) != 0);
               }
               commit(kBarEmpty + st);
-              if (++st == kStages) { st = 0; phase ^= 1u; }
+              next_stage();
             }
           }
-          if (!ok) break;
           commit(b ? kBarPvDone1 : kBarPvDone0);
+          return true;
+        };
+        if (is_qk) {
+          if (!(ok = wait_bar(bar(kBarQFull), k & 1, p))) break;
+          ptx::tc_fence_after();
+          for (int j = 0; j < nt && ok; ++j) ok = issue_qk(j);
+        } else {
+          for (int j = 0; j < nt && ok; ++j) ok = issue_pv(j);
         }
         tile += nt;
         ++k;
       }
-      // Drain: every MMA issued above has completed once this barrier fires.
+      // Drain: every MMA issued above (both threads commit) has completed once
+      // this barrier fires.
       commit(kBarDrain);
       wait_bar(bar(kBarDrain), 0, p);
     }

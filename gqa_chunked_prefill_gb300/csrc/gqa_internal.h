@@ -23,9 +23,10 @@ constexpr int kBlockN = 128;  // keys per KV tile
 
 // Softmax warps of the attention kernel (fp8: 0 BF16, 1 FP8 QK^T, 2 FP8 QK^T and
 // PV): 4, one thread per MMA row; with quantised PV 8, two threads per row on 64
-// of a tile's 128 scores each. Then one TMA warp and one MMA warp.
+// of a tile's 128 scores each. Then one TMA warp and two MMA-issuing warps (QK^T,
+// PV).
 constexpr int fwd_softmax_warps(int fp8) { return fp8 == 2 ? 8 : 4; }
-constexpr int fwd_threads(int fp8) { return (fwd_softmax_warps(fp8) + 2) * 32; }
+constexpr int fwd_threads(int fp8) { return (fwd_softmax_warps(fp8) + 3) * 32; }
 
 struct FwdParams {
   CUtensorMap tmap_q;  // Q [q_len][24][256], box (64 d, 6 heads, 21 tokens), 128B swizzle
