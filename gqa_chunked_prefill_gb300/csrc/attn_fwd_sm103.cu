@@ -12,8 +12,9 @@
 //    single 3-D TMA box per 64-wide d chunk; rows 126/127 are idle (zeroed,
 //    never stored). Every K/V tile is fetched once per 126 query rows.
 //  * The report's two-stage KV software pipeline with a delayed V load (§3)
-//    becomes a 5-deep ring of 32 KB shared-memory stages fed by TMA and
-//    tracked by mbarriers; K of tile j+2 streams while V of tile j is used.
+//    becomes five 32 KB shared-memory stages fed by TMA and tracked by
+//    mbarriers, split into a K ring and a V ring (one reader each); K of tile
+//    j+2 streams while V of tile j is used.
 //  * S = Q K^T and O += P V are tcgen05 MMAs (kind::f16, BF16 in, FP32 out).
 //    Tensor memory (512 columns) holds O (128 x 256 FP32), one S tile
 //    (128 x 128 FP32) and two BF16 P tiles (64 columns each) that feed the PV
@@ -23,13 +24,14 @@
 //    the PV that read it has completed (pv_done[b]). tcgen05 only orders
 //    consecutive MMAs that share accumulator and shape, so these two barriers
 //    are what makes the S -> QK^T and P -> PV reuse safe.
-//  * Warp specialisation: one warp issues TMA, one issues MMAs (one thread), and
-//    the softmax warps take the MMA rows (tensor-memory lanes). BF16 QK^T: warps
-//    0-3, one thread per row, so row max and row sum need no cross-thread
-//    reduction. Quantised PV, where the softmax (not the tensor core) sets the
-//    pace: warps 0-7, two threads per row on 64 keys of each tile each, which
-//    trade the row's tile maximum through shared memory; two warps per
-//    scheduler hide each other's latencies.
+//  * Warp specialisation: one warp issues TMA, two issue MMAs (one thread each:
+//    QK^T and PV, so that one keeps the tensor pipe fed while the other waits
+//    on a barrier), and the softmax warps take the MMA rows (tensor-memory
+//    lanes). BF16 and FP8 QK^T: warps 0-3, one thread per row, so row max and
+//    row sum need no cross-thread reduction. Quantised PV, where the softmax
+//    (not the tensor core) sets the pace: warps 0-7, two threads per row on 64
+//    keys of each tile each, which trade the row's tile maximum through shared
+//    memory; two warps per scheduler hide each other's latencies.
 //  * Online softmax in base 2 with the scale folded into one FMA. O is only
 //    rescaled when a row's running max grows by more than 2^8; otherwise the
 //    stale max is kept, which is exact after the final division by the row sum.
