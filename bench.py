@@ -57,8 +57,8 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # source it was measured on; reported as null once the source no longer matches.
 KNOWN_TRAFFIC: dict = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (1 pass) on the full launch:
-    # 793.67 MB read + 52.23 MB written.
-    "q4096_kv32768": {"bytes": 845_899_008, "kernel_sha256": "ece52f2e92ee434a399e8d81ed8868564305009aaff5102ab1359d445524a78d"},
+    # 843.03 MB read + 53.50 MB written.
+    "q4096_kv32768": {"bytes": 896_535_296, "kernel_sha256": "aa81062ab0b3555249df096bb1b4037983607d3ca489b64487ae613755781071"},
 }
 
 
@@ -83,6 +83,32 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def bf16_peak(peaks: dict, peak_kind: str, clocks):
+    """BF16 tensor peak for a timed region: the sustained cuBLAS figure when the region ran
+    at the power cap (its clock record shows sw_power_cap, as a seconds-long cuBLAS loop
+    does), else the burst figure. Returns (peak, burst peak, source text)."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = peaks.get("bf16_tflops_sustained")
+    if clocks and "sw_power_cap" in (clocks.get("reasons") or []) and sustained:
+        mhz = clocks.get("sm_mhz")
+        return (float(sustained), burst,
+                f"{peak_kind} bf16_tflops_sustained (the timed region ran at the power cap: "
+                f"sw_power_cap, SM clock median {mhz} MHz)")
+    return burst, burst, f"{peak_kind} bf16_tflops (burst; kernel timed alone at full clock)"
+
+
+def sampled(fn, device_index: int):
+    """Run fn() with the clock sampler around it; returns (fn's result, clock record)."""
+    smp = clock_sampler(device_index)
+    smp.start()
+    smp.mark(True)
+    try:
+        out = fn()
+    finally:
+        smp.mark(False)
+    return out, smp.stop()
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -388,8 +414,7 @@ def main():
     clocks = sampler.stop() if sampler else None
 
     # ---- every workload shape, timed like the headline (same steps, flush, events) ----
-    peaks_, _ = load_peaks()
-    peak_bf16 = float(peaks_.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peaks_, peak_kind_ = load_peaks()
 
     def time_workload(wl):
         wq, wk, wv = (t.to(dev) for t in make_workload(wl))
@@ -410,27 +435,35 @@ def main():
             for x in e:
                 x.record(stream)
         torch.cuda.synchronize(dev)
-        for i in range(args.steps):
-            flush.zero_()
-            a, b, f0, f1 = wev[i]
-            a.record(stream)
-            wcall((f0, f1))
-            b.record(stream)
-        torch.cuda.synchronize(dev)
+
+        def steps():
+            for i in range(args.steps):
+                flush.zero_()
+                a, b, f0, f1 = wev[i]
+                a.record(stream)
+                wcall((f0, f1))
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+
+        _, wclocks = sampled(steps, local_rank)
         if gqa.gqa_prefill_poll(stream) != 0:
             raise RuntimeError(f"device-side error during {wl.name}")
         return ([a.elapsed_time(b) for a, b, _, _ in wev],
-                [a.elapsed_time(b) for _, _, a, b in wev], wplan)
+                [a.elapsed_time(b) for _, _, a, b in wev], wplan, wclocks)
 
-    def workload_entry(wl, s_ms, f_ms, wplan):
+    def workload_entry(wl, s_ms, f_ms, wplan, wclocks):
         wflops = effective_flops(wl)
         ms = max_over_ranks(sum(s_ms) / len(s_ms), pg, dev)
         kms = sum(f_ms) / len(f_ms)
+        wpeak, wburst, _ = bf16_peak(peaks_, peak_kind_, wclocks)
         return {"value": round(job_throughput(world, wflops, ms), 2), "unit": UNIT,
                 "ms_per_step": round(ms, 4), "ms_median": round(statistics.median(s_ms), 4),
                 "kernel_ms": round(kms, 4),
-                "pct_of_peak": round(100.0 * wflops / (ms * 1e-3) / 1e12 / peak_bf16, 2),
-                "roofline_frac": round(wflops / (kms * 1e-3) / 1e12 / peak_bf16, 4),
+                "pct_of_peak": round(100.0 * wflops / (ms * 1e-3) / 1e12 / wpeak, 2),
+                "roofline_frac": round(wflops / (kms * 1e-3) / 1e12 / wpeak, 4),
+                "roofline_frac_vs_burst": round(wflops / (kms * 1e-3) / 1e12 / wburst, 4),
+                "peak": wpeak,
+                "clocks": {k_: wclocks.get(k_) for k_ in ("sm_mhz", "reasons")} if wclocks else None,
                 "effective_gflop_per_step": round(wflops / 1e9, 2),
                 "plan": {k_: wplan[k_] for k_ in ("variant", "head_rounds", "tail_items",
                                                   "tail_splits", "grid", "kernels_per_call")}}
@@ -438,7 +471,7 @@ def main():
     workloads = {}
     for name_, wl in WORKLOADS.items():
         if name_ == w.name:
-            workloads[name_] = workload_entry(w, step_ms, fwd_ms, plan)
+            workloads[name_] = workload_entry(w, step_ms, fwd_ms, plan, clocks)
         else:
             workloads[name_] = workload_entry(wl, *time_workload(wl))
     torch.cuda.empty_cache()
@@ -595,7 +628,7 @@ def main():
             flush.zero_()
             fplan = fcall()
         f_steps = min(args.steps, 100)
-        f_ms, f_fwd = timed(fcall, f_steps, with_fwd=True)
+        (f_ms, f_fwd), f_clocks = sampled(lambda: timed(fcall, f_steps, with_fwd=True), local_rank)
         if gqa.gqa_prefill_poll(stream) != 0:
             raise RuntimeError("device-side error during the FP8 steps")
         f_ms = max_over_ranks(f_ms, pg, dev)
@@ -651,7 +684,8 @@ def main():
         for _ in range(3):
             flush.zero_()
             pvplan = pvcall()
-        pv_ms, pv_fwd = timed(pvcall, f_steps, with_fwd=True)
+        (pv_ms, pv_fwd), pv_clocks = sampled(lambda: timed(pvcall, f_steps, with_fwd=True),
+                                             local_rank)
         if gqa.gqa_prefill_poll(stream) != 0:
             raise RuntimeError("device-side error during the FP8 PV steps")
         pv_ms = max_over_ranks(pv_ms, pg, dev)
@@ -660,6 +694,7 @@ def main():
                 src, v8, vs8, w.kv_len, w.n_kv_heads, w.head_dim, vstride, stream=stream)),
             v.numel() * 2)
         fp8pv = {"steps": f_steps, "value": round(job_throughput(world, flops, pv_ms), 2),
+                 "clocks": pv_clocks,
                  "unit": UNIT, "ms_per_step": round(pv_ms, 4), "kernel_ms": round(pv_fwd, 4),
                  "kernels_per_call": pvplan["kernels_per_call"],
                  "quantize_v_us": round(qv_ms * 1e3, 1),
@@ -668,6 +703,7 @@ def main():
                          f"timed apart on {v_rot} rotating copies"}
         del v8
         fp8 = {"steps": f_steps, "value": round(job_throughput(world, flops, f_ms), 2),
+               "clocks": f_clocks,
                "unit": UNIT, "ms_per_step": round(f_ms, 4), "kernel_ms": round(f_fwd, 4),
                "kernels_per_call": fplan["kernels_per_call"],
                "quantize_q_us": round(qq_ms * 1e3, 1), "quantize_k_us": round(qk_ms * 1e3, 1),
@@ -813,22 +849,27 @@ def main():
     value = job_throughput(world, flops, ms_per_step)
     fwd_avg_ms = sum(fwd_ms) / len(fwd_ms)
     achieved = flops / (fwd_avg_ms * 1e-3) / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak, peak_burst, peak_src = bf16_peak(peaks, peak_kind, clocks)
     if fp8:
         # QK^T (half the FLOPs) at the FP8 rate = measured BF16 x 2 (the nominal FP8:BF16
         # ratio), PV at the measured BF16 rate.
-        mixed = 1.0 / (0.5 / (2.0 * peak) + 0.5 / peak)
+        fpk, fburst, fsrc = bf16_peak(peaks, peak_kind, fp8.get("clocks"))
+        mixed = 1.0 / (0.5 / (2.0 * fpk) + 0.5 / fpk)
+        mixed_burst = 1.0 / (0.5 / (2.0 * fburst) + 0.5 / fburst)
         f_ach = flops / (fp8["kernel_ms"] * 1e-3) / 1e12
         fp8["roofline"] = {"bound": "tensor", "achieved": round(f_ach, 2), "peak": round(mixed, 1),
                            "unit": "TFLOP/s", "frac": round(f_ach / mixed, 4),
-                           "peak_source": f"{peak_kind} bf16_tflops: QK^T at 2x, PV at 1x"}
+                           "frac_vs_burst": round(f_ach / mixed_burst, 4),
+                           "peak_source": f"{fsrc}: QK^T at 2x, PV at 1x"}
     if fp8pv:
         # both halves at the FP8 rate: measured BF16 x 2 (the nominal FP8:BF16 ratio)
+        ppk, pburst, psrc = bf16_peak(peaks, peak_kind, fp8pv.get("clocks"))
         pv_ach = flops / (fp8pv["kernel_ms"] * 1e-3) / 1e12
         fp8pv["roofline"] = {"bound": "tensor", "achieved": round(pv_ach, 2),
-                             "peak": round(2.0 * peak, 1), "unit": "TFLOP/s",
-                             "frac": round(pv_ach / (2.0 * peak), 4),
-                             "peak_source": f"{peak_kind} bf16_tflops x 2 (QK^T and PV in E4M3)"}
+                             "peak": round(2.0 * ppk, 1), "unit": "TFLOP/s",
+                             "frac": round(pv_ach / (2.0 * ppk), 4),
+                             "frac_vs_burst": round(pv_ach / (2.0 * pburst), 4),
+                             "peak_source": f"{psrc} x 2 (QK^T and PV in E4M3)"}
     known = KNOWN_TRAFFIC.get(w.name)
     traffic = known["bytes"] if known and known["kernel_sha256"] == kernel_source_sha() else None
 
@@ -861,9 +902,10 @@ def main():
             "bound": "tensor",
             "achieved": round(achieved, 2),
             "peak": peak,
-            "peak_source": f"{peak_kind} bf16_tflops (burst; kernel timed alone)",
+            "peak_source": peak_src,
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
+            "frac_vs_burst": round(achieved / peak_burst, 4),
             "traffic": traffic,
             "kernel": "gqa_attn_fwd_sm103_kernel",
             "kernel_ms": round(fwd_avg_ms, 4),
