@@ -907,26 +907,18 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
         }
         const float m_new = fmaxf(m_ref, m_tile);
         const bool need = m_new > m_ref + (kFp8Pv ? kRescaleThresholdPv : kRescaleThreshold);
+        // O correction: P_j is computed against the new reference at once; O (which
+        // must first hold PV_{j-1}) is rescaled after P_j is stored, just before
+        // p_full, by which time PV_{j-1} has normally completed.
+        bool rescale = false;
+        float alpha = 1.0f;
         if (j == 0) {
           if (need) m_ref = m_new;  // O is overwritten by this unit's first PV
         } else if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ptx::ex2_approx(m_ref - m_new) : 1.0f;
+          alpha = need ? ptx::ex2_approx(m_ref - m_new) : 1.0f;
           if (need) m_ref = m_new;
           l *= alpha;
-          // O must hold PV_{j-1} (which read P[(T-1)&1], use (T-1)>>1) before it is rescaled.
-          ok = __all_sync(0xffffffffu, wait_bar(bar((T - 1) & 1u ? kBarPvDone1 : kBarPvDone0),
-                                                ((T - 1) >> 1) & 1u, p));
-          if (!ok) break;
-          ptx::tc_fence_after();
-#pragma unroll 1
-          for (int c = oc0; c < oc0 + kHeadDim / kHalves; c += 32) {
-            uint32_t o[32];
-            ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            ptx::tmem_st_x32(lane_addr + kTmemO + c, o);
-          }
-          ptx::tmem_st_wait();
+          rescale = true;
         }
         const float m_use = (m_ref == kNegInf) ? 0.0f : m_ref;
         // BF16 P: two values per tensor-memory column; E4M3 P (quantised PV): four.
@@ -963,6 +955,22 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
         // Key k of the tile sits in P column k / 2 (BF16) or k / 4 (E4M3).
         tmem_st_n(lane_addr + kTmemP + 64u * b + (kFp8Pv ? kc0 / 4 : kc0 / 2), pk);
         ptx::tmem_st_wait();
+        if (rescale) {  // warp-uniform
+          // O must hold PV_{j-1} (which read P[(T-1)&1], use (T-1)>>1) before it is rescaled.
+          ok = __all_sync(0xffffffffu, wait_bar(bar((T - 1) & 1u ? kBarPvDone1 : kBarPvDone0),
+                                                ((T - 1) >> 1) & 1u, p));
+          if (!ok) break;
+          ptx::tc_fence_after();
+#pragma unroll 1
+          for (int c = oc0; c < oc0 + kHeadDim / kHalves; c += 32) {
+            uint32_t o[32];
+            ptx::tmem_ld_x32(lane_addr + kTmemO + c, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st_x32(lane_addr + kTmemO + c, o);
+          }
+          ptx::tmem_st_wait();
+        }
         ptx::tc_fence_before();
         arrive_leader(b ? kBarPFull1 : kBarPFull0);
       }
