@@ -167,7 +167,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Fw
 // holding keys key0 .. key0+rows-1 of the tile (kr: its first key past kv_len);
 // key r, chunk c at (r / 8) * sbo + c * lbo + (r % 8) * 128 (the stage layout's
 // strides; a 128-byte row stays in place under the 128-byte swizzle). Out of
-// line (rare: once per item that reaches the last KV tile) so the MMA thread's
+// line (rare: once per item that reaches the last KV tile) so the PV thread's
 // loop stays small.
 __device__ __noinline__ void zero_v_tail(uint32_t base, int nch, uint32_t sbo, uint32_t lbo,
                                          int key0, int rows, int kr, bool remote) {
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;  // position in the pair
   const bool leader = rank == 0;
-  // Barriers the leader's MMA thread waits on, as seen from this CTA.
+  // Barriers the leader's MMA threads wait on, as seen from this CTA.
   auto lbar = [&](uint32_t id) { return kPair ? ptx::map_to_cta(bar(id), 0) : bar(id); };
   auto arrive_leader = [&](uint32_t id) {
     if constexpr (kPair) ptx::mbar_arrive_cluster(lbar(id)); else ptx::mbar_arrive(bar(id));
@@ -609,7 +609,7 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
           q_issued = true;
           q_parity = k & 1;
         }
-        // Consumption order of the MMA warp: K0, K1, V0, K2, V1, ..., V(nt-1).
+        // Load order: K0, K1, V0, K2, V1, ..., V(nt-1) (K into the K ring, V into the V ring).
         const int nt = w.n1 - w.n0;
         for (int j = 0; j < nt && ok; ++j) {
           ok = next_tile(sq, w.n0 + j, true, w.g);
@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
         ++k;
       }
       // Every copy issued must have landed before the CTA exits. On the normal
-      // path the MMA thread already waited for all of them (these return at
+      // path the MMA threads already waited for all of them (these return at
       // once); after a time-out they may still be in flight. In a pair all
       // copies complete on the leader's barriers, so the leader drains for both.
       if (leader) {
