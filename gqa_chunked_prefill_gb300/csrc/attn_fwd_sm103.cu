@@ -24,10 +24,10 @@
 //    the PV that read it has completed (pv_done[b]). tcgen05 only orders
 //    consecutive MMAs that share accumulator and shape, so these two barriers
 //    are what makes the S -> QK^T and P -> PV reuse safe.
-//  * Warp specialisation: one warp issues TMA, two issue MMAs (one thread each:
-//    QK^T and PV, so that one keeps the tensor pipe fed while the other waits
-//    on a barrier), and the softmax warps take the MMA rows (tensor-memory
-//    lanes). BF16 and FP8 QK^T: warps 0-3, one thread per row, so row max and
+//  * Warp specialisation: one warp issues TMA (two, one per ring, on paged
+//    K/V), two issue MMAs (one thread each: QK^T and PV,
+//    so that one keeps the tensor pipe fed while the other waits on a
+//    barrier), and the softmax warps take the MMA rows (tensor-memory lanes). BF16 and FP8 QK^T: warps 0-3, one thread per row, so row max and
 //    row sum need no cross-thread reduction. Quantised PV, where the softmax
 //    (not the tensor core) sets the pace: warps 0-7, two threads per row on 64
 //    keys of each tile each, which trade the row's tile maximum through shared
@@ -61,6 +61,11 @@ namespace gqa {
 namespace {
 
 constexpr int kStages = 5;
+// A compile-time flag as a value (selects a generic lambda's instantiation).
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
 constexpr uint32_t kQChunkBytes = 128 * 128;   // 128 rows x 64 bf16 (one 128B-swizzle column)
 constexpr uint32_t kQBoxBytes = 126 * 128;     // the 21x6 rows one TMA box writes
 constexpr uint32_t kQBytes = 4 * kQChunkBytes;  // d = 256 -> 4 chunks
@@ -157,6 +162,23 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Fw
   }
 }
 
+// wait_bar for a thread off the critical path (the paged kernel's two TMA
+// producers): it sleeps in the barrier until the phase completes (or 20 us
+// pass, then checks the time-out) instead of polling, leaving the issue slots
+// of its scheduler to the softmax warp that shares it (polling cost the pair
+// kernel ~3 % with two producer warps).
+__device__ __forceinline__ bool wait_bar_idle(uint32_t bar, uint32_t parity, const FwdParams& p) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (;;) {
+    if (ptx::mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+      atomicExch(p.status, static_cast<int>(GQA_ERR_DEVICE_TIMEOUT));
+      return false;
+    }
+  }
+}
+
 // The V rows of the tile holding key kv_len-1 that lie past kv_len may hold
 // anything: in a paged cache, the last page's unused slots; in a dense batch, the
 // next sequence's values. Their P is exactly 0, but 0 * NaN is not, so they are
@@ -203,22 +225,19 @@ __device__ __noinline__ void issue_dense_v_pieces(const CUtensorMap* map16, uint
     }
 }
 
-// Paged K/V, the rare case: a box that crosses pages (or the V box of the tile
-// holding key kv_len-1) goes as pieces (gqa_paged.h), one 5-D copy per piece
-// covering all `nch` chunks (paged stage layout, see the kernel). `table`: the
-// sequence's block-table row; `bar`: the barrier the copies complete on (the
-// pair leader's, mapped, for pairs). Out of line so the producer's common loop
-// stays small.
+// Paged K/V: a box that crosses pages (or the V box of the tile holding key
+// kv_len-1) goes as pieces (gqa_paged.h's map_paged_run), one 5-D copy per
+// piece covering all `nch` chunks (paged stage layout, see the kernel). `bar`:
+// the barrier the copies complete on (the pair leader's, mapped, for pairs).
+// Inlined: as a call it cost the producer ~1,500 more cycles per box (per-tile
+// clock traces, page 64).
 template <bool kPair>
-__device__ __noinline__ void issue_paged_pieces(const PagedGeom& pgeo, const int* table,
-                                                int* status, const CUtensorMap* sub_map,
-                                                uint32_t dst, uint32_t bar, int r0, int rows,
-                                                int nch, int chunk0, int g, bool v_fix,
-                                                uint64_t pol) {
-  PagedRun run;
-  map_paged_run(pgeo, r0, rows, v_fix, [&](int pg) { return __ldg(table + pg); }, run);
-  if (run.bad) atomicExch(status, static_cast<int>(GQA_ERR_PAGE_TABLE));
-  for (int i = 0; i < run.n; ++i) {
+__device__ __forceinline__ void issue_paged_pieces(const PagedRun& run, const CUtensorMap* sub_map,
+                                                   uint32_t dst, uint32_t bar, int nch, int chunk0,
+                                                   int g, uint64_t pol) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {  // unrolled: run.row stays in registers
+    if (i >= run.n) break;
     // Piece i is 8-key groups [i*sub/8, (i+1)*sub/8) of the stage: contiguous.
     const uint32_t d = dst + i * run.sub * nch * 128;
     if constexpr (kPair) ptx::tma_load_5d_pair(d, sub_map, bar, 0, 0, chunk0, run.row[i] / 8, g, pol);
@@ -233,18 +252,20 @@ __device__ __noinline__ void issue_paged_pieces(const PagedGeom& pgeo, const int
 // destination on 128 bytes, which 16-key pieces are not). Pieces past the
 // cache or on a bad table entry are not copied but zeroed, and only the bytes
 // actually copied are expected on `bar`; this thread's arrive (after the
-// zeroing) is the slot's one arrival. Out of line, like issue_paged_pieces.
-__device__ __noinline__ void issue_paged_scales(const PagedGeom& pgeo, const int* table,
-                                                int* status, const float* scale_row,
-                                                uint32_t dst, uint32_t bar, int r0,
-                                                uint64_t pol) {
+// zeroing) is the slot's one arrival. Inlined, like issue_paged_pieces.
+__device__ __forceinline__ void issue_paged_scales(const PagedGeom pgeo, const int* table,
+                                                   int* status, const float* scale_row,
+                                                   uint32_t dst, uint32_t bar, int r0,
+                                                   uint64_t pol) {
   PagedRun run;
   map_paged_run(pgeo, r0, kBlockN, false, [&](int pg) { return __ldg(table + pg); }, run);
   if (run.bad) atomicExch(status, static_cast<int>(GQA_ERR_PAGE_TABLE));
   const int n = run.n == 0 ? 1 : run.n;
   const int keys = run.n == 0 ? kBlockN : run.sub;
   uint32_t bytes = 0;
-  for (int i = 0; i < n; ++i) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {  // unrolled: run.row stays in registers
+    if (i >= n) break;
     if (run.row[i] < pgeo.oob_row) {
       bytes += keys * 4;
     } else {
@@ -252,9 +273,12 @@ __device__ __noinline__ void issue_paged_scales(const PagedGeom& pgeo, const int
     }
   }
   ptx::mbar_arrive_expect_tx(bar, bytes);
-  for (int i = 0; i < n; ++i)
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i >= n) break;
     if (run.row[i] < pgeo.oob_row)
       ptx::bulk_load(dst + i * keys * 4, scale_row + run.row[i], keys * 4, bar, pol);
+  }
 }
 
 // kPair = false: one CTA per work item (21 tokens x 6 heads = 126 MMA rows).
@@ -320,19 +344,22 @@ __device__ __forceinline__ void transpose8_quads(uint4 (&e)[8], int j) {
 // sequences packed end to end (the V box of a sequence's last tile goes in 16-key
 // pieces so that the next sequence's values never reach it).
 template <bool kPair, int kKv, int kFp8>
-__global__ void __launch_bounds__(fwd_threads(kFp8), 1)
+__global__ void __launch_bounds__(fwd_threads(kFp8, kKv), 1)
     gqa_attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
   constexpr bool kPaged = kKv == 1;
   constexpr bool kDenseBatch = kKv == 2;
   static_assert(kFp8 != 2 || kKv == 0, "quantised PV reads the dense V of one sequence");
   constexpr bool kFp8Pv = kFp8 == 2;
-  // Warp roles: softmax warps 0 .. kSmWarps-1, then the TMA warp and the two MMA warps.
+  // Warp roles: softmax warps 0 .. kSmWarps-1, then the TMA warp, the two MMA
+  // warps and, for paged K/V, the V TMA warp.
   // With 8 softmax warps, warps q and q + 4 share the MMA rows (tensor-memory
   // lanes) 32q .. 32q+31 and take keys 0-63 and 64-127 of every tile.
   constexpr int kSmWarps = fwd_softmax_warps(kFp8);
   constexpr int kTmaWarp = kSmWarps;
   constexpr int kMmaWarp = kSmWarps + 1;  // QK^T issuer; allocates tensor memory
   constexpr int kPvWarp = kSmWarps + 2;   // PV issuer
+  constexpr bool kSplitProducer = fwd_split_producer(kKv);
+  constexpr int kTmaVWarp = kSmWarps + 3; // paged K/V: V producer (kTmaWarp: Q and K)
   constexpr int kHalves = kSmWarps / 4;  // softmax threads per MMA row
   constexpr int kCols = 128 / kHalves;   // scores of a tile per softmax thread
   static_assert(kHalves == 1 || kFp8 == 2, "the split softmax uses the exchange slots of the FP8 layout");
@@ -458,116 +485,158 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
   // KV tile holding key kv_len-1 of a sequence when it is partial (else -1).
   auto v_fix_tile = [](const SeqGeo& sq) { return sq.kv_len % kBlockN ? (sq.kv_len - 1) / kBlockN : -1; };
 
-  if (warp == kTmaWarp) {
-    // ======================= TMA producer ======================================
+  if (warp == kTmaWarp || (kSplitProducer && warp == kTmaVWarp)) {
+    // ======================= TMA producers =====================================
+    // Dense K/V: one thread, lane 0 of warp kTmaWarp, loads Q and fills both
+    // rings in the order K0, K1, V0, K2, V1, ... Paged K/V: two threads each fill
+    // one ring in tile order, lane 0 of warp kTmaWarp Q, the K ring and (FP8)
+    // the key scales, lane 0 of warp kTmaVWarp the V ring. Issuing a copy
+    // occupies the thread for a few hundred cycles, and a paged box adds its
+    // block-table reads, or, where it crosses pages, one copy per piece: one
+    // thread for both rings was the bottleneck (page 64: the pair kernel took
+    // twice as long as on dense K/V; page 784: 1.3x; the one-CTA kernel, whose V
+    // ring holds one tile, 1.17x even at page 1024). On dense K/V the second
+    // thread gains nothing and its warp cost ~2 % (it shares a scheduler with a
+    // softmax warp), so there one thread stays.
+    constexpr bool split = kSplitProducer;
     if (lane == 0) {
-      ptx::prefetch_tmap(&p.tmap_q);
-      ptx::prefetch_tmap(&p.tmap_k);
-      ptx::prefetch_tmap(&p.tmap_v);
-      if constexpr (kFp8) ptx::prefetch_tmap(&p.tmap_ks);
-      if constexpr (kPaged) {
-        ptx::prefetch_tmap(&p.tmap_k_sub);
-        ptx::prefetch_tmap(&p.tmap_v_sub);
-        ptx::prefetch_tmap(&p.tmap_v16);
-      }
-      // K/V tiles stay in L2 for the other items that read them; in decode-sized
-      // calls no other item does, and they go first.
-      const uint64_t pol_kv = p.kv_read_once ? ptx::policy_evict_first() : ptx::policy_evict_last();
-      const uint64_t pol_q = ptx::policy_evict_first();
-      uint32_t kst = 0, kph = 0, vst = kStagesK, vph = 0;  // next stage and phase of each ring
-      uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load issued / its phase
-      uint32_t sc_count = 0, sc_issued_mask = 0, sc_issued_parity = 0;  // FP8 key-scale ring
-      bool q_issued = false;
-      uint32_t q_parity = 0;
-      bool ok = true;
-      auto load = [&](uint32_t dst, const CUtensorMap* map, uint32_t id, int c0, int c1, int c2,
-                      uint64_t pol) {
-        if constexpr (kPair) ptx::tma_load_3d_pair(dst, map, lbar(id), c0, c1, c2, pol);
-        else ptx::tma_load_3d(dst, map, bar(id), c0, c1, c2, pol);
-      };
-      // A whole K/V box: 4-D (64 d, key, head, chunk) dense, 5-D (64 d, key % 8,
-      // chunk, key / 8, head) paged; both with the stage layout described above.
-      auto load_box = [&](uint32_t dst, const CUtensorMap* map, uint32_t id, int row, int g,
-                          int chunk0) {
-        if constexpr (kPaged) {
-          if constexpr (kPair) ptx::tma_load_5d_pair(dst, map, lbar(id), 0, 0, chunk0, row / 8, g, pol_kv);
-          else ptx::tma_load_5d(dst, map, bar(id), 0, 0, chunk0, row / 8, g, pol_kv);
-        } else {
-          if constexpr (kPair) ptx::tma_load_4d_pair(dst, map, lbar(id), 0, row, g, chunk0, pol_kv);
-          else ptx::tma_load_4d(dst, map, bar(id), 0, row, g, chunk0, pol_kv);
+      auto produce = [&](auto do_k_c, auto do_v_c) {
+        constexpr bool do_k = decltype(do_k_c)::value;  // Q, the K ring, key scales
+        constexpr bool do_v = decltype(do_v_c)::value;  // the V ring
+        if constexpr (do_k) {
+          ptx::prefetch_tmap(&p.tmap_q);
+          ptx::prefetch_tmap(&p.tmap_k);
+          if constexpr (kFp8) ptx::prefetch_tmap(&p.tmap_ks);
+          if constexpr (kPaged) ptx::prefetch_tmap(&p.tmap_k_sub);
         }
-      };
-      // Block-table entries (paged K/V); the K and V streams each keep their
-      // last entry in registers (they run one tile apart; both are reset when
-      // an item of another sequence starts).
-      int cached_pg[2] = {-1, -1}, cached_entry[2] = {0, 0};
-      // One K tile is two 32 KB stages (d halves) in the one-CTA kernel and one
-      // stage (this CTA's 64 keys) in a pair; likewise for V (key halves / this
-      // CTA's 128 columns). A whole box is one copy; a paged box that crosses a
-      // page is one copy per piece.
-      auto next_tile = [&](const SeqGeo& sq, int n, bool is_k, int g) -> bool {
-        const bool v_fix = (kPaged || kDenseBatch) && !is_k && n == v_fix_tile(sq);
-        const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
-        const CUtensorMap* sub_map = is_k ? &p.tmap_k_sub : (v_fix ? &p.tmap_v16 : &p.tmap_v_sub);
-        const int halves = is_k ? kKStagesPerTile : kVStagesPerTile;
-        for (int half = 0; half < halves; ++half) {
-          uint32_t& st = is_k ? kst : vst;
-          uint32_t& phase = is_k ? kph : vph;
-          if (!wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)) return false;
-          const uint32_t dst = stage_smem + st * kStageBytes;
-          const uint32_t bytes = is_k ? kKStageBytes : (kFp8Pv ? kVStageBytesPv : kStageBytes);
-          if (leader) ptx::mbar_arrive_expect_tx(bar(kBarFull + st), (kPair ? 2 : 1) * bytes);
-          // Box geometry: first key, keys per box, chunks and their stride in
-          // shared memory, first chunk.
-          int r0, rows, nb, chunk0;
-          if constexpr (kPair) {
-            r0 = n * kBlockN + (is_k ? 64 * static_cast<int>(rank) : 0);
-            rows = is_k ? 64 : 128;
-            nb = is_k ? static_cast<int>(kNchK) : 2;
-            chunk0 = is_k ? 0 : 2 * static_cast<int>(rank);
-          } else {
-            r0 = n * kBlockN + (is_k ? 0 : 64 * half);
-            rows = is_k ? 128 : 64;
-            nb = is_k ? static_cast<int>(kNchK) : 4;
-            chunk0 = is_k ? static_cast<int>(kNchK) * half : 0;
-          }
-          int row = sq.kv_start + r0;  // dense K/V: the box is the keys themselves
-          bool whole = true;
+        if constexpr (do_v) {
+          ptx::prefetch_tmap(&p.tmap_v);
           if constexpr (kPaged) {
-            const int sid = is_k ? 0 : 1;
-            const int* table = p.block_table + static_cast<size_t>(sq.src) * p.bt_stride;
-            auto read = [&](int pg) -> int {
-              if (pg != cached_pg[sid]) {
-                cached_entry[sid] = __ldg(table + pg);
-                cached_pg[sid] = pg;
-              }
-              return cached_entry[sid];
-            };
-            const PagedGeom pgeo{sq.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
-            bool bad = false;
-            whole = paged_whole_box(pgeo, r0, rows, v_fix, read, &row, &bad);
-            if (bad) atomicExch(p.status, static_cast<int>(GQA_ERR_PAGE_TABLE));
-            if (!whole)
-              issue_paged_pieces<kPair>(pgeo, table, p.status, sub_map, dst,
-                                        kPair ? lbar(kBarFull + st) : bar(kBarFull + st), r0, rows,
-                                        nb, chunk0, g, v_fix, pol_kv);
+            ptx::prefetch_tmap(&p.tmap_v_sub);
+            ptx::prefetch_tmap(&p.tmap_v16);
           }
-          if (kFp8Pv && !is_k)  // one box (128 keys, 256 or 128 channels, head g)
-            load(dst, &p.tmap_v, kBarFull + st, sq.kv_start + n * kBlockN,
-                 kPair ? 128 * static_cast<int>(rank) : 0, g, pol_kv);
-          else if (kDenseBatch && v_fix)
-            issue_dense_v_pieces<kPair>(&p.tmap_v16, dst, kPair ? lbar(kBarFull + st) : bar(kBarFull + st),
-                                        sq.kv_start, sq.kv_len, p.oob_row, r0, rows, nb, chunk0, g,
-                                        pol_kv);
-          else if (whole)
-            load_box(dst, full, kBarFull + st, row, g, chunk0);
-          issued_mask |= 1u << st;
-          issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
-          if (is_k) { if (++st == kStagesK) { st = 0; phase ^= 1u; } }
-          else if (++st == kStages) { st = kStagesK; phase ^= 1u; }
         }
-        if constexpr (kFp8) {
-          if (is_k) {
+        // K/V tiles stay in L2 for the other items that read them; in decode-sized
+        // calls no other item does, and they go first.
+        const uint64_t pol_kv = p.kv_read_once ? ptx::policy_evict_first() : ptx::policy_evict_last();
+        const uint64_t pol_q = ptx::policy_evict_first();
+        // This thread's stages: ring0 .. ring_end-1 (absolute indices).
+        constexpr uint32_t ring0 = do_k ? 0u : kStagesK;
+        constexpr uint32_t ring_end = do_v ? static_cast<uint32_t>(kStages) : kStagesK;
+        uint32_t kst = 0, kph = 0, vst = kStagesK, vph = 0;  // next stage and phase of each ring
+        uint32_t issued_mask = 0, issued_parity = 0;  // per stage: a load issued / its phase
+        uint32_t sc_count = 0, sc_issued_mask = 0, sc_issued_parity = 0;  // FP8 key-scale ring
+        bool q_issued = false;
+        uint32_t q_parity = 0;
+        bool ok = true;
+        auto load = [&](uint32_t dst, const CUtensorMap* map, uint32_t id, int c0, int c1, int c2,
+                        uint64_t pol) {
+          if constexpr (kPair) ptx::tma_load_3d_pair(dst, map, lbar(id), c0, c1, c2, pol);
+          else ptx::tma_load_3d(dst, map, bar(id), c0, c1, c2, pol);
+        };
+        // A whole K/V box: 4-D (64 d, key, head, chunk) dense, 5-D (64 d, key % 8,
+        // chunk, key / 8, head) paged; both with the stage layout described above.
+        auto load_box = [&](uint32_t dst, const CUtensorMap* map, uint32_t id, int row, int g,
+                            int chunk0) {
+          if constexpr (kPaged) {
+            if constexpr (kPair) ptx::tma_load_5d_pair(dst, map, lbar(id), 0, 0, chunk0, row / 8, g, pol_kv);
+            else ptx::tma_load_5d(dst, map, bar(id), 0, 0, chunk0, row / 8, g, pol_kv);
+          } else {
+            if constexpr (kPair) ptx::tma_load_4d_pair(dst, map, lbar(id), 0, row, g, chunk0, pol_kv);
+            else ptx::tma_load_4d(dst, map, bar(id), 0, row, g, chunk0, pol_kv);
+          }
+        };
+        // Block-table entries (paged K/V): the K and V streams each keep the last
+        // one they read, reset when an item of another sequence starts.
+        [[maybe_unused]] int cached_pg[2] = {-1, -1}, cached_entry[2] = {0, 0};
+        // One K tile is two 32 KB stages (d halves) in the one-CTA kernel and one
+        // stage (this CTA's 64 keys) in a pair; likewise for V (key halves / this
+        // CTA's 128 columns). A whole box is one copy; a paged box that crosses a
+        // page is one copy per piece.
+        auto next_tile = [&](const SeqGeo& sq, int n, auto is_k_c, int g) -> bool {
+          constexpr bool is_k = decltype(is_k_c)::value;
+          const bool v_fix = (kPaged || kDenseBatch) && !is_k && n == v_fix_tile(sq);
+          const CUtensorMap* full = is_k ? &p.tmap_k : &p.tmap_v;
+          [[maybe_unused]] const CUtensorMap* sub_map =
+              is_k ? &p.tmap_k_sub : (v_fix ? &p.tmap_v16 : &p.tmap_v_sub);
+          constexpr int halves = is_k ? kKStagesPerTile : kVStagesPerTile;
+#pragma unroll 1
+          for (int half = 0; half < halves; ++half) {
+            uint32_t& st = is_k ? kst : vst;
+            uint32_t& phase = is_k ? kph : vph;
+            // The box's geometry and its block-table entries do not depend on the
+            // stage: they are worked out (and the reads issued) before the wait for
+            // a free stage, so that once one frees only the copies are left.
+            // Box geometry: first key, keys per box, chunks and their stride in
+            // shared memory, first chunk.
+            int r0, rows, nb, chunk0;
+            if constexpr (kPair) {
+              r0 = n * kBlockN + (is_k ? 64 * static_cast<int>(rank) : 0);
+              rows = is_k ? 64 : 128;
+              nb = is_k ? static_cast<int>(kNchK) : 2;
+              chunk0 = is_k ? 0 : 2 * static_cast<int>(rank);
+            } else {
+              r0 = n * kBlockN + (is_k ? 0 : 64 * half);
+              rows = is_k ? 128 : 64;
+              nb = is_k ? static_cast<int>(kNchK) : 4;
+              chunk0 = is_k ? static_cast<int>(kNchK) * half : 0;
+            }
+            int row = sq.kv_start + r0;  // dense K/V: the box is the keys themselves
+            bool whole = true;
+            [[maybe_unused]] PagedRun run;  // the pieces of a paged box that crosses pages
+            if constexpr (kPaged) {
+              const int* table = p.block_table + static_cast<size_t>(sq.src) * p.bt_stride;
+              constexpr int sid = is_k ? 0 : 1;
+              auto read = [&](int pg) -> int {
+                if (pg != cached_pg[sid]) {
+                  cached_entry[sid] = __ldg(table + pg);
+                  cached_pg[sid] = pg;
+                }
+                return cached_entry[sid];
+              };
+              const PagedGeom pgeo{sq.kv_len, p.page_size, p.num_pages, p.sub_rows, p.oob_row};
+              bool bad = false;
+              whole = paged_whole_box(pgeo, r0, rows, v_fix, read, &row, &bad);
+              if (!whole) {
+                map_paged_run(pgeo, r0, rows, v_fix, [&](int pg) { return __ldg(table + pg); }, run);
+                bad = run.bad;
+              }
+              if (bad) atomicExch(p.status, static_cast<int>(GQA_ERR_PAGE_TABLE));
+            }
+            if (!(split ? wait_bar_idle(bar(kBarEmpty + st), phase ^ 1u, p)
+                        : wait_bar(bar(kBarEmpty + st), phase ^ 1u, p)))
+              return false;
+            const uint32_t dst = stage_smem + st * kStageBytes;
+            const uint32_t bytes = is_k ? kKStageBytes : (kFp8Pv ? kVStageBytesPv : kStageBytes);
+            if (leader) ptx::mbar_arrive_expect_tx(bar(kBarFull + st), (kPair ? 2 : 1) * bytes);
+            if constexpr (kPaged) {
+              if (!whole)
+                issue_paged_pieces<kPair>(run, sub_map, dst,
+                                          kPair ? lbar(kBarFull + st) : bar(kBarFull + st), nb,
+                                          chunk0, g, pol_kv);
+            }
+            if (kFp8Pv && !is_k)  // one box (128 keys, 256 or 128 channels, head g)
+              load(dst, &p.tmap_v, kBarFull + st, sq.kv_start + n * kBlockN,
+                   kPair ? 128 * static_cast<int>(rank) : 0, g, pol_kv);
+            else if (kDenseBatch && v_fix)
+              issue_dense_v_pieces<kPair>(&p.tmap_v16, dst, kPair ? lbar(kBarFull + st) : bar(kBarFull + st),
+                                          sq.kv_start, sq.kv_len, p.oob_row, r0, rows, nb, chunk0, g,
+                                          pol_kv);
+            else if (whole)
+              load_box(dst, full, kBarFull + st, row, g, chunk0);
+            issued_mask |= 1u << st;
+            issued_parity = (issued_parity & ~(1u << st)) | (phase << st);
+            if (is_k) {
+              if (++st == kStagesK) {
+                st = 0;
+                phase ^= 1u;
+              }
+            } else if (++st == kStages) {
+              st = kStagesK;
+              phase ^= 1u;
+            }
+          }
+          if constexpr (kFp8 && is_k) {
             // The tile's 128 key scales of group g, for this CTA's softmax warps
             // (each CTA of a pair loads its own copy on its own barrier).
             const uint32_t slot = sc_count % kScSlots, use = sc_count / kScSlots;
@@ -588,50 +657,59 @@ __global__ void __launch_bounds__(fwd_threads(kFp8), 1)
             sc_issued_parity = (sc_issued_parity & ~(1u << slot)) | ((use & 1u) << slot);
             ++sc_count;
           }
+          return true;
+        };
+        int k = 0, last_seq = -1;
+        Piece w;
+        while (ok && pieces.next(w)) {
+          const SeqGeo& sq = p.batch.seq[w.seq];
+          if constexpr (kPaged) {
+            if (w.seq != last_seq) cached_pg[0] = cached_pg[1] = -1;
+          }
+          last_seq = w.seq;
+          if constexpr (do_k) {
+            if (k > 0 && !(ok = wait_bar(bar(kBarQEmpty), (k - 1) & 1, p))) break;
+            if (!(p.withhold_q && k == 0)) {
+              if (leader)
+                ptx::mbar_arrive_expect_tx(bar(kBarQFull), (kPair ? 2 : 1) * kQChunks * kQBoxBytes);
+              for (int c = 0; c < kQChunks; ++c)
+                load(q_smem + c * kQChunkBytes, &p.tmap_q, kBarQFull, kChunkElems * c, kGroup * w.g,
+                     sq.q_start + tpi * w.qt + kTokPerTile * static_cast<int>(rank), pol_q);
+              q_issued = true;
+              q_parity = k & 1;
+            }
+          }
+          if constexpr (do_k && do_v) {
+            // K0, K1, V0, K2, V1, ..., V(nt-1)
+            const int nt = w.n1 - w.n0;
+            for (int j = 0; j < nt && ok; ++j) {
+              ok = next_tile(sq, w.n0 + j, BoolC<true>{}, w.g);
+              if (ok && j >= 1) ok = next_tile(sq, w.n0 + j - 1, BoolC<false>{}, w.g);
+            }
+            if (ok) ok = next_tile(sq, w.n1 - 1, BoolC<false>{}, w.g);
+          } else {
+            for (int n = w.n0; n < w.n1 && ok; ++n) ok = next_tile(sq, n, BoolC<do_k>{}, w.g);
+          }
+          ++k;
         }
-        return true;
+        // Every copy issued must have landed before the CTA exits. On the normal
+        // path the MMA threads already waited for all of them (these return at
+        // once); after a time-out they may still be in flight. In a pair all
+        // copies complete on the leader's barriers, so the leader drains for both.
+        if (leader) {
+          for (uint32_t s = ring0; s < ring_end; ++s)
+            if (issued_mask & (1u << s)) wait_bar(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
+          if (q_issued) wait_bar(bar(kBarQFull), q_parity, p);
+        }
+        if constexpr (kFp8 && do_k) {  // key scales complete on each CTA's own barriers
+          for (int s = 0; s < kScSlots; ++s)
+            if (sc_issued_mask & (1u << s))
+              wait_bar(bar(kBarScFull + s), (sc_issued_parity >> s) & 1u, p);
+        }
       };
-      int k = 0, last_seq = -1;
-      Piece w;
-      while (ok && pieces.next(w)) {
-        const SeqGeo& sq = p.batch.seq[w.seq];
-        if constexpr (kPaged) {
-          if (w.seq != last_seq) cached_pg[0] = cached_pg[1] = -1;
-        }
-        last_seq = w.seq;
-        if (k > 0 && !(ok = wait_bar(bar(kBarQEmpty), (k - 1) & 1, p))) break;
-        if (!(p.withhold_q && k == 0)) {
-          if (leader)
-            ptx::mbar_arrive_expect_tx(bar(kBarQFull), (kPair ? 2 : 1) * kQChunks * kQBoxBytes);
-          for (int c = 0; c < kQChunks; ++c)
-            load(q_smem + c * kQChunkBytes, &p.tmap_q, kBarQFull, kChunkElems * c, kGroup * w.g,
-                 sq.q_start + tpi * w.qt + kTokPerTile * static_cast<int>(rank), pol_q);
-          q_issued = true;
-          q_parity = k & 1;
-        }
-        // Load order: K0, K1, V0, K2, V1, ..., V(nt-1) (K into the K ring, V into the V ring).
-        const int nt = w.n1 - w.n0;
-        for (int j = 0; j < nt && ok; ++j) {
-          ok = next_tile(sq, w.n0 + j, true, w.g);
-          if (ok && j >= 1) ok = next_tile(sq, w.n0 + j - 1, false, w.g);
-        }
-        if (ok) ok = next_tile(sq, w.n1 - 1, false, w.g);
-        ++k;
-      }
-      // Every copy issued must have landed before the CTA exits. On the normal
-      // path the MMA threads already waited for all of them (these return at
-      // once); after a time-out they may still be in flight. In a pair all
-      // copies complete on the leader's barriers, so the leader drains for both.
-      if (leader) {
-        for (int s = 0; s < kStages; ++s)
-          if (issued_mask & (1u << s)) wait_bar(bar(kBarFull + s), (issued_parity >> s) & 1u, p);
-        if (q_issued) wait_bar(bar(kBarQFull), q_parity, p);
-      }
-      if constexpr (kFp8) {  // key scales complete on each CTA's own barriers
-        for (int s = 0; s < kScSlots; ++s)
-          if (sc_issued_mask & (1u << s))
-            wait_bar(bar(kBarScFull + s), (sc_issued_parity >> s) & 1u, p);
-      }
+      if constexpr (!split) produce(BoolC<true>{}, BoolC<true>{});
+      else if (warp == kTmaWarp) produce(BoolC<true>{}, BoolC<false>{});
+      else produce(BoolC<false>{}, BoolC<true>{});
     }
     __syncwarp();
   } else if (warp == kMmaWarp || warp == kPvWarp) {
@@ -1403,21 +1481,28 @@ cudaLaunchConfig_t launch_config(dim3 grid, dim3 block, size_t smem, bool pair,
 }  // namespace
 
 cudaError_t max_active_pairs(int* pairs) {
-  // The smaller of the 4- and 8-softmax-warp pair kernels' counts (block sizes differ).
-  int n[2] = {0, 0};
-  for (int i = 0; i < 2; ++i) {
-    const int fp8 = 2 * i;
+  // The smallest count over the pair kernels' block sizes: 4 softmax warps (dense),
+  // 8 (quantised PV), 4 with the second TMA warp (paged).
+  struct Shape {
+    int fp8, kv;
+    void (*kernel)(FwdParams);
+  };
+  const Shape shapes[3] = {{0, 0, gqa_attn_fwd_sm103_kernel<true, 0, 0>},
+                           {2, 0, gqa_attn_fwd_sm103_kernel<true, 0, 2>},
+                           {0, 1, gqa_attn_fwd_sm103_kernel<true, 1, 0>}};
+  int best = 1 << 30;
+  for (const Shape& sh : shapes) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg =
-        launch_config(dim3(2), dim3(fwd_threads(fp8)), kSmemAlloc, true, nullptr, attr);
+    cudaLaunchConfig_t cfg = launch_config(dim3(2), dim3(fwd_threads(sh.fp8, sh.kv)), kSmemAlloc,
+                                           true, nullptr, attr);
     cfg.attrs = attr + 1;  // occupancy of the cluster shape only
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaOccupancyMaxActiveClusters(
-        n + i, fp8 ? gqa_attn_fwd_sm103_kernel<true, 0, 2> : gqa_attn_fwd_sm103_kernel<true, 0, 0>,
-        &cfg);
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, sh.kernel, &cfg);
     if (e != cudaSuccess) return e;
+    best = std::min(best, n);
   }
-  *pairs = std::min(n[0], n[1]);
+  *pairs = best;
   return cudaSuccess;
 }
 
@@ -1437,8 +1522,9 @@ cudaError_t launch_fwd_of(const cudaLaunchConfig_t& cfg, const FwdParams& p, int
 cudaError_t launch_fwd(const FwdParams& p, int grid, bool pair, int kv, int fp8,
                        cudaStream_t stream) {
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = launch_config(dim3(static_cast<unsigned>(grid)), dim3(fwd_threads(fp8)),
-                                               kSmemAlloc, pair, stream, attr);
+  const cudaLaunchConfig_t cfg =
+      launch_config(dim3(static_cast<unsigned>(grid)), dim3(fwd_threads(fp8, kv)), kSmemAlloc,
+                    pair, stream, attr);
   return pair ? launch_fwd_of<true>(cfg, p, kv, fp8) : launch_fwd_of<false>(cfg, p, kv, fp8);
 }
 

@@ -23,10 +23,13 @@ constexpr int kBlockN = 128;  // keys per KV tile
 
 // Softmax warps of the attention kernel (fp8: 0 BF16, 1 FP8 QK^T, 2 FP8 QK^T and
 // PV): 4, one thread per MMA row; with quantised PV 8, two threads per row on 64
-// of a tile's 128 scores each. Then one TMA warp and two MMA-issuing warps (QK^T,
-// PV).
+// of a tile's 128 scores each. Then the TMA warp, two MMA-issuing warps (QK^T,
+// PV) and, for paged K/V (kv == 1), a second TMA warp for the V ring.
 constexpr int fwd_softmax_warps(int fp8) { return fp8 == 2 ? 8 : 4; }
-constexpr int fwd_threads(int fp8) { return (fwd_softmax_warps(fp8) + 3) * 32; }
+constexpr bool fwd_split_producer(int kv) { return kv == 1; }
+constexpr int fwd_threads(int fp8, int kv) {
+  return (fwd_softmax_warps(fp8) + (fwd_split_producer(kv) ? 4 : 3)) * 32;
+}
 
 struct FwdParams {
   CUtensorMap tmap_q;  // Q [q_len][24][256], box (64 d, 6 heads, 21 tokens), 128B swizzle

@@ -50,6 +50,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, with the longest time (ns) the thread may stay suspended
+// waiting for the phase; it resumes when the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 // 16 zero bytes to shared memory: this CTA's (shared::cta address) or a CTA of
 // the cluster (shared::cluster address from mapa).
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {

@@ -1,9 +1,10 @@
 """The attention kernel's barrier protocol, checked on a model of its roles.
 
-gqa_attn_fwd_sm103_kernel runs five roles per CTA (pair): the TMA producer, the
-softmax warps, the QK^T-issuing thread and the PV-issuing thread, which hand
-work to one another through mbarriers. This test restates, per work unit of nt
-KV tiles, the order in which each role waits and arrives, and checks:
+gqa_attn_fwd_sm103_kernel runs these roles per CTA (pair): the TMA producer
+(two on paged K/V: Q/K and V), the softmax warps, the QK^T-issuing thread and
+the PV-issuing thread, which hand work to one another through mbarriers. This
+test restates, per work unit of nt KV tiles, the order in which each role waits
+and arrives, and checks:
 
 * no deadlock: a greedy run of all roles completes, with and without the
   data-dependent waits (the softmax's O rescale waits for the previous PV);
@@ -14,8 +15,11 @@ KV tiles, the order in which each role waits and arrives, and checks:
   happens-before (program order plus arrive -> wait), not from timing.
 
 The kernel splits its five K/V stages into a K ring read by the QK^T thread and
-a V ring read by the PV thread. A negative control runs the same check on one
-shared ring read by both threads (an earlier design): it must be flagged.
+a V ring read by the PV thread. One producer fills both in the order K0, K1,
+V0, K2, V1, ...; on paged K/V each ring has its own producer, filling it in
+tile order. A negative control runs the same check on one shared ring filled by
+one producer and read by both MMA threads (an earlier design): it must be
+flagged.
 """
 import collections
 import itertools
@@ -37,15 +41,24 @@ def test_ring_split_matches_the_kernel():
     src = open(KERNEL).read()
     assert "constexpr int kStages = 5;" in src
     assert "kStagesK = kKStagesPerTile == 2 ? 3 : 2;" in src
+    # one producer thread for both rings (dense), one per ring (paged)
+    assert "if constexpr (!split) produce(BoolC<true>{}, BoolC<true>{});" in src
+    assert "else if (warp == kTmaWarp) produce(BoolC<true>{}, BoolC<false>{});" in src
+    assert "else produce(BoolC<false>{}, BoolC<true>{});" in src
+    hdr = open(os.path.join(os.path.dirname(KERNEL), "gqa_internal.h")).read()
+    assert "constexpr bool fwd_split_producer(int kv) { return kv == 1; }" in hdr
 
 
-def roles_for(units, kk, kv, shared_ring=False, rescale=True):
-    """Event lists (("wait"|"arrive", barrier-phase)) of the four roles. units: tiles per
-    work unit; kk / kv: stages per K / V tile (pair 1 / 1, one-CTA BF16 2 / 2, one-CTA
-    FP8 QK^T 1 / 2). Ring barriers are named by (ring, position)."""
+def roles_for(units, kk, kv, shared_ring=False, rescale=True, split_producer=False):
+    """Event lists (("wait"|"arrive"|"fill", barrier-phase)) of the roles. units: tiles
+    per work unit; kk / kv: stages per K / V tile (pair 1 / 1, one-CTA BF16 2 / 2,
+    one-CTA FP8 QK^T 1 / 2). Ring barriers are named by (ring, position). One
+    producer fills the rings in the order K0, K1, V0, K2, V1, ... (with shared_ring,
+    one ring); with split_producer a second one fills the V ring."""
+    assert not (shared_ring and split_producer)
     n_k = STAGES if shared_ring else k_ring_stages(kk)
     n_v = STAGES if shared_ring else STAGES - n_k
-    prod, sm, qk, pv = [], [], [], []
+    prod, prod_v, sm, qk, pv = [], [], [], [], []
     pos = {"K": 0, "V": 0}
     ring = {"K": "K", "V": "K" if shared_ring else "V"}  # one ring: V positions in K's
     n_of = {"K": n_k, "V": n_v}
@@ -54,19 +67,24 @@ def roles_for(units, kk, kv, shared_ring=False, rescale=True):
         if u:
             prod.append(("wait", ("QEmpty", u - 1)))
         prod.append(("arrive", ("QFull", u)))
-        order = []  # the producer's order: K0, K1, V0, K2, V1, ..., V_{nt-1}
-        for j in range(nt):
-            order += [("K", t0 + j, h) for h in range(kk)]
-            if j:
-                order += [("V", t0 + j - 1, h) for h in range(kv)]
-        order += [("V", t0 + nt - 1, h) for h in range(kv)]
+        if not split_producer:  # one producer: K0, K1, V0, K2, V1, ..., V_{nt-1}
+            order = []
+            for j in range(nt):
+                order += [("K", t0 + j, h) for h in range(kk)]
+                if j:
+                    order += [("V", t0 + j - 1, h) for h in range(kv)]
+            order += [("V", t0 + nt - 1, h) for h in range(kv)]
+        else:  # each producer fills its ring in tile order
+            order = [("K", t0 + j, h) for j in range(nt) for h in range(kk)]
+            order += [("V", t0 + j, h) for j in range(nt) for h in range(kv)]
         where = {}
         for kind, t, h in order:
             r = ring[kind]
             p = pos[r]
+            out = prod_v if (kind == "V" and split_producer) else prod
             if p >= n_of[kind]:
-                prod.append(("wait", (r + "Empty", p - n_of[kind])))
-            prod.append(("fill", (r + "Full", p)))
+                out.append(("wait", (r + "Empty", p - n_of[kind])))
+            out.append(("fill", (r + "Full", p)))
             where[(kind, t, h)] = (r, p)
             pos[r] += 1
         for j in range(nt):
@@ -106,7 +124,10 @@ def roles_for(units, kk, kv, shared_ring=False, rescale=True):
                 pv.append(("arrive", (r + "Empty", p)))
             pv.append(("arrive", ("PvDone", t)))
         t0 += nt
-    return {"prod": prod, "softmax": sm, "qk": qk, "pv": pv}, n_of
+    roles = {"prod": prod, "softmax": sm, "qk": qk, "pv": pv}
+    if split_producer:
+        roles["prod_v"] = prod_v
+    return roles, n_of
 
 
 def completes(roles):
@@ -174,19 +195,21 @@ LAYOUTS = [(1, 1), (2, 2), (1, 2)]  # stages per K / V tile: pair, one-CTA BF16,
 UNITS = [u for n in (1, 2, 3) for u in itertools.product([1, 2, 3, 5], repeat=n)]
 
 
+@pytest.mark.parametrize("split_producer", [False, True])
 @pytest.mark.parametrize("kk,kv", LAYOUTS)
-def test_no_deadlock(kk, kv):
+def test_no_deadlock(kk, kv, split_producer):
     for units in UNITS:
         for rescale in (True, False):
-            roles, _ = roles_for(list(units), kk, kv, rescale=rescale)
+            roles, _ = roles_for(list(units), kk, kv, rescale=rescale, split_producer=split_producer)
             assert completes(roles), (units, kk, kv, rescale)
 
 
+@pytest.mark.parametrize("split_producer", [False, True])
 @pytest.mark.parametrize("kk,kv", LAYOUTS)
-def test_every_ring_wait_is_phase_safe(kk, kv):
+def test_every_ring_wait_is_phase_safe(kk, kv, split_producer):
     # Without the rescale waits there are fewest happens-before edges: the worst case.
     for units in UNITS[:20]:
-        roles, n_of = roles_for(list(units), kk, kv, rescale=False)
+        roles, n_of = roles_for(list(units), kk, kv, rescale=False, split_producer=split_producer)
         assert unsafe_ring_waits(roles, n_of) == [], (units, kk, kv)
 
 
