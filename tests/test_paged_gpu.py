@@ -56,7 +56,7 @@ def check_paged(q, k, v, page_size, seed, what, rows=None, **force):
     return plan_p
 
 
-PAGE_SIZES = [16, 48, 64, 128, SERVING_PAGE_SIZE]
+PAGE_SIZES = [16, 32, 48, 64, 128, SERVING_PAGE_SIZE, 1024]
 SHAPES = [(1, 1), (5, 300), (43, 300), (100, 100), (129, 1000), (22, 2000)]
 
 
