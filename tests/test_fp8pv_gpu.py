@@ -75,7 +75,7 @@ def check_pv(out, lse, ref_o, ref_l, bound, what):
     return err
 
 
-@pytest.mark.parametrize("kv_len", [1, 37, 300, 4097])
+@pytest.mark.parametrize("kv_len", [1, 37, 300, 513, 2048, 4097])
 def test_quantize_v_matches_oracle_bit_for_bit(cuda_device, kv_len):
     q, k, v = make_qkv(1, kv_len, seed=kv_len + 3)
     _, _, _, _, _, v8, vs, vstride = quantize_all_gpu(q, k, v)
