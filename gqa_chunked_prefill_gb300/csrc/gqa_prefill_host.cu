@@ -39,6 +39,13 @@ constexpr double kTileUs = 1.5;              // planning estimate per tile, one-
 // GB300 the pair kernel is ~1.1x faster per tile (4096x32768: 1.75 ms vs
 // 1.92 ms; 3072x16384: 0.67 ms vs 0.74 ms): each SM streams half the operands.
 constexpr double kPairTileUs = 1.35;
+// Paged K/V: against dense K/V the one-CTA kernel's launch takes 13 % longer at
+// 1024-key pages, 30 % at 784 and up to 2x at 16 (512x32768), the pair's 0-5 %
+// at 1024 and 784 (each SM brings in half of every tile, and the paged boxes'
+// extra copies and block-table reads cost it less). Paged calls weigh the
+// one-CTA plan's estimate by this factor; measured, the pair then won on every
+// paged shape tried (512x32768, 512x4096, 3072x16384; pages 16 to 1024).
+constexpr double kPagedOneCtaFactor = 1.25;
 constexpr double kMergeBytesPerUs = 6.0e6;   // effective bandwidth of the merge pass (partials in L2)
 constexpr double kMergeLaunchUs = 3.0;       // its launch, mostly hidden by programmatic launch
 constexpr int64_t kPartialRowBytes = (kHeadDim + 1) * 4;  // FP32 O row + base-2 LSE
@@ -275,7 +282,7 @@ double best_plan_of(const std::vector<SeqIn>& seqs, int num_sms, int variant, in
 // max_pairs: CTA pairs that can be resident at once. force_grid caps the CTAs
 // launched (a pair counts as two).
 void compute_plan(const std::vector<SeqIn>& seqs, int num_sms, int max_pairs, int force_splits,
-                  int force_grid, int force_variant, gqa_prefill_plan* plan) {
+                  int force_grid, int force_variant, bool paged, gqa_prefill_plan* plan) {
   const int cap = force_grid > 0 ? std::min(force_grid, num_sms) : num_sms;
   const int workers1 = std::max(1, cap);
   const int workers2 = std::max(1, std::min(max_pairs, cap / 2));
@@ -288,18 +295,19 @@ void compute_plan(const std::vector<SeqIn>& seqs, int num_sms, int max_pairs, in
     return;
   }
   gqa_prefill_plan one{}, pair{};
-  const double t1 = best_plan_of(seqs, num_sms, 1, workers1, force_splits, &one);
+  const double t1 = best_plan_of(seqs, num_sms, 1, workers1, force_splits, &one) *
+                    (paged ? kPagedOneCtaFactor : 1.0);
   const double t2 = best_plan_of(seqs, num_sms, 2, workers2, force_splits, &pair);
   *plan = t2 < 0.98 * t1 ? pair : one;
 }
 
-// Plans keyed by everything they depend on: the device, the options and the
-// (q_len, kv_len) of every sequence in the caller's order.
+// Plans keyed by everything they depend on: the device, the options, dense or
+// paged K/V and the (q_len, kv_len) of every sequence in the caller's order.
 void cached_plan(const std::vector<SeqIn>& seqs, int num_sms, int max_pairs, int force_splits,
-                 int force_grid, int force_variant, gqa_prefill_plan* plan) {
+                 int force_grid, int force_variant, bool paged, gqa_prefill_plan* plan) {
   static std::mutex mu;
   static std::map<std::vector<int>, gqa_prefill_plan> cache;
-  std::vector<int> key{num_sms, max_pairs, force_splits, force_grid, force_variant};
+  std::vector<int> key{num_sms, max_pairs, force_splits, force_grid, force_variant, paged ? 1 : 0};
   for (const SeqIn& s : seqs) {
     key.push_back(s.q_len);
     key.push_back(s.kv_len);
@@ -312,7 +320,7 @@ void cached_plan(const std::vector<SeqIn>& seqs, int num_sms, int max_pairs, int
       return;
     }
   }
-  compute_plan(seqs, num_sms, max_pairs, force_splits, force_grid, force_variant, plan);
+  compute_plan(seqs, num_sms, max_pairs, force_splits, force_grid, force_variant, paged, plan);
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache.emplace(std::move(key), *plan);
@@ -762,7 +770,8 @@ gqa_status run(const CallIO& io, const std::vector<SeqIn>& seqs, int total_q, in
   if ((st = device_info(&dev)) != GQA_OK) return st;
   gqa_prefill_plan plan{};
   cached_plan(seqs, dev->num_sms, dev->max_pairs, opts ? opts->force_splits : 0,
-              opts ? opts->force_grid : 0, opts ? opts->force_variant : 0, &plan);
+              opts ? opts->force_grid : 0, opts ? opts->force_variant : 0, io.pkv != nullptr,
+              &plan);
   if (plan_out) *plan_out = plan;
   auto stream = static_cast<cudaStream_t>(stream_ptr);
   void* ws = nullptr;
@@ -830,7 +839,7 @@ gqa_status run_noalloc(const void* q, const void* k, const void* v, void* out, f
   if ((st = noalloc_scratch(&scratch)) != GQA_OK) return st;
   const std::vector<SeqIn> seqs{SeqIn{0, q_len, 0, kv_len, 0}};
   gqa_prefill_plan plan{};
-  cached_plan(seqs, dev->num_sms, dev->max_pairs, 0, 0, 0, &plan);
+  cached_plan(seqs, dev->num_sms, dev->max_pairs, 0, 0, 0, false, &plan);
   if (static_cast<uint64_t>(plan.workspace_bytes) > kNoAllocScratchBytes) return GQA_ERR_SCRATCH;
   // Every partial row the merge reads is written by the attention kernel first,
   // so the scratch needs no clearing between calls.
@@ -1175,7 +1184,7 @@ gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32
   if (total_q == 0) return GQA_OK;
   // The attention calls plan with min(occupancy pairs, num_sms / 2) (device_info).
   const int pairs = max_pairs < 0 ? num_sms / 2 : std::min(max_pairs, num_sms / 2);
-  gqa::cached_plan(seqs, num_sms, pairs, force_splits, force_grid, force_variant, plan);
+  gqa::cached_plan(seqs, num_sms, pairs, force_splits, force_grid, force_variant, false, plan);
   return GQA_OK;
 }
 

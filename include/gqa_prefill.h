@@ -252,7 +252,13 @@ gqa_status gqa_prefill_attn_paged(const void* q, const void* k_cache, const void
                                   void* out, float* lse, int q_len, int kv_len, int n_q_heads,
                                   int n_kv_heads, int head_dim, float scale, void* stream);
 
-/* gqa_prefill_attn_paged with options and the plan (as gqa_prefill_attn_ex). */
+/* gqa_prefill_attn_paged with options and the plan (as gqa_prefill_attn_ex).
+ * Paged calls (this one and the paged batch calls) plan like the dense calls
+ * except that, when force_variant is 0, they prefer the CTA-pair kernel: its
+ * paged tiles run within a few percent of its dense ones, the one-CTA kernel's
+ * do not. So a paged call's plan equals gqa_prefill_make_plan's for the same
+ * shape only where both choose the same variant (force_variant set, or the
+ * pair winning on dense K/V too). */
 gqa_status gqa_prefill_attn_paged_ex(const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_table, int num_pages, int page_size,
                                      void* out, float* lse, int q_len, int kv_len,

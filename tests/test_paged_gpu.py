@@ -43,7 +43,12 @@ def check_paged(q, k, v, page_size, seed, what, rows=None, **force):
     kc, vc, table = make_paged_cache(k, v, page_size, seed)
     out_p, lse_p, plan_p, status = run_paged(q, kc, vc, table, k.shape[0], SCALE, **force)
     assert status == 0, f"{what}: device status {status}"
-    out_d, lse_d, plan_d = run_gpu(q, k, v, SCALE, **force)
+    # Paged calls may prefer the CTA pair where dense ones would not: the dense
+    # call runs the variant the paged plan chose (the same plan, so the same tiles).
+    dense_force = dict(force)
+    if not dense_force.get("force_variant"):
+        dense_force["force_variant"] = plan_p["variant"]
+    out_d, lse_d, plan_d = run_gpu(q, k, v, SCALE, **dense_force)
     assert plan_p == plan_d
     assert torch.equal(out_p, out_d) and torch.equal(lse_p, lse_d), f"{what}: paged != dense"
     if rows is None:
