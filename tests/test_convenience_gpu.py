@@ -20,8 +20,20 @@ def test_wrappers_match_entry_points(cuda_device):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
     kc, vc, table, kv_lens = make_paged_batch(k.cpu(), v.cpu(), cu_k, 784, seed=78)
-    o3, l3 = gqa.attention_paged(q, kc.cuda(), vc.cuda(), table.cuda(), kv_lens, cu_q, SCALE)
-    assert torch.equal(o3, o1) and torch.equal(l3, l1)
+    kc, vc, table = kc.cuda(), vc.cuda(), table.cuda()
+    o3, l3 = gqa.attention_paged(q, kc, vc, table, kv_lens, cu_q, SCALE)
+    o3e = torch.empty_like(q)
+    l3e = torch.empty_like(l1)
+    _, plan_p = gqa.gqa_prefill_attn_paged_varlen_ex(q, kc, vc, table, table.shape[1], kc.shape[0],
+                                                     784, o3e, l3e, cu_q, kv_lens, 24, 4, 256, SCALE)
+    assert torch.equal(o3, o3e) and torch.equal(l3, l3e)
+    # Paged calls may prefer the CTA pair where dense ones do not: the dense batch
+    # with the paged plan's variant gives the same bits.
+    o3d = torch.empty_like(q)
+    l3d = torch.empty_like(l1)
+    gqa.gqa_prefill_attn_varlen_ex(q, k, v, o3d, l3d, cu_q, cu_k, 24, 4, 256, SCALE,
+                                   force_variant=plan_p["variant"])
+    assert torch.equal(o3, o3d) and torch.equal(l3, l3d)
 
     q8, qs = gqa.quantize_fp8(q)
     k8, ks = gqa.quantize_fp8(k, cu_k)
@@ -34,9 +46,22 @@ def test_wrappers_match_entry_points(cuda_device):
 
     qs1, ks1, vs1 = (t.cuda() for t in make_qkv(50, 400, seed=79))
     o6, l6 = gqa.attention(qs1, ks1, vs1, SCALE)
+    o6e = torch.empty_like(qs1)
+    l6e = torch.empty_like(l6)
+    gqa.gqa_prefill_attn(qs1, ks1, vs1, o6e, l6e, 50, 400, 24, 4, 256, SCALE)
+    assert torch.equal(o6, o6e) and torch.equal(l6, l6e)
     tbl = torch.arange(1, dtype=torch.int32, device="cuda")
-    o7, l7 = gqa.attention_paged(qs1, ks1.reshape(1, 400, 4, 256), vs1.reshape(1, 400, 4, 256),
-                                 tbl, 400, scale=SCALE)
+    kc1, vc1 = ks1.reshape(1, 400, 4, 256), vs1.reshape(1, 400, 4, 256)
+    o7, l7 = gqa.attention_paged(qs1, kc1, vc1, tbl, 400, scale=SCALE)
+    o7e = torch.empty_like(qs1)
+    l7e = torch.empty_like(l6)
+    _, plan7 = gqa.gqa_prefill_attn_paged_ex(qs1, kc1, vc1, tbl, 1, 400, o7e, l7e, 50, 400, 24, 4,
+                                             256, SCALE)
+    o6d = torch.empty_like(qs1)
+    l6d = torch.empty_like(l6)
+    gqa.gqa_prefill_attn_ex(qs1, ks1, vs1, o6d, l6d, 50, 400, 24, 4, 256, SCALE,
+                            force_variant=plan7["variant"])
     torch.cuda.synchronize()
     assert gqa.gqa_prefill_poll() == 0
-    assert torch.equal(o6, o7) and torch.equal(l6, l7)
+    assert torch.equal(o7, o7e) and torch.equal(l7, l7e)
+    assert torch.equal(o7, o6d) and torch.equal(l7, l6d)
