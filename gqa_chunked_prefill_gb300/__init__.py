@@ -11,7 +11,7 @@ from ._binding import (FORCE_BALANCED_TAIL, GqaError, GqaStatus, gqa_prefill_abi
                        gqa_prefill_attn_fp8qk_varlen_ex, gqa_prefill_attn_paged_fp8qk_varlen_ex,
                        gqa_prefill_attn_fp8qkpv, gqa_prefill_attn_fp8qkpv_ex, gqa_quantize_v_fp8,
                        gqa_prefill_attn_varlen, gqa_prefill_attn_varlen_ex, gqa_prefill_device_info,
-                       gqa_prefill_make_plan,
+                       gqa_prefill_make_plan, gqa_prefill_make_plan_paged_varlen,
                        gqa_prefill_make_plan_varlen, gqa_prefill_poll, gqa_quantize_k_fp8,
                        gqa_quantize_k_fp8_varlen, gqa_quantize_q_fp8, gqa_status_string,
                        key_scale_columns, lib)

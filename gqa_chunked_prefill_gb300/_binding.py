@@ -101,6 +101,9 @@ lib.gqa_prefill_attn_paged_varlen_ex.restype = _i
 lib.gqa_prefill_make_plan_varlen.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                              ctypes.POINTER(PrefillPlan)]
 lib.gqa_prefill_make_plan_varlen.restype = _i
+lib.gqa_prefill_make_plan_paged_varlen.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                                   ctypes.POINTER(PrefillPlan)]
+lib.gqa_prefill_make_plan_paged_varlen.restype = _i
 lib.gqa_quantize_k_fp8_varlen.argtypes = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]
 lib.gqa_quantize_k_fp8_varlen.restype = _i
 lib.gqa_prefill_attn_fp8qk_varlen_ex.argtypes = [_vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp,
@@ -472,6 +475,22 @@ def gqa_prefill_make_plan_varlen(cu_seqlens_q, cu_seqlens_k, n_q_heads, n_kv_hea
     rc = lib.gqa_prefill_make_plan_varlen(pq, pk, len(cu_seqlens_q) - 1, n_q_heads, n_kv_heads,
                                           head_dim, num_sms, max_pairs, force_splits, force_grid,
                                           force_variant, ctypes.byref(plan))
+    if check:
+        _check(rc)
+    return rc, plan.as_dict()
+
+
+def gqa_prefill_make_plan_paged_varlen(cu_seqlens_q, kv_lens, n_q_heads, n_kv_heads, head_dim,
+                                       num_sms, max_pairs=-1, force_splits=0, force_grid=0,
+                                       force_variant=0, check=True):
+    """The plan of a paged call or paged batch (kv_lens: host ints per sequence)."""
+    cq, pq = _host_i32(cu_seqlens_q)
+    kl, pk = _host_i32(kv_lens)
+    plan = PrefillPlan()
+    rc = lib.gqa_prefill_make_plan_paged_varlen(pq, pk, len(cu_seqlens_q) - 1, n_q_heads,
+                                                n_kv_heads, head_dim, num_sms, max_pairs,
+                                                force_splits, force_grid, force_variant,
+                                                ctypes.byref(plan))
     if check:
         _check(rc)
     return rc, plan.as_dict()

@@ -1164,18 +1164,20 @@ gqa_status gqa_prefill_device_info(int* num_sms, int* max_pairs) {
   return GQA_OK;
 }
 
-gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
-                                        int batch, int n_q_heads, int n_kv_heads, int head_dim,
-                                        int num_sms, int max_pairs, int force_splits,
-                                        int force_grid, int force_variant,
-                                        gqa_prefill_plan* plan) {
+namespace {
+// Host-only planning of a batch given as (cu_seqlens_q, cu_seqlens_k) (dense) or
+// (cu_seqlens_q, kv_lens) (paged): the plan the attention call computes.
+gqa_status host_plan(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                     const int32_t* kv_lens, int batch, int n_q_heads, int n_kv_heads,
+                     int head_dim, int num_sms, int max_pairs, int force_splits, int force_grid,
+                     int force_variant, bool paged, gqa_prefill_plan* plan) {
   if (!plan) return GQA_ERR_NULL;
   std::memset(plan, 0, sizeof(*plan));
   std::vector<gqa::SeqIn> seqs;
   int total_q = 0;
   int64_t total_kv = 0;
-  if (batch > 0 && !cu_seqlens_k) return GQA_ERR_NULL;
-  gqa_status st = gqa::batch_from_host(cu_seqlens_q, cu_seqlens_k, nullptr, batch, &seqs,
+  if (batch > 0 && !cu_seqlens_k && !kv_lens) return GQA_ERR_NULL;
+  gqa_status st = gqa::batch_from_host(cu_seqlens_q, cu_seqlens_k, kv_lens, batch, &seqs,
                                        &total_q, &total_kv);
   if (st != GQA_OK) return st;
   if ((st = gqa::validate_heads(n_q_heads, n_kv_heads, head_dim, 1.0f / 16.0f)) != GQA_OK)
@@ -1184,8 +1186,35 @@ gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32
   if (total_q == 0) return GQA_OK;
   // The attention calls plan with min(occupancy pairs, num_sms / 2) (device_info).
   const int pairs = max_pairs < 0 ? num_sms / 2 : std::min(max_pairs, num_sms / 2);
-  gqa::cached_plan(seqs, num_sms, pairs, force_splits, force_grid, force_variant, false, plan);
+  gqa::cached_plan(seqs, num_sms, pairs, force_splits, force_grid, force_variant, paged, plan);
   return GQA_OK;
+}
+}  // namespace
+
+gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                                        int batch, int n_q_heads, int n_kv_heads, int head_dim,
+                                        int num_sms, int max_pairs, int force_splits,
+                                        int force_grid, int force_variant,
+                                        gqa_prefill_plan* plan) {
+  if (batch > 0 && !cu_seqlens_k) {
+    if (plan) std::memset(plan, 0, sizeof(*plan));
+    return GQA_ERR_NULL;
+  }
+  return host_plan(cu_seqlens_q, cu_seqlens_k, nullptr, batch, n_q_heads, n_kv_heads, head_dim,
+                   num_sms, max_pairs, force_splits, force_grid, force_variant, false, plan);
+}
+
+gqa_status gqa_prefill_make_plan_paged_varlen(const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                              int batch, int n_q_heads, int n_kv_heads,
+                                              int head_dim, int num_sms, int max_pairs,
+                                              int force_splits, int force_grid, int force_variant,
+                                              gqa_prefill_plan* plan) {
+  if (batch > 0 && !kv_lens) {
+    if (plan) std::memset(plan, 0, sizeof(*plan));
+    return GQA_ERR_NULL;
+  }
+  return host_plan(cu_seqlens_q, nullptr, kv_lens, batch, n_q_heads, n_kv_heads, head_dim,
+                   num_sms, max_pairs, force_splits, force_grid, force_variant, true, plan);
 }
 
 gqa_status gqa_prefill_poll(void* stream, int* device_status) {

@@ -319,6 +319,17 @@ gqa_status gqa_prefill_make_plan_varlen(const int32_t* cu_seqlens_q, const int32
                                         int batch, int n_q_heads, int n_kv_heads, int head_dim,
                                         int num_sms, int max_pairs, int force_splits,
                                         int force_grid, int force_variant, gqa_prefill_plan* plan);
+/* Host-only planning of a paged call (gqa_prefill_attn_paged[_ex], one sequence:
+ * batch 1, cu_seqlens_q {0, q_len}, kv_lens {kv_len}) or paged batch
+ * (gqa_prefill_attn_paged_varlen[_ex]); kv_lens HOST int32 [batch]. Paged calls
+ * prefer the CTA-pair kernel (see gqa_prefill_attn_paged_ex), so this can differ
+ * from gqa_prefill_make_plan_varlen for the same lengths. Same arguments,
+ * validation and errors as gqa_prefill_make_plan_varlen otherwise. */
+gqa_status gqa_prefill_make_plan_paged_varlen(const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                              int batch, int n_q_heads, int n_kv_heads,
+                                              int head_dim, int num_sms, int max_pairs,
+                                              int force_splits, int force_grid, int force_variant,
+                                              gqa_prefill_plan* plan);
 
 /*
  * Quantised QK^T (gfx936 DCU上实现INT8 QK MMAC：分页访存、Fragment映射与GQA适配, §1

@@ -263,6 +263,38 @@ def test_varlen_refusals_before_any_cuda_call(gqa):
     assert pf(3, [40, 1]) == S.ERR_SHAPE              # second sequence: q_len 2 > kv_len 1
 
 
+def test_paged_plans_prefer_the_pair(gqa):
+    """Paged calls weigh the one-CTA plan up: 512x32768 is planned one CTA per item
+    on dense K/V and as CTA pairs on paged K/V; where the pair wins on dense K/V
+    too (4096x32768) both plans are the same; with no pair resident both use one
+    CTA; a forced variant is honoured by both."""
+    def both(ql, kl, **kw):
+        _, d = gqa.gqa_prefill_make_plan_varlen([0, ql], [0, kl], 24, 4, 256, 152, 76, **kw)
+        _, p = gqa.gqa_prefill_make_plan_paged_varlen([0, ql], [kl], 24, 4, 256, 152, 76, **kw)
+        return d, p
+    d, p = both(512, 32768)
+    assert d["variant"] == 1 and p["variant"] == 2
+    d, p = both(4096, 32768)
+    assert d == p and p["variant"] == 2
+    for v in (1, 2):
+        d, p = both(512, 32768, force_variant=v)
+        assert d == p and p["variant"] == v
+    _, p0 = gqa.gqa_prefill_make_plan_paged_varlen([0, 512], [32768], 24, 4, 256, 152, 0)
+    assert p0["variant"] == 1
+    # a batch: the same lengths as cu_seqlens_k or as kv_lens give the same dense plan
+    lens = [(43, 300), (1, 4096), (129, 1000)]
+    cu_q, cu_k, kv = [0], [0], []
+    for ql, kl in lens:
+        cu_q.append(cu_q[-1] + ql)
+        cu_k.append(cu_k[-1] + kl)
+        kv.append(kl)
+    _, d = gqa.gqa_prefill_make_plan_varlen(cu_q, cu_k, 24, 4, 256, 152, 76, force_variant=1)
+    _, p = gqa.gqa_prefill_make_plan_paged_varlen(cu_q, kv, 24, 4, 256, 152, 76, force_variant=1)
+    assert d == p
+    assert gqa.gqa_prefill_make_plan_paged_varlen([0, 5], [4], 24, 4, 256, 152, check=False)[0] \
+        == gqa.GqaStatus.ERR_SHAPE  # q_len > kv_len
+
+
 @pytest.mark.parametrize("lens", [[(4096, 32768)], [(43, 300), (1, 4096), (0, 50), (129, 1000)],
                                   [(1, 1000)] * 40, [(512, 4096), (300, 20000), (2000, 2000)],
                                   [(21, 21)] * 128])

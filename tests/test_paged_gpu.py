@@ -103,6 +103,21 @@ def test_paged_workload_full_size(cuda_device, name, page_size):
     assert unchecked_items(rows, w.q_len, 21 * plan["variant"]) == []
 
 
+@pytest.mark.parametrize("q_len,kv_len", [(512, 32768), (512, 4096), (43, 300), (1, 2000)])
+def test_paged_plan_is_the_host_plan(cuda_device, q_len, kv_len):
+    """The plan a paged call reports is the host-only paged planner's for the
+    device's SM count and co-resident pairs (paged calls may prefer the pair)."""
+    import gqa_chunked_prefill_gb300 as gqa
+    q, k, v = make_qkv(q_len, kv_len, seed=q_len + kv_len)
+    kc, vc, table = make_paged_cache(k, v, SERVING_PAGE_SIZE, seed=31)
+    _, _, plan, status = run_paged(q, kc, vc, table, kv_len, SCALE)
+    assert status == 0
+    sms, pairs = gqa.gqa_prefill_device_info()
+    _, host_plan = gqa.gqa_prefill_make_plan_paged_varlen([0, q_len], [kv_len], 24, 4, 256, sms,
+                                                          max_pairs=pairs)
+    assert plan == host_plan
+
+
 @pytest.mark.parametrize("bad", ["past_end", "negative"])
 @pytest.mark.parametrize("variant", [1, 2])
 def test_block_table_entry_outside_cache_reads_zeros(cuda_device, bad, variant):
