@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define GQA_PREFILL_ABI_VERSION 11
+#define GQA_PREFILL_ABI_VERSION 12
 
 typedef enum gqa_status {
   GQA_OK = 0,

@@ -50,7 +50,7 @@ def test_bounds_checked_build_exports_the_same_abi(gqa):
 
 
 def test_abi_version(gqa):
-    assert gqa.gqa_prefill_abi_version() == 11
+    assert gqa.gqa_prefill_abi_version() == 12
 
 
 def test_refusals_before_any_cuda_call(gqa):
